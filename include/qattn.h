@@ -1,0 +1,198 @@
+/*
+ * qattn -- the attention step of a Qwen2 decoder layer over a block-paged KV
+ * cache, as a C ABI over hand-written sm_103a CUDA kernels.
+ *
+ * The step (restated from the pages it comes from):
+ *   1. rotate-half RoPE with rope_theta = 1e6 on the query and key heads of
+ *      the fused QKV projection output -- get_rope(head_dim,
+ *      rotary_dim=head_dim, max_position, base=rope_theta) in
+ *      "Qwen2大模型架构解析与vLLM优化实践" section 2.2; the 1e6 default in
+ *      "Qwen2 模型结构代码详解" section 2 (配置解析);
+ *   2. the new K/V rows written into fixed-size cache blocks through a slot
+ *      mapping -- PagedAttention block cache (vLLM-deploys-Qwen notes,
+ *      gsyq.cn, section 2.1) and the per-sequence block_table plus
+ *      prepare_prefill context of the nano-vllm Qwen3 skeleton page,
+ *      section 5;
+ *   3. grouped-query attention, num_heads / num_kv_heads query heads per KV
+ *      head, scale head_dim ** -0.5 ("Qwen2 模型结构代码详解" section 2;
+ *      Attention(...) in "Qwen2大模型架构解析与vLLM优化实践" section 4.1),
+ *      gathering each sequence's blocks through its block table: decode, and
+ *      causal varlen / chunked prefill (FlashAttention-2 varlen in the Qwen
+ *      engineering notes, 0539edu.com, section 2.1).
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers unless the argument says host.
+ *     The caller owns every buffer; the library allocates no device memory
+ *     and keeps no state between calls.
+ *   - bf16 everywhere for activations and cache; int32 for every index.
+ *   - Cache layout: k_cache and v_cache are [num_blocks][num_kv_heads]
+ *     [block_size][head_dim] bf16, contiguous.  Token slot s lives in block
+ *     s / block_size at offset s % block_size.  Both base pointers must be
+ *     16-byte aligned.
+ *   - Query head h reads KV head h / (num_heads / num_kv_heads).
+ *   - Row strides are in elements and must be multiples of 8 (16 bytes);
+ *     head h of a row starts at element h * head_dim of the row.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream).  The return value reports host-side
+ *     argument checks and launch errors only.
+ *   - Data-dependent errors are found on the device: the offending element
+ *     is skipped and a bit is OR-ed into *err_word (a device int32 that the
+ *     caller zeroes; may be NULL).  Kernels never trap.  Outputs of a row
+ *     that raised an error bit are unspecified.
+ *   - Supported today: head_dim 128, block_size 16, num_heads a multiple of
+ *     num_kv_heads with at most 8 query heads per KV head, num_heads <= 128.
+ *     Anything else returns QATTN_ERR_UNSUPPORTED without launching.
+ *   - A call with zero tokens / zero sequences returns QATTN_OK and launches
+ *     nothing.
+ */
+#ifndef QATTN_H_
+#define QATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Model shape of one attention layer. */
+typedef struct qattn_dims {
+  int32_t num_heads;    /* H: query heads */
+  int32_t num_kv_heads; /* Hkv: key/value heads (GQA group = H / Hkv) */
+  int32_t head_dim;     /* D (128) */
+  int32_t block_size;   /* tokens per cache block (16) */
+  float scale;          /* softmax scale; <= 0 selects head_dim ** -0.5 */
+} qattn_dims;
+
+/* Host-side return codes. */
+enum {
+  QATTN_OK = 0,
+  QATTN_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad stride/alignment */
+  QATTN_ERR_UNSUPPORTED = 2, /* shape outside the supported set above */
+  QATTN_ERR_CUDA = 3,        /* a CUDA runtime/driver call or launch failed */
+  QATTN_ERR_WORKSPACE = 4    /* workspace missing or smaller than required */
+};
+
+/* Bits OR-ed into the optional device error word. */
+enum {
+  QATTN_DEVERR_SLOT = 1,      /* slot_mapping entry >= num_blocks * block_size */
+  QATTN_DEVERR_BLOCK = 2,     /* block_tables entry outside [0, num_blocks) */
+  QATTN_DEVERR_CONTEXT = 4,   /* context_len <= 0, > max_context_len, or
+                                 smaller than the sequence's query count;
+                                 bad cu_seqlens_q */
+  QATTN_DEVERR_TIMEOUT = 8,   /* a bounded wait inside a kernel gave up */
+  QATTN_DEVERR_POSITION = 16  /* position outside [0, max_pos) */
+};
+
+/* Human-readable name of a return code (static storage). */
+const char* qattn_status_string(int status);
+
+/* Library version as major * 10000 + minor * 100 + patch. */
+int qattn_version(void);
+
+/* Build the RoPE cos/sin table on the HOST, once per model (the table that
+ * get_rope(head_dim, rotary_dim=head_dim, max_position, base) owns;
+ * "Qwen2大模型架构解析与vLLM优化实践" section 2.2).  host_cos_sin receives
+ * [max_pos][head_dim] fp32: columns i < head_dim/2 hold
+ * cos(pos * theta^(-2i/head_dim)) and column head_dim/2 + i the matching
+ * sin, each evaluated in fp64 and rounded to fp32.  The caller copies it to
+ * the device.  Returns QATTN_INVALID_ARG for a null pointer, max_pos <= 0,
+ * an odd head_dim or theta <= 0. */
+int qattn_rope_table_build(float* host_cos_sin, int32_t max_pos,
+                           int32_t head_dim, double theta);
+
+/* Step 1 + 2: rotate-half RoPE and cache append, one launch.
+ *   q        [num_tokens, q_row_stride] bf16, rotated IN PLACE (heads
+ *            0 .. num_heads-1 of each row);
+ *   k, v     [num_tokens, *_row_stride] bf16, read only (num_kv_heads heads
+ *            per row); k is rotated on the way into k_cache, v copied as is.
+ *            For the fused QKV output [T, (H + 2 Hkv) * D] pass
+ *            q = base, k = base + H*D, v = base + (H + Hkv)*D and the same
+ *            row stride (H + 2 Hkv) * D for all three;
+ *   positions    [num_tokens] int32 rotary position of each token;
+ *   slot_mapping [num_tokens] int32 cache slot of each token, < 0 = padding
+ *            (q is still rotated, nothing is written to the cache);
+ *   cos_sin  [max_pos, head_dim] fp32 table from qattn_rope_table_build.
+ * Rotation arithmetic, element pair (i, i + D/2):
+ *   y_i = x_i c - x_{i+D/2} s,  y_{i+D/2} = x_{i+D/2} c + x_i s,
+ * every product and sum rounded to fp32 (no fused multiply-add), the result
+ * rounded to bf16 nearest-even -- so the cache contents are bit-reproducible.
+ * Device errors: QATTN_DEVERR_POSITION (token skipped entirely),
+ * QATTN_DEVERR_SLOT (cache write skipped).  Duplicate non-negative slots in
+ * one call are undefined. */
+int qattn_rope_cache_append(void* q, int64_t q_row_stride, const void* k,
+                            int64_t k_row_stride, const void* v,
+                            int64_t v_row_stride, const int32_t* positions,
+                            const int32_t* slot_mapping, int32_t num_tokens,
+                            void* k_cache, void* v_cache, int32_t num_blocks,
+                            const float* cos_sin, int32_t max_pos,
+                            qattn_dims dims, int32_t* err_word, void* stream);
+
+/* Bytes of device workspace qattn_paged_decode needs (256-byte aligned
+ * pointer, contents need not be initialised).  Depends only on the
+ * arguments. */
+size_t qattn_paged_decode_workspace_size(int32_t num_seqs,
+                                         int32_t max_context_len,
+                                         qattn_dims dims);
+
+/* Step 3, decode: one query row per sequence.
+ *   out          [num_seqs, num_heads, head_dim] bf16, contiguous;
+ *   q            [num_seqs, q_row_stride] bf16 (already rotated);
+ *   block_tables [num_seqs, max_blocks_per_seq] int32 physical block ids;
+ *   context_lens [num_seqs] int32 tokens in the cache for each sequence,
+ *                including the one appended this step (the query sits at
+ *                position context_len - 1 and sees every cached token);
+ *   max_context_len  host upper bound on context_lens (sizes the split
+ *                workspace; a larger device value raises
+ *                QATTN_DEVERR_CONTEXT).
+ * out[b, h] = sum_j softmax_j(scale * q[b,h] . k_j) v_j over j <
+ * context_lens[b], keys and values of KV head h / (H / Hkv).  Accumulation
+ * is fp32; the work is split into fixed token ranges whose partial results
+ * (normalised output and log-sum-exp) are merged by a second kernel in a
+ * fixed order, so results are run-to-run bit-identical.  Rows with
+ * context_len <= 0 are written as zeros with QATTN_DEVERR_CONTEXT. */
+int qattn_paged_decode(void* out, const void* q, int64_t q_row_stride,
+                       const void* k_cache, const void* v_cache,
+                       int32_t num_blocks, const int32_t* block_tables,
+                       int32_t max_blocks_per_seq, const int32_t* context_lens,
+                       int32_t num_seqs, int32_t max_context_len,
+                       qattn_dims dims, void* workspace, size_t workspace_bytes,
+                       int32_t* err_word, void* stream);
+
+/* Bytes of device workspace qattn_varlen_prefill needs (same rules). */
+size_t qattn_varlen_prefill_workspace_size(int32_t num_seqs,
+                                           int32_t max_context_len,
+                                           qattn_dims dims);
+
+/* Step 3, causal varlen / chunked prefill over a mixed batch.
+ *   out          [total_q, num_heads, head_dim] bf16, contiguous;
+ *   q            [total_q, q_row_stride] bf16 (already rotated);
+ *   cu_seqlens_q [num_seqs + 1] int32, cu_seqlens_q[0] = 0,
+ *                cu_seqlens_q[num_seqs] = total_q: query rows of sequence b
+ *                are cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1;
+ *   max_q_len    host upper bound on any sequence's query count;
+ *   context_lens [num_seqs] tokens in the cache for each sequence after
+ *                this step's append (cached + new).
+ * Query i of sequence b (q_len = cu_seqlens_q[b+1] - cu_seqlens_q[b],
+ * L = context_lens[b]) sits at position L - q_len + i and attends keys
+ * 0 .. L - q_len + i (causal, aligned to the end of the context).
+ * Sequences with q_len == 1 are decode rows and take the decode kernel's
+ * path; longer ones use the tensor-core prefill kernel.  Both run on
+ * `stream`.  Rows of a sequence with q_len > L or L <= 0 are zeroed with
+ * QATTN_DEVERR_CONTEXT. */
+int qattn_varlen_prefill(void* out, const void* q, int64_t q_row_stride,
+                         const int32_t* cu_seqlens_q, int32_t num_seqs,
+                         int32_t total_q, int32_t max_q_len,
+                         const void* k_cache, const void* v_cache,
+                         int32_t num_blocks, const int32_t* block_tables,
+                         int32_t max_blocks_per_seq,
+                         const int32_t* context_lens, int32_t max_context_len,
+                         qattn_dims dims, void* workspace,
+                         size_t workspace_bytes, int32_t* err_word,
+                         void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QATTN_H_ */

@@ -1,0 +1,462 @@
+"""Pins for the CPU oracle (no GPU).
+
+The oracle is only trusted once it agrees with something other than itself:
+the configuration values the pages print (tests/golden), closed forms of the
+rotation and of the softmax, invariants (rotation preserves the norm, the
+relative-position identity, block relabelling, GQA == MHA on repeated heads,
+split == unsplit), special cases (one key returns V, equal keys average V)
+and a multiprecision brute force on tiny inputs.  Each pin is chosen so that
+a plausible mistake -- a dropped scale, a wrong sign or pairing in the
+rotation, a wrong head grouping, a transposed or mis-indexed gather, a
+wrong causal offset -- fails at least one of them.
+"""
+import cmath
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_gqa_07_gb300 import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def u16(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16).copy()
+
+
+def bf16_of(x) -> np.ndarray:
+    """Round fp64 values to bf16 payloads (via torch, an independent path)."""
+    return u16(torch.tensor(np.asarray(x, dtype=np.float32)).to(torch.bfloat16))
+
+
+def f64(u: np.ndarray) -> np.ndarray:
+    return oracle.bf16_to_f64(u)
+
+
+# ------------------------------------------------------------ golden ----
+
+def test_golden_qwen2_7b_config_and_derived_shape():
+    g = json.load(open(os.path.join(GOLDEN, "qwen2_7b_config.json")))
+    head_dim = g["hidden_size"] // g["num_attention_heads"]
+    assert head_dim == g["stated"]["head_dim"] == W.HEAD_DIM
+    assert g["num_attention_heads"] // g["num_key_value_heads"] == g["stated"]["gqa_group"]
+    assert W.QWEN2_7B == dict(num_heads=g["num_attention_heads"],
+                              num_kv_heads=g["num_key_value_heads"])
+    assert W.ROPE_THETA == g["rope_theta"] == g["stated"]["rope_theta_default"]
+    assert W.MAX_POS == g["max_position_embeddings"]
+    assert (head_dim ** -0.5) ** -2 == pytest.approx(g["stated"]["scaling_squared_inverse"])
+
+
+def test_golden_qwen3_config():
+    g = json.load(open(os.path.join(GOLDEN, "qwen3_0_6b_config.json")))
+    assert W.QWEN3_0_6B == dict(num_heads=g["num_attention_heads"],
+                                num_kv_heads=g["num_key_value_heads"])
+    assert g["head_dim"] == W.HEAD_DIM
+
+
+def test_fourteen_token_prefill_gives_fourteen_rows():
+    """nano-vllm page section 5: 14 tokens at positions 0..13 -> 14 rows."""
+    g = json.load(open(os.path.join(GOLDEN, "qwen3_0_6b_config.json")))["integration_check"]
+    n = g["prefill_tokens"]
+    w = W.custom(16, 8, ctx=[n], q_lens=[n], seed=3)
+    qkv = u16(w.qkv)
+    kc, vc = u16(w.k_cache), u16(w.v_cache)
+    cs = oracle.rope_table(w.theta, 64, 128)
+    assert oracle.rope_cache_append(qkv, w.positions, w.slot_mapping, kc, vc, cs,
+                                    16, 8, 128, 16) == 0
+    q = np.ascontiguousarray(qkv[:, :16 * 128])
+    out, err = oracle.paged_attention(q, kc, vc, w.block_tables, w.context_lens,
+                                      16, 8, 128, 16, cu_seqlens_q=w.cu_seqlens_q)
+    assert err == 0 and out.shape == (g["rows_out"], 16, 128)
+    # causal row 0 sees only key 0: it returns v_0 exactly
+    v0 = f64(vc[int(w.block_tables[0, 0]), :, 0, :])  # [Hkv, D]
+    assert np.array_equal(out[0], np.repeat(v0, 2, axis=0))
+
+
+# ------------------------------------------------------------- table ----
+
+def test_table_position_zero_is_identity():
+    t = oracle.rope_table(1e6, 4, 128)
+    assert np.all(t[0, :64] == 1.0) and np.all(t[0, 64:] == 0.0)
+
+
+def test_table_first_frequency_is_one():
+    """i = 0: theta^0 = 1, so column 0 is cos(pos) and column D/2 sin(pos)."""
+    P = 32768
+    t = oracle.rope_table(1e6, P, 128)
+    pos = np.arange(P, dtype=np.float64)
+    assert np.array_equal(t[:, 0], np.cos(pos).astype(np.float32))
+    assert np.array_equal(t[:, 64], np.sin(pos).astype(np.float32))
+
+
+def test_table_quarter_frequency_closed_form():
+    """i = D/4: theta^(-1/2) = 1e-3 for theta = 1e6 (and 1e-2 for 1e4)."""
+    for theta, f in ((1e6, 1e-3), (1e4, 1e-2)):
+        t = oracle.rope_table(theta, 4096, 128)
+        pos = np.arange(4096, dtype=np.float64)
+        np.testing.assert_allclose(t[:, 32], np.cos(pos * f), rtol=0, atol=2e-7)
+        np.testing.assert_allclose(t[:, 96], np.sin(pos * f), rtol=0, atol=2e-7)
+
+
+def test_theta_pitfall_changes_table():
+    """The pages' pitfall: rope_theta 1e4 instead of 1e6 gives other angles."""
+    a = oracle.rope_table(1e6, 256, 128)
+    b = oracle.rope_table(1e4, 256, 128)
+    assert np.array_equal(a[:, 0], b[:, 0])           # frequency 1 in both
+    assert np.count_nonzero(a[1:, 1:64] != b[1:, 1:64]) > 0.99 * 255 * 63
+
+
+# -------------------------------------------------------------- RoPE ----
+
+def test_rope_d2_is_complex_multiplication():
+    """D = 2: rotate-half is x1 + i x2 times e^(i pos)."""
+    rng = np.random.default_rng(0)
+    for _ in range(50):
+        x = rng.standard_normal(2)
+        pos = float(rng.integers(0, 32768))
+        y = oracle.rope_head_f64(x, pos, 1e6)
+        z = complex(x[0], x[1]) * cmath.exp(1j * pos)
+        assert abs(y[0] - z.real) < 1e-12 and abs(y[1] - z.imag) < 1e-12
+
+
+def test_rope_pairs_i_with_i_plus_half():
+    """One-hot inputs: e_i only mixes with e_{i+D/2}, with the signs of a
+    counter-clockwise rotation."""
+    D, pos = 8, 5.0
+    for i in range(D // 2):
+        c = math.cos(pos * 1e6 ** (-2 * i / D))
+        s = math.sin(pos * 1e6 ** (-2 * i / D))
+        e = np.zeros(D); e[i] = 1.0
+        y = oracle.rope_head_f64(e, pos, 1e6)
+        want = np.zeros(D); want[i] = c; want[i + D // 2] = s
+        np.testing.assert_allclose(y, want, atol=1e-15)
+        e = np.zeros(D); e[i + D // 2] = 1.0
+        y = oracle.rope_head_f64(e, pos, 1e6)
+        want = np.zeros(D); want[i] = -s; want[i + D // 2] = c
+        np.testing.assert_allclose(y, want, atol=1e-15)
+
+
+def test_rope_preserves_norm():
+    rng = np.random.default_rng(1)
+    for _ in range(20):
+        x = rng.standard_normal(128)
+        y = oracle.rope_head_f64(x, float(rng.integers(0, 32768)), 1e6)
+        assert abs(np.linalg.norm(y) - np.linalg.norm(x)) < 1e-12
+
+
+def test_rope_relative_position_identity():
+    """rot(q, m) . rot(k, n) depends only on m - n."""
+    rng = np.random.default_rng(2)
+    for _ in range(40):
+        q, k = rng.standard_normal(128), rng.standard_normal(128)
+        m, n, s = (float(v) for v in rng.integers(0, 16384, 3))
+        a = oracle.rope_head_f64(q, m, 1e6) @ oracle.rope_head_f64(k, n, 1e6)
+        b = oracle.rope_head_f64(q, m + s, 1e6) @ oracle.rope_head_f64(k, n + s, 1e6)
+        assert abs(a - b) < 1e-9 * (1 + abs(a))
+
+
+def test_rope_exact_position_zero_keeps_bits():
+    g = torch.Generator().manual_seed(4)
+    x = u16(torch.randn(128, generator=g).to(torch.bfloat16))
+    row = oracle.rope_table(1e6, 1, 128)[0]
+    assert np.array_equal(oracle.rope_head_exact(x, row), x)
+
+
+def test_rope_exact_within_fp32_bound_of_f64():
+    """The fp32 recipe lands within half a bf16 ulp of the exact rotation of
+    the same bf16 input plus the fp32 error of its two products and the
+    table's rounding (bounded by 4 * 2^-24 * (|x1 c| + |x2 s|))."""
+    g = torch.Generator().manual_seed(5)
+    t = oracle.rope_table(1e6, 32768, 128)
+    for pos in [1, 2, 3, 100, 4095, 17000, 32767]:
+        xb = u16(torch.randn(128, generator=g).to(torch.bfloat16))
+        y = f64(oracle.rope_head_exact(xb, t[pos]))
+        x = f64(xb)
+        ref = oracle.rope_head_f64(x, float(pos), 1e6)
+        mag = np.abs(np.concatenate([x[:64], x[64:]])) + np.abs(np.concatenate([x[64:], x[:64]]))
+        ulp = np.spacing(np.abs(ref).astype(np.float32)).astype(np.float64) * 2 ** 16
+        bound = 0.5 * ulp + 4 * 2.0 ** -24 * mag
+        assert np.all(np.abs(y - ref) <= bound), pos
+
+
+# ------------------------------------------------------------ append ----
+
+def test_append_hand_example():
+    """2 blocks of 16, one KV head, D = 8; tokens at position 0 (rotation is
+    the identity there) go to slots 17, 0, 31; a padding token (slot -1)
+    writes nothing.  Every other cache entry keeps the sentinel."""
+    H, Hkv, D, BS = 2, 1, 8, 16
+    g = torch.Generator().manual_seed(6)
+    qkv = u16(torch.randn(4, (H + 2 * Hkv) * D, generator=g).to(torch.bfloat16))
+    q_before = qkv[:, :H * D].copy()
+    kc = np.full((2, Hkv, BS, D), W.SENTINEL_BF16, dtype=np.uint16)
+    vc = kc.copy()
+    table = oracle.rope_table(1e6, 8, D)
+    err = oracle.rope_cache_append(qkv, np.zeros(4, np.int32),
+                                   np.array([17, 0, 31, -1], np.int32),
+                                   kc, vc, table, H, Hkv, D, BS)
+    assert err == 0
+    want_k = np.full_like(kc, W.SENTINEL_BF16)
+    want_v = want_k.copy()
+    for t, (blk, off) in enumerate([(1, 1), (0, 0), (1, 15)]):
+        want_k[blk, 0, off] = qkv[t, H * D:(H + 1) * D]
+        want_v[blk, 0, off] = qkv[t, (H + 1) * D:]
+    assert np.array_equal(kc, want_k) and np.array_equal(vc, want_v)
+    assert np.array_equal(qkv[:, :H * D], q_before)
+
+
+def test_append_rotates_k_and_q_at_position():
+    H, Hkv, D, BS = 2, 2, 128, 16
+    g = torch.Generator().manual_seed(7)
+    qkv = u16(torch.randn(3, (H + 2 * Hkv) * D, generator=g).to(torch.bfloat16))
+    orig = qkv.copy()
+    kc = np.full((3, Hkv, BS, D), W.SENTINEL_BF16, dtype=np.uint16)
+    vc = kc.copy()
+    table = oracle.rope_table(1e6, 100, D)
+    pos = np.array([5, 99, 40], np.int32)
+    slots = np.array([33, 2, 47], np.int32)
+    assert oracle.rope_cache_append(qkv, pos, slots, kc, vc, table, H, Hkv, D, BS) == 0
+    for t in range(3):
+        for h in range(H):
+            want = oracle.rope_head_exact(orig[t, h * D:(h + 1) * D], table[pos[t]])
+            assert np.array_equal(qkv[t, h * D:(h + 1) * D], want)
+        blk, off = divmod(int(slots[t]), BS)
+        for gh in range(Hkv):
+            kin = orig[t, (H + gh) * D:(H + gh + 1) * D]
+            assert np.array_equal(kc[blk, gh, off], oracle.rope_head_exact(kin, table[pos[t]]))
+            assert np.array_equal(vc[blk, gh, off], orig[t, (H + Hkv + gh) * D:(H + Hkv + gh + 1) * D])
+    assert np.array_equal(qkv[:, H * D:], orig[:, H * D:])   # k, v rows untouched
+
+
+def test_append_error_bits():
+    H, Hkv, D, BS = 1, 1, 8, 16
+    qkv = np.zeros((3, 3 * D), np.uint16)
+    kc = np.full((1, 1, BS, D), W.SENTINEL_BF16, np.uint16)
+    vc = kc.copy()
+    table = oracle.rope_table(1e6, 10, D)
+    err = oracle.rope_cache_append(qkv, np.array([0, 10, 1], np.int32),
+                                   np.array([16, 0, 3], np.int32), kc, vc, table,
+                                   H, Hkv, D, BS)
+    assert err == oracle.ERR_SLOT | oracle.ERR_POSITION
+    assert np.all(kc[0, 0, 0] == W.SENTINEL_BF16)    # bad-position token skipped
+    assert np.all(kc[0, 0, 3] == 0)                   # good token written
+
+
+def test_theta_pitfall_changes_cache():
+    w = W.build(0)
+    outs = []
+    for theta in (1e6, 1e4):
+        qkv, kc, vc = u16(w.qkv), u16(w.k_cache), u16(w.v_cache)
+        table = oracle.rope_table(theta, 256, 128)
+        oracle.rope_cache_append(qkv, w.positions, w.slot_mapping, kc, vc, table,
+                                 16, 8, 128, 16)
+        outs.append(kc)
+    assert not np.array_equal(outs[0], outs[1])
+
+
+# --------------------------------------------------------- attention ----
+
+def _run_workload(w, theta=1e6, partition=0):
+    qkv, kc, vc = u16(w.qkv), u16(w.k_cache), u16(w.v_cache)
+    H, Hkv, D = w.num_heads, w.num_kv_heads, w.head_dim
+    table = oracle.rope_table(theta, w.max_pos, D)
+    assert oracle.rope_cache_append(qkv, w.positions, w.slot_mapping, kc, vc, table,
+                                    H, Hkv, D, w.block_size) == 0
+    q = np.ascontiguousarray(qkv[:, :H * D])
+    cu = None if w.is_decode else w.cu_seqlens_q
+    out, err = oracle.paged_attention(q, kc, vc, w.block_tables, w.context_lens, H,
+                                      Hkv, D, w.block_size, cu_seqlens_q=cu,
+                                      partition_tokens=partition)
+    assert err == 0
+    return out, kc, vc, q
+
+
+def test_block_permutation_invariance():
+    w = W.build(0)
+    a, kca, _, _ = _run_workload(w)
+    wp = W.permute_blocks(w, seed=11)
+    b, kcb, _, _ = _run_workload(wp)
+    assert np.array_equal(a, b)
+    # logical cache identical: block x of one is block pi(x) of the other
+    for bidx in range(w.num_seqs):
+        for j in range(int(w.context_lens[bidx])):
+            x = int(w.block_tables[bidx, j // 16])
+            y = int(wp.block_tables[bidx, j // 16])
+            assert np.array_equal(kca[x, :, j % 16], kcb[y, :, j % 16])
+
+
+def test_one_token_context_returns_v_exactly():
+    w = W.custom(4, 2, ctx=[1, 1, 1], q_lens=[1, 1, 1], seed=12)
+    out, kc, vc, _ = _run_workload(w)
+    for b in range(3):
+        v = f64(vc[int(w.block_tables[b, 0]), :, 0, :])
+        assert np.array_equal(out[b], np.repeat(v, 2, axis=0))
+
+
+def test_equal_keys_average_values():
+    H, Hkv, D, BS, L = 2, 1, 128, 16, 37
+    g = torch.Generator().manual_seed(13)
+    k_row = u16(torch.randn(D, generator=g).to(torch.bfloat16))
+    kc = np.tile(k_row, (3, Hkv, BS, 1)).astype(np.uint16)
+    vc = u16(torch.randn(3, Hkv, BS, D, generator=g).to(torch.bfloat16))
+    q = u16(torch.randn(1, H * D, generator=g).to(torch.bfloat16))
+    bt = np.array([[2, 0, 1]], np.int32)
+    out, err = oracle.paged_attention(q, kc, vc, bt, np.array([L], np.int32), H, Hkv, D, BS)
+    vals = np.stack([f64(vc[bt[0, j // BS], 0, j % BS]) for j in range(L)])
+    np.testing.assert_allclose(out[0, 0], vals.mean(axis=0), rtol=0, atol=1e-13)
+    np.testing.assert_allclose(out[0, 1], vals.mean(axis=0), rtol=0, atol=1e-13)
+
+
+def _gather_contiguous(w, kc, vc, b):
+    L = int(w.context_lens[b])
+    idx = [(int(w.block_tables[b, j // 16]), j % 16) for j in range(L)]
+    k = np.stack([kc[x, :, o] for x, o in idx])   # [L, Hkv, D]
+    v = np.stack([vc[x, :, o] for x, o in idx])
+    return np.ascontiguousarray(k), np.ascontiguousarray(v)
+
+
+def test_paged_equals_contiguous():
+    w = W.build(0)
+    out, kc, vc, q = _run_workload(w)
+    for b in range(w.num_seqs):
+        k, v = _gather_contiguous(w, kc, vc, b)
+        ref = oracle.contiguous_attention(q[b:b + 1].reshape(1, 16, 128), k, v, 16, 8, 128)
+        assert np.array_equal(out[b], ref[0])
+
+
+def _numpy_attention(q, k, v, scale, causal_offset=None):
+    """Dense fp64 attention for one head: q [n, D], k/v [L, D]."""
+    s = (q @ k.T) * scale
+    if causal_offset is not None:
+        n, L = s.shape
+        mask = np.arange(L)[None, :] > (causal_offset + np.arange(n))[:, None]
+        s = np.where(mask, -np.inf, s)
+    s = s - s.max(axis=1, keepdims=True)
+    p = np.exp(s)
+    p /= p.sum(axis=1, keepdims=True)
+    return p @ v
+
+
+def test_mha_case_matches_dense_numpy():
+    w = W.custom(4, 4, ctx=[50, 7], q_lens=[1, 1], seed=14)
+    out, kc, vc, q = _run_workload(w)
+    for b in range(2):
+        k, v = _gather_contiguous(w, kc, vc, b)
+        for h in range(4):
+            ref = _numpy_attention(f64(q[b, h * 128:(h + 1) * 128])[None],
+                                   f64(k[:, h]), f64(v[:, h]), 128 ** -0.5)
+            np.testing.assert_allclose(out[b, h], ref[0], rtol=1e-12, atol=1e-13)
+
+
+def test_gqa_equals_mha_on_repeated_heads():
+    """Query head h uses KV head h // G: GQA equals MHA over K/V heads
+    repeated G times consecutively."""
+    H, Hkv, D, BS, G = 8, 2, 128, 16, 4
+    g = torch.Generator().manual_seed(15)
+    kc = u16(torch.randn(6, Hkv, BS, D, generator=g).to(torch.bfloat16))
+    vc = u16(torch.randn(6, Hkv, BS, D, generator=g).to(torch.bfloat16))
+    q = u16(torch.randn(2, H * D, generator=g).to(torch.bfloat16))
+    bt = np.array([[5, 1, 3], [0, 2, 4]], np.int32)
+    cl = np.array([40, 33], np.int32)
+    gqa, e1 = oracle.paged_attention(q, kc, vc, bt, cl, H, Hkv, D, BS)
+    mha, e2 = oracle.paged_attention(q, np.ascontiguousarray(np.repeat(kc, G, axis=1)),
+                                     np.ascontiguousarray(np.repeat(vc, G, axis=1)),
+                                     bt, cl, H, H, D, BS)
+    assert e1 == e2 == 0 and np.array_equal(gqa, mha)
+
+
+def test_brute_force_multiprecision():
+    """Tiny integer-valued inputs, D in {4, 8}, L <= 5, blocks of 2 tokens:
+    the softmax is evaluated with 40-digit arithmetic."""
+    mp = pytest.importorskip("mpmath")
+    mp.mp.dps = 40
+    rng = np.random.default_rng(16)
+    for D in (4, 8):
+        for L in range(1, 6):
+            H, Hkv, BS = 2, 1, 2
+            nb = (L + BS - 1) // BS
+            q = rng.integers(-3, 4, (1, H * D)).astype(np.float64)
+            k = rng.integers(-3, 4, (nb, Hkv, BS, D)).astype(np.float64)
+            v = rng.integers(-3, 4, (nb, Hkv, BS, D)).astype(np.float64)
+            perm = rng.permutation(nb).astype(np.int32)
+            kc = np.empty_like(k); vc = np.empty_like(v)
+            kc[perm] = k; vc[perm] = v      # logical block i lives at perm[i]
+            out, err = oracle.paged_attention(bf16_of(q), bf16_of(kc), bf16_of(vc),
+                                              perm[None, :], np.array([L], np.int32),
+                                              H, Hkv, D, BS)
+            assert err == 0
+            scale = mp.mpf(D) ** mp.mpf(-0.5)
+            for h in range(H):
+                z = [scale * sum(mp.mpf(q[0, h * D + d]) * mp.mpf(k[j // BS, 0, j % BS, d])
+                                 for d in range(D)) for j in range(L)]
+                e = [mp.e ** zi for zi in z]
+                tot = sum(e)
+                for d in range(D):
+                    ref = sum(e[j] * mp.mpf(v[j // BS, 0, j % BS, d]) for j in range(L)) / tot
+                    assert abs(out[0, h, d] - float(ref)) <= 1e-13 * (1 + abs(float(ref)))
+
+
+@pytest.mark.parametrize("partition", [1, 3, 16, 100, 512])
+def test_split_kv_merge_equals_unsplit(partition):
+    w = W.build(0)
+    a, *_ = _run_workload(w)
+    b, *_ = _run_workload(w, partition=partition)
+    np.testing.assert_allclose(b, a, rtol=1e-12, atol=1e-13)
+
+
+def test_chunked_prefill_equals_successive_decodes():
+    """A chunk of n queries at the end of a context of L equals n decode
+    steps with contexts L - n + 1 .. L."""
+    n, L = 9, 40
+    w = W.custom(4, 2, ctx=[L], q_lens=[n], seed=17)
+    out, kc, vc, q = _run_workload(w)
+    for i in range(n):
+        d, err = oracle.paged_attention(q[i:i + 1], kc, vc, w.block_tables,
+                                        np.array([L - n + 1 + i], np.int32), 4, 2, 128, 16)
+        assert err == 0 and np.array_equal(d[0], out[i])
+
+
+def test_full_causal_prefill_matches_dense_numpy():
+    L = 23
+    w = W.custom(2, 1, ctx=[L], q_lens=[L], seed=18)
+    out, kc, vc, q = _run_workload(w)
+    k, v = _gather_contiguous(w, kc, vc, 0)
+    for h in range(2):
+        ref = _numpy_attention(f64(q[:, h * 128:(h + 1) * 128]), f64(k[:, 0]), f64(v[:, 0]),
+                               128 ** -0.5, causal_offset=0)
+        np.testing.assert_allclose(out[:, h], ref, rtol=1e-12, atol=1e-13)
+    assert np.array_equal(out[0, 0], f64(v[0, 0]))
+
+
+def test_attention_error_rows():
+    H, Hkv, D, BS = 2, 1, 8, 16
+    kc = np.zeros((2, Hkv, BS, D), np.uint16)
+    vc = np.full((2, Hkv, BS, D), 0x3F80, np.uint16)   # 1.0
+    q = np.zeros((3, H * D), np.uint16)
+    bt = np.array([[0, 1], [7, 1], [1, 0]], np.int32)
+    cl = np.array([0, 5, 20], np.int32)
+    out, err = oracle.paged_attention(q, kc, vc, bt, cl, H, Hkv, D, BS)
+    assert err == oracle.ERR_CONTEXT | oracle.ERR_BLOCK
+    assert np.all(out[0] == 0) and np.all(out[1] == 0)
+    assert np.allclose(out[2], 1.0)
+
+
+def test_workload_recipes():
+    """The five workloads have the shapes their descriptions give."""
+    w = W.build(0)
+    assert w.context_lens.tolist() == [17, 64, 100, 255] and w.num_blocks == 64
+    assert sorted(w.block_tables[w.block_tables >= 0].tolist()) != []
+    w = W.build(1)
+    assert w.num_seqs == 64 and int(w.context_lens.min()) >= 128 and int(w.context_lens.max()) <= 4096
+    w = W.build(2)
+    assert w.num_tokens == 2108 and w.q_lens[:4] == [512] * 4 and w.q_lens[4:] == [1] * 60
+    assert w.num_seqs == 64
+    w = W.build(4)
+    bt = w.block_tables
+    assert w.num_seqs == 128 and bool((bt[:, :128] == bt[0, :128]).all())
+    assert int(w.context_lens.min()) >= 2048 + 64 and int(w.context_lens.max()) <= 2048 + 512
