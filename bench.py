@@ -1,0 +1,514 @@
+"""Benchmark of one attention step over a paged KV cache on GB300.
+
+A step is the whole path for one batch: RoPE + cache append of the new tokens
+(qattn_rope_cache_append), then paged GQA attention (qattn_paged_decode for a
+decode workload, qattn_varlen_prefill for a mixed one).  Inputs are resident
+in HBM when timing starts; L2 is flushed (a 512 MB buffer is written)
+before every timed step, and each step is timed with CUDA events on the
+launching stream.  The headline workload is the Qwen2-7B-shaped decode step
+(28 query / 4 KV heads, head_dim 128, batch 64, contexts U[128, 4096], block
+size 16, random block placement).
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle on a
+bounded sample of the same workload instead.
+
+Multi-GPU (torchrun): every rank runs its own replica of the workload (the
+step shards by sequence with no exchange), the time is the max over ranks and
+the value counts all ranks' bytes ("scaling": "weak").
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from paged_kv_gqa_07_gb300 import workloads as W  # noqa: E402
+
+METRIC = "paged GQA decode: KV HBM GB/s (% of GB300 peak), seqs/s; prefill tokens/s"
+DEFAULT_WORKLOAD = "qwen2_7b_decode_b64"
+L2_FLUSH_BYTES = 512 << 20
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=W.WORKLOAD_NAMES)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-clocks", action="store_true")
+    return p.parse_args()
+
+
+# ----------------------------------------------------------- distributed --
+
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            if backend == "nccl":
+                torch.cuda.set_device(self.local_rank)
+            dist.init_process_group(backend)
+            self.pg = dist
+
+    @classmethod
+    def single(cls):
+        d = cls.__new__(cls)
+        d.world, d.rank, d.local_rank, d.pg = int(os.environ.get("WORLD_SIZE", "1")), 0, 0, None
+        return d
+
+    def barrier(self):
+        if self.pg is not None:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if self.pg is None:
+            return x
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def sum(self, x: float) -> float:
+        if self.pg is None:
+            return x
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.SUM)
+        return float(t.item())
+
+    def close(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+# ---------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, local_index: int, enabled=True):
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        ids = [x.strip() for x in vis.split(",") if x.strip()]
+        self.gpu = ids[local_index] if local_index < len(ids) else str(local_index)
+        self.enabled = enabled
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        if not self.enabled:
+            return self
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=2)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.lines:
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ peaks etc --
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def kernel_source_sha(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "paged_kv_gqa_07_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, workload: str, sha: str):
+    """DRAM bytes per launch from the committed ncu summary of this kernel on
+    this workload, if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.txt")
+    try:
+        kv = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("source_sha") != sha:
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+# ----------------------------------------------------------------- ours --
+
+def run_ours(args, dist: Dist):
+    import numpy as np  # noqa: F401
+    from paged_kv_gqa_07_gb300 import build as B
+    from paged_kv_gqa_07_gb300 import qattn as Q
+
+    B.build()
+    Q.load_library()
+    dev = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(dev)
+    w = W.build(args.workload, seed=W.SEED_BASE + W.WORKLOAD_NAMES.index(args.workload) + 1000 * dist.rank)
+    H, Hkv, D, BS = w.num_heads, w.num_kv_heads, w.head_dim, w.block_size
+    dims = Q.make_dims(H, Hkv, D, BS)
+    g = W.to_device(w, dev)
+    qkv0 = g.qkv.clone()
+    table = Q.qattn_rope_table_build(w.max_pos, D, w.theta).to(dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    decode = w.is_decode
+    max_ctx = w.max_context_len
+    ws_size = (Q.qattn_paged_decode_workspace_size(w.num_seqs, max_ctx, dims) if decode
+               else Q.qattn_varlen_prefill_workspace_size(w.num_seqs, max_ctx, dims))
+    ws = torch.empty(max(ws_size, 256), dtype=torch.uint8, device=dev)
+    out = torch.empty((w.num_tokens, H, D), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def append():
+        Q.qattn_rope_cache_append(g.q_view(), g.k_view(), g.v_view(), g.positions, g.slot_mapping,
+                                  g.k_cache, g.v_cache, table, dims, err)
+
+    def attend():
+        if decode:
+            Q.qattn_paged_decode(out, g.q_view(), g.k_cache, g.v_cache, g.block_tables,
+                                 g.context_lens, max_ctx, dims, ws, err)
+        else:
+            Q.qattn_varlen_prefill(out, g.q_view(), g.cu_seqlens_q, w.max_q_len, g.k_cache,
+                                   g.v_cache, g.block_tables, g.context_lens, max_ctx, dims, ws,
+                                   err)
+
+    for _ in range(args.warmup):
+        g.qkv.copy_(qkv0)
+        append()
+        attend()
+    torch.cuda.synchronize(dev)
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    with ClockSampler(dev.index, enabled=not args.no_clocks) as clocks:
+        dist.barrier()
+        torch.cuda.synchronize(dev)
+        for s in range(args.steps):
+            flush.fill_(s & 0xff)        # evict the cache and KV from L2
+            g.qkv.copy_(qkv0)            # every step starts from the same rows
+            ev[s][0].record(stream)
+            append()
+            ev[s][1].record(stream)
+            attend()
+            ev[s][2].record(stream)
+        torch.cuda.synchronize(dev)
+        dist.barrier()
+    assert int(err.item()) == 0, f"device error bits {int(err.item())}"
+    step_ms = [ev[s][0].elapsed_time(ev[s][2]) for s in range(args.steps)]
+    attn_ms = [ev[s][1].elapsed_time(ev[s][2]) for s in range(args.steps)]
+    app_ms = [ev[s][0].elapsed_time(ev[s][1]) for s in range(args.steps)]
+    local_total_ms = sum(step_ms)
+    total_ms = dist.max(local_total_ms)
+    ms_per_step = total_ms / args.steps
+
+    kv_bytes = w.kv_bytes_read()
+    qo_bytes = 2 * w.num_tokens * H * D * 2
+    all_kv = dist.sum(kv_bytes)
+    value = all_kv * args.steps / (total_ms * 1e-3) / 1e9
+    seqs_per_s = dist.sum(w.num_seqs) * args.steps / (total_ms * 1e-3)
+    tokens_per_s = dist.sum(w.num_tokens) * args.steps / (total_ms * 1e-3)
+
+    hbm_peak, tf_peak, peak_kind = measured_peaks()
+    attn_avg_s = statistics.mean(attn_ms) * 1e-3
+    result = {}
+    if decode:
+        alg = kv_bytes + qo_bytes
+        achieved = alg / attn_avg_s / 1e9
+        sha = kernel_source_sha(["paged_decode.cu", "common.cuh"])
+        traffic = profiled_traffic("paged_decode_kernel", args.workload, sha)
+        result["roofline"] = {"bound": "hbm", "kernel": "paged_decode_kernel (+ decode_merge_kernel)",
+                              "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                              "frac": round(achieved / hbm_peak, 4), "peak_kind": peak_kind,
+                              "traffic": traffic, "algorithmic_bytes_per_launch": alg}
+    else:
+        flops = 4 * D * w.causal_pairs()
+        achieved = flops / attn_avg_s / 1e12
+        result["roofline"] = {"bound": "tensor", "kernel": "varlen prefill + decode rows",
+                              "achieved": round(achieved, 2), "peak": tf_peak, "unit": "TFLOP/s",
+                              "frac": round(achieved / tf_peak, 4), "peak_kind": peak_kind,
+                              "traffic": None, "algorithmic_flops_per_launch": flops}
+
+    # ---- end to end through the C ABI with host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, w, dims, g, table, ws, err, dev, decode, max_ctx, dist)
+
+    clk = clocks.summary()
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": dist.world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) q/k/v and cache, random block placement)",
+        "config": {"workload": args.workload, "num_heads": H, "num_kv_heads": Hkv,
+                   "head_dim": D, "block_size": BS, "batch": w.num_seqs,
+                   "new_tokens": w.num_tokens, "kv_bytes_per_step": kv_bytes,
+                   "max_context_len": max_ctx, "l2": "flushed before every timed step (512 MB write)",
+                   "parallelism": f"replicas x{dist.world}"},
+        "seqs_per_s": round(seqs_per_s, 1),
+        "tokens_per_s": round(tokens_per_s, 1),
+        "append_ms": round(statistics.mean(app_ms), 5),
+        "attention_ms": round(statistics.mean(attn_ms), 5),
+        "gpu_launches": 3 * args.steps if decode else 4 * args.steps,
+        **result,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if clk is not None:
+        line["clocks"] = clk
+    if dist.rank == 0 and not args.no_cpu_baseline and dist.world == 1:
+        line["cpu_baseline"] = cpu_baseline(w, kv_bytes)
+    return line
+
+
+def run_e2e(args, w, dims, g, table, ws, err, dev, decode, max_ctx, dist):
+    """Same step through the public API, inputs copied from pinned host memory
+    each step and the attention output read back."""
+    from paged_kv_gqa_07_gb300 import qattn as Q
+
+    H, D = w.num_heads, w.head_dim
+    host_in = {k: getattr(w, k).pin_memory() for k in
+               ("qkv", "positions", "slot_mapping", "block_tables", "context_lens", "cu_seqlens_q")}
+    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
+    out = torch.empty((w.num_tokens, H, D), dtype=torch.bfloat16, device=dev)
+    host_out = torch.empty_like(out, device="cpu").pin_memory()
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    Hkv = w.num_kv_heads
+
+    def step():
+        for k in host_in:
+            dev_in[k].copy_(host_in[k], non_blocking=True)
+        qkv = dev_in["qkv"]
+        Q.qattn_rope_cache_append(qkv[:, :H * D], qkv[:, H * D:(H + Hkv) * D],
+                                  qkv[:, (H + Hkv) * D:], dev_in["positions"],
+                                  dev_in["slot_mapping"], g.k_cache, g.v_cache, table, dims, err)
+        if decode:
+            Q.qattn_paged_decode(out, qkv[:, :H * D], g.k_cache, g.v_cache, dev_in["block_tables"],
+                                 dev_in["context_lens"], max_ctx, dims, ws, err)
+        else:
+            Q.qattn_varlen_prefill(out, qkv[:, :H * D], dev_in["cu_seqlens_q"], w.max_q_len,
+                                   g.k_cache, g.v_cache, dev_in["block_tables"],
+                                   dev_in["context_lens"], max_ctx, dims, ws, err)
+        host_out.copy_(out, non_blocking=True)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    dist.barrier()
+    for s in range(args.steps):
+        flush.fill_(s & 0xff)
+        evs[s][0].record(stream)
+        step()
+        evs[s][1].record(stream)
+    torch.cuda.synchronize(dev)
+    dist.barrier()
+    total_ms = dist.max(sum(a.elapsed_time(b) for a, b in evs))
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = host_out.numel() * host_out.element_size()
+    value = dist.sum(w.kv_bytes_read()) * args.steps / (total_ms * 1e-3) / 1e9
+    return {"value": round(value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(total_ms / args.steps, 5)}
+
+
+# --------------------------------------------------------------- oracle --
+
+def oracle_sample(w: W.Workload, n_seqs: int):
+    """The first n_seqs sequences of the workload as a smaller workload."""
+    q_lens = w.q_lens[:n_seqs]
+    T = sum(q_lens)
+    sub = dict(w.__dict__)
+    sub.update(qkv=w.qkv[:T].contiguous(), positions=w.positions[:T].contiguous(),
+               slot_mapping=w.slot_mapping[:T].contiguous(),
+               block_tables=w.block_tables[:n_seqs].contiguous(),
+               context_lens=w.context_lens[:n_seqs].contiguous(),
+               cu_seqlens_q=w.cu_seqlens_q[:n_seqs + 1].contiguous(), q_lens=q_lens)
+    return W.Workload(**sub)
+
+
+def oracle_time(w: W.Workload, n_seqs: int, reps: int = 1):
+    """Seconds per oracle step (append + attention) on a sample, and its KV bytes."""
+    import numpy as np
+
+    import oracle
+
+    s = oracle_sample(w, n_seqs)
+    H, Hkv, D, BS = s.num_heads, s.num_kv_heads, s.head_dim, s.block_size
+    table = oracle.rope_table(s.theta, s.max_pos, D)
+
+    def u16(t):
+        return t.contiguous().view(torch.int16).numpy().view(np.uint16).copy()
+    kc0, vc0 = u16(s.k_cache), u16(s.v_cache)
+    times = []
+    for _ in range(reps):
+        qkv = u16(s.qkv)
+        kc, vc = kc0.copy(), vc0.copy()
+        t0 = time.perf_counter()
+        oracle.rope_cache_append(qkv, s.positions, s.slot_mapping, kc, vc, table, H, Hkv, D, BS)
+        q = np.ascontiguousarray(qkv[:, :H * D])
+        oracle.paged_attention(q, kc, vc, s.block_tables, s.context_lens, H, Hkv, D, BS,
+                               cu_seqlens_q=None if s.is_decode else s.cu_seqlens_q)
+        times.append(time.perf_counter() - t0)
+    return statistics.median(times), s.kv_bytes_read(), s
+
+
+def sample_size(w: W.Workload) -> int:
+    """Sequences per oracle step: the whole batch unless that is more than
+    about 2e9 fp64 multiply-adds (a few seconds on the host)."""
+    per_seq = [2 * w.num_heads * w.head_dim * int(L) * q for L, q in
+               zip(w.context_lens.tolist(), w.q_lens)]
+    n, tot = 0, 0
+    for c in per_seq:
+        if n > 0 and tot + c > 2e9:
+            break
+        n, tot = n + 1, tot + c
+    return max(1, n)
+
+
+def cpu_baseline(w: W.Workload, kv_bytes_full: int, budget_s: float = 10.0):
+    """The oracle, as it stands, timed on this host: repeated over a sample
+    of the workload for about budget_s seconds."""
+    import oracle
+    n = sample_size(w)
+    total, reps, kvb = 0.0, 0, 0
+    while total < budget_s or reps == 0:
+        sec, kvb, _ = oracle_time(w, n)
+        total += sec
+        reps += 1
+    return {"value": round(kvb * reps / total / 1e9, 4), "unit": "GB/s",
+            "cores": oracle.default_threads(), "kind": "oracle",
+            "sample": f"first {n} of {w.num_seqs} sequences ({kvb} of {kv_bytes_full} KV bytes) "
+                      f"x {reps} repetitions, append + attention in fp64, {total:.1f} s"}
+
+
+def run_reference(args, dist: Dist):
+    import oracle
+    w = W.build(args.workload)
+    n = sample_size(w)
+    for _ in range(args.warmup):
+        oracle_time(w, n)
+    t0 = time.perf_counter()
+    per = []
+    for _ in range(args.steps):
+        sec, kvb, s = oracle_time(w, n)
+        per.append(sec)
+    total = time.perf_counter() - t0
+    value = kvb * args.steps / sum(per) / 1e9
+    sample = (f"first {n} of {w.num_seqs} sequences per step ({kvb} KV bytes), "
+              "append + attention in fp64")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * sum(per) / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "batch_sampled": n},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "kind": "oracle",
+                         "cores": oracle.default_threads(), "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "wall_s": round(total, 2),
+    }
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        # The reference arm is the CPU oracle: rank 0 alone runs it.
+        if int(os.environ.get("RANK", "0")) == 0:
+            print(json.dumps(run_reference(args, Dist.single())), flush=True)
+        return
+    dist = Dist()
+    try:
+        line = run_ours(args, dist)
+        if dist.rank == 0:
+            print(json.dumps(line), flush=True)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()

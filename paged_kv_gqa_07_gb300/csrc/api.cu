@@ -1,0 +1,346 @@
+// C-ABI layer of the qattn library: argument validation, launch sizing,
+// tensor-map encoding and status strings.  No device memory is allocated
+// here; every buffer belongs to the caller.
+#include <math.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+using namespace qattn;
+
+namespace {
+
+constexpr int kVersion = 100;  // 0.1.0
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_dims(const qattn_dims& d) {
+  if (d.num_heads <= 0 || d.num_kv_heads <= 0 || d.head_dim <= 0 || d.block_size <= 0)
+    return QATTN_ERR_INVALID_ARG;
+  if (d.head_dim != kHeadDim || d.block_size != kBlockSize) return QATTN_ERR_UNSUPPORTED;
+  if (d.num_heads % d.num_kv_heads != 0) return QATTN_ERR_UNSUPPORTED;
+  if (d.num_heads / d.num_kv_heads > 8 || d.num_heads > 128) return QATTN_ERR_UNSUPPORTED;
+  if (!(d.scale == d.scale) || isinf(d.scale)) return QATTN_ERR_INVALID_ARG;
+  return QATTN_OK;
+}
+
+float scale_of(const qattn_dims& d) {
+  return d.scale > 0.f ? d.scale : 1.0f / sqrtf(static_cast<float>(d.head_dim));
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ------------------------------------------------------------ device info --
+
+int num_sms_current() {
+  static std::mutex mu;
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+  std::lock_guard<std::mutex> lk(mu);
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+// ------------------------------------------------------------ tensor maps --
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// The paged cache [num_blocks][Hkv][16][128] bf16 seen as a 2-D tensor of
+// num_blocks * Hkv * 16 rows by 128 columns; a box is 16 rows x 64 columns
+// (128 bytes, the widest a 128-byte swizzle allows), so one (block, kv head)
+// tile is two boxes at x = 0 and x = 64.
+bool encode_cache_map(CUtensorMap* map, const void* cache, int32_t num_blocks,
+                      int32_t num_kv_heads) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim),
+                              static_cast<cuuint64_t>(num_blocks) * num_kv_heads * kBlockSize};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDim) * 2};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kBlockSize)};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(cache), dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// A small cache of encoded maps: the same caches are used call after call.
+struct MapEntry {
+  const void* ptr;
+  int32_t num_blocks;
+  int32_t num_kv_heads;
+  CUtensorMap map;
+};
+
+bool cached_cache_map(CUtensorMap* out, const void* cache, int32_t num_blocks,
+                      int32_t num_kv_heads) {
+  static std::mutex mu;
+  static MapEntry entries[16];
+  static int used = 0, next = 0;
+  std::lock_guard<std::mutex> lk(mu);
+  for (int i = 0; i < used; ++i) {
+    if (entries[i].ptr == cache && entries[i].num_blocks == num_blocks &&
+        entries[i].num_kv_heads == num_kv_heads) {
+      *out = entries[i].map;
+      return true;
+    }
+  }
+  MapEntry e;
+  e.ptr = cache;
+  e.num_blocks = num_blocks;
+  e.num_kv_heads = num_kv_heads;
+  if (!encode_cache_map(&e.map, cache, num_blocks, num_kv_heads)) return false;
+  entries[next] = e;
+  next = (next + 1) % 16;
+  if (used < 16) ++used;
+  *out = e.map;
+  return true;
+}
+
+int check_cache(const void* k_cache, const void* v_cache, int32_t num_blocks,
+                const qattn_dims& d) {
+  if (k_cache == nullptr || v_cache == nullptr || num_blocks <= 0) return QATTN_ERR_INVALID_ARG;
+  if (!aligned16(k_cache) || !aligned16(v_cache)) return QATTN_ERR_INVALID_ARG;
+  // TMA row coordinates are 32-bit.
+  if (static_cast<int64_t>(num_blocks) * d.num_kv_heads * kBlockSize >= (1ll << 31))
+    return QATTN_ERR_UNSUPPORTED;
+  return QATTN_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? QATTN_OK : QATTN_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* qattn_status_string(int status) {
+  switch (status) {
+    case QATTN_OK: return "ok";
+    case QATTN_ERR_INVALID_ARG: return "invalid argument";
+    case QATTN_ERR_UNSUPPORTED: return "unsupported shape";
+    case QATTN_ERR_CUDA: return "CUDA error";
+    case QATTN_ERR_WORKSPACE: return "workspace missing or too small";
+    default: return "unknown status";
+  }
+}
+
+int qattn_version(void) { return kVersion; }
+
+int qattn_rope_table_build(float* host_cos_sin, int32_t max_pos, int32_t head_dim,
+                           double theta) {
+  if (host_cos_sin == nullptr || max_pos <= 0 || head_dim <= 0 || (head_dim & 1) ||
+      !(theta > 0.0))
+    return QATTN_ERR_INVALID_ARG;
+  const int32_t half = head_dim / 2;
+  for (int32_t i = 0; i < half; ++i) {
+    const double inv_freq = pow(theta, -(2.0 * i) / head_dim);
+    for (int32_t pos = 0; pos < max_pos; ++pos) {
+      const double ang = static_cast<double>(pos) * inv_freq;
+      host_cos_sin[static_cast<int64_t>(pos) * head_dim + i] = static_cast<float>(cos(ang));
+      host_cos_sin[static_cast<int64_t>(pos) * head_dim + half + i] =
+          static_cast<float>(sin(ang));
+    }
+  }
+  return QATTN_OK;
+}
+
+int qattn_rope_cache_append(void* q, int64_t q_row_stride, const void* k, int64_t k_row_stride,
+                            const void* v, int64_t v_row_stride, const int32_t* positions,
+                            const int32_t* slot_mapping, int32_t num_tokens, void* k_cache,
+                            void* v_cache, int32_t num_blocks, const float* cos_sin,
+                            int32_t max_pos, qattn_dims dims, int32_t* err_word, void* stream) {
+  int st = check_dims(dims);
+  if (st != QATTN_OK) return st;
+  if (num_tokens < 0) return QATTN_ERR_INVALID_ARG;
+  if (num_tokens == 0) return QATTN_OK;
+  if (q == nullptr || k == nullptr || v == nullptr || positions == nullptr ||
+      slot_mapping == nullptr || cos_sin == nullptr || max_pos <= 0)
+    return QATTN_ERR_INVALID_ARG;
+  st = check_cache(k_cache, v_cache, num_blocks, dims);
+  if (st != QATTN_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(cos_sin))
+    return QATTN_ERR_INVALID_ARG;
+  if (q_row_stride % 8 || k_row_stride % 8 || v_row_stride % 8) return QATTN_ERR_INVALID_ARG;
+  if (q_row_stride < static_cast<int64_t>(dims.num_heads) * kHeadDim ||
+      k_row_stride < static_cast<int64_t>(dims.num_kv_heads) * kHeadDim ||
+      v_row_stride < static_cast<int64_t>(dims.num_kv_heads) * kHeadDim)
+    return QATTN_ERR_INVALID_ARG;
+  RopeAppendArgs a;
+  a.q = q;
+  a.q_row_stride = q_row_stride;
+  a.k = k;
+  a.k_row_stride = k_row_stride;
+  a.v = v;
+  a.v_row_stride = v_row_stride;
+  a.positions = positions;
+  a.slot_mapping = slot_mapping;
+  a.num_tokens = num_tokens;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.num_blocks = num_blocks;
+  a.cos_sin = cos_sin;
+  a.max_pos = max_pos;
+  a.num_heads = dims.num_heads;
+  a.num_kv_heads = dims.num_kv_heads;
+  a.err_word = err_word;
+  return cuda_status(launch_rope_append(a, static_cast<cudaStream_t>(stream)));
+}
+
+size_t qattn_paged_decode_workspace_size(int32_t num_seqs, int32_t max_context_len,
+                                         qattn_dims dims) {
+  if (check_dims(dims) != QATTN_OK || num_seqs < 0 || max_context_len < 0) return 0;
+  return decode_workspace_bytes(num_seqs, max_context_len, dims.num_kv_heads,
+                                dims.num_heads / dims.num_kv_heads);
+}
+
+namespace {
+
+int decode_common(void* out, const void* q, int64_t q_row_stride, const int32_t* cu_seqlens_q,
+                  const void* k_cache, const void* v_cache, int32_t num_blocks,
+                  const int32_t* block_tables, int32_t max_blocks_per_seq,
+                  const int32_t* context_lens, int32_t num_seqs, int32_t max_context_len,
+                  const qattn_dims& dims, void* workspace, size_t workspace_bytes,
+                  int32_t* err_word, cudaStream_t stream, const CUtensorMap& kmap,
+                  const CUtensorMap& vmap, int num_sms) {
+  const size_t need = qattn_paged_decode_workspace_size(num_seqs, max_context_len, dims);
+  if (workspace == nullptr || workspace_bytes < need ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return QATTN_ERR_WORKSPACE;
+  DecodeArgs a;
+  a.out = out;
+  a.q = q;
+  a.q_row_stride = q_row_stride;
+  a.cu_seqlens_q = cu_seqlens_q;
+  a.context_lens = context_lens;
+  a.block_tables = block_tables;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.num_seqs = num_seqs;
+  a.num_blocks = num_blocks;
+  a.max_context_len = max_context_len;
+  a.num_heads = dims.num_heads;
+  a.num_kv_heads = dims.num_kv_heads;
+  a.scale_log2 = scale_of(dims) * kLog2e;
+  a.err_word = err_word;
+  a.ws = carve_decode_workspace(workspace, num_seqs, max_context_len, dims.num_kv_heads,
+                                dims.num_heads / dims.num_kv_heads);
+  return cuda_status(launch_paged_decode(a, kmap, vmap, num_sms, stream));
+}
+
+int check_attention_args(void* out, const void* q, int64_t q_row_stride, const void* k_cache,
+                         const void* v_cache, int32_t num_blocks, const int32_t* block_tables,
+                         int32_t max_blocks_per_seq, const int32_t* context_lens,
+                         int32_t max_context_len, const qattn_dims& dims) {
+  if (out == nullptr || q == nullptr || block_tables == nullptr || context_lens == nullptr)
+    return QATTN_ERR_INVALID_ARG;
+  if (max_blocks_per_seq <= 0 || max_context_len <= 0) return QATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(out) || q_row_stride % 8 ||
+      q_row_stride < static_cast<int64_t>(dims.num_heads) * kHeadDim)
+    return QATTN_ERR_INVALID_ARG;
+  return check_cache(k_cache, v_cache, num_blocks, dims);
+}
+
+}  // namespace
+
+int qattn_paged_decode(void* out, const void* q, int64_t q_row_stride, const void* k_cache,
+                       const void* v_cache, int32_t num_blocks, const int32_t* block_tables,
+                       int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t num_seqs,
+                       int32_t max_context_len, qattn_dims dims, void* workspace,
+                       size_t workspace_bytes, int32_t* err_word, void* stream) {
+  int st = check_dims(dims);
+  if (st != QATTN_OK) return st;
+  if (num_seqs < 0) return QATTN_ERR_INVALID_ARG;
+  if (num_seqs == 0) return QATTN_OK;
+  st = check_attention_args(out, q, q_row_stride, k_cache, v_cache, num_blocks, block_tables,
+                            max_blocks_per_seq, context_lens, max_context_len, dims);
+  if (st != QATTN_OK) return st;
+  CUtensorMap kmap, vmap;
+  if (!cached_cache_map(&kmap, k_cache, num_blocks, dims.num_kv_heads) ||
+      !cached_cache_map(&vmap, v_cache, num_blocks, dims.num_kv_heads))
+    return QATTN_ERR_CUDA;
+  const int sms = num_sms_current();
+  if (sms <= 0) return QATTN_ERR_CUDA;
+  return decode_common(out, q, q_row_stride, nullptr, k_cache, v_cache, num_blocks, block_tables,
+                       max_blocks_per_seq, context_lens, num_seqs, max_context_len, dims,
+                       workspace, workspace_bytes, err_word, static_cast<cudaStream_t>(stream),
+                       kmap, vmap, sms);
+}
+
+size_t qattn_varlen_prefill_workspace_size(int32_t num_seqs, int32_t max_context_len,
+                                           qattn_dims dims) {
+  return qattn_paged_decode_workspace_size(num_seqs, max_context_len, dims);
+}
+
+int qattn_varlen_prefill(void* out, const void* q, int64_t q_row_stride,
+                         const int32_t* cu_seqlens_q, int32_t num_seqs, int32_t total_q,
+                         int32_t max_q_len, const void* k_cache, const void* v_cache,
+                         int32_t num_blocks, const int32_t* block_tables,
+                         int32_t max_blocks_per_seq, const int32_t* context_lens,
+                         int32_t max_context_len, qattn_dims dims, void* workspace,
+                         size_t workspace_bytes, int32_t* err_word, void* stream) {
+  int st = check_dims(dims);
+  if (st != QATTN_OK) return st;
+  if (num_seqs < 0 || total_q < 0 || max_q_len < 0) return QATTN_ERR_INVALID_ARG;
+  if (num_seqs == 0 || total_q == 0) return QATTN_OK;
+  if (cu_seqlens_q == nullptr || max_q_len == 0) return QATTN_ERR_INVALID_ARG;
+  st = check_attention_args(out, q, q_row_stride, k_cache, v_cache, num_blocks, block_tables,
+                            max_blocks_per_seq, context_lens, max_context_len, dims);
+  if (st != QATTN_OK) return st;
+  CUtensorMap kmap, vmap;
+  if (!cached_cache_map(&kmap, k_cache, num_blocks, dims.num_kv_heads) ||
+      !cached_cache_map(&vmap, v_cache, num_blocks, dims.num_kv_heads))
+    return QATTN_ERR_CUDA;
+  const int sms = num_sms_current();
+  if (sms <= 0) return QATTN_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // Decode rows (one query) of the batch.
+  st = decode_common(out, q, q_row_stride, cu_seqlens_q, k_cache, v_cache, num_blocks,
+                     block_tables, max_blocks_per_seq, context_lens, num_seqs, max_context_len,
+                     dims, workspace, workspace_bytes, err_word, s, kmap, vmap, sms);
+  if (st != QATTN_OK || max_q_len < 2) return st;
+  // Prefill rows (two or more queries): tensor-core kernel.
+  PrefillArgs p;
+  p.out = out;
+  p.q = q;
+  p.q_row_stride = q_row_stride;
+  p.cu_seqlens_q = cu_seqlens_q;
+  p.context_lens = context_lens;
+  p.block_tables = block_tables;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.num_seqs = num_seqs;
+  p.num_blocks = num_blocks;
+  p.max_q_len = max_q_len;
+  p.max_context_len = max_context_len;
+  p.num_heads = dims.num_heads;
+  p.num_kv_heads = dims.num_kv_heads;
+  p.scale_log2 = scale_of(dims) * kLog2e;
+  p.err_word = err_word;
+  const cudaError_t e = launch_varlen_prefill(p, kmap, vmap, sms, s);
+  return e == cudaErrorNotSupported ? QATTN_ERR_UNSUPPORTED : cuda_status(e);
+}
+
+}  // extern "C"

@@ -1,0 +1,637 @@
+// Kernels K2 (paged GQA decode) and K2r (split merge).
+//
+// What is computed: for every decode sequence b and query head h, with KV
+// head g = h / G (G = num_heads / num_kv_heads),
+//     out[b, h] = sum_j softmax_j(scale * q[b, h] . k_j) v_j,  j < L_b,
+// keys and values gathered through the sequence's block table -- the
+// grouped-query attention with scaling head_dim ** -0.5 of
+// "Qwen2 模型结构代码详解" section 2 over the PagedAttention block cache of
+// the vLLM-deploys-Qwen notes section 2.1.
+//
+// Design (GB300): the decode step is bound by HBM bandwidth on KV bytes, so
+// the kernel is built to read every KV byte exactly once, at full rate.
+//   * Work space: the (sequence, kv head) units, each cut into chunks of 32
+//     tokens (two 16-token blocks).  All chunks of all units form one
+//     ordered list; a persistent grid of one CTA per SM gives every CTA an
+//     equal contiguous run of the list (at least 8 chunks), so long and short
+//     sequences balance perfectly.  A unit that straddles CTAs is finished
+//     by K2r, which merges the per-CTA partial results (normalised output
+//     plus log2-sum-exp) in a fixed order: results are deterministic.
+//   * One producer warp streams the run through a ring of shared-memory
+//     stages with 2-D TMA loads (a (block, kv head) tile of K or V is 16 rows
+//     x 256 B, loaded as two 128-byte-swizzled 16 x 64 boxes), and bulk-
+//     copies each unit's G query heads.  Eight consumer warps take chunks
+//     round-robin.  Stage hand-off uses mbarriers (full: TMA byte count,
+//     empty: consumer release).
+//   * A consumer warp holds the whole GQA group: QK^T is lane-per-token (lane
+//     j owns token j's 256-byte key row, read conflict-free thanks to the
+//     swizzle, and broadcast-reads the fp32 query heads, pre-scaled by
+//     scale * log2 e), so each key byte serves all G heads with no shuffle
+//     reduction; the chunk max per head is one 5-step shuffle tree; PV is
+//     lane-per-dimension (4 dims per lane) with p broadcast from shared
+//     memory.  Each warp keeps its own online-softmax state (running max m,
+//     lane-partial sums l, output o) and the warps are merged at the end of
+//     every unit.
+//   * Every wait is bounded (see common.cuh); on a timeout the kernel raises
+//     QATTN_DEVERR_TIMEOUT, drains its copies in flight and returns.
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace qattn {
+namespace {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kProducerWarp = kConsumerWarps;
+constexpr int kStages = 9;
+constexpr int kBoxBytes = kBlockSize * 128;     // 16 rows x 128 B
+constexpr int kTileBytes = 2 * kBoxBytes;       // one (block, kv head) tile of K or V
+constexpr int kKBytes = 2 * kTileBytes;         // two blocks of K
+constexpr int kStageBytes = 2 * kKBytes;        // K + V of one chunk
+constexpr int kMaxGroup = 8;
+
+// Shared-memory layout (offsets from a 1024-byte aligned base).
+constexpr int kOffStages = 0;
+constexpr int kOffQStage = kOffStages + kStages * kStageBytes;       // 2 x [8][128] bf16
+constexpr int kOffQf = kOffQStage + 2 * kMaxGroup * kHeadDim * 2;    // [8][128] fp32
+constexpr int kOffP = kOffQf + kMaxGroup * kHeadDim * 4;             // [warps][8][32] fp32
+constexpr int kOffMo = kOffP + kConsumerWarps * kMaxGroup * 32 * 4;  // [warps][8][128] fp32
+constexpr int kOffMl = kOffMo + kConsumerWarps * kMaxGroup * kHeadDim * 4;  // [warps][8][2]
+constexpr int kOffBars = kOffMl + kConsumerWarps * kMaxGroup * 2 * 4;
+constexpr int kNumBars = 2 * kStages + 4 + 1;
+constexpr int kOffMisc = kOffBars + kNumBars * 8;
+constexpr int kSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
+
+struct Misc {
+  int abort;
+  int total;
+  int b0;
+  int off0;
+  int warp_sums[kConsumerWarps + 1];
+};
+
+__device__ __forceinline__ int seq_chunks(const DecodeArgs& a, int b, int* L_out) {
+  const int L = a.context_lens[b];
+  *L_out = L;
+  if (a.cu_seqlens_q != nullptr) {
+    if (a.cu_seqlens_q[b + 1] - a.cu_seqlens_q[b] != 1) return 0;
+  }
+  if (L < 1 || L > a.max_context_len || L > a.max_blocks_per_seq * kBlockSize) return 0;
+  return (L + kChunkTokens - 1) / kChunkTokens;
+}
+
+// Position in the chunk list: sequence b, kv head g, chunk i of nch.
+struct Walk {
+  int b, g, i, nch, L;
+};
+
+__device__ __forceinline__ void walk_next(Walk& w, const DecodeArgs& a) {
+  if (++w.i < w.nch) return;
+  w.i = 0;
+  if (++w.g < a.num_kv_heads) return;
+  w.g = 0;
+  for (;;) {
+    ++w.b;
+    if (w.b >= a.num_seqs) {
+      w.nch = 0;
+      return;
+    }
+    w.nch = seq_chunks(a, w.b, &w.L);
+    if (w.nch > 0) return;
+  }
+}
+
+__device__ __forceinline__ Walk shfl_walk(const Walk& w, int src) {
+  Walk r;
+  r.b = __shfl_sync(0xffffffffu, w.b, src);
+  r.g = __shfl_sync(0xffffffffu, w.g, src);
+  r.i = __shfl_sync(0xffffffffu, w.i, src);
+  r.nch = __shfl_sync(0xffffffffu, w.nch, src);
+  r.L = __shfl_sync(0xffffffffu, w.L, src);
+  return r;
+}
+
+__device__ __forceinline__ int64_t q_row_of(const DecodeArgs& a, int b) {
+  return a.cu_seqlens_q != nullptr ? static_cast<int64_t>(a.cu_seqlens_q[b]) : b;
+}
+
+// Block-wide inclusive scan over all kThreads threads.
+__device__ __forceinline__ int block_scan(int v, int* warp_sums, int* block_total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  if (lane == 31) warp_sums[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < kConsumerWarps + 1 ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += n;
+    }
+    if (lane < kConsumerWarps + 1) warp_sums[lane] = w;
+  }
+  __syncthreads();
+  const int add = warp > 0 ? warp_sums[warp - 1] : 0;
+  *block_total = warp_sums[kConsumerWarps];
+  __syncthreads();
+  return v + add;
+}
+
+template <int G>
+__global__ void __launch_bounds__(kThreads, 1)
+    paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
+                        const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kOffBars);
+  uint64_t* empty = full + kStages;
+  uint64_t* qfull = empty + kStages;
+  uint64_t* qempty = qfull + 2;
+  uint64_t* cbar = qempty + 2;
+  Misc* misc = reinterpret_cast<Misc*>(smem + kOffMisc);
+  volatile int* abort_flag = &misc->abort;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int Hkv = a.num_kv_heads;
+  const int B = a.num_seqs;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&qfull[s], 1);
+      mbar_init(&qempty[s], 1);
+    }
+    mbar_init(cbar, kConsumerWarps);
+    misc->abort = 0;
+    misc->b0 = -1;
+    misc->off0 = 0;
+    fence_barrier_init();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    tma_prefetch_desc(&kmap);
+    tma_prefetch_desc(&vmap);
+  }
+
+  // ---- plan: total chunk count, this CTA's run [c0, c1), its first unit ----
+  int local = 0;
+  for (int b = tid; b < B; b += kThreads) {
+    int L;
+    local += Hkv * seq_chunks(a, b, &L);
+  }
+  int total;
+  block_scan(local, misc->warp_sums, &total);
+  const int C = max(kMinChunksPerCta, (total + static_cast<int>(gridDim.x) - 1) /
+                                          static_cast<int>(gridDim.x));
+  const int c0 = static_cast<int>(blockIdx.x) * C;
+  const int c1 = min(total, c0 + C);
+  int running = 0;
+  for (int base = 0; base < B; base += kThreads) {
+    const int b = base + tid;
+    int L = 0;
+    const int u = b < B ? Hkv * seq_chunks(a, b, &L) : 0;
+    int tile_total;
+    const int incl = block_scan(u, misc->warp_sums, &tile_total);
+    const int excl = running + incl - u;
+    if (blockIdx.x == 0 && b < B) a.ws.cum[b] = excl;
+    if (u > 0 && excl <= c0 && c0 < excl + u) {
+      misc->b0 = b;
+      misc->off0 = c0 - excl;
+    }
+    running += tile_total;
+  }
+  if (blockIdx.x == 0 && tid == 0) a.ws.cum[B] = C;
+  __syncthreads();
+  if (c0 >= c1) return;  // no work for this CTA (nothing issued yet)
+  const int nloc = c1 - c0;
+
+  Walk w0;
+  w0.b = misc->b0;
+  w0.nch = seq_chunks(a, w0.b, &w0.L);
+  w0.g = misc->off0 / w0.nch;
+  w0.i = misc->off0 % w0.nch;
+
+  const uint32_t smem_base = smem_u32(smem);
+  if (warp == kProducerWarp) {
+    // ================================ producer ================================
+    Walk bw = w0;
+    int n = 0, seg = -1, q_issued = 0;
+    bool ok = true;
+    while (n < nloc && ok) {
+      const int cnt = min(32, nloc - n);
+      Walk mw = bw;
+      for (int k = 0; k < lane && k < cnt - 1; ++k) walk_next(mw, a);
+      int id0 = -1, id1 = -1;
+      int64_t qrow = 0;
+      if (lane < cnt) {
+        const int ntok = min(kChunkTokens, mw.L - mw.i * kChunkTokens);
+        const int* row = a.block_tables + static_cast<int64_t>(mw.b) * a.max_blocks_per_seq;
+        id0 = row[2 * mw.i];
+        if (ntok > kBlockSize) id1 = row[2 * mw.i + 1];
+        if (id0 < 0 || id0 >= a.num_blocks || (ntok > kBlockSize && (id1 < 0 || id1 >= a.num_blocks))) {
+          set_err(a.err_word, QATTN_DEVERR_BLOCK);
+          if (id0 < 0 || id0 >= a.num_blocks) id0 = -1;
+          if (id1 < 0 || id1 >= a.num_blocks) id1 = -1;
+        }
+        if (mw.i == 0 || n + lane == 0) qrow = q_row_of(a, mw.b);
+      }
+      for (int c = 0; c < cnt; ++c) {
+        const int cb = __shfl_sync(0xffffffffu, mw.g, c);
+        const int ci = __shfl_sync(0xffffffffu, mw.i, c);
+        const int cid0 = __shfl_sync(0xffffffffu, id0, c);
+        const int cid1 = __shfl_sync(0xffffffffu, id1, c);
+        const int64_t cq = __shfl_sync(0xffffffffu, qrow, c);
+        if (lane == 0) {
+          const int g = cb;
+          if (ci == 0 || n == 0) {
+            ++seg;
+            const int slot = seg & 1;
+            if (!mbar_wait(&qempty[slot], ((seg >> 1) & 1) ^ 1, abort_flag)) {
+              ok = false;
+            } else {
+              const __nv_bfloat16* qsrc = static_cast<const __nv_bfloat16*>(a.q) +
+                                          cq * a.q_row_stride +
+                                          static_cast<int64_t>(g) * G * kHeadDim;
+              mbar_arrive_expect_tx(&qfull[slot], G * kHeadDim * 2);
+              bulk_load(smem + kOffQStage + slot * kMaxGroup * kHeadDim * 2, qsrc,
+                        G * kHeadDim * 2, &qfull[slot]);
+              ++q_issued;
+            }
+          }
+          const int stage = n % kStages;
+          if (ok && !mbar_wait(&empty[stage], ((n / kStages) & 1) ^ 1, abort_flag)) ok = false;
+          if (ok) {
+            const uint32_t bytes = (cid0 >= 0 ? kKBytes : 0) + (cid1 >= 0 ? kKBytes : 0);
+            if (bytes == 0) {
+              mbar_arrive(&full[stage]);
+            } else {
+              mbar_arrive_expect_tx(&full[stage], bytes);
+              uint8_t* st = smem + kOffStages + stage * kStageBytes;
+#pragma unroll
+              for (int j = 0; j < 2; ++j) {
+                const int id = j ? cid1 : cid0;
+                if (id < 0) continue;
+                const int32_t y = (id * Hkv + g) * kBlockSize;
+                tma_load_2d(st + j * kTileBytes, &kmap, 0, y, &full[stage]);
+                tma_load_2d(st + j * kTileBytes + kBoxBytes, &kmap, 64, y, &full[stage]);
+                tma_load_2d(st + kKBytes + j * kTileBytes, &vmap, 0, y, &full[stage]);
+                tma_load_2d(st + kKBytes + j * kTileBytes + kBoxBytes, &vmap, 64, y,
+                            &full[stage]);
+              }
+            }
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        ++n;
+      }
+      bw = shfl_walk(mw, cnt - 1);
+      walk_next(bw, a);
+    }
+    // Drain: every stage's most recent load must land before the CTA exits.
+    if (lane == 0) {
+      const int issued = n;
+      for (int s = 0; s < kStages && s < issued; ++s) {
+        const int last = s + ((issued - 1 - s) / kStages) * kStages;
+        if (!mbar_wait_drain(&full[s], (last / kStages) & 1)) break;
+      }
+      // q copy k went to slot k & 1 with phase parity (k >> 1) & 1.
+      for (int k = q_issued - 1; k >= 0 && k >= q_issued - 2; --k)
+        mbar_wait_drain(&qfull[k & 1], (k >> 1) & 1);
+      if (*abort_flag) set_err(a.err_word, QATTN_DEVERR_TIMEOUT);
+    }
+    return;
+  }
+
+  // ================================= consumers ================================
+  const uint32_t qf_addr = smem_base + kOffQf;
+  const uint32_t p_addr = smem_base + kOffP + warp * (kMaxGroup * 32 * 4);
+  float* pbuf = reinterpret_cast<float*>(smem + kOffP) + warp * kMaxGroup * 32;
+  float* mo = reinterpret_cast<float*>(smem + kOffMo);
+  float* ml = reinterpret_cast<float*>(smem + kOffMl);
+  int cphase = 0;
+
+  float m[G], l[G], o[G][4];
+  Walk cw = w0;
+  int seg = -1;
+  bool ok = true;
+  for (int n = 0; n < nloc && ok; ++n, walk_next(cw, a)) {
+    const bool seg_start = (n == 0) || (cw.i == 0);
+    const bool seg_end = (n == nloc - 1) || (cw.i == cw.nch - 1);
+    if (seg_start) {
+      ++seg;
+      const int slot = seg & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&qfull[slot], (seg >> 1) & 1, abort_flag))) {
+        ok = false;
+        break;
+      }
+      const __nv_bfloat16* qs = reinterpret_cast<const __nv_bfloat16*>(
+          smem + kOffQStage + slot * kMaxGroup * kHeadDim * 2);
+      float* qfw = reinterpret_cast<float*>(smem + kOffQf);
+      for (int e = tid; e < G * kHeadDim; e += kConsumerWarps * 32)
+        qfw[e] = __bfloat162float(qs[e]) * a.scale_log2;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(cbar);
+      if (!__all_sync(0xffffffffu, mbar_wait(cbar, cphase & 1, abort_flag))) {
+        ok = false;
+        break;
+      }
+      ++cphase;
+      if (tid == 0) mbar_arrive(&qempty[slot]);
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        m[h] = -INFINITY;
+        l[h] = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[h][e] = 0.f;
+      }
+    }
+
+    if (n % kConsumerWarps == warp) {
+      const int stage = n % kStages;
+      if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], (n / kStages) & 1, abort_flag))) {
+        ok = false;
+        break;
+      }
+      const uint32_t sK = smem_base + kOffStages + stage * kStageBytes;
+      const uint32_t sV = sK + kKBytes;
+      const int ntok = min(kChunkTokens, cw.L - cw.i * kChunkTokens);
+
+      // ---- S = q . k, lane-per-token ----
+      float s[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) s[h] = 0.f;
+      {
+        const int r = lane & 15;
+        const uint32_t rowbase = sK + (lane >> 4) * kTileBytes + r * 128;
+#pragma unroll 4
+        for (int c = 0; c < 16; ++c) {
+          const uint32_t addr =
+              rowbase + (c >> 3) * kBoxBytes + ((((c & 7) ^ (r & 7))) << 4);
+          const uint4 kv = lds128(addr);
+          float k[8];
+          k[0] = bf16lo_to_f32(kv.x); k[1] = bf16hi_to_f32(kv.x);
+          k[2] = bf16lo_to_f32(kv.y); k[3] = bf16hi_to_f32(kv.y);
+          k[4] = bf16lo_to_f32(kv.z); k[5] = bf16hi_to_f32(kv.z);
+          k[6] = bf16lo_to_f32(kv.w); k[7] = bf16hi_to_f32(kv.w);
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            const float4 qa = lds128f(qf_addr + (h * kHeadDim + c * 8) * 4);
+            const float4 qb = lds128f(qf_addr + (h * kHeadDim + c * 8 + 4) * 4);
+            float acc = s[h];
+            acc = fmaf(qa.x, k[0], acc);
+            acc = fmaf(qa.y, k[1], acc);
+            acc = fmaf(qa.z, k[2], acc);
+            acc = fmaf(qa.w, k[3], acc);
+            acc = fmaf(qb.x, k[4], acc);
+            acc = fmaf(qb.y, k[5], acc);
+            acc = fmaf(qb.z, k[6], acc);
+            acc = fmaf(qb.w, k[7], acc);
+            s[h] = acc;
+          }
+        }
+      }
+
+      // ---- online softmax (log2 domain) ----
+      const bool valid = lane < ntok;
+      float alpha[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float sv = valid ? s[h] : -INFINITY;
+        const float mnew = fmaxf(m[h], warp_max(sv));
+        alpha[h] = exp2f(m[h] - mnew);
+        const float p = exp2f(sv - mnew);
+        l[h] = fmaf(l[h], alpha[h], p);
+        m[h] = mnew;
+        pbuf[h * 32 + lane] = p;
+      }
+      if (ntok < kChunkTokens) {
+        // Rows past the end of the context hold stale or never-written
+        // data; zero this lane's slice of them so 0 * garbage stays 0.
+        for (int j = ntok; j < kChunkTokens; ++j) {
+          const int r = j & 15;
+          const uint32_t addr = sV + (j >> 4) * kTileBytes + (lane >> 4) * kBoxBytes + r * 128 +
+                                (((((lane & 15) >> 1) ^ (r & 7))) << 4) + (lane & 1) * 8;
+          asm volatile("st.shared.v2.u32 [%0], {%1, %1};" ::"r"(addr), "r"(0u) : "memory");
+        }
+      }
+      __syncwarp();
+
+      // ---- o = alpha * o + P V, lane-per-4-dims ----
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[h][e] *= alpha[h];
+      }
+      const uint32_t vlane = sV + (lane >> 4) * kBoxBytes + (lane & 1) * 8;
+      const int vchunk = (lane & 15) >> 1;
+#pragma unroll 2
+      for (int j4 = 0; j4 < 8; ++j4) {
+        float4 p4[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) p4[h] = lds128f(p_addr + (h * 32 + j4 * 4) * 4);
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const int j = j4 * 4 + jj;
+          const int r = j & 15;
+          const uint2 vv =
+              lds64(vlane + (j >> 4) * kTileBytes + r * 128 + ((vchunk ^ (r & 7)) << 4));
+          const float v0 = bf16lo_to_f32(vv.x), v1 = bf16hi_to_f32(vv.x);
+          const float v2 = bf16lo_to_f32(vv.y), v3 = bf16hi_to_f32(vv.y);
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            const float p = jj == 0 ? p4[h].x : jj == 1 ? p4[h].y : jj == 2 ? p4[h].z : p4[h].w;
+            o[h][0] = fmaf(p, v0, o[h][0]);
+            o[h][1] = fmaf(p, v1, o[h][1]);
+            o[h][2] = fmaf(p, v2, o[h][2]);
+            o[h][3] = fmaf(p, v3, o[h][3]);
+          }
+        }
+      }
+      if (ntok < kChunkTokens) fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[stage]);
+    }
+
+    if (seg_end) {
+      // ---- merge the warps' states for this unit ----
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float lt = warp_sum(l[h]);
+        *reinterpret_cast<float4*>(&mo[((warp * kMaxGroup) + h) * kHeadDim + lane * 4]) =
+            make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
+        if (lane == 0) {
+          ml[(warp * kMaxGroup + h) * 2 + 0] = m[h];
+          ml[(warp * kMaxGroup + h) * 2 + 1] = lt;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(cbar);
+      if (!__all_sync(0xffffffffu, mbar_wait(cbar, cphase & 1, abort_flag))) {
+        ok = false;
+        break;
+      }
+      ++cphase;
+      const int gidx = c0 + n;
+      const int u0 = gidx - cw.i;  // list index of this unit's first chunk
+      const int first = u0 / C, last = (u0 + cw.nch - 1) / C;
+      const int nparts = last - first + 1;
+      const int part = static_cast<int>(blockIdx.x) - first;
+      const int64_t row = q_row_of(a, cw.b);
+      for (int idx = tid; idx < G * 32; idx += kConsumerWarps * 32) {
+        const int h = idx >> 5, d4 = idx & 31;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, ml[(w * kMaxGroup + h) * 2]);
+        float den = 0.f;
+        float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          const float f = exp2f(ml[(w * kMaxGroup + h) * 2] - M);
+          den = fmaf(f, ml[(w * kMaxGroup + h) * 2 + 1], den);
+          const float4 ov =
+              *reinterpret_cast<const float4*>(&mo[((w * kMaxGroup) + h) * kHeadDim + d4 * 4]);
+          num.x = fmaf(f, ov.x, num.x);
+          num.y = fmaf(f, ov.y, num.y);
+          num.z = fmaf(f, ov.z, num.z);
+          num.w = fmaf(f, ov.w, num.w);
+        }
+        const float inv = 1.f / den;
+        const float4 res = make_float4(num.x * inv, num.y * inv, num.z * inv, num.w * inv);
+        const int head = cw.g * G + h;
+        if (nparts == 1) {
+          uint2 packed;
+          packed.x = pack_bf16x2_rn(res.x, res.y);
+          packed.y = pack_bf16x2_rn(res.z, res.w);
+          *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) +
+                                    (row * a.num_heads + head) * kHeadDim + d4 * 4) = packed;
+        } else if (part >= 0 && part < a.ws.max_parts) {
+          const int64_t pidx =
+              (static_cast<int64_t>(cw.b) * Hkv + cw.g) * a.ws.max_parts + part;
+          *reinterpret_cast<float4*>(a.ws.part_o + (pidx * G + h) * kHeadDim + d4 * 4) = res;
+          if (d4 == 0) a.ws.lse[pidx * G + h] = M + log2f(den);
+        }
+      }
+    }
+  }
+  if (!ok && lane == 0) set_err(a.err_word, QATTN_DEVERR_TIMEOUT);
+}
+
+// K2r: merge the partial results of units that straddled CTAs, and write
+// zero rows for decode sequences whose context is invalid.
+template <int G>
+__global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a) {
+  const int Hkv = a.num_kv_heads;
+  const int b = blockIdx.x / Hkv, g = blockIdx.x % Hkv;
+  const int d = threadIdx.x;
+  if (a.cu_seqlens_q != nullptr) {
+    const int ql = a.cu_seqlens_q[b + 1] - a.cu_seqlens_q[b];
+    if (ql < 1) {
+      if (g == 0 && d == 0) set_err(a.err_word, QATTN_DEVERR_CONTEXT);
+      return;
+    }
+    if (ql != 1) return;  // a prefill sequence: the prefill kernel owns it
+  }
+  int L;
+  const int nch = seq_chunks(a, b, &L);
+  const int64_t row = q_row_of(a, b);
+  __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(a.out) +
+                        (row * a.num_heads + static_cast<int64_t>(g) * G) * kHeadDim;
+  if (nch == 0) {
+    for (int h = 0; h < G; ++h) outp[h * kHeadDim + d] = __float2bfloat16_rn(0.f);
+    if (g == 0 && d == 0) set_err(a.err_word, QATTN_DEVERR_CONTEXT);
+    return;
+  }
+  const int C = a.ws.cum[a.num_seqs];
+  const int u0 = a.ws.cum[b] + g * nch;
+  const int first = u0 / C, last = (u0 + nch - 1) / C;
+  const int nparts = last - first + 1;
+  if (nparts == 1) return;
+  if (nparts > a.ws.max_parts) {
+    if (d == 0) set_err(a.err_word, QATTN_DEVERR_CONTEXT);
+    return;
+  }
+  const int64_t pbase = (static_cast<int64_t>(b) * Hkv + g) * a.ws.max_parts;
+  for (int h = 0; h < G; ++h) {
+    float M = -INFINITY;
+    for (int p = 0; p < nparts; ++p) M = fmaxf(M, a.ws.lse[(pbase + p) * G + h]);
+    float den = 0.f, num = 0.f;
+    for (int p = 0; p < nparts; ++p) {
+      const float f = exp2f(a.ws.lse[(pbase + p) * G + h] - M);
+      den += f;
+      num = fmaf(f, a.ws.part_o[((pbase + p) * G + h) * kHeadDim + d], num);
+    }
+    outp[h * kHeadDim + d] = __float2bfloat16_rn(num / den);
+  }
+}
+
+template <int G>
+cudaError_t launch_g(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                     int num_sms, cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<G>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  paged_decode_kernel<G><<<num_sms, kThreads, kSmemBytes, stream>>>(kmap, vmap, a);
+  cudaError_t e = cudaPeekAtLastError();
+  if (e != cudaSuccess) return e;
+  decode_merge_kernel<G><<<a.num_seqs * a.num_kv_heads, 128, 0, stream>>>(a);
+  return cudaPeekAtLastError();
+}
+
+}  // namespace
+
+size_t decode_workspace_bytes(int32_t num_seqs, int32_t max_context_len, int32_t num_kv_heads,
+                              int32_t group) {
+  const int64_t nch = (static_cast<int64_t>(max_context_len) + kChunkTokens - 1) / kChunkTokens;
+  const int64_t max_parts = (nch + kMinChunksPerCta - 1) / kMinChunksPerCta + 1;
+  auto al = [](int64_t x) { return (x + 255) / 256 * 256; };
+  const int64_t units = static_cast<int64_t>(num_seqs) * num_kv_heads * max_parts * group;
+  return static_cast<size_t>(al((num_seqs + 1) * 4) + al(units * 4) + al(units * kHeadDim * 4));
+}
+
+DecodeWorkspace carve_decode_workspace(void* base, int32_t num_seqs, int32_t max_context_len,
+                                       int32_t num_kv_heads, int32_t group) {
+  const int64_t nch = (static_cast<int64_t>(max_context_len) + kChunkTokens - 1) / kChunkTokens;
+  const int64_t max_parts = (nch + kMinChunksPerCta - 1) / kMinChunksPerCta + 1;
+  auto al = [](int64_t x) { return (x + 255) / 256 * 256; };
+  const int64_t units = static_cast<int64_t>(num_seqs) * num_kv_heads * max_parts * group;
+  uint8_t* p = static_cast<uint8_t*>(base);
+  DecodeWorkspace w;
+  w.cum = reinterpret_cast<int32_t*>(p);
+  p += al((num_seqs + 1) * 4);
+  w.lse = reinterpret_cast<float*>(p);
+  p += al(units * 4);
+  w.part_o = reinterpret_cast<float*>(p);
+  w.max_parts = static_cast<int32_t>(max_parts);
+  return w;
+}
+
+cudaError_t launch_paged_decode(const DecodeArgs& a, const CUtensorMap& kmap,
+                                const CUtensorMap& vmap, int num_sms, cudaStream_t stream) {
+  switch (a.num_heads / a.num_kv_heads) {
+    case 1: return launch_g<1>(a, kmap, vmap, num_sms, stream);
+    case 2: return launch_g<2>(a, kmap, vmap, num_sms, stream);
+    case 3: return launch_g<3>(a, kmap, vmap, num_sms, stream);
+    case 4: return launch_g<4>(a, kmap, vmap, num_sms, stream);
+    case 5: return launch_g<5>(a, kmap, vmap, num_sms, stream);
+    case 6: return launch_g<6>(a, kmap, vmap, num_sms, stream);
+    case 7: return launch_g<7>(a, kmap, vmap, num_sms, stream);
+    case 8: return launch_g<8>(a, kmap, vmap, num_sms, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace qattn

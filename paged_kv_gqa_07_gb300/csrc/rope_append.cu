@@ -1,0 +1,139 @@
+// Kernel K1: rotate-half RoPE on the query and key heads of each new token,
+// and the write of its key/value rows into the paged cache.
+//
+// Follows get_rope(head_dim, rotary_dim=head_dim, max_position, base) in
+// "Qwen2大模型架构解析与vLLM优化实践" section 2.2 (full-width rotate-half,
+// rope_theta = 1e6 per "Qwen2 模型结构代码详解" section 2), and the block
+// cache written through a slot mapping (vLLM-deploys-Qwen notes section 2.1;
+// nano-vllm Qwen3 skeleton page section 5).
+//
+// Work decomposition: one thread per (token, head, 8-pair slice).  A query
+// or key head of 128 dims is 64 rotation pairs (i, i + 64); eight threads
+// cover it, each loading two 16-byte vectors (dims i..i+7 and i+64..i+71)
+// and the matching 32-byte cos and sin slices of the table row.  A value
+// head is a plain 256-byte copy done by sixteen threads with 16-byte
+// vectors.  All global accesses of a warp are contiguous 128-byte runs.
+//
+// The rotation is evaluated with explicitly rounded fp32 operations
+// (__fmul_rn / __fsub_rn / __fadd_rn, no contraction into FMA) and rounded
+// to bf16 nearest-even, so the cache contents are bit-reproducible.
+#include "common.cuh"
+#include "internal.h"
+
+namespace qattn {
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ void rotate8(const uint4& x1, const uint4& x2, const float* c,
+                                        const float* s, uint4& y1, uint4& y2) {
+  const uint32_t* a = reinterpret_cast<const uint32_t*>(&x1);
+  const uint32_t* b = reinterpret_cast<const uint32_t*>(&x2);
+  uint32_t* o1 = reinterpret_cast<uint32_t*>(&y1);
+  uint32_t* o2 = reinterpret_cast<uint32_t*>(&y2);
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    float lo1[2] = {bf16lo_to_f32(a[w]), bf16hi_to_f32(a[w])};
+    float hi1[2] = {bf16lo_to_f32(b[w]), bf16hi_to_f32(b[w])};
+    float r1[2], r2[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const float cc = c[2 * w + e], ss = s[2 * w + e];
+      r1[e] = __fsub_rn(__fmul_rn(lo1[e], cc), __fmul_rn(hi1[e], ss));
+      r2[e] = __fadd_rn(__fmul_rn(hi1[e], cc), __fmul_rn(lo1[e], ss));
+    }
+    o1[w] = pack_bf16x2_rn(r1[0], r1[1]);
+    o2[w] = pack_bf16x2_rn(r2[0], r2[1]);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) rope_append_kernel(RopeAppendArgs a,
+                                                               int tasks_per_token) {
+  const int64_t gid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+  const int64_t t = gid / tasks_per_token;
+  if (t >= a.num_tokens) return;
+  const int r = static_cast<int>(gid - t * tasks_per_token);
+  const int H = a.num_heads, Hkv = a.num_kv_heads;
+  const int nrot = (H + Hkv) * 8;
+
+  const int pos = a.positions[t];
+  if (pos < 0 || pos >= a.max_pos) {
+    if (r == 0) set_err(a.err_word, QATTN_DEVERR_POSITION);
+    return;
+  }
+  const int slot = a.slot_mapping[t];
+  const int64_t num_slots = static_cast<int64_t>(a.num_blocks) * kBlockSize;
+  bool write_cache = slot >= 0;
+  if (write_cache && slot >= num_slots) {
+    if (r == 0) set_err(a.err_word, QATTN_DEVERR_SLOT);
+    write_cache = false;
+  }
+  int64_t cache_row = 0;  // element offset of (block, kv head 0, offset) in the cache
+  if (write_cache) {
+    const int blk = slot / kBlockSize, off = slot % kBlockSize;
+    cache_row = (static_cast<int64_t>(blk) * Hkv * kBlockSize + off) * kHeadDim;
+  }
+
+  if (r < nrot) {
+    const int head = r >> 3;
+    const int part = r & 7;
+    const float* row = a.cos_sin + static_cast<int64_t>(pos) * kHeadDim;
+    float c[8], s[8];
+    {
+      const float4 c0 = __ldg(reinterpret_cast<const float4*>(row + part * 8));
+      const float4 c1 = __ldg(reinterpret_cast<const float4*>(row + part * 8 + 4));
+      const float4 s0 = __ldg(reinterpret_cast<const float4*>(row + 64 + part * 8));
+      const float4 s1 = __ldg(reinterpret_cast<const float4*>(row + 64 + part * 8 + 4));
+      c[0] = c0.x; c[1] = c0.y; c[2] = c0.z; c[3] = c0.w;
+      c[4] = c1.x; c[5] = c1.y; c[6] = c1.z; c[7] = c1.w;
+      s[0] = s0.x; s[1] = s0.y; s[2] = s0.z; s[3] = s0.w;
+      s[4] = s1.x; s[5] = s1.y; s[6] = s1.z; s[7] = s1.w;
+    }
+    if (head < H) {
+      __nv_bfloat16* src = static_cast<__nv_bfloat16*>(a.q) + t * a.q_row_stride +
+                           static_cast<int64_t>(head) * kHeadDim;
+      uint4* p1 = reinterpret_cast<uint4*>(src + part * 8);
+      uint4* p2 = reinterpret_cast<uint4*>(src + 64 + part * 8);
+      const uint4 x1 = *p1, x2 = *p2;
+      uint4 y1, y2;
+      rotate8(x1, x2, c, s, y1, y2);
+      *p1 = y1;
+      *p2 = y2;
+    } else {
+      if (!write_cache) return;
+      const int g = head - H;
+      const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(a.k) + t * a.k_row_stride +
+                                 static_cast<int64_t>(g) * kHeadDim;
+      const uint4 x1 = *reinterpret_cast<const uint4*>(src + part * 8);
+      const uint4 x2 = *reinterpret_cast<const uint4*>(src + 64 + part * 8);
+      uint4 y1, y2;
+      rotate8(x1, x2, c, s, y1, y2);
+      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.k_cache) + cache_row +
+                           static_cast<int64_t>(g) * kBlockSize * kHeadDim;
+      *reinterpret_cast<uint4*>(dst + part * 8) = y1;
+      *reinterpret_cast<uint4*>(dst + 64 + part * 8) = y2;
+    }
+  } else {
+    if (!write_cache) return;
+    const int r2 = r - nrot;
+    const int g = r2 >> 4, part = r2 & 15;
+    const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(a.v) + t * a.v_row_stride +
+                               static_cast<int64_t>(g) * kHeadDim;
+    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.v_cache) + cache_row +
+                         static_cast<int64_t>(g) * kBlockSize * kHeadDim;
+    *reinterpret_cast<uint4*>(dst + part * 8) = *reinterpret_cast<const uint4*>(src + part * 8);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_rope_append(const RopeAppendArgs& a, cudaStream_t stream) {
+  const int tasks_per_token = (a.num_heads + a.num_kv_heads) * 8 + a.num_kv_heads * 16;
+  const int64_t total = static_cast<int64_t>(a.num_tokens) * tasks_per_token;
+  const int64_t blocks = (total + kThreads - 1) / kThreads;
+  if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
+  rope_append_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(a, tasks_per_token);
+  return cudaPeekAtLastError();
+}
+
+}  // namespace qattn

@@ -1,0 +1,122 @@
+"""C-ABI library checks that need no GPU: it builds, loads, exports every
+symbol include/qattn.h declares, validates arguments on the host before any
+CUDA call, and its host-side RoPE table equals the oracle's bit for bit."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from paged_kv_gqa_07_gb300 import build as B
+from paged_kv_gqa_07_gb300 import qattn as Q
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return Q.load_library()
+
+
+def declared_symbols():
+    src = open(os.path.join(ROOT, "include", "qattn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(qattn_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_header_declares_the_three_entry_points():
+    syms = declared_symbols()
+    for name in ("qattn_rope_cache_append", "qattn_paged_decode", "qattn_varlen_prefill"):
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+    assert sorted(Q.EXPORTED) == declared_symbols()
+
+
+def test_status_strings_and_version(lib):
+    assert Q.qattn_status_string(0) == "ok"
+    assert "workspace" in Q.qattn_status_string(4)
+    assert Q.qattn_version() >= 100
+
+
+def test_host_rope_table_equals_oracle(lib):
+    """The library's host table and the oracle's own table are computed by
+    separate code from the same definition: they must agree bit for bit."""
+    for theta in (1e6, 1e4):
+        t = Q.qattn_rope_table_build(4096, 128, theta).numpy()
+        o = oracle.rope_table(theta, 4096, 128)
+        assert np.array_equal(t.view(np.uint32), o.view(np.uint32))
+
+
+def test_host_rope_table_full_length(lib):
+    t = Q.qattn_rope_table_build(32768, 128, 1e6).numpy()
+    o = oracle.rope_table(1e6, 32768, 128)
+    assert np.array_equal(t.view(np.uint32), o.view(np.uint32))
+
+
+def test_table_build_rejects_bad_args(lib):
+    buf = (ctypes.c_float * 16)()
+    assert lib.qattn_rope_table_build(None, 4, 4, 1e6) == Q.QATTN_ERR_INVALID_ARG
+    assert lib.qattn_rope_table_build(buf, 4, 3, 1e6) == Q.QATTN_ERR_INVALID_ARG
+    assert lib.qattn_rope_table_build(buf, 0, 4, 1e6) == Q.QATTN_ERR_INVALID_ARG
+    assert lib.qattn_rope_table_build(buf, 4, 4, -1.0) == Q.QATTN_ERR_INVALID_ARG
+
+
+def test_workspace_size_grows_with_context(lib):
+    d = Q.make_dims(28, 4)
+    a = Q.qattn_paged_decode_workspace_size(64, 4096, d)
+    b = Q.qattn_paged_decode_workspace_size(64, 32768, d)
+    assert 0 < a < b
+    assert Q.qattn_paged_decode_workspace_size(64, 4096, Q.make_dims(28, 5)) == 0
+
+
+def test_host_validation_before_any_cuda_call(lib):
+    """Every rejected call returns before touching CUDA (this machine may
+    have no GPU): unsupported shapes, null pointers, bad strides."""
+    fake = ctypes.c_void_p(256)
+    d = Q.make_dims(28, 4)
+    st = lib.qattn_rope_cache_append(fake, 28 * 128 + 1024, fake, 0, fake, 0, fake, fake, 4,
+                                     fake, fake, 10, fake, 100, Q.make_dims(28, 4, 64), None, None)
+    assert st == Q.QATTN_ERR_UNSUPPORTED                      # head_dim 64
+    st = lib.qattn_rope_cache_append(fake, 4608, fake, 4608, fake, 4608, fake, fake, 4,
+                                     fake, fake, 10, fake, 100, Q.make_dims(28, 4, 128, 32), None,
+                                     None)
+    assert st == Q.QATTN_ERR_UNSUPPORTED                      # block_size 32
+    st = lib.qattn_rope_cache_append(fake, 4608, fake, 4608, fake, 4608, fake, fake, 4,
+                                     fake, fake, 10, fake, 100, Q.make_dims(27, 4), None, None)
+    assert st == Q.QATTN_ERR_UNSUPPORTED                      # 27 % 4
+    st = lib.qattn_rope_cache_append(fake, 4608, fake, 4608, fake, 4608, None, fake, 4,
+                                     fake, fake, 10, fake, 100, d, None, None)
+    assert st == Q.QATTN_ERR_INVALID_ARG                      # null positions
+    st = lib.qattn_rope_cache_append(fake, 4607, fake, 4608, fake, 4608, fake, fake, 4,
+                                     fake, fake, 10, fake, 100, d, None, None)
+    assert st == Q.QATTN_ERR_INVALID_ARG                      # stride % 8
+    st = lib.qattn_rope_cache_append(None, 0, None, 0, None, 0, None, None, 0,
+                                     None, None, 0, None, 0, d, None, None)
+    assert st == Q.QATTN_OK                                   # zero tokens: no-op
+    st = lib.qattn_paged_decode(fake, fake, 4608, fake, fake, 10, fake, 4, fake, 0, 100, d,
+                                fake, 0, None, None)
+    assert st == Q.QATTN_OK                                   # zero sequences: no-op
+    st = lib.qattn_paged_decode(None, fake, 4608, fake, fake, 10, fake, 4, fake, 3, 100, d,
+                                fake, 1 << 20, None, None)
+    assert st == Q.QATTN_ERR_INVALID_ARG                      # null out
+    st = lib.qattn_paged_decode(fake, ctypes.c_void_p(258), 4608, fake, fake, 10, fake, 4, fake,
+                                3, 100, d, fake, 1 << 20, None, None)
+    assert st == Q.QATTN_ERR_INVALID_ARG                      # misaligned q
+    st = lib.qattn_varlen_prefill(fake, fake, 4608, None, 3, 10, 4, fake, fake, 10, fake, 4, fake,
+                                  100, d, fake, 1 << 20, None, None)
+    assert st == Q.QATTN_ERR_INVALID_ARG                      # null cu_seqlens_q
+    st = lib.qattn_paged_decode(fake, fake, 4608, fake, fake, 10, fake, 4, fake, 3, 100,
+                                Q.make_dims(72, 8), fake, 1 << 20, None, None)
+    assert st == Q.QATTN_ERR_UNSUPPORTED                      # group 9 > 8
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    with pytest.raises(RuntimeError, match="not found"):
+        Q.load_library(str(tmp_path / "missing.so"))
