@@ -333,6 +333,7 @@ int qattn_varlen_prefill(void* out, const void* q, int64_t q_row_stride,
   p.max_blocks_per_seq = max_blocks_per_seq;
   p.num_seqs = num_seqs;
   p.num_blocks = num_blocks;
+  p.total_q = total_q;
   p.max_q_len = max_q_len;
   p.max_context_len = max_context_len;
   p.num_heads = dims.num_heads;

@@ -83,6 +83,7 @@ struct PrefillArgs {
   int32_t max_blocks_per_seq;
   int32_t num_seqs;
   int32_t num_blocks;
+  int32_t total_q;
   int32_t max_q_len;
   int32_t max_context_len;
   int32_t num_heads;
