@@ -42,10 +42,10 @@
 namespace qattn {
 namespace {
 
-constexpr int kConsumerWarps = 8;
+constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kProducerWarp = kConsumerWarps;
-constexpr int kStages = 9;
+constexpr int kStages = 11;
 constexpr int kBoxBytes = kBlockSize * 128;     // 16 rows x 128 B
 constexpr int kTileBytes = 2 * kBoxBytes;       // one (block, kv head) tile of K or V
 constexpr int kKBytes = 2 * kTileBytes;         // two blocks of K
@@ -62,7 +62,9 @@ constexpr int kOffMl = kOffMo + kConsumerWarps * kMaxGroup * kHeadDim * 4;  // [
 constexpr int kOffBars = kOffMl + kConsumerWarps * kMaxGroup * 2 * 4;
 constexpr int kNumBars = 2 * kStages + 4 + 1;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
-constexpr int kSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
+constexpr int kOffLens = kOffMisc + 64;                               // [kMaxSmemSeqs] int32
+constexpr int kMaxSmemSeqs = 4096;
+constexpr int kSmemBytes = kOffLens + kMaxSmemSeqs * 4 + 1024;  // + alignment slack
 
 struct Misc {
   int abort;
@@ -72,13 +74,27 @@ struct Misc {
   int warp_sums[kConsumerWarps + 1];
 };
 
-__device__ __forceinline__ int seq_chunks(const DecodeArgs& a, int b, int* L_out) {
+// Context length of decode sequence b if it is valid for this kernel, else 0.
+__device__ __forceinline__ int seq_len_eff(const DecodeArgs& a, int b) {
   const int L = a.context_lens[b];
-  *L_out = L;
   if (a.cu_seqlens_q != nullptr) {
     if (a.cu_seqlens_q[b + 1] - a.cu_seqlens_q[b] != 1) return 0;
   }
   if (L < 1 || L > a.max_context_len || L > a.max_blocks_per_seq * kBlockSize) return 0;
+  return L;
+}
+
+__device__ __forceinline__ int seq_chunks(const DecodeArgs& a, int b, int* L_out) {
+  const int L = seq_len_eff(a, b);
+  *L_out = L;
+  return (L + kChunkTokens - 1) / kChunkTokens;
+}
+
+// The same, served from the shared-memory copy when the batch fits in it.
+__device__ __forceinline__ int seq_chunks_cached(const DecodeArgs& a, const int* s_len, int b,
+                                                 int* L_out) {
+  const int L = a.num_seqs <= kMaxSmemSeqs ? s_len[b] : seq_len_eff(a, b);
+  *L_out = L;
   return (L + kChunkTokens - 1) / kChunkTokens;
 }
 
@@ -87,7 +103,7 @@ struct Walk {
   int b, g, i, nch, L;
 };
 
-__device__ __forceinline__ void walk_next(Walk& w, const DecodeArgs& a) {
+__device__ __forceinline__ void walk_next(Walk& w, const DecodeArgs& a, const int* s_len) {
   if (++w.i < w.nch) return;
   w.i = 0;
   if (++w.g < a.num_kv_heads) return;
@@ -98,7 +114,7 @@ __device__ __forceinline__ void walk_next(Walk& w, const DecodeArgs& a) {
       w.nch = 0;
       return;
     }
-    w.nch = seq_chunks(a, w.b, &w.L);
+    w.nch = seq_chunks_cached(a, s_len, w.b, &w.L);
     if (w.nch > 0) return;
   }
 }
@@ -156,6 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* qempty = qfull + 2;
   uint64_t* cbar = qempty + 2;
   Misc* misc = reinterpret_cast<Misc*>(smem + kOffMisc);
+  int* s_len = reinterpret_cast<int*>(smem + kOffLens);
   volatile int* abort_flag = &misc->abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -185,8 +202,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- plan: total chunk count, this CTA's run [c0, c1), its first unit ----
   int local = 0;
   for (int b = tid; b < B; b += kThreads) {
-    int L;
-    local += Hkv * seq_chunks(a, b, &L);
+    const int L = seq_len_eff(a, b);
+    if (B <= kMaxSmemSeqs) s_len[b] = L;
+    local += Hkv * ((L + kChunkTokens - 1) / kChunkTokens);
   }
   int total;
   block_scan(local, misc->warp_sums, &total);
@@ -198,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int base = 0; base < B; base += kThreads) {
     const int b = base + tid;
     int L = 0;
-    const int u = b < B ? Hkv * seq_chunks(a, b, &L) : 0;
+    const int u = b < B ? Hkv * seq_chunks_cached(a, s_len, b, &L) : 0;
     int tile_total;
     const int incl = block_scan(u, misc->warp_sums, &tile_total);
     const int excl = running + incl - u;
@@ -216,42 +234,66 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   Walk w0;
   w0.b = misc->b0;
-  w0.nch = seq_chunks(a, w0.b, &w0.L);
+  w0.nch = seq_chunks_cached(a, s_len, w0.b, &w0.L);
   w0.g = misc->off0 / w0.nch;
   w0.i = misc->off0 % w0.nch;
 
   const uint32_t smem_base = smem_u32(smem);
   if (warp == kProducerWarp) {
     // ================================ producer ================================
-    Walk bw = w0;
+    // Chunks are handled in batches of 32: lane l owns chunk (batch start + l),
+    // walks to it and loads its block ids; the next batch's walk and id loads
+    // are issued before the current batch's copies so their latency hides.
     int n = 0, seg = -1, q_issued = 0;
     bool ok = true;
-    while (n < nloc && ok) {
-      const int cnt = min(32, nloc - n);
-      Walk mw = bw;
-      for (int k = 0; k < lane && k < cnt - 1; ++k) walk_next(mw, a);
-      int id0 = -1, id1 = -1;
-      int64_t qrow = 0;
+    auto prepare = [&](const Walk& start, int cnt, Walk& mw, int& id0, int& id1,
+                       int64_t& qrow, int n_first) {
+      mw = start;
+      for (int k = 0; k < lane && k < cnt - 1; ++k) walk_next(mw, a, s_len);
+      id0 = -1;
+      id1 = -1;
+      qrow = 0;
       if (lane < cnt) {
         const int ntok = min(kChunkTokens, mw.L - mw.i * kChunkTokens);
         const int* row = a.block_tables + static_cast<int64_t>(mw.b) * a.max_blocks_per_seq;
         id0 = row[2 * mw.i];
         if (ntok > kBlockSize) id1 = row[2 * mw.i + 1];
-        if (id0 < 0 || id0 >= a.num_blocks || (ntok > kBlockSize && (id1 < 0 || id1 >= a.num_blocks))) {
-          set_err(a.err_word, QATTN_DEVERR_BLOCK);
-          if (id0 < 0 || id0 >= a.num_blocks) id0 = -1;
-          if (id1 < 0 || id1 >= a.num_blocks) id1 = -1;
-        }
-        if (mw.i == 0 || n + lane == 0) qrow = q_row_of(a, mw.b);
+        if (mw.i == 0 || n_first + lane == 0) qrow = q_row_of(a, mw.b);
+      }
+    };
+    Walk mw;
+    int id0, id1;
+    int64_t qrow;
+    int cnt = min(32, nloc);
+    prepare(w0, cnt, mw, id0, id1, qrow, 0);
+    while (n < nloc && ok) {
+      // next batch, issued ahead
+      const int n_next = n + cnt;
+      const int cnt2 = min(32, nloc - n_next);
+      Walk mw2;
+      int id0b = -1, id1b = -1;
+      int64_t qrowb = 0;
+      if (cnt2 > 0) {
+        Walk start = shfl_walk(mw, cnt - 1);
+        walk_next(start, a, s_len);
+        prepare(start, cnt2, mw2, id0b, id1b, qrowb, n_next);
+      }
+      // validate this batch's ids (the loads have landed by now)
+      if (lane < cnt) {
+        const bool bad0 = id0 < 0 || id0 >= a.num_blocks;
+        const int ntok = min(kChunkTokens, mw.L - mw.i * kChunkTokens);
+        const bool bad1 = ntok > kBlockSize && (id1 < 0 || id1 >= a.num_blocks);
+        if (bad0 || bad1) set_err(a.err_word, QATTN_DEVERR_BLOCK);
+        if (bad0) id0 = -1;
+        if (bad1) id1 = -1;
       }
       for (int c = 0; c < cnt; ++c) {
-        const int cb = __shfl_sync(0xffffffffu, mw.g, c);
+        const int g = __shfl_sync(0xffffffffu, mw.g, c);
         const int ci = __shfl_sync(0xffffffffu, mw.i, c);
         const int cid0 = __shfl_sync(0xffffffffu, id0, c);
         const int cid1 = __shfl_sync(0xffffffffu, id1, c);
         const int64_t cq = __shfl_sync(0xffffffffu, qrow, c);
         if (lane == 0) {
-          const int g = cb;
           if (ci == 0 || n == 0) {
             ++seg;
             const int slot = seg & 1;
@@ -294,8 +336,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         ++n;
       }
-      bw = shfl_walk(mw, cnt - 1);
-      walk_next(bw, a);
+      mw = mw2;
+      id0 = id0b;
+      id1 = id1b;
+      qrow = qrowb;
+      cnt = cnt2;
     }
     // Drain: every stage's most recent load must land before the CTA exits.
     if (lane == 0) {
@@ -320,11 +365,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* ml = reinterpret_cast<float*>(smem + kOffMl);
   int cphase = 0;
 
-  float m[G], l[G], o[G][4];
+  // Online-softmax state of this warp for the current unit: running max m
+  // (log2 domain), this lane's share of the sum l, and the output of this
+  // lane's 4 dimensions kept as (even-token, odd-token) partial pairs.
+  float m[G], l[G];
+  float2 acc[G][4];
   Walk cw = w0;
   int seg = -1;
   bool ok = true;
-  for (int n = 0; n < nloc && ok; ++n, walk_next(cw, a)) {
+  for (int n = 0; n < nloc && ok; ++n, walk_next(cw, a, s_len)) {
     const bool seg_start = (n == 0) || (cw.i == 0);
     const bool seg_end = (n == nloc - 1) || (cw.i == cw.nch - 1);
     if (seg_start) {
@@ -352,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         m[h] = -INFINITY;
         l[h] = 0.f;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) o[h][e] = 0.f;
+        for (int e = 0; e < 4; ++e) acc[h][e] = make_float2(0.f, 0.f);
       }
     }
 
@@ -366,10 +415,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t sV = sK + kKBytes;
       const int ntok = min(kChunkTokens, cw.L - cw.i * kChunkTokens);
 
-      // ---- S = q . k, lane-per-token ----
-      float s[G];
+      // ---- S = q . k, lane-per-token, packed pairs of dimensions ----
+      float2 s2[G];
 #pragma unroll
-      for (int h = 0; h < G; ++h) s[h] = 0.f;
+      for (int h = 0; h < G; ++h) s2[h] = make_float2(0.f, 0.f);
       {
         const int r = lane & 15;
         const uint32_t rowbase = sK + (lane >> 4) * kTileBytes + r * 128;
@@ -378,25 +427,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t addr =
               rowbase + (c >> 3) * kBoxBytes + ((((c & 7) ^ (r & 7))) << 4);
           const uint4 kv = lds128(addr);
-          float k[8];
-          k[0] = bf16lo_to_f32(kv.x); k[1] = bf16hi_to_f32(kv.x);
-          k[2] = bf16lo_to_f32(kv.y); k[3] = bf16hi_to_f32(kv.y);
-          k[4] = bf16lo_to_f32(kv.z); k[5] = bf16hi_to_f32(kv.z);
-          k[6] = bf16lo_to_f32(kv.w); k[7] = bf16hi_to_f32(kv.w);
+          const float2 k01 = make_float2(bf16lo_to_f32(kv.x), bf16hi_to_f32(kv.x));
+          const float2 k23 = make_float2(bf16lo_to_f32(kv.y), bf16hi_to_f32(kv.y));
+          const float2 k45 = make_float2(bf16lo_to_f32(kv.z), bf16hi_to_f32(kv.z));
+          const float2 k67 = make_float2(bf16lo_to_f32(kv.w), bf16hi_to_f32(kv.w));
 #pragma unroll
           for (int h = 0; h < G; ++h) {
             const float4 qa = lds128f(qf_addr + (h * kHeadDim + c * 8) * 4);
             const float4 qb = lds128f(qf_addr + (h * kHeadDim + c * 8 + 4) * 4);
-            float acc = s[h];
-            acc = fmaf(qa.x, k[0], acc);
-            acc = fmaf(qa.y, k[1], acc);
-            acc = fmaf(qa.z, k[2], acc);
-            acc = fmaf(qa.w, k[3], acc);
-            acc = fmaf(qb.x, k[4], acc);
-            acc = fmaf(qb.y, k[5], acc);
-            acc = fmaf(qb.z, k[6], acc);
-            acc = fmaf(qb.w, k[7], acc);
-            s[h] = acc;
+            float2 t = s2[h];
+            t = __ffma2_rn(make_float2(qa.x, qa.y), k01, t);
+            t = __ffma2_rn(make_float2(qa.z, qa.w), k23, t);
+            t = __ffma2_rn(make_float2(qb.x, qb.y), k45, t);
+            t = __ffma2_rn(make_float2(qb.z, qb.w), k67, t);
+            s2[h] = t;
           }
         }
       }
@@ -406,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float alpha[G];
 #pragma unroll
       for (int h = 0; h < G; ++h) {
-        const float sv = valid ? s[h] : -INFINITY;
+        const float sv = valid ? s2[h].x + s2[h].y : -INFINITY;
         const float mnew = fmaxf(m[h], warp_max(sv));
         alpha[h] = exp2f(m[h] - mnew);
         const float p = exp2f(sv - mnew);
@@ -426,11 +470,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
 
-      // ---- o = alpha * o + P V, lane-per-4-dims ----
+      // ---- acc = alpha * acc + P V over token pairs, lane-per-4-dims ----
 #pragma unroll
       for (int h = 0; h < G; ++h) {
+        const float2 a2 = make_float2(alpha[h], alpha[h]);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) o[h][e] *= alpha[h];
+        for (int e = 0; e < 4; ++e) acc[h][e] = __fmul2_rn(acc[h][e], a2);
       }
       const uint32_t vlane = sV + (lane >> 4) * kBoxBytes + (lane & 1) * 8;
       const int vchunk = (lane & 15) >> 1;
@@ -440,20 +485,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int h = 0; h < G; ++h) p4[h] = lds128f(p_addr + (h * 32 + j4 * 4) * 4);
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const int j = j4 * 4 + jj;
-          const int r = j & 15;
-          const uint2 vv =
-              lds64(vlane + (j >> 4) * kTileBytes + r * 128 + ((vchunk ^ (r & 7)) << 4));
-          const float v0 = bf16lo_to_f32(vv.x), v1 = bf16hi_to_f32(vv.x);
-          const float v2 = bf16lo_to_f32(vv.y), v3 = bf16hi_to_f32(vv.y);
+        for (int pr = 0; pr < 2; ++pr) {
+          const int j = j4 * 4 + pr * 2;  // tokens j, j + 1 (same block: j is even)
+          const int r0 = j & 15, r1 = r0 + 1;
+          const uint32_t vb = vlane + (j >> 4) * kTileBytes;
+          const uint2 v0 = lds64(vb + r0 * 128 + ((vchunk ^ (r0 & 7)) << 4));
+          const uint2 v1 = lds64(vb + r1 * 128 + ((vchunk ^ (r1 & 7)) << 4));
+          const float2 d0 = make_float2(bf16lo_to_f32(v0.x), bf16lo_to_f32(v1.x));
+          const float2 d1 = make_float2(bf16hi_to_f32(v0.x), bf16hi_to_f32(v1.x));
+          const float2 d2 = make_float2(bf16lo_to_f32(v0.y), bf16lo_to_f32(v1.y));
+          const float2 d3 = make_float2(bf16hi_to_f32(v0.y), bf16hi_to_f32(v1.y));
 #pragma unroll
           for (int h = 0; h < G; ++h) {
-            const float p = jj == 0 ? p4[h].x : jj == 1 ? p4[h].y : jj == 2 ? p4[h].z : p4[h].w;
-            o[h][0] = fmaf(p, v0, o[h][0]);
-            o[h][1] = fmaf(p, v1, o[h][1]);
-            o[h][2] = fmaf(p, v2, o[h][2]);
-            o[h][3] = fmaf(p, v3, o[h][3]);
+            const float2 pp = pr == 0 ? make_float2(p4[h].x, p4[h].y)
+                                      : make_float2(p4[h].z, p4[h].w);
+            acc[h][0] = __ffma2_rn(pp, d0, acc[h][0]);
+            acc[h][1] = __ffma2_rn(pp, d1, acc[h][1]);
+            acc[h][2] = __ffma2_rn(pp, d2, acc[h][2]);
+            acc[h][3] = __ffma2_rn(pp, d3, acc[h][3]);
           }
         }
       }
@@ -468,7 +517,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int h = 0; h < G; ++h) {
         const float lt = warp_sum(l[h]);
         *reinterpret_cast<float4*>(&mo[((warp * kMaxGroup) + h) * kHeadDim + lane * 4]) =
-            make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
+            make_float4(acc[h][0].x + acc[h][0].y, acc[h][1].x + acc[h][1].y,
+                        acc[h][2].x + acc[h][2].y, acc[h][3].x + acc[h][3].y);
         if (lane == 0) {
           ml[(warp * kMaxGroup + h) * 2 + 0] = m[h];
           ml[(warp * kMaxGroup + h) * 2 + 1] = lt;
@@ -527,16 +577,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // K2r: merge the partial results of units that straddled CTAs, and write
-// zero rows for decode sequences whose context is invalid.
+// zero rows for decode sequences whose context is invalid.  One CTA per
+// (sequence, kv head); thread (h, d4) owns 4 dimensions of query head h.
 template <int G>
-__global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(G * 32) decode_merge_kernel(const DecodeArgs a) {
   const int Hkv = a.num_kv_heads;
   const int b = blockIdx.x / Hkv, g = blockIdx.x % Hkv;
-  const int d = threadIdx.x;
+  const int h = threadIdx.x >> 5, d4 = threadIdx.x & 31;
   if (a.cu_seqlens_q != nullptr) {
     const int ql = a.cu_seqlens_q[b + 1] - a.cu_seqlens_q[b];
     if (ql < 1) {
-      if (g == 0 && d == 0) set_err(a.err_word, QATTN_DEVERR_CONTEXT);
+      if (g == 0 && threadIdx.x == 0) set_err(a.err_word, QATTN_DEVERR_CONTEXT);
       return;
     }
     if (ql != 1) return;  // a prefill sequence: the prefill kernel owns it
@@ -545,10 +596,11 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a) {
   const int nch = seq_chunks(a, b, &L);
   const int64_t row = q_row_of(a, b);
   __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(a.out) +
-                        (row * a.num_heads + static_cast<int64_t>(g) * G) * kHeadDim;
+                        (row * a.num_heads + static_cast<int64_t>(g) * G + h) * kHeadDim +
+                        d4 * 4;
   if (nch == 0) {
-    for (int h = 0; h < G; ++h) outp[h * kHeadDim + d] = __float2bfloat16_rn(0.f);
-    if (g == 0 && d == 0) set_err(a.err_word, QATTN_DEVERR_CONTEXT);
+    *reinterpret_cast<uint2*>(outp) = make_uint2(0u, 0u);
+    if (g == 0 && threadIdx.x == 0) set_err(a.err_word, QATTN_DEVERR_CONTEXT);
     return;
   }
   const int C = a.ws.cum[a.num_seqs];
@@ -557,21 +609,31 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a) {
   const int nparts = last - first + 1;
   if (nparts == 1) return;
   if (nparts > a.ws.max_parts) {
-    if (d == 0) set_err(a.err_word, QATTN_DEVERR_CONTEXT);
+    if (threadIdx.x == 0) set_err(a.err_word, QATTN_DEVERR_CONTEXT);
     return;
   }
   const int64_t pbase = (static_cast<int64_t>(b) * Hkv + g) * a.ws.max_parts;
-  for (int h = 0; h < G; ++h) {
-    float M = -INFINITY;
-    for (int p = 0; p < nparts; ++p) M = fmaxf(M, a.ws.lse[(pbase + p) * G + h]);
-    float den = 0.f, num = 0.f;
-    for (int p = 0; p < nparts; ++p) {
-      const float f = exp2f(a.ws.lse[(pbase + p) * G + h] - M);
-      den += f;
-      num = fmaf(f, a.ws.part_o[((pbase + p) * G + h) * kHeadDim + d], num);
-    }
-    outp[h * kHeadDim + d] = __float2bfloat16_rn(num / den);
+  float M = -INFINITY;
+#pragma unroll 4
+  for (int p = 0; p < nparts; ++p) M = fmaxf(M, a.ws.lse[(pbase + p) * G + h]);
+  float den = 0.f;
+  float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+  for (int p = 0; p < nparts; ++p) {
+    const float f = exp2f(a.ws.lse[(pbase + p) * G + h] - M);
+    const float4 o =
+        *reinterpret_cast<const float4*>(a.ws.part_o + ((pbase + p) * G + h) * kHeadDim + d4 * 4);
+    den += f;
+    num.x = fmaf(f, o.x, num.x);
+    num.y = fmaf(f, o.y, num.y);
+    num.z = fmaf(f, o.z, num.z);
+    num.w = fmaf(f, o.w, num.w);
   }
+  const float inv = 1.f / den;
+  uint2 packed;
+  packed.x = pack_bf16x2_rn(num.x * inv, num.y * inv);
+  packed.y = pack_bf16x2_rn(num.z * inv, num.w * inv);
+  *reinterpret_cast<uint2*>(outp) = packed;
 }
 
 template <int G>
@@ -587,7 +649,7 @@ cudaError_t launch_g(const DecodeArgs& a, const CUtensorMap& kmap, const CUtenso
   paged_decode_kernel<G><<<num_sms, kThreads, kSmemBytes, stream>>>(kmap, vmap, a);
   cudaError_t e = cudaPeekAtLastError();
   if (e != cudaSuccess) return e;
-  decode_merge_kernel<G><<<a.num_seqs * a.num_kv_heads, 128, 0, stream>>>(a);
+  decode_merge_kernel<G><<<a.num_seqs * a.num_kv_heads, G * 32, 0, stream>>>(a);
   return cudaPeekAtLastError();
 }
 
