@@ -159,6 +159,32 @@ int qattn_paged_decode(void* out, const void* q, int64_t q_row_stride,
                        qattn_dims dims, void* workspace, size_t workspace_bytes,
                        int32_t* err_word, void* stream);
 
+/* qattn_paged_decode for callers that cannot allocate device memory (code
+ * running inside someone else's CUDA-graph capture, a serving loop whose
+ * memory pool is fixed at start-up, a host that only lends the tensors it
+ * computes on).  Same arguments and results as qattn_paged_decode, without
+ * the workspace: the split-KV partial results go to a 32 MiB scratch array
+ * compiled into this library, which every GPU that loads the library keeps
+ * until the process exits.  This entry point has no counterpart on the
+ * pages; it exists only because of those callers.
+ *   - Shapes whose qattn_paged_decode_workspace_size() exceeds 32 MiB
+ *     (33554432 bytes) are refused with QATTN_ERR_WORKSPACE before any
+ *     launch (e.g. 64 sequences x 4096 tokens x 28 heads needs ~16 MiB).
+ *   - The first call on a device, with that device current, looks up the
+ *     array's device address (cudaGetSymbolAddress); make that first call
+ *     before any stream capture.  No call allocates or frees memory.
+ *   - All calls share the array and it keeps the previous call's contents;
+ *     nothing in it needs to start at zero.  Calls whose kernels may run at
+ *     the same time on the GPU (unordered streams) race on it: order them,
+ *     or use qattn_paged_decode with workspaces of your own. */
+int qattn_paged_decode_noalloc(void* out, const void* q, int64_t q_row_stride,
+                               const void* k_cache, const void* v_cache,
+                               int32_t num_blocks, const int32_t* block_tables,
+                               int32_t max_blocks_per_seq,
+                               const int32_t* context_lens, int32_t num_seqs,
+                               int32_t max_context_len, qattn_dims dims,
+                               int32_t* err_word, void* stream);
+
 /* Bytes of device workspace qattn_varlen_prefill needs (same rules). */
 size_t qattn_varlen_prefill_workspace_size(int32_t num_seqs,
                                            int32_t max_context_len,

@@ -38,6 +38,7 @@ EXPORTED = [
     "qattn_rope_cache_append",
     "qattn_paged_decode_workspace_size",
     "qattn_paged_decode",
+    "qattn_paged_decode_noalloc",
     "qattn_varlen_prefill_workspace_size",
     "qattn_varlen_prefill",
 ]
