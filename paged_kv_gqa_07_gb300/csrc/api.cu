@@ -2,6 +2,7 @@
 // tensor-map encoding and status strings.  No device memory is allocated
 // here; every buffer belongs to the caller.
 #include <math.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <mutex>
@@ -122,6 +123,43 @@ bool cached_cache_map(CUtensorMap* out, const void* cache, int32_t num_blocks,
   return true;
 }
 
+// The query rows seen as a 3-D tensor [rows][num_heads][128]; a box is one
+// row's G consecutive heads x 64 columns (half a head), 128-byte swizzled:
+// the tensor-core decode loads a KV head's query group with two boxes.
+bool encode_q_group_map(CUtensorMap* map, const void* q, int64_t q_row_stride, int32_t rows,
+                        int32_t num_heads, int32_t group) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim),
+                              static_cast<cuuint64_t>(num_heads),
+                              static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim) * 2,
+                                 static_cast<cuuint64_t>(q_row_stride) * 2};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(group), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Which decode kernel serves a group size: the tensor-core kernel for groups
+// of 3..8 query heads per KV head, the CUDA-core kernel for 1 and 2.  The
+// environment variable QATTN_DECODE_KERNEL=cuda|tc forces one (tc only
+// where it supports the group).
+bool use_tc_decode(int group) {
+  static int forced = [] {
+    const char* e = getenv("QATTN_DECODE_KERNEL");
+    if (e == nullptr) return 0;
+    if (strcmp(e, "cuda") == 0) return 1;
+    if (strcmp(e, "tc") == 0) return 2;
+    return 0;
+  }();
+  const bool tc_ok = group >= 3 && group <= 8;
+  if (forced == 1) return false;
+  if (forced == 2) return tc_ok;
+  return tc_ok;
+}
+
 int check_cache(const void* k_cache, const void* v_cache, int32_t num_blocks,
                 const qattn_dims& d) {
   if (k_cache == nullptr || v_cache == nullptr || num_blocks <= 0) return QATTN_ERR_INVALID_ARG;
@@ -220,7 +258,8 @@ size_t qattn_paged_decode_workspace_size(int32_t num_seqs, int32_t max_context_l
 
 namespace {
 
-int decode_common(void* out, const void* q, int64_t q_row_stride, const int32_t* cu_seqlens_q,
+int decode_common(void* out, const void* q, int64_t q_row_stride, int32_t q_rows,
+                  const int32_t* cu_seqlens_q,
                   const void* k_cache, const void* v_cache, int32_t num_blocks,
                   const int32_t* block_tables, int32_t max_blocks_per_seq,
                   const int32_t* context_lens, int32_t num_seqs, int32_t max_context_len,
@@ -248,6 +287,15 @@ int decode_common(void* out, const void* q, int64_t q_row_stride, const int32_t*
   a.err_word = err_word;
   a.ws = carve_decode_workspace(workspace, num_seqs, max_context_len, dims.num_kv_heads,
                                 dims.num_heads / dims.num_kv_heads);
+  const int group = dims.num_heads / dims.num_kv_heads;
+  if (use_tc_decode(group)) {
+    CUtensorMap qmap;
+    if (!encode_q_group_map(&qmap, q, q_row_stride, q_rows, dims.num_heads, group))
+      return QATTN_ERR_CUDA;
+    a.tile_tokens = kTcTileTokens;
+    return cuda_status(launch_paged_decode_tc(a, kmap, vmap, qmap, num_sms, stream));
+  }
+  a.tile_tokens = kChunkTokens;
   return cuda_status(launch_paged_decode(a, kmap, vmap, num_sms, stream));
 }
 
@@ -284,7 +332,8 @@ int qattn_paged_decode(void* out, const void* q, int64_t q_row_stride, const voi
     return QATTN_ERR_CUDA;
   const int sms = num_sms_current();
   if (sms <= 0) return QATTN_ERR_CUDA;
-  return decode_common(out, q, q_row_stride, nullptr, k_cache, v_cache, num_blocks, block_tables,
+  return decode_common(out, q, q_row_stride, num_seqs, nullptr, k_cache, v_cache, num_blocks,
+                       block_tables,
                        max_blocks_per_seq, context_lens, num_seqs, max_context_len, dims,
                        workspace, workspace_bytes, err_word, static_cast<cudaStream_t>(stream),
                        kmap, vmap, sms);
@@ -318,7 +367,7 @@ int qattn_varlen_prefill(void* out, const void* q, int64_t q_row_stride,
   if (sms <= 0) return QATTN_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // Decode rows (one query) of the batch.
-  st = decode_common(out, q, q_row_stride, cu_seqlens_q, k_cache, v_cache, num_blocks,
+  st = decode_common(out, q, q_row_stride, total_q, cu_seqlens_q, k_cache, v_cache, num_blocks,
                      block_tables, max_blocks_per_seq, context_lens, num_seqs, max_context_len,
                      dims, workspace, workspace_bytes, err_word, s, kmap, vmap, sms);
   if (st != QATTN_OK || max_q_len < 2) return st;

@@ -68,9 +68,19 @@ struct DecodeArgs {
   float scale_log2;        // softmax scale * log2(e)
   int32_t* err_word;
   DecodeWorkspace ws;
+  int32_t tile_tokens;     // tokens per work unit of the kernel that ran (merge needs it)
 };
+// CUDA-core decode (K2): 32-token chunks, the GQA group on CUDA cores.
 cudaError_t launch_paged_decode(const DecodeArgs& a, const CUtensorMap& kmap,
                                 const CUtensorMap& vmap, int num_sms, cudaStream_t stream);
+// Tensor-core decode (K2t): 128-token tiles, the GQA group as the MMA N dimension.
+constexpr int kTcTileTokens = 128;
+constexpr int kTcMinTilesPerCta = 2;
+cudaError_t launch_paged_decode_tc(const DecodeArgs& a, const CUtensorMap& kmap,
+                                   const CUtensorMap& vmap, const CUtensorMap& qmap,
+                                   int num_sms, cudaStream_t stream);
+// K2r for either decode kernel (reads a.tile_tokens).
+cudaError_t launch_decode_merge(const DecodeArgs& a, cudaStream_t stream);
 
 // ---- varlen prefill (varlen_prefill.cu) ----
 struct PrefillArgs {

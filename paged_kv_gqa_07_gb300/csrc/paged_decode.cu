@@ -592,8 +592,8 @@ __global__ void __launch_bounds__(G * 32) decode_merge_kernel(const DecodeArgs a
     }
     if (ql != 1) return;  // a prefill sequence: the prefill kernel owns it
   }
-  int L;
-  const int nch = seq_chunks(a, b, &L);
+  const int L = seq_len_eff(a, b);
+  const int nch = (L + a.tile_tokens - 1) / a.tile_tokens;
   const int64_t row = q_row_of(a, b);
   __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(a.out) +
                         (row * a.num_heads + static_cast<int64_t>(g) * G + h) * kHeadDim +
@@ -649,6 +649,11 @@ cudaError_t launch_g(const DecodeArgs& a, const CUtensorMap& kmap, const CUtenso
   paged_decode_kernel<G><<<num_sms, kThreads, kSmemBytes, stream>>>(kmap, vmap, a);
   cudaError_t e = cudaPeekAtLastError();
   if (e != cudaSuccess) return e;
+  return launch_decode_merge(a, stream);
+}
+
+template <int G>
+cudaError_t launch_merge_g(const DecodeArgs& a, cudaStream_t stream) {
   decode_merge_kernel<G><<<a.num_seqs * a.num_kv_heads, G * 32, 0, stream>>>(a);
   return cudaPeekAtLastError();
 }
@@ -679,6 +684,20 @@ DecodeWorkspace carve_decode_workspace(void* base, int32_t num_seqs, int32_t max
   w.part_o = reinterpret_cast<float*>(p);
   w.max_parts = static_cast<int32_t>(max_parts);
   return w;
+}
+
+cudaError_t launch_decode_merge(const DecodeArgs& a, cudaStream_t stream) {
+  switch (a.num_heads / a.num_kv_heads) {
+    case 1: return launch_merge_g<1>(a, stream);
+    case 2: return launch_merge_g<2>(a, stream);
+    case 3: return launch_merge_g<3>(a, stream);
+    case 4: return launch_merge_g<4>(a, stream);
+    case 5: return launch_merge_g<5>(a, stream);
+    case 6: return launch_merge_g<6>(a, stream);
+    case 7: return launch_merge_g<7>(a, stream);
+    case 8: return launch_merge_g<8>(a, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_paged_decode(const DecodeArgs& a, const CUtensorMap& kmap,

@@ -1,0 +1,655 @@
+// Kernel K2t: paged GQA decode with the group's dot products on tcgen05.
+//
+// What is computed is the decode attention of the grouped-query layer
+// ("Qwen2 模型结构代码详解" section 2: 28 query heads share 4 KV heads, scale
+// head_dim ** -0.5) over the PagedAttention block cache (vLLM-deploys-Qwen
+// notes section 2.1): for each decode sequence b and query head h with KV
+// head g = h / G,  out[b, h] = sum_j softmax_j(scale * q[b,h] . k_j) v_j.
+//
+// Why tensor cores here.  All G query heads of a group read the same keys,
+// so per KV tile the work is a dense product of the tile (tokens x 128) with
+// the group (128 x G).  Done on CUDA cores that costs ~2400 warp
+// instructions per 16 KB of KV for G = 7 (measured), which caps the kernel
+// well below HBM speed; on tcgen05 the same tile is 16 instructions of one
+// thread.  The layout puts tokens on the MMA M dimension (128) and the group
+// on N (padded to 16), so the K tile straight from the cache is the K-major
+// A operand and the V tile is the MN-major A operand of the transposed
+// product -- nothing is re-laid:
+//     S^T[tok, h]  = K[tok, :] . Q^T[:, h]           (M = 128, N = 16, K = 128)
+//     O^T[d, h]   += V^T[d, tok] . P^T[tok, h]        (M = 128, N = 16, K = 128)
+// The online-softmax state (per-head running max and sum over tokens) is
+// reduced across the 128 token threads with warp shuffles plus one exchange
+// between the four softmax warps per tile.
+//
+// Structure (one CTA per SM, persistent):
+//   * work list: (sequence, kv head) units cut into 128-token tiles (eight
+//     16-token blocks); each CTA takes an equal contiguous run of tiles
+//     (>= 2); units that straddle CTAs are merged by K2r as for K2.
+//   * warp 4 issues TMA: Q^T of a unit (a G x 128 box of the query rows),
+//     K and V tiles (16 x 64 boxes, 128-byte swizzle) into 3-deep K and V
+//     rings; warp 5 (one thread) issues tcgen05.mma and commits; warps 0-3
+//     (thread = token for S, thread = dimension for O) run the softmax and
+//     write P^T as bf16 into swizzled shared memory.
+//   * O is rescaled lazily (only when a head's max grows by more than 2^8).
+//   * keys past the context are masked in S and their V rows zeroed.
+//   * every wait is bounded; on a timeout all roles unwind, drain their
+//     copies and MMAs, and TMEM is freed.
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace qattn {
+namespace {
+
+constexpr int kTile = kTcTileTokens;  // 128 tokens
+constexpr int kN = 16;                // MMA N: the query group padded to 16 heads
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kThreads = 6 * 32;
+constexpr int kHalfBytes = kTile * 128;  // 128 rows x 128 B (one d-half of a tile)
+constexpr int kTileBytes = 2 * kHalfBytes;
+constexpr int kKStages = 3;
+constexpr int kVStages = 3;
+constexpr int kSmallHalf = kN * 128;     // 16 rows x 128 B
+constexpr int kSmallBytes = 2 * kSmallHalf;
+constexpr uint32_t kTmemCols = 64;
+constexpr uint32_t kColO = 32;
+constexpr float kLazyRescale = 8.0f;
+constexpr int kMaxSmemSeqs = 2048;
+
+constexpr int kOffK = 0;
+constexpr int kOffV = kOffK + kKStages * kTileBytes;
+constexpr int kOffQ = kOffV + kVStages * kTileBytes;  // 2 slots of Q^T
+constexpr int kOffP = kOffQ + 2 * kSmallBytes;        // 2 buffers of P^T
+constexpr int kOffRed = kOffP + 2 * kSmallBytes;      // [2][4][16] fp32
+constexpr int kOffLsum = kOffRed + 2 * 4 * kN * 4;    // [4][16] fp32
+constexpr int kOffBars = kOffLsum + 4 * kN * 4;
+// k_full[3] k_empty[3] v_full[3] v_empty[3] q_full[2] q_empty[2] s_full[2]
+// s_free[2] p_full[2] p_free[2] o_done o_free rbar mma_done
+constexpr int kNumBars = 3 * 4 + 2 * 6 + 4;
+constexpr int kOffMisc = kOffBars + kNumBars * 8;
+constexpr int kOffLens = kOffMisc + 64;
+constexpr int kSmemBytes = kOffLens + kMaxSmemSeqs * 4 + 1024;
+
+struct Misc {
+  uint32_t tmem;
+  int abort;
+  int b0;
+  int off0;
+  int warp_sums[6];
+};
+
+__device__ __forceinline__ int seq_len_eff(const DecodeArgs& a, int b) {
+  const int L = a.context_lens[b];
+  if (a.cu_seqlens_q != nullptr) {
+    if (a.cu_seqlens_q[b + 1] - a.cu_seqlens_q[b] != 1) return 0;
+  }
+  if (L < 1 || L > a.max_context_len || L > a.max_blocks_per_seq * kBlockSize) return 0;
+  return L;
+}
+
+__device__ __forceinline__ int seq_len_cached(const DecodeArgs& a, const int* s_len, int b) {
+  return a.num_seqs <= kMaxSmemSeqs ? s_len[b] : seq_len_eff(a, b);
+}
+
+struct Walk {
+  int b, g, i, nt, L;  // sequence, kv head, tile i of nt, context length
+};
+
+__device__ __forceinline__ void walk_next(Walk& w, const DecodeArgs& a, const int* s_len) {
+  if (++w.i < w.nt) return;
+  w.i = 0;
+  if (++w.g < a.num_kv_heads) return;
+  w.g = 0;
+  for (;;) {
+    ++w.b;
+    if (w.b >= a.num_seqs) {
+      w.nt = 0;
+      return;
+    }
+    w.L = seq_len_cached(a, s_len, w.b);
+    w.nt = (w.L + kTile - 1) / kTile;
+    if (w.nt > 0) return;
+  }
+}
+
+__device__ __forceinline__ Walk shfl_walk_helper(const Walk& w, int src) {
+  Walk r;
+  r.b = __shfl_sync(0xffffffffu, w.b, src);
+  r.g = __shfl_sync(0xffffffffu, w.g, src);
+  r.i = __shfl_sync(0xffffffffu, w.i, src);
+  r.nt = __shfl_sync(0xffffffffu, w.nt, src);
+  r.L = __shfl_sync(0xffffffffu, w.L, src);
+  return r;
+}
+
+__device__ __forceinline__ int64_t q_row_of(const DecodeArgs& a, int b) {
+  return a.cu_seqlens_q != nullptr ? static_cast<int64_t>(a.cu_seqlens_q[b]) : b;
+}
+
+// Inclusive scan over the CTA's 192 threads.
+__device__ __forceinline__ int block_scan(int v, int* warp_sums, int* block_total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  if (lane == 31) warp_sums[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < 6 ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += n;
+    }
+    if (lane < 6) warp_sums[lane] = w;
+  }
+  __syncthreads();
+  const int add = warp > 0 ? warp_sums[warp - 1] : 0;
+  *block_total = warp_sums[5];
+  __syncthreads();
+  return v + add;
+}
+
+template <int G>
+__global__ void __launch_bounds__(kThreads, 1)
+    paged_decode_tc_kernel(const __grid_constant__ CUtensorMap kmap,
+                           const __grid_constant__ CUtensorMap vmap,
+                           const __grid_constant__ CUtensorMap qmap, const DecodeArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBars);
+  uint64_t* k_full = bars;
+  uint64_t* k_empty = bars + 3;
+  uint64_t* v_full = bars + 6;
+  uint64_t* v_empty = bars + 9;
+  uint64_t* q_full = bars + 12;
+  uint64_t* q_empty = bars + 14;
+  uint64_t* s_full = bars + 16;
+  uint64_t* s_free = bars + 18;
+  uint64_t* p_full = bars + 20;
+  uint64_t* p_free = bars + 22;
+  uint64_t* o_done = bars + 24;
+  uint64_t* o_free = bars + 25;
+  uint64_t* rbar = bars + 26;
+  uint64_t* mma_done = bars + 27;
+  Misc* misc = reinterpret_cast<Misc*>(smem + kOffMisc);
+  int* s_len = reinterpret_cast<int*>(smem + kOffLens);
+  float* red = reinterpret_cast<float*>(smem + kOffRed);
+  float* lsum = reinterpret_cast<float*>(smem + kOffLsum);
+  volatile int* abort_flag = &misc->abort;
+  const uint32_t sbase = smem_u32(smem);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int Hkv = a.num_kv_heads;
+  const int B = a.num_seqs;
+
+  // ---- plan: tile count, this CTA's run [c0, c1), its first unit ----
+  if (tid == 0) {
+    misc->abort = 0;
+    misc->b0 = -1;
+    misc->off0 = 0;
+  }
+  int local = 0;
+  for (int b = tid; b < B; b += kThreads) {
+    const int L = seq_len_eff(a, b);
+    if (B <= kMaxSmemSeqs) s_len[b] = L;
+    local += Hkv * ((L + kTile - 1) / kTile);
+  }
+  int total;
+  block_scan(local, misc->warp_sums, &total);
+  const int C = max(kTcMinTilesPerCta, (total + static_cast<int>(gridDim.x) - 1) /
+                                           static_cast<int>(gridDim.x));
+  const int c0 = static_cast<int>(blockIdx.x) * C;
+  const int c1 = min(total, c0 + C);
+  int running = 0;
+  for (int base = 0; base < B; base += kThreads) {
+    const int b = base + tid;
+    const int L = b < B ? seq_len_cached(a, s_len, b) : 0;
+    const int u = Hkv * ((L + kTile - 1) / kTile);
+    int tile_total;
+    const int incl = block_scan(u, misc->warp_sums, &tile_total);
+    const int excl = running + incl - u;
+    if (blockIdx.x == 0 && b < B) a.ws.cum[b] = excl;
+    if (u > 0 && excl <= c0 && c0 < excl + u) {
+      misc->b0 = b;
+      misc->off0 = c0 - excl;
+    }
+    running += tile_total;
+  }
+  if (blockIdx.x == 0 && tid == 0) a.ws.cum[B] = C;
+  __syncthreads();
+  if (c0 >= c1) return;  // nothing for this CTA: no barrier, copy or TMEM in use yet
+  const int nloc = c1 - c0;
+
+  // ---- set-up: barriers, zeroed Q^T / P^T buffers, TMEM ----
+  if (tid == 0) {
+    for (int s = 0; s < 3; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&q_full[s], 1);
+      mbar_init(&q_empty[s], 1);
+      mbar_init(&s_full[s], 1);
+      mbar_init(&s_free[s], 4);
+      mbar_init(&p_full[s], 4);
+      mbar_init(&p_free[s], 1);
+    }
+    mbar_init(o_done, 1);
+    mbar_init(o_free, 4);
+    mbar_init(rbar, 4);
+    mbar_init(mma_done, 1);
+    fence_barrier_init();
+  }
+  for (int i = tid; i < 4 * kSmallBytes / 16; i += kThreads)
+    sts128(sbase + kOffQ + i * 16, 0u, 0u, 0u, 0u);  // rows >= G of Q^T stay zero
+  fence_proxy_async_smem();
+  if (warp == kMmaWarp) {
+    tmem_alloc(&misc->tmem, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc->tmem;
+
+  Walk w0;
+  w0.b = misc->b0;
+  w0.L = seq_len_cached(a, s_len, w0.b);
+  w0.nt = (w0.L + kTile - 1) / kTile;
+  w0.g = misc->off0 / w0.nt;
+  w0.i = misc->off0 % w0.nt;
+
+  if (warp == kProducerWarp) {
+    // ================================ producer ================================
+    // Batches of 32 tiles: lane l walks to tile (batch start + l) and loads
+    // its eight block ids; lane 0 then issues the copies tile by tile.
+    if (lane == 0) {
+      tma_prefetch_desc(&kmap);
+      tma_prefetch_desc(&vmap);
+      tma_prefetch_desc(&qmap);
+    }
+    Walk bw = w0;
+    int n = 0, seg = -1;
+    bool ok = true;
+    while (n < nloc && ok) {
+      const int cnt = min(32, nloc - n);
+      Walk mw = bw;
+      for (int k = 0; k < lane && k < cnt - 1; ++k) walk_next(mw, a, s_len);
+      int ids[8];
+      int64_t qrow = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) ids[j] = -1;
+      if (lane < cnt) {
+        const int ntok = min(kTile, mw.L - mw.i * kTile);
+        const int nblk = (ntok + kBlockSize - 1) / kBlockSize;
+        const int* row = a.block_tables + static_cast<int64_t>(mw.b) * a.max_blocks_per_seq +
+                         mw.i * (kTile / kBlockSize);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (j < nblk) ids[j] = row[j];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (j < nblk && (ids[j] < 0 || ids[j] >= a.num_blocks)) {
+            set_err(a.err_word, QATTN_DEVERR_BLOCK);
+            ids[j] = -1;
+          }
+        }
+        if (mw.i == 0 || n + lane == 0) qrow = q_row_of(a, mw.b);
+      }
+      for (int c = 0; c < cnt && ok; ++c) {
+        const int g = __shfl_sync(0xffffffffu, mw.g, c);
+        const int ci = __shfl_sync(0xffffffffu, mw.i, c);
+        const int64_t cq = __shfl_sync(0xffffffffu, qrow, c);
+        int cid[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) cid[j] = __shfl_sync(0xffffffffu, ids[j], c);
+        if (lane == 0) {
+          uint32_t nvalid = 0;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) nvalid += cid[j] >= 0 ? 1u : 0u;
+          if (ci == 0 || n == 0) {
+            ++seg;
+            const int qs = seg & 1;
+            ok = mbar_wait(&q_empty[qs], ((seg >> 1) & 1) ^ 1, abort_flag);
+            if (ok) {
+              mbar_arrive_expect_tx(&q_full[qs], 2 * G * 128);
+              uint8_t* qdst = smem + kOffQ + qs * kSmallBytes;
+              tma_load_3d(qdst, &qmap, 0, g * G, static_cast<int32_t>(cq), &q_full[qs]);
+              tma_load_3d(qdst + kSmallHalf, &qmap, 64, g * G, static_cast<int32_t>(cq),
+                          &q_full[qs]);
+            }
+          }
+          const int ks = n % kKStages;
+          ok = ok && mbar_wait(&k_empty[ks], ((n / kKStages) & 1) ^ 1, abort_flag);
+          if (ok) {
+            mbar_arrive_expect_tx(&k_full[ks], nvalid * 2 * kBlockSize * 128);
+            uint8_t* kdst = smem + kOffK + ks * kTileBytes;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              if (cid[j] < 0) continue;
+              const int32_t y = (cid[j] * Hkv + g) * kBlockSize;
+              tma_load_2d(kdst + j * kBlockSize * 128, &kmap, 0, y, &k_full[ks]);
+              tma_load_2d(kdst + kHalfBytes + j * kBlockSize * 128, &kmap, 64, y, &k_full[ks]);
+            }
+          }
+          const int vs = n % kVStages;
+          ok = ok && mbar_wait(&v_empty[vs], ((n / kVStages) & 1) ^ 1, abort_flag);
+          if (ok) {
+            mbar_arrive_expect_tx(&v_full[vs], nvalid * 2 * kBlockSize * 128);
+            uint8_t* vdst = smem + kOffV + vs * kTileBytes;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              if (cid[j] < 0) continue;
+              const int32_t y = (cid[j] * Hkv + g) * kBlockSize;
+              tma_load_2d(vdst + j * kBlockSize * 128, &vmap, 0, y, &v_full[vs]);
+              tma_load_2d(vdst + kHalfBytes + j * kBlockSize * 128, &vmap, 64, y, &v_full[vs]);
+            }
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (ok) ++n;
+      }
+      bw = shfl_walk_helper(mw, cnt - 1);
+      walk_next(bw, a, s_len);
+    }
+    // Drain: the most recent K, V and Q copies land before the CTA exits.
+    if (lane == 0) {
+      for (int j = n - 1; j >= 0 && j >= n - 3; --j) {
+        mbar_wait_drain(&k_full[j % kKStages], (j / kKStages) & 1);
+        mbar_wait_drain(&v_full[j % kVStages], (j / kVStages) & 1);
+      }
+      for (int s = seg; s >= 0 && s >= seg - 1; --s) mbar_wait_drain(&q_full[s & 1], (s >> 1) & 1);
+      if (*abort_flag) set_err(a.err_word, QATTN_DEVERR_TIMEOUT);
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ============================== MMA issuer ===============================
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(kTile, kN, false, false);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(kHeadDim, kN, false, true);
+      bool ok = true;
+      Walk mw = w0;
+      int seg = -1;
+      int prev_first = 0;   // tile n-1 opened its unit (PV starts a fresh accumulator)
+      int prev_seg = -1;    // segment index of tile n-1
+      auto issue_pv = [&](int j, bool first_of_seg, int seg_of_j) {
+        const int pb = j & 1;
+        ok = ok && mbar_wait(&p_full[pb], (j >> 1) & 1, abort_flag);
+        ok = ok && mbar_wait(&v_full[j % kVStages], (j / kVStages) & 1, abort_flag);
+        if (ok && first_of_seg && seg_of_j > 0)
+          ok = mbar_wait(o_free, (seg_of_j - 1) & 1, abort_flag);
+        if (!ok) return;
+        tc_fence_after();
+        const uint32_t sv = sbase + kOffV + (j % kVStages) * kTileBytes;
+        const uint32_t sp = sbase + kOffP + pb * kSmallBytes;
+#pragma unroll
+        for (int k = 0; k < kTile / 16; ++k) {
+          const uint64_t ad = sdesc_sw128(sv + k * (16 * 128), kHalfBytes, 1024);
+          const uint64_t bd = sdesc_sw128(sp + (k >> 2) * kSmallHalf + (k & 3) * 32, 16, 1024);
+          mma_bf16_ss(tmem + kColO, ad, bd, idesc_pv, (first_of_seg && k == 0) ? 0u : 1u);
+        }
+        mma_commit(o_done);
+        mma_commit(&v_empty[j % kVStages]);
+        mma_commit(&p_free[pb]);
+      };
+      for (int n = 0; n < nloc && ok; ++n, walk_next(mw, a, s_len)) {
+        const bool seg_start = (n == 0) || (mw.i == 0);
+        const bool seg_end = (n == nloc - 1) || (mw.i == mw.nt - 1);
+        if (seg_start) {
+          ++seg;
+          ok = mbar_wait(&q_full[seg & 1], (seg >> 1) & 1, abort_flag);
+        }
+        const int ks = n % kKStages, sb = n & 1;
+        ok = ok && mbar_wait(&k_full[ks], (n / kKStages) & 1, abort_flag);
+        if (ok && n >= 2) ok = mbar_wait(&s_free[sb], ((n >> 1) & 1) ^ 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t sk = sbase + kOffK + ks * kTileBytes;
+        const uint32_t sq = sbase + kOffQ + (seg & 1) * kSmallBytes;
+#pragma unroll
+        for (int k = 0; k < kHeadDim / 16; ++k) {
+          const uint64_t ad = sdesc_sw128(sk + (k >> 2) * kHalfBytes + (k & 3) * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(sq + (k >> 2) * kSmallHalf + (k & 3) * 32, 16, 1024);
+          mma_bf16_ss(tmem + sb * kN, ad, bd, idesc_qk, k > 0 ? 1u : 0u);
+        }
+        mma_commit(&s_full[sb]);
+        mma_commit(&k_empty[ks]);
+        if (seg_end) mma_commit(&q_empty[seg & 1]);
+        if (n > 0) issue_pv(n - 1, prev_first != 0, prev_seg);
+        prev_first = seg_start ? 1 : 0;
+        prev_seg = seg;
+      }
+      if (ok && nloc > 0) issue_pv(nloc - 1, prev_first != 0, prev_seg);
+      // Drain: every MMA issued above completes before TMEM is released.
+      mma_commit(mma_done);
+      mbar_wait_drain(mma_done, 0);
+    }
+    __syncwarp();
+  } else {
+    // =============================== softmax ================================
+    const int t = tid;  // token row of S^T / dimension row of O^T = TMEM lane
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    float m_used[G], l_t[G];
+    int rphase = 0;
+    bool ok = true;
+    Walk sw = w0;
+    int seg = -1;
+    for (int n = 0; n < nloc; ++n, walk_next(sw, a, s_len)) {
+      const bool seg_start = (n == 0) || (sw.i == 0);
+      const bool seg_end = (n == nloc - 1) || (sw.i == sw.nt - 1);
+      if (seg_start) {
+        ++seg;
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          m_used[h] = -INFINITY;
+          l_t[h] = 0.f;
+        }
+      }
+      const int sb = n & 1, pb = n & 1;
+      const int nvalid_tok = min(kTile, sw.L - sw.i * kTile);
+      const bool valid = t < nvalid_tok;
+
+      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[sb], (n >> 1) & 1, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float s[kN];
+      tmem_ld16(lane_addr + sb * kN, s);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_free[sb]);
+
+      // per-head max over the tile's tokens: shuffle tree, then 4 warps
+      float* rd = red + (n & 1) * 4 * kN;
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        s[h] = valid ? s[h] * a.scale_log2 : -INFINITY;
+        const float wm = warp_max(s[h]);
+        if (lane == 0) rd[warp * kN + h] = wm;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(rbar);
+      if (!__all_sync(0xffffffffu, mbar_wait(rbar, rphase & 1, abort_flag))) {
+        ok = false;
+        break;
+      }
+      ++rphase;
+      float alpha[G];
+      bool any_rescale = false;
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float tmax =
+            fmaxf(fmaxf(rd[0 * kN + h], rd[1 * kN + h]), fmaxf(rd[2 * kN + h], rd[3 * kN + h]));
+        alpha[h] = 1.f;
+        if (seg_start) {
+          m_used[h] = tmax;
+        } else if (tmax > m_used[h] + kLazyRescale) {
+          alpha[h] = exp2f(m_used[h] - tmax);
+          m_used[h] = tmax;
+          any_rescale = true;
+        }
+      }
+      if (any_rescale) {
+        // O^T holds the unit's tiles so far: wait for PV(n-1), scale row t.
+        if (!__all_sync(0xffffffffu, mbar_wait(o_done, (n - 1) & 1, abort_flag))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        float o[kN];
+        tmem_ld16(lane_addr + kColO, o);
+#pragma unroll
+        for (int h = 0; h < G; ++h) o[h] *= alpha[h];
+        tmem_st16(lane_addr + kColO, o);
+#pragma unroll
+        for (int h = 0; h < G; ++h) l_t[h] *= alpha[h];
+      }
+      // P^T row h, token t (bf16) into buffer pb once PV(n-2) has read it.
+      if (n >= 2) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&p_free[pb], ((n >> 1) & 1) ^ 1, abort_flag))) {
+          ok = false;
+          break;
+        }
+      }
+      {
+        float p[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          p[h] = exp2f(s[h] - m_used[h]);
+          l_t[h] += p[h];
+        }
+        const uint32_t pbase = sbase + kOffP + pb * kSmallBytes + (t >> 6) * kSmallHalf;
+        const int c = t & 63;
+#pragma unroll
+        for (int h = 0; h < kN; ++h) {
+          const uint32_t addr = pbase + h * 128 + ((((c >> 3) ^ (h & 7))) << 4) + (c & 7) * 2;
+          const unsigned short bits =
+              h < G ? __bfloat16_as_ushort(__float2bfloat16_rn(p[h < G ? h : 0])) : 0;
+          asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(bits) : "memory");
+        }
+      }
+      if (nvalid_tok < kTile) {
+        // V rows of tokens past the context: zero them before P V reads them.
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(&v_full[n % kVStages], (n / kVStages) & 1, abort_flag))) {
+          ok = false;
+          break;
+        }
+        if (!valid) {
+          const uint32_t vrow = sbase + kOffV + (n % kVStages) * kTileBytes + t * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            sts128(vrow + c * 16, 0u, 0u, 0u, 0u);
+            sts128(vrow + kHalfBytes + c * 16, 0u, 0u, 0u, 0u);
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[pb]);
+
+      if (seg_end) {
+        // ---- unit done in this CTA: total l per head, O^T / l ----
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float ws = warp_sum(l_t[h]);
+          if (lane == 0) lsum[warp * kN + h] = ws;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(rbar);
+        if (!__all_sync(0xffffffffu, mbar_wait(rbar, rphase & 1, abort_flag))) {
+          ok = false;
+          break;
+        }
+        ++rphase;
+        float ltot[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+          ltot[h] = (lsum[0 * kN + h] + lsum[1 * kN + h]) + (lsum[2 * kN + h] + lsum[3 * kN + h]);
+        if (!__all_sync(0xffffffffu, mbar_wait(o_done, n & 1, abort_flag))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        float o[kN];
+        tmem_ld16(lane_addr + kColO, o);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(o_free);
+
+        const int gidx = c0 + n;
+        const int u0 = gidx - sw.i;
+        const int first = u0 / C, last = (u0 + sw.nt - 1) / C;
+        const int nparts = last - first + 1;
+        const int part = static_cast<int>(blockIdx.x) - first;
+        const int64_t row = q_row_of(a, sw.b);
+        if (nparts == 1) {
+          __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) +
+                                (row * a.num_heads + static_cast<int64_t>(sw.g) * G) * kHeadDim;
+#pragma unroll
+          for (int h = 0; h < G; ++h)
+            orow[h * kHeadDim + t] = __float2bfloat16_rn(o[h] / ltot[h]);
+        } else if (part >= 0 && part < a.ws.max_parts) {
+          const int64_t pidx = (static_cast<int64_t>(sw.b) * Hkv + sw.g) * a.ws.max_parts + part;
+#pragma unroll
+          for (int h = 0; h < G; ++h) a.ws.part_o[(pidx * G + h) * kHeadDim + t] = o[h] / ltot[h];
+          if (t < G) {
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+              if (h == t) a.ws.lse[pidx * G + h] = m_used[h] + log2f(ltot[h]);
+          }
+        }
+      }
+    }
+    if (!ok && lane == 0) set_err(a.err_word, QATTN_DEVERR_TIMEOUT);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
+}
+
+template <int G>
+cudaError_t launch_tc_g(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                        const CUtensorMap& qmap, int num_sms, cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(paged_decode_tc_kernel<G>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  paged_decode_tc_kernel<G><<<num_sms, kThreads, kSmemBytes, stream>>>(kmap, vmap, qmap, a);
+  cudaError_t e = cudaPeekAtLastError();
+  if (e != cudaSuccess) return e;
+  return launch_decode_merge(a, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_paged_decode_tc(const DecodeArgs& a, const CUtensorMap& kmap,
+                                   const CUtensorMap& vmap, const CUtensorMap& qmap, int num_sms,
+                                   cudaStream_t stream) {
+  switch (a.num_heads / a.num_kv_heads) {
+    case 3: return launch_tc_g<3>(a, kmap, vmap, qmap, num_sms, stream);
+    case 4: return launch_tc_g<4>(a, kmap, vmap, qmap, num_sms, stream);
+    case 5: return launch_tc_g<5>(a, kmap, vmap, qmap, num_sms, stream);
+    case 6: return launch_tc_g<6>(a, kmap, vmap, qmap, num_sms, stream);
+    case 7: return launch_tc_g<7>(a, kmap, vmap, qmap, num_sms, stream);
+    case 8: return launch_tc_g<8>(a, kmap, vmap, qmap, num_sms, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace qattn
