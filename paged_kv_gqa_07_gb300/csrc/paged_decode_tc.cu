@@ -398,7 +398,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(o_done);
         mma_commit(&v_empty[j % kVStages]);
-        mma_commit(&p_free[pb]);
       };
       for (int n = 0; n < nloc && ok; ++n, walk_next(mw, a, s_len)) {
         const bool seg_start = (n == 0) || (mw.i == 0);
@@ -439,6 +438,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     float m_used[G], l_t[G];
     int rphase = 0;
+    // o_done completes one phase per P V MMA group.  A parity wait is only
+    // sound while the waiter is at most one phase behind, so every tile n
+    // waits for PV(n-1) (and a unit's last tile for PV(n)); o_seen counts
+    // the groups already observed so no phase is waited for twice.
+    int o_seen = 0;
+    auto wait_pv = [&](int j) -> bool {
+      while (o_seen <= j) {
+        if (!__all_sync(0xffffffffu, mbar_wait(o_done, o_seen & 1, abort_flag))) return false;
+        ++o_seen;
+      }
+      return true;
+    };
     bool ok = true;
     Walk sw = w0;
     int seg = -1;
@@ -483,6 +494,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       ++rphase;
+      // PV(n-1) done: O^T may be rescaled and P^T buffer pb (last read by
+      // PV(n-2)) may be rewritten.
+      if (n > 0 && !wait_pv(n - 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
       float alpha[G];
       bool any_rescale = false;
 #pragma unroll
@@ -499,12 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (any_rescale) {
-        // O^T holds the unit's tiles so far: wait for PV(n-1), scale row t.
-        if (!__all_sync(0xffffffffu, mbar_wait(o_done, (n - 1) & 1, abort_flag))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
+        // O^T holds the unit's tiles so far (PV(n-1) is done): scale row t.
         float o[kN];
         tmem_ld16(lane_addr + kColO, o);
 #pragma unroll
@@ -513,13 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int h = 0; h < G; ++h) l_t[h] *= alpha[h];
       }
-      // P^T row h, token t (bf16) into buffer pb once PV(n-2) has read it.
-      if (n >= 2) {
-        if (!__all_sync(0xffffffffu, mbar_wait(&p_free[pb], ((n >> 1) & 1) ^ 1, abort_flag))) {
-          ok = false;
-          break;
-        }
-      }
+      // P^T row h, token t (bf16) into buffer pb.
       {
         float p[G];
 #pragma unroll
@@ -537,13 +544,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(bits) : "memory");
         }
       }
+      // V(n) must have landed before its tail rows are zeroed.  The wait is
+      // made on every tile so this slot's phases are observed in order.
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait(&v_full[n % kVStages], (n / kVStages) & 1, abort_flag))) {
+        ok = false;
+        break;
+      }
       if (nvalid_tok < kTile) {
         // V rows of tokens past the context: zero them before P V reads them.
-        if (!__all_sync(0xffffffffu,
-                        mbar_wait(&v_full[n % kVStages], (n / kVStages) & 1, abort_flag))) {
-          ok = false;
-          break;
-        }
         if (!valid) {
           const uint32_t vrow = sbase + kOffV + (n % kVStages) * kTileBytes + t * 128;
 #pragma unroll
@@ -576,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int h = 0; h < G; ++h)
           ltot[h] = (lsum[0 * kN + h] + lsum[1 * kN + h]) + (lsum[2 * kN + h] + lsum[3 * kN + h]);
-        if (!__all_sync(0xffffffffu, mbar_wait(o_done, n & 1, abort_flag))) {
+        if (!wait_pv(n)) {
           ok = false;
           break;
         }
