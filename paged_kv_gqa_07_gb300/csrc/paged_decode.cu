@@ -293,6 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int cid0 = __shfl_sync(0xffffffffu, id0, c);
         const int cid1 = __shfl_sync(0xffffffffu, id1, c);
         const int64_t cq = __shfl_sync(0xffffffffu, qrow, c);
+        const int stage = n % kStages;
         if (lane == 0) {
           if (ci == 0 || n == 0) {
             ++seg;
@@ -309,7 +310,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               ++q_issued;
             }
           }
-          const int stage = n % kStages;
           if (ok && !mbar_wait(&empty[stage], ((n / kStages) & 1) ^ 1, abort_flag)) ok = false;
           if (ok) {
             const uint32_t bytes = (cid0 >= 0 ? kKBytes : 0) + (cid1 >= 0 ? kKBytes : 0);
@@ -317,23 +317,23 @@ __global__ void __launch_bounds__(kThreads, 1)
               mbar_arrive(&full[stage]);
             } else {
               mbar_arrive_expect_tx(&full[stage], bytes);
-              uint8_t* st = smem + kOffStages + stage * kStageBytes;
-#pragma unroll
-              for (int j = 0; j < 2; ++j) {
-                const int id = j ? cid1 : cid0;
-                if (id < 0) continue;
-                const int32_t y = (id * Hkv + g) * kBlockSize;
-                tma_load_2d(st + j * kTileBytes, &kmap, 0, y, &full[stage]);
-                tma_load_2d(st + j * kTileBytes + kBoxBytes, &kmap, 64, y, &full[stage]);
-                tma_load_2d(st + kKBytes + j * kTileBytes, &vmap, 0, y, &full[stage]);
-                tma_load_2d(st + kKBytes + j * kTileBytes + kBoxBytes, &vmap, 64, y,
-                            &full[stage]);
-              }
             }
           }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
+        // Lanes 0..7 each issue one 16 x 64 box: lane = block j (bit 2),
+        // K or V (bit 1), column half (bit 0) -- one warp-wide instruction.
+        if (lane < 8) {
+          const int j = lane >> 2, isv = (lane >> 1) & 1, half = lane & 1;
+          const int id = j ? cid1 : cid0;
+          if (id >= 0) {
+            const int32_t y = (id * Hkv + g) * kBlockSize;
+            uint8_t* dst = smem + kOffStages + stage * kStageBytes + isv * kKBytes +
+                           j * kTileBytes + half * kBoxBytes;
+            tma_load_2d(dst, isv ? &vmap : &kmap, half * 64, y, &full[stage]);
+          }
+        }
         ++n;
       }
       mw = mw2;

@@ -49,8 +49,8 @@ constexpr int kMmaWarp = 5;
 constexpr int kThreads = 6 * 32;
 constexpr int kHalfBytes = kTile * 128;  // 128 rows x 128 B (one d-half of a tile)
 constexpr int kTileBytes = 2 * kHalfBytes;
-constexpr int kKStages = 3;
-constexpr int kVStages = 3;
+constexpr int kKStages = 2;
+constexpr int kVStages = 4;
 constexpr int kSmallHalf = kN * 128;     // 16 rows x 128 B
 constexpr int kSmallBytes = 2 * kSmallHalf;
 constexpr uint32_t kTmemCols = 64;
@@ -65,9 +65,9 @@ constexpr int kOffP = kOffQ + 2 * kSmallBytes;        // 2 buffers of P^T
 constexpr int kOffRed = kOffP + 2 * kSmallBytes;      // [2][4][16] fp32
 constexpr int kOffLsum = kOffRed + 2 * 4 * kN * 4;    // [4][16] fp32
 constexpr int kOffBars = kOffLsum + 4 * kN * 4;
-// k_full[3] k_empty[3] v_full[3] v_empty[3] q_full[2] q_empty[2] s_full[2]
-// s_free[2] p_full[2] p_free[2] o_done o_free rbar mma_done
-constexpr int kNumBars = 3 * 4 + 2 * 6 + 4;
+// k_full[2] k_empty[2] v_full[4] v_empty[4] q_full[2] q_empty[2] s_full[2]
+// s_free[2] p_full[2] pv_done[2] o_free rbar mma_done
+constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 * 6 + 3;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
 constexpr int kOffLens = kOffMisc + 64;
 constexpr int kSmemBytes = kOffLens + kMaxSmemSeqs * 4 + 1024;
@@ -164,19 +164,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBars);
   uint64_t* k_full = bars;
-  uint64_t* k_empty = bars + 3;
-  uint64_t* v_full = bars + 6;
-  uint64_t* v_empty = bars + 9;
-  uint64_t* q_full = bars + 12;
-  uint64_t* q_empty = bars + 14;
-  uint64_t* s_full = bars + 16;
-  uint64_t* s_free = bars + 18;
-  uint64_t* p_full = bars + 20;
-  uint64_t* p_free = bars + 22;
-  uint64_t* o_done = bars + 24;
-  uint64_t* o_free = bars + 25;
-  uint64_t* rbar = bars + 26;
-  uint64_t* mma_done = bars + 27;
+  uint64_t* k_empty = k_full + kKStages;
+  uint64_t* v_full = k_empty + kKStages;
+  uint64_t* v_empty = v_full + kVStages;
+  uint64_t* q_full = v_empty + kVStages;
+  uint64_t* q_empty = q_full + 2;
+  uint64_t* s_full = q_empty + 2;
+  uint64_t* s_free = s_full + 2;
+  uint64_t* p_full = s_free + 2;
+  // pv_done[b]: one phase per P V group that read P^T buffer b (tiles of
+  // parity b).  Waiters are never more than one phase behind on either.
+  uint64_t* pv_done = p_full + 2;
+  uint64_t* o_free = pv_done + 2;
+  uint64_t* rbar = o_free + 1;
+  uint64_t* mma_done = rbar + 1;
   Misc* misc = reinterpret_cast<Misc*>(smem + kOffMisc);
   int* s_len = reinterpret_cast<int*>(smem + kOffLens);
   float* red = reinterpret_cast<float*>(smem + kOffRed);
@@ -228,9 +229,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- set-up: barriers, zeroed Q^T / P^T buffers, TMEM ----
   if (tid == 0) {
-    for (int s = 0; s < 3; ++s) {
+    for (int s = 0; s < kKStages; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
     }
@@ -240,9 +243,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s_full[s], 1);
       mbar_init(&s_free[s], 4);
       mbar_init(&p_full[s], 4);
-      mbar_init(&p_free[s], 1);
+      mbar_init(&pv_done[s], 1);
     }
-    mbar_init(o_done, 1);
     mbar_init(o_free, 4);
     mbar_init(rbar, 4);
     mbar_init(mma_done, 1);
@@ -277,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&qmap);
     }
     Walk bw = w0;
-    int n = 0, seg = -1;
+    int n = 0, seg = -1, k_extra = 0;
     bool ok = true;
     while (n < nloc && ok) {
       const int cnt = min(32, nloc - n);
@@ -308,64 +310,69 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int g = __shfl_sync(0xffffffffu, mw.g, c);
         const int ci = __shfl_sync(0xffffffffu, mw.i, c);
         const int64_t cq = __shfl_sync(0xffffffffu, qrow, c);
-        int cid[8];
+        // Lane j (< 8) issues block j's boxes itself: one warp-wide TMA
+        // instruction then moves eight boxes (a single lane issuing all 32
+        // boxes of a tile was measured at ~55 ns per box).
+        int myid = -1;
+        uint32_t nvalid = 0;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) cid[j] = __shfl_sync(0xffffffffu, ids[j], c);
-        if (lane == 0) {
-          uint32_t nvalid = 0;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) nvalid += cid[j] >= 0 ? 1u : 0u;
-          if (ci == 0 || n == 0) {
-            ++seg;
-            const int qs = seg & 1;
-            ok = mbar_wait(&q_empty[qs], ((seg >> 1) & 1) ^ 1, abort_flag);
-            if (ok) {
-              mbar_arrive_expect_tx(&q_full[qs], 2 * G * 128);
-              uint8_t* qdst = smem + kOffQ + qs * kSmallBytes;
-              tma_load_3d(qdst, &qmap, 0, g * G, static_cast<int32_t>(cq), &q_full[qs]);
-              tma_load_3d(qdst + kSmallHalf, &qmap, 64, g * G, static_cast<int32_t>(cq),
-                          &q_full[qs]);
-            }
-          }
-          const int ks = n % kKStages;
-          ok = ok && mbar_wait(&k_empty[ks], ((n / kKStages) & 1) ^ 1, abort_flag);
+        for (int j = 0; j < 8; ++j) {
+          const int v = __shfl_sync(0xffffffffu, ids[j], c);
+          if (lane == j) myid = v;
+          nvalid += v >= 0 ? 1u : 0u;
+        }
+        const int32_t y = (myid * Hkv + g) * kBlockSize;
+        if (lane == 0 && (ci == 0 || n == 0)) {
+          ++seg;
+          const int qs = seg & 1;
+          ok = mbar_wait(&q_empty[qs], ((seg >> 1) & 1) ^ 1, abort_flag);
           if (ok) {
-            mbar_arrive_expect_tx(&k_full[ks], nvalid * 2 * kBlockSize * 128);
-            uint8_t* kdst = smem + kOffK + ks * kTileBytes;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              if (cid[j] < 0) continue;
-              const int32_t y = (cid[j] * Hkv + g) * kBlockSize;
-              tma_load_2d(kdst + j * kBlockSize * 128, &kmap, 0, y, &k_full[ks]);
-              tma_load_2d(kdst + kHalfBytes + j * kBlockSize * 128, &kmap, 64, y, &k_full[ks]);
-            }
-          }
-          const int vs = n % kVStages;
-          ok = ok && mbar_wait(&v_empty[vs], ((n / kVStages) & 1) ^ 1, abort_flag);
-          if (ok) {
-            mbar_arrive_expect_tx(&v_full[vs], nvalid * 2 * kBlockSize * 128);
-            uint8_t* vdst = smem + kOffV + vs * kTileBytes;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              if (cid[j] < 0) continue;
-              const int32_t y = (cid[j] * Hkv + g) * kBlockSize;
-              tma_load_2d(vdst + j * kBlockSize * 128, &vmap, 0, y, &v_full[vs]);
-              tma_load_2d(vdst + kHalfBytes + j * kBlockSize * 128, &vmap, 64, y, &v_full[vs]);
-            }
+            mbar_arrive_expect_tx(&q_full[qs], 2 * G * 128);
+            uint8_t* qdst = smem + kOffQ + qs * kSmallBytes;
+            tma_load_3d(qdst, &qmap, 0, g * G, static_cast<int32_t>(cq), &q_full[qs]);
+            tma_load_3d(qdst + kSmallHalf, &qmap, 64, g * G, static_cast<int32_t>(cq),
+                        &q_full[qs]);
           }
         }
+        const int ks = n % kKStages;
+        if (lane == 0 && ok) {
+          ok = mbar_wait(&k_empty[ks], ((n / kKStages) & 1) ^ 1, abort_flag);
+          if (ok) mbar_arrive_expect_tx(&k_full[ks], nvalid * 2 * kBlockSize * 128);
+        }
         ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (ok) ++n;
+        if (!ok) break;
+        if (lane < 8 && myid >= 0) {
+          uint8_t* kdst = smem + kOffK + ks * kTileBytes + lane * kBlockSize * 128;
+          tma_load_2d(kdst, &kmap, 0, y, &k_full[ks]);
+          tma_load_2d(kdst + kHalfBytes, &kmap, 64, y, &k_full[ks]);
+        }
+        const int vs = n % kVStages;
+        if (lane == 0) {
+          ok = mbar_wait(&v_empty[vs], ((n / kVStages) & 1) ^ 1, abort_flag);
+          if (ok) mbar_arrive_expect_tx(&v_full[vs], nvalid * 2 * kBlockSize * 128);
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) {
+          k_extra = 1;  // K(n) is in flight without V(n): the drain waits for it
+          break;
+        }
+        if (lane < 8 && myid >= 0) {
+          uint8_t* vdst = smem + kOffV + vs * kTileBytes + lane * kBlockSize * 128;
+          tma_load_2d(vdst, &vmap, 0, y, &v_full[vs]);
+          tma_load_2d(vdst + kHalfBytes, &vmap, 64, y, &v_full[vs]);
+        }
+        ++n;
       }
       bw = shfl_walk_helper(mw, cnt - 1);
       walk_next(bw, a, s_len);
     }
     // Drain: the most recent K, V and Q copies land before the CTA exits.
     if (lane == 0) {
-      for (int j = n - 1; j >= 0 && j >= n - 3; --j) {
+      const int nk = n + k_extra;
+      for (int j = nk - 1; j >= 0 && j >= nk - kKStages; --j)
         mbar_wait_drain(&k_full[j % kKStages], (j / kKStages) & 1);
+      for (int j = n - 1; j >= 0 && j >= n - kVStages; --j)
         mbar_wait_drain(&v_full[j % kVStages], (j / kVStages) & 1);
-      }
       for (int s = seg; s >= 0 && s >= seg - 1; --s) mbar_wait_drain(&q_full[s & 1], (s >> 1) & 1);
       if (*abort_flag) set_err(a.err_word, QATTN_DEVERR_TIMEOUT);
     }
@@ -396,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t bd = sdesc_sw128(sp + (k >> 2) * kSmallHalf + (k & 3) * 32, 16, 1024);
           mma_bf16_ss(tmem + kColO, ad, bd, idesc_pv, (first_of_seg && k == 0) ? 0u : 1u);
         }
-        mma_commit(o_done);
+        mma_commit(&pv_done[pb]);
         mma_commit(&v_empty[j % kVStages]);
       };
       for (int n = 0; n < nloc && ok; ++n, walk_next(mw, a, s_len)) {
@@ -438,17 +445,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     float m_used[G], l_t[G];
     int rphase = 0;
-    // o_done completes one phase per P V MMA group.  A parity wait is only
-    // sound while the waiter is at most one phase behind, so every tile n
-    // waits for PV(n-1) (and a unit's last tile for PV(n)); o_seen counts
-    // the groups already observed so no phase is waited for twice.
-    int o_seen = 0;
+    // PV(j) completes phase j >> 1 of pv_done[j & 1].  Tile n always waits
+    // for PV(n-2) (P^T buffer reuse), so when it later waits for PV(n-1)
+    // (rescale) or PV(n) (end of unit) neither barrier is two phases behind
+    // -- the condition a parity wait needs.
     auto wait_pv = [&](int j) -> bool {
-      while (o_seen <= j) {
-        if (!__all_sync(0xffffffffu, mbar_wait(o_done, o_seen & 1, abort_flag))) return false;
-        ++o_seen;
-      }
-      return true;
+      return __all_sync(0xffffffffu, mbar_wait(&pv_done[j & 1], (j >> 1) & 1, abort_flag));
     };
     bool ok = true;
     Walk sw = w0;
@@ -494,13 +496,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       ++rphase;
-      // PV(n-1) done: O^T may be rescaled and P^T buffer pb (last read by
-      // PV(n-2)) may be rewritten.
-      if (n > 0 && !wait_pv(n - 1)) {
+      // P^T buffer pb was last read by PV(n-2).
+      if (n >= 2 && !wait_pv(n - 2)) {
         ok = false;
         break;
       }
-      tc_fence_after();
       float alpha[G];
       bool any_rescale = false;
 #pragma unroll
@@ -517,7 +517,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (any_rescale) {
-        // O^T holds the unit's tiles so far (PV(n-1) is done): scale row t.
+        // O^T holds the unit's tiles so far: wait for PV(n-1), scale row t.
+        if (!wait_pv(n - 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
         float o[kN];
         tmem_ld16(lane_addr + kColO, o);
 #pragma unroll
