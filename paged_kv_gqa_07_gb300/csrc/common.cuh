@@ -35,6 +35,23 @@ __device__ __forceinline__ void set_err(int32_t* err_word, int32_t bits) {
   if (err_word != nullptr) atomicOr(err_word, bits);
 }
 
+// ------------------------------------------------- dependent launches ----
+//
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while the previous kernel on the stream is still
+// running, once that kernel has executed launch_dependents (or exited).
+// Everything a kernel reads that the previous kernel may write must come
+// after grid_dep_wait(), which returns once the previous grid has finished
+// and its memory is visible.
+
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------ mbarrier ----
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

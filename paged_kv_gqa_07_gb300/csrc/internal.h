@@ -7,9 +7,54 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/qattn.h"
 
 namespace qattn {
+
+// Launch with programmatic stream serialization (see grid_dep_wait).
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// How a decode kernel cuts its list of T work units (chunks or tiles) into
+// contiguous runs, one per CTA of a grid of P CTAs.  With T >= min_run * P
+// the runs are balanced: CTA k owns [floor(k T / P), floor((k+1) T / P)),
+// every run at least min_run long.  Otherwise runs are exactly min_run long
+// and only the first ceil(T / min_run) CTAs work.  Either way a unit of n
+// consecutive work items touches at most ceil(n / min_run) + 1 runs.
+struct RunSplit {
+  int total;    // T
+  int ctas;     // P
+  int min_run;  // minimum run length
+  __host__ __device__ bool balanced() const {
+    return static_cast<long long>(total) >= static_cast<long long>(min_run) * ctas;
+  }
+  __host__ __device__ int begin(int k) const {
+    if (balanced()) return static_cast<int>(static_cast<long long>(k) * total / ctas);
+    const long long b = static_cast<long long>(k) * min_run;
+    return b < total ? static_cast<int>(b) : total;
+  }
+  // The CTA whose run holds work item u (0 <= u < total).
+  __host__ __device__ int cta_of(int u) const {
+    if (balanced())
+      return static_cast<int>((static_cast<long long>(u + 1) * ctas - 1) / total);
+    return u / min_run;
+  }
+};
 
 // ---- rope + cache append (rope_append.cu) ----
 struct RopeAppendArgs {
@@ -41,7 +86,9 @@ constexpr int kChunkTokens = 32;
 constexpr int kMinChunksPerCta = 8;
 
 struct DecodeWorkspace {
-  int32_t* cum;    // [num_seqs] chunk-space offset of each sequence (+ header)
+  int32_t* cum;    // [num_seqs] work-list offset of each sequence, then a
+                   // header: [num_seqs] = total, [num_seqs + 1] = grid size,
+                   // [num_seqs + 2] = minimum run
   float* lse;      // [num_seqs * Hkv * max_parts * group]
   float* part_o;   // [num_seqs * Hkv * max_parts * group * 128]
   int32_t max_parts;
@@ -79,6 +126,52 @@ constexpr int kTcMinTilesPerCta = 2;
 cudaError_t launch_paged_decode_tc(const DecodeArgs& a, const CUtensorMap& kmap,
                                    const CUtensorMap& vmap, const CUtensorMap& qmap,
                                    int num_sms, cudaStream_t stream);
+#ifdef __CUDACC__
+// Context length of decode sequence b if it is valid for a decode kernel
+// (one query row; 1 <= L <= max_context_len; within the block table), else 0.
+__device__ __forceinline__ int decode_len_eff(const DecodeArgs& a, int b) {
+  const int L = a.context_lens[b];
+  if (a.cu_seqlens_q != nullptr) {
+    if (a.cu_seqlens_q[b + 1] - a.cu_seqlens_q[b] != 1) return 0;
+  }
+  if (L < 1 || L > a.max_context_len || L > a.max_blocks_per_seq * 16) return 0;
+  return L;
+}
+
+// Called by one full warp of CTA 0 of a decode kernel: waits for the
+// previous grid, then writes the work-list offset of every sequence (units
+// of `unit_tokens` tokens, one list entry per (sequence, kv head, unit)) and
+// the run-split header [total, grid size, minimum run] the merge kernel
+// reads.  s_len: the kernel's shared copy of decode_len_eff per sequence, or
+// null when the batch did not fit in it.
+__device__ __forceinline__ void write_unit_offsets(const DecodeArgs& a, const int* s_len,
+                                                   int total, int unit_tokens, int min_run) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int lane = threadIdx.x & 31;
+  int run = 0;
+  for (int base = 0; base < a.num_seqs; base += 32) {
+    const int b = base + lane;
+    int u = 0;
+    if (b < a.num_seqs) {
+      const int L = s_len != nullptr ? s_len[b] : decode_len_eff(a, b);
+      u = a.num_kv_heads * ((L + unit_tokens - 1) / unit_tokens);
+    }
+    int incl = u;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += n;
+    }
+    if (b < a.num_seqs) a.ws.cum[b] = run + incl - u;
+    run += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (lane == 0) {
+    a.ws.cum[a.num_seqs] = total;
+    a.ws.cum[a.num_seqs + 1] = static_cast<int>(gridDim.x);
+    a.ws.cum[a.num_seqs + 2] = min_run;
+  }
+}
+#endif
 // K2r for either decode kernel (reads a.tile_tokens).
 cudaError_t launch_decode_merge(const DecodeArgs& a, cudaStream_t stream);
 

@@ -208,10 +208,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   int total;
   block_scan(local, misc->warp_sums, &total);
-  const int C = max(kMinChunksPerCta, (total + static_cast<int>(gridDim.x) - 1) /
-                                          static_cast<int>(gridDim.x));
-  const int c0 = static_cast<int>(blockIdx.x) * C;
-  const int c1 = min(total, c0 + C);
+  const RunSplit split{total, static_cast<int>(gridDim.x), kMinChunksPerCta};
+  const int c0 = split.begin(blockIdx.x);
+  const int c1 = split.begin(blockIdx.x + 1);
   int running = 0;
   for (int base = 0; base < B; base += kThreads) {
     const int b = base + tid;
@@ -220,15 +219,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     int tile_total;
     const int incl = block_scan(u, misc->warp_sums, &tile_total);
     const int excl = running + incl - u;
-    if (blockIdx.x == 0 && b < B) a.ws.cum[b] = excl;
     if (u > 0 && excl <= c0 && c0 < excl + u) {
       misc->b0 = b;
       misc->off0 = c0 - excl;
     }
     running += tile_total;
   }
-  if (blockIdx.x == 0 && tid == 0) a.ws.cum[B] = C;
   __syncthreads();
+  // The merge kernel may launch now; it waits for this grid to finish.
+  grid_dep_launch();
   if (c0 >= c1) return;  // no work for this CTA (nothing issued yet)
   const int nloc = c1 - c0;
 
@@ -266,6 +265,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     int64_t qrow;
     int cnt = min(32, nloc);
     prepare(w0, cnt, mw, id0, id1, qrow, 0);
+    // Queries and the cache may come from the previous kernel on the stream
+    // (the RoPE + append step): nothing of theirs is read before this.
+    grid_dep_wait();
     while (n < nloc && ok) {
       // next batch, issued ahead
       const int n_next = n + cnt;
@@ -368,6 +370,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Online-softmax state of this warp for the current unit: running max m
   // (log2 domain), this lane's share of the sum l, and the output of this
   // lane's 4 dimensions kept as (even-token, odd-token) partial pairs.
+  if (blockIdx.x == 0 && warp == 0)
+    write_unit_offsets(a, B <= kMaxSmemSeqs ? s_len : nullptr, total, kChunkTokens,
+                       kMinChunksPerCta);
+
   float m[G], l[G];
   float2 acc[G][4];
   Walk cw = w0;
@@ -533,7 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++cphase;
       const int gidx = c0 + n;
       const int u0 = gidx - cw.i;  // list index of this unit's first chunk
-      const int first = u0 / C, last = (u0 + cw.nch - 1) / C;
+      const int first = split.cta_of(u0), last = split.cta_of(u0 + cw.nch - 1);
       const int nparts = last - first + 1;
       const int part = static_cast<int>(blockIdx.x) - first;
       const int64_t row = q_row_of(a, cw.b);
@@ -581,6 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // (sequence, kv head); thread (h, d4) owns 4 dimensions of query head h.
 template <int G>
 __global__ void __launch_bounds__(G * 32) decode_merge_kernel(const DecodeArgs a) {
+  grid_dep_wait();  // the partials come from the decode grid
   const int Hkv = a.num_kv_heads;
   const int b = blockIdx.x / Hkv, g = blockIdx.x % Hkv;
   const int h = threadIdx.x >> 5, d4 = threadIdx.x & 31;
@@ -603,9 +610,10 @@ __global__ void __launch_bounds__(G * 32) decode_merge_kernel(const DecodeArgs a
     if (g == 0 && threadIdx.x == 0) set_err(a.err_word, QATTN_DEVERR_CONTEXT);
     return;
   }
-  const int C = a.ws.cum[a.num_seqs];
+  const RunSplit split{a.ws.cum[a.num_seqs], a.ws.cum[a.num_seqs + 1],
+                       a.ws.cum[a.num_seqs + 2]};
   const int u0 = a.ws.cum[b] + g * nch;
-  const int first = u0 / C, last = (u0 + nch - 1) / C;
+  const int first = split.cta_of(u0), last = split.cta_of(u0 + nch - 1);
   const int nparts = last - first + 1;
   if (nparts == 1) return;
   if (nparts > a.ws.max_parts) {
@@ -646,15 +654,20 @@ cudaError_t launch_g(const DecodeArgs& a, const CUtensorMap& kmap, const CUtenso
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  paged_decode_kernel<G><<<num_sms, kThreads, kSmemBytes, stream>>>(kmap, vmap, a);
-  cudaError_t e = cudaPeekAtLastError();
+  cudaError_t e =
+      launch_pdl(paged_decode_kernel<G>, dim3(num_sms), dim3(kThreads), kSmemBytes, stream, kmap,
+                 vmap, a);
+  if (e != cudaSuccess) return e;
+  e = cudaPeekAtLastError();
   if (e != cudaSuccess) return e;
   return launch_decode_merge(a, stream);
 }
 
 template <int G>
 cudaError_t launch_merge_g(const DecodeArgs& a, cudaStream_t stream) {
-  decode_merge_kernel<G><<<a.num_seqs * a.num_kv_heads, G * 32, 0, stream>>>(a);
+  cudaError_t e = launch_pdl(decode_merge_kernel<G>, dim3(a.num_seqs * a.num_kv_heads),
+                             dim3(G * 32), 0, stream, a);
+  if (e != cudaSuccess) return e;
   return cudaPeekAtLastError();
 }
 
@@ -666,7 +679,7 @@ size_t decode_workspace_bytes(int32_t num_seqs, int32_t max_context_len, int32_t
   const int64_t max_parts = (nch + kMinChunksPerCta - 1) / kMinChunksPerCta + 1;
   auto al = [](int64_t x) { return (x + 255) / 256 * 256; };
   const int64_t units = static_cast<int64_t>(num_seqs) * num_kv_heads * max_parts * group;
-  return static_cast<size_t>(al((num_seqs + 1) * 4) + al(units * 4) + al(units * kHeadDim * 4));
+  return static_cast<size_t>(al((num_seqs + 3) * 4) + al(units * 4) + al(units * kHeadDim * 4));
 }
 
 DecodeWorkspace carve_decode_workspace(void* base, int32_t num_seqs, int32_t max_context_len,
@@ -678,7 +691,7 @@ DecodeWorkspace carve_decode_workspace(void* base, int32_t num_seqs, int32_t max
   uint8_t* p = static_cast<uint8_t*>(base);
   DecodeWorkspace w;
   w.cum = reinterpret_cast<int32_t*>(p);
-  p += al((num_seqs + 1) * 4);
+  p += al((num_seqs + 3) * 4);
   w.lse = reinterpret_cast<float*>(p);
   p += al(units * 4);
   w.part_o = reinterpret_cast<float*>(p);

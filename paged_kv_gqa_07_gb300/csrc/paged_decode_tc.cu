@@ -49,8 +49,8 @@ constexpr int kMmaWarp = 5;
 constexpr int kThreads = 6 * 32;
 constexpr int kHalfBytes = kTile * 128;  // 128 rows x 128 B (one d-half of a tile)
 constexpr int kTileBytes = 2 * kHalfBytes;
-constexpr int kKStages = 2;
-constexpr int kVStages = 4;
+constexpr int kKStages = 3;
+constexpr int kVStages = 3;
 constexpr int kSmallHalf = kN * 128;     // 16 rows x 128 B
 constexpr int kSmallBytes = 2 * kSmallHalf;
 constexpr uint32_t kTmemCols = 64;
@@ -203,10 +203,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   int total;
   block_scan(local, misc->warp_sums, &total);
-  const int C = max(kTcMinTilesPerCta, (total + static_cast<int>(gridDim.x) - 1) /
-                                           static_cast<int>(gridDim.x));
-  const int c0 = static_cast<int>(blockIdx.x) * C;
-  const int c1 = min(total, c0 + C);
+  const RunSplit split{total, static_cast<int>(gridDim.x), kTcMinTilesPerCta};
+  const int c0 = split.begin(blockIdx.x);
+  const int c1 = split.begin(blockIdx.x + 1);
   int running = 0;
   for (int base = 0; base < B; base += kThreads) {
     const int b = base + tid;
@@ -215,15 +214,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     int tile_total;
     const int incl = block_scan(u, misc->warp_sums, &tile_total);
     const int excl = running + incl - u;
-    if (blockIdx.x == 0 && b < B) a.ws.cum[b] = excl;
     if (u > 0 && excl <= c0 && c0 < excl + u) {
       misc->b0 = b;
       misc->off0 = c0 - excl;
     }
     running += tile_total;
   }
-  if (blockIdx.x == 0 && tid == 0) a.ws.cum[B] = C;
   __syncthreads();
+  // The merge kernel may launch now; it waits for this grid to finish.
+  grid_dep_launch();
   if (c0 >= c1) return;  // nothing for this CTA: no barrier, copy or TMEM in use yet
   const int nloc = c1 - c0;
 
@@ -281,6 +280,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     Walk bw = w0;
     int n = 0, seg = -1, k_extra = 0;
     bool ok = true;
+    // Queries and the cache may come from the previous kernel on the stream
+    // (the RoPE + append step): nothing of theirs is read before this.
+    grid_dep_wait();
     while (n < nloc && ok) {
       const int cnt = min(32, nloc - n);
       Walk mw = bw;
@@ -441,6 +443,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // =============================== softmax ================================
+    if (blockIdx.x == 0 && warp == 0)
+      write_unit_offsets(a, B <= kMaxSmemSeqs ? s_len : nullptr, total, kTile,
+                         kTcMinTilesPerCta);
     const int t = tid;  // token row of S^T / dimension row of O^T = TMEM lane
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     float m_used[G], l_t[G];
@@ -603,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         const int gidx = c0 + n;
         const int u0 = gidx - sw.i;
-        const int first = u0 / C, last = (u0 + sw.nt - 1) / C;
+        const int first = split.cta_of(u0), last = split.cta_of(u0 + sw.nt - 1);
         const int nparts = last - first + 1;
         const int part = static_cast<int>(blockIdx.x) - first;
         const int64_t row = q_row_of(a, sw.b);
@@ -644,8 +649,10 @@ cudaError_t launch_tc_g(const DecodeArgs& a, const CUtensorMap& kmap, const CUte
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  paged_decode_tc_kernel<G><<<num_sms, kThreads, kSmemBytes, stream>>>(kmap, vmap, qmap, a);
-  cudaError_t e = cudaPeekAtLastError();
+  cudaError_t e = launch_pdl(paged_decode_tc_kernel<G>, dim3(num_sms), dim3(kThreads),
+                             kSmemBytes, stream, kmap, vmap, qmap, a);
+  if (e != cudaSuccess) return e;
+  e = cudaPeekAtLastError();
   if (e != cudaSuccess) return e;
   return launch_decode_merge(a, stream);
 }

@@ -49,6 +49,9 @@ __device__ __forceinline__ void rotate8(const uint4& x1, const uint4& x2, const 
 
 __global__ void __launch_bounds__(kThreads) rope_append_kernel(RopeAppendArgs a,
                                                                int tasks_per_token) {
+  // A following decode kernel may start its set-up now; it reads nothing
+  // this kernel writes before its own grid_dep_wait().
+  grid_dep_launch();
   const int64_t gid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
   const int64_t t = gid / tasks_per_token;
   if (t >= a.num_tokens) return;
