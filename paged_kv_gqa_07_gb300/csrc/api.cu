@@ -71,20 +71,29 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// The paged cache [num_blocks][Hkv][16][128] bf16 seen as a 2-D tensor of
-// num_blocks * Hkv * 16 rows by 128 columns; a box is 16 rows x 64 columns
-// (128 bytes, the widest a 128-byte swizzle allows), so one (block, kv head)
-// tile is two boxes at x = 0 and x = 64.
+// The paged cache [num_blocks][Hkv][16][128] bf16 seen as a 4-D tensor
+// (64 columns, 8 rows, 2 column halves, num_blocks * Hkv * 2 row groups):
+// element (c, r, h, m) is row 8m + r, column 64h + c of the 2-D
+// [num_blocks * Hkv * 16][128] view.  A box of (64, 8, 2, 2) is one whole
+// (block, kv head) tile -- 4 KB in one copy -- and lands in shared memory as
+// [row group][column half][8 rows][128 B] with the 128-byte swizzle: each
+// 8-row x 128-byte atom sits on its own 1 KB, the two halves of a row group
+// 1 KB apart and consecutive row groups 2 KB apart, which is the K-major
+// (and, for V, MN-major) operand layout the tensor-core kernels describe
+// with an 8-row-group stride of 2 KB, and what the CUDA-core kernel
+// addresses directly.
 bool encode_cache_map(CUtensorMap* map, const void* cache, int32_t num_blocks,
                       int32_t num_kv_heads) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim),
-                              static_cast<cuuint64_t>(num_blocks) * num_kv_heads * kBlockSize};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDim) * 2};
-  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kBlockSize)};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(cache), dims, strides,
+  const cuuint64_t dims[4] = {64, 8, 2,
+                              static_cast<cuuint64_t>(num_blocks) * num_kv_heads * 2};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(kHeadDim) * 2,  // next row
+                                 128,                                     // next half
+                                 static_cast<cuuint64_t>(kHeadDim) * 2 * 8};  // next group
+  const cuuint32_t box[4] = {64, 8, 2, 2};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(cache), dims, strides,
             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -164,7 +173,7 @@ int check_cache(const void* k_cache, const void* v_cache, int32_t num_blocks,
                 const qattn_dims& d) {
   if (k_cache == nullptr || v_cache == nullptr || num_blocks <= 0) return QATTN_ERR_INVALID_ARG;
   if (!aligned16(k_cache) || !aligned16(v_cache)) return QATTN_ERR_INVALID_ARG;
-  // TMA row coordinates are 32-bit.
+  // TMA coordinates are 32-bit.
   if (static_cast<int64_t>(num_blocks) * d.num_kv_heads * kBlockSize >= (1ll << 31))
     return QATTN_ERR_UNSUPPORTED;
   return QATTN_OK;

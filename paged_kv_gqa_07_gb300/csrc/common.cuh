@@ -151,6 +151,15 @@ __device__ __forceinline__ void tma_load_2d_hint(void* smem_dst, const CUtensorM
       : "memory");
 }
 
+// Asks the TMA unit to bring one box of a 2-D tensor into L2 (no shared
+// memory, no completion signal).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
 // Contiguous bulk copy global -> shared (16-byte aligned, size % 16 == 0).
 __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes,
                                           uint64_t* bar) {
@@ -352,6 +361,26 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) 
       "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
       "r"(__float_as_uint(v[15]))
       : "memory");
+}
+
+// One (block, kv head) tile of the paged cache (4-D view, see the cache
+// tensor map): `tile` = block id * num_kv_heads + kv head.
+__device__ __forceinline__ void tma_load_cache_tile(void* smem_dst, const CUtensorMap* map,
+                                                    int32_t tile, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(0), "r"(0), "r"(tile * 2),
+      "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Byte offset, inside a cache tile in shared memory, of 16-byte chunk
+// `chunk` (0..15 along the 128 dims) of row `r` (0..15): the layout is
+// [row group][column half][8 rows][128 B], 128-byte swizzled.
+__device__ __forceinline__ uint32_t tile_chunk_offset(int r, int chunk) {
+  return static_cast<uint32_t>((r >> 3) * 2048 + (chunk >> 3) * 1024 + (r & 7) * 128 +
+                               (((chunk & 7) ^ (r & 7)) << 4));
 }
 
 // 3-D tiled load of one box into shared memory, completing on `bar`.

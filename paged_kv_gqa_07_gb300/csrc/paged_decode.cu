@@ -272,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // next batch, issued ahead
       const int n_next = n + cnt;
       const int cnt2 = min(32, nloc - n_next);
-      Walk mw2;
+      Walk mw2 = mw;
       int id0b = -1, id1b = -1;
       int64_t qrowb = 0;
       if (cnt2 > 0) {
@@ -324,16 +324,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
-        // Lanes 0..7 each issue one 16 x 64 box: lane = block j (bit 2),
-        // K or V (bit 1), column half (bit 0) -- one warp-wide instruction.
-        if (lane < 8) {
-          const int j = lane >> 2, isv = (lane >> 1) & 1, half = lane & 1;
+        // Lanes 0..3 each copy one whole 4 KB (block, kv head) tile: lane =
+        // block j (bit 1), K or V (bit 0) -- one warp-wide instruction.
+        if (lane < 4) {
+          const int j = lane >> 1, isv = lane & 1;
           const int id = j ? cid1 : cid0;
           if (id >= 0) {
-            const int32_t y = (id * Hkv + g) * kBlockSize;
-            uint8_t* dst = smem + kOffStages + stage * kStageBytes + isv * kKBytes +
-                           j * kTileBytes + half * kBoxBytes;
-            tma_load_2d(dst, isv ? &vmap : &kmap, half * 64, y, &full[stage]);
+            uint8_t* dst = smem + kOffStages + stage * kStageBytes + isv * kKBytes + j * kTileBytes;
+            tma_load_cache_tile(dst, isv ? &vmap : &kmap, id * Hkv + g, &full[stage]);
           }
         }
         ++n;
@@ -427,11 +425,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int h = 0; h < G; ++h) s2[h] = make_float2(0.f, 0.f);
       {
         const int r = lane & 15;
-        const uint32_t rowbase = sK + (lane >> 4) * kTileBytes + r * 128;
+        const uint32_t rowbase = sK + (lane >> 4) * kTileBytes;
 #pragma unroll 4
         for (int c = 0; c < 16; ++c) {
-          const uint32_t addr =
-              rowbase + (c >> 3) * kBoxBytes + ((((c & 7) ^ (r & 7))) << 4);
+          const uint32_t addr = rowbase + tile_chunk_offset(r, c);
           const uint4 kv = lds128(addr);
           const float2 k01 = make_float2(bf16lo_to_f32(kv.x), bf16hi_to_f32(kv.x));
           const float2 k23 = make_float2(bf16lo_to_f32(kv.y), bf16hi_to_f32(kv.y));
@@ -468,9 +465,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Rows past the end of the context hold stale or never-written
         // data; zero this lane's slice of them so 0 * garbage stays 0.
         for (int j = ntok; j < kChunkTokens; ++j) {
-          const int r = j & 15;
-          const uint32_t addr = sV + (j >> 4) * kTileBytes + (lane >> 4) * kBoxBytes + r * 128 +
-                                (((((lane & 15) >> 1) ^ (r & 7))) << 4) + (lane & 1) * 8;
+          const uint32_t addr = sV + (j >> 4) * kTileBytes +
+                                tile_chunk_offset(j & 15, lane >> 1) + (lane & 1) * 8;
           asm volatile("st.shared.v2.u32 [%0], {%1, %1};" ::"r"(addr), "r"(0u) : "memory");
         }
       }
@@ -483,8 +479,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[h][e] = __fmul2_rn(acc[h][e], a2);
       }
-      const uint32_t vlane = sV + (lane >> 4) * kBoxBytes + (lane & 1) * 8;
-      const int vchunk = (lane & 15) >> 1;
+      // This lane's 4 dims are 16-byte chunk lane/2 of a row, bytes (lane&1)*8..
+      const int vchunk = lane >> 1;
+      const uint32_t vlane = sV + (lane & 1) * 8;
 #pragma unroll 2
       for (int j4 = 0; j4 < 8; ++j4) {
         float4 p4[G];
@@ -495,8 +492,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int j = j4 * 4 + pr * 2;  // tokens j, j + 1 (same block: j is even)
           const int r0 = j & 15, r1 = r0 + 1;
           const uint32_t vb = vlane + (j >> 4) * kTileBytes;
-          const uint2 v0 = lds64(vb + r0 * 128 + ((vchunk ^ (r0 & 7)) << 4));
-          const uint2 v1 = lds64(vb + r1 * 128 + ((vchunk ^ (r1 & 7)) << 4));
+          const uint2 v0 = lds64(vb + tile_chunk_offset(r0, vchunk));
+          const uint2 v1 = lds64(vb + tile_chunk_offset(r1, vchunk));
           const float2 d0 = make_float2(bf16lo_to_f32(v0.x), bf16lo_to_f32(v1.x));
           const float2 d1 = make_float2(bf16hi_to_f32(v0.x), bf16hi_to_f32(v1.x));
           const float2 d2 = make_float2(bf16lo_to_f32(v0.y), bf16lo_to_f32(v1.y));

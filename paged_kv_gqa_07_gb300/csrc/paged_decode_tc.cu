@@ -47,8 +47,8 @@ constexpr int kN = 16;                // MMA N: the query group padded to 16 hea
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr int kThreads = 6 * 32;
-constexpr int kHalfBytes = kTile * 128;  // 128 rows x 128 B (one d-half of a tile)
-constexpr int kTileBytes = 2 * kHalfBytes;
+constexpr int kCacheTileBytes = kBlockSize * kHeadDim * 2;  // one (block, kv head): 4 KB
+constexpr int kTileBytes = (kTile / kBlockSize) * kCacheTileBytes;  // 8 blocks: 32 KB
 constexpr int kKStages = 3;
 constexpr int kVStages = 3;
 constexpr int kSmallHalf = kN * 128;     // 16 rows x 128 B
@@ -323,7 +323,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == j) myid = v;
           nvalid += v >= 0 ? 1u : 0u;
         }
-        const int32_t y = (myid * Hkv + g) * kBlockSize;
         if (lane == 0 && (ci == 0 || n == 0)) {
           ++seg;
           const int qs = seg & 1;
@@ -344,9 +343,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         if (lane < 8 && myid >= 0) {
-          uint8_t* kdst = smem + kOffK + ks * kTileBytes + lane * kBlockSize * 128;
-          tma_load_2d(kdst, &kmap, 0, y, &k_full[ks]);
-          tma_load_2d(kdst + kHalfBytes, &kmap, 64, y, &k_full[ks]);
+          tma_load_cache_tile(smem + kOffK + ks * kTileBytes + lane * kCacheTileBytes, &kmap,
+                              myid * Hkv + g, &k_full[ks]);
         }
         const int vs = n % kVStages;
         if (lane == 0) {
@@ -359,9 +357,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         if (lane < 8 && myid >= 0) {
-          uint8_t* vdst = smem + kOffV + vs * kTileBytes + lane * kBlockSize * 128;
-          tma_load_2d(vdst, &vmap, 0, y, &v_full[vs]);
-          tma_load_2d(vdst + kHalfBytes, &vmap, 64, y, &v_full[vs]);
+          tma_load_cache_tile(smem + kOffV + vs * kTileBytes + lane * kCacheTileBytes, &vmap,
+                              myid * Hkv + g, &v_full[vs]);
         }
         ++n;
       }
@@ -401,7 +398,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sp = sbase + kOffP + pb * kSmallBytes;
 #pragma unroll
         for (int k = 0; k < kTile / 16; ++k) {
-          const uint64_t ad = sdesc_sw128(sv + k * (16 * 128), kHalfBytes, 1024);
+          // V tile as the MN-major A: the two 64-dim halves 1 KB apart (LBO),
+          // 8-token groups 2 KB apart (SBO); K step k = tokens 16k..16k+15.
+          const uint64_t ad = sdesc_sw128(sv + k * 4096, 1024, 2048);
           const uint64_t bd = sdesc_sw128(sp + (k >> 2) * kSmallHalf + (k & 3) * 32, 16, 1024);
           mma_bf16_ss(tmem + kColO, ad, bd, idesc_pv, (first_of_seg && k == 0) ? 0u : 1u);
         }
@@ -424,7 +423,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sq = sbase + kOffQ + (seg & 1) * kSmallBytes;
 #pragma unroll
         for (int k = 0; k < kHeadDim / 16; ++k) {
-          const uint64_t ad = sdesc_sw128(sk + (k >> 2) * kHalfBytes + (k & 3) * 32, 16, 1024);
+          // K tile as the K-major A: dim half k/4 at +1 KB, 8-token groups 2 KB apart.
+          const uint64_t ad = sdesc_sw128(sk + (k >> 2) * 1024 + (k & 3) * 32, 16, 2048);
           const uint64_t bd = sdesc_sw128(sq + (k >> 2) * kSmallHalf + (k & 3) * 32, 16, 1024);
           mma_bf16_ss(tmem + sb * kN, ad, bd, idesc_qk, k > 0 ? 1u : 0u);
         }
@@ -564,12 +564,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (nvalid_tok < kTile) {
         // V rows of tokens past the context: zero them before P V reads them.
         if (!valid) {
-          const uint32_t vrow = sbase + kOffV + (n % kVStages) * kTileBytes + t * 128;
+          const uint32_t vtile = sbase + kOffV + (n % kVStages) * kTileBytes +
+                                 (t >> 4) * kCacheTileBytes;
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            sts128(vrow + c * 16, 0u, 0u, 0u, 0u);
-            sts128(vrow + kHalfBytes + c * 16, 0u, 0u, 0u, 0u);
-          }
+          for (int c = 0; c < 16; ++c) sts128(vtile + tile_chunk_offset(t & 15, c), 0u, 0u, 0u, 0u);
         }
       }
       fence_proxy_async_smem();

@@ -45,8 +45,9 @@ constexpr int kN = 128;                 // keys per KV tile
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr int kThreads = 6 * 32;
-constexpr int kHalfBytes = 128 * 128;   // 128 rows x 128 B
+constexpr int kHalfBytes = 128 * 128;   // 128 rows x 128 B (Q and P: [half][row])
 constexpr int kTileBytes = 2 * kHalfBytes;
+constexpr int kCacheTileBytes = kBlockSize * kHeadDim * 2;  // one (block, kv head): 4 KB
 constexpr int kStages = 2;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 256;
@@ -168,21 +169,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = mbar_wait(&kv_empty[st], ((kt >> 1) & 1) ^ 1, abort_flag);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
-      const int32_t y = (id * a.num_kv_heads + g) * kBlockSize;
-      uint8_t* kdst = smem + kOffK + st * kTileBytes + lane * (kBlockSize * 128);
-      uint8_t* vdst = smem + kOffV + st * kTileBytes + lane * (kBlockSize * 128);
+      uint8_t* kdst = smem + kOffK + st * kTileBytes + lane * kCacheTileBytes;
+      uint8_t* vdst = smem + kOffV + st * kTileBytes + lane * kCacheTileBytes;
       if (lane == 0) mbar_arrive_expect_tx(&k_full[st], nvalid * 2 * kBlockSize * 128);
       __syncwarp();
       if (id >= 0) {
-        tma_load_2d(kdst, &kmap, 0, y, &k_full[st]);
-        tma_load_2d(kdst + kHalfBytes, &kmap, 64, y, &k_full[st]);
+        tma_load_cache_tile(kdst, &kmap, id * a.num_kv_heads + g, &k_full[st]);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive_expect_tx(&v_full[st], nvalid * 2 * kBlockSize * 128);
       __syncwarp();
       if (id >= 0) {
-        tma_load_2d(vdst, &vmap, 0, y, &v_full[st]);
-        tma_load_2d(vdst + kHalfBytes, &vmap, 64, y, &v_full[st]);
+        tma_load_cache_tile(vdst, &vmap, id * a.num_kv_heads + g, &v_full[st]);
       }
       ++issued;
     }
@@ -211,7 +209,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int k = 0; k < kN / 16; ++k) {
           const uint64_t ad = sdesc_sw128(sp + (k >> 2) * kHalfBytes + (k & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(sv + k * (16 * 128), kHalfBytes, 1024);
+          // V tile as the MN-major B: dim halves 1 KB apart (LBO), 8-key
+          // groups 2 KB apart (SBO); K step k = keys 16k..16k+15.
+          const uint64_t bd = sdesc_sw128(sv + k * 4096, 1024, 2048);
           mma_bf16_ss(tmem + kColO, ad, bd, idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
         }
         mma_commit(o_done);
@@ -227,7 +227,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int k = 0; k < kHeadDim / 16; ++k) {
           const uint64_t ad = sdesc_sw128(sq + (k >> 2) * kHalfBytes + (k & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(sk + (k >> 2) * kHalfBytes + (k & 3) * 32, 16, 1024);
+          // K tile as the K-major B: dim half k/4 at +1 KB, 8-key groups 2 KB apart.
+          const uint64_t bd = sdesc_sw128(sk + (k >> 2) * 1024 + (k & 3) * 32, 16, 2048);
           mma_bf16_ss(tmem + st * kN, ad, bd, idesc_qk, k > 0 ? 1u : 0u);
         }
         mma_commit(&s_full[st]);
@@ -333,12 +334,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         if (kbase + r >= L) {
-          const uint32_t vrow = sbase + kOffV + sb * kTileBytes + r * 128;
+          const uint32_t vtile = sbase + kOffV + sb * kTileBytes + (r >> 4) * kCacheTileBytes;
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            sts128(vrow + c * 16, 0u, 0u, 0u, 0u);
-            sts128(vrow + kHalfBytes + c * 16, 0u, 0u, 0u, 0u);
-          }
+          for (int c = 0; c < 16; ++c) sts128(vtile + tile_chunk_offset(r & 15, c), 0u, 0u, 0u, 0u);
         }
       }
       fence_proxy_async_smem();
