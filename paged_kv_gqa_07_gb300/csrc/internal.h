@@ -127,6 +127,23 @@ cudaError_t launch_paged_decode_tc(const DecodeArgs& a, const CUtensorMap& kmap,
                                    const CUtensorMap& vmap, const CUtensorMap& qmap,
                                    int num_sms, cudaStream_t stream);
 #ifdef __CUDACC__
+// Every CTA of a decode kernel touches the context lengths (planning) and,
+// right after, a slice of the block tables it cannot know in advance.
+// Prefetching both whole arrays into L2 at entry turns the second of those
+// two dependent DRAM round trips into an L2 hit.  (Inputs only: these are
+// never written by the previous kernel on the stream.)
+__device__ __forceinline__ void prefetch_decode_metadata(const DecodeArgs& a) {
+  const char* bt = reinterpret_cast<const char*>(a.block_tables);
+  const int64_t bt_bytes = static_cast<int64_t>(a.num_seqs) * a.max_blocks_per_seq * 4;
+  for (int64_t off = static_cast<int64_t>(threadIdx.x) * 128; off < bt_bytes;
+       off += static_cast<int64_t>(blockDim.x) * 128)
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(bt + off));
+  const char* cl = reinterpret_cast<const char*>(a.context_lens);
+  for (int64_t off = static_cast<int64_t>(threadIdx.x) * 128; off < a.num_seqs * 4LL;
+       off += static_cast<int64_t>(blockDim.x) * 128)
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(cl + off));
+}
+
 // Context length of decode sequence b if it is valid for a decode kernel
 // (one query row; 1 <= L <= max_context_len; within the block table), else 0.
 __device__ __forceinline__ int decode_len_eff(const DecodeArgs& a, int b) {

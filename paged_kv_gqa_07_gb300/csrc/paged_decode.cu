@@ -199,6 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&vmap);
   }
 
+  prefetch_decode_metadata(a);
   // ---- plan: total chunk count, this CTA's run [c0, c1), its first unit ----
   int local = 0;
   for (int b = tid; b < B; b += kThreads) {

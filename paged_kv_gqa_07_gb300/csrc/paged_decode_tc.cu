@@ -189,6 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int Hkv = a.num_kv_heads;
   const int B = a.num_seqs;
 
+  prefetch_decode_metadata(a);
   // ---- plan: tile count, this CTA's run [c0, c1), its first unit ----
   if (tid == 0) {
     misc->abort = 0;
@@ -278,8 +279,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&qmap);
     }
     Walk bw = w0;
-    int n = 0, seg = -1, k_extra = 0;
+    // V of a tile is issued one tile after its K (order K0 K1 V0 K2 V1 ...):
+    // V lands about when P V needs it instead of idling in its ring slot
+    // while the softmax runs, and at start-up the first K tiles are served
+    // ahead of the V burst.
+    int n = 0, seg = -1, nv = 0;
+    int prev_id = -1, prev_g = 0;
+    uint32_t prev_nvalid = 0;
     bool ok = true;
+    auto issue_v = [&](int j, int id_lane, int gg, uint32_t nval) -> bool {
+      const int vs = j % kVStages;
+      bool okv = true;
+      if (lane == 0) {
+        okv = mbar_wait(&v_empty[vs], ((j / kVStages) & 1) ^ 1, abort_flag);
+        if (okv) mbar_arrive_expect_tx(&v_full[vs], nval * 2 * kBlockSize * 128);
+      }
+      okv = __shfl_sync(0xffffffffu, okv, 0);
+      if (!okv) return false;
+      if (lane < 8 && id_lane >= 0)
+        tma_load_cache_tile(smem + kOffV + vs * kTileBytes + lane * kCacheTileBytes, &vmap,
+                            id_lane * Hkv + gg, &v_full[vs]);
+      ++nv;
+      return true;
+    };
     // Queries and the cache may come from the previous kernel on the stream
     // (the RoPE + append step): nothing of theirs is read before this.
     grid_dep_wait();
@@ -346,31 +368,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_cache_tile(smem + kOffK + ks * kTileBytes + lane * kCacheTileBytes, &kmap,
                               myid * Hkv + g, &k_full[ks]);
         }
-        const int vs = n % kVStages;
-        if (lane == 0) {
-          ok = mbar_wait(&v_empty[vs], ((n / kVStages) & 1) ^ 1, abort_flag);
-          if (ok) mbar_arrive_expect_tx(&v_full[vs], nvalid * 2 * kBlockSize * 128);
-        }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) {
-          k_extra = 1;  // K(n) is in flight without V(n): the drain waits for it
+        ++n;  // K(n) issued
+        if (n >= 2 && !issue_v(n - 2, prev_id, prev_g, prev_nvalid)) {
+          ok = false;
           break;
         }
-        if (lane < 8 && myid >= 0) {
-          tma_load_cache_tile(smem + kOffV + vs * kTileBytes + lane * kCacheTileBytes, &vmap,
-                              myid * Hkv + g, &v_full[vs]);
-        }
-        ++n;
+        prev_id = myid;
+        prev_g = g;
+        prev_nvalid = nvalid;
       }
       bw = shfl_walk_helper(mw, cnt - 1);
       walk_next(bw, a, s_len);
     }
+    if (ok && n > 0 && nv < n) issue_v(n - 1, prev_id, prev_g, prev_nvalid);
     // Drain: the most recent K, V and Q copies land before the CTA exits.
     if (lane == 0) {
-      const int nk = n + k_extra;
+      const int nk = n;
       for (int j = nk - 1; j >= 0 && j >= nk - kKStages; --j)
         mbar_wait_drain(&k_full[j % kKStages], (j / kKStages) & 1);
-      for (int j = n - 1; j >= 0 && j >= n - kVStages; --j)
+      for (int j = nv - 1; j >= 0 && j >= nv - kVStages; --j)
         mbar_wait_drain(&v_full[j % kVStages], (j / kVStages) & 1);
       for (int s = seg; s >= 0 && s >= seg - 1; --s) mbar_wait_drain(&q_full[s & 1], (s >> 1) & 1);
       if (*abort_flag) set_err(a.err_word, QATTN_DEVERR_TIMEOUT);
@@ -381,61 +397,89 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(kTile, kN, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(kHeadDim, kN, false, true);
+      // QK and PV are each issued in tile order, but whichever is ready goes
+      // first: PV(j) as soon as P(j) and V(j) are in (it frees V's ring
+      // slot, the resource the producer waits on longest), QK(n) as soon as
+      // K(n) is in and S buffer n & 1 is free.  Readiness is probed without
+      // blocking; waiting on one condition while the other is ready used to
+      // hold V slots for a K load.
       bool ok = true;
-      Walk mw = w0;
-      int seg = -1;
-      int prev_first = 0;   // tile n-1 opened its unit (PV starts a fresh accumulator)
-      int prev_seg = -1;    // segment index of tile n-1
-      auto issue_pv = [&](int j, bool first_of_seg, int seg_of_j) {
-        const int pb = j & 1;
-        ok = ok && mbar_wait(&p_full[pb], (j >> 1) & 1, abort_flag);
-        ok = ok && mbar_wait(&v_full[j % kVStages], (j / kVStages) & 1, abort_flag);
-        if (ok && first_of_seg && seg_of_j > 0)
-          ok = mbar_wait(o_free, (seg_of_j - 1) & 1, abort_flag);
-        if (!ok) return;
-        tc_fence_after();
-        const uint32_t sv = sbase + kOffV + (j % kVStages) * kTileBytes;
-        const uint32_t sp = sbase + kOffP + pb * kSmallBytes;
+      Walk qw = w0, pw = w0;
+      int qn = 0, pn = 0, qseg = -1, pseg = -1;
+      uint64_t idle_since = 0;
+      while (pn < nloc && ok) {
+        bool progressed = false;
+        if (pn < qn) {
+          const bool first = (pn == 0) || (pw.i == 0);
+          const int seg_j = pseg + (first ? 1 : 0);
+          const int pb = pn & 1;
+          bool ready = mbar_test(&p_full[pb], (pn >> 1) & 1) &&
+                       mbar_test(&v_full[pn % kVStages], (pn / kVStages) & 1);
+          if (ready && first && seg_j > 0) ready = mbar_test(o_free, (seg_j - 1) & 1);
+          if (ready) {
+            tc_fence_after();
+            const uint32_t sv = sbase + kOffV + (pn % kVStages) * kTileBytes;
+            const uint32_t sp = sbase + kOffP + pb * kSmallBytes;
 #pragma unroll
-        for (int k = 0; k < kTile / 16; ++k) {
-          // V tile as the MN-major A: the two 64-dim halves 1 KB apart (LBO),
-          // 8-token groups 2 KB apart (SBO); K step k = tokens 16k..16k+15.
-          const uint64_t ad = sdesc_sw128(sv + k * 4096, 1024, 2048);
-          const uint64_t bd = sdesc_sw128(sp + (k >> 2) * kSmallHalf + (k & 3) * 32, 16, 1024);
-          mma_bf16_ss(tmem + kColO, ad, bd, idesc_pv, (first_of_seg && k == 0) ? 0u : 1u);
+            for (int k = 0; k < kTile / 16; ++k) {
+              // V tile as the MN-major A: the two 64-dim halves 1 KB apart
+              // (LBO), 8-token groups 2 KB apart (SBO); K step k = tokens
+              // 16k..16k+15.
+              const uint64_t ad = sdesc_sw128(sv + k * 4096, 1024, 2048);
+              const uint64_t bd =
+                  sdesc_sw128(sp + (k >> 2) * kSmallHalf + (k & 3) * 32, 16, 1024);
+              mma_bf16_ss(tmem + kColO, ad, bd, idesc_pv, (first && k == 0) ? 0u : 1u);
+            }
+            mma_commit(&pv_done[pb]);
+            mma_commit(&v_empty[pn % kVStages]);
+            if (first) pseg = seg_j;
+            ++pn;
+            walk_next(pw, a, s_len);
+            progressed = true;
+          }
         }
-        mma_commit(&pv_done[pb]);
-        mma_commit(&v_empty[j % kVStages]);
-      };
-      for (int n = 0; n < nloc && ok; ++n, walk_next(mw, a, s_len)) {
-        const bool seg_start = (n == 0) || (mw.i == 0);
-        const bool seg_end = (n == nloc - 1) || (mw.i == mw.nt - 1);
-        if (seg_start) {
-          ++seg;
-          ok = mbar_wait(&q_full[seg & 1], (seg >> 1) & 1, abort_flag);
-        }
-        const int ks = n % kKStages, sb = n & 1;
-        ok = ok && mbar_wait(&k_full[ks], (n / kKStages) & 1, abort_flag);
-        if (ok && n >= 2) ok = mbar_wait(&s_free[sb], ((n >> 1) & 1) ^ 1, abort_flag);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t sk = sbase + kOffK + ks * kTileBytes;
-        const uint32_t sq = sbase + kOffQ + (seg & 1) * kSmallBytes;
+        if (qn < nloc) {
+          const bool first = (qn == 0) || (qw.i == 0);
+          const bool last = (qn == nloc - 1) || (qw.i == qw.nt - 1);
+          const int seg_q = qseg + (first ? 1 : 0);
+          const int ks = qn % kKStages, sb = qn & 1;
+          bool ready = mbar_test(&k_full[ks], (qn / kKStages) & 1);
+          if (ready && qn >= 2) ready = mbar_test(&s_free[sb], ((qn >> 1) & 1) ^ 1);
+          if (ready && first) ready = mbar_test(&q_full[seg_q & 1], (seg_q >> 1) & 1);
+          if (ready) {
+            tc_fence_after();
+            const uint32_t sk = sbase + kOffK + ks * kTileBytes;
+            const uint32_t sq = sbase + kOffQ + (seg_q & 1) * kSmallBytes;
 #pragma unroll
-        for (int k = 0; k < kHeadDim / 16; ++k) {
-          // K tile as the K-major A: dim half k/4 at +1 KB, 8-token groups 2 KB apart.
-          const uint64_t ad = sdesc_sw128(sk + (k >> 2) * 1024 + (k & 3) * 32, 16, 2048);
-          const uint64_t bd = sdesc_sw128(sq + (k >> 2) * kSmallHalf + (k & 3) * 32, 16, 1024);
-          mma_bf16_ss(tmem + sb * kN, ad, bd, idesc_qk, k > 0 ? 1u : 0u);
+            for (int k = 0; k < kHeadDim / 16; ++k) {
+              // K tile as the K-major A: dim half k/4 at +1 KB, 8-token groups
+              // 2 KB apart.
+              const uint64_t ad = sdesc_sw128(sk + (k >> 2) * 1024 + (k & 3) * 32, 16, 2048);
+              const uint64_t bd =
+                  sdesc_sw128(sq + (k >> 2) * kSmallHalf + (k & 3) * 32, 16, 1024);
+              mma_bf16_ss(tmem + sb * kN, ad, bd, idesc_qk, k > 0 ? 1u : 0u);
+            }
+            mma_commit(&s_full[sb]);
+            mma_commit(&k_empty[ks]);
+            if (last) mma_commit(&q_empty[seg_q & 1]);
+            if (first) qseg = seg_q;
+            ++qn;
+            walk_next(qw, a, s_len);
+            progressed = true;
+          }
         }
-        mma_commit(&s_full[sb]);
-        mma_commit(&k_empty[ks]);
-        if (seg_end) mma_commit(&q_empty[seg & 1]);
-        if (n > 0) issue_pv(n - 1, prev_first != 0, prev_seg);
-        prev_first = seg_start ? 1 : 0;
-        prev_seg = seg;
+        if (progressed) {
+          idle_since = 0;
+        } else {
+          const uint64_t now = globaltimer_ns();
+          if (idle_since == 0) {
+            idle_since = now;
+          } else if (*abort_flag || now - idle_since > kWaitTimeoutNs) {
+            *abort_flag = 1;
+            ok = false;
+          }
+        }
       }
-      if (ok && nloc > 0) issue_pv(nloc - 1, prev_first != 0, prev_seg);
       // Drain: every MMA issued above completes before TMEM is released.
       mma_commit(mma_done);
       mbar_wait_drain(mma_done, 0);
@@ -554,15 +598,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(bits) : "memory");
         }
       }
-      // V(n) must have landed before its tail rows are zeroed.  The wait is
-      // made on every tile so this slot's phases are observed in order.
-      if (!__all_sync(0xffffffffu,
-                      mbar_wait(&v_full[n % kVStages], (n / kVStages) & 1, abort_flag))) {
-        ok = false;
-        break;
-      }
       if (nvalid_tok < kTile) {
-        // V rows of tokens past the context: zero them before P V reads them.
+        // V rows of tokens past the context: zero them before P V reads
+        // them, once V(n) has landed.  (PV(n-2) is done, hence V(n-3) landed:
+        // this slot's barrier is at most one phase behind.)
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(&v_full[n % kVStages], (n / kVStages) & 1, abort_flag))) {
+          ok = false;
+          break;
+        }
         if (!valid) {
           const uint32_t vtile = sbase + kOffV + (n % kVStages) * kTileBytes +
                                  (t >> 4) * kCacheTileBytes;
