@@ -304,9 +304,13 @@ def run_ours(args, dist: Dist):
     if decode:
         alg = kv_bytes + qo_bytes
         achieved = alg / attn_avg_s / 1e9
-        sha = kernel_source_sha(["paged_decode.cu", "common.cuh"])
-        traffic = profiled_traffic("paged_decode_kernel", args.workload, sha)
-        result["roofline"] = {"bound": "hbm", "kernel": "paged_decode_kernel (+ decode_merge_kernel)",
+        if Q.qattn_paged_decode_kernel(dims) == Q.QATTN_DECODE_TENSOR_CORE:
+            kname, src = "paged_decode_tc_kernel", "paged_decode_tc.cu"
+        else:
+            kname, src = "paged_decode_kernel", "paged_decode.cu"
+        sha = kernel_source_sha([src, "common.cuh", "internal.h"])
+        traffic = profiled_traffic(kname, args.workload, sha)
+        result["roofline"] = {"bound": "hbm", "kernel": kname,
                               "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                               "frac": round(achieved / hbm_peak, 4), "peak_kind": peak_kind,
                               "traffic": traffic, "algorithmic_bytes_per_launch": alg}
@@ -346,6 +350,8 @@ def run_ours(args, dist: Dist):
         "tokens_per_s": round(tokens_per_s, 1),
         "append_ms": round(statistics.mean(app_ms), 5),
         "attention_ms": round(statistics.mean(attn_ms), 5),
+        # per step: RoPE + append, the decode kernel and its merge kernel
+        # (and, with prefill rows, the prefill kernel)
         "gpu_launches": 3 * args.steps if decode else 4 * args.steps,
         **result,
     }

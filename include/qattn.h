@@ -130,10 +130,23 @@ int qattn_rope_cache_append(void* q, int64_t q_row_stride, const void* k,
 
 /* Bytes of device workspace qattn_paged_decode needs (256-byte aligned
  * pointer, contents need not be initialised).  Depends only on the
- * arguments. */
+ * arguments.  The workspace holds the split-KV partial results between the
+ * decode kernel and the merge kernel of one call; two calls whose kernels
+ * can overlap on the GPU must not share a workspace. */
 size_t qattn_paged_decode_workspace_size(int32_t num_seqs,
                                          int32_t max_context_len,
                                          qattn_dims dims);
+
+/* Which kernel qattn_paged_decode (and the decode rows of
+ * qattn_varlen_prefill) launches for these dims: QATTN_DECODE_CUDA_CORE
+ * (groups of 1-2 query heads per KV head: the group's dot products on CUDA
+ * cores) or QATTN_DECODE_TENSOR_CORE (groups of 3-8: tcgen05 with the group
+ * as the MMA N dimension).  The environment variable QATTN_DECODE_KERNEL
+ * ("cuda" or "tc"), read once per process, overrides the choice where the
+ * kernel supports the group.  Returns -1 for invalid dims. */
+#define QATTN_DECODE_CUDA_CORE 0
+#define QATTN_DECODE_TENSOR_CORE 1
+int qattn_paged_decode_kernel(qattn_dims dims);
 
 /* Step 3, decode: one query row per sequence.
  *   out          [num_seqs, num_heads, head_dim] bf16, contiguous;

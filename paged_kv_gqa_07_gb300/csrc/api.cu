@@ -258,6 +258,12 @@ int qattn_rope_cache_append(void* q, int64_t q_row_stride, const void* k, int64_
   return cuda_status(launch_rope_append(a, static_cast<cudaStream_t>(stream)));
 }
 
+int qattn_paged_decode_kernel(qattn_dims dims) {
+  if (check_dims(dims) != QATTN_OK) return -1;
+  return use_tc_decode(dims.num_heads / dims.num_kv_heads) ? QATTN_DECODE_TENSOR_CORE
+                                                            : QATTN_DECODE_CUDA_CORE;
+}
+
 size_t qattn_paged_decode_workspace_size(int32_t num_seqs, int32_t max_context_len,
                                          qattn_dims dims) {
   if (check_dims(dims) != QATTN_OK || num_seqs < 0 || max_context_len < 0) return 0;
@@ -301,10 +307,8 @@ int decode_common(void* out, const void* q, int64_t q_row_stride, int32_t q_rows
     CUtensorMap qmap;
     if (!encode_q_group_map(&qmap, q, q_row_stride, q_rows, dims.num_heads, group))
       return QATTN_ERR_CUDA;
-    a.tile_tokens = kTcTileTokens;
     return cuda_status(launch_paged_decode_tc(a, kmap, vmap, qmap, num_sms, stream));
   }
-  a.tile_tokens = kChunkTokens;
   return cuda_status(launch_paged_decode(a, kmap, vmap, num_sms, stream));
 }
 

@@ -86,11 +86,10 @@ constexpr int kChunkTokens = 32;
 constexpr int kMinChunksPerCta = 8;
 
 struct DecodeWorkspace {
-  int32_t* cum;    // [num_seqs] work-list offset of each sequence, then a
-                   // header: [num_seqs] = total, [num_seqs + 1] = grid size,
-                   // [num_seqs + 2] = minimum run
-  float* lse;      // [num_seqs * Hkv * max_parts * group]
-  float* part_o;   // [num_seqs * Hkv * max_parts * group * 128]
+  int32_t* nparts;  // [num_seqs * Hkv] parts of each (sequence, kv head) unit, written
+                    // by the decode kernel (0: no valid context), read by the merge
+  float* lse;       // [num_seqs * Hkv * max_parts * group] log2-sum-exp of each part
+  float* part_o;    // [num_seqs * Hkv * max_parts * group * 128] normalised O of each part
   int32_t max_parts;
 };
 
@@ -115,7 +114,6 @@ struct DecodeArgs {
   float scale_log2;        // softmax scale * log2(e)
   int32_t* err_word;
   DecodeWorkspace ws;
-  int32_t tile_tokens;     // tokens per work unit of the kernel that ran (merge needs it)
 };
 // CUDA-core decode (K2): 32-token chunks, the GQA group on CUDA cores.
 cudaError_t launch_paged_decode(const DecodeArgs& a, const CUtensorMap& kmap,
@@ -155,41 +153,47 @@ __device__ __forceinline__ int decode_len_eff(const DecodeArgs& a, int b) {
   return L;
 }
 
-// Called by one full warp of CTA 0 of a decode kernel: waits for the
-// previous grid, then writes the work-list offset of every sequence (units
-// of `unit_tokens` tokens, one list entry per (sequence, kv head, unit)) and
-// the run-split header [total, grid size, minimum run] the merge kernel
-// reads.  s_len: the kernel's shared copy of decode_len_eff per sequence, or
-// null when the batch did not fit in it.
-__device__ __forceinline__ void write_unit_offsets(const DecodeArgs& a, const int* s_len,
-                                                   int total, int unit_tokens, int min_run) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int lane = threadIdx.x & 31;
-  int run = 0;
-  for (int base = 0; base < a.num_seqs; base += 32) {
-    const int b = base + lane;
-    int u = 0;
-    if (b < a.num_seqs) {
-      const int L = s_len != nullptr ? s_len[b] : decode_len_eff(a, b);
-      u = a.num_kv_heads * ((L + unit_tokens - 1) / unit_tokens);
+// A unit that straddles CTAs leaves one partial result per CTA (O
+// normalised by its own sum, LSE in log2 units) -- the split-KV scheme of
+// the decode pages -- and the merge kernel K2r combines them.  The CTA that
+// holds a unit's first part records how many parts it has.
+__device__ __forceinline__ void record_parts(const DecodeArgs& a, int64_t seg, int nparts) {
+  a.ws.nparts[seg] = nparts;
+}
+
+// Whole CTA, before any early exit.  Sequences b = blockIdx.x (mod grid):
+// a decode row with no valid context gets a zero output row, no parts and
+// the CONTEXT error bit; an empty varlen sequence (no query rows) gets the
+// bit alone.
+// s_len: the kernel's shared copy of decode_len_eff, or null.  Output is
+// written only after the previous grid on the stream, which may write the
+// same rows, has finished.
+__device__ __forceinline__ void finish_invalid_rows(const DecodeArgs& a, const int* s_len) {
+  for (int b = blockIdx.x; b < a.num_seqs; b += gridDim.x) {
+    int64_t row = b;
+    if (a.cu_seqlens_q != nullptr) {
+      const int ql = a.cu_seqlens_q[b + 1] - a.cu_seqlens_q[b];
+      if (ql != 1) {
+        if (ql < 1 && threadIdx.x == 0) set_err(a.err_word, QATTN_DEVERR_CONTEXT);
+        continue;  // a prefill sequence: the prefill kernel owns it
+      }
+      row = a.cu_seqlens_q[b];
     }
-    int incl = u;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int n = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += n;
-    }
-    if (b < a.num_seqs) a.ws.cum[b] = run + incl - u;
-    run += __shfl_sync(0xffffffffu, incl, 31);
-  }
-  if (lane == 0) {
-    a.ws.cum[a.num_seqs] = total;
-    a.ws.cum[a.num_seqs + 1] = static_cast<int>(gridDim.x);
-    a.ws.cum[a.num_seqs + 2] = min_run;
+    const int L = s_len != nullptr ? s_len[b] : decode_len_eff(a, b);
+    if (L > 0) continue;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    for (int g = threadIdx.x; g < a.num_kv_heads; g += blockDim.x)
+      a.ws.nparts[static_cast<int64_t>(b) * a.num_kv_heads + g] = 0;
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) +
+                                          row * a.num_heads * kHeadDim);
+    for (int i = threadIdx.x; i < a.num_heads * (kHeadDim / 8); i += blockDim.x)
+      dst[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (threadIdx.x == 0) set_err(a.err_word, QATTN_DEVERR_CONTEXT);
   }
 }
 #endif
-// K2r for either decode kernel (reads a.tile_tokens).
+
+// K2r: merge the parts of straddling units (either decode kernel's).
 cudaError_t launch_decode_merge(const DecodeArgs& a, cudaStream_t stream);
 
 // ---- varlen prefill (varlen_prefill.cu) ----

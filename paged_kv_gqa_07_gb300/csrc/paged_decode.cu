@@ -1,4 +1,5 @@
-// Kernels K2 (paged GQA decode) and K2r (split merge).
+// Kernels K2 (paged GQA decode on CUDA cores, the default for groups of one
+// or two query heads per KV head) and K2r (merge of split units).
 //
 // What is computed: for every decode sequence b and query head h, with KV
 // head g = h / G (G = num_heads / num_kv_heads),
@@ -14,15 +15,14 @@
 //     tokens (two 16-token blocks).  All chunks of all units form one
 //     ordered list; a persistent grid of one CTA per SM gives every CTA an
 //     equal contiguous run of the list (at least 8 chunks), so long and short
-//     sequences balance perfectly.  A unit that straddles CTAs is finished
-//     by K2r, which merges the per-CTA partial results (normalised output
-//     plus log2-sum-exp) in a fixed order: results are deterministic.
+//     sequences balance.  A unit that straddles CTAs leaves one partial
+//     result per CTA (normalised output plus log2-sum-exp); K2r merges them
+//     in part order, so results are deterministic.
 //   * One producer warp streams the run through a ring of shared-memory
-//     stages with 2-D TMA loads (a (block, kv head) tile of K or V is 16 rows
-//     x 256 B, loaded as two 128-byte-swizzled 16 x 64 boxes), and bulk-
-//     copies each unit's G query heads.  Eight consumer warps take chunks
-//     round-robin.  Stage hand-off uses mbarriers (full: TMA byte count,
-//     empty: consumer release).
+//     stages with one 4-D TMA per (block, kv head) tile of K or V (16 rows x
+//     256 B, 128-byte swizzle) and copies each unit's G query heads.  Four
+//     consumer warps take chunks round-robin.  Stage hand-off uses
+//     mbarriers (full: TMA byte count, empty: consumer release).
 //   * A consumer warp holds the whole GQA group: QK^T is lane-per-token (lane
 //     j owns token j's 256-byte key row, read conflict-free thanks to the
 //     swizzle, and broadcast-reads the fp32 query heads, pre-scaled by
@@ -84,13 +84,8 @@ __device__ __forceinline__ int seq_len_eff(const DecodeArgs& a, int b) {
   return L;
 }
 
-__device__ __forceinline__ int seq_chunks(const DecodeArgs& a, int b, int* L_out) {
-  const int L = seq_len_eff(a, b);
-  *L_out = L;
-  return (L + kChunkTokens - 1) / kChunkTokens;
-}
-
-// The same, served from the shared-memory copy when the batch fits in it.
+// Chunks of sequence b (and its effective length), served from the
+// shared-memory copy when the batch fits in it.
 __device__ __forceinline__ int seq_chunks_cached(const DecodeArgs& a, const int* s_len, int b,
                                                  int* L_out) {
   const int L = a.num_seqs <= kMaxSmemSeqs ? s_len[b] : seq_len_eff(a, b);
@@ -227,8 +222,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     running += tile_total;
   }
   __syncthreads();
-  // The merge kernel may launch now; it waits for this grid to finish.
+  // The next kernel on the stream may start its own set-up now.
   grid_dep_launch();
+  finish_invalid_rows(a, B <= kMaxSmemSeqs ? s_len : nullptr);
   if (c0 >= c1) return;  // no work for this CTA (nothing issued yet)
   const int nloc = c1 - c0;
 
@@ -369,9 +365,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Online-softmax state of this warp for the current unit: running max m
   // (log2 domain), this lane's share of the sum l, and the output of this
   // lane's 4 dimensions kept as (even-token, odd-token) partial pairs.
-  if (blockIdx.x == 0 && warp == 0)
-    write_unit_offsets(a, B <= kMaxSmemSeqs ? s_len : nullptr, total, kChunkTokens,
-                       kMinChunksPerCta);
 
   float m[G], l[G];
   float2 acc[G][4];
@@ -541,6 +534,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nparts = last - first + 1;
       const int part = static_cast<int>(blockIdx.x) - first;
       const int64_t row = q_row_of(a, cw.b);
+      const int64_t seg_id = static_cast<int64_t>(cw.b) * Hkv + cw.g;
+      const bool fits = nparts <= a.ws.max_parts;
+      if (!fits && tid == 0) set_err(a.err_word, QATTN_DEVERR_CONTEXT);
       for (int idx = tid; idx < G * 32; idx += kConsumerWarps * 32) {
         const int h = idx >> 5, d4 = idx & 31;
         float M = -INFINITY;
@@ -568,78 +564,100 @@ __global__ void __launch_bounds__(kThreads, 1)
           packed.y = pack_bf16x2_rn(res.z, res.w);
           *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) +
                                     (row * a.num_heads + head) * kHeadDim + d4 * 4) = packed;
-        } else if (part >= 0 && part < a.ws.max_parts) {
-          const int64_t pidx =
-              (static_cast<int64_t>(cw.b) * Hkv + cw.g) * a.ws.max_parts + part;
+        } else if (fits) {
+          const int64_t pidx = seg_id * a.ws.max_parts + part;
           *reinterpret_cast<float4*>(a.ws.part_o + (pidx * G + h) * kHeadDim + d4 * 4) = res;
           if (d4 == 0) a.ws.lse[pidx * G + h] = M + log2f(den);
         }
       }
+      if (part == 0 && tid == 0) record_parts(a, seg_id, fits ? nparts : 0);
     }
   }
   if (!ok && lane == 0) set_err(a.err_word, QATTN_DEVERR_TIMEOUT);
 }
 
-// K2r: merge the partial results of units that straddled CTAs, and write
-// zero rows for decode sequences whose context is invalid.  One CTA per
-// (sequence, kv head); thread (h, d4) owns 4 dimensions of query head h.
-template <int G>
-__global__ void __launch_bounds__(G * 32) decode_merge_kernel(const DecodeArgs a) {
-  grid_dep_wait();  // the partials come from the decode grid
+// K2r: merge the parts of units that straddled CTAs (either decode
+// kernel).  One warp per (sequence, kv head) unit; lane = 4 dimensions.
+//   out[row, g*G + h] = sum_p 2^(lse_p - M) o_p / sum_p 2^(lse_p - M),
+// folded in part order with a running maximum M (deterministic); the loads
+// of a batch of NB parts (all heads) are issued together.
+template <int G, int NB>
+__global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a) {
+  grid_dep_wait();  // the parts come from the decode grid
   const int Hkv = a.num_kv_heads;
-  const int b = blockIdx.x / Hkv, g = blockIdx.x % Hkv;
-  const int h = threadIdx.x >> 5, d4 = threadIdx.x & 31;
+  const int64_t seg = static_cast<int64_t>(blockIdx.x) * 4 + (threadIdx.x >> 5);
+  if (seg >= static_cast<int64_t>(a.num_seqs) * Hkv) return;
+  const int b = static_cast<int>(seg / Hkv), g = static_cast<int>(seg % Hkv);
+  const int lane = threadIdx.x & 31;
+  int64_t row = b;
   if (a.cu_seqlens_q != nullptr) {
-    const int ql = a.cu_seqlens_q[b + 1] - a.cu_seqlens_q[b];
-    if (ql < 1) {
-      if (g == 0 && threadIdx.x == 0) set_err(a.err_word, QATTN_DEVERR_CONTEXT);
-      return;
+    row = a.cu_seqlens_q[b];
+    if (a.cu_seqlens_q[b + 1] - row != 1) return;  // not a decode row
+  }
+  const int nparts = a.ws.nparts[seg];
+  if (nparts <= 1) return;
+  const int64_t pbase = seg * a.ws.max_parts * G;
+  const float* lse = a.ws.lse + pbase;
+  const float* po = a.ws.part_o + pbase * kHeadDim + lane * 4;
+  float m[G], den[G];
+  float4 num[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    m[h] = -INFINITY;
+    den[h] = 0.f;
+    num[h] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  for (int p0 = 0; p0 < nparts; p0 += NB) {
+    float lv[NB][G];
+    float4 ov[NB][G];
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        if (p0 + j < nparts) {
+          const int k = (p0 + j) * G + h;
+          lv[j][h] = lse[k];
+          ov[j][h] = *reinterpret_cast<const float4*>(po + static_cast<int64_t>(k) * kHeadDim);
+        }
+      }
     }
-    if (ql != 1) return;  // a prefill sequence: the prefill kernel owns it
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+      if (p0 + j < nparts) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float mn = fmaxf(m[h], lv[j][h]);
+          const float sc = exp2f(m[h] - mn);  // 0 for the first part
+          const float f = exp2f(lv[j][h] - mn);
+          den[h] = fmaf(den[h], sc, f);
+          num[h].x = fmaf(num[h].x, sc, f * ov[j][h].x);
+          num[h].y = fmaf(num[h].y, sc, f * ov[j][h].y);
+          num[h].z = fmaf(num[h].z, sc, f * ov[j][h].z);
+          num[h].w = fmaf(num[h].w, sc, f * ov[j][h].w);
+          m[h] = mn;
+        }
+      }
+    }
   }
-  const int L = seq_len_eff(a, b);
-  const int nch = (L + a.tile_tokens - 1) / a.tile_tokens;
-  const int64_t row = q_row_of(a, b);
-  __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(a.out) +
-                        (row * a.num_heads + static_cast<int64_t>(g) * G + h) * kHeadDim +
-                        d4 * 4;
-  if (nch == 0) {
-    *reinterpret_cast<uint2*>(outp) = make_uint2(0u, 0u);
-    if (g == 0 && threadIdx.x == 0) set_err(a.err_word, QATTN_DEVERR_CONTEXT);
-    return;
+  __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) +
+                        (row * a.num_heads + static_cast<int64_t>(g) * G) * kHeadDim + lane * 4;
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    const float inv = 1.f / den[h];
+    uint2 packed;
+    packed.x = pack_bf16x2_rn(num[h].x * inv, num[h].y * inv);
+    packed.y = pack_bf16x2_rn(num[h].z * inv, num[h].w * inv);
+    *reinterpret_cast<uint2*>(orow + h * kHeadDim) = packed;
   }
-  const RunSplit split{a.ws.cum[a.num_seqs], a.ws.cum[a.num_seqs + 1],
-                       a.ws.cum[a.num_seqs + 2]};
-  const int u0 = a.ws.cum[b] + g * nch;
-  const int first = split.cta_of(u0), last = split.cta_of(u0 + nch - 1);
-  const int nparts = last - first + 1;
-  if (nparts == 1) return;
-  if (nparts > a.ws.max_parts) {
-    if (threadIdx.x == 0) set_err(a.err_word, QATTN_DEVERR_CONTEXT);
-    return;
-  }
-  const int64_t pbase = (static_cast<int64_t>(b) * Hkv + g) * a.ws.max_parts;
-  float M = -INFINITY;
-#pragma unroll 4
-  for (int p = 0; p < nparts; ++p) M = fmaxf(M, a.ws.lse[(pbase + p) * G + h]);
-  float den = 0.f;
-  float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-  for (int p = 0; p < nparts; ++p) {
-    const float f = exp2f(a.ws.lse[(pbase + p) * G + h] - M);
-    const float4 o =
-        *reinterpret_cast<const float4*>(a.ws.part_o + ((pbase + p) * G + h) * kHeadDim + d4 * 4);
-    den += f;
-    num.x = fmaf(f, o.x, num.x);
-    num.y = fmaf(f, o.y, num.y);
-    num.z = fmaf(f, o.z, num.z);
-    num.w = fmaf(f, o.w, num.w);
-  }
-  const float inv = 1.f / den;
-  uint2 packed;
-  packed.x = pack_bf16x2_rn(num.x * inv, num.y * inv);
-  packed.y = pack_bf16x2_rn(num.z * inv, num.w * inv);
-  *reinterpret_cast<uint2*>(outp) = packed;
+}
+
+template <int G>
+cudaError_t launch_merge_g(const DecodeArgs& a, cudaStream_t stream) {
+  const int64_t segs = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads;
+  cudaError_t e = launch_pdl(decode_merge_kernel<G, (G >= 4 ? 2 : 8 / G)>,
+                             dim3(static_cast<unsigned>((segs + 3) / 4)), dim3(128), 0, stream, a);
+  if (e != cudaSuccess) return e;
+  return cudaPeekAtLastError();
 }
 
 template <int G>
@@ -661,14 +679,6 @@ cudaError_t launch_g(const DecodeArgs& a, const CUtensorMap& kmap, const CUtenso
   return launch_decode_merge(a, stream);
 }
 
-template <int G>
-cudaError_t launch_merge_g(const DecodeArgs& a, cudaStream_t stream) {
-  cudaError_t e = launch_pdl(decode_merge_kernel<G>, dim3(a.num_seqs * a.num_kv_heads),
-                             dim3(G * 32), 0, stream, a);
-  if (e != cudaSuccess) return e;
-  return cudaPeekAtLastError();
-}
-
 }  // namespace
 
 size_t decode_workspace_bytes(int32_t num_seqs, int32_t max_context_len, int32_t num_kv_heads,
@@ -677,7 +687,8 @@ size_t decode_workspace_bytes(int32_t num_seqs, int32_t max_context_len, int32_t
   const int64_t max_parts = (nch + kMinChunksPerCta - 1) / kMinChunksPerCta + 1;
   auto al = [](int64_t x) { return (x + 255) / 256 * 256; };
   const int64_t units = static_cast<int64_t>(num_seqs) * num_kv_heads * max_parts * group;
-  return static_cast<size_t>(al((num_seqs + 3) * 4) + al(units * 4) + al(units * kHeadDim * 4));
+  return static_cast<size_t>(al(static_cast<int64_t>(num_seqs) * num_kv_heads * 4) +
+                             al(units * 4) + al(units * kHeadDim * 4));
 }
 
 DecodeWorkspace carve_decode_workspace(void* base, int32_t num_seqs, int32_t max_context_len,
@@ -688,8 +699,8 @@ DecodeWorkspace carve_decode_workspace(void* base, int32_t num_seqs, int32_t max
   const int64_t units = static_cast<int64_t>(num_seqs) * num_kv_heads * max_parts * group;
   uint8_t* p = static_cast<uint8_t*>(base);
   DecodeWorkspace w;
-  w.cum = reinterpret_cast<int32_t*>(p);
-  p += al((num_seqs + 3) * 4);
+  w.nparts = reinterpret_cast<int32_t*>(p);
+  p += al(static_cast<int64_t>(num_seqs) * num_kv_heads * 4);
   w.lse = reinterpret_cast<float*>(p);
   p += al(units * 4);
   w.part_o = reinterpret_cast<float*>(p);

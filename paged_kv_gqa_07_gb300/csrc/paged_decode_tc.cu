@@ -24,7 +24,10 @@
 // Structure (one CTA per SM, persistent):
 //   * work list: (sequence, kv head) units cut into 128-token tiles (eight
 //     16-token blocks); each CTA takes an equal contiguous run of tiles
-//     (>= 2); units that straddle CTAs are merged by K2r as for K2.
+//     (>= 2); a unit that straddles CTAs leaves one partial result per CTA,
+//     merged in part order by K2r (a round trip to memory inside this
+//     kernel costs ~3 us while every SM streams, so the merge waits for the
+//     grid to finish; K2r's CTAs launch early and wait on the grid).
 //   * warp 4 issues TMA: Q^T of a unit (a G x 128 box of the query rows),
 //     K and V tiles (16 x 64 boxes, 128-byte swizzle) into 3-deep K and V
 //     rings; warp 5 (one thread) issues tcgen05.mma and commits; warps 0-3
@@ -54,7 +57,7 @@ constexpr int kVStages = 3;
 constexpr int kSmallHalf = kN * 128;     // 16 rows x 128 B
 constexpr int kSmallBytes = 2 * kSmallHalf;
 constexpr uint32_t kTmemCols = 64;
-constexpr uint32_t kColO = 32;
+constexpr uint32_t kColO = 32;   // O^T of unit u at kColO + (u & 1) * kN
 constexpr float kLazyRescale = 8.0f;
 constexpr int kMaxSmemSeqs = 2048;
 
@@ -63,11 +66,11 @@ constexpr int kOffV = kOffK + kKStages * kTileBytes;
 constexpr int kOffQ = kOffV + kVStages * kTileBytes;  // 2 slots of Q^T
 constexpr int kOffP = kOffQ + 2 * kSmallBytes;        // 2 buffers of P^T
 constexpr int kOffRed = kOffP + 2 * kSmallBytes;      // [2][4][16] fp32
-constexpr int kOffLsum = kOffRed + 2 * 4 * kN * 4;    // [4][16] fp32
-constexpr int kOffBars = kOffLsum + 4 * kN * 4;
+constexpr int kOffLsum = kOffRed + 2 * 4 * kN * 4;    // [2][4][16] fp32
+constexpr int kOffBars = kOffLsum + 2 * 4 * kN * 4;
 // k_full[2] k_empty[2] v_full[4] v_empty[4] q_full[2] q_empty[2] s_full[2]
-// s_free[2] p_full[2] pv_done[2] o_free rbar mma_done
-constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 * 6 + 3;
+// s_free[2] p_full[2] pv_done[2] o_free[2] rbar mma_done
+constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 * 7 + 2;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
 constexpr int kOffLens = kOffMisc + 64;
 constexpr int kSmemBytes = kOffLens + kMaxSmemSeqs * 4 + 1024;
@@ -175,8 +178,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // pv_done[b]: one phase per P V group that read P^T buffer b (tiles of
   // parity b).  Waiters are never more than one phase behind on either.
   uint64_t* pv_done = p_full + 2;
+  // o_free[b]: the softmax has read O^T slot b (units of parity b).
   uint64_t* o_free = pv_done + 2;
-  uint64_t* rbar = o_free + 1;
+  uint64_t* rbar = o_free + 2;
   uint64_t* mma_done = rbar + 1;
   Misc* misc = reinterpret_cast<Misc*>(smem + kOffMisc);
   int* s_len = reinterpret_cast<int*>(smem + kOffLens);
@@ -222,8 +226,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     running += tile_total;
   }
   __syncthreads();
-  // The merge kernel may launch now; it waits for this grid to finish.
+  // The next kernel on the stream may start its own set-up now.
   grid_dep_launch();
+  finish_invalid_rows(a, B <= kMaxSmemSeqs ? s_len : nullptr);
   if (c0 >= c1) return;  // nothing for this CTA: no barrier, copy or TMEM in use yet
   const int nloc = c1 - c0;
 
@@ -245,7 +250,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&p_full[s], 4);
       mbar_init(&pv_done[s], 1);
     }
-    mbar_init(o_free, 4);
+    mbar_init(&o_free[0], 4);
+    mbar_init(&o_free[1], 4);
     mbar_init(rbar, 4);
     mbar_init(mma_done, 1);
     fence_barrier_init();
@@ -415,7 +421,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int pb = pn & 1;
           bool ready = mbar_test(&p_full[pb], (pn >> 1) & 1) &&
                        mbar_test(&v_full[pn % kVStages], (pn / kVStages) & 1);
-          if (ready && first && seg_j > 0) ready = mbar_test(o_free, (seg_j - 1) & 1);
+          // A unit's first P V overwrites O^T slot seg_j & 1, last read
+          // for unit seg_j - 2.
+          if (ready && first && seg_j >= 2)
+            ready = mbar_test(&o_free[seg_j & 1], ((seg_j >> 1) - 1) & 1);
           if (ready) {
             tc_fence_after();
             const uint32_t sv = sbase + kOffV + (pn % kVStages) * kTileBytes;
@@ -428,7 +437,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint64_t ad = sdesc_sw128(sv + k * 4096, 1024, 2048);
               const uint64_t bd =
                   sdesc_sw128(sp + (k >> 2) * kSmallHalf + (k & 3) * 32, 16, 1024);
-              mma_bf16_ss(tmem + kColO, ad, bd, idesc_pv, (first && k == 0) ? 0u : 1u);
+              mma_bf16_ss(tmem + kColO + (seg_j & 1) * kN, ad, bd, idesc_pv,
+                          (first && k == 0) ? 0u : 1u);
             }
             mma_commit(&pv_done[pb]);
             mma_commit(&v_empty[pn % kVStages]);
@@ -487,19 +497,61 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // =============================== softmax ================================
-    if (blockIdx.x == 0 && warp == 0)
-      write_unit_offsets(a, B <= kMaxSmemSeqs ? s_len : nullptr, total, kTile,
-                         kTcMinTilesPerCta);
     const int t = tid;  // token row of S^T / dimension row of O^T = TMEM lane
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     float m_used[G], l_t[G];
+    // A unit's epilogue (its last P V, O^T / l, output or partial) waits on
+    // that P V, so it is deferred by one tile: the next unit's first tile
+    // is scored and its P^T handed over first.  Its row sums travel with
+    // that tile's max exchange; its O^T stays in its own TMEM slot.
+    float m_pend[G], l_pend[G];
+    bool pend = false;
+    int pend_seg = 0;
+    Walk pend_w = w0;
     int rphase = 0;
     // PV(j) completes phase j >> 1 of pv_done[j & 1].  Tile n always waits
     // for PV(n-2) (P^T buffer reuse), so when it later waits for PV(n-1)
-    // (rescale) or PV(n) (end of unit) neither barrier is two phases behind
-    // -- the condition a parity wait needs.
+    // (rescale, deferred epilogue) or PV(n) (last tile) neither barrier is
+    // two phases behind -- the condition a parity wait needs.
     auto wait_pv = [&](int j) -> bool {
       return __all_sync(0xffffffffu, mbar_wait(&pv_done[j & 1], (j >> 1) & 1, abort_flag));
+    };
+    // Epilogue of unit `useg` whose last tile here is j (walk state uw):
+    // out = O^T / l, or this CTA's part of a unit that straddles CTAs.
+    auto finish = [&](const Walk& uw, int j, int useg, const float* mu,
+                      const float* ltot) -> bool {
+      if (!wait_pv(j)) return false;
+      tc_fence_after();
+      float o[kN];
+      tmem_ld16(lane_addr + kColO + (useg & 1) * kN, o);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&o_free[useg & 1]);
+      const int u0 = c0 + j - uw.i;  // list index of the unit's first tile
+      const int first = split.cta_of(u0), last = split.cta_of(u0 + uw.nt - 1);
+      const int nparts = last - first + 1;
+      const int part = static_cast<int>(blockIdx.x) - first;
+      const int64_t row = q_row_of(a, uw.b);
+      const int64_t seg_id = static_cast<int64_t>(uw.b) * Hkv + uw.g;
+      if (nparts == 1) {
+        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) +
+                              (row * a.num_heads + static_cast<int64_t>(uw.g) * G) * kHeadDim;
+#pragma unroll
+        for (int h = 0; h < G; ++h) orow[h * kHeadDim + t] = __float2bfloat16_rn(o[h] / ltot[h]);
+      } else if (nparts <= a.ws.max_parts) {
+        const int64_t pidx = seg_id * a.ws.max_parts + part;
+#pragma unroll
+        for (int h = 0; h < G; ++h) a.ws.part_o[(pidx * G + h) * kHeadDim + t] = o[h] / ltot[h];
+        if (t < G) {
+#pragma unroll
+          for (int h = 0; h < G; ++h)
+            if (h == t) a.ws.lse[pidx * G + h] = mu[h] + log2f(ltot[h]);
+        }
+      } else if (t == 0) {
+        set_err(a.err_word, QATTN_DEVERR_CONTEXT);
+      }
+      if (part == 0 && t == 0) record_parts(a, seg_id, nparts <= a.ws.max_parts ? nparts : 0);
+      return true;
     };
     bool ok = true;
     Walk sw = w0;
@@ -530,13 +582,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_free[sb]);
 
-      // per-head max over the tile's tokens: shuffle tree, then 4 warps
+      // per-head max over the tile's tokens: shuffle tree, then 4 warps; the
+      // deferred unit's row sums ride along.
       float* rd = red + (n & 1) * 4 * kN;
+      float* ls = lsum + (n & 1) * 4 * kN;
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         s[h] = valid ? s[h] * a.scale_log2 : -INFINITY;
         const float wm = warp_max(s[h]);
         if (lane == 0) rd[warp * kN + h] = wm;
+      }
+      if (pend) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float ws = warp_sum(l_pend[h]);
+          if (lane == 0) ls[warp * kN + h] = ws;
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(rbar);
@@ -573,10 +634,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         float o[kN];
-        tmem_ld16(lane_addr + kColO, o);
+        tmem_ld16(lane_addr + kColO + (seg & 1) * kN, o);
 #pragma unroll
         for (int h = 0; h < G; ++h) o[h] *= alpha[h];
-        tmem_st16(lane_addr + kColO, o);
+        tmem_st16(lane_addr + kColO + (seg & 1) * kN, o);
 #pragma unroll
         for (int h = 0; h < G; ++h) l_t[h] *= alpha[h];
       }
@@ -619,12 +680,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[pb]);
 
-      if (seg_end) {
-        // ---- unit done in this CTA: total l per head, O^T / l ----
+      if (pend) {
+        // the previous unit ended at tile n-1
+        float ltot[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+          ltot[h] = (ls[0 * kN + h] + ls[1 * kN + h]) + (ls[2 * kN + h] + ls[3 * kN + h]);
+        if (!finish(pend_w, n - 1, pend_seg, m_pend, ltot)) {
+          ok = false;
+          break;
+        }
+        pend = false;
+      }
+      if (seg_end && n < nloc - 1) {
+        pend = true;
+        pend_seg = seg;
+        pend_w = sw;
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          m_pend[h] = m_used[h];
+          l_pend[h] = l_t[h];
+        }
+      } else if (seg_end) {
+        // the run's last tile: its own row-sum exchange, then the epilogue
+        float* ls2 = lsum + ((n + 1) & 1) * 4 * kN;
 #pragma unroll
         for (int h = 0; h < G; ++h) {
           const float ws = warp_sum(l_t[h]);
-          if (lane == 0) lsum[warp * kN + h] = ws;
+          if (lane == 0) ls2[warp * kN + h] = ws;
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(rbar);
@@ -636,39 +719,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         float ltot[G];
 #pragma unroll
         for (int h = 0; h < G; ++h)
-          ltot[h] = (lsum[0 * kN + h] + lsum[1 * kN + h]) + (lsum[2 * kN + h] + lsum[3 * kN + h]);
-        if (!wait_pv(n)) {
+          ltot[h] = (ls2[0 * kN + h] + ls2[1 * kN + h]) + (ls2[2 * kN + h] + ls2[3 * kN + h]);
+        if (!finish(sw, n, seg, m_used, ltot)) {
           ok = false;
           break;
-        }
-        tc_fence_after();
-        float o[kN];
-        tmem_ld16(lane_addr + kColO, o);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(o_free);
-
-        const int gidx = c0 + n;
-        const int u0 = gidx - sw.i;
-        const int first = split.cta_of(u0), last = split.cta_of(u0 + sw.nt - 1);
-        const int nparts = last - first + 1;
-        const int part = static_cast<int>(blockIdx.x) - first;
-        const int64_t row = q_row_of(a, sw.b);
-        if (nparts == 1) {
-          __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) +
-                                (row * a.num_heads + static_cast<int64_t>(sw.g) * G) * kHeadDim;
-#pragma unroll
-          for (int h = 0; h < G; ++h)
-            orow[h * kHeadDim + t] = __float2bfloat16_rn(o[h] / ltot[h]);
-        } else if (part >= 0 && part < a.ws.max_parts) {
-          const int64_t pidx = (static_cast<int64_t>(sw.b) * Hkv + sw.g) * a.ws.max_parts + part;
-#pragma unroll
-          for (int h = 0; h < G; ++h) a.ws.part_o[(pidx * G + h) * kHeadDim + t] = o[h] / ltot[h];
-          if (t < G) {
-#pragma unroll
-            for (int h = 0; h < G; ++h)
-              if (h == t) a.ws.lse[pidx * G + h] = m_used[h] + log2f(ltot[h]);
-          }
         }
       }
     }

@@ -36,6 +36,7 @@ EXPORTED = [
     "qattn_version",
     "qattn_rope_table_build",
     "qattn_rope_cache_append",
+    "qattn_paged_decode_kernel",
     "qattn_paged_decode_workspace_size",
     "qattn_paged_decode",
     "qattn_paged_decode_noalloc",
@@ -88,6 +89,8 @@ def load_library(path: str | None = None):
         L.qattn_rope_cache_append.argtypes = [
             _P, _I64, _P, _I64, _P, _I64, _P, _P, _I32, _P, _P, _I32, _P, _I32, qattn_dims, _P, _P]
         L.qattn_rope_cache_append.restype = ctypes.c_int
+        L.qattn_paged_decode_kernel.argtypes = [qattn_dims]
+        L.qattn_paged_decode_kernel.restype = ctypes.c_int
         L.qattn_paged_decode_workspace_size.argtypes = [_I32, _I32, qattn_dims]
         L.qattn_paged_decode_workspace_size.restype = _SZ
         L.qattn_paged_decode.argtypes = [
@@ -168,6 +171,15 @@ def qattn_rope_cache_append(q, k, v, positions, slot_mapping, k_cache, v_cache, 
         int(k_cache.shape[0]), _dev_ptr(cos_sin, "cos_sin", torch.float32), int(cos_sin.shape[0]),
         dims, _dev_ptr(err_word, "err_word", torch.int32), _stream(stream))
     _check("qattn_rope_cache_append", rc)
+
+
+QATTN_DECODE_CUDA_CORE = 0
+QATTN_DECODE_TENSOR_CORE = 1
+
+
+def qattn_paged_decode_kernel(dims) -> int:
+    """QATTN_DECODE_CUDA_CORE or QATTN_DECODE_TENSOR_CORE: the decode kernel used for dims."""
+    return int(lib().qattn_paged_decode_kernel(dims))
 
 
 def qattn_paged_decode_workspace_size(num_seqs: int, max_context_len: int, dims) -> int:

@@ -76,6 +76,17 @@ def test_workspace_size_grows_with_context(lib):
     assert Q.qattn_paged_decode_workspace_size(64, 4096, Q.make_dims(28, 5)) == 0
 
 
+@pytest.mark.skipif("QATTN_DECODE_KERNEL" in os.environ, reason="kernel choice forced")
+def test_decode_kernel_choice(lib):
+    # Groups of 1-2 query heads per KV head stay on CUDA cores; 3-8 use tcgen05.
+    assert Q.qattn_paged_decode_kernel(Q.make_dims(16, 16)) == Q.QATTN_DECODE_CUDA_CORE
+    assert Q.qattn_paged_decode_kernel(Q.make_dims(16, 8)) == Q.QATTN_DECODE_CUDA_CORE
+    assert Q.qattn_paged_decode_kernel(Q.make_dims(12, 4)) == Q.QATTN_DECODE_TENSOR_CORE
+    assert Q.qattn_paged_decode_kernel(Q.make_dims(28, 4)) == Q.QATTN_DECODE_TENSOR_CORE
+    assert Q.qattn_paged_decode_kernel(Q.make_dims(32, 4)) == Q.QATTN_DECODE_TENSOR_CORE
+    assert Q.qattn_paged_decode_kernel(Q.make_dims(28, 5)) == -1
+
+
 def test_host_validation_before_any_cuda_call(lib):
     """Every rejected call returns before touching CUDA (this machine may
     have no GPU): unsupported shapes, null pointers, bad strides."""

@@ -190,3 +190,50 @@ def test_workspace_too_small_is_rejected():
         Q.qattn_paged_decode(r.out, r.g.q_view(), r.g.k_cache, r.g.v_cache, r.g.block_tables,
                              r.g.context_lens, r.max_ctx, r.dims, small, r.err)
     assert ei.value.status == Q.QATTN_ERR_WORKSPACE
+
+
+# ------------------------------------------------------ workspace ----
+
+def test_decode_workspace_needs_no_initialisation():
+    """The split-KV parts and their counts live in the workspace.  A
+    workspace of random bytes, and one reused across shapes, give the clean
+    result."""
+    ref = GpuRun(W.build(1)).append().attend().sync().out.clone()
+    w1, w3 = W.build(1), W.build(3)
+    r1, r3 = GpuRun(w1).append(), GpuRun(w3).append()
+    size = max(r1.ws.numel(), r3.ws.numel())
+    gen = torch.Generator(device=r1.dev).manual_seed(77)
+    ws = torch.randint(0, 256, (size,), dtype=torch.uint8, device=r1.dev, generator=gen)
+    r1.ws, r3.ws = ws, ws
+    r1.attend().sync()
+    assert r1.err_bits == 0 and torch.equal(r1.out, ref)
+    r3.attend().sync()                        # other segments, other part counts
+    _, _, _, ref3, _, _ = oracle_for(3)
+    assert r3.err_bits == 0
+    assert_close(r3.out, ref3)
+    r1.attend().sync()
+    assert r1.err_bits == 0 and torch.equal(r1.out, ref)
+
+
+@pytest.mark.parametrize("idx", [1, 3])
+def test_decode_graph_replay(idx):
+    """The step (append, decode, merge; chained by programmatic dependent
+    launch) captured in a CUDA graph replays to the same result."""
+    w = W.build(idx)
+    r = GpuRun(w)
+    qkv0 = r.g.qkv.clone()
+    r.append().attend().sync()
+    first = r.out.clone()
+    s = torch.cuda.Stream(device=r.dev)
+    s.wait_stream(torch.cuda.current_stream(r.dev))
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            r.g.qkv.copy_(qkv0)
+            r.append().attend()
+    for _ in range(3):
+        r.out.zero_()
+        graph.replay()
+        r.sync()
+        assert r.err_bits == 0
+        assert torch.equal(r.out, first)
