@@ -209,7 +209,8 @@ size_t qattn_varlen_prefill_workspace_size(int32_t num_seqs,
  *   cu_seqlens_q [num_seqs + 1] int32, cu_seqlens_q[0] = 0,
  *                cu_seqlens_q[num_seqs] = total_q: query rows of sequence b
  *                are cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1;
- *   max_q_len    host upper bound on any sequence's query count;
+ *   max_q_len    host upper bound on any sequence's query count, at most
+ *                49152 (QATTN_ERR_UNSUPPORTED above, before any launch);
  *   context_lens [num_seqs] tokens in the cache for each sequence after
  *                this step's append (cached + new).
  * Query i of sequence b (q_len = cu_seqlens_q[b+1] - cu_seqlens_q[b],

@@ -369,6 +369,7 @@ int qattn_varlen_prefill(void* out, const void* q, int64_t q_row_stride,
   if (num_seqs < 0 || total_q < 0 || max_q_len < 0) return QATTN_ERR_INVALID_ARG;
   if (num_seqs == 0 || total_q == 0) return QATTN_OK;
   if (cu_seqlens_q == nullptr || max_q_len == 0) return QATTN_ERR_INVALID_ARG;
+  if ((max_q_len + 127) / 128 > kPrefillMaxPairs) return QATTN_ERR_UNSUPPORTED;
   st = check_attention_args(out, q, q_row_stride, k_cache, v_cache, num_blocks, block_tables,
                             max_blocks_per_seq, context_lens, max_context_len, dims);
   if (st != QATTN_OK) return st;

@@ -215,6 +215,10 @@ struct PrefillArgs {
   float scale_log2;
   int32_t* err_word;
 };
+// A prefill launch plans at most this many (sequence, 128-row tile) pairs;
+// larger calls are split into launches over sequence ranges, and a single
+// sequence of more than kPrefillMaxPairs * 128 new tokens is unsupported.
+constexpr int kPrefillMaxPairs = 384;
 cudaError_t launch_varlen_prefill(const PrefillArgs& a, const CUtensorMap& kmap,
                                   const CUtensorMap& vmap, int num_sms, cudaStream_t stream);
 

@@ -582,6 +582,35 @@ __global__ void __launch_bounds__(kThreads, 1)
 // folded in part order with a running maximum M (deterministic); the loads
 // of a batch of NB parts (all heads) are issued together.
 template <int G, int NB>
+__device__ __forceinline__ void fold_parts(const float (&lv)[NB][G], const float4 (&ov)[NB][G],
+                                           int count, float (&m)[G], float (&den)[G],
+                                           float4 (&num)[G]) {
+#pragma unroll
+  for (int j = 0; j < NB; ++j) {
+    if (j < count) {
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float mn = fmaxf(m[h], lv[j][h]);
+        const float sc = exp2f(m[h] - mn);  // 0 for the first part
+        const float f = exp2f(lv[j][h] - mn);
+        den[h] = fmaf(den[h], sc, f);
+        num[h].x = fmaf(num[h].x, sc, f * ov[j][h].x);
+        num[h].y = fmaf(num[h].y, sc, f * ov[j][h].y);
+        num[h].z = fmaf(num[h].z, sc, f * ov[j][h].z);
+        num[h].w = fmaf(num[h].w, sc, f * ov[j][h].w);
+        m[h] = mn;
+      }
+    }
+  }
+}
+
+// K2r: merge the parts of units that straddled CTAs (either decode
+// kernel).  One warp per (sequence, kv head) unit; lane = 4 dimensions.
+//   out[row, g*G + h] = sum_p 2^(lse_p - M) o_p / sum_p 2^(lse_p - M),
+// folded in part order with a running maximum M (deterministic).  The
+// first NB parts are loaded together with the part count (their addresses
+// do not depend on it), so the usual merge is one memory round trip.
+template <int G, int NB>
 __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a) {
   grid_dep_wait();  // the parts come from the decode grid
   const int Hkv = a.num_kv_heads;
@@ -589,16 +618,30 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a) {
   if (seg >= static_cast<int64_t>(a.num_seqs) * Hkv) return;
   const int b = static_cast<int>(seg / Hkv), g = static_cast<int>(seg % Hkv);
   const int lane = threadIdx.x & 31;
-  int64_t row = b;
-  if (a.cu_seqlens_q != nullptr) {
-    row = a.cu_seqlens_q[b];
-    if (a.cu_seqlens_q[b + 1] - row != 1) return;  // not a decode row
-  }
-  const int nparts = a.ws.nparts[seg];
-  if (nparts <= 1) return;
   const int64_t pbase = seg * a.ws.max_parts * G;
   const float* lse = a.ws.lse + pbase;
   const float* po = a.ws.part_o + pbase * kHeadDim + lane * 4;
+  const int nparts = a.ws.nparts[seg];
+  int64_t row = b;
+  int ql = 1;
+  if (a.cu_seqlens_q != nullptr) {
+    row = a.cu_seqlens_q[b];
+    ql = a.cu_seqlens_q[b + 1] - static_cast<int>(row);
+  }
+  float lv[NB][G];
+  float4 ov[NB][G];
+#pragma unroll
+  for (int j = 0; j < NB; ++j) {
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      if (j < a.ws.max_parts) {  // inside this unit's part slots
+        lv[j][h] = lse[j * G + h];
+        ov[j][h] =
+            *reinterpret_cast<const float4*>(po + static_cast<int64_t>(j * G + h) * kHeadDim);
+      }
+    }
+  }
+  if (ql != 1 || nparts <= 1) return;  // not a decode row, or written by the decode kernel
   float m[G], den[G];
   float4 num[G];
 #pragma unroll
@@ -607,9 +650,8 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a) {
     den[h] = 0.f;
     num[h] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  for (int p0 = 0; p0 < nparts; p0 += NB) {
-    float lv[NB][G];
-    float4 ov[NB][G];
+  fold_parts<G, NB>(lv, ov, nparts, m, den, num);
+  for (int p0 = NB; p0 < nparts; p0 += NB) {
 #pragma unroll
     for (int j = 0; j < NB; ++j) {
 #pragma unroll
@@ -621,23 +663,7 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a) {
         }
       }
     }
-#pragma unroll
-    for (int j = 0; j < NB; ++j) {
-      if (p0 + j < nparts) {
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float mn = fmaxf(m[h], lv[j][h]);
-          const float sc = exp2f(m[h] - mn);  // 0 for the first part
-          const float f = exp2f(lv[j][h] - mn);
-          den[h] = fmaf(den[h], sc, f);
-          num[h].x = fmaf(num[h].x, sc, f * ov[j][h].x);
-          num[h].y = fmaf(num[h].y, sc, f * ov[j][h].y);
-          num[h].z = fmaf(num[h].z, sc, f * ov[j][h].z);
-          num[h].w = fmaf(num[h].w, sc, f * ov[j][h].w);
-          m[h] = mn;
-        }
-      }
-    }
+    fold_parts<G, NB>(lv, ov, nparts - p0, m, den, num);
   }
   __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) +
                         (row * a.num_heads + static_cast<int64_t>(g) * G) * kHeadDim + lane * 4;

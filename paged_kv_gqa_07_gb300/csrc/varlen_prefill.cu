@@ -11,19 +11,26 @@
 //
 // Design (GB300): the prefill tiles are dense contractions, so they run on
 // the 5th-generation tensor cores with the accumulators in tensor memory.
-//   * One CTA = one (sequence, query head, 128-row query tile).  Rows are
-//     query tokens; the K/V tiles are 128 keys = eight 16-token blocks,
-//     gathered through the block table with 2-D TMA (16 x 64 boxes, 128-byte
-//     swizzle) into [d-half][key][64] shared-memory tiles -- exactly the
-//     K-major layout tcgen05 reads for B of S = Q K^T and the MN-major layout
-//     it reads for B of O = P V, so no data is re-laid.
-//   * Warp roles: warp 4 issues TMA (Q once, then K and V per tile through a
-//     2-stage ring), one thread of warp 5 issues tcgen05.mma (S = Q K^T into
-//     one of two 128-column S buffers in TMEM, O += P V into a third), warps
-//     0-3 own TMEM lanes 0-127 = the 128 query rows and do the online softmax:
-//     S row from TMEM, causal mask (only on tiles that cross the diagonal),
-//     row max, exp2, P written as bf16 into shared memory in the swizzled
-//     K-major layout.  S(kt+1) is computed while softmax(kt) runs.
+//   * Work: items (sequence, 128-row query tile, query head).  A persistent
+//     grid of one CTA per SM; every CTA builds the same list of (sequence,
+//     row tile) pairs, ranks them by KV tile count (largest first) and takes
+//     items in a snake order over the ranked list, heads innermost (the G
+//     heads of a KV group then run side by side and share the KV tiles in
+//     L2).  Decode rows (one query) are left to the decode kernel.
+//   * Warp roles: warp 8 copies Q of an item and its K tiles (eight 16-token
+//     blocks gathered through the block table, one 4 KB TMA box per (block,
+//     kv head), 128-byte swizzle) into a 2-deep ring; warp 10 copies the V
+//     tiles into their own ring; one thread of warp 9 issues tcgen05.mma as
+//     soon as each operand set is ready (S = Q K^T into one of two TMEM S
+//     buffers, O += P V into the item's TMEM O slot); warps 0-7 do the
+//     online softmax, two per TMEM lane quarter (rows 32q .. 32q + 31), one
+//     per half of the 128 keys of a tile: S half-row from TMEM, causal mask
+//     (only on tiles that cross the diagonal), half-row max swapped with the
+//     partner warp through TMEM, exp2, P as bf16 into one of two
+//     shared-memory P buffers (K-major, swizzled: the A operand of P V).
+//     With two S, two P and two O slots, S(n+1) and P V(n) run on the tensor
+//     cores while the softmax works on tile n, and an item's last P V and
+//     epilogue overlap the next item's first tile.
 //   * O is rescaled lazily: the running max is only moved when the new max
 //     exceeds it by more than 8 (log2 units), so most tiles skip the TMEM
 //     round trip; P values stay <= 2^8, well inside bf16.
@@ -42,155 +49,306 @@ namespace {
 
 constexpr int kM = 128;                 // query rows per tile
 constexpr int kN = 128;                 // keys per KV tile
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr int kThreads = 6 * 32;
+constexpr int kSoftmaxWarps = 8;        // two per TMEM lane quarter: column halves
+constexpr int kProducerWarp = 8;        // Q and K copies
+constexpr int kMmaWarp = 9;
+constexpr int kVProducerWarp = 10;      // V copies
+constexpr int kWarps = 11;
+constexpr int kThreads = kWarps * 32;
 constexpr int kHalfBytes = 128 * 128;   // 128 rows x 128 B (Q and P: [half][row])
 constexpr int kTileBytes = 2 * kHalfBytes;
 constexpr int kCacheTileBytes = kBlockSize * kHeadDim * 2;  // one (block, kv head): 4 KB
-constexpr int kStages = 2;
-constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemCols = 512;     // S[2] at 0 / 128, O[2] at 256 / 384
 constexpr uint32_t kColO = 256;
 constexpr float kLazyRescale = 8.0f;
 
 constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kTileBytes;
-constexpr int kOffV = kOffK + kStages * kTileBytes;
-constexpr int kOffP = kOffV + kStages * kTileBytes;
-constexpr int kOffBars = kOffP + kTileBytes;
-// barriers: q_full, k_full[2], v_full[2], kv_empty[2], s_full[2], s_free[2],
-//           p_full, o_done, mma_done
-constexpr int kNumBars = 14;
+constexpr int kOffK = kOffQ + kTileBytes;          // 2 stages
+constexpr int kOffV = kOffK + 2 * kTileBytes;      // 2 stages
+constexpr int kOffP = kOffV + 2 * kTileBytes;      // 2 buffers
+constexpr int kOffPairs = kOffP + 2 * kTileBytes;  // int[kPrefillMaxPairs], ranked
+constexpr int kOffDesc = kOffPairs + kPrefillMaxPairs * 4;  // ItemDesc[2]
+constexpr int kOffNkv = kOffDesc + 2 * 32;         // int[8]: MMA's item lengths
+constexpr int kOffBars = kOffNkv + 8 * 4;
+// q_full q_empty desc_full[2] desc_empty[2] k_full[2] k_empty[2] v_full[2]
+// v_empty[2] s_full[2] s_free[2] p_full[2] pv_done[2] o_free[2] mma_done
+// pair[4]
+constexpr int kNumBars = 2 + 2 * 11 + 1 + 4;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
-constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+constexpr int kSmemBytes = kOffMisc + 64 + 1024;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
-__device__ __forceinline__ void zero_rows(const PrefillArgs& a, int64_t row0, int rows, int h) {
-  for (int i = threadIdx.x; i < rows * (kHeadDim / 8); i += blockDim.x) {
-    const int r = i / (kHeadDim / 8), c = i % (kHeadDim / 8);
-    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) +
-                              ((row0 + r) * a.num_heads + h) * kHeadDim + c * 8) =
-        make_uint4(0, 0, 0, 0);
-  }
+struct ItemDesc {
+  int64_t row0;  // first query row of the tile
+  int rows;      // valid rows (<= 128)
+  int pos0;      // position of row 0
+  int nkv;       // KV tiles it attends
+  int b;         // sequence
+  int h;         // query head
+  int L;         // context length
+};
+static_assert(sizeof(ItemDesc) <= 32, "descriptor slot");
+
+struct Misc {
+  uint32_t tmem;
+  int abort;
+  int npairs;
+  int nitems;
+  int warp_sums[kWarps];
+};
+
+__device__ __forceinline__ bool prefill_ctx_ok(const PrefillArgs& a, int L, int ql) {
+  return L >= ql && L <= a.max_context_len && L <= a.max_blocks_per_seq * kBlockSize;
 }
 
+// Inclusive scan over the CTA's threads.
+__device__ __forceinline__ int block_scan(int v, int* warp_sums, int* block_total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  if (lane == 31) warp_sums[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < kWarps ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += n;
+    }
+    if (lane < kWarps) warp_sums[lane] = w;
+  }
+  __syncthreads();
+  const int add = warp > 0 ? warp_sums[warp - 1] : 0;
+  *block_total = warp_sums[kWarps - 1];
+  __syncthreads();
+  return v + add;
+}
+
+// Item r of this CTA: index into the ranked (pair, head) list, snake order.
+__device__ __forceinline__ int item_index(int r) {
+  const int P = gridDim.x, k = blockIdx.x;
+  return r * P + ((r & 1) ? (P - 1 - k) : k);
+}
+
+// 11 warps: 3 on three of the four SM sub-partitions, so at most 168
+// registers a thread.
 __global__ void __launch_bounds__(kThreads, 1)
     varlen_prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                           const __grid_constant__ CUtensorMap kmap,
                           const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
-  const int mt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int q0 = a.cu_seqlens_q[b];
-  const int q_len = a.cu_seqlens_q[b + 1] - q0;
-  if (q_len < 2 || mt * kM >= q_len) return;  // decode rows take the decode kernel
-  const int L = a.context_lens[b];
-  const int rows = min(kM, q_len - mt * kM);
-  const int64_t row0 = static_cast<int64_t>(q0) + mt * kM;
-  const int G = a.num_heads / a.num_kv_heads;
-  const int g = h / G;
-  if (L < q_len || L > a.max_context_len || L > a.max_blocks_per_seq * kBlockSize) {
-    zero_rows(a, row0, rows, h);
-    if (tid == 0 && h == 0 && mt == 0) set_err(a.err_word, QATTN_DEVERR_CONTEXT);
-    return;
-  }
-  const int pos0 = L - q_len + mt * kM;  // position of tile row 0
-  const int n_kv = (pos0 + rows - 1) / kN + 1;
-  const int nblk = (L + kBlockSize - 1) / kBlockSize;
-
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBars);
   uint64_t* q_full = bars + 0;
-  uint64_t* k_full = bars + 1;
-  uint64_t* v_full = bars + 3;
-  uint64_t* kv_empty = bars + 5;
-  uint64_t* s_full = bars + 7;
-  uint64_t* s_free = bars + 9;
-  uint64_t* p_full = bars + 11;
-  uint64_t* o_done = bars + 12;
-  uint64_t* mma_done = bars + 13;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+  uint64_t* q_empty = bars + 1;
+  uint64_t* desc_full = bars + 2;
+  uint64_t* desc_empty = bars + 4;
+  uint64_t* k_full = bars + 6;
+  uint64_t* k_empty = bars + 8;
+  uint64_t* v_full = bars + 10;
+  uint64_t* v_empty = bars + 12;
+  uint64_t* s_full = bars + 14;
+  uint64_t* s_free = bars + 16;
+  uint64_t* p_full = bars + 18;
+  uint64_t* pv_done = bars + 20;  // PV(n) completes phase n >> 1 of pv_done[n & 1]
+  uint64_t* o_free = bars + 22;   // the softmax has read O slot r & 1 of item r
+  uint64_t* mma_done = bars + 24;
+  // pair[q]: the two softmax warps of lane quarter q have swapped their
+  // partial row statistics (one phase per KV tile, plus one at the end)
+  uint64_t* pair = bars + 25;
+  Misc* misc = reinterpret_cast<Misc*>(smem + kOffMisc);
+  ItemDesc* desc = reinterpret_cast<ItemDesc*>(smem + kOffDesc);
+  int* pairs = reinterpret_cast<int*>(smem + kOffPairs);
+  int* nkv_ring = reinterpret_cast<int*>(smem + kOffNkv);
+  volatile int* abort_flag = &misc->abort;
   const uint32_t sbase = smem_u32(smem);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int B = a.num_seqs, H = a.num_heads;
+  const int G = H / a.num_kv_heads;
 
+  // ---- plan: the (sequence, row tile) pairs, ranked by KV tiles ----
+  // (scratch for the unranked list: the P buffers, unused until the loop)
+  int* sp = reinterpret_cast<int*>(smem + kOffP);
+  int* sc = sp + kPrefillMaxPairs;
+  int running = 0;
+  for (int base = 0; base < B; base += kThreads) {
+    const int b = base + tid;
+    int np = 0, ql = 0, L = 0;
+    if (b < B) {
+      ql = a.cu_seqlens_q[b + 1] - a.cu_seqlens_q[b];
+      L = a.context_lens[b];
+      if (ql >= 2 && prefill_ctx_ok(a, L, ql)) np = (ql + kM - 1) / kM;
+    }
+    int tot;
+    const int incl = block_scan(np, misc->warp_sums, &tot);
+    for (int mt = 0; mt < np; ++mt) {
+      const int idx = running + incl - np + mt;
+      if (idx < kPrefillMaxPairs) {
+        const int rows = min(kM, ql - mt * kM);
+        const int pos0 = L - ql + mt * kM;
+        sp[idx] = (b << 11) | mt;
+        sc[idx] = (pos0 + rows - 1) / kN + 1;
+      }
+    }
+    running += tot;
+  }
+  __syncthreads();
+  const int NP = min(running, kPrefillMaxPairs);
+  if (running > kPrefillMaxPairs && blockIdx.x == 0 && tid == 0)
+    set_err(a.err_word, QATTN_DEVERR_CONTEXT);
+  for (int i = tid; i < NP; i += kThreads) {
+    const int ci = sc[i];
+    int rank = 0;
+    for (int j = 0; j < NP; ++j) {
+      const int cj = sc[j];
+      rank += (cj > ci || (cj == ci && j < i)) ? 1 : 0;
+    }
+    pairs[rank] = sp[i];
+  }
+  if (tid == 0) {
+    const int NI = NP * H;
+    int n = 0;
+    while (item_index(n) < NI) ++n;
+    misc->nitems = n;
+    misc->abort = 0;
+  }
+  __syncthreads();
+
+  // Prefill sequences with an invalid context: zero rows and the CONTEXT bit.
+  for (int b = blockIdx.x; b < B; b += gridDim.x) {
+    const int q0 = a.cu_seqlens_q[b];
+    const int ql = a.cu_seqlens_q[b + 1] - q0;
+    if (ql < 2 || prefill_ctx_ok(a, a.context_lens[b], ql)) continue;
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) +
+                                          static_cast<int64_t>(q0) * H * kHeadDim);
+    for (int64_t i = tid; i < static_cast<int64_t>(ql) * H * (kHeadDim / 8); i += kThreads)
+      dst[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (tid == 0) set_err(a.err_word, QATTN_DEVERR_CONTEXT);
+  }
+  const int nitems = misc->nitems;
+  if (nitems == 0) return;  // no barrier, copy or TMEM in use yet
+
+  // ---- set-up: barriers, TMEM ----
   if (tid == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < kStages; ++s) {
+    mbar_init(q_empty, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&desc_full[s], 1);
+      mbar_init(&desc_empty[s], 1 + kSoftmaxWarps);  // the MMA thread, the softmax warps
       mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
       mbar_init(&v_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&v_empty[s], 1);
       mbar_init(&s_full[s], 1);
-      mbar_init(&s_free[s], 4);
+      mbar_init(&s_free[s], kSoftmaxWarps);
+      mbar_init(&p_full[s], kSoftmaxWarps);
+      mbar_init(&pv_done[s], 1);
+      mbar_init(&o_free[s], kSoftmaxWarps);
     }
-    mbar_init(p_full, 4);
-    mbar_init(o_done, 1);
     mbar_init(mma_done, 1);
-    *abort_flag = 0;
+    for (int q = 0; q < 4; ++q) mbar_init(&pair[q], 2);
     fence_barrier_init();
   }
   if (warp == kMmaWarp) {
-    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_alloc(&misc->tmem, kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
+  const uint32_t tmem = misc->tmem;
 
-  if (warp == kProducerWarp) {
-    // ================================ producer ================================
+  if (warp == kProducerWarp || warp == kVProducerWarp) {
+    // =============================== producers ================================
+    // Warp 8 writes the item descriptors and copies Q and the K tiles; warp
+    // 10 copies the V tiles on its own, so a K copy never waits behind a V
+    // ring slot (V slots free only after P V, one tile after K slots).
+    const bool is_v = warp == kVProducerWarp;
+    uint64_t* full = is_v ? v_full : k_full;
+    uint64_t* empty = is_v ? v_empty : k_empty;
+    const CUtensorMap* map = is_v ? &vmap : &kmap;
+    uint8_t* ring = smem + (is_v ? kOffV : kOffK);
     if (lane == 0) {
-      tma_prefetch_desc(&qmap);
-      tma_prefetch_desc(&kmap);
-      tma_prefetch_desc(&vmap);
-      mbar_arrive_expect_tx(q_full, kTileBytes);
-      tma_load_2d(smem + kOffQ, &qmap, h * kHeadDim, static_cast<int32_t>(row0), q_full);
-      tma_load_2d(smem + kOffQ + kHalfBytes, &qmap, h * kHeadDim + 64,
-                  static_cast<int32_t>(row0), q_full);
+      tma_prefetch_desc(map);
+      if (!is_v) tma_prefetch_desc(&qmap);
     }
-    const int* bt = a.block_tables + static_cast<int64_t>(b) * a.max_blocks_per_seq;
-    int issued = 0;
+    int n = 0;       // tiles whose copies were issued (all items)
+    int qn = 0;      // Q copies issued
     bool ok = true;
-    for (int kt = 0; kt < n_kv; ++kt) {
-      const int st = kt & 1;
-      int id = -1;
-      if (lane < 8) {
-        const int bi = kt * 8 + lane;
-        if (bi < nblk) {
-          id = bt[bi];
-          if (id < 0 || id >= a.num_blocks) {
-            set_err(a.err_word, QATTN_DEVERR_BLOCK);
-            id = -1;
-          }
+    for (int r = 0; r < nitems && ok; ++r) {
+      const int idx = item_index(r);
+      const int pr = pairs[idx / H];
+      const int b = pr >> 11, mt = pr & 2047, h = idx % H, g = h / G;
+      const int q0 = a.cu_seqlens_q[b];
+      const int ql = a.cu_seqlens_q[b + 1] - q0;
+      const int L = a.context_lens[b];
+      const int rows = min(kM, ql - mt * kM);
+      const int pos0 = L - ql + mt * kM;
+      const int nkv = (pos0 + rows - 1) / kN + 1;
+      const int64_t row0 = static_cast<int64_t>(q0) + mt * kM;
+      if (!is_v && lane == 0) {
+        // descriptor slot r & 1 was last read for item r - 2
+        ok = r < 2 || mbar_wait(&desc_empty[r & 1], ((r >> 1) & 1) ^ 1, abort_flag);
+        if (ok) {
+          ItemDesc& d = desc[r & 1];
+          d.row0 = row0;
+          d.rows = rows;
+          d.pos0 = pos0;
+          d.nkv = nkv;
+          d.b = b;
+          d.h = h;
+          d.L = L;
+          mbar_arrive(&desc_full[r & 1]);
+        }
+        // Q buffer: the previous item's last Q K^T is done
+        ok = ok && (r == 0 || mbar_wait(q_empty, (r - 1) & 1, abort_flag));
+        if (ok) {
+          mbar_arrive_expect_tx(q_full, kTileBytes);
+          tma_load_2d(smem + kOffQ, &qmap, h * kHeadDim, static_cast<int32_t>(row0), q_full);
+          tma_load_2d(smem + kOffQ + kHalfBytes, &qmap, h * kHeadDim + 64,
+                      static_cast<int32_t>(row0), q_full);
+          ++qn;
         }
       }
-      const int nvalid = __popc(__ballot_sync(0xffffffffu, id >= 0));
-      if (lane == 0 && kt >= kStages)
-        ok = mbar_wait(&kv_empty[st], ((kt >> 1) & 1) ^ 1, abort_flag);
       ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      uint8_t* kdst = smem + kOffK + st * kTileBytes + lane * kCacheTileBytes;
-      uint8_t* vdst = smem + kOffV + st * kTileBytes + lane * kCacheTileBytes;
-      if (lane == 0) mbar_arrive_expect_tx(&k_full[st], nvalid * 2 * kBlockSize * 128);
-      __syncwarp();
-      if (id >= 0) {
-        tma_load_cache_tile(kdst, &kmap, id * a.num_kv_heads + g, &k_full[st]);
+      const int* bt = a.block_tables + static_cast<int64_t>(b) * a.max_blocks_per_seq;
+      const int nblk = (L + kBlockSize - 1) / kBlockSize;
+      for (int kt = 0; kt < nkv && ok; ++kt) {
+        const int st = n & 1;
+        int id = -1;
+        if (lane < 8) {
+          const int bi = kt * 8 + lane;
+          if (bi < nblk) {
+            id = bt[bi];
+            if (id < 0 || id >= a.num_blocks) {
+              if (!is_v) set_err(a.err_word, QATTN_DEVERR_BLOCK);
+              id = -1;
+            }
+          }
+        }
+        const uint32_t nvalid = __popc(__ballot_sync(0xffffffffu, id >= 0));
+        if (lane == 0) {
+          ok = n < 2 || mbar_wait(&empty[st], ((n >> 1) & 1) ^ 1, abort_flag);
+          if (ok) mbar_arrive_expect_tx(&full[st], nvalid * kCacheTileBytes);
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        if (id >= 0)
+          tma_load_cache_tile(ring + st * kTileBytes + lane * kCacheTileBytes, map,
+                              id * a.num_kv_heads + g, &full[st]);
+        ++n;
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive_expect_tx(&v_full[st], nvalid * 2 * kBlockSize * 128);
-      __syncwarp();
-      if (id >= 0) {
-        tma_load_cache_tile(vdst, &vmap, id * a.num_kv_heads + g, &v_full[st]);
-      }
-      ++issued;
     }
-    // Drain: the copies of the last (up to two) issued tiles and of Q.
+    // Drain: the copies of the last (up to two) tiles and of the last Q land
+    // before the CTA exits.
     if (lane == 0) {
-      for (int j = issued - 1; j >= 0 && j >= issued - kStages; --j) {
-        mbar_wait_drain(&k_full[j & 1], (j >> 1) & 1);
-        mbar_wait_drain(&v_full[j & 1], (j >> 1) & 1);
-      }
-      mbar_wait_drain(q_full, 0);
+      for (int j = n - 1; j >= 0 && j >= n - 2; --j) mbar_wait_drain(&full[j & 1], (j >> 1) & 1);
+      if (qn > 0) mbar_wait_drain(q_full, (qn - 1) & 1);
+      if (*abort_flag) set_err(a.err_word, QATTN_DEVERR_TIMEOUT);
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
@@ -198,43 +356,95 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(kM, kN, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(kM, kHeadDim, true);
-      const uint32_t sq = sbase + kOffQ, sp = sbase + kOffP;
-      bool ok = mbar_wait(q_full, 0, abort_flag);
-      auto issue_pv = [&](int j) {
-        ok = ok && mbar_wait(p_full, j & 1, abort_flag);
-        ok = ok && mbar_wait(&v_full[j & 1], (j >> 1) & 1, abort_flag);
-        if (!ok) return;
-        tc_fence_after();
-        const uint32_t sv = sbase + kOffV + (j & 1) * kTileBytes;
+      const uint32_t sq = sbase + kOffQ;
+      // Q K^T and P V are each issued in order, whichever is ready first
+      // (readiness probed without blocking).
+      int qr = 0, qkt = 0, q_nkv = 0;  // Q K^T stream: item, its tile, its length
+      int pr = 0, pkt = 0;             // P V stream
+      int qn = 0, pn = 0;              // KV tiles of each stream so far
+      bool ok = true;
+      uint64_t idle_since = 0;
+      while (pr < nitems && ok) {
+        bool progressed = false;
+        if (pn < qn) {
+          const bool first = pkt == 0;
+          bool ready = mbar_test(&p_full[pn & 1], (pn >> 1) & 1) &&
+                       mbar_test(&v_full[pn & 1], (pn >> 1) & 1);
+          // an item's first P V overwrites O slot pr & 1, last read for item pr - 2
+          if (ready && first && pr >= 2) ready = mbar_test(&o_free[pr & 1], ((pr >> 1) - 1) & 1);
+          if (ready) {
+            tc_fence_after();
+            const uint32_t sv = sbase + kOffV + (pn & 1) * kTileBytes;
+            const uint32_t sp_ = sbase + kOffP + (pn & 1) * kTileBytes;
 #pragma unroll
-        for (int k = 0; k < kN / 16; ++k) {
-          const uint64_t ad = sdesc_sw128(sp + (k >> 2) * kHalfBytes + (k & 3) * 32, 16, 1024);
-          // V tile as the MN-major B: dim halves 1 KB apart (LBO), 8-key
-          // groups 2 KB apart (SBO); K step k = keys 16k..16k+15.
-          const uint64_t bd = sdesc_sw128(sv + k * 4096, 1024, 2048);
-          mma_bf16_ss(tmem + kColO, ad, bd, idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < kN / 16; ++k) {
+              const uint64_t ad =
+                  sdesc_sw128(sp_ + (k >> 2) * kHalfBytes + (k & 3) * 32, 16, 1024);
+              // V tile as the MN-major B: dim halves 1 KB apart (LBO), 8-key
+              // groups 2 KB apart (SBO); K step k = keys 16k..16k+15.
+              const uint64_t bd = sdesc_sw128(sv + k * 4096, 1024, 2048);
+              mma_bf16_ss(tmem + kColO + (pr & 1) * kHeadDim, ad, bd, idesc_pv,
+                          (first && k == 0) ? 0u : 1u);
+            }
+            mma_commit(&pv_done[pn & 1]);
+            mma_commit(&v_empty[pn & 1]);
+            ++pn;
+            if (++pkt == nkv_ring[pr & 7]) {
+              pkt = 0;
+              ++pr;
+            }
+            progressed = true;
+          }
         }
-        mma_commit(o_done);
-        mma_commit(&kv_empty[j & 1]);
-      };
-      for (int kt = 0; kt < n_kv && ok; ++kt) {
-        const int st = kt & 1;
-        ok = mbar_wait(&k_full[st], (kt >> 1) & 1, abort_flag);
-        if (ok && kt >= kStages) ok = mbar_wait(&s_free[st], ((kt >> 1) & 1) ^ 1, abort_flag);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t sk = sbase + kOffK + st * kTileBytes;
+        if (qr < nitems) {
+          if (q_nkv == 0 && mbar_test(&desc_full[qr & 1], (qr >> 1) & 1)) {
+            q_nkv = desc[qr & 1].nkv;
+            nkv_ring[qr & 7] = q_nkv;
+            mbar_arrive(&desc_empty[qr & 1]);
+            progressed = true;
+          }
+          if (q_nkv > 0) {
+            bool ready = mbar_test(&k_full[qn & 1], (qn >> 1) & 1);
+            if (ready && qn >= 2) ready = mbar_test(&s_free[qn & 1], ((qn >> 1) & 1) ^ 1);
+            if (ready && qkt == 0) ready = mbar_test(q_full, qr & 1);
+            // (the P V stream must not fall more than 8 items behind: nkv_ring)
+            if (ready && qr - pr >= 7) ready = false;
+            if (ready) {
+              tc_fence_after();
+              const uint32_t sk = sbase + kOffK + (qn & 1) * kTileBytes;
 #pragma unroll
-        for (int k = 0; k < kHeadDim / 16; ++k) {
-          const uint64_t ad = sdesc_sw128(sq + (k >> 2) * kHalfBytes + (k & 3) * 32, 16, 1024);
-          // K tile as the K-major B: dim half k/4 at +1 KB, 8-key groups 2 KB apart.
-          const uint64_t bd = sdesc_sw128(sk + (k >> 2) * 1024 + (k & 3) * 32, 16, 2048);
-          mma_bf16_ss(tmem + st * kN, ad, bd, idesc_qk, k > 0 ? 1u : 0u);
+              for (int k = 0; k < kHeadDim / 16; ++k) {
+                const uint64_t ad =
+                    sdesc_sw128(sq + (k >> 2) * kHalfBytes + (k & 3) * 32, 16, 1024);
+                // K tile as the K-major B: dim half k/4 at +1 KB, 8-key groups 2 KB apart.
+                const uint64_t bd = sdesc_sw128(sk + (k >> 2) * 1024 + (k & 3) * 32, 16, 2048);
+                mma_bf16_ss(tmem + (qn & 1) * kN, ad, bd, idesc_qk, k > 0 ? 1u : 0u);
+              }
+              mma_commit(&s_full[qn & 1]);
+              mma_commit(&k_empty[qn & 1]);
+              if (qkt == q_nkv - 1) mma_commit(q_empty);
+              ++qn;
+              if (++qkt == q_nkv) {
+                qkt = 0;
+                q_nkv = 0;
+                ++qr;
+              }
+              progressed = true;
+            }
+          }
         }
-        mma_commit(&s_full[st]);
-        if (kt > 0) issue_pv(kt - 1);
+        if (progressed) {
+          idle_since = 0;
+        } else {
+          const uint64_t now = globaltimer_ns();
+          if (idle_since == 0) {
+            idle_since = now;
+          } else if (*abort_flag || now - idle_since > kWaitTimeoutNs) {
+            *abort_flag = 1;
+            ok = false;
+          }
+        }
       }
-      if (ok) issue_pv(n_kv - 1);
       // Drain: every MMA issued above completes before TMEM is released.
       mma_commit(mma_done);
       mbar_wait_drain(mma_done, 0);
@@ -242,118 +452,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // =============================== softmax ================================
-    const int r = tid;  // tile row = TMEM lane
-    const bool row_valid = r < rows;
-    const int key_lim = row_valid ? pos0 + r : 0;  // keys <= key_lim are visible
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    const uint32_t sp_row = sbase + kOffP + r * 128;
-    float m_run = -INFINITY, l_run = 0.f;
-    bool ok = true;
-    for (int kt = 0; kt < n_kv; ++kt) {
-      const int sb = kt & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[sb], (kt >> 1) & 1, abort_flag))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      float s[kN];
-#pragma unroll
-      for (int c4 = 0; c4 < kN / 32; ++c4) {
-        float t[32];
-        tmem_ld32(lane_addr + sb * kN + c4 * 32, t);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[c4 * 32 + i] = t[i];
-      }
+    // Warp w owns TMEM lane quarter w & 3 (query rows t) and column half
+    // hf = w >> 2: keys 64 hf .. 64 hf + 63 of every S tile, P columns of
+    // that half, O dims of that half.  The two warps of a quarter swap their
+    // half-row max (and, at an item's end, half-row sums) through two spare
+    // TMEM columns of the S buffer they both just read.
+    const int q4 = warp & 3, hf = warp >> 2;
+    const int t = q4 * 32 + lane;  // tile row = TMEM lane
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q4 * 32) << 16);
+    auto wait_pv = [&](int j) -> bool {
+      return __all_sync(0xffffffffu, mbar_wait(&pv_done[j & 1], (j >> 1) & 1, abort_flag));
+    };
+    // Swap (a, b) with the partner warp through TMEM columns `col` (own
+    // half) / `col` of the other half; phase `ph` of the pair barrier.
+    auto swap2 = [&](uint32_t col_base, int ph, float a, float b, float& pa, float& pb) -> bool {
+      tmem_st2(lane_addr + col_base + 64 * hf, a, b);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[sb]);
-
-      const int kbase = kt * kN;
-      float mx = -INFINITY;
-      if (kbase + kN - 1 > key_lim) {
-#pragma unroll
-        for (int c = 0; c < kN; ++c) {
-          s[c] = (kbase + c <= key_lim) ? s[c] * a.scale_log2 : -INFINITY;
-          mx = fmaxf(mx, s[c]);
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < kN; ++c) {
-          s[c] *= a.scale_log2;
-          mx = fmaxf(mx, s[c]);
-        }
-      }
-      // PV(kt-1) must be done before O is rescaled or P is overwritten.
-      if (kt > 0) {
-        if (!__all_sync(0xffffffffu, mbar_wait(o_done, (kt - 1) & 1, abort_flag))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-      }
-      const float m_new = fmaxf(m_run, mx);
-      if (kt == 0) {
-        m_run = m_new;
-      } else {
-        const bool rescale = m_new > m_run + kLazyRescale;
-        if (__any_sync(0xffffffffu, rescale)) {
-          const float alpha = rescale ? exp2f(m_run - m_new) : 1.f;
-#pragma unroll
-          for (int c4 = 0; c4 < kHeadDim / 32; ++c4) {
-            float o[32];
-            tmem_ld32(lane_addr + kColO + c4 * 32, o);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] *= alpha;
-            tmem_st32(lane_addr + kColO + c4 * 32, o);
-          }
-          if (rescale) {
-            l_run *= alpha;
-            m_run = m_new;
-          }
-        }
-      }
-      float sum = 0.f;
-#pragma unroll
-      for (int cc = 0; cc < kN / 8; ++cc) {
-        float p[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          p[i] = exp2f(s[cc * 8 + i] - m_run);
-          sum += p[i];
-        }
-        const int half = cc >> 3, chunk = cc & 7;
-        sts128(sp_row + half * kHalfBytes + ((chunk ^ (r & 7)) << 4), pack_bf16x2_rn(p[0], p[1]),
-               pack_bf16x2_rn(p[2], p[3]), pack_bf16x2_rn(p[4], p[5]),
-               pack_bf16x2_rn(p[6], p[7]));
-      }
-      l_run += sum;
-      if (kbase + kN > L) {
-        // The tile reaches past the context: zero V rows of keys >= L.
-        if (!__all_sync(0xffffffffu, mbar_wait(&v_full[sb], (kt >> 1) & 1, abort_flag))) {
-          ok = false;
-          break;
-        }
-        if (kbase + r >= L) {
-          const uint32_t vtile = sbase + kOffV + sb * kTileBytes + (r >> 4) * kCacheTileBytes;
-#pragma unroll
-          for (int c = 0; c < 16; ++c) sts128(vtile + tile_chunk_offset(r & 15, c), 0u, 0u, 0u, 0u);
-        }
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
-    }
-    if (ok && __all_sync(0xffffffffu, mbar_wait(o_done, (n_kv - 1) & 1, abort_flag))) {
+      if (lane == 0) mbar_arrive(&pair[q4]);
+      if (!__all_sync(0xffffffffu, mbar_wait(&pair[q4], ph & 1, abort_flag))) return false;
       tc_fence_after();
-      const float inv = 1.f / l_run;
+      tmem_ld2(lane_addr + col_base + 64 * (1 - hf), pa, pb);
+      return true;
+    };
+    // Epilogue of item pr (last tile pn, row sum l): this half's O dims / l.
+    auto finish = [&](int64_t prow0, int prows, int ph, float l, int pn, int pr) -> bool {
+      if (!wait_pv(pn)) return false;
+      tc_fence_after();
+      const float inv = 1.f / l;
+      const bool valid = t < prows;
       __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) +
-                            ((row0 + r) * a.num_heads + h) * kHeadDim;
-#pragma unroll
-      for (int c4 = 0; c4 < kHeadDim / 32; ++c4) {
+                            ((prow0 + t) * H + ph) * kHeadDim + 64 * hf;
+      const uint32_t col = kColO + (pr & 1) * kHeadDim + 64 * hf;
+#pragma unroll 1
+      for (int c4 = 0; c4 < 2; ++c4) {
         float o[32];
-        tmem_ld32(lane_addr + kColO + c4 * 32, o);
-        if (row_valid) {
+        tmem_ld32(lane_addr + col + c4 * 32, o);
+        if (valid) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             uint4 v;
@@ -365,8 +500,165 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-    } else {
-      ok = false;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&o_free[pr & 1]);
+      return true;
+    };
+    bool pend = false;
+    int64_t pend_row0 = 0;
+    int pend_rows = 0, pend_h = 0;
+    float pend_l = 0.f;  // this half's row sum of the pending item
+    int pend_n = 0, pend_r = 0;
+    int n = 0;  // KV tiles consumed (all items) = pair barrier phases so far
+    bool ok = true;
+    for (int r = 0; r < nitems && ok; ++r) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&desc_full[r & 1], (r >> 1) & 1, abort_flag))) {
+        ok = false;
+        break;
+      }
+      const int64_t d_row0 = desc[r & 1].row0;
+      const int d_rows = desc[r & 1].rows, d_h = desc[r & 1].h;
+      const int d_nkv = desc[r & 1].nkv, d_L = desc[r & 1].L;
+      const int key_lim = t < d_rows ? desc[r & 1].pos0 + t : 0;  // keys <= key_lim are visible
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&desc_empty[r & 1]);
+      const uint32_t o_col = kColO + (r & 1) * kHeadDim + 64 * hf;  // this item's O, my dims
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int kt = 0; kt < d_nkv; ++kt, ++n) {
+        const int sb = n & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(&s_full[sb], (n >> 1) & 1, abort_flag))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        float s[64];
+        tmem_ld64(lane_addr + sb * kN + 64 * hf, s);
+
+        // Half-row max of the raw scores (scale > 0 commutes with max), eight
+        // accumulators; keys past the causal limit are -inf.
+        const int kbase = kt * kN + 64 * hf;
+        if (kbase + 63 > key_lim) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if (kbase + c > key_lim) s[c] = -INFINITY;
+        }
+        float mx8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx8[i] = s[i];
+#pragma unroll
+        for (int c = 8; c < 64; c += 8) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], s[c + i]);
+        }
+        const float mh = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        float mh2, lp2;
+        if (!swap2(sb * kN, n, mh, pend ? pend_l : 0.f, mh2, lp2)) {
+          ok = false;
+          break;
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_free[sb]);
+        const float mx = fmaxf(mh, mh2) * a.scale_log2;
+
+        // P buffer sb was last read by PV(n-2).
+        if (n >= 2 && !wait_pv(n - 2)) {
+          ok = false;
+          break;
+        }
+        if (kt == 0) {
+          m_run = mx;
+        } else {
+          const bool rescale = mx > m_run + kLazyRescale;
+          if (__any_sync(0xffffffffu, rescale)) {
+            // O holds the item's tiles so far: wait for PV(n-1), scale my dims.
+            if (!wait_pv(n - 1)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const float alpha = rescale ? exp2f(m_run - mx) : 1.f;
+#pragma unroll 1
+            for (int c4 = 0; c4 < 4; ++c4) {
+              float o[16];
+              tmem_ld16(lane_addr + o_col + c4 * 16, o);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) o[i] *= alpha;
+              tmem_st16(lane_addr + o_col + c4 * 16, o);
+            }
+            if (rescale) {
+              l_run *= alpha;
+              m_run = mx;
+            }
+          }
+        }
+        // p = 2^(scale_log2 * s - m): one FMA and one exp2 per score; eight
+        // partial sums; P half hf of row t, swizzled K-major.
+        float sum8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) sum8[i] = 0.f;
+        const uint32_t sp_row = sbase + kOffP + sb * kTileBytes + hf * kHalfBytes + t * 128;
+        const float neg_m = -m_run;
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+          float p[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            p[i] = exp2f(fmaf(s[cc * 8 + i], a.scale_log2, neg_m));
+            sum8[i] += p[i];
+          }
+          sts128(sp_row + ((cc ^ (t & 7)) << 4), pack_bf16x2_rn(p[0], p[1]),
+                 pack_bf16x2_rn(p[2], p[3]), pack_bf16x2_rn(p[4], p[5]),
+                 pack_bf16x2_rn(p[6], p[7]));
+        }
+        l_run += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
+                 ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+        if (kt * kN + kN > d_L) {
+          // The tile reaches past the context: zero V rows of keys >= L once
+          // V(n) has landed (PV(n-2) is done, so this barrier is at most one
+          // phase behind); this warp zeroes its half of each such row.
+          if (!__all_sync(0xffffffffu, mbar_wait(&v_full[sb], (n >> 1) & 1, abort_flag))) {
+            ok = false;
+            break;
+          }
+          if (kt * kN + t >= d_L) {
+            const uint32_t vtile = sbase + kOffV + sb * kTileBytes + (t >> 4) * kCacheTileBytes;
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              sts128(vtile + tile_chunk_offset(t & 15, 8 * hf + c), 0u, 0u, 0u, 0u);
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[sb]);
+        if (pend) {  // the previous item ended at tile n - 1; its sums came with the swap
+          if (!finish(pend_row0, pend_rows, pend_h, pend_l + lp2, pend_n, pend_r)) {
+            ok = false;
+            break;
+          }
+          pend = false;
+        }
+      }
+      if (!ok) break;
+      // The item's epilogue waits for its last P V: it runs after the next
+      // item's first tile (O has a slot per item parity).
+      pend = true;
+      pend_row0 = d_row0;
+      pend_rows = d_rows;
+      pend_h = d_h;
+      pend_l = l_run;
+      pend_n = n - 1;
+      pend_r = r;
+    }
+    if (ok && pend) {
+      // The last item: swap the half-row sums through S buffer 0 (no Q K^T
+      // is left to write it), then its epilogue.
+      float unused, lp2;
+      ok = swap2(0, n, 0.f, pend_l, unused, lp2) &&
+           finish(pend_row0, pend_rows, pend_h, pend_l + lp2, pend_n, pend_r);
     }
     if (!ok && lane == 0) set_err(a.err_word, QATTN_DEVERR_TIMEOUT);
   }
@@ -410,7 +702,7 @@ bool encode_q_map(CUtensorMap* map, const void* q, int64_t q_row_stride, int tot
 }  // namespace
 
 cudaError_t launch_varlen_prefill(const PrefillArgs& a, const CUtensorMap& kmap,
-                                  const CUtensorMap& vmap, int /*num_sms*/, cudaStream_t stream) {
+                                  const CUtensorMap& vmap, int num_sms, cudaStream_t stream) {
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(varlen_prefill_kernel,
@@ -421,11 +713,22 @@ cudaError_t launch_varlen_prefill(const PrefillArgs& a, const CUtensorMap& kmap,
   CUtensorMap qmap;
   if (!encode_q_map(&qmap, a.q, a.q_row_stride, a.total_q, a.num_heads))
     return cudaErrorInvalidValue;
-  const int mtiles = (a.max_q_len + kM - 1) / kM;
-  if (a.num_seqs > 65535 || a.num_heads > 65535) return cudaErrorInvalidConfiguration;
-  dim3 grid(mtiles, a.num_heads, a.num_seqs);
-  varlen_prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(qmap, kmap, vmap, a);
-  return cudaPeekAtLastError();
+  // A launch plans at most kPrefillMaxPairs (sequence, 128-row tile) pairs:
+  // batches of sequences keep every launch within that.
+  const int tiles_per_seq = (a.max_q_len + kM - 1) / kM;
+  if (tiles_per_seq > kPrefillMaxPairs) return cudaErrorNotSupported;
+  const int batch = kPrefillMaxPairs / tiles_per_seq;
+  for (int s0 = 0; s0 < a.num_seqs; s0 += batch) {
+    PrefillArgs p = a;
+    p.num_seqs = a.num_seqs - s0 < batch ? a.num_seqs - s0 : batch;
+    p.cu_seqlens_q = a.cu_seqlens_q + s0;
+    p.context_lens = a.context_lens + s0;
+    p.block_tables = a.block_tables + static_cast<int64_t>(s0) * a.max_blocks_per_seq;
+    varlen_prefill_kernel<<<num_sms, kThreads, kSmemBytes, stream>>>(qmap, kmap, vmap, p);
+    const cudaError_t e = cudaPeekAtLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace qattn

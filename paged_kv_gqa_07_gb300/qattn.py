@@ -219,3 +219,4 @@ def qattn_varlen_prefill(out, q, cu_seqlens_q, max_q_len, k_cache, v_cache, bloc
         int(workspace.numel() * workspace.element_size()),
         _dev_ptr(err_word, "err_word", torch.int32), _stream(stream))
     _check("qattn_varlen_prefill", rc)
+

@@ -123,6 +123,9 @@ def test_host_validation_before_any_cuda_call(lib):
     st = lib.qattn_varlen_prefill(fake, fake, 4608, None, 3, 10, 4, fake, fake, 10, fake, 4, fake,
                                   100, d, fake, 1 << 20, None, None)
     assert st == Q.QATTN_ERR_INVALID_ARG                      # null cu_seqlens_q
+    st = lib.qattn_varlen_prefill(fake, fake, 4608, fake, 3, 50000, 49153, fake, fake, 10, fake,
+                                  4, fake, 60000, d, fake, 1 << 30, None, None)
+    assert st == Q.QATTN_ERR_UNSUPPORTED                      # a 49153-token chunk
     st = lib.qattn_paged_decode(fake, fake, 4608, fake, fake, 10, fake, 4, fake, 3, 100,
                                 Q.make_dims(72, 8), fake, 1 << 20, None, None)
     assert st == Q.QATTN_ERR_UNSUPPORTED                      # group 9 > 8

@@ -102,3 +102,34 @@ def test_prefill_context_error_rows():
     assert torch.count_nonzero(r.out[:20]) == 0
     _, _, _, ref, _, _ = oracle_step(w)
     assert_close(r.out, ref, rows=slice(20, 50))
+
+
+def test_prefill_split_into_sequence_batches():
+    """A generous max_q_len hint (40000 tokens: 313 row tiles per sequence)
+    makes the library plan one sequence per launch; the result is the same
+    as the one-launch plan, bit for bit."""
+    w = W.custom(28, 4, ctx=[700, 40, 333, 520], q_lens=[300, 1, 200, 129], seed=304)
+    r = GpuRun(w).append().attend(varlen=True).sync()
+    first = r.out.clone()
+    g = r.g
+    r.out.zero_()
+    Q.qattn_varlen_prefill(r.out, g.q_view(), g.cu_seqlens_q, 40000, g.k_cache, g.v_cache,
+                           g.block_tables, g.context_lens, r.max_ctx, r.dims, r.ws, r.err)
+    r.sync()
+    assert r.err_bits == 0
+    assert torch.equal(r.out, first)
+    _, _, _, ref, _, _ = oracle_step(w)
+    assert_close(r.out, ref)
+
+
+def test_prefill_many_tiles_ranked_order():
+    """More (sequence, row tile) pairs than CTAs and KV lengths from 1 to 12
+    tiles: every item is computed once whatever the ranked order."""
+    ctx = [1500, 90, 700, 1300, 260, 1100, 30, 900]
+    ql = [600, 90, 650, 130, 260, 1000, 2, 400]
+    w = W.custom(8, 2, ctx=ctx, q_lens=ql, seed=305)
+    _, _, _, ref, _, e2 = oracle_step(w)
+    r = GpuRun(w).append().attend(varlen=True).sync()
+    assert r.err_bits == 0 and e2 == 0
+    assert_close(r.out, ref)
+
