@@ -228,8 +228,14 @@ def run_ours(args, dist: Dist):
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     decode = w.is_decode
     max_ctx = w.max_context_len
-    ws_size = (Q.qattn_paged_decode_workspace_size(w.num_seqs, max_ctx, dims) if decode
-               else Q.qattn_varlen_prefill_workspace_size(w.num_seqs, max_ctx, dims))
+    # a decode batch on a shared cached prefix takes the shared-prefix entry point
+    prefix = w.shared_prefix_tokens if decode else 0
+    if prefix:
+        ws_size = Q.qattn_paged_decode_shared_prefix_workspace_size(w.num_seqs, max_ctx, dims)
+    elif decode:
+        ws_size = Q.qattn_paged_decode_workspace_size(w.num_seqs, max_ctx, dims)
+    else:
+        ws_size = Q.qattn_varlen_prefill_workspace_size(w.num_seqs, max_ctx, dims)
     ws = torch.empty(max(ws_size, 256), dtype=torch.uint8, device=dev)
     out = torch.empty((w.num_tokens, H, D), dtype=torch.bfloat16, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -240,7 +246,11 @@ def run_ours(args, dist: Dist):
                                   g.k_cache, g.v_cache, table, dims, err)
 
     def attend():
-        if decode:
+        if prefix:
+            Q.qattn_paged_decode_shared_prefix(out, g.q_view(), g.k_cache, g.v_cache,
+                                               g.block_tables, g.context_lens, max_ctx, prefix,
+                                               dims, ws, err)
+        elif decode:
             Q.qattn_paged_decode(out, g.q_view(), g.k_cache, g.v_cache, g.block_tables,
                                  g.context_lens, max_ctx, dims, ws, err)
         else:
@@ -301,7 +311,17 @@ def run_ours(args, dist: Dist):
     hbm_peak, tf_peak, peak_kind = measured_peaks()
     attn_avg_s = statistics.mean(attn_ms) * 1e-3
     result = {}
-    if decode:
+    if prefix:
+        # HBM-bound on the distinct blocks: each is read from DRAM once
+        alg = w.unique_kv_bytes() + qo_bytes
+        achieved = alg / attn_avg_s / 1e9
+        result["roofline"] = {"bound": "hbm",
+                              "kernel": "varlen_prefill_kernel (prefix pass) + paged_decode",
+                              "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                              "frac": round(achieved / hbm_peak, 4), "peak_kind": peak_kind,
+                              "traffic": None, "algorithmic_bytes_per_launch": alg,
+                              "logical_kv_bytes_per_launch": kv_bytes}
+    elif decode:
         alg = kv_bytes + qo_bytes
         achieved = alg / attn_avg_s / 1e9
         if Q.qattn_paged_decode_kernel(dims) == Q.QATTN_DECODE_TENSOR_CORE:
@@ -325,7 +345,7 @@ def run_ours(args, dist: Dist):
     # ---- end to end through the C ABI with host buffers ----
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, w, dims, g, table, ws, err, dev, decode, max_ctx, dist)
+        e2e = run_e2e(args, w, dims, g, table, ws, err, dev, decode, max_ctx, dist, prefix)
 
     clk = clocks.summary()
     line = {
@@ -352,7 +372,7 @@ def run_ours(args, dist: Dist):
         "attention_ms": round(statistics.mean(attn_ms), 5),
         # per step: RoPE + append, the decode kernel and its merge kernel
         # (and, with prefill rows, the prefill kernel)
-        "gpu_launches": 3 * args.steps if decode else 4 * args.steps,
+        "gpu_launches": (4 if prefix else 3 if decode else 4) * args.steps,
         **result,
     }
     if e2e is not None:
@@ -364,7 +384,7 @@ def run_ours(args, dist: Dist):
     return line
 
 
-def run_e2e(args, w, dims, g, table, ws, err, dev, decode, max_ctx, dist):
+def run_e2e(args, w, dims, g, table, ws, err, dev, decode, max_ctx, dist, prefix=0):
     """Same step through the public API, inputs copied from pinned host memory
     each step and the attention output read back."""
     from paged_kv_gqa_07_gb300 import qattn as Q
@@ -386,7 +406,11 @@ def run_e2e(args, w, dims, g, table, ws, err, dev, decode, max_ctx, dist):
         Q.qattn_rope_cache_append(qkv[:, :H * D], qkv[:, H * D:(H + Hkv) * D],
                                   qkv[:, (H + Hkv) * D:], dev_in["positions"],
                                   dev_in["slot_mapping"], g.k_cache, g.v_cache, table, dims, err)
-        if decode:
+        if prefix:
+            Q.qattn_paged_decode_shared_prefix(out, qkv[:, :H * D], g.k_cache, g.v_cache,
+                                               dev_in["block_tables"], dev_in["context_lens"],
+                                               max_ctx, prefix, dims, ws, err)
+        elif decode:
             Q.qattn_paged_decode(out, qkv[:, :H * D], g.k_cache, g.v_cache, dev_in["block_tables"],
                                  dev_in["context_lens"], max_ctx, dims, ws, err)
         else:

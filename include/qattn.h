@@ -81,7 +81,9 @@ enum {
                                  smaller than the sequence's query count;
                                  bad cu_seqlens_q */
   QATTN_DEVERR_TIMEOUT = 8,   /* a bounded wait inside a kernel gave up */
-  QATTN_DEVERR_POSITION = 16  /* position outside [0, max_pos) */
+  QATTN_DEVERR_POSITION = 16, /* position outside [0, max_pos) */
+  QATTN_DEVERR_PREFIX = 32    /* a block table does not start with the shared
+                                 prefix blocks of row 0 */
 };
 
 /* Human-readable name of a return code (static storage). */
@@ -138,12 +140,12 @@ size_t qattn_paged_decode_workspace_size(int32_t num_seqs,
                                          qattn_dims dims);
 
 /* Which kernel qattn_paged_decode (and the decode rows of
- * qattn_varlen_prefill) launches for these dims: QATTN_DECODE_CUDA_CORE
- * (groups of 1-2 query heads per KV head: the group's dot products on CUDA
- * cores) or QATTN_DECODE_TENSOR_CORE (groups of 3-8: tcgen05 with the group
- * as the MMA N dimension).  The environment variable QATTN_DECODE_KERNEL
- * ("cuda" or "tc"), read once per process, overrides the choice where the
- * kernel supports the group.  Returns -1 for invalid dims. */
+ * qattn_varlen_prefill, and the shared-prefix decode) launches for these
+ * dims: QATTN_DECODE_TENSOR_CORE (tcgen05 with the query group as the MMA N
+ * dimension; the default for every group size) or QATTN_DECODE_CUDA_CORE
+ * (the group's dot products on CUDA cores), selected by the environment
+ * variable QATTN_DECODE_KERNEL=cuda (read once per process).  Returns -1
+ * for invalid dims. */
 #define QATTN_DECODE_CUDA_CORE 0
 #define QATTN_DECODE_TENSOR_CORE 1
 int qattn_paged_decode_kernel(qattn_dims dims);
@@ -171,6 +173,37 @@ int qattn_paged_decode(void* out, const void* q, int64_t q_row_stride,
                        int32_t num_seqs, int32_t max_context_len,
                        qattn_dims dims, void* workspace, size_t workspace_bytes,
                        int32_t* err_word, void* stream);
+
+/* Bytes of workspace qattn_paged_decode_shared_prefix needs (same rules as
+ * qattn_paged_decode_workspace_size; room for the prefix parts too). */
+size_t qattn_paged_decode_shared_prefix_workspace_size(int32_t num_seqs,
+                                                       int32_t max_context_len,
+                                                       qattn_dims dims);
+
+/* qattn_paged_decode for a batch whose sequences share a cached prefix
+ * (prefix caching, "Qwen2 模型结构代码详解" sections 3-4, over the shared
+ * blocks of the PagedAttention cache, vLLM-deploys-Qwen notes section 2.1): tokens
+ * 0 .. shared_prefix_len - 1 of EVERY sequence are the same cached tokens
+ * in the same physical blocks, block_tables[b][j] == block_tables[0][j] for
+ * j < shared_prefix_len / 16.  Same arguments and result as
+ * qattn_paged_decode, plus
+ *   shared_prefix_len  host, a multiple of 16, 0 <= it < every context_len
+ *                      (0: plain decode), < max_context_len.
+ * The prefix is attended once per kv head for the whole batch on tensor
+ * cores (all sequences' query groups against the prefix tiles, split over
+ * the SMs), each sequence's remaining tokens by the decode kernels, and the
+ * parts are merged in a fixed order (deterministic).  Device errors: those
+ * of qattn_paged_decode, a context_len <= shared_prefix_len gives a zero row
+ * and QATTN_DEVERR_CONTEXT, a table that does not start with row 0's prefix
+ * blocks QATTN_DEVERR_PREFIX (its result is then unspecified). */
+int qattn_paged_decode_shared_prefix(void* out, const void* q, int64_t q_row_stride,
+                                     const void* k_cache, const void* v_cache,
+                                     int32_t num_blocks, const int32_t* block_tables,
+                                     int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                     int32_t num_seqs, int32_t max_context_len,
+                                     int32_t shared_prefix_len, qattn_dims dims,
+                                     void* workspace, size_t workspace_bytes,
+                                     int32_t* err_word, void* stream);
 
 /* qattn_paged_decode for callers that cannot allocate device memory (code
  * running inside someone else's CUDA-graph capture, a serving loop whose

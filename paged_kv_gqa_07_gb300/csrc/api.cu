@@ -136,7 +136,7 @@ bool cached_cache_map(CUtensorMap* out, const void* cache, int32_t num_blocks,
 // row's G consecutive heads x 64 columns (half a head), 128-byte swizzled:
 // the tensor-core decode loads a KV head's query group with two boxes.
 bool encode_q_group_map(CUtensorMap* map, const void* q, int64_t q_row_stride, int32_t rows,
-                        int32_t num_heads, int32_t group) {
+                        int32_t num_heads, int32_t group, int32_t rows_per_box = 1) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim),
@@ -144,17 +144,17 @@ bool encode_q_group_map(CUtensorMap* map, const void* q, int64_t q_row_stride, i
                               static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim) * 2,
                                  static_cast<cuuint64_t>(q_row_stride) * 2};
-  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(group), 1};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(group),
+                             static_cast<cuuint32_t>(rows_per_box)};
   const cuuint32_t estr[3] = {1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Which decode kernel serves a group size: the tensor-core kernel for groups
-// of 3..8 query heads per KV head, the CUDA-core kernel for 1 and 2.  The
-// environment variable QATTN_DECODE_KERNEL=cuda|tc forces one (tc only
-// where it supports the group).
+// Which decode kernel serves a group size: the tensor-core kernel (measured
+// faster for every group size, 1..8); the environment variable
+// QATTN_DECODE_KERNEL=cuda selects the CUDA-core kernel instead.
 bool use_tc_decode(int group) {
   static int forced = [] {
     const char* e = getenv("QATTN_DECODE_KERNEL");
@@ -163,10 +163,8 @@ bool use_tc_decode(int group) {
     if (strcmp(e, "tc") == 0) return 2;
     return 0;
   }();
-  const bool tc_ok = group >= 3 && group <= 8;
   if (forced == 1) return false;
-  if (forced == 2) return tc_ok;
-  return tc_ok;
+  return group >= 1 && group <= 8;
 }
 
 int check_cache(const void* k_cache, const void* v_cache, int32_t num_blocks,
@@ -280,8 +278,10 @@ int decode_common(void* out, const void* q, int64_t q_row_stride, int32_t q_rows
                   const int32_t* context_lens, int32_t num_seqs, int32_t max_context_len,
                   const qattn_dims& dims, void* workspace, size_t workspace_bytes,
                   int32_t* err_word, cudaStream_t stream, const CUtensorMap& kmap,
-                  const CUtensorMap& vmap, int num_sms) {
-  const size_t need = qattn_paged_decode_workspace_size(num_seqs, max_context_len, dims);
+                  const CUtensorMap& vmap, int num_sms, int32_t prefix_len = 0,
+                  int32_t part_base = 0, int32_t extra_parts = 0) {
+  const size_t need = decode_workspace_bytes(num_seqs, max_context_len, dims.num_kv_heads,
+                                             dims.num_heads / dims.num_kv_heads, extra_parts);
   if (workspace == nullptr || workspace_bytes < need ||
       (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return QATTN_ERR_WORKSPACE;
@@ -301,7 +301,9 @@ int decode_common(void* out, const void* q, int64_t q_row_stride, int32_t q_rows
   a.scale_log2 = scale_of(dims) * kLog2e;
   a.err_word = err_word;
   a.ws = carve_decode_workspace(workspace, num_seqs, max_context_len, dims.num_kv_heads,
-                                dims.num_heads / dims.num_kv_heads);
+                                dims.num_heads / dims.num_kv_heads, extra_parts);
+  a.prefix_len = prefix_len;
+  a.part_base = part_base;
   const int group = dims.num_heads / dims.num_kv_heads;
   if (use_tc_decode(group)) {
     CUtensorMap qmap;
@@ -350,6 +352,92 @@ int qattn_paged_decode(void* out, const void* q, int64_t q_row_stride, const voi
                        max_blocks_per_seq, context_lens, num_seqs, max_context_len, dims,
                        workspace, workspace_bytes, err_word, static_cast<cudaStream_t>(stream),
                        kmap, vmap, sms);
+}
+
+size_t qattn_paged_decode_shared_prefix_workspace_size(int32_t num_seqs,
+                                                       int32_t max_context_len,
+                                                       qattn_dims dims) {
+  if (check_dims(dims) != QATTN_OK || num_seqs < 0 || max_context_len < 0) return 0;
+  return decode_workspace_bytes(num_seqs, max_context_len, dims.num_kv_heads,
+                                dims.num_heads / dims.num_kv_heads, kMaxPrefixSplits);
+}
+
+int qattn_paged_decode_shared_prefix(void* out, const void* q, int64_t q_row_stride,
+                                     const void* k_cache, const void* v_cache,
+                                     int32_t num_blocks, const int32_t* block_tables,
+                                     int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                     int32_t num_seqs, int32_t max_context_len,
+                                     int32_t shared_prefix_len, qattn_dims dims,
+                                     void* workspace, size_t workspace_bytes, int32_t* err_word,
+                                     void* stream) {
+  int st = check_dims(dims);
+  if (st != QATTN_OK) return st;
+  if (num_seqs < 0) return QATTN_ERR_INVALID_ARG;
+  if (num_seqs == 0) return QATTN_OK;
+  st = check_attention_args(out, q, q_row_stride, k_cache, v_cache, num_blocks, block_tables,
+                            max_blocks_per_seq, context_lens, max_context_len, dims);
+  if (st != QATTN_OK) return st;
+  if (shared_prefix_len < 0 || shared_prefix_len % kBlockSize != 0 ||
+      shared_prefix_len >= max_context_len || shared_prefix_len > max_blocks_per_seq * kBlockSize)
+    return QATTN_ERR_INVALID_ARG;
+  const size_t need =
+      qattn_paged_decode_shared_prefix_workspace_size(num_seqs, max_context_len, dims);
+  if (workspace == nullptr || workspace_bytes < need ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return QATTN_ERR_WORKSPACE;
+  CUtensorMap kmap, vmap;
+  if (!cached_cache_map(&kmap, k_cache, num_blocks, dims.num_kv_heads) ||
+      !cached_cache_map(&vmap, v_cache, num_blocks, dims.num_kv_heads))
+    return QATTN_ERR_CUDA;
+  const int sms = num_sms_current();
+  if (sms <= 0) return QATTN_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (shared_prefix_len == 0)
+    return decode_common(out, q, q_row_stride, num_seqs, nullptr, k_cache, v_cache, num_blocks,
+                         block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                         max_context_len, dims, workspace, workspace_bytes, err_word, s, kmap,
+                         vmap, sms, 0, 0, kMaxPrefixSplits);
+  // Pass 1: the prefix, once per kv head for all sequences (tensor cores),
+  // as parts 0 .. splits - 1 of every unit.
+  const int group = dims.num_heads / dims.num_kv_heads;
+  const int rows_per_tile = 128 / group;
+  const int row_tiles = (num_seqs + rows_per_tile - 1) / rows_per_tile;
+  const int prefix_tiles = (shared_prefix_len + 127) / 128;
+  int splits = sms / (dims.num_kv_heads * row_tiles);
+  if (splits > prefix_tiles) splits = prefix_tiles;
+  if (splits > kMaxPrefixSplits) splits = kMaxPrefixSplits;
+  if (splits < 1) splits = 1;
+  CUtensorMap qmap;
+  if (!encode_q_group_map(&qmap, q, q_row_stride, num_seqs, dims.num_heads, group,
+                          rows_per_tile))
+    return QATTN_ERR_CUDA;
+  PrefillArgs p{};
+  p.q = q;
+  p.q_row_stride = q_row_stride;
+  p.context_lens = context_lens;
+  p.block_tables = block_tables;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.num_seqs = num_seqs;
+  p.num_blocks = num_blocks;
+  p.total_q = num_seqs;
+  p.max_q_len = 1;
+  p.max_context_len = max_context_len;
+  p.num_heads = dims.num_heads;
+  p.num_kv_heads = dims.num_kv_heads;
+  p.scale_log2 = scale_of(dims) * kLog2e;
+  p.err_word = err_word;
+  p.prefix_len = shared_prefix_len;
+  p.prefix_splits = splits;
+  p.ws = carve_decode_workspace(workspace, num_seqs, max_context_len, dims.num_kv_heads, group,
+                                kMaxPrefixSplits);
+  st = cuda_status(launch_shared_prefix(p, qmap, kmap, vmap, sms, s));
+  if (st != QATTN_OK) return st;
+  // Pass 2: each sequence's own tokens (the decode kernels, parts from
+  // `splits` on), then the merge of all parts.
+  return decode_common(out, q, q_row_stride, num_seqs, nullptr, k_cache, v_cache, num_blocks,
+                       block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                       max_context_len, dims, workspace, workspace_bytes, err_word, s, kmap,
+                       vmap, sms, shared_prefix_len, splits, kMaxPrefixSplits);
 }
 
 size_t qattn_varlen_prefill_workspace_size(int32_t num_seqs, int32_t max_context_len,
@@ -403,6 +491,9 @@ int qattn_varlen_prefill(void* out, const void* q, int64_t q_row_stride,
   p.num_kv_heads = dims.num_kv_heads;
   p.scale_log2 = scale_of(dims) * kLog2e;
   p.err_word = err_word;
+  p.prefix_len = 0;
+  p.prefix_splits = 0;
+  p.ws = DecodeWorkspace{};
   const cudaError_t e = launch_varlen_prefill(p, kmap, vmap, sms, s);
   return e == cudaErrorNotSupported ? QATTN_ERR_UNSUPPORTED : cuda_status(e);
 }

@@ -93,10 +93,13 @@ struct DecodeWorkspace {
   int32_t max_parts;
 };
 
+// extra_parts: part slots a unit needs beyond its own split (shared-prefix
+// parts).
 size_t decode_workspace_bytes(int32_t num_seqs, int32_t max_context_len, int32_t num_kv_heads,
-                              int32_t group);
+                              int32_t group, int32_t extra_parts = 0);
 DecodeWorkspace carve_decode_workspace(void* base, int32_t num_seqs, int32_t max_context_len,
-                                       int32_t num_kv_heads, int32_t group);
+                                       int32_t num_kv_heads, int32_t group,
+                                       int32_t extra_parts = 0);
 
 struct DecodeArgs {
   void* out;               // [rows, H, D] bf16
@@ -114,6 +117,12 @@ struct DecodeArgs {
   float scale_log2;        // softmax scale * log2(e)
   int32_t* err_word;
   DecodeWorkspace ws;
+  // Shared-prefix (cascade) mode: the kernel attends only to tokens
+  // prefix_len .. L - 1 of every sequence (the prefix is done elsewhere),
+  // and writes every unit as parts part_base + i of the workspace instead of
+  // output rows.  Plain decode: both 0.
+  int32_t prefix_len;
+  int32_t part_base;
 };
 // CUDA-core decode (K2): 32-token chunks, the GQA group on CUDA cores.
 cudaError_t launch_paged_decode(const DecodeArgs& a, const CUtensorMap& kmap,
@@ -142,15 +151,21 @@ __device__ __forceinline__ void prefetch_decode_metadata(const DecodeArgs& a) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(cl + off));
 }
 
-// Context length of decode sequence b if it is valid for a decode kernel
-// (one query row; 1 <= L <= max_context_len; within the block table), else 0.
+// Tokens of decode sequence b the kernel attends to (L - prefix_len) if the
+// row is valid for a decode kernel (one query row; prefix_len < L <=
+// max_context_len; within the block table), else 0.
 __device__ __forceinline__ int decode_len_eff(const DecodeArgs& a, int b) {
   const int L = a.context_lens[b];
   if (a.cu_seqlens_q != nullptr) {
     if (a.cu_seqlens_q[b + 1] - a.cu_seqlens_q[b] != 1) return 0;
   }
-  if (L < 1 || L > a.max_context_len || L > a.max_blocks_per_seq * 16) return 0;
-  return L;
+  if (L <= a.prefix_len || L > a.max_context_len || L > a.max_blocks_per_seq * 16) return 0;
+  return L - a.prefix_len;
+}
+
+// Block-table entries of sequence b from its first attended token on.
+__device__ __forceinline__ const int32_t* decode_block_row(const DecodeArgs& a, int b) {
+  return a.block_tables + static_cast<int64_t>(b) * a.max_blocks_per_seq + a.prefix_len / 16;
 }
 
 // A unit that straddles CTAs leaves one partial result per CTA (O
@@ -214,6 +229,13 @@ struct PrefillArgs {
   int32_t num_kv_heads;
   float scale_log2;
   int32_t* err_word;
+  // Shared-prefix pass (the same kernel, prefix_len > 0): every sequence's
+  // query group against tokens 0 .. prefix_len - 1, held in the blocks of
+  // table row 0; the result goes to the decode workspace as parts
+  // 0 .. prefix_splits - 1 of every (sequence, kv head) unit.
+  int32_t prefix_len;
+  int32_t prefix_splits;
+  DecodeWorkspace ws;
 };
 // A prefill launch plans at most this many (sequence, 128-row tile) pairs;
 // larger calls are split into launches over sequence ranges, and a single
@@ -221,5 +243,11 @@ struct PrefillArgs {
 constexpr int kPrefillMaxPairs = 384;
 cudaError_t launch_varlen_prefill(const PrefillArgs& a, const CUtensorMap& kmap,
                                   const CUtensorMap& vmap, int num_sms, cudaStream_t stream);
+// The shared-prefix pass; qmap: the query rows as [rows][heads][128] with a
+// box of 64 dims x G heads x (128 / G) rows.
+constexpr int kMaxPrefixSplits = 32;
+cudaError_t launch_shared_prefix(const PrefillArgs& a, const CUtensorMap& qmap,
+                                 const CUtensorMap& kmap, const CUtensorMap& vmap, int num_sms,
+                                 cudaStream_t stream);
 
 }  // namespace qattn

@@ -76,12 +76,7 @@ struct Misc {
 
 // Context length of decode sequence b if it is valid for this kernel, else 0.
 __device__ __forceinline__ int seq_len_eff(const DecodeArgs& a, int b) {
-  const int L = a.context_lens[b];
-  if (a.cu_seqlens_q != nullptr) {
-    if (a.cu_seqlens_q[b + 1] - a.cu_seqlens_q[b] != 1) return 0;
-  }
-  if (L < 1 || L > a.max_context_len || L > a.max_blocks_per_seq * kBlockSize) return 0;
-  return L;
+  return decode_len_eff(a, b);
 }
 
 // Chunks of sequence b (and its effective length), served from the
@@ -251,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       qrow = 0;
       if (lane < cnt) {
         const int ntok = min(kChunkTokens, mw.L - mw.i * kChunkTokens);
-        const int* row = a.block_tables + static_cast<int64_t>(mw.b) * a.max_blocks_per_seq;
+        const int* row = decode_block_row(a, mw.b);
         id0 = row[2 * mw.i];
         if (ntok > kBlockSize) id1 = row[2 * mw.i + 1];
         if (mw.i == 0 || n_first + lane == 0) qrow = q_row_of(a, mw.b);
@@ -535,7 +530,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int part = static_cast<int>(blockIdx.x) - first;
       const int64_t row = q_row_of(a, cw.b);
       const int64_t seg_id = static_cast<int64_t>(cw.b) * Hkv + cw.g;
-      const bool fits = nparts <= a.ws.max_parts;
+      const bool fits = a.part_base + nparts <= a.ws.max_parts;
+      const bool as_part = nparts > 1 || a.part_base > 0;
       if (!fits && tid == 0) set_err(a.err_word, QATTN_DEVERR_CONTEXT);
       for (int idx = tid; idx < G * 32; idx += kConsumerWarps * 32) {
         const int h = idx >> 5, d4 = idx & 31;
@@ -558,19 +554,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float inv = 1.f / den;
         const float4 res = make_float4(num.x * inv, num.y * inv, num.z * inv, num.w * inv);
         const int head = cw.g * G + h;
-        if (nparts == 1) {
+        if (!as_part) {
           uint2 packed;
           packed.x = pack_bf16x2_rn(res.x, res.y);
           packed.y = pack_bf16x2_rn(res.z, res.w);
           *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) +
                                     (row * a.num_heads + head) * kHeadDim + d4 * 4) = packed;
         } else if (fits) {
-          const int64_t pidx = seg_id * a.ws.max_parts + part;
+          const int64_t pidx = seg_id * a.ws.max_parts + a.part_base + part;
           *reinterpret_cast<float4*>(a.ws.part_o + (pidx * G + h) * kHeadDim + d4 * 4) = res;
           if (d4 == 0) a.ws.lse[pidx * G + h] = M + log2f(den);
         }
       }
-      if (part == 0 && tid == 0) record_parts(a, seg_id, fits ? nparts : 0);
+      if (part == 0 && tid == 0) record_parts(a, seg_id, fits ? a.part_base + nparts : 0);
     }
   }
   if (!ok && lane == 0) set_err(a.err_word, QATTN_DEVERR_TIMEOUT);
@@ -708,9 +704,9 @@ cudaError_t launch_g(const DecodeArgs& a, const CUtensorMap& kmap, const CUtenso
 }  // namespace
 
 size_t decode_workspace_bytes(int32_t num_seqs, int32_t max_context_len, int32_t num_kv_heads,
-                              int32_t group) {
+                              int32_t group, int32_t extra_parts) {
   const int64_t nch = (static_cast<int64_t>(max_context_len) + kChunkTokens - 1) / kChunkTokens;
-  const int64_t max_parts = (nch + kMinChunksPerCta - 1) / kMinChunksPerCta + 1;
+  const int64_t max_parts = (nch + kMinChunksPerCta - 1) / kMinChunksPerCta + 1 + extra_parts;
   auto al = [](int64_t x) { return (x + 255) / 256 * 256; };
   const int64_t units = static_cast<int64_t>(num_seqs) * num_kv_heads * max_parts * group;
   return static_cast<size_t>(al(static_cast<int64_t>(num_seqs) * num_kv_heads * 4) +
@@ -718,9 +714,9 @@ size_t decode_workspace_bytes(int32_t num_seqs, int32_t max_context_len, int32_t
 }
 
 DecodeWorkspace carve_decode_workspace(void* base, int32_t num_seqs, int32_t max_context_len,
-                                       int32_t num_kv_heads, int32_t group) {
+                                       int32_t num_kv_heads, int32_t group, int32_t extra_parts) {
   const int64_t nch = (static_cast<int64_t>(max_context_len) + kChunkTokens - 1) / kChunkTokens;
-  const int64_t max_parts = (nch + kMinChunksPerCta - 1) / kMinChunksPerCta + 1;
+  const int64_t max_parts = (nch + kMinChunksPerCta - 1) / kMinChunksPerCta + 1 + extra_parts;
   auto al = [](int64_t x) { return (x + 255) / 256 * 256; };
   const int64_t units = static_cast<int64_t>(num_seqs) * num_kv_heads * max_parts * group;
   uint8_t* p = static_cast<uint8_t*>(base);

@@ -84,12 +84,7 @@ struct Misc {
 };
 
 __device__ __forceinline__ int seq_len_eff(const DecodeArgs& a, int b) {
-  const int L = a.context_lens[b];
-  if (a.cu_seqlens_q != nullptr) {
-    if (a.cu_seqlens_q[b + 1] - a.cu_seqlens_q[b] != 1) return 0;
-  }
-  if (L < 1 || L > a.max_context_len || L > a.max_blocks_per_seq * kBlockSize) return 0;
-  return L;
+  return decode_len_eff(a, b);
 }
 
 __device__ __forceinline__ int seq_len_cached(const DecodeArgs& a, const int* s_len, int b) {
@@ -322,8 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane < cnt) {
         const int ntok = min(kTile, mw.L - mw.i * kTile);
         const int nblk = (ntok + kBlockSize - 1) / kBlockSize;
-        const int* row = a.block_tables + static_cast<int64_t>(mw.b) * a.max_blocks_per_seq +
-                         mw.i * (kTile / kBlockSize);
+        const int* row = decode_block_row(a, mw.b) + mw.i * (kTile / kBlockSize);
 #pragma unroll
         for (int j = 0; j < 8; ++j)
           if (j < nblk) ids[j] = row[j];
@@ -533,13 +527,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int part = static_cast<int>(blockIdx.x) - first;
       const int64_t row = q_row_of(a, uw.b);
       const int64_t seg_id = static_cast<int64_t>(uw.b) * Hkv + uw.g;
-      if (nparts == 1) {
+      const bool fits = a.part_base + nparts <= a.ws.max_parts;
+      if (nparts == 1 && a.part_base == 0) {
         __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) +
                               (row * a.num_heads + static_cast<int64_t>(uw.g) * G) * kHeadDim;
 #pragma unroll
         for (int h = 0; h < G; ++h) orow[h * kHeadDim + t] = __float2bfloat16_rn(o[h] / ltot[h]);
-      } else if (nparts <= a.ws.max_parts) {
-        const int64_t pidx = seg_id * a.ws.max_parts + part;
+      } else if (fits) {
+        const int64_t pidx = seg_id * a.ws.max_parts + a.part_base + part;
 #pragma unroll
         for (int h = 0; h < G; ++h) a.ws.part_o[(pidx * G + h) * kHeadDim + t] = o[h] / ltot[h];
         if (t < G) {
@@ -550,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else if (t == 0) {
         set_err(a.err_word, QATTN_DEVERR_CONTEXT);
       }
-      if (part == 0 && t == 0) record_parts(a, seg_id, nparts <= a.ws.max_parts ? nparts : 0);
+      if (part == 0 && t == 0) record_parts(a, seg_id, fits ? a.part_base + nparts : 0);
       return true;
     };
     bool ok = true;
@@ -641,21 +636,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int h = 0; h < G; ++h) l_t[h] *= alpha[h];
       }
-      // P^T row h, token t (bf16) into buffer pb.
+      // P^T row h, token t (bf16) into buffer pb.  The row sums add the
+      // bf16-rounded weights the MMA multiplies, so numerator and
+      // denominator of O / l use the same weights (a consistent softmax;
+      // summing the fp32 values would leave a 2^-9 relative mismatch per key).
       {
-        float p[G];
+        unsigned short pbits[G];
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-          p[h] = exp2f(s[h] - m_used[h]);
-          l_t[h] += p[h];
+          pbits[h] = __bfloat16_as_ushort(__float2bfloat16_rn(exp2f(s[h] - m_used[h])));
+          l_t[h] += __uint_as_float(static_cast<uint32_t>(pbits[h]) << 16);
         }
         const uint32_t pbase = sbase + kOffP + pb * kSmallBytes + (t >> 6) * kSmallHalf;
         const int c = t & 63;
 #pragma unroll
         for (int h = 0; h < kN; ++h) {
           const uint32_t addr = pbase + h * 128 + ((((c >> 3) ^ (h & 7))) << 4) + (c & 7) * 2;
-          const unsigned short bits =
-              h < G ? __bfloat16_as_ushort(__float2bfloat16_rn(p[h < G ? h : 0])) : 0;
+          const unsigned short bits = h < G ? pbits[h < G ? h : 0] : 0;
           asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(bits) : "memory");
         }
       }
@@ -759,6 +756,8 @@ cudaError_t launch_paged_decode_tc(const DecodeArgs& a, const CUtensorMap& kmap,
                                    const CUtensorMap& vmap, const CUtensorMap& qmap, int num_sms,
                                    cudaStream_t stream) {
   switch (a.num_heads / a.num_kv_heads) {
+    case 1: return launch_tc_g<1>(a, kmap, vmap, qmap, num_sms, stream);
+    case 2: return launch_tc_g<2>(a, kmap, vmap, qmap, num_sms, stream);
     case 3: return launch_tc_g<3>(a, kmap, vmap, qmap, num_sms, stream);
     case 4: return launch_tc_g<4>(a, kmap, vmap, qmap, num_sms, stream);
     case 5: return launch_tc_g<5>(a, kmap, vmap, qmap, num_sms, stream);

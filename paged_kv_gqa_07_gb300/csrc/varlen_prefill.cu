@@ -68,7 +68,7 @@ constexpr int kOffV = kOffK + 2 * kTileBytes;      // 2 stages
 constexpr int kOffP = kOffV + 2 * kTileBytes;      // 2 buffers
 constexpr int kOffPairs = kOffP + 2 * kTileBytes;  // int[kPrefillMaxPairs], ranked
 constexpr int kOffDesc = kOffPairs + kPrefillMaxPairs * 4;  // ItemDesc[2]
-constexpr int kOffNkv = kOffDesc + 2 * 32;         // int[8]: MMA's item lengths
+constexpr int kOffNkv = kOffDesc + 2 * 64;         // int[8]: MMA's item lengths
 constexpr int kOffBars = kOffNkv + 8 * 4;
 // q_full q_empty desc_full[2] desc_empty[2] k_full[2] k_empty[2] v_full[2]
 // v_empty[2] s_full[2] s_free[2] p_full[2] pv_done[2] o_free[2] mma_done
@@ -79,15 +79,18 @@ constexpr int kSmemBytes = kOffMisc + 64 + 1024;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
 struct ItemDesc {
-  int64_t row0;  // first query row of the tile
+  int64_t row0;  // prefill: first query row of the tile
   int rows;      // valid rows (<= 128)
-  int pos0;      // position of row 0
+  int pos0;      // prefill: position of row 0 (row t sees keys <= pos0 + t)
   int nkv;       // KV tiles it attends
-  int b;         // sequence
-  int h;         // query head
-  int L;         // context length
+  int kt0;       // first of them (shared-prefix splits)
+  int b;         // prefill: sequence; shared prefix: first sequence of the tile
+  int h;         // prefill: query head; shared prefix: kv head
+  int L;         // keys >= L do not exist
+  int part;      // shared prefix: split index = part number in the workspace
+  int causal;
 };
-static_assert(sizeof(ItemDesc) <= 32, "descriptor slot");
+static_assert(sizeof(ItemDesc) <= 64, "descriptor slot");
 
 struct Misc {
   uint32_t tmem;
@@ -170,12 +173,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int B = a.num_seqs, H = a.num_heads;
   const int G = H / a.num_kv_heads;
 
+  const bool prefix_mode = a.prefix_len > 0;
+  // Shared-prefix pass: rows of a tile are (sequence, head of the group)
+  // pairs, R sequences a tile; items (kv head, split, row tile).
+  const int R = kM / G;
+  const int MT = (B + R - 1) / R;
+  const int TP = (a.prefix_len + kN - 1) / kN;  // prefix KV tiles
+  const int S = a.prefix_splits;
+
   // ---- plan: the (sequence, row tile) pairs, ranked by KV tiles ----
   // (scratch for the unranked list: the P buffers, unused until the loop)
   int* sp = reinterpret_cast<int*>(smem + kOffP);
   int* sc = sp + kPrefillMaxPairs;
   int running = 0;
-  for (int base = 0; base < B; base += kThreads) {
+  for (int base = 0; base < B && !prefix_mode; base += kThreads) {
     const int b = base + tid;
     int np = 0, ql = 0, L = 0;
     if (b < B) {
@@ -200,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int NP = min(running, kPrefillMaxPairs);
   if (running > kPrefillMaxPairs && blockIdx.x == 0 && tid == 0)
     set_err(a.err_word, QATTN_DEVERR_CONTEXT);
-  for (int i = tid; i < NP; i += kThreads) {
+  for (int i = tid; i < NP && !prefix_mode; i += kThreads) {
     const int ci = sc[i];
     int rank = 0;
     for (int j = 0; j < NP; ++j) {
@@ -210,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     pairs[rank] = sp[i];
   }
   if (tid == 0) {
-    const int NI = NP * H;
+    const int NI = prefix_mode ? a.num_kv_heads * S * MT : NP * H;
     int n = 0;
     while (item_index(n) < NI) ++n;
     misc->nitems = n;
@@ -218,8 +229,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
 
+  if (prefix_mode) {
+    // Every sequence's table must start with row 0's prefix blocks.
+    const int nb = a.prefix_len / kBlockSize;
+    const int64_t pairs_total = static_cast<int64_t>(B - 1) * nb;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + tid; i < pairs_total;
+         i += static_cast<int64_t>(gridDim.x) * kThreads) {
+      const int b = 1 + static_cast<int>(i / nb), j = static_cast<int>(i % nb);
+      if (a.block_tables[static_cast<int64_t>(b) * a.max_blocks_per_seq + j] != a.block_tables[j])
+        set_err(a.err_word, QATTN_DEVERR_PREFIX);
+    }
+  }
   // Prefill sequences with an invalid context: zero rows and the CONTEXT bit.
-  for (int b = blockIdx.x; b < B; b += gridDim.x) {
+  for (int b = blockIdx.x; b < B && !prefix_mode; b += gridDim.x) {
     const int q0 = a.cu_seqlens_q[b];
     const int ql = a.cu_seqlens_q[b + 1] - q0;
     if (ql < 2 || prefill_ctx_ok(a, a.context_lens[b], ql)) continue;
@@ -281,15 +303,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int r = 0; r < nitems && ok; ++r) {
       const int idx = item_index(r);
-      const int pr = pairs[idx / H];
-      const int b = pr >> 11, mt = pr & 2047, h = idx % H, g = h / G;
-      const int q0 = a.cu_seqlens_q[b];
-      const int ql = a.cu_seqlens_q[b + 1] - q0;
-      const int L = a.context_lens[b];
-      const int rows = min(kM, ql - mt * kM);
-      const int pos0 = L - ql + mt * kM;
-      const int nkv = (pos0 + rows - 1) / kN + 1;
-      const int64_t row0 = static_cast<int64_t>(q0) + mt * kM;
+      int b, mt, h, g, L, rows, pos0, nkv, kt0 = 0, part = 0;
+      int64_t row0 = 0;
+      if (prefix_mode) {
+        // item = ((g * S + split) * MT + mt): row tiles of one (kv head,
+        // split) run side by side and share its KV tiles in L2
+        mt = idx % MT;
+        part = (idx / MT) % S;
+        g = idx / (MT * S);
+        h = g;
+        b = mt * R;
+        L = a.prefix_len;
+        rows = min(R, B - b) * G;
+        pos0 = 0;
+        kt0 = static_cast<int>(static_cast<int64_t>(part) * TP / S);
+        nkv = static_cast<int>(static_cast<int64_t>(part + 1) * TP / S) - kt0;
+      } else {
+        const int pr = pairs[idx / H];
+        b = pr >> 11;
+        mt = pr & 2047;
+        h = idx % H;
+        g = h / G;
+        const int q0 = a.cu_seqlens_q[b];
+        const int ql = a.cu_seqlens_q[b + 1] - q0;
+        L = a.context_lens[b];
+        rows = min(kM, ql - mt * kM);
+        pos0 = L - ql + mt * kM;
+        nkv = (pos0 + rows - 1) / kN + 1;
+        row0 = static_cast<int64_t>(q0) + mt * kM;
+      }
       if (!is_v && lane == 0) {
         // descriptor slot r & 1 was last read for item r - 2
         ok = r < 2 || mbar_wait(&desc_empty[r & 1], ((r >> 1) & 1) ^ 1, abort_flag);
@@ -299,14 +341,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           d.rows = rows;
           d.pos0 = pos0;
           d.nkv = nkv;
+          d.kt0 = kt0;
           d.b = b;
           d.h = h;
           d.L = L;
+          d.part = part;
+          d.causal = prefix_mode ? 0 : 1;
           mbar_arrive(&desc_full[r & 1]);
         }
         // Q buffer: the previous item's last Q K^T is done
         ok = ok && (r == 0 || mbar_wait(q_empty, (r - 1) & 1, abort_flag));
-        if (ok) {
+        if (ok && prefix_mode) {
+          // R sequences x the G heads of kv head g: rows (sequence, head),
+          // 128 B each; rows past the batch read as zeros
+          mbar_arrive_expect_tx(q_full, 2 * 128 * R * G);
+          tma_load_3d(smem + kOffQ, &qmap, 0, g * G, b, q_full);
+          tma_load_3d(smem + kOffQ + kHalfBytes, &qmap, 64, g * G, b, q_full);
+          ++qn;
+        } else if (ok) {
           mbar_arrive_expect_tx(q_full, kTileBytes);
           tma_load_2d(smem + kOffQ, &qmap, h * kHeadDim, static_cast<int32_t>(row0), q_full);
           tma_load_2d(smem + kOffQ + kHalfBytes, &qmap, h * kHeadDim + 64,
@@ -315,13 +367,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
-      const int* bt = a.block_tables + static_cast<int64_t>(b) * a.max_blocks_per_seq;
+      // the shared prefix lives in the blocks of table row 0
+      const int* bt = a.block_tables + (prefix_mode ? 0 : static_cast<int64_t>(b) * a.max_blocks_per_seq);
       const int nblk = (L + kBlockSize - 1) / kBlockSize;
       for (int kt = 0; kt < nkv && ok; ++kt) {
         const int st = n & 1;
         int id = -1;
         if (lane < 8) {
-          const int bi = kt * 8 + lane;
+          const int bi = (kt0 + kt) * 8 + lane;
           if (bi < nblk) {
             id = bt[bi];
             if (id < 0 || id >= a.num_blocks) {
@@ -476,40 +529,66 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
     // Epilogue of item pr (last tile pn, row sum l): this half's O dims / l.
-    auto finish = [&](int64_t prow0, int prows, int ph, float l, int pn, int pr) -> bool {
-      if (!wait_pv(pn)) return false;
+    // Epilogue of item pr (last tile pn, row max m and sum l): this half's O
+    // dims / l -- bf16 output rows (prefill), or the item's split-KV part
+    // (normalised O, log2-sum-exp) of each (sequence, head) row (shared
+    // prefix).
+    struct Pending {
+      int64_t row0;
+      int rows, h, b, part, n, r;
+      float m, l;
+    };
+    auto finish = [&](const Pending& pd, float l) -> bool {
+      if (!wait_pv(pd.n)) return false;
       tc_fence_after();
       const float inv = 1.f / l;
-      const bool valid = t < prows;
-      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) +
-                            ((prow0 + t) * H + ph) * kHeadDim + 64 * hf;
-      const uint32_t col = kColO + (pr & 1) * kHeadDim + 64 * hf;
+      const bool valid = t < pd.rows;
+      const uint32_t col = kColO + (pd.r & 1) * kHeadDim + 64 * hf;
+      if (prefix_mode) {
+        const int j = t % G;
+        const int64_t seg = static_cast<int64_t>(pd.b + t / G) * a.num_kv_heads + pd.h;
+        const int64_t pidx = seg * a.ws.max_parts + pd.part;
+        float* optr = a.ws.part_o + (pidx * G + j) * kHeadDim + 64 * hf;
 #pragma unroll 1
-      for (int c4 = 0; c4 < 2; ++c4) {
-        float o[32];
-        tmem_ld32(lane_addr + col + c4 * 32, o);
-        if (valid) {
+        for (int c4 = 0; c4 < 2; ++c4) {
+          float o[32];
+          tmem_ld32(lane_addr + col + c4 * 32, o);
+          if (valid) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint4 v;
-            v.x = pack_bf16x2_rn(o[q * 8 + 0] * inv, o[q * 8 + 1] * inv);
-            v.y = pack_bf16x2_rn(o[q * 8 + 2] * inv, o[q * 8 + 3] * inv);
-            v.z = pack_bf16x2_rn(o[q * 8 + 4] * inv, o[q * 8 + 5] * inv);
-            v.w = pack_bf16x2_rn(o[q * 8 + 6] * inv, o[q * 8 + 7] * inv);
-            *reinterpret_cast<uint4*>(orow + c4 * 32 + q * 8) = v;
+            for (int q = 0; q < 8; ++q)
+              *reinterpret_cast<float4*>(optr + c4 * 32 + q * 4) =
+                  make_float4(o[q * 4] * inv, o[q * 4 + 1] * inv, o[q * 4 + 2] * inv,
+                              o[q * 4 + 3] * inv);
+          }
+        }
+        if (valid && hf == 0) a.ws.lse[pidx * G + j] = pd.m + log2f(l);
+      } else {
+        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) +
+                              ((pd.row0 + t) * H + pd.h) * kHeadDim + 64 * hf;
+#pragma unroll 1
+        for (int c4 = 0; c4 < 2; ++c4) {
+          float o[32];
+          tmem_ld32(lane_addr + col + c4 * 32, o);
+          if (valid) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint4 v;
+              v.x = pack_bf16x2_rn(o[q * 8 + 0] * inv, o[q * 8 + 1] * inv);
+              v.y = pack_bf16x2_rn(o[q * 8 + 2] * inv, o[q * 8 + 3] * inv);
+              v.z = pack_bf16x2_rn(o[q * 8 + 4] * inv, o[q * 8 + 5] * inv);
+              v.w = pack_bf16x2_rn(o[q * 8 + 6] * inv, o[q * 8 + 7] * inv);
+              *reinterpret_cast<uint4*>(orow + c4 * 32 + q * 8) = v;
+            }
           }
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&o_free[pr & 1]);
+      if (lane == 0) mbar_arrive(&o_free[pd.r & 1]);
       return true;
     };
     bool pend = false;
-    int64_t pend_row0 = 0;
-    int pend_rows = 0, pend_h = 0;
-    float pend_l = 0.f;  // this half's row sum of the pending item
-    int pend_n = 0, pend_r = 0;
+    Pending pending{};  // pending.l: this half's row sum of the pending item
     int n = 0;  // KV tiles consumed (all items) = pair barrier phases so far
     bool ok = true;
     for (int r = 0; r < nitems && ok; ++r) {
@@ -520,7 +599,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t d_row0 = desc[r & 1].row0;
       const int d_rows = desc[r & 1].rows, d_h = desc[r & 1].h;
       const int d_nkv = desc[r & 1].nkv, d_L = desc[r & 1].L;
-      const int key_lim = t < d_rows ? desc[r & 1].pos0 + t : 0;  // keys <= key_lim are visible
+      const int d_kt0 = desc[r & 1].kt0, d_b = desc[r & 1].b, d_part = desc[r & 1].part;
+      // keys <= key_lim are visible
+      const int key_lim = desc[r & 1].causal ? (t < d_rows ? desc[r & 1].pos0 + t : 0) : d_L - 1;
       __syncwarp();
       if (lane == 0) mbar_arrive(&desc_empty[r & 1]);
       const uint32_t o_col = kColO + (r & 1) * kHeadDim + 64 * hf;  // this item's O, my dims
@@ -537,7 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         // Half-row max of the raw scores (scale > 0 commutes with max), eight
         // accumulators; keys past the causal limit are -inf.
-        const int kbase = kt * kN + 64 * hf;
+        const int kbase = (d_kt0 + kt) * kN + 64 * hf;
         if (kbase + 63 > key_lim) {
 #pragma unroll
           for (int c = 0; c < 64; ++c)
@@ -554,7 +635,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float mh = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                                fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
         float mh2, lp2;
-        if (!swap2(sb * kN, n, mh, pend ? pend_l : 0.f, mh2, lp2)) {
+        if (!swap2(sb * kN, n, mh, pend ? pending.l : 0.f, mh2, lp2)) {
           ok = false;
           break;
         }
@@ -615,7 +696,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         l_run += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
                  ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
-        if (kt * kN + kN > d_L) {
+        if ((d_kt0 + kt) * kN + kN > d_L) {
           // The tile reaches past the context: zero V rows of keys >= L once
           // V(n) has landed (PV(n-2) is done, so this barrier is at most one
           // phase behind); this warp zeroes its half of each such row.
@@ -623,7 +704,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          if (kt * kN + t >= d_L) {
+          if ((d_kt0 + kt) * kN + t >= d_L) {
             const uint32_t vtile = sbase + kOffV + sb * kTileBytes + (t >> 4) * kCacheTileBytes;
 #pragma unroll
             for (int c = 0; c < 8; ++c)
@@ -635,7 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_full[sb]);
         if (pend) {  // the previous item ended at tile n - 1; its sums came with the swap
-          if (!finish(pend_row0, pend_rows, pend_h, pend_l + lp2, pend_n, pend_r)) {
+          if (!finish(pending, pending.l + lp2)) {
             ok = false;
             break;
           }
@@ -646,19 +727,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       // The item's epilogue waits for its last P V: it runs after the next
       // item's first tile (O has a slot per item parity).
       pend = true;
-      pend_row0 = d_row0;
-      pend_rows = d_rows;
-      pend_h = d_h;
-      pend_l = l_run;
-      pend_n = n - 1;
-      pend_r = r;
+      pending.row0 = d_row0;
+      pending.rows = d_rows;
+      pending.h = d_h;
+      pending.b = d_b;
+      pending.part = d_part;
+      pending.m = m_run;
+      pending.l = l_run;
+      pending.n = n - 1;
+      pending.r = r;
     }
     if (ok && pend) {
       // The last item: swap the half-row sums through S buffer 0 (no Q K^T
       // is left to write it), then its epilogue.
       float unused, lp2;
-      ok = swap2(0, n, 0.f, pend_l, unused, lp2) &&
-           finish(pend_row0, pend_rows, pend_h, pend_l + lp2, pend_n, pend_r);
+      ok = swap2(0, n, 0.f, pending.l, unused, lp2) && finish(pending, pending.l + lp2);
     }
     if (!ok && lane == 0) set_err(a.err_word, QATTN_DEVERR_TIMEOUT);
   }
@@ -701,8 +784,8 @@ bool encode_q_map(CUtensorMap* map, const void* q, int64_t q_row_stride, int tot
 
 }  // namespace
 
-cudaError_t launch_varlen_prefill(const PrefillArgs& a, const CUtensorMap& kmap,
-                                  const CUtensorMap& vmap, int num_sms, cudaStream_t stream) {
+namespace {
+cudaError_t set_smem_attr() {
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(varlen_prefill_kernel,
@@ -710,6 +793,28 @@ cudaError_t launch_varlen_prefill(const PrefillArgs& a, const CUtensorMap& kmap,
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
+  return cudaSuccess;
+}
+}  // namespace
+
+cudaError_t launch_shared_prefix(const PrefillArgs& a, const CUtensorMap& qmap,
+                                 const CUtensorMap& kmap, const CUtensorMap& vmap, int num_sms,
+                                 cudaStream_t stream) {
+  cudaError_t e = set_smem_attr();
+  if (e != cudaSuccess) return e;
+  const int G = a.num_heads / a.num_kv_heads;
+  const int R = kM / G;
+  const int64_t items =
+      static_cast<int64_t>(a.num_kv_heads) * a.prefix_splits * ((a.num_seqs + R - 1) / R);
+  const int grid = static_cast<int>(items < num_sms ? items : num_sms);
+  varlen_prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(qmap, kmap, vmap, a);
+  return cudaPeekAtLastError();
+}
+
+cudaError_t launch_varlen_prefill(const PrefillArgs& a, const CUtensorMap& kmap,
+                                  const CUtensorMap& vmap, int num_sms, cudaStream_t stream) {
+  cudaError_t es = set_smem_attr();
+  if (es != cudaSuccess) return es;
   CUtensorMap qmap;
   if (!encode_q_map(&qmap, a.q, a.q_row_stride, a.total_q, a.num_heads))
     return cudaErrorInvalidValue;

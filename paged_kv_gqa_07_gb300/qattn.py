@@ -30,6 +30,7 @@ DEVERR_BLOCK = 2
 DEVERR_CONTEXT = 4
 DEVERR_TIMEOUT = 8
 DEVERR_POSITION = 16
+DEVERR_PREFIX = 32
 
 EXPORTED = [
     "qattn_status_string",
@@ -40,6 +41,8 @@ EXPORTED = [
     "qattn_paged_decode_workspace_size",
     "qattn_paged_decode",
     "qattn_paged_decode_noalloc",
+    "qattn_paged_decode_shared_prefix_workspace_size",
+    "qattn_paged_decode_shared_prefix",
     "qattn_varlen_prefill_workspace_size",
     "qattn_varlen_prefill",
 ]
@@ -96,6 +99,12 @@ def load_library(path: str | None = None):
         L.qattn_paged_decode.argtypes = [
             _P, _P, _I64, _P, _P, _I32, _P, _I32, _P, _I32, _I32, qattn_dims, _P, _SZ, _P, _P]
         L.qattn_paged_decode.restype = ctypes.c_int
+        L.qattn_paged_decode_shared_prefix_workspace_size.argtypes = [_I32, _I32, qattn_dims]
+        L.qattn_paged_decode_shared_prefix_workspace_size.restype = _SZ
+        L.qattn_paged_decode_shared_prefix.argtypes = [
+            _P, _P, _I64, _P, _P, _I32, _P, _I32, _P, _I32, _I32, _I32, qattn_dims, _P, _SZ, _P,
+            _P]
+        L.qattn_paged_decode_shared_prefix.restype = ctypes.c_int
         L.qattn_varlen_prefill_workspace_size.argtypes = [_I32, _I32, qattn_dims]
         L.qattn_varlen_prefill_workspace_size.restype = _SZ
         L.qattn_varlen_prefill.argtypes = [
@@ -198,6 +207,27 @@ def qattn_paged_decode(out, q, k_cache, v_cache, block_tables, context_lens, max
         _dev_ptr(workspace, "workspace"), int(workspace.numel() * workspace.element_size()),
         _dev_ptr(err_word, "err_word", torch.int32), _stream(stream))
     _check("qattn_paged_decode", rc)
+
+
+def qattn_paged_decode_shared_prefix_workspace_size(num_seqs: int, max_context_len: int,
+                                                    dims) -> int:
+    return int(lib().qattn_paged_decode_shared_prefix_workspace_size(
+        int(num_seqs), int(max_context_len), dims))
+
+
+def qattn_paged_decode_shared_prefix(out, q, k_cache, v_cache, block_tables, context_lens,
+                                     max_context_len, shared_prefix_len, dims, workspace,
+                                     err_word=None, stream=None):
+    qp, qs = _rows(q, "q")
+    rc = lib().qattn_paged_decode_shared_prefix(
+        _dev_ptr(out, "out", torch.bfloat16), qp, qs,
+        _dev_ptr(k_cache, "k_cache", torch.bfloat16), _dev_ptr(v_cache, "v_cache", torch.bfloat16),
+        int(k_cache.shape[0]), _dev_ptr(block_tables, "block_tables", torch.int32),
+        int(block_tables.shape[1]), _dev_ptr(context_lens, "context_lens", torch.int32),
+        int(context_lens.shape[0]), int(max_context_len), int(shared_prefix_len), dims,
+        _dev_ptr(workspace, "workspace"), int(workspace.numel() * workspace.element_size()),
+        _dev_ptr(err_word, "err_word", torch.int32), _stream(stream))
+    _check("qattn_paged_decode_shared_prefix", rc)
 
 
 def qattn_varlen_prefill_workspace_size(num_seqs: int, max_context_len: int, dims) -> int:

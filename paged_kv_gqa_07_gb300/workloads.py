@@ -62,6 +62,7 @@ class Workload:
     cu_seqlens_q: torch.Tensor   # [B + 1] int32
     q_lens: list = field(default_factory=list)
     seed: int = 0
+    shared_prefix_tokens: int = 0  # tokens every table starts with in the same blocks
 
     # ----------------------------------------------------------- views ----
     @property
@@ -207,6 +208,21 @@ def custom(num_heads, num_kv_heads, ctx, q_lens, seed=1, pool_slack=0.1,
     block placement (used by edge-case tests)."""
     gen = torch.Generator().manual_seed(seed)
     shape = dict(num_heads=num_heads, num_kv_heads=num_kv_heads)
+    if shared_prefix_tokens:
+        # every table starts with the same blocks for the first
+        # shared_prefix_tokens tokens (a multiple of the block size)
+        assert shared_prefix_tokens % BLOCK_SIZE == 0
+        pb = shared_prefix_tokens // BLOCK_SIZE
+        own = [max(0, (L + BLOCK_SIZE - 1) // BLOCK_SIZE - pb) for L in ctx]
+        pool = pb + sum(own) + max(8, int(sum(own) * pool_slack)) + 1
+        perm = torch.randperm(pool, generator=gen)
+        shared = perm[:pb].tolist()
+        tables, used = [], pb
+        for nb in own:
+            tables.append(shared + perm[used:used + nb].tolist())
+            used += nb
+        return _assemble("custom", seed, gen, shape, list(ctx), list(q_lens), tables, pool,
+                         shared_prefix_tokens=shared_prefix_tokens)
     return _random_placement("custom", seed, gen, shape, list(ctx), list(q_lens),
                              slack=pool_slack)
 
@@ -276,7 +292,8 @@ def _assemble(name, seed, gen, shape, ctx, q_lens, tables, pool,
                     positions=positions, slot_mapping=slots, k_cache=k_cache,
                     v_cache=v_cache, block_tables=bt,
                     context_lens=torch.tensor(ctx, dtype=torch.int32),
-                    cu_seqlens_q=cu, q_lens=list(q_lens), seed=seed)
+                    cu_seqlens_q=cu, q_lens=list(q_lens), seed=seed,
+                    shared_prefix_tokens=shared_prefix_tokens)
 
 
 def to_device(w: Workload, device) -> Workload:

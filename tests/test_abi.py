@@ -78,9 +78,9 @@ def test_workspace_size_grows_with_context(lib):
 
 @pytest.mark.skipif("QATTN_DECODE_KERNEL" in os.environ, reason="kernel choice forced")
 def test_decode_kernel_choice(lib):
-    # Groups of 1-2 query heads per KV head stay on CUDA cores; 3-8 use tcgen05.
-    assert Q.qattn_paged_decode_kernel(Q.make_dims(16, 16)) == Q.QATTN_DECODE_CUDA_CORE
-    assert Q.qattn_paged_decode_kernel(Q.make_dims(16, 8)) == Q.QATTN_DECODE_CUDA_CORE
+    # tcgen05 decode for every group size unless QATTN_DECODE_KERNEL=cuda
+    assert Q.qattn_paged_decode_kernel(Q.make_dims(16, 16)) == Q.QATTN_DECODE_TENSOR_CORE
+    assert Q.qattn_paged_decode_kernel(Q.make_dims(16, 8)) == Q.QATTN_DECODE_TENSOR_CORE
     assert Q.qattn_paged_decode_kernel(Q.make_dims(12, 4)) == Q.QATTN_DECODE_TENSOR_CORE
     assert Q.qattn_paged_decode_kernel(Q.make_dims(28, 4)) == Q.QATTN_DECODE_TENSOR_CORE
     assert Q.qattn_paged_decode_kernel(Q.make_dims(32, 4)) == Q.QATTN_DECODE_TENSOR_CORE

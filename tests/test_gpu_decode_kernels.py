@@ -1,7 +1,6 @@
-"""Both decode kernels against the oracle: the tensor-core kernel (default
-for groups of 3..8 query heads per KV head) and the CUDA-core kernel (default
-for groups of 1 and 2), each forced in a fresh process through
-QATTN_DECODE_KERNEL."""
+"""Both decode kernels against the oracle: the tensor-core kernel (the
+default) and the CUDA-core kernel, each selected in a fresh process through
+QATTN_DECODE_KERNEL, on group sizes 1 to 8."""
 import os
 import subprocess
 import sys
@@ -21,7 +20,9 @@ from _util import GpuRun, assert_close, oracle_step
 cases = [W.build(1), W.build(0),
          W.custom(28, 4, ctx=[1, 15, 16, 17, 127, 128, 129, 300, 1000], q_lens=[1] * 9, seed=51),
          W.custom(24, 8, ctx=[5, 130, 257, 2000], q_lens=[1] * 4, seed=52),
-         W.custom(32, 4, ctx=[64, 4096], q_lens=[1] * 2, seed=53)]
+         W.custom(32, 4, ctx=[64, 4096], q_lens=[1] * 2, seed=53),
+         W.custom(8, 8, ctx=[1, 33, 128, 129, 700], q_lens=[1] * 5, seed=54),
+         W.custom(16, 8, ctx=[2, 160, 1500], q_lens=[1] * 3, seed=55)]
 for w in cases:
     _, _, _, ref, _, _ = oracle_step(w)
     r = GpuRun(w).append().attend().sync()
