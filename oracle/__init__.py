@@ -14,6 +14,11 @@ What each function follows (pages named by title and section):
   k and v into fixed-size cache blocks through a slot mapping (PagedAttention
   block cache, vLLM-deploys-Qwen notes section 2.1; nano-vllm block_table and
   prepare_prefill, Qwen3 skeleton page section 5).
+* :func:`rope_cache_append_ex`, :func:`add_bias_head`, :func:`rmsnorm_head`
+  -- the same append with the qkv projection bias (bias=True,
+  "Qwen2大模型架构解析与vLLM优化实践") and the Qwen3 per-head q_norm /
+  k_norm RMSNorms (nano-vllm Qwen3 skeleton page, module tree) applied
+  before RoPE.
 * :func:`paged_attention` -- grouped-query attention with scaling
   head_dim ** -0.5 ("Qwen2 模型结构代码详解" section 2; Attention(...) in
   "Qwen2大模型架构解析与vLLM优化实践" section 4.1), gathering keys through the
@@ -83,6 +88,13 @@ def lib():
                 _P, _I64, _P, _I64, _P, _I64, _P, _P, _I32, _P, _P, _I32, _P,
                 _I32, _I32, _I32, _I32, _I32]
             L.oracle_rope_cache_append.restype = _I32
+            L.oracle_add_bias_head.argtypes = [_P, _P, _I32, _P]
+            L.oracle_add_bias_head.restype = None
+            L.oracle_rmsnorm_head.argtypes = [_P, _P, _I32, _F64, _P]
+            L.oracle_rmsnorm_head.restype = None
+            L.oracle_rope_cache_append_ex.argtypes = (
+                L.oracle_rope_cache_append.argtypes + [_P, _P, _P, _F64])
+            L.oracle_rope_cache_append_ex.restype = _I32
             L.oracle_paged_attention.argtypes = [
                 _P, _P, _I64, _P, _I32, _P, _P, _I32, _P, _I32, _P, _I32, _I32,
                 _I32, _I32, _F64, _I32, _I32]
@@ -184,6 +196,48 @@ def rope_cache_append(qkv, positions, slot_mapping, k_cache, v_cache, cos_sin,
         base, W, base + H * D * 2, W, base + (H + Hkv) * D * 2, W,
         _ptr(pos), _ptr(slots), int(pos.shape[0]), _ptr(k_cache), _ptr(v_cache),
         int(k_cache.shape[0]), _ptr(cs), cs.shape[0], H, Hkv, D, block_size))
+
+
+def add_bias_head(x, b):
+    """bf16(float(x) + float(b)) element-wise on uint16 bf16 bit arrays."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    b = np.ascontiguousarray(b, dtype=np.uint16)
+    y = np.empty_like(x)
+    lib().oracle_add_bias_head(_ptr(x), _ptr(b), int(x.size), _ptr(y))
+    return y
+
+
+def rmsnorm_head(x, w, eps):
+    """RMSNorm of one head vector (uint16 bf16 bits) with weight w, eps."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    w = np.ascontiguousarray(w, dtype=np.uint16)
+    y = np.empty_like(x)
+    lib().oracle_rmsnorm_head(_ptr(x), _ptr(w), int(x.size), float(eps), _ptr(y))
+    return y
+
+
+def rope_cache_append_ex(qkv, positions, slot_mapping, k_cache, v_cache, cos_sin,
+                         num_heads, num_kv_heads, head_dim, block_size, bias=None,
+                         q_norm_w=None, k_norm_w=None, eps=1e-6):
+    """rope_cache_append with the qkv projection bias ([(H + 2 Hkv) D] bf16
+    bits) added first and the per-head RMSNorms (weights [D]) of q and k
+    before RoPE; None skips a step.  In place; returns the error bits."""
+    assert qkv.dtype == np.uint16 and qkv.flags["C_CONTIGUOUS"]
+    H, Hkv, D = num_heads, num_kv_heads, head_dim
+    W = qkv.shape[1]
+    assert W == (H + 2 * Hkv) * D
+    pos = _i32(positions)
+    slots = _i32(slot_mapping)
+    cs = np.ascontiguousarray(cos_sin, dtype=np.float32)
+    keep = [None if a is None else np.ascontiguousarray(a, dtype=np.uint16)
+            for a in (bias, q_norm_w, k_norm_w)]
+    ptrs = [None if a is None else _ptr(a) for a in keep]
+    base = qkv.ctypes.data
+    return int(lib().oracle_rope_cache_append_ex(
+        base, W, base + H * D * 2, W, base + (H + Hkv) * D * 2, W,
+        _ptr(pos), _ptr(slots), int(pos.shape[0]), _ptr(k_cache), _ptr(v_cache),
+        int(k_cache.shape[0]), _ptr(cs), cs.shape[0], H, Hkv, D, block_size,
+        ptrs[0], ptrs[1], ptrs[2], float(eps)))
 
 
 def paged_attention(q, k_cache, v_cache, block_tables, context_lens,

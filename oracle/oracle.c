@@ -177,6 +177,108 @@ int32_t oracle_rope_cache_append(
   return err;
 }
 
+/* --------------------------- qkv bias and per-head RMSNorm (Qwen3) ---- */
+
+/* The qkv projection's bias: "Qwen2大模型架构解析与vLLM优化实践" (qkv_proj
+ * with bias=True) and the nano-vllm Qwen3 skeleton (qkv_bias from
+ * attention_bias).  Reading: the biased projection output is a bf16 tensor,
+ * x' = bf16(float(x) + float(b)) -- one rounding (the fp32 sum of two bf16
+ * values is exact unless their exponents differ by more than 16). */
+void oracle_add_bias_head(const uint16_t* x, const uint16_t* b, int32_t n, uint16_t* y) {
+  for (int32_t i = 0; i < n; ++i) {
+    float s = bf16_to_f32(x[i]) + bf16_to_f32(b[i]);
+    y[i] = f32_to_bf16_rne(s);
+  }
+}
+
+/* RMSNorm of one head vector with a per-dimension weight (the Qwen3
+ * attention's q_norm / k_norm, nano-vllm Qwen3 skeleton page, module tree;
+ * eps = rms_norm_eps): y_i = x_i / sqrt(mean(x^2) + eps) * w_i.  Reading,
+ * as a bf16 tensor op: the sum of squares in fp64 (exact for bf16 inputs
+ * whose magnitudes span less than 2^18, so the summation order does not
+ * matter); v = fp32(mean + eps) rounded once; r = 1 / sqrt(v) with
+ * correctly rounded fp32 sqrt and division; y_i = bf16(fp32(fp32(x_i * r) *
+ * w_i)). */
+void oracle_rmsnorm_head(const uint16_t* x, const uint16_t* w, int32_t n, double eps,
+                         uint16_t* y) {
+  double ss = 0.0;
+  for (int32_t i = 0; i < n; ++i) {
+    double xi = bf16_to_f64(x[i]);
+    ss += xi * xi;
+  }
+  float v = (float)(ss / (double)n + eps);
+  float r = 1.0f / sqrtf(v);
+  for (int32_t i = 0; i < n; ++i) {
+    float t = bf16_to_f32(x[i]) * r;
+    float u = t * bf16_to_f32(w[i]);
+    y[i] = f32_to_bf16_rne(u);
+  }
+}
+
+/* oracle_rope_cache_append with the projection bias and the Qwen3 head
+ * norms first: for each token, q heads: q = rope(norm_q(bias(q))); k heads:
+ * k = rope(norm_k(bias(k))) into the cache; v heads: v = bias(v) into the
+ * cache.  Any of bias / q_norm_w / k_norm_w may be NULL (step skipped).
+ * bias: [(H + 2 Hkv) * D] (q heads, then k, then v); norm weights: [D]. */
+int32_t oracle_rope_cache_append_ex(
+    uint16_t* q, int64_t q_row_stride, const uint16_t* k, int64_t k_row_stride,
+    const uint16_t* v, int64_t v_row_stride, const int32_t* positions,
+    const int32_t* slot_mapping, int32_t num_tokens, uint16_t* k_cache,
+    uint16_t* v_cache, int32_t num_blocks, const float* cos_sin,
+    int32_t max_pos, int32_t num_heads, int32_t num_kv_heads,
+    int32_t head_dim, int32_t block_size, const uint16_t* bias,
+    const uint16_t* q_norm_w, const uint16_t* k_norm_w, double eps) {
+  int32_t err = 0;
+  const int32_t D = head_dim;
+  uint16_t* a = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)D);
+  uint16_t* b = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)D);
+  for (int32_t t = 0; t < num_tokens; ++t) {
+    int32_t pos = positions[t];
+    if (pos < 0 || pos >= max_pos) {
+      err |= OR_ERR_POSITION;
+      continue;
+    }
+    const float* row = cos_sin + (int64_t)pos * D;
+    for (int32_t h = 0; h < num_heads; ++h) {
+      uint16_t* qh = q + (int64_t)t * q_row_stride + (int64_t)h * D;
+      memcpy(a, qh, sizeof(uint16_t) * (size_t)D);
+      if (bias) oracle_add_bias_head(a, bias + (int64_t)h * D, D, a);
+      if (q_norm_w) {
+        oracle_rmsnorm_head(a, q_norm_w, D, eps, b);
+        memcpy(a, b, sizeof(uint16_t) * (size_t)D);
+      }
+      oracle_rope_head_exact(a, D, row, qh);
+    }
+    int32_t slot = slot_mapping[t];
+    if (slot < 0) continue; /* padding token */
+    if ((int64_t)slot >= (int64_t)num_blocks * block_size) {
+      err |= OR_ERR_SLOT;
+      continue;
+    }
+    int32_t blk = slot / block_size, off = slot % block_size;
+    for (int32_t g = 0; g < num_kv_heads; ++g) {
+      int64_t dst = (((int64_t)blk * num_kv_heads + g) * block_size + off) * D;
+      const uint16_t* kh = k + (int64_t)t * k_row_stride + (int64_t)g * D;
+      const uint16_t* vh = v + (int64_t)t * v_row_stride + (int64_t)g * D;
+      memcpy(a, kh, sizeof(uint16_t) * (size_t)D);
+      if (bias) oracle_add_bias_head(a, bias + (int64_t)(num_heads + g) * D, D, a);
+      if (k_norm_w) {
+        oracle_rmsnorm_head(a, k_norm_w, D, eps, b);
+        memcpy(a, b, sizeof(uint16_t) * (size_t)D);
+      }
+      oracle_rope_head_exact(a, D, row, k_cache + dst);
+      if (bias)
+        oracle_add_bias_head(vh, bias + (int64_t)(num_heads + num_kv_heads + g) * D, D,
+                             v_cache + dst);
+      else
+        memcpy(v_cache + dst, vh, sizeof(uint16_t) * (size_t)D);
+    }
+  }
+  free(a);
+  free(b);
+  return err;
+}
+
 /* ------------------------------------------------------- attention ---- */
 
 typedef struct {

@@ -259,6 +259,128 @@ def test_theta_pitfall_changes_cache():
     assert not np.array_equal(outs[0], outs[1])
 
 
+# --------------------------------- qkv bias, Qwen3 per-head RMSNorm ----
+
+def test_bias_add_rounds_once_to_nearest_even():
+    one = bf16_of([1.0])[0]
+    assert one == 0x3F80
+    # 1 + 2^-8 is half an ulp above 1.0: ties to even -> 1.0
+    assert oracle.add_bias_head(np.array([one]), bf16_of([2.0 ** -8]))[0] == 0x3F80
+    # 1 + 3 * 2^-8 is halfway between 1 + 2^-7 and 1 + 2^-6: even -> 1 + 2^-6
+    assert oracle.add_bias_head(np.array([one]), bf16_of([3 * 2.0 ** -8]))[0] == 0x3F82
+    g = torch.Generator().manual_seed(11)
+    x = u16(torch.randn(300, generator=g).to(torch.bfloat16))
+    assert np.array_equal(oracle.add_bias_head(x, np.zeros_like(x)), x)      # zero bias
+    neg = x ^ np.uint16(0x8000)                                              # b = -x
+    assert np.all(f64(oracle.add_bias_head(x, neg)) == 0.0)
+    # against fp64 addition then bf16 rounding (exact sums for these values)
+    b = u16(torch.randn(300, generator=g).to(torch.bfloat16))
+    assert np.array_equal(oracle.add_bias_head(x, b), bf16_of(f64(x) + f64(b)))
+
+
+def test_rmsnorm_closed_forms():
+    D = 128
+    w1 = bf16_of(np.ones(D))
+    two = bf16_of(np.full(D, 2.0))
+    # constant 2.0: mean(x^2) = 4, r = 1/2 exactly, y = 1.0 exactly
+    assert np.all(f64(oracle.rmsnorm_head(two, w1, 0.0)) == 1.0)
+    # ... and y_i = w_i exactly for any weights
+    g = torch.Generator().manual_seed(12)
+    w = u16(torch.randn(D, generator=g).to(torch.bfloat16))
+    assert np.array_equal(oracle.rmsnorm_head(two, w, 0.0), w)
+    # sign is kept per element
+    alt = bf16_of(np.where(np.arange(D) % 2 == 0, 2.0, -2.0))
+    assert np.array_equal(f64(oracle.rmsnorm_head(alt, w1, 0.0)),
+                          np.where(np.arange(D) % 2 == 0, 1.0, -1.0))
+    # the zero vector stays zero with eps > 0 (no 0/0)
+    z = np.zeros(D, np.uint16)
+    assert np.all(f64(oracle.rmsnorm_head(z, w1, 1e-6)) == 0.0)
+
+
+def test_rmsnorm_scale_invariance_and_unit_rms():
+    D = 128
+    g = torch.Generator().manual_seed(13)
+    x = torch.randn(D, generator=g).to(torch.bfloat16)
+    w1 = bf16_of(np.ones(D))
+    y = oracle.rmsnorm_head(u16(x), w1, 0.0)
+    for k in (-6, -1, 3, 9):          # power-of-two scaling is exact in bf16 and fp32
+        assert np.array_equal(oracle.rmsnorm_head(u16(x * (2.0 ** k)), w1, 0.0), y)
+    yv = f64(y)
+    assert abs(np.sqrt(np.mean(yv * yv)) - 1.0) < 4e-3       # unit RMS up to bf16 rounding
+    # the defining formula in fp64, within one bf16 rounding of the output
+    xv = f64(u16(x))
+    wv = f64(u16(torch.randn(D, generator=g).to(torch.bfloat16)))
+    ref = xv / np.sqrt(np.mean(xv * xv) + 1e-6) * wv
+    got = f64(oracle.rmsnorm_head(u16(x), bf16_of(wv), 1e-6))
+    assert np.all(np.abs(got - ref) <= np.abs(ref) * 2.0 ** -8 + 1e-30)
+
+
+def test_append_ex_without_extras_equals_append():
+    w = W.build(0)
+    a_qkv, a_kc, a_vc = u16(w.qkv), u16(w.k_cache), u16(w.v_cache)
+    b_qkv, b_kc, b_vc = a_qkv.copy(), a_kc.copy(), a_vc.copy()
+    table = oracle.rope_table(1e6, w.max_pos, 128)
+    e1 = oracle.rope_cache_append(a_qkv, w.positions, w.slot_mapping, a_kc, a_vc, table,
+                                  16, 8, 128, 16)
+    e2 = oracle.rope_cache_append_ex(b_qkv, w.positions, w.slot_mapping, b_kc, b_vc, table,
+                                     16, 8, 128, 16)
+    assert e1 == e2 == 0
+    assert np.array_equal(a_qkv, b_qkv) and np.array_equal(a_kc, b_kc)
+    assert np.array_equal(a_vc, b_vc)
+
+
+def test_append_ex_bias_goes_to_the_right_head():
+    """A bias that is nonzero only on kv head 1 of k changes only that head
+    in the cache, by bias-then-rope of the raw k."""
+    H, Hkv, D, BS = 4, 2, 128, 16
+    g = torch.Generator().manual_seed(14)
+    qkv0 = u16(torch.randn(3, (H + 2 * Hkv) * D, generator=g).to(torch.bfloat16))
+    pos = np.array([0, 7, 30], np.int32)
+    slots = np.array([3, 20, 41], np.int32)
+    table = oracle.rope_table(1e6, 64, D)
+    bias = np.zeros((H + 2 * Hkv) * D, np.uint16)
+    bias[(H + 1) * D:(H + 2) * D] = bf16_of(np.linspace(-1, 1, D))
+    runs = []
+    for bb in (None, bias):
+        qkv = qkv0.copy()
+        kc = np.full((3, Hkv, BS, D), W.SENTINEL_BF16, np.uint16)
+        vc = kc.copy()
+        assert oracle.rope_cache_append_ex(qkv, pos, slots, kc, vc, table, H, Hkv, D, BS,
+                                           bias=bb) == 0
+        runs.append((qkv, kc, vc))
+    (q0, k0, v0), (q1, k1, v1) = runs
+    assert np.array_equal(q0, q1) and np.array_equal(v0, v1)
+    assert np.array_equal(k0[:, 0], k1[:, 0])
+    for t in range(3):
+        blk, off = divmod(int(slots[t]), BS)
+        kin = qkv0[t, (H + 1) * D:(H + 2) * D]
+        want = oracle.rope_head_exact(oracle.add_bias_head(kin, bias[(H + 1) * D:(H + 2) * D]),
+                                      table[pos[t]])
+        assert np.array_equal(k1[blk, 1, off], want)
+
+
+def test_append_ex_norm_then_rope_has_unit_rms():
+    """With unit weights, a normalised head rotated by RoPE keeps RMS 1 (RoPE
+    preserves the norm), for q in place and k in the cache."""
+    H, Hkv, D, BS = 2, 1, 128, 16
+    g = torch.Generator().manual_seed(15)
+    qkv = u16((3.0 * torch.randn(2, (H + 2 * Hkv) * D, generator=g)).to(torch.bfloat16))
+    kc = np.full((1, Hkv, BS, D), W.SENTINEL_BF16, np.uint16)
+    vc = kc.copy()
+    table = oracle.rope_table(1e6, 100, D)
+    w1 = bf16_of(np.ones(D))
+    assert oracle.rope_cache_append_ex(qkv, np.array([17, 90], np.int32),
+                                       np.array([4, 9], np.int32), kc, vc, table, H, Hkv, D,
+                                       BS, q_norm_w=w1, k_norm_w=w1, eps=1e-6) == 0
+    for t in range(2):
+        for h in range(H):
+            y = f64(qkv[t, h * D:(h + 1) * D])
+            assert abs(np.sqrt(np.mean(y * y)) - 1.0) < 8e-3
+    for off in (4, 9):
+        y = f64(kc[0, 0, off])
+        assert abs(np.sqrt(np.mean(y * y)) - 1.0) < 8e-3
+
+
 # --------------------------------------------------------- attention ----
 
 def _run_workload(w, theta=1e6, partition=0):
