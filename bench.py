@@ -53,6 +53,9 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-clocks", action="store_true")
+    p.add_argument("--extras", choices=["none", "bias", "qknorm", "both"], default="none",
+                   help="add the qkv projection bias and/or the Qwen3 q/k RMSNorms to the "
+                        "RoPE + append step (synthetic weights)")
     return p.parse_args()
 
 
@@ -241,9 +244,23 @@ def run_ours(args, dist: Dist):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    gx = torch.Generator().manual_seed(W.SEED_BASE + 77)
+    bias = qn = kn = None
+    if args.extras in ("bias", "both"):
+        bias = (0.5 * torch.randn((H + 2 * Hkv) * D, generator=gx)).to(torch.bfloat16).to(dev)
+    if args.extras in ("qknorm", "both"):
+        qn = (1.0 + 0.2 * torch.randn(D, generator=gx)).to(torch.bfloat16).to(dev)
+        kn = (1.0 + 0.2 * torch.randn(D, generator=gx)).to(torch.bfloat16).to(dev)
+
     def append():
-        Q.qattn_rope_cache_append(g.q_view(), g.k_view(), g.v_view(), g.positions, g.slot_mapping,
-                                  g.k_cache, g.v_cache, table, dims, err)
+        if args.extras == "none":
+            Q.qattn_rope_cache_append(g.q_view(), g.k_view(), g.v_view(), g.positions,
+                                      g.slot_mapping, g.k_cache, g.v_cache, table, dims, err)
+        else:
+            Q.qattn_rope_cache_append_ex(g.q_view(), g.k_view(), g.v_view(), g.positions,
+                                         g.slot_mapping, g.k_cache, g.v_cache, table, dims,
+                                         qkv_bias=bias, q_norm_weight=qn, k_norm_weight=kn,
+                                         err_word=err)
 
     def attend():
         if prefix:
@@ -365,6 +382,7 @@ def run_ours(args, dist: Dist):
                    "head_dim": D, "block_size": BS, "batch": w.num_seqs,
                    "new_tokens": w.num_tokens, "kv_bytes_per_step": kv_bytes,
                    "max_context_len": max_ctx, "l2": "flushed before every timed step (512 MB write)",
+                   "append_extras": args.extras,
                    "parallelism": f"replicas x{dist.world}"},
         "seqs_per_s": round(seqs_per_s, 1),
         "tokens_per_s": round(tokens_per_s, 1),

@@ -130,6 +130,34 @@ int qattn_rope_cache_append(void* q, int64_t q_row_stride, const void* k,
                             const float* cos_sin, int32_t max_pos,
                             qattn_dims dims, int32_t* err_word, void* stream);
 
+/* qattn_rope_cache_append with two optional steps before the rotation, for
+ * the layers whose projection output has not had them yet:
+ *   qkv_bias       [(H + 2 Hkv) * head_dim] bf16 (q heads, then k, then v),
+ *                  or NULL: x' = bf16(x + b), one rounding (the Qwen2 qkv
+ *                  projection's bias=True, "Qwen2大模型架构解析与vLLM优化实践";
+ *                  v too);
+ *   q_norm_weight, k_norm_weight  [head_dim] bf16, or NULL: the Qwen3
+ *                  attention's per-head RMSNorm of q and of k (nano-vllm Qwen3
+ *                  skeleton page, module tree q_norm / k_norm), applied after
+ *                  the bias: ss = the sum of squares of the head in fp32,
+ *                  slice p = dims 8p .. 8p+7 then 64+8p .. 64+8p+7 summed in
+ *                  order, the 8 slice sums as ((s0+s1)+(s2+s3))+((s4+s5)+
+ *                  (s6+s7)); v = fp32(ss / head_dim + norm_eps), r = 1 /
+ *                  sqrt(v) (correctly rounded fp32), y = bf16(fp32(fp32(x *
+ *                  r) * w)), every fp32 step rounded, no fused multiply-add;
+ *   norm_eps       rms_norm_eps (1e-6 for Qwen2/Qwen3), 0 <= eps < 1.
+ * The cache stays bit-reproducible.  Pointers must be 16-byte aligned.
+ * Same errors as qattn_rope_cache_append. */
+int qattn_rope_cache_append_ex(void* q, int64_t q_row_stride, const void* k,
+                               int64_t k_row_stride, const void* v,
+                               int64_t v_row_stride, const int32_t* positions,
+                               const int32_t* slot_mapping, int32_t num_tokens,
+                               void* k_cache, void* v_cache, int32_t num_blocks,
+                               const float* cos_sin, int32_t max_pos,
+                               const void* qkv_bias, const void* q_norm_weight,
+                               const void* k_norm_weight, float norm_eps,
+                               qattn_dims dims, int32_t* err_word, void* stream);
+
 /* Bytes of device workspace qattn_paged_decode needs (256-byte aligned
  * pointer, contents need not be initialised).  Depends only on the
  * arguments.  The workspace holds the split-KV partial results between the

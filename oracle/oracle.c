@@ -194,19 +194,38 @@ void oracle_add_bias_head(const uint16_t* x, const uint16_t* b, int32_t n, uint1
 /* RMSNorm of one head vector with a per-dimension weight (the Qwen3
  * attention's q_norm / k_norm, nano-vllm Qwen3 skeleton page, module tree;
  * eps = rms_norm_eps): y_i = x_i / sqrt(mean(x^2) + eps) * w_i.  Reading,
- * as a bf16 tensor op: the sum of squares in fp64 (exact for bf16 inputs
- * whose magnitudes span less than 2^18, so the summation order does not
- * matter); v = fp32(mean + eps) rounded once; r = 1 / sqrt(v) with
- * correctly rounded fp32 sqrt and division; y_i = bf16(fp32(fp32(x_i * r) *
- * w_i)). */
+ * as a bf16 tensor op with fp32 arithmetic, every product and sum rounded
+ * (no fused multiply-add): the head's n values are taken as 8 slices, slice
+ * p = values 8p .. 8p+7 followed by values n/2+8p .. n/2+8p+7 (n = 128);
+ * each slice's squares are summed in that order, the 8 slice sums are added
+ * as the tree ((s0+s1)+(s2+s3))+((s4+s5)+(s6+s7)); v = fp32(ss/n + eps);
+ * r = 1 / sqrt(v) with correctly rounded sqrt and division;
+ * y_i = bf16(fp32(fp32(x_i * r) * w_i)).  n must be 128 (16 values a
+ * slice). */
 void oracle_rmsnorm_head(const uint16_t* x, const uint16_t* w, int32_t n, double eps,
                          uint16_t* y) {
-  double ss = 0.0;
-  for (int32_t i = 0; i < n; ++i) {
-    double xi = bf16_to_f64(x[i]);
-    ss += xi * xi;
+  const int32_t half = n / 2;
+  float part[8];
+  for (int32_t p = 0; p < 8; ++p) {
+    float acc = 0.0f;
+    for (int32_t j = 0; j < 8; ++j) {
+      float v = bf16_to_f32(x[8 * p + j]);
+      float sq = v * v;
+      acc = acc + sq;
+    }
+    for (int32_t j = 0; j < 8; ++j) {
+      float v = bf16_to_f32(x[half + 8 * p + j]);
+      float sq = v * v;
+      acc = acc + sq;
+    }
+    part[p] = acc;
   }
-  float v = (float)(ss / (double)n + eps);
+  float t01 = part[0] + part[1], t23 = part[2] + part[3];
+  float t45 = part[4] + part[5], t67 = part[6] + part[7];
+  float u0 = t01 + t23, u1 = t45 + t67;
+  float ss = u0 + u1;
+  float mean = ss * (1.0f / (float)n);
+  float v = mean + (float)eps;
   float r = 1.0f / sqrtf(v);
   for (int32_t i = 0; i < n; ++i) {
     float t = bf16_to_f32(x[i]) * r;

@@ -214,11 +214,14 @@ int qattn_rope_table_build(float* host_cos_sin, int32_t max_pos, int32_t head_di
   return QATTN_OK;
 }
 
-int qattn_rope_cache_append(void* q, int64_t q_row_stride, const void* k, int64_t k_row_stride,
-                            const void* v, int64_t v_row_stride, const int32_t* positions,
-                            const int32_t* slot_mapping, int32_t num_tokens, void* k_cache,
-                            void* v_cache, int32_t num_blocks, const float* cos_sin,
-                            int32_t max_pos, qattn_dims dims, int32_t* err_word, void* stream) {
+int qattn_rope_cache_append_ex(void* q, int64_t q_row_stride, const void* k,
+                               int64_t k_row_stride, const void* v, int64_t v_row_stride,
+                               const int32_t* positions, const int32_t* slot_mapping,
+                               int32_t num_tokens, void* k_cache, void* v_cache,
+                               int32_t num_blocks, const float* cos_sin, int32_t max_pos,
+                               const void* qkv_bias, const void* q_norm_weight,
+                               const void* k_norm_weight, float norm_eps, qattn_dims dims,
+                               int32_t* err_word, void* stream) {
   int st = check_dims(dims);
   if (st != QATTN_OK) return st;
   if (num_tokens < 0) return QATTN_ERR_INVALID_ARG;
@@ -231,6 +234,11 @@ int qattn_rope_cache_append(void* q, int64_t q_row_stride, const void* k, int64_
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(cos_sin))
     return QATTN_ERR_INVALID_ARG;
   if (q_row_stride % 8 || k_row_stride % 8 || v_row_stride % 8) return QATTN_ERR_INVALID_ARG;
+  if (!aligned16(qkv_bias) || !aligned16(q_norm_weight) || !aligned16(k_norm_weight))
+    return QATTN_ERR_INVALID_ARG;
+  if ((q_norm_weight != nullptr || k_norm_weight != nullptr) &&
+      !(norm_eps >= 0.0f && norm_eps < 1.0f))
+    return QATTN_ERR_INVALID_ARG;
   if (q_row_stride < static_cast<int64_t>(dims.num_heads) * kHeadDim ||
       k_row_stride < static_cast<int64_t>(dims.num_kv_heads) * kHeadDim ||
       v_row_stride < static_cast<int64_t>(dims.num_kv_heads) * kHeadDim)
@@ -253,7 +261,22 @@ int qattn_rope_cache_append(void* q, int64_t q_row_stride, const void* k, int64_
   a.num_heads = dims.num_heads;
   a.num_kv_heads = dims.num_kv_heads;
   a.err_word = err_word;
+  a.bias = qkv_bias;
+  a.q_norm_w = q_norm_weight;
+  a.k_norm_w = k_norm_weight;
+  a.norm_eps = norm_eps;
   return cuda_status(launch_rope_append(a, static_cast<cudaStream_t>(stream)));
+}
+
+int qattn_rope_cache_append(void* q, int64_t q_row_stride, const void* k, int64_t k_row_stride,
+                            const void* v, int64_t v_row_stride, const int32_t* positions,
+                            const int32_t* slot_mapping, int32_t num_tokens, void* k_cache,
+                            void* v_cache, int32_t num_blocks, const float* cos_sin,
+                            int32_t max_pos, qattn_dims dims, int32_t* err_word, void* stream) {
+  return qattn_rope_cache_append_ex(q, q_row_stride, k, k_row_stride, v, v_row_stride,
+                                    positions, slot_mapping, num_tokens, k_cache, v_cache,
+                                    num_blocks, cos_sin, max_pos, nullptr, nullptr, nullptr,
+                                    0.0f, dims, err_word, stream);
 }
 
 int qattn_paged_decode_kernel(qattn_dims dims) {

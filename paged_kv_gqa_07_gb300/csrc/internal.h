@@ -75,6 +75,13 @@ struct RopeAppendArgs {
   int32_t num_heads;
   int32_t num_kv_heads;
   int32_t* err_word;
+  // Optional steps before RoPE (null: skipped): the qkv projection bias
+  // [(H + 2 Hkv) * 128] bf16, and Qwen3's per-head RMSNorm weights [128]
+  // bf16 for q and for k, with eps.
+  const void* bias;
+  const void* q_norm_w;
+  const void* k_norm_w;
+  float norm_eps;
 };
 cudaError_t launch_rope_append(const RopeAppendArgs& a, cudaStream_t stream);
 

@@ -17,6 +17,15 @@
 // The rotation is evaluated with explicitly rounded fp32 operations
 // (__fmul_rn / __fsub_rn / __fadd_rn, no contraction into FMA) and rounded
 // to bf16 nearest-even, so the cache contents are bit-reproducible.
+//
+// Optional steps before RoPE (the Qwen2 qkv projection's bias=True,
+// "Qwen2大模型架构解析与vLLM优化实践"; the Qwen3 attention's q_norm / k_norm
+// RMSNorms, nano-vllm Qwen3 skeleton page, module tree), each a bf16 tensor
+// operation: x' = bf16(x + b) rounded once; RMSNorm over the head's 128
+// values with the sum of squares in fp32 in a fixed order (8 slices of 16,
+// then a pairwise tree -- see rmsnorm_group), v = fp32(mean + eps),
+// r = 1 / sqrt(v) with correctly rounded fp32 sqrt and division,
+// y = bf16(fp32(fp32(x * r) * w)).
 #include "common.cuh"
 #include "internal.h"
 
@@ -47,6 +56,63 @@ __device__ __forceinline__ void rotate8(const uint4& x1, const uint4& x2, const 
   }
 }
 
+// 8 bf16 + 8 bf16 -> 8 bf16, each sum rounded once.
+__device__ __forceinline__ uint4 add_bias8(const uint4& x, const __nv_bfloat16* b) {
+  const uint4 bb = *reinterpret_cast<const uint4*>(b);
+  const uint32_t* xs = reinterpret_cast<const uint32_t*>(&x);
+  const uint32_t* bs = reinterpret_cast<const uint32_t*>(&bb);
+  uint4 y;
+  uint32_t* ys = reinterpret_cast<uint32_t*>(&y);
+#pragma unroll
+  for (int w = 0; w < 4; ++w)
+    ys[w] = pack_bf16x2_rn(__fadd_rn(bf16lo_to_f32(xs[w]), bf16lo_to_f32(bs[w])),
+                           __fadd_rn(bf16hi_to_f32(xs[w]), bf16hi_to_f32(bs[w])));
+  return y;
+}
+
+// RMSNorm of one head whose 128 values are spread over the 8 lanes of an
+// aligned lane group (x1: dims 8p .. 8p+7, x2: dims 64+8p .. 64+8p+7 of
+// lane p of the group).  Sum of squares in fp32, each step rounded: lane p
+// adds its 16 squares in dimension order, then the butterfly over the group
+// forms ((s0+s1)+(s2+s3))+((s4+s5)+(s6+s7)) in every lane.
+__device__ __forceinline__ void rmsnorm_group(uint4& x1, uint4& x2, const __nv_bfloat16* w,
+                                              int part, float eps) {
+  const uint32_t mask = 0xffu << ((threadIdx.x & 31) & 24);
+  uint32_t* u1 = reinterpret_cast<uint32_t*>(&x1);
+  uint32_t* u2 = reinterpret_cast<uint32_t*>(&x2);
+  float ss = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float a = bf16lo_to_f32(u1[i]), b = bf16hi_to_f32(u1[i]);
+    ss = __fadd_rn(ss, __fmul_rn(a, a));
+    ss = __fadd_rn(ss, __fmul_rn(b, b));
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float c = bf16lo_to_f32(u2[i]), d = bf16hi_to_f32(u2[i]);
+    ss = __fadd_rn(ss, __fmul_rn(c, c));
+    ss = __fadd_rn(ss, __fmul_rn(d, d));
+  }
+  ss = __fadd_rn(ss, __shfl_xor_sync(mask, ss, 1));
+  ss = __fadd_rn(ss, __shfl_xor_sync(mask, ss, 2));
+  ss = __fadd_rn(ss, __shfl_xor_sync(mask, ss, 4));
+  const float v = __fadd_rn(__fmul_rn(ss, 1.0f / 128.0f), eps);
+  const float r = __fdiv_rn(1.0f, __fsqrt_rn(v));
+  const uint4 w1 = *reinterpret_cast<const uint4*>(w + part * 8);
+  const uint4 w2 = *reinterpret_cast<const uint4*>(w + 64 + part * 8);
+  const uint32_t* ws1 = reinterpret_cast<const uint32_t*>(&w1);
+  const uint32_t* ws2 = reinterpret_cast<const uint32_t*>(&w2);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    u1[i] = pack_bf16x2_rn(__fmul_rn(__fmul_rn(bf16lo_to_f32(u1[i]), r), bf16lo_to_f32(ws1[i])),
+                           __fmul_rn(__fmul_rn(bf16hi_to_f32(u1[i]), r), bf16hi_to_f32(ws1[i])));
+    u2[i] = pack_bf16x2_rn(__fmul_rn(__fmul_rn(bf16lo_to_f32(u2[i]), r), bf16lo_to_f32(ws2[i])),
+                           __fmul_rn(__fmul_rn(bf16hi_to_f32(u2[i]), r), bf16hi_to_f32(ws2[i])));
+  }
+}
+
+// kExtras: bias and/or norms present (the plain step compiles without them).
+template <bool kExtras>
 __global__ void __launch_bounds__(kThreads) rope_append_kernel(RopeAppendArgs a,
                                                                int tasks_per_token) {
   // A following decode kernel may start its set-up now; it reads nothing
@@ -92,23 +158,41 @@ __global__ void __launch_bounds__(kThreads) rope_append_kernel(RopeAppendArgs a,
       s[0] = s0.x; s[1] = s0.y; s[2] = s0.z; s[3] = s0.w;
       s[4] = s1.x; s[5] = s1.y; s[6] = s1.z; s[7] = s1.w;
     }
+    // bias and norm first (head = q head h, or H + kv head g: also the
+    // head's row in the bias)
+    const __nv_bfloat16* bias =
+        kExtras && a.bias
+            ? static_cast<const __nv_bfloat16*>(a.bias) + static_cast<int64_t>(head) * kHeadDim
+            : nullptr;
     if (head < H) {
       __nv_bfloat16* src = static_cast<__nv_bfloat16*>(a.q) + t * a.q_row_stride +
                            static_cast<int64_t>(head) * kHeadDim;
       uint4* p1 = reinterpret_cast<uint4*>(src + part * 8);
       uint4* p2 = reinterpret_cast<uint4*>(src + 64 + part * 8);
-      const uint4 x1 = *p1, x2 = *p2;
+      uint4 x1 = *p1, x2 = *p2;
+      if (bias) {
+        x1 = add_bias8(x1, bias + part * 8);
+        x2 = add_bias8(x2, bias + 64 + part * 8);
+      }
+      if (kExtras && a.q_norm_w)
+        rmsnorm_group(x1, x2, static_cast<const __nv_bfloat16*>(a.q_norm_w), part, a.norm_eps);
       uint4 y1, y2;
       rotate8(x1, x2, c, s, y1, y2);
       *p1 = y1;
       *p2 = y2;
     } else {
-      if (!write_cache) return;
+      if (!write_cache) return;  // the whole lane group: same token
       const int g = head - H;
       const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(a.k) + t * a.k_row_stride +
                                  static_cast<int64_t>(g) * kHeadDim;
-      const uint4 x1 = *reinterpret_cast<const uint4*>(src + part * 8);
-      const uint4 x2 = *reinterpret_cast<const uint4*>(src + 64 + part * 8);
+      uint4 x1 = *reinterpret_cast<const uint4*>(src + part * 8);
+      uint4 x2 = *reinterpret_cast<const uint4*>(src + 64 + part * 8);
+      if (bias) {
+        x1 = add_bias8(x1, bias + part * 8);
+        x2 = add_bias8(x2, bias + 64 + part * 8);
+      }
+      if (kExtras && a.k_norm_w)
+        rmsnorm_group(x1, x2, static_cast<const __nv_bfloat16*>(a.k_norm_w), part, a.norm_eps);
       uint4 y1, y2;
       rotate8(x1, x2, c, s, y1, y2);
       __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.k_cache) + cache_row +
@@ -124,7 +208,11 @@ __global__ void __launch_bounds__(kThreads) rope_append_kernel(RopeAppendArgs a,
                                static_cast<int64_t>(g) * kHeadDim;
     __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.v_cache) + cache_row +
                          static_cast<int64_t>(g) * kBlockSize * kHeadDim;
-    *reinterpret_cast<uint4*>(dst + part * 8) = *reinterpret_cast<const uint4*>(src + part * 8);
+    uint4 x = *reinterpret_cast<const uint4*>(src + part * 8);
+    if (kExtras && a.bias)
+      x = add_bias8(x, static_cast<const __nv_bfloat16*>(a.bias) +
+                           static_cast<int64_t>(H + Hkv + g) * kHeadDim + part * 8);
+    *reinterpret_cast<uint4*>(dst + part * 8) = x;
   }
 }
 
@@ -135,7 +223,12 @@ cudaError_t launch_rope_append(const RopeAppendArgs& a, cudaStream_t stream) {
   const int64_t total = static_cast<int64_t>(a.num_tokens) * tasks_per_token;
   const int64_t blocks = (total + kThreads - 1) / kThreads;
   if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
-  rope_append_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(a, tasks_per_token);
+  if (a.bias != nullptr || a.q_norm_w != nullptr || a.k_norm_w != nullptr)
+    rope_append_kernel<true><<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(
+        a, tasks_per_token);
+  else
+    rope_append_kernel<false><<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(
+        a, tasks_per_token);
   return cudaPeekAtLastError();
 }
 

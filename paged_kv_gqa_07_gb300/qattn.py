@@ -37,6 +37,7 @@ EXPORTED = [
     "qattn_version",
     "qattn_rope_table_build",
     "qattn_rope_cache_append",
+    "qattn_rope_cache_append_ex",
     "qattn_paged_decode_kernel",
     "qattn_paged_decode_workspace_size",
     "qattn_paged_decode",
@@ -92,6 +93,10 @@ def load_library(path: str | None = None):
         L.qattn_rope_cache_append.argtypes = [
             _P, _I64, _P, _I64, _P, _I64, _P, _P, _I32, _P, _P, _I32, _P, _I32, qattn_dims, _P, _P]
         L.qattn_rope_cache_append.restype = ctypes.c_int
+        L.qattn_rope_cache_append_ex.argtypes = [
+            _P, _I64, _P, _I64, _P, _I64, _P, _P, _I32, _P, _P, _I32, _P, _I32, _P, _P, _P,
+            ctypes.c_float, qattn_dims, _P, _P]
+        L.qattn_rope_cache_append_ex.restype = ctypes.c_int
         L.qattn_paged_decode_kernel.argtypes = [qattn_dims]
         L.qattn_paged_decode_kernel.restype = ctypes.c_int
         L.qattn_paged_decode_workspace_size.argtypes = [_I32, _I32, qattn_dims]
@@ -180,6 +185,26 @@ def qattn_rope_cache_append(q, k, v, positions, slot_mapping, k_cache, v_cache, 
         int(k_cache.shape[0]), _dev_ptr(cos_sin, "cos_sin", torch.float32), int(cos_sin.shape[0]),
         dims, _dev_ptr(err_word, "err_word", torch.int32), _stream(stream))
     _check("qattn_rope_cache_append", rc)
+
+
+def qattn_rope_cache_append_ex(q, k, v, positions, slot_mapping, k_cache, v_cache, cos_sin, dims,
+                               qkv_bias=None, q_norm_weight=None, k_norm_weight=None,
+                               norm_eps=1e-6, err_word=None, stream=None):
+    """qattn_rope_cache_append with the qkv projection bias and the Qwen3
+    per-head q/k RMSNorms applied before the rotation (None skips a step)."""
+    qp, qs = _rows(q, "q")
+    kp, ks = _rows(k, "k")
+    vp, vs = _rows(v, "v")
+    rc = lib().qattn_rope_cache_append_ex(
+        qp, qs, kp, ks, vp, vs, _dev_ptr(positions, "positions", torch.int32),
+        _dev_ptr(slot_mapping, "slot_mapping", torch.int32), int(positions.shape[0]),
+        _dev_ptr(k_cache, "k_cache", torch.bfloat16), _dev_ptr(v_cache, "v_cache", torch.bfloat16),
+        int(k_cache.shape[0]), _dev_ptr(cos_sin, "cos_sin", torch.float32), int(cos_sin.shape[0]),
+        _dev_ptr(qkv_bias, "qkv_bias", torch.bfloat16),
+        _dev_ptr(q_norm_weight, "q_norm_weight", torch.bfloat16),
+        _dev_ptr(k_norm_weight, "k_norm_weight", torch.bfloat16), float(norm_eps), dims,
+        _dev_ptr(err_word, "err_word", torch.int32), _stream(stream))
+    _check("qattn_rope_cache_append_ex", rc)
 
 
 QATTN_DECODE_CUDA_CORE = 0
