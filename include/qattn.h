@@ -103,6 +103,29 @@ int qattn_version(void);
 int qattn_rope_table_build(float* host_cos_sin, int32_t max_pos,
                            int32_t head_dim, double theta);
 
+/* The same table with rope_scaling ("Qwen2大模型架构解析与vLLM优化实践"
+ * section 7.1: rope_scaling = {type, factor, original_max_position}):
+ *   QATTN_ROPE_SCALING_NONE     the table above;
+ *   QATTN_ROPE_SCALING_LINEAR   position interpolation: angle =
+ *                               (pos / factor) * theta^(-2i/D);
+ *   QATTN_ROPE_SCALING_DYNAMIC  dynamic NTK: when max_pos exceeds
+ *                               original_max_position the base becomes
+ *                               theta * (factor * max_pos /
+ *                               original_max_position - (factor - 1))
+ *                               ^ (D / (D - 2)); otherwise unchanged.  max_pos
+ *                               stands for the batch's sequence-length bound
+ *                               (a longer batch builds a new table).
+ * Angles in fp64, rounded to fp32.  QATTN_ERR_INVALID_ARG for a null pointer,
+ * max_pos <= 0, head_dim odd or <= 2, theta <= 0, an unknown scaling,
+ * factor < 1, or a dynamic table without original_max_position > 0. */
+#define QATTN_ROPE_SCALING_NONE 0
+#define QATTN_ROPE_SCALING_LINEAR 1
+#define QATTN_ROPE_SCALING_DYNAMIC 2
+int qattn_rope_table_build_scaled(float* host_cos_sin, int32_t max_pos,
+                                  int32_t head_dim, double theta,
+                                  int32_t scaling, double factor,
+                                  int32_t original_max_position);
+
 /* Step 1 + 2: rotate-half RoPE and cache append, one launch.
  *   q        [num_tokens, q_row_stride] bf16, rotated IN PLACE (heads
  *            0 .. num_heads-1 of each row);

@@ -10,6 +10,9 @@ What each function follows (pages named by title and section):
 * :func:`rope_table`   -- get_rope(head_dim, rotary_dim=head_dim, max_position,
   base=rope_theta) in "Qwen2大模型架构解析与vLLM优化实践" section 2.2, with
   rope_theta = 1e6 from "Qwen2 模型结构代码详解" section 2.
+* :func:`rope_table_scaled` -- the table with rope_scaling (linear, or
+  dynamic NTK: a raised base when the table covers more than the original
+  positions), "Qwen2大模型架构解析与vLLM优化实践" section 7.1.
 * :func:`rope_cache_append` -- rotate-half RoPE on q and k, then the write of
   k and v into fixed-size cache blocks through a slot mapping (PagedAttention
   block cache, vLLM-deploys-Qwen notes section 2.1; nano-vllm block_table and
@@ -80,6 +83,8 @@ def lib():
             L = ctypes.CDLL(path)
             L.oracle_rope_table.argtypes = [_F64, _I32, _I32, _P]
             L.oracle_rope_table.restype = ctypes.c_int
+            L.oracle_rope_table_scaled.argtypes = [_F64, _I32, _I32, _I32, _F64, _I32, _P]
+            L.oracle_rope_table_scaled.restype = ctypes.c_int
             L.oracle_rope_head_exact.argtypes = [_P, _I32, _P, _P]
             L.oracle_rope_head_exact.restype = None
             L.oracle_rope_head_f64.argtypes = [_P, _I32, _F64, _F64, _P]
@@ -148,6 +153,21 @@ def rope_table(theta: float, max_pos: int, head_dim: int) -> np.ndarray:
     """[max_pos, head_dim] fp32: cos in columns < D/2, sin in the rest."""
     out = np.empty((max_pos, head_dim), dtype=np.float32)
     rc = lib().oracle_rope_table(float(theta), int(max_pos), int(head_dim), _ptr(out))
+    if rc != 0:
+        raise ValueError("bad rope table arguments")
+    return out
+
+
+SCALING_NONE, SCALING_LINEAR, SCALING_DYNAMIC = 0, 1, 2
+
+
+def rope_table_scaled(theta: float, max_pos: int, head_dim: int, scaling: int,
+                      factor: float = 1.0, original_max: int = 0) -> np.ndarray:
+    """rope_table with rope_scaling: 0 none, 1 linear, 2 dynamic NTK."""
+    out = np.empty((max_pos, head_dim), dtype=np.float32)
+    rc = lib().oracle_rope_table_scaled(float(theta), int(max_pos), int(head_dim),
+                                        int(scaling), float(factor), int(original_max),
+                                        _ptr(out))
     if rc != 0:
         raise ValueError("bad rope table arguments")
     return out

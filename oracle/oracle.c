@@ -94,6 +94,43 @@ int oracle_rope_table(double theta, int32_t max_pos, int32_t head_dim,
   return 0;
 }
 
+/* RoPE tables with rope_scaling ("Qwen2大模型架构解析与vLLM优化实践" section
+ * 7.1, rope_scaling {type, factor, original_max_position}):
+ *   scaling 0: none (the table above);
+ *   scaling 1: linear -- positions divided by factor, angle = (pos/factor) *
+ *              theta^(-2i/D);
+ *   scaling 2: dynamic NTK -- the base is raised when the table must cover
+ *              more than original_max positions: for max_pos > original_max,
+ *              base = theta * (factor * max_pos / original_max - (factor - 1))
+ *              ^ (D / (D - 2)), else base = theta; angle = pos * base^(-2i/D).
+ *              The table's max_pos plays the current sequence-length bound
+ *              ("dynamic": a longer batch rebuilds its table).
+ * Angles in fp64, cos and sin rounded to fp32. */
+int oracle_rope_table_scaled(double theta, int32_t max_pos, int32_t head_dim,
+                             int32_t scaling, double factor, int32_t original_max,
+                             float* cos_sin) {
+  if (max_pos <= 0 || head_dim <= 2 || (head_dim & 1) || !(theta > 0.0)) return -1;
+  if (scaling < 0 || scaling > 2) return -1;
+  if (scaling != 0 && !(factor >= 1.0)) return -1;
+  if (scaling == 2 && original_max <= 0) return -1;
+  const int32_t half = head_dim / 2;
+  double base = theta;
+  if (scaling == 2 && max_pos > original_max) {
+    double s = factor * (double)max_pos / (double)original_max - (factor - 1.0);
+    base = theta * pow(s, (double)head_dim / (double)(head_dim - 2));
+  }
+  for (int32_t pos = 0; pos < max_pos; ++pos) {
+    double p = scaling == 1 ? (double)pos / factor : (double)pos;
+    for (int32_t i = 0; i < half; ++i) {
+      double inv_freq = pow(base, -(2.0 * (double)i) / (double)head_dim);
+      double angle = p * inv_freq;
+      cos_sin[(int64_t)pos * head_dim + i] = (float)cos(angle);
+      cos_sin[(int64_t)pos * head_dim + half + i] = (float)sin(angle);
+    }
+  }
+  return 0;
+}
+
 /* ------------------------------------------------------- RoPE apply ---- */
 
 /* Rotate-half on one head vector, fp32 recipe: for i < D/2,

@@ -214,6 +214,38 @@ int qattn_rope_table_build(float* host_cos_sin, int32_t max_pos, int32_t head_di
   return QATTN_OK;
 }
 
+int qattn_rope_table_build_scaled(float* host_cos_sin, int32_t max_pos, int32_t head_dim,
+                                  double theta, int32_t scaling, double factor,
+                                  int32_t original_max_position) {
+  if (host_cos_sin == nullptr || max_pos <= 0 || head_dim <= 2 || (head_dim & 1) ||
+      !(theta > 0.0))
+    return QATTN_ERR_INVALID_ARG;
+  if (scaling < QATTN_ROPE_SCALING_NONE || scaling > QATTN_ROPE_SCALING_DYNAMIC)
+    return QATTN_ERR_INVALID_ARG;
+  if (scaling != QATTN_ROPE_SCALING_NONE && !(factor >= 1.0)) return QATTN_ERR_INVALID_ARG;
+  if (scaling == QATTN_ROPE_SCALING_DYNAMIC && original_max_position <= 0)
+    return QATTN_ERR_INVALID_ARG;
+  const int32_t half = head_dim / 2;
+  double base = theta;
+  if (scaling == QATTN_ROPE_SCALING_DYNAMIC && max_pos > original_max_position) {
+    const double grow = factor * static_cast<double>(max_pos) / original_max_position -
+                        (factor - 1.0);
+    base = theta * pow(grow, static_cast<double>(head_dim) / (head_dim - 2));
+  }
+  for (int32_t i = 0; i < half; ++i) {
+    const double inv_freq = pow(base, -(2.0 * i) / head_dim);
+    for (int32_t pos = 0; pos < max_pos; ++pos) {
+      const double p =
+          scaling == QATTN_ROPE_SCALING_LINEAR ? static_cast<double>(pos) / factor : pos;
+      const double ang = p * inv_freq;
+      host_cos_sin[static_cast<int64_t>(pos) * head_dim + i] = static_cast<float>(cos(ang));
+      host_cos_sin[static_cast<int64_t>(pos) * head_dim + half + i] =
+          static_cast<float>(sin(ang));
+    }
+  }
+  return QATTN_OK;
+}
+
 int qattn_rope_cache_append_ex(void* q, int64_t q_row_stride, const void* k,
                                int64_t k_row_stride, const void* v, int64_t v_row_stride,
                                const int32_t* positions, const int32_t* slot_mapping,

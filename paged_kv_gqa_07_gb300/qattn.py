@@ -36,6 +36,7 @@ EXPORTED = [
     "qattn_status_string",
     "qattn_version",
     "qattn_rope_table_build",
+    "qattn_rope_table_build_scaled",
     "qattn_rope_cache_append",
     "qattn_rope_cache_append_ex",
     "qattn_paged_decode_kernel",
@@ -90,6 +91,9 @@ def load_library(path: str | None = None):
         L.qattn_version.restype = ctypes.c_int
         L.qattn_rope_table_build.argtypes = [_P, _I32, _I32, ctypes.c_double]
         L.qattn_rope_table_build.restype = ctypes.c_int
+        L.qattn_rope_table_build_scaled.argtypes = [_P, _I32, _I32, ctypes.c_double, _I32,
+                                                    ctypes.c_double, _I32]
+        L.qattn_rope_table_build_scaled.restype = ctypes.c_int
         L.qattn_rope_cache_append.argtypes = [
             _P, _I64, _P, _I64, _P, _I64, _P, _P, _I32, _P, _P, _I32, _P, _I32, qattn_dims, _P, _P]
         L.qattn_rope_cache_append.restype = ctypes.c_int
@@ -170,6 +174,21 @@ def qattn_rope_table_build(max_pos: int, head_dim: int, theta: float) -> torch.T
     out = torch.empty((max_pos, head_dim), dtype=torch.float32)
     _check("qattn_rope_table_build",
            lib().qattn_rope_table_build(out.data_ptr(), int(max_pos), int(head_dim), float(theta)))
+    return out
+
+
+QATTN_ROPE_SCALING_NONE, QATTN_ROPE_SCALING_LINEAR, QATTN_ROPE_SCALING_DYNAMIC = 0, 1, 2
+
+
+def qattn_rope_table_build_scaled(max_pos: int, head_dim: int, theta: float, scaling: int,
+                                  factor: float = 1.0, original_max_position: int = 0
+                                  ) -> torch.Tensor:
+    """Host-built table with rope_scaling (none, linear, dynamic NTK)."""
+    out = torch.empty((max_pos, head_dim), dtype=torch.float32)
+    _check("qattn_rope_table_build_scaled",
+           lib().qattn_rope_table_build_scaled(out.data_ptr(), int(max_pos), int(head_dim),
+                                               float(theta), int(scaling), float(factor),
+                                               int(original_max_position)))
     return out
 
 

@@ -60,12 +60,26 @@ def test_host_rope_table_full_length(lib):
     assert np.array_equal(t.view(np.uint32), o.view(np.uint32))
 
 
+@pytest.mark.parametrize("scaling,factor,orig,max_pos", [(0, 1.0, 0, 64), (1, 2.0, 0, 300),
+                                                        (1, 4.0, 0, 130), (2, 2.0, 100, 300),
+                                                        (2, 2.0, 4096, 300)])
+def test_host_scaled_table_equals_oracle(lib, scaling, factor, orig, max_pos):
+    t = Q.qattn_rope_table_build_scaled(max_pos, 128, 1e6, scaling, factor, orig).numpy()
+    o = oracle.rope_table_scaled(1e6, max_pos, 128, scaling, factor, orig)
+    assert np.array_equal(t.view(np.uint32), o.view(np.uint32))
+
+
 def test_table_build_rejects_bad_args(lib):
     buf = (ctypes.c_float * 16)()
     assert lib.qattn_rope_table_build(None, 4, 4, 1e6) == Q.QATTN_ERR_INVALID_ARG
     assert lib.qattn_rope_table_build(buf, 4, 3, 1e6) == Q.QATTN_ERR_INVALID_ARG
     assert lib.qattn_rope_table_build(buf, 0, 4, 1e6) == Q.QATTN_ERR_INVALID_ARG
     assert lib.qattn_rope_table_build(buf, 4, 4, -1.0) == Q.QATTN_ERR_INVALID_ARG
+    f = lib.qattn_rope_table_build_scaled
+    assert f(buf, 4, 4, 1e6, 3, 2.0, 10) == Q.QATTN_ERR_INVALID_ARG     # unknown scaling
+    assert f(buf, 4, 4, 1e6, 1, 0.5, 0) == Q.QATTN_ERR_INVALID_ARG      # factor < 1
+    assert f(buf, 4, 4, 1e6, 2, 2.0, 0) == Q.QATTN_ERR_INVALID_ARG      # dynamic, no original
+    assert f(buf, 4, 2, 1e6, 1, 2.0, 0) == Q.QATTN_ERR_INVALID_ARG      # head_dim 2
 
 
 def test_workspace_size_grows_with_context(lib):

@@ -103,3 +103,23 @@ def test_append_ex_rejects_bad_args():
         Q.qattn_rope_cache_append_ex(g.q_view(), g.k_view(), g.v_view(), g.positions,
                                      g.slot_mapping, g.k_cache, g.v_cache, r.table, r.dims,
                                      q_norm_weight=qn[1:], err_word=r.err)   # misaligned
+
+
+def test_append_with_dynamic_ntk_table():
+    """A dynamic-NTK table (factor 2, original 4096) covering 8192 positions:
+    the append is bit-exact against the oracle with the oracle's table."""
+    w = W.custom(16, 8, ctx=[8000, 5000, 4200, 300], q_lens=[3, 1, 2, 1], seed=520)
+    table_h = Q.qattn_rope_table_build_scaled(8192, 128, w.theta, Q.QATTN_ROPE_SCALING_DYNAMIC,
+                                              2.0, 4096)
+    to = oracle.rope_table_scaled(w.theta, 8192, 128, oracle.SCALING_DYNAMIC, 2.0, 4096)
+    assert np.array_equal(table_h.numpy().view(np.uint32), to.view(np.uint32))
+    qkv, kc, vc = u16(w.qkv), u16(w.k_cache), u16(w.v_cache)
+    e = oracle.rope_cache_append(qkv, w.positions, w.slot_mapping, kc, vc, to, 16, 8, 128, 16)
+    r = GpuRun(w)
+    g = r.g
+    Q.qattn_rope_cache_append(g.q_view(), g.k_view(), g.v_view(), g.positions, g.slot_mapping,
+                              g.k_cache, g.v_cache, table_h.to(r.dev), r.dims, r.err)
+    r.sync()
+    assert e == 0 and r.err_bits == 0
+    assert np.array_equal(u16(r.g.k_cache), kc) and np.array_equal(u16(r.g.v_cache), vc)
+    assert np.array_equal(u16(r.g.qkv), qkv)

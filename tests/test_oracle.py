@@ -259,6 +259,48 @@ def test_theta_pitfall_changes_cache():
     assert not np.array_equal(outs[0], outs[1])
 
 
+# ------------------------------------------------------- rope_scaling ----
+
+def test_scaled_table_reduces_to_plain():
+    plain = oracle.rope_table(1e6, 300, 128)
+    assert np.array_equal(oracle.rope_table_scaled(1e6, 300, 128, oracle.SCALING_NONE), plain)
+    assert np.array_equal(oracle.rope_table_scaled(1e6, 300, 128, oracle.SCALING_LINEAR, 1.0),
+                          plain)
+    # dynamic NTK leaves a table within the original length untouched
+    assert np.array_equal(
+        oracle.rope_table_scaled(1e6, 300, 128, oracle.SCALING_DYNAMIC, 2.0, 4096), plain)
+
+
+def test_linear_scaling_is_position_interpolation():
+    plain = oracle.rope_table(1e6, 400, 128)
+    for f in (2, 4):
+        t = oracle.rope_table_scaled(1e6, 400 * f, 128, oracle.SCALING_LINEAR, float(f))
+        assert np.array_equal(t[::f], plain)         # row f*k == plain row k, bit for bit
+
+
+def test_dynamic_ntk_base_closed_form():
+    """factor 2, original 4096, a table of 8192 rows: base' = theta * 3^(D/(D-2)).
+    Frequency 0 stays 1; the lowest frequency theta^(-(D-2)/D) is divided by
+    exactly (2 * 8192/4096 - 1) = 3."""
+    D, theta = 128, 1e6
+    t = oracle.rope_table_scaled(theta, 8192, D, oracle.SCALING_DYNAMIC, 2.0, 4096)
+    plain = oracle.rope_table(theta, 8192, D)
+    assert np.array_equal(t[:, 0], plain[:, 0])       # cos(pos) at frequency 1
+    lowest = theta ** (-(D - 2) / D)
+    ang = np.arctan2(t[1:50, D - 1].astype(np.float64), t[1:50, D // 2 - 1].astype(np.float64))
+    assert np.allclose(ang / np.arange(1, 50), lowest / 3.0, rtol=1e-5)
+    # and a longer table gets a larger base (lower frequency)
+    t2 = oracle.rope_table_scaled(theta, 16384, D, oracle.SCALING_DYNAMIC, 2.0, 4096)
+    assert t2[1, D - 1] < t[1, D - 1]
+
+
+def test_scaled_table_rejects_bad_args():
+    for args in [(1e6, 10, 128, 3, 2.0, 4096), (1e6, 10, 128, 1, 0.5, 0),
+                 (1e6, 10, 128, 2, 2.0, 0), (1e6, 10, 2, 1, 2.0, 0)]:
+        with pytest.raises(ValueError):
+            oracle.rope_table_scaled(*args)
+
+
 # --------------------------------- qkv bias, Qwen3 per-head RMSNorm ----
 
 def test_bias_add_rounds_once_to_nearest_even():
