@@ -39,7 +39,7 @@
  *     is skipped and a bit is OR-ed into *err_word (a device int32 that the
  *     caller zeroes; may be NULL).  Kernels never trap.  Outputs of a row
  *     that raised an error bit are unspecified.
- *   - Supported today: head_dim 128, block_size 16, num_heads a multiple of
+ *   - Supported today: head_dim 128, block_size 16, 32 or 64, num_heads a multiple of
  *     num_kv_heads with at most 8 query heads per KV head, num_heads <= 128.
  *     Anything else returns QATTN_ERR_UNSUPPORTED without launching.
  *   - A call with zero tokens / zero sequences returns QATTN_OK and launches
@@ -60,7 +60,7 @@ typedef struct qattn_dims {
   int32_t num_heads;    /* H: query heads */
   int32_t num_kv_heads; /* Hkv: key/value heads (GQA group = H / Hkv) */
   int32_t head_dim;     /* D (128) */
-  int32_t block_size;   /* tokens per cache block (16) */
+  int32_t block_size;   /* tokens per cache block (16, 32 or 64) */
   float scale;          /* softmax scale; <= 0 selects head_dim ** -0.5 */
 } qattn_dims;
 
@@ -194,8 +194,9 @@ size_t qattn_paged_decode_workspace_size(int32_t num_seqs,
  * qattn_varlen_prefill, and the shared-prefix decode) launches for these
  * dims: QATTN_DECODE_TENSOR_CORE (tcgen05 with the query group as the MMA N
  * dimension; the default for every group size) or QATTN_DECODE_CUDA_CORE
- * (the group's dot products on CUDA cores), selected by the environment
- * variable QATTN_DECODE_KERNEL=cuda (read once per process).  Returns -1
+ * (the group's dot products on CUDA cores; 16-token blocks only), selected
+ * by the environment variable QATTN_DECODE_KERNEL=cuda (read once per
+ * process) when block_size is 16.  Returns -1
  * for invalid dims. */
 #define QATTN_DECODE_CUDA_CORE 0
 #define QATTN_DECODE_TENSOR_CORE 1
@@ -236,9 +237,9 @@ size_t qattn_paged_decode_shared_prefix_workspace_size(int32_t num_seqs,
  * blocks of the PagedAttention cache, vLLM-deploys-Qwen notes section 2.1): tokens
  * 0 .. shared_prefix_len - 1 of EVERY sequence are the same cached tokens
  * in the same physical blocks, block_tables[b][j] == block_tables[0][j] for
- * j < shared_prefix_len / 16.  Same arguments and result as
+ * j < shared_prefix_len / block_size.  Same arguments and result as
  * qattn_paged_decode, plus
- *   shared_prefix_len  host, a multiple of 16, 0 <= it < every context_len
+ *   shared_prefix_len  host, a multiple of block_size, 0 <= it < every context_len
  *                      (0: plain decode), < max_context_len.
  * The prefix is attended once per kv head for the whole batch on tensor
  * cores (all sequences' query groups against the prefix tiles, split over

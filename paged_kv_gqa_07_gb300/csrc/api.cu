@@ -21,7 +21,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 int check_dims(const qattn_dims& d) {
   if (d.num_heads <= 0 || d.num_kv_heads <= 0 || d.head_dim <= 0 || d.block_size <= 0)
     return QATTN_ERR_INVALID_ARG;
-  if (d.head_dim != kHeadDim || d.block_size != kBlockSize) return QATTN_ERR_UNSUPPORTED;
+  if (d.head_dim != kHeadDim) return QATTN_ERR_UNSUPPORTED;
+  if (d.block_size != 16 && d.block_size != 32 && d.block_size != 64) return QATTN_ERR_UNSUPPORTED;
   if (d.num_heads % d.num_kv_heads != 0) return QATTN_ERR_UNSUPPORTED;
   if (d.num_heads / d.num_kv_heads > 8 || d.num_heads > 128) return QATTN_ERR_UNSUPPORTED;
   if (!(d.scale == d.scale) || isinf(d.scale)) return QATTN_ERR_INVALID_ARG;
@@ -71,27 +72,28 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// The paged cache [num_blocks][Hkv][16][128] bf16 seen as a 4-D tensor
-// (64 columns, 8 rows, 2 column halves, num_blocks * Hkv * 2 row groups):
-// element (c, r, h, m) is row 8m + r, column 64h + c of the 2-D
-// [num_blocks * Hkv * 16][128] view.  A box of (64, 8, 2, 2) is one whole
-// (block, kv head) tile -- 4 KB in one copy -- and lands in shared memory as
-// [row group][column half][8 rows][128 B] with the 128-byte swizzle: each
-// 8-row x 128-byte atom sits on its own 1 KB, the two halves of a row group
-// 1 KB apart and consecutive row groups 2 KB apart, which is the K-major
-// (and, for V, MN-major) operand layout the tensor-core kernels describe
-// with an 8-row-group stride of 2 KB, and what the CUDA-core kernel
-// addresses directly.
+// The paged cache [num_blocks][Hkv][BS][128] bf16 (BS = block size) seen as a
+// 4-D tensor (64 columns, 8 rows, 2 column halves, num_blocks * Hkv * BS / 8
+// row groups): element (c, r, h, m) is row 8m + r, column 64h + c of the 2-D
+// [num_blocks * Hkv * BS][128] view.  A box of (64, 8, 2, BS / 8) is one whole
+// (block, kv head) tile -- BS * 256 bytes in one copy -- and lands in shared
+// memory as [row group][column half][8 rows][128 B] with the 128-byte
+// swizzle: each 8-row x 128-byte atom sits on its own 1 KB, the two halves of
+// a row group 1 KB apart and consecutive row groups 2 KB apart, which is the
+// K-major (and, for V, MN-major) operand layout the tensor-core kernels
+// describe with an 8-row-group stride of 2 KB, and what the CUDA-core kernel
+// addresses directly.  Blocks placed one after another in shared memory thus
+// form one uniform run of row groups whatever BS is.
 bool encode_cache_map(CUtensorMap* map, const void* cache, int32_t num_blocks,
-                      int32_t num_kv_heads) {
+                      int32_t num_kv_heads, int32_t block_size) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
-  const cuuint64_t dims[4] = {64, 8, 2,
-                              static_cast<cuuint64_t>(num_blocks) * num_kv_heads * 2};
+  const cuuint64_t dims[4] = {
+      64, 8, 2, static_cast<cuuint64_t>(num_blocks) * num_kv_heads * (block_size / 8)};
   const cuuint64_t strides[3] = {static_cast<cuuint64_t>(kHeadDim) * 2,  // next row
                                  128,                                     // next half
                                  static_cast<cuuint64_t>(kHeadDim) * 2 * 8};  // next group
-  const cuuint32_t box[4] = {64, 8, 2, 2};
+  const cuuint32_t box[4] = {64, 8, 2, static_cast<cuuint32_t>(block_size / 8)};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(cache), dims, strides,
             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -104,18 +106,19 @@ struct MapEntry {
   const void* ptr;
   int32_t num_blocks;
   int32_t num_kv_heads;
+  int32_t block_size;
   CUtensorMap map;
 };
 
 bool cached_cache_map(CUtensorMap* out, const void* cache, int32_t num_blocks,
-                      int32_t num_kv_heads) {
+                      int32_t num_kv_heads, int32_t block_size) {
   static std::mutex mu;
   static MapEntry entries[16];
   static int used = 0, next = 0;
   std::lock_guard<std::mutex> lk(mu);
   for (int i = 0; i < used; ++i) {
     if (entries[i].ptr == cache && entries[i].num_blocks == num_blocks &&
-        entries[i].num_kv_heads == num_kv_heads) {
+        entries[i].num_kv_heads == num_kv_heads && entries[i].block_size == block_size) {
       *out = entries[i].map;
       return true;
     }
@@ -124,7 +127,8 @@ bool cached_cache_map(CUtensorMap* out, const void* cache, int32_t num_blocks,
   e.ptr = cache;
   e.num_blocks = num_blocks;
   e.num_kv_heads = num_kv_heads;
-  if (!encode_cache_map(&e.map, cache, num_blocks, num_kv_heads)) return false;
+  e.block_size = block_size;
+  if (!encode_cache_map(&e.map, cache, num_blocks, num_kv_heads, block_size)) return false;
   entries[next] = e;
   next = (next + 1) % 16;
   if (used < 16) ++used;
@@ -152,10 +156,11 @@ bool encode_q_group_map(CUtensorMap* map, const void* q, int64_t q_row_stride, i
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Which decode kernel serves a group size: the tensor-core kernel (measured
+// Which decode kernel serves a shape: the tensor-core kernel (measured
 // faster for every group size, 1..8); the environment variable
-// QATTN_DECODE_KERNEL=cuda selects the CUDA-core kernel instead.
-bool use_tc_decode(int group) {
+// QATTN_DECODE_KERNEL=cuda selects the CUDA-core kernel instead where it
+// applies (16-token blocks).
+bool use_tc_decode(int group, int block_size) {
   static int forced = [] {
     const char* e = getenv("QATTN_DECODE_KERNEL");
     if (e == nullptr) return 0;
@@ -163,6 +168,7 @@ bool use_tc_decode(int group) {
     if (strcmp(e, "tc") == 0) return 2;
     return 0;
   }();
+  if (block_size != kBlockSize) return true;
   if (forced == 1) return false;
   return group >= 1 && group <= 8;
 }
@@ -172,7 +178,7 @@ int check_cache(const void* k_cache, const void* v_cache, int32_t num_blocks,
   if (k_cache == nullptr || v_cache == nullptr || num_blocks <= 0) return QATTN_ERR_INVALID_ARG;
   if (!aligned16(k_cache) || !aligned16(v_cache)) return QATTN_ERR_INVALID_ARG;
   // TMA coordinates are 32-bit.
-  if (static_cast<int64_t>(num_blocks) * d.num_kv_heads * kBlockSize >= (1ll << 31))
+  if (static_cast<int64_t>(num_blocks) * d.num_kv_heads * d.block_size >= (1ll << 31))
     return QATTN_ERR_UNSUPPORTED;
   return QATTN_OK;
 }
@@ -292,6 +298,7 @@ int qattn_rope_cache_append_ex(void* q, int64_t q_row_stride, const void* k,
   a.max_pos = max_pos;
   a.num_heads = dims.num_heads;
   a.num_kv_heads = dims.num_kv_heads;
+  a.block_size = dims.block_size;
   a.err_word = err_word;
   a.bias = qkv_bias;
   a.q_norm_w = q_norm_weight;
@@ -313,8 +320,9 @@ int qattn_rope_cache_append(void* q, int64_t q_row_stride, const void* k, int64_
 
 int qattn_paged_decode_kernel(qattn_dims dims) {
   if (check_dims(dims) != QATTN_OK) return -1;
-  return use_tc_decode(dims.num_heads / dims.num_kv_heads) ? QATTN_DECODE_TENSOR_CORE
-                                                            : QATTN_DECODE_CUDA_CORE;
+  return use_tc_decode(dims.num_heads / dims.num_kv_heads, dims.block_size)
+             ? QATTN_DECODE_TENSOR_CORE
+             : QATTN_DECODE_CUDA_CORE;
 }
 
 size_t qattn_paged_decode_workspace_size(int32_t num_seqs, int32_t max_context_len,
@@ -353,6 +361,7 @@ int decode_common(void* out, const void* q, int64_t q_row_stride, int32_t q_rows
   a.max_context_len = max_context_len;
   a.num_heads = dims.num_heads;
   a.num_kv_heads = dims.num_kv_heads;
+  a.block_size = dims.block_size;
   a.scale_log2 = scale_of(dims) * kLog2e;
   a.err_word = err_word;
   a.ws = carve_decode_workspace(workspace, num_seqs, max_context_len, dims.num_kv_heads,
@@ -360,7 +369,7 @@ int decode_common(void* out, const void* q, int64_t q_row_stride, int32_t q_rows
   a.prefix_len = prefix_len;
   a.part_base = part_base;
   const int group = dims.num_heads / dims.num_kv_heads;
-  if (use_tc_decode(group)) {
+  if (use_tc_decode(group, dims.block_size)) {
     CUtensorMap qmap;
     if (!encode_q_group_map(&qmap, q, q_row_stride, q_rows, dims.num_heads, group))
       return QATTN_ERR_CUDA;
@@ -397,8 +406,8 @@ int qattn_paged_decode(void* out, const void* q, int64_t q_row_stride, const voi
                             max_blocks_per_seq, context_lens, max_context_len, dims);
   if (st != QATTN_OK) return st;
   CUtensorMap kmap, vmap;
-  if (!cached_cache_map(&kmap, k_cache, num_blocks, dims.num_kv_heads) ||
-      !cached_cache_map(&vmap, v_cache, num_blocks, dims.num_kv_heads))
+  if (!cached_cache_map(&kmap, k_cache, num_blocks, dims.num_kv_heads, dims.block_size) ||
+      !cached_cache_map(&vmap, v_cache, num_blocks, dims.num_kv_heads, dims.block_size))
     return QATTN_ERR_CUDA;
   const int sms = num_sms_current();
   if (sms <= 0) return QATTN_ERR_CUDA;
@@ -432,8 +441,9 @@ int qattn_paged_decode_shared_prefix(void* out, const void* q, int64_t q_row_str
   st = check_attention_args(out, q, q_row_stride, k_cache, v_cache, num_blocks, block_tables,
                             max_blocks_per_seq, context_lens, max_context_len, dims);
   if (st != QATTN_OK) return st;
-  if (shared_prefix_len < 0 || shared_prefix_len % kBlockSize != 0 ||
-      shared_prefix_len >= max_context_len || shared_prefix_len > max_blocks_per_seq * kBlockSize)
+  if (shared_prefix_len < 0 || shared_prefix_len % dims.block_size != 0 ||
+      shared_prefix_len >= max_context_len ||
+      shared_prefix_len > static_cast<int64_t>(max_blocks_per_seq) * dims.block_size)
     return QATTN_ERR_INVALID_ARG;
   const size_t need =
       qattn_paged_decode_shared_prefix_workspace_size(num_seqs, max_context_len, dims);
@@ -441,8 +451,8 @@ int qattn_paged_decode_shared_prefix(void* out, const void* q, int64_t q_row_str
       (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return QATTN_ERR_WORKSPACE;
   CUtensorMap kmap, vmap;
-  if (!cached_cache_map(&kmap, k_cache, num_blocks, dims.num_kv_heads) ||
-      !cached_cache_map(&vmap, v_cache, num_blocks, dims.num_kv_heads))
+  if (!cached_cache_map(&kmap, k_cache, num_blocks, dims.num_kv_heads, dims.block_size) ||
+      !cached_cache_map(&vmap, v_cache, num_blocks, dims.num_kv_heads, dims.block_size))
     return QATTN_ERR_CUDA;
   const int sms = num_sms_current();
   if (sms <= 0) return QATTN_ERR_CUDA;
@@ -479,6 +489,7 @@ int qattn_paged_decode_shared_prefix(void* out, const void* q, int64_t q_row_str
   p.max_context_len = max_context_len;
   p.num_heads = dims.num_heads;
   p.num_kv_heads = dims.num_kv_heads;
+  p.block_size = dims.block_size;
   p.scale_log2 = scale_of(dims) * kLog2e;
   p.err_word = err_word;
   p.prefix_len = shared_prefix_len;
@@ -517,8 +528,8 @@ int qattn_varlen_prefill(void* out, const void* q, int64_t q_row_stride,
                             max_blocks_per_seq, context_lens, max_context_len, dims);
   if (st != QATTN_OK) return st;
   CUtensorMap kmap, vmap;
-  if (!cached_cache_map(&kmap, k_cache, num_blocks, dims.num_kv_heads) ||
-      !cached_cache_map(&vmap, v_cache, num_blocks, dims.num_kv_heads))
+  if (!cached_cache_map(&kmap, k_cache, num_blocks, dims.num_kv_heads, dims.block_size) ||
+      !cached_cache_map(&vmap, v_cache, num_blocks, dims.num_kv_heads, dims.block_size))
     return QATTN_ERR_CUDA;
   const int sms = num_sms_current();
   if (sms <= 0) return QATTN_ERR_CUDA;
@@ -544,6 +555,7 @@ int qattn_varlen_prefill(void* out, const void* q, int64_t q_row_stride,
   p.max_context_len = max_context_len;
   p.num_heads = dims.num_heads;
   p.num_kv_heads = dims.num_kv_heads;
+  p.block_size = dims.block_size;
   p.scale_log2 = scale_of(dims) * kLog2e;
   p.err_word = err_word;
   p.prefix_len = 0;

@@ -16,7 +16,7 @@
 namespace qattn {
 
 constexpr int kHeadDim = 128;
-constexpr int kBlockSize = 16;
+constexpr int kBlockSize = 16;      // the CUDA-core decode's block size; others take 16/32/64
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s
 
 // ------------------------------------------------------------ addresses ---
@@ -470,13 +470,14 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) 
 }
 
 // One (block, kv head) tile of the paged cache (4-D view, see the cache
-// tensor map): `tile` = block id * num_kv_heads + kv head.
+// tensor map): `tile` = block id * num_kv_heads + kv head, `groups` = the
+// block's 8-row groups (block_size / 8; the map's box has that many).
 __device__ __forceinline__ void tma_load_cache_tile(void* smem_dst, const CUtensorMap* map,
-                                                    int32_t tile, uint64_t* bar) {
+                                                    int32_t tile, int32_t groups, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(0), "r"(0), "r"(tile * 2),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(0), "r"(0), "r"(tile * groups),
       "r"(smem_u32(bar))
       : "memory");
 }

@@ -74,6 +74,7 @@ struct RopeAppendArgs {
   int32_t max_pos;
   int32_t num_heads;
   int32_t num_kv_heads;
+  int32_t block_size;      // tokens per cache block: 16, 32 or 64
   int32_t* err_word;
   // Optional steps before RoPE (null: skipped): the qkv projection bias
   // [(H + 2 Hkv) * 128] bf16, and Qwen3's per-head RMSNorm weights [128]
@@ -121,6 +122,7 @@ struct DecodeArgs {
   int32_t max_context_len;
   int32_t num_heads;
   int32_t num_kv_heads;
+  int32_t block_size;      // tokens per cache block: 16, 32 or 64 (16 for K2)
   float scale_log2;        // softmax scale * log2(e)
   int32_t* err_word;
   DecodeWorkspace ws;
@@ -166,13 +168,15 @@ __device__ __forceinline__ int decode_len_eff(const DecodeArgs& a, int b) {
   if (a.cu_seqlens_q != nullptr) {
     if (a.cu_seqlens_q[b + 1] - a.cu_seqlens_q[b] != 1) return 0;
   }
-  if (L <= a.prefix_len || L > a.max_context_len || L > a.max_blocks_per_seq * 16) return 0;
+  if (L <= a.prefix_len || L > a.max_context_len || L > a.max_blocks_per_seq * a.block_size)
+    return 0;
   return L - a.prefix_len;
 }
 
 // Block-table entries of sequence b from its first attended token on.
 __device__ __forceinline__ const int32_t* decode_block_row(const DecodeArgs& a, int b) {
-  return a.block_tables + static_cast<int64_t>(b) * a.max_blocks_per_seq + a.prefix_len / 16;
+  return a.block_tables + static_cast<int64_t>(b) * a.max_blocks_per_seq +
+         a.prefix_len / a.block_size;
 }
 
 // A unit that straddles CTAs leaves one partial result per CTA (O
@@ -234,6 +238,7 @@ struct PrefillArgs {
   int32_t max_context_len;
   int32_t num_heads;
   int32_t num_kv_heads;
+  int32_t block_size;      // tokens per cache block: 16, 32 or 64
   float scale_log2;
   int32_t* err_word;
   // Shared-prefix pass (the same kernel, prefix_len > 0): every sequence's

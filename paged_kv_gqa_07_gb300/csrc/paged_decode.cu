@@ -323,7 +323,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int id = j ? cid1 : cid0;
           if (id >= 0) {
             uint8_t* dst = smem + kOffStages + stage * kStageBytes + isv * kKBytes + j * kTileBytes;
-            tma_load_cache_tile(dst, isv ? &vmap : &kmap, id * Hkv + g, &full[stage]);
+            tma_load_cache_tile(dst, isv ? &vmap : &kmap, id * Hkv + g, kBlockSize / 8,
+                                &full[stage]);
           }
         }
         ++n;

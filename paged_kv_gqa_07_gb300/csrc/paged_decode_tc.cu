@@ -50,8 +50,11 @@ constexpr int kN = 16;                // MMA N: the query group padded to 16 hea
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr int kThreads = 6 * 32;
-constexpr int kCacheTileBytes = kBlockSize * kHeadDim * 2;  // one (block, kv head): 4 KB
-constexpr int kTileBytes = (kTile / kBlockSize) * kCacheTileBytes;  // 8 blocks: 32 KB
+// A tile of 128 tokens lands as 8-token row groups 2 KB apart whatever the
+// block size (a block's box is block_size / 8 such groups), so the code below
+// addresses it in 16-token / 4 KB units.
+constexpr int kCacheTileBytes = 16 * kHeadDim * 2;  // 16 tokens: 4 KB
+constexpr int kTileBytes = kTile * kHeadDim * 2;    // 32 KB
 constexpr int kKStages = 3;
 constexpr int kVStages = 3;
 constexpr int kSmallHalf = kN * 128;     // 16 rows x 128 B
@@ -187,6 +190,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Hkv = a.num_kv_heads;
   const int B = a.num_seqs;
+  const int bpt = kTile / a.block_size;    // cache blocks per tile: 8, 4 or 2
+  const int groups = a.block_size / 8;     // 8-row groups per block box
+  const uint32_t blk_bytes = static_cast<uint32_t>(a.block_size) * kHeadDim * 2;
 
   prefetch_decode_metadata(a);
   // ---- plan: tile count, this CTA's run [c0, c1), its first unit ----
@@ -273,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kProducerWarp) {
     // ================================ producer ================================
     // Batches of 32 tiles: lane l walks to tile (batch start + l) and loads
-    // its eight block ids; lane 0 then issues the copies tile by tile.
+    // its block ids (up to eight); lane 0 then issues the copies tile by tile.
     if (lane == 0) {
       tma_prefetch_desc(&kmap);
       tma_prefetch_desc(&vmap);
@@ -293,13 +299,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool okv = true;
       if (lane == 0) {
         okv = mbar_wait(&v_empty[vs], ((j / kVStages) & 1) ^ 1, abort_flag);
-        if (okv) mbar_arrive_expect_tx(&v_full[vs], nval * 2 * kBlockSize * 128);
+        if (okv) mbar_arrive_expect_tx(&v_full[vs], nval * blk_bytes);
       }
       okv = __shfl_sync(0xffffffffu, okv, 0);
       if (!okv) return false;
-      if (lane < 8 && id_lane >= 0)
-        tma_load_cache_tile(smem + kOffV + vs * kTileBytes + lane * kCacheTileBytes, &vmap,
-                            id_lane * Hkv + gg, &v_full[vs]);
+      if (lane < bpt && id_lane >= 0)
+        tma_load_cache_tile(smem + kOffV + vs * kTileBytes + lane * blk_bytes, &vmap,
+                            id_lane * Hkv + gg, groups, &v_full[vs]);
       ++nv;
       return true;
     };
@@ -316,8 +322,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < 8; ++j) ids[j] = -1;
       if (lane < cnt) {
         const int ntok = min(kTile, mw.L - mw.i * kTile);
-        const int nblk = (ntok + kBlockSize - 1) / kBlockSize;
-        const int* row = decode_block_row(a, mw.b) + mw.i * (kTile / kBlockSize);
+        const int nblk = (ntok + a.block_size - 1) / a.block_size;
+        const int* row = decode_block_row(a, mw.b) + mw.i * bpt;
 #pragma unroll
         for (int j = 0; j < 8; ++j)
           if (j < nblk) ids[j] = row[j];
@@ -334,9 +340,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int g = __shfl_sync(0xffffffffu, mw.g, c);
         const int ci = __shfl_sync(0xffffffffu, mw.i, c);
         const int64_t cq = __shfl_sync(0xffffffffu, qrow, c);
-        // Lane j (< 8) issues block j's boxes itself: one warp-wide TMA
-        // instruction then moves eight boxes (a single lane issuing all 32
-        // boxes of a tile was measured at ~55 ns per box).
+        // Lane j (< blocks per tile) issues block j's box itself: one
+        // warp-wide TMA instruction then moves the tile's boxes (a single lane
+        // issuing all 32 boxes of a tile was measured at ~55 ns per box).
         int myid = -1;
         uint32_t nvalid = 0;
 #pragma unroll
@@ -360,13 +366,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ks = n % kKStages;
         if (lane == 0 && ok) {
           ok = mbar_wait(&k_empty[ks], ((n / kKStages) & 1) ^ 1, abort_flag);
-          if (ok) mbar_arrive_expect_tx(&k_full[ks], nvalid * 2 * kBlockSize * 128);
+          if (ok) mbar_arrive_expect_tx(&k_full[ks], nvalid * blk_bytes);
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
-        if (lane < 8 && myid >= 0) {
-          tma_load_cache_tile(smem + kOffK + ks * kTileBytes + lane * kCacheTileBytes, &kmap,
-                              myid * Hkv + g, &k_full[ks]);
+        if (lane < bpt && myid >= 0) {
+          tma_load_cache_tile(smem + kOffK + ks * kTileBytes + lane * blk_bytes, &kmap,
+                              myid * Hkv + g, groups, &k_full[ks]);
         }
         ++n;  // K(n) issued
         if (n >= 2 && !issue_v(n - 2, prev_id, prev_g, prev_nvalid)) {

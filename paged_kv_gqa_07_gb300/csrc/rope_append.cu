@@ -131,7 +131,8 @@ __global__ void __launch_bounds__(kThreads) rope_append_kernel(RopeAppendArgs a,
     return;
   }
   const int slot = a.slot_mapping[t];
-  const int64_t num_slots = static_cast<int64_t>(a.num_blocks) * kBlockSize;
+  const int BS = a.block_size;
+  const int64_t num_slots = static_cast<int64_t>(a.num_blocks) * BS;
   bool write_cache = slot >= 0;
   if (write_cache && slot >= num_slots) {
     if (r == 0) set_err(a.err_word, QATTN_DEVERR_SLOT);
@@ -139,8 +140,8 @@ __global__ void __launch_bounds__(kThreads) rope_append_kernel(RopeAppendArgs a,
   }
   int64_t cache_row = 0;  // element offset of (block, kv head 0, offset) in the cache
   if (write_cache) {
-    const int blk = slot / kBlockSize, off = slot % kBlockSize;
-    cache_row = (static_cast<int64_t>(blk) * Hkv * kBlockSize + off) * kHeadDim;
+    const int blk = slot / BS, off = slot % BS;
+    cache_row = (static_cast<int64_t>(blk) * Hkv * BS + off) * kHeadDim;
   }
 
   if (r < nrot) {
@@ -196,7 +197,7 @@ __global__ void __launch_bounds__(kThreads) rope_append_kernel(RopeAppendArgs a,
       uint4 y1, y2;
       rotate8(x1, x2, c, s, y1, y2);
       __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.k_cache) + cache_row +
-                           static_cast<int64_t>(g) * kBlockSize * kHeadDim;
+                           static_cast<int64_t>(g) * BS * kHeadDim;
       *reinterpret_cast<uint4*>(dst + part * 8) = y1;
       *reinterpret_cast<uint4*>(dst + 64 + part * 8) = y2;
     }
@@ -207,7 +208,7 @@ __global__ void __launch_bounds__(kThreads) rope_append_kernel(RopeAppendArgs a,
     const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(a.v) + t * a.v_row_stride +
                                static_cast<int64_t>(g) * kHeadDim;
     __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.v_cache) + cache_row +
-                         static_cast<int64_t>(g) * kBlockSize * kHeadDim;
+                         static_cast<int64_t>(g) * BS * kHeadDim;
     uint4 x = *reinterpret_cast<const uint4*>(src + part * 8);
     if (kExtras && a.bias)
       x = add_bias8(x, static_cast<const __nv_bfloat16*>(a.bias) +

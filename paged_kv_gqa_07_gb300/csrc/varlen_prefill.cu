@@ -57,7 +57,10 @@ constexpr int kWarps = 11;
 constexpr int kThreads = kWarps * 32;
 constexpr int kHalfBytes = 128 * 128;   // 128 rows x 128 B (Q and P: [half][row])
 constexpr int kTileBytes = 2 * kHalfBytes;
-constexpr int kCacheTileBytes = kBlockSize * kHeadDim * 2;  // one (block, kv head): 4 KB
+// A 128-token K/V tile lands as 8-token row groups 2 KB apart whatever the
+// block size (each block's box is block_size / 8 groups); the V zeroing below
+// addresses it in 16-token / 4 KB units.
+constexpr int kCacheTileBytes = 16 * kHeadDim * 2;  // 16 tokens: 4 KB
 constexpr uint32_t kTmemCols = 512;     // S[2] at 0 / 128, O[2] at 256 / 384
 constexpr uint32_t kColO = 256;
 constexpr float kLazyRescale = 8.0f;
@@ -101,7 +104,7 @@ struct Misc {
 };
 
 __device__ __forceinline__ bool prefill_ctx_ok(const PrefillArgs& a, int L, int ql) {
-  return L >= ql && L <= a.max_context_len && L <= a.max_blocks_per_seq * kBlockSize;
+  return L >= ql && L <= a.max_context_len && L <= a.max_blocks_per_seq * a.block_size;
 }
 
 // Inclusive scan over the CTA's threads.
@@ -231,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (prefix_mode) {
     // Every sequence's table must start with row 0's prefix blocks.
-    const int nb = a.prefix_len / kBlockSize;
+    const int nb = a.prefix_len / a.block_size;
     const int64_t pairs_total = static_cast<int64_t>(B - 1) * nb;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + tid; i < pairs_total;
          i += static_cast<int64_t>(gridDim.x) * kThreads) {
@@ -294,6 +297,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* empty = is_v ? v_empty : k_empty;
     const CUtensorMap* map = is_v ? &vmap : &kmap;
     uint8_t* ring = smem + (is_v ? kOffV : kOffK);
+    const int bpt = 128 / a.block_size;   // cache blocks per tile: 8, 4 or 2
+    const int groups = a.block_size / 8;  // 8-row groups per block box
+    const uint32_t blk_bytes = static_cast<uint32_t>(a.block_size) * kHeadDim * 2;
     if (lane == 0) {
       tma_prefetch_desc(map);
       if (!is_v) tma_prefetch_desc(&qmap);
@@ -369,12 +375,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __shfl_sync(0xffffffffu, ok, 0);
       // the shared prefix lives in the blocks of table row 0
       const int* bt = a.block_tables + (prefix_mode ? 0 : static_cast<int64_t>(b) * a.max_blocks_per_seq);
-      const int nblk = (L + kBlockSize - 1) / kBlockSize;
+      const int nblk = (L + a.block_size - 1) / a.block_size;
       for (int kt = 0; kt < nkv && ok; ++kt) {
         const int st = n & 1;
         int id = -1;
-        if (lane < 8) {
-          const int bi = (kt0 + kt) * 8 + lane;
+        if (lane < bpt) {
+          const int bi = (kt0 + kt) * bpt + lane;
           if (bi < nblk) {
             id = bt[bi];
             if (id < 0 || id >= a.num_blocks) {
@@ -386,13 +392,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t nvalid = __popc(__ballot_sync(0xffffffffu, id >= 0));
         if (lane == 0) {
           ok = n < 2 || mbar_wait(&empty[st], ((n >> 1) & 1) ^ 1, abort_flag);
-          if (ok) mbar_arrive_expect_tx(&full[st], nvalid * kCacheTileBytes);
+          if (ok) mbar_arrive_expect_tx(&full[st], nvalid * blk_bytes);
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         if (id >= 0)
-          tma_load_cache_tile(ring + st * kTileBytes + lane * kCacheTileBytes, map,
-                              id * a.num_kv_heads + g, &full[st]);
+          tma_load_cache_tile(ring + st * kTileBytes + lane * blk_bytes, map,
+                              id * a.num_kv_heads + g, groups, &full[st]);
         ++n;
       }
     }

@@ -203,17 +203,19 @@ def build(name_or_index, seed: int | None = None, *, scale_batch: float = 1.0) -
 
 
 def custom(num_heads, num_kv_heads, ctx, q_lens, seed=1, pool_slack=0.1,
-           shared_prefix_tokens=0) -> Workload:
+           shared_prefix_tokens=0, block_size=BLOCK_SIZE) -> Workload:
     """A workload with explicit context lengths and query counts, random
-    block placement (used by edge-case tests)."""
+    block placement (used by edge-case tests); ``block_size`` tokens per
+    cache block (16, 32 or 64)."""
     gen = torch.Generator().manual_seed(seed)
     shape = dict(num_heads=num_heads, num_kv_heads=num_kv_heads)
+    BS = block_size
     if shared_prefix_tokens:
         # every table starts with the same blocks for the first
         # shared_prefix_tokens tokens (a multiple of the block size)
-        assert shared_prefix_tokens % BLOCK_SIZE == 0
-        pb = shared_prefix_tokens // BLOCK_SIZE
-        own = [max(0, (L + BLOCK_SIZE - 1) // BLOCK_SIZE - pb) for L in ctx]
+        assert shared_prefix_tokens % BS == 0
+        pb = shared_prefix_tokens // BS
+        own = [max(0, (L + BS - 1) // BS - pb) for L in ctx]
         pool = pb + sum(own) + max(8, int(sum(own) * pool_slack)) + 1
         perm = torch.randperm(pool, generator=gen)
         shared = perm[:pb].tolist()
@@ -222,13 +224,13 @@ def custom(num_heads, num_kv_heads, ctx, q_lens, seed=1, pool_slack=0.1,
             tables.append(shared + perm[used:used + nb].tolist())
             used += nb
         return _assemble("custom", seed, gen, shape, list(ctx), list(q_lens), tables, pool,
-                         shared_prefix_tokens=shared_prefix_tokens)
+                         shared_prefix_tokens=shared_prefix_tokens, block_size=BS)
     return _random_placement("custom", seed, gen, shape, list(ctx), list(q_lens),
-                             slack=pool_slack)
+                             slack=pool_slack, block_size=BS)
 
 
-def _random_placement(name, seed, gen, shape, ctx, q_lens, slack=0.1):
-    need = [(L + BLOCK_SIZE - 1) // BLOCK_SIZE for L in ctx]
+def _random_placement(name, seed, gen, shape, ctx, q_lens, slack=0.1, block_size=BLOCK_SIZE):
+    need = [(L + block_size - 1) // block_size for L in ctx]
     total = sum(need)
     pool = total + int(total * slack) + 1
     perm = torch.randperm(pool, generator=gen)
@@ -236,13 +238,13 @@ def _random_placement(name, seed, gen, shape, ctx, q_lens, slack=0.1):
     for nb in need:
         tables.append(perm[used:used + nb].tolist())
         used += nb
-    return _assemble(name, seed, gen, shape, ctx, q_lens, tables, pool)
+    return _assemble(name, seed, gen, shape, ctx, q_lens, tables, pool, block_size=block_size)
 
 
 def _assemble(name, seed, gen, shape, ctx, q_lens, tables, pool,
-              shared_prefix_tokens=0) -> Workload:
+              shared_prefix_tokens=0, block_size=BLOCK_SIZE) -> Workload:
     H, Hkv = shape["num_heads"], shape["num_kv_heads"]
-    D, BS = HEAD_DIM, BLOCK_SIZE
+    D, BS = HEAD_DIM, block_size
     B = len(ctx)
     max_blocks = max(1, max(len(t) for t in tables))
     bt = torch.zeros((B, max_blocks), dtype=torch.int32)

@@ -99,6 +99,9 @@ def test_decode_kernel_choice(lib):
     assert Q.qattn_paged_decode_kernel(Q.make_dims(28, 4)) == Q.QATTN_DECODE_TENSOR_CORE
     assert Q.qattn_paged_decode_kernel(Q.make_dims(32, 4)) == Q.QATTN_DECODE_TENSOR_CORE
     assert Q.qattn_paged_decode_kernel(Q.make_dims(28, 5)) == -1
+    assert Q.qattn_paged_decode_kernel(Q.make_dims(28, 4, 128, 32)) == Q.QATTN_DECODE_TENSOR_CORE
+    assert Q.qattn_paged_decode_kernel(Q.make_dims(28, 4, 128, 64)) == Q.QATTN_DECODE_TENSOR_CORE
+    assert Q.qattn_paged_decode_kernel(Q.make_dims(28, 4, 128, 128)) == -1
 
 
 def test_host_validation_before_any_cuda_call(lib):
@@ -110,9 +113,13 @@ def test_host_validation_before_any_cuda_call(lib):
                                      fake, fake, 10, fake, 100, Q.make_dims(28, 4, 64), None, None)
     assert st == Q.QATTN_ERR_UNSUPPORTED                      # head_dim 64
     st = lib.qattn_rope_cache_append(fake, 4608, fake, 4608, fake, 4608, fake, fake, 4,
-                                     fake, fake, 10, fake, 100, Q.make_dims(28, 4, 128, 32), None,
+                                     fake, fake, 10, fake, 100, Q.make_dims(28, 4, 128, 48), None,
                                      None)
-    assert st == Q.QATTN_ERR_UNSUPPORTED                      # block_size 32
+    assert st == Q.QATTN_ERR_UNSUPPORTED                      # block_size 48
+    st = lib.qattn_rope_cache_append(fake, 4608, fake, 4608, fake, 4608, fake, fake, 4,
+                                     fake, fake, 10, fake, 100, Q.make_dims(28, 4, 128, 8), None,
+                                     None)
+    assert st == Q.QATTN_ERR_UNSUPPORTED                      # block_size 8
     st = lib.qattn_rope_cache_append(fake, 4608, fake, 4608, fake, 4608, fake, fake, 4,
                                      fake, fake, 10, fake, 100, Q.make_dims(27, 4), None, None)
     assert st == Q.QATTN_ERR_UNSUPPORTED                      # 27 % 4
