@@ -454,6 +454,59 @@ def test_block_permutation_invariance():
             assert np.array_equal(kca[x, :, j % 16], kcb[y, :, j % 16])
 
 
+def _relayout(w, bs):
+    """The same logical cache contents and new tokens in blocks of ``bs``
+    tokens, placed in reverse order (a plain host copy, no oracle code)."""
+    B, Hkv, D = w.num_seqs, w.num_kv_heads, w.head_dim
+    need = [(int(L) + bs - 1) // bs for L in w.context_lens]
+    pool = sum(need) + 1
+    order = list(range(pool))[::-1]
+    bt = np.zeros((B, max(need)), dtype=np.int32)
+    used = 0
+    for b, n in enumerate(need):
+        bt[b, :n] = order[used:used + n]
+        used += n
+    kc = np.full((pool, Hkv, bs, D), 0x7FC1, dtype=np.uint16)
+    vc = kc.copy()
+    k0, v0 = u16(w.k_cache), u16(w.v_cache)
+    slots = np.array(w.slot_mapping, dtype=np.int32).copy()
+    t = 0
+    for b in range(B):
+        L = int(w.context_lens[b])
+        for j in range(L):
+            x = int(w.block_tables[b, j // w.block_size])
+            kc[bt[b, j // bs], :, j % bs] = k0[x, :, j % w.block_size]
+            vc[bt[b, j // bs], :, j % bs] = v0[x, :, j % w.block_size]
+        for i in range(w.q_lens[b]):
+            p = L - w.q_lens[b] + i
+            slots[t] = bt[b, p // bs] * bs + p % bs
+            t += 1
+    return kc, vc, bt, slots
+
+
+@pytest.mark.parametrize("bs", [32, 64])
+def test_block_size_invariance(bs):
+    """16-, 32- and 64-token blocks holding the same tokens give the same
+    append rows and bit-identical attention (prefill and decode rows)."""
+    w = W.custom(8, 2, ctx=[5, 40, 100, 200], q_lens=[3, 1, 40, 1], seed=14)
+    ref, kc16, vc16, _ = _run_workload(w)
+    kc, vc, bt, slots = _relayout(w, bs)
+    qkv = u16(w.qkv)
+    H, Hkv, D = w.num_heads, w.num_kv_heads, w.head_dim
+    table = oracle.rope_table(1e6, w.max_pos, D)
+    assert oracle.rope_cache_append(qkv, w.positions, slots, kc, vc, table, H, Hkv, D, bs) == 0
+    q = np.ascontiguousarray(qkv[:, :H * D])
+    out, err = oracle.paged_attention(q, kc, vc, bt, w.context_lens, H, Hkv, D, bs,
+                                      cu_seqlens_q=w.cu_seqlens_q)
+    assert err == 0
+    assert np.array_equal(out, ref)
+    for b in range(w.num_seqs):
+        for j in range(int(w.context_lens[b])):
+            x = int(w.block_tables[b, j // 16])
+            assert np.array_equal(kc[bt[b, j // bs], :, j % bs], kc16[x, :, j % 16])
+            assert np.array_equal(vc[bt[b, j // bs], :, j % bs], vc16[x, :, j % 16])
+
+
 def test_one_token_context_returns_v_exactly():
     w = W.custom(4, 2, ctx=[1, 1, 1], q_lens=[1, 1, 1], seed=12)
     out, kc, vc, _ = _run_workload(w)
