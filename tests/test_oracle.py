@@ -469,7 +469,7 @@ def _relayout(w, bs):
     kc = np.full((pool, Hkv, bs, D), 0x7FC1, dtype=np.uint16)
     vc = kc.copy()
     k0, v0 = u16(w.k_cache), u16(w.v_cache)
-    slots = np.array(w.slot_mapping, dtype=np.int32).copy()
+    slots = w.slot_mapping.numpy().astype(np.int32).copy()
     t = 0
     for b in range(B):
         L = int(w.context_lens[b])
