@@ -29,6 +29,12 @@ What each function follows (pages named by title and section):
   (FlashAttention-2 varlen, Qwen engineering notes section 2.1), optionally
   in the split-KV partition + log-sum-exp merge form.
 * :func:`contiguous_attention` -- the same attention on unpaged K/V.
+* :func:`f32_to_e4m3`, :func:`e4m3_to_f64`, :func:`rope_cache_append_fp8`,
+  :func:`paged_attention_fp8` -- the FP8 KV cache (kv_cache_dtype "fp8",
+  fp8_e4m3fn, a cache scale per tensor: "Qwen2大模型架构解析与vLLM优化实践"
+  sections 4.1, 4.2 and 6.3): the OCP E4M3 format written out from its
+  definition, codes = e4m3(x / scale) of the bf16 values a bf16 cache would
+  hold, attention over code * scale.
 
 Every function here is pinned by ``tests/test_oracle.py`` against closed
 forms, invariants, a brute-force multiprecision softmax and the configuration
@@ -111,6 +117,17 @@ def lib():
             L.oracle_f32_to_bf16.restype = ctypes.c_uint16
             L.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
             L.oracle_bf16_to_f64.restype = _F64
+            L.oracle_f32_to_e4m3_array.argtypes = [_P, _I64, _P]
+            L.oracle_f32_to_e4m3_array.restype = None
+            L.oracle_e4m3_to_f64_array.argtypes = [_P, _I64, _P]
+            L.oracle_e4m3_to_f64_array.restype = None
+            L.oracle_rope_cache_append_fp8.argtypes = (
+                L.oracle_rope_cache_append_ex.argtypes + [ctypes.c_float, ctypes.c_float])
+            L.oracle_rope_cache_append_fp8.restype = _I32
+            L.oracle_paged_attention_fp8.argtypes = [
+                _P, _P, _I64, _P, _I32, _P, _P, _F64, _F64, _I32, _P, _I32, _P, _I32,
+                _I32, _I32, _I32, _F64, _I32, _I32]
+            L.oracle_paged_attention_fp8.restype = _I32
             _lib = L
     return _lib
 
@@ -301,6 +318,85 @@ def contiguous_attention(q, k, v, num_heads, num_kv_heads, head_dim, scale=None)
     if rc != 0:
         raise ValueError("bad contiguous attention arguments")
     return out
+
+
+def f32_to_e4m3(x) -> np.ndarray:
+    """fp32 values -> e4m3fn codes (uint8), nearest-even, saturating."""
+    f = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(f.shape, dtype=np.uint8)
+    lib().oracle_f32_to_e4m3_array(_ptr(f), int(f.size), _ptr(out))
+    return out
+
+
+def e4m3_to_f64(c) -> np.ndarray:
+    """e4m3fn codes (uint8) -> their values (NaN for the NaN codes)."""
+    c = np.ascontiguousarray(c, dtype=np.uint8)
+    out = np.empty(c.shape, dtype=np.float64)
+    lib().oracle_e4m3_to_f64_array(_ptr(c), int(c.size), _ptr(out))
+    return out
+
+
+def rope_cache_append_fp8(qkv, positions, slot_mapping, k_cache, v_cache, cos_sin,
+                          num_heads, num_kv_heads, head_dim, block_size, k_scale, v_scale,
+                          bias=None, q_norm_w=None, k_norm_w=None, eps=1e-6):
+    """rope_cache_append_ex into uint8 e4m3 caches: k and v are stored as
+    e4m3(x / k_scale) and e4m3(x / v_scale) of the bf16 rows a bf16 cache
+    would receive.  In place; returns the error bits."""
+    assert qkv.dtype == np.uint16 and qkv.flags["C_CONTIGUOUS"]
+    assert k_cache.dtype == np.uint8 and k_cache.flags["C_CONTIGUOUS"]
+    assert v_cache.dtype == np.uint8 and v_cache.flags["C_CONTIGUOUS"]
+    H, Hkv, D = num_heads, num_kv_heads, head_dim
+    W = qkv.shape[1]
+    assert W == (H + 2 * Hkv) * D
+    pos = _i32(positions)
+    slots = _i32(slot_mapping)
+    cs = np.ascontiguousarray(cos_sin, dtype=np.float32)
+    keep = [None if a is None else np.ascontiguousarray(a, dtype=np.uint16)
+            for a in (bias, q_norm_w, k_norm_w)]
+    ptrs = [None if a is None else _ptr(a) for a in keep]
+    base = qkv.ctypes.data
+    return int(lib().oracle_rope_cache_append_fp8(
+        base, W, base + H * D * 2, W, base + (H + Hkv) * D * 2, W,
+        _ptr(pos), _ptr(slots), int(pos.shape[0]), _ptr(k_cache), _ptr(v_cache),
+        int(k_cache.shape[0]), _ptr(cs), cs.shape[0], H, Hkv, D, block_size,
+        ptrs[0], ptrs[1], ptrs[2], float(eps), float(k_scale), float(v_scale)))
+
+
+def paged_attention_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+                        num_heads, num_kv_heads, head_dim, block_size, scale=None,
+                        cu_seqlens_q=None, partition_tokens=0, nthreads=None):
+    """paged_attention over uint8 e4m3 caches read as code * scale."""
+    qn = _u16(q)
+    if qn.ndim == 3:
+        qn = qn.reshape(qn.shape[0], -1)
+    kc = np.ascontiguousarray(_as_numpy(k_cache), dtype=np.uint8)
+    vc = np.ascontiguousarray(_as_numpy(v_cache), dtype=np.uint8)
+    bt = _i32(block_tables)
+    cl = _i32(context_lens)
+    cu = None if cu_seqlens_q is None else _i32(cu_seqlens_q)
+    num_seqs = int(cl.shape[0])
+    rows = num_seqs if cu is None else int(cu[-1])
+    out = np.zeros((rows, num_heads, head_dim), dtype=np.float64)
+    if scale is None:
+        scale = float(head_dim) ** -0.5
+    err = lib().oracle_paged_attention_fp8(
+        _ptr(out), _ptr(qn), qn.shape[1], _ptr(cu), num_seqs, _ptr(kc), _ptr(vc),
+        float(k_scale), float(v_scale), int(kc.shape[0]), _ptr(bt), int(bt.shape[1]),
+        _ptr(cl), num_heads, num_kv_heads, head_dim, block_size, float(scale),
+        int(partition_tokens), int(nthreads or default_threads()))
+    if err < 0:
+        raise ValueError("bad attention arguments")
+    return out, int(err)
+
+
+def _as_numpy(a):
+    try:
+        import torch
+        if isinstance(a, torch.Tensor):
+            return a.detach().cpu().contiguous().view(torch.uint8).numpy()
+    except ImportError:
+        pass
+    return np.asarray(a)
 
 
 def bf16_round(x: np.ndarray) -> np.ndarray:

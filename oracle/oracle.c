@@ -35,7 +35,12 @@
  *     q_len new tokens and context L sits at position L - q_len + i and sees
  *     keys 0 .. L - q_len + i;
  *   - a row whose context is invalid, or whose block id is out of range,
- *     is written as zeros and an error bit is returned.
+ *     is written as zeros and an error bit is returned;
+ *   - an FP8 cache ([p2] sections 4.1-4.2 and 6.3: kv_cache_dtype "fp8",
+ *     fp8_e4m3fn, a cache scale per tensor) holds the e4m3fn code of
+ *     x / scale for the bf16 value x a bf16 cache would hold (fp32 division,
+ *     then round-to-nearest-even, saturating to +-448); attention reads
+ *     code * scale.
  */
 #include <math.h>
 #include <pthread.h>
@@ -72,6 +77,70 @@ static uint16_t f32_to_bf16_rne(float f) {
 
 uint16_t oracle_f32_to_bf16(float f) { return f32_to_bf16_rne(f); }
 double oracle_bf16_to_f64(uint16_t b) { return bf16_to_f64(b); }
+
+/* ---------------------------------------------------------- e4m3fn ---- */
+
+/* The OCP 8-bit float E4M3 ("fn": finite, no infinities): sign bit, 4
+ * exponent bits with bias 7, 3 mantissa bits.  Exponent field 0 holds the
+ * subnormals m * 2^-9; field e > 0 holds (1 + m/8) * 2^(e-7); the codes
+ * S.1111.111 are NaN, so the largest finite value is 1.75 * 2^8 = 448. */
+double oracle_e4m3_to_f64(uint8_t c) {
+  const int e = (c >> 3) & 15, m = c & 7;
+  if (e == 15 && m == 7) return NAN;
+  const double mag = e == 0 ? ldexp((double)m, -9) : ldexp(1.0 + m / 8.0, e - 7);
+  return (c & 0x80) ? -mag : mag;
+}
+
+/* Rounds v / 2^q to an integer, ties to even (v >= 0, exact in double). */
+static double round_half_even_scaled(double v, int q) {
+  const double x = ldexp(v, -q);
+  const double f = floor(x);
+  const double r = x - f;
+  if (r > 0.5) return f + 1.0;
+  if (r < 0.5) return f;
+  return fmod(f, 2.0) == 0.0 ? f : f + 1.0;
+}
+
+/* fp32 -> e4m3fn code, round to nearest even, saturating: a magnitude that
+ * rounds above 448 (and an infinity) gives the largest finite code; NaN
+ * gives 0x7F. */
+uint8_t oracle_f32_to_e4m3(float f) {
+  if (f != f) return 0x7F;
+  const uint8_t sign = signbit(f) ? 0x80 : 0x00;
+  const double a = fabs((double)f);
+  if (a >= 448.0) return sign | 0x7E;
+  if (a < ldexp(1.0, -6)) {
+    /* subnormal grid: multiples of 2^-9 (8 of them reach 2^-6, the first
+     * normal, code 0x08) */
+    const double m = round_half_even_scaled(a, -9);
+    return sign | (uint8_t)m;
+  }
+  int ex;
+  frexp(a, &ex);          /* a = fr * 2^ex, fr in [0.5, 1) */
+  int E = ex - 1;         /* a in [2^E, 2^(E+1)) */
+  double mm = round_half_even_scaled(a - ldexp(1.0, E), E - 3);  /* eighths */
+  if (mm == 8.0) {
+    mm = 0.0;
+    ++E;
+  }
+  if (E > 8 || (E == 8 && mm > 6.0)) return sign | 0x7E;
+  return sign | (uint8_t)(((E + 7) << 3) | (int)mm);
+}
+
+void oracle_f32_to_e4m3_array(const float* x, int64_t n, uint8_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_f32_to_e4m3(x[i]);
+}
+
+void oracle_e4m3_to_f64_array(const uint8_t* c, int64_t n, double* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_to_f64(c[i]);
+}
+
+/* The cache code of a bf16 value x under a per-tensor scale: e4m3(x / s),
+ * the division in fp32 (correctly rounded). */
+static uint8_t quantize_kv(uint16_t x, float s) {
+  const float q = bf16_to_f32(x) / s;
+  return oracle_f32_to_e4m3(q);
+}
 
 /* ------------------------------------------------------- RoPE table ---- */
 
@@ -335,9 +404,56 @@ int32_t oracle_rope_cache_append_ex(
   return err;
 }
 
+/* The append into an FP8 cache: every step of oracle_rope_cache_append_ex
+ * up to the bf16 K (rotated) and V rows a bf16 cache would receive, then
+ * each value is stored as quantize_kv(x, k_scale) / quantize_kv(x, v_scale).
+ * q is rotated in place as before. */
+int32_t oracle_rope_cache_append_fp8(
+    uint16_t* q, int64_t q_row_stride, const uint16_t* k, int64_t k_row_stride,
+    const uint16_t* v, int64_t v_row_stride, const int32_t* positions,
+    const int32_t* slot_mapping, int32_t num_tokens, uint8_t* k_cache,
+    uint8_t* v_cache, int32_t num_blocks, const float* cos_sin,
+    int32_t max_pos, int32_t num_heads, int32_t num_kv_heads,
+    int32_t head_dim, int32_t block_size, const uint16_t* bias,
+    const uint16_t* q_norm_w, const uint16_t* k_norm_w, double eps,
+    float k_scale, float v_scale) {
+  const int32_t D = head_dim;
+  /* one token at a time through the bf16 append into a one-block scratch
+   * cache, then quantised */
+  uint16_t* kb = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)num_kv_heads * D);
+  uint16_t* vb = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)num_kv_heads * D);
+  int32_t err = 0;
+  for (int32_t t = 0; t < num_tokens; ++t) {
+    int32_t slot = slot_mapping[t];
+    const int32_t zero = 0;
+    const int32_t e = oracle_rope_cache_append_ex(
+        q + (int64_t)t * q_row_stride, q_row_stride, k + (int64_t)t * k_row_stride,
+        k_row_stride, v + (int64_t)t * v_row_stride, v_row_stride, positions + t,
+        slot < 0 ? &slot : &zero, 1, kb, vb, 1, cos_sin, max_pos, num_heads,
+        num_kv_heads, D, 1, bias, q_norm_w, k_norm_w, eps);
+    err |= e;
+    if (e || slot < 0) continue;
+    if ((int64_t)slot >= (int64_t)num_blocks * block_size) {
+      err |= OR_ERR_SLOT;
+      continue;
+    }
+    const int32_t blk = slot / block_size, off = slot % block_size;
+    for (int32_t g = 0; g < num_kv_heads; ++g) {
+      const int64_t dst = (((int64_t)blk * num_kv_heads + g) * block_size + off) * D;
+      for (int32_t d = 0; d < D; ++d) {
+        k_cache[dst + d] = quantize_kv(kb[(int64_t)g * D + d], k_scale);
+        v_cache[dst + d] = quantize_kv(vb[(int64_t)g * D + d], v_scale);
+      }
+    }
+  }
+  free(kb);
+  free(vb);
+  return err;
+}
+
 /* ------------------------------------------------------- attention ---- */
 
-typedef struct {
+typedef struct attn_job_s {
   double* out;
   const uint16_t* q;
   int64_t q_row_stride;
@@ -345,6 +461,9 @@ typedef struct {
   int32_t num_seqs;
   const uint16_t* k_cache;
   const uint16_t* v_cache;
+  const uint8_t* k_cache8; /* FP8 cache (k_cache / v_cache unused) or NULL */
+  const uint8_t* v_cache8;
+  double k_scale, v_scale;
   int32_t num_blocks;
   const int32_t* block_tables;
   int32_t max_blocks_per_seq;
@@ -357,6 +476,11 @@ typedef struct {
   int32_t err;
   pthread_mutex_t lock;
 } attn_job;
+
+/* Element i of the K or V cache as the attention sees it: the bf16 value,
+ * or code * scale for an FP8 cache. */
+static double k_at(const struct attn_job_s* J, int64_t i);
+static double v_at(const struct attn_job_s* J, int64_t i);
 
 /* One query row, one head.  Keys 0 .. last (inclusive) of sequence b.
  * Without partitions: o = sum_j softmax(z)_j v_j with
@@ -378,10 +502,9 @@ static int32_t attend_row(const attn_job* J, int32_t b, const uint16_t* qh,
   for (int32_t j = 0; j < nkeys; ++j) {
     int32_t blk = J->block_tables[(int64_t)b * J->max_blocks_per_seq + j / BS];
     int32_t off = j % BS;
-    const uint16_t* kj =
-        J->k_cache + (((int64_t)blk * J->num_kv_heads + g) * BS + off) * D;
+    const int64_t kj = (((int64_t)blk * J->num_kv_heads + g) * BS + off) * D;
     double dot = 0.0;
-    for (int32_t d = 0; d < D; ++d) dot += bf16_to_f64(qh[d]) * bf16_to_f64(kj[d]);
+    for (int32_t d = 0; d < D; ++d) dot += bf16_to_f64(qh[d]) * k_at(J, kj + d);
     z[j] = J->scale * dot;
   }
   const int32_t P = J->partition_tokens > 0 ? J->partition_tokens : nkeys;
@@ -398,9 +521,8 @@ static int32_t attend_row(const attn_job* J, int32_t b, const uint16_t* qh,
       double p = exp(z[j] - mx);
       sum += p;
       int32_t blk = J->block_tables[(int64_t)b * J->max_blocks_per_seq + j / BS];
-      const uint16_t* vj =
-          J->v_cache + (((int64_t)blk * J->num_kv_heads + g) * BS + j % BS) * D;
-      for (int32_t d = 0; d < D; ++d) os[(int64_t)s * D + d] += p * bf16_to_f64(vj[d]);
+      const int64_t vj = (((int64_t)blk * J->num_kv_heads + g) * BS + j % BS) * D;
+      for (int32_t d = 0; d < D; ++d) os[(int64_t)s * D + d] += p * v_at(J, vj + d);
     }
     m[s] = mx;
     l[s] = sum;
@@ -419,6 +541,14 @@ static int32_t attend_row(const attn_job* J, int32_t b, const uint16_t* qh,
   free(l);
   free(os);
   return 0;
+}
+
+static double k_at(const attn_job* J, int64_t i) {
+  return J->k_cache8 ? oracle_e4m3_to_f64(J->k_cache8[i]) * J->k_scale : bf16_to_f64(J->k_cache[i]);
+}
+
+static double v_at(const attn_job* J, int64_t i) {
+  return J->v_cache8 ? oracle_e4m3_to_f64(J->v_cache8[i]) * J->v_scale : bf16_to_f64(J->v_cache[i]);
 }
 
 /* Work unit = (sequence, query head); units are handed out in order. */
@@ -464,6 +594,8 @@ static void* attn_worker(void* arg) {
  * to sequence b) and for causal varlen / chunked prefill (query rows
  * cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 belong to sequence b).
  * out: [rows][num_heads][head_dim] fp64 (not rounded).  Returns error bits. */
+static int32_t run_attention(attn_job* J, int32_t nthreads);
+
 int32_t oracle_paged_attention(
     double* out, const uint16_t* q, int64_t q_row_stride,
     const int32_t* cu_seqlens_q, int32_t num_seqs, const uint16_t* k_cache,
@@ -491,6 +623,47 @@ int32_t oracle_paged_attention(
   J.block_size = block_size;
   J.scale = scale;
   J.partition_tokens = partition_tokens;
+  return run_attention(&J, nthreads);
+}
+
+/* The same over an FP8 (e4m3fn) cache: key and value elements are
+ * code * k_scale and code * v_scale. */
+int32_t oracle_paged_attention_fp8(
+    double* out, const uint16_t* q, int64_t q_row_stride,
+    const int32_t* cu_seqlens_q, int32_t num_seqs, const uint8_t* k_cache,
+    const uint8_t* v_cache, double k_scale, double v_scale, int32_t num_blocks,
+    const int32_t* block_tables, int32_t max_blocks_per_seq,
+    const int32_t* context_lens, int32_t num_heads, int32_t num_kv_heads,
+    int32_t head_dim, int32_t block_size, double scale, int32_t partition_tokens,
+    int32_t nthreads) {
+  if (num_kv_heads <= 0 || num_heads % num_kv_heads) return -1;
+  attn_job J;
+  memset(&J, 0, sizeof J);
+  J.out = out;
+  J.q = q;
+  J.q_row_stride = q_row_stride;
+  J.cu_seqlens_q = cu_seqlens_q;
+  J.num_seqs = num_seqs;
+  J.k_cache8 = k_cache;
+  J.v_cache8 = v_cache;
+  J.k_scale = k_scale;
+  J.v_scale = v_scale;
+  J.num_blocks = num_blocks;
+  J.block_tables = block_tables;
+  J.max_blocks_per_seq = max_blocks_per_seq;
+  J.context_lens = context_lens;
+  J.num_heads = num_heads;
+  J.num_kv_heads = num_kv_heads;
+  J.head_dim = head_dim;
+  J.block_size = block_size;
+  J.scale = scale;
+  J.partition_tokens = partition_tokens;
+  return run_attention(&J, nthreads);
+}
+
+/* Runs the (sequence, head) units of a job over nthreads threads. */
+static int32_t run_attention(attn_job* Jp, int32_t nthreads) {
+  attn_job J = *Jp;
   pthread_mutex_init(&J.lock, NULL);
   if (nthreads < 1) nthreads = 1;
   if (nthreads > 256) nthreads = 256;

@@ -677,3 +677,164 @@ def test_workload_recipes():
     bt = w.block_tables
     assert w.num_seqs == 128 and bool((bt[:, :128] == bt[0, :128]).all())
     assert int(w.context_lens.min()) >= 2048 + 64 and int(w.context_lens.max()) <= 2048 + 512
+
+
+# ------------------------------------------------------ FP8 (e4m3fn) ----
+#
+# The FP8 KV cache: kv_cache_dtype "fp8" with fp8_e4m3fn and a cache scale
+# per tensor ("Qwen2大模型架构解析与vLLM优化实践" sections 4.1, 4.2, 6.3).
+
+def test_e4m3_closed_forms():
+    v = oracle.e4m3_to_f64(np.arange(256, dtype=np.uint8))
+    assert v[0x00] == 0.0 and np.signbit(v[0x80])
+    assert v[0x38] == 1.0                      # exponent field 7 = bias
+    assert v[0x7E] == 448.0                    # largest finite: 1.75 * 2^8
+    assert v[0x08] == 2.0 ** -6                # smallest normal
+    assert v[0x01] == 2.0 ** -9                # smallest subnormal
+    assert v[0x07] == 7 * 2.0 ** -9            # largest subnormal
+    assert v[0x3C] == 1.5 and v[0x40] == 2.0
+    assert np.isnan(v[0x7F]) and np.isnan(v[0xFF])
+    assert np.sum(np.isnan(v)) == 2
+    assert np.array_equal(v[0x80:0xFF], -v[0x00:0x7F])
+    fin = v[:0x7F]
+    assert np.all(np.diff(fin) > 0)            # codes 0..126 increase
+
+
+def test_e4m3_decode_matches_torch_float8():
+    t = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+    v = oracle.e4m3_to_f64(np.arange(256, dtype=np.uint8))
+    assert np.array_equal(np.isnan(t), np.isnan(v))
+    assert np.array_equal(t[~np.isnan(t)], v[~np.isnan(v)])
+
+
+def _nearest_e4m3(x):
+    """Brute force: the finite code nearest to x, ties to the even code,
+    magnitudes past 448 saturated."""
+    vals = np.array([float(np.ldexp(1.0 + (c & 7) / 8.0, ((c >> 3) & 15) - 7)) if c >> 3
+                     else float(np.ldexp(c & 7, -9)) for c in range(0x7F)])
+    out = []
+    for xv in np.asarray(x, dtype=np.float64):
+        a = min(abs(xv), 448.0)
+        d = np.abs(vals - a)
+        best = np.flatnonzero(d == d.min())
+        c = int(best[0]) if len(best) == 1 else int(best[best % 2 == 0][0])
+        out.append(c | (0x80 if np.signbit(xv) else 0))
+    return np.array(out, dtype=np.uint8)
+
+
+def test_e4m3_encode_brute_force_nearest_even():
+    v = oracle.e4m3_to_f64(np.arange(0x7F, dtype=np.uint8))
+    mids = (v[:-1] + v[1:]) / 2                # every tie
+    rng = np.random.default_rng(21)
+    x = np.concatenate([mids, -mids, v, -v, rng.standard_normal(3000) * 50,
+                        rng.standard_normal(500) * 2.0 ** -7, [447.9, 448.0, 460.0, 464.0,
+                                                               1e6, -1e6, 2.0 ** -10,
+                                                               3 * 2.0 ** -11]])
+    x = x.astype(np.float32)
+    assert np.array_equal(oracle.f32_to_e4m3(x), _nearest_e4m3(x.astype(np.float64)))
+    # the midpoint between 1 and 1.125 goes to 1 (even), between 1.125 and
+    # 1.25 to 1.25 (even)
+    assert oracle.f32_to_e4m3(np.float32(1.0625)) == 0x38
+    assert oracle.f32_to_e4m3(np.float32(1.1875)) == 0x3A
+    assert oracle.f32_to_e4m3(np.float32(np.inf)) == 0x7E
+    assert oracle.f32_to_e4m3(np.float32(-np.inf)) == 0xFE
+    assert oracle.f32_to_e4m3(np.float32(np.nan)) == 0x7F
+
+
+def test_e4m3_encode_matches_torch_in_range():
+    rng = np.random.default_rng(22)
+    x = (rng.standard_normal(200000) * np.exp(rng.uniform(-12, 6, 200000))).astype(np.float32)
+    x = x[np.abs(x) <= 448]
+    t = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(oracle.f32_to_e4m3(x), t)
+
+
+def _fp8_caches(w):
+    shape = tuple(w.k_cache.shape)
+    return np.zeros(shape, dtype=np.uint8), np.zeros(shape, dtype=np.uint8)
+
+
+def test_append_fp8_is_bf16_append_then_quantize():
+    w = W.custom(8, 2, ctx=[5, 40, 100], q_lens=[5, 1, 7], seed=23)
+    H, Hkv, D, BS = w.num_heads, w.num_kv_heads, w.head_dim, w.block_size
+    table = oracle.rope_table(1e6, w.max_pos, D)
+    q16, kc16, vc16 = u16(w.qkv), u16(w.k_cache), u16(w.v_cache)
+    assert oracle.rope_cache_append(q16, w.positions, w.slot_mapping, kc16, vc16, table,
+                                    H, Hkv, D, BS) == 0
+    q8 = u16(w.qkv)
+    kc8, vc8 = _fp8_caches(w)
+    ks, vs = 0.037, 0.011
+    assert oracle.rope_cache_append_fp8(q8, w.positions, w.slot_mapping, kc8, vc8, table,
+                                        H, Hkv, D, BS, ks, vs) == 0
+    assert np.array_equal(q8, q16)             # q as before
+    slots = w.slot_mapping.numpy()
+    blk, off = slots // BS, slots % BS
+    k16 = f64(kc16[blk, :, off]).astype(np.float32)
+    v16 = f64(vc16[blk, :, off]).astype(np.float32)
+    assert np.array_equal(kc8[blk, :, off], oracle.f32_to_e4m3(k16 / np.float32(ks)))
+    assert np.array_equal(vc8[blk, :, off], oracle.f32_to_e4m3(v16 / np.float32(vs)))
+    # untouched slots stay as they were
+    mask = np.ones(kc8.shape[:1] + kc8.shape[2:3], dtype=bool)
+    mask[blk, off] = False
+    assert not kc8.transpose(0, 2, 1, 3)[mask].any()
+
+
+def test_append_fp8_hand_example():
+    """Position 0 (no rotation): k = 1.0 under k_scale 0.5 is 2.0 = 0x40;
+    v = 3.0 under v_scale 2 is 1.5 = 0x3C; v = 1000 saturates to 0x7E."""
+    H, Hkv, D, BS = 1, 1, 128, 16
+    qkv = np.zeros((1, (H + 2 * Hkv) * D), dtype=np.uint16)
+    qkv[0, D:2 * D] = oracle.bf16_round(np.full(D, 1.0))
+    qkv[0, 2 * D:] = oracle.bf16_round(np.full(D, 3.0))
+    qkv[0, 2 * D + 5] = oracle.bf16_round(np.array([1000.0]))[0]
+    kc = np.zeros((2, Hkv, BS, D), dtype=np.uint8)
+    vc = kc.copy()
+    table = oracle.rope_table(1e6, 8, D)
+    assert oracle.rope_cache_append_fp8(qkv, [0], [19], kc, vc, table, H, Hkv, D, BS,
+                                        0.5, 2.0) == 0
+    assert np.all(kc[1, 0, 3] == 0x40)
+    assert vc[1, 0, 3, 5] == 0x7E
+    assert np.all(np.delete(vc[1, 0, 3], 5) == 0x3C)
+    assert not kc[0].any() and not vc[0].any()
+
+
+def test_attention_fp8_equals_bf16_on_representable_values():
+    """Codes whose values times a power-of-two scale are bf16 numbers: the
+    FP8 attention equals the bf16 attention over those numbers exactly."""
+    w = W.custom(8, 2, ctx=[3, 70, 200], q_lens=[1, 1, 1], seed=24)
+    rng = np.random.default_rng(24)
+    codes_k = rng.integers(0, 256, size=w.k_cache.shape, dtype=np.uint8)
+    codes_v = rng.integers(0, 256, size=w.v_cache.shape, dtype=np.uint8)
+    for c in (codes_k, codes_v):
+        c[(c & 0x7F) == 0x7F] = 0x3A            # no NaN codes
+    ks, vs = 2.0 ** -3, 2.0 ** 2
+    kb = oracle.bf16_round(oracle.e4m3_to_f64(codes_k) * ks)
+    vb = oracle.bf16_round(oracle.e4m3_to_f64(codes_v) * vs)
+    assert np.array_equal(f64(kb), oracle.e4m3_to_f64(codes_k) * ks)
+    q = u16(w.q_view())
+    H, Hkv, D, BS = w.num_heads, w.num_kv_heads, w.head_dim, w.block_size
+    ref, e1 = oracle.paged_attention(q, kb, vb, w.block_tables, w.context_lens, H, Hkv, D, BS)
+    out, e2 = oracle.paged_attention_fp8(q, codes_k, codes_v, ks, vs, w.block_tables,
+                                         w.context_lens, H, Hkv, D, BS)
+    assert e1 == 0 and e2 == 0
+    assert np.array_equal(out, ref)
+
+
+def test_attention_fp8_scale_identities():
+    """v_scale multiplies the output; k_scale multiplies the logits."""
+    w = W.custom(4, 2, ctx=[50, 300], q_lens=[4, 1], seed=25)
+    rng = np.random.default_rng(25)
+    ck = rng.integers(0, 0x7F, size=w.k_cache.shape, dtype=np.uint8) | \
+        (rng.integers(0, 2, size=w.k_cache.shape, dtype=np.uint8) << 7)
+    cv = rng.integers(0, 0x7F, size=w.v_cache.shape, dtype=np.uint8) | \
+        (rng.integers(0, 2, size=w.v_cache.shape, dtype=np.uint8) << 7)
+    q = u16(w.q_view())
+    H, Hkv, D, BS = w.num_heads, w.num_kv_heads, w.head_dim, w.block_size
+    args = (w.block_tables, w.context_lens, H, Hkv, D, BS)
+    base, _ = oracle.paged_attention_fp8(q, ck, cv, 0.01, 1.0, *args,
+                                         cu_seqlens_q=w.cu_seqlens_q)
+    sv, _ = oracle.paged_attention_fp8(q, ck, cv, 0.01, 0.3, *args, cu_seqlens_q=w.cu_seqlens_q)
+    assert np.allclose(sv, 0.3 * base, rtol=1e-12, atol=0)
+    sk, _ = oracle.paged_attention_fp8(q, ck, cv, 1.0, 1.0, *args, cu_seqlens_q=w.cu_seqlens_q,
+                                       scale=0.01 * D ** -0.5)
+    assert np.allclose(sk, base, rtol=1e-12, atol=1e-15)
