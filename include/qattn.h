@@ -181,6 +181,38 @@ int qattn_rope_cache_append_ex(void* q, int64_t q_row_stride, const void* k,
                                const void* k_norm_weight, float norm_eps,
                                qattn_dims dims, int32_t* err_word, void* stream);
 
+/* ---- FP8 KV cache ----------------------------------------------------
+ *
+ * kv_cache_dtype "fp8": fp8_e4m3fn codes with one cache scale per tensor
+ * (the K scale and the V scale of the layer), "Qwen2大模型架构解析与vLLM
+ * 优化实践" sections 4.1 (KV cache quantisation), 4.2 (the cache scale
+ * loaded per tensor, kv_cache_dtype="fp8") and 6.3 (fp8_e4m3fn).  The cache
+ * has the bf16 cache's shape with 1-byte elements: [num_blocks][Hkv]
+ * [block_size][head_dim] uint8, 16-byte aligned.  Element x of a bf16 cache
+ * is stored as e4m3(x / scale): the fp32 quotient (correctly rounded)
+ * rounded to the nearest e4m3fn value, ties to even, magnitudes past 448
+ * saturated to 448.  The attention entry points read code * scale: the
+ * codes are converted exactly to f16 and both tensor-core products run in
+ * f16 with fp32 accumulation (q and the softmax weights are rounded to f16;
+ * q must stay within f16's range, |q| < 65504), k_scale multiplies the
+ * logits' scale and v_scale the output.  Scales must be finite, positive
+ * and normal fp32 (QATTN_ERR_INVALID_ARG otherwise). */
+
+/* qattn_rope_cache_append_ex into an FP8 cache: the bf16 key (after bias,
+ * norm and RoPE) and value rows are stored as e4m3(x / k_scale) and
+ * e4m3(x / v_scale).  q is rotated in place exactly as by the bf16 entry
+ * points.  Same arguments and errors otherwise. */
+int qattn_rope_cache_append_fp8(void* q, int64_t q_row_stride, const void* k,
+                                int64_t k_row_stride, const void* v,
+                                int64_t v_row_stride, const int32_t* positions,
+                                const int32_t* slot_mapping, int32_t num_tokens,
+                                void* k_cache, void* v_cache, int32_t num_blocks,
+                                const float* cos_sin, int32_t max_pos,
+                                const void* qkv_bias, const void* q_norm_weight,
+                                const void* k_norm_weight, float norm_eps,
+                                float k_scale, float v_scale, qattn_dims dims,
+                                int32_t* err_word, void* stream);
+
 /* Bytes of device workspace qattn_paged_decode needs (256-byte aligned
  * pointer, contents need not be initialised).  Depends only on the
  * arguments.  The workspace holds the split-KV partial results between the
@@ -225,6 +257,20 @@ int qattn_paged_decode(void* out, const void* q, int64_t q_row_stride,
                        int32_t num_seqs, int32_t max_context_len,
                        qattn_dims dims, void* workspace, size_t workspace_bytes,
                        int32_t* err_word, void* stream);
+
+/* qattn_paged_decode over FP8 caches (uint8 e4m3 codes, see above):
+ * out = attention over code * k_scale keys and code * v_scale values, on
+ * the tensor-core kernel for every group size and block size.  Workspace
+ * as qattn_paged_decode_workspace_size.  Same arguments and errors as
+ * qattn_paged_decode, plus QATTN_ERR_INVALID_ARG for an invalid scale. */
+int qattn_paged_decode_fp8(void* out, const void* q, int64_t q_row_stride,
+                           const void* k_cache, const void* v_cache,
+                           int32_t num_blocks, const int32_t* block_tables,
+                           int32_t max_blocks_per_seq,
+                           const int32_t* context_lens, int32_t num_seqs,
+                           int32_t max_context_len, float k_scale, float v_scale,
+                           qattn_dims dims, void* workspace, size_t workspace_bytes,
+                           int32_t* err_word, void* stream);
 
 /* Bytes of workspace qattn_paged_decode_shared_prefix needs (same rules as
  * qattn_paged_decode_workspace_size; room for the prefix parts too). */

@@ -101,24 +101,46 @@ bool encode_cache_map(CUtensorMap* map, const void* cache, int32_t num_blocks,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// An FP8 (e4m3) cache [num_blocks][Hkv][BS][128] uint8 seen as a 2-D tensor
+// of 128-byte token rows; a box of (128, BS) is one (block, kv head) tile,
+// landing as BS rows of 128 B with the 128-byte swizzle (row r's 16-byte
+// chunk c at c ^ (r & 7)).
+bool encode_cache_map_fp8(CUtensorMap* map, const void* cache, int32_t num_blocks,
+                          int32_t num_kv_heads, int32_t block_size) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {
+      static_cast<cuuint64_t>(kHeadDim),
+      static_cast<cuuint64_t>(num_blocks) * num_kv_heads * block_size};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDim)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kHeadDim),
+                             static_cast<cuuint32_t>(block_size)};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(cache), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // A small cache of encoded maps: the same caches are used call after call.
 struct MapEntry {
   const void* ptr;
   int32_t num_blocks;
   int32_t num_kv_heads;
   int32_t block_size;
+  int32_t fp8;
   CUtensorMap map;
 };
 
 bool cached_cache_map(CUtensorMap* out, const void* cache, int32_t num_blocks,
-                      int32_t num_kv_heads, int32_t block_size) {
+                      int32_t num_kv_heads, int32_t block_size, int32_t fp8 = 0) {
   static std::mutex mu;
   static MapEntry entries[16];
   static int used = 0, next = 0;
   std::lock_guard<std::mutex> lk(mu);
   for (int i = 0; i < used; ++i) {
     if (entries[i].ptr == cache && entries[i].num_blocks == num_blocks &&
-        entries[i].num_kv_heads == num_kv_heads && entries[i].block_size == block_size) {
+        entries[i].num_kv_heads == num_kv_heads && entries[i].block_size == block_size &&
+        entries[i].fp8 == fp8) {
       *out = entries[i].map;
       return true;
     }
@@ -128,7 +150,10 @@ bool cached_cache_map(CUtensorMap* out, const void* cache, int32_t num_blocks,
   e.num_blocks = num_blocks;
   e.num_kv_heads = num_kv_heads;
   e.block_size = block_size;
-  if (!encode_cache_map(&e.map, cache, num_blocks, num_kv_heads, block_size)) return false;
+  e.fp8 = fp8;
+  if (!(fp8 ? encode_cache_map_fp8(&e.map, cache, num_blocks, num_kv_heads, block_size)
+            : encode_cache_map(&e.map, cache, num_blocks, num_kv_heads, block_size)))
+    return false;
   entries[next] = e;
   next = (next + 1) % 16;
   if (used < 16) ++used;
@@ -184,6 +209,9 @@ int check_cache(const void* k_cache, const void* v_cache, int32_t num_blocks,
 }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? QATTN_OK : QATTN_ERR_CUDA; }
+
+// A cache scale: finite, positive and normal (its reciprocal stays finite).
+bool valid_scale(float s) { return s == s && !isinf(s) && s >= 1.17549435e-38f; }
 
 }  // namespace
 
@@ -252,14 +280,14 @@ int qattn_rope_table_build_scaled(float* host_cos_sin, int32_t max_pos, int32_t 
   return QATTN_OK;
 }
 
-int qattn_rope_cache_append_ex(void* q, int64_t q_row_stride, const void* k,
-                               int64_t k_row_stride, const void* v, int64_t v_row_stride,
-                               const int32_t* positions, const int32_t* slot_mapping,
-                               int32_t num_tokens, void* k_cache, void* v_cache,
-                               int32_t num_blocks, const float* cos_sin, int32_t max_pos,
-                               const void* qkv_bias, const void* q_norm_weight,
-                               const void* k_norm_weight, float norm_eps, qattn_dims dims,
-                               int32_t* err_word, void* stream) {
+// The append into a bf16 cache (kv_fp8 = 0) or an e4m3 cache.
+static int append_common(void* q, int64_t q_row_stride, const void* k, int64_t k_row_stride,
+                         const void* v, int64_t v_row_stride, const int32_t* positions,
+                         const int32_t* slot_mapping, int32_t num_tokens, void* k_cache,
+                         void* v_cache, int32_t num_blocks, const float* cos_sin,
+                         int32_t max_pos, const void* qkv_bias, const void* q_norm_weight,
+                         const void* k_norm_weight, float norm_eps, int kv_fp8, float k_scale,
+                         float v_scale, qattn_dims dims, int32_t* err_word, void* stream) {
   int st = check_dims(dims);
   if (st != QATTN_OK) return st;
   if (num_tokens < 0) return QATTN_ERR_INVALID_ARG;
@@ -304,7 +332,40 @@ int qattn_rope_cache_append_ex(void* q, int64_t q_row_stride, const void* k,
   a.q_norm_w = q_norm_weight;
   a.k_norm_w = k_norm_weight;
   a.norm_eps = norm_eps;
+  a.kv_fp8 = kv_fp8;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
   return cuda_status(launch_rope_append(a, static_cast<cudaStream_t>(stream)));
+}
+
+int qattn_rope_cache_append_ex(void* q, int64_t q_row_stride, const void* k,
+                               int64_t k_row_stride, const void* v, int64_t v_row_stride,
+                               const int32_t* positions, const int32_t* slot_mapping,
+                               int32_t num_tokens, void* k_cache, void* v_cache,
+                               int32_t num_blocks, const float* cos_sin, int32_t max_pos,
+                               const void* qkv_bias, const void* q_norm_weight,
+                               const void* k_norm_weight, float norm_eps, qattn_dims dims,
+                               int32_t* err_word, void* stream) {
+  return append_common(q, q_row_stride, k, k_row_stride, v, v_row_stride, positions,
+                       slot_mapping, num_tokens, k_cache, v_cache, num_blocks, cos_sin, max_pos,
+                       qkv_bias, q_norm_weight, k_norm_weight, norm_eps, 0, 1.0f, 1.0f, dims,
+                       err_word, stream);
+}
+
+int qattn_rope_cache_append_fp8(void* q, int64_t q_row_stride, const void* k,
+                                int64_t k_row_stride, const void* v, int64_t v_row_stride,
+                                const int32_t* positions, const int32_t* slot_mapping,
+                                int32_t num_tokens, void* k_cache, void* v_cache,
+                                int32_t num_blocks, const float* cos_sin, int32_t max_pos,
+                                const void* qkv_bias, const void* q_norm_weight,
+                                const void* k_norm_weight, float norm_eps, float k_scale,
+                                float v_scale, qattn_dims dims, int32_t* err_word,
+                                void* stream) {
+  if (!valid_scale(k_scale) || !valid_scale(v_scale)) return QATTN_ERR_INVALID_ARG;
+  return append_common(q, q_row_stride, k, k_row_stride, v, v_row_stride, positions,
+                       slot_mapping, num_tokens, k_cache, v_cache, num_blocks, cos_sin, max_pos,
+                       qkv_bias, q_norm_weight, k_norm_weight, norm_eps, 1, k_scale, v_scale,
+                       dims, err_word, stream);
 }
 
 int qattn_rope_cache_append(void* q, int64_t q_row_stride, const void* k, int64_t k_row_stride,
@@ -342,7 +403,8 @@ int decode_common(void* out, const void* q, int64_t q_row_stride, int32_t q_rows
                   const qattn_dims& dims, void* workspace, size_t workspace_bytes,
                   int32_t* err_word, cudaStream_t stream, const CUtensorMap& kmap,
                   const CUtensorMap& vmap, int num_sms, int32_t prefix_len = 0,
-                  int32_t part_base = 0, int32_t extra_parts = 0) {
+                  int32_t part_base = 0, int32_t extra_parts = 0, int32_t kv_fp8 = 0,
+                  float k_scale = 1.0f, float v_scale = 1.0f) {
   const size_t need = decode_workspace_bytes(num_seqs, max_context_len, dims.num_kv_heads,
                                              dims.num_heads / dims.num_kv_heads, extra_parts);
   if (workspace == nullptr || workspace_bytes < need ||
@@ -362,14 +424,16 @@ int decode_common(void* out, const void* q, int64_t q_row_stride, int32_t q_rows
   a.num_heads = dims.num_heads;
   a.num_kv_heads = dims.num_kv_heads;
   a.block_size = dims.block_size;
-  a.scale_log2 = scale_of(dims) * kLog2e;
+  a.scale_log2 = scale_of(dims) * kLog2e * (kv_fp8 ? k_scale : 1.0f);
+  a.kv_fp8 = kv_fp8;
+  a.v_scale = kv_fp8 ? v_scale : 1.0f;
   a.err_word = err_word;
   a.ws = carve_decode_workspace(workspace, num_seqs, max_context_len, dims.num_kv_heads,
                                 dims.num_heads / dims.num_kv_heads, extra_parts);
   a.prefix_len = prefix_len;
   a.part_base = part_base;
   const int group = dims.num_heads / dims.num_kv_heads;
-  if (use_tc_decode(group, dims.block_size)) {
+  if (kv_fp8 || use_tc_decode(group, dims.block_size)) {
     CUtensorMap qmap;
     if (!encode_q_group_map(&qmap, q, q_row_stride, q_rows, dims.num_heads, group))
       return QATTN_ERR_CUDA;
@@ -416,6 +480,33 @@ int qattn_paged_decode(void* out, const void* q, int64_t q_row_stride, const voi
                        max_blocks_per_seq, context_lens, num_seqs, max_context_len, dims,
                        workspace, workspace_bytes, err_word, static_cast<cudaStream_t>(stream),
                        kmap, vmap, sms);
+}
+
+int qattn_paged_decode_fp8(void* out, const void* q, int64_t q_row_stride, const void* k_cache,
+                           const void* v_cache, int32_t num_blocks, const int32_t* block_tables,
+                           int32_t max_blocks_per_seq, const int32_t* context_lens,
+                           int32_t num_seqs, int32_t max_context_len, float k_scale,
+                           float v_scale, qattn_dims dims, void* workspace,
+                           size_t workspace_bytes, int32_t* err_word, void* stream) {
+  int st = check_dims(dims);
+  if (st != QATTN_OK) return st;
+  if (num_seqs < 0 || !valid_scale(k_scale) || !valid_scale(v_scale))
+    return QATTN_ERR_INVALID_ARG;
+  if (num_seqs == 0) return QATTN_OK;
+  st = check_attention_args(out, q, q_row_stride, k_cache, v_cache, num_blocks, block_tables,
+                            max_blocks_per_seq, context_lens, max_context_len, dims);
+  if (st != QATTN_OK) return st;
+  CUtensorMap kmap, vmap;
+  if (!cached_cache_map(&kmap, k_cache, num_blocks, dims.num_kv_heads, dims.block_size, 1) ||
+      !cached_cache_map(&vmap, v_cache, num_blocks, dims.num_kv_heads, dims.block_size, 1))
+    return QATTN_ERR_CUDA;
+  const int sms = num_sms_current();
+  if (sms <= 0) return QATTN_ERR_CUDA;
+  return decode_common(out, q, q_row_stride, num_seqs, nullptr, k_cache, v_cache, num_blocks,
+                       block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                       max_context_len, dims, workspace, workspace_bytes, err_word,
+                       static_cast<cudaStream_t>(stream), kmap, vmap, sms, 0, 0, 0, 1, k_scale,
+                       v_scale);
 }
 
 size_t qattn_paged_decode_shared_prefix_workspace_size(int32_t num_seqs,

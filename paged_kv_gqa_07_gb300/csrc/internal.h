@@ -76,6 +76,9 @@ struct RopeAppendArgs {
   int32_t num_kv_heads;
   int32_t block_size;      // tokens per cache block: 16, 32 or 64
   int32_t* err_word;
+  // FP8 cache: e4m3 codes of x / k_scale and x / v_scale
+  int32_t kv_fp8;
+  float k_scale, v_scale;
   // Optional steps before RoPE (null: skipped): the qkv projection bias
   // [(H + 2 Hkv) * 128] bf16, and Qwen3's per-head RMSNorm weights [128]
   // bf16 for q and for k, with eps.
@@ -123,7 +126,9 @@ struct DecodeArgs {
   int32_t num_heads;
   int32_t num_kv_heads;
   int32_t block_size;      // tokens per cache block: 16, 32 or 64 (16 for K2)
-  float scale_log2;        // softmax scale * log2(e)
+  float scale_log2;        // softmax scale * log2(e) (* k_scale for an FP8 cache)
+  int32_t kv_fp8;          // the caches hold e4m3 codes (tensor-core kernel only)
+  float v_scale;           // FP8: multiplies the output
   int32_t* err_word;
   DecodeWorkspace ws;
   // Shared-prefix (cascade) mode: the kernel attends only to tokens

@@ -37,6 +37,18 @@
 //   * keys past the context are masked in S and their V rows zeroed.
 //   * every wait is bounded; on a timeout all roles unwind, drain their
 //     copies and MMAs, and TMEM is freed.
+//
+// FP8 cache (kFp8; kv_cache_dtype "fp8", fp8_e4m3fn codes with a cache
+// scale per tensor, "Qwen2大模型架构解析与vLLM优化实践" sections 4.1, 4.2,
+// 6.3): the cache tiles are half the bytes (128 B per token row) and land
+// by TMA in 4-deep 16 KB rings; four more warps (6-9, thread = token row)
+// dequantise them -- the e4m3 -> f16 conversion is exact -- K into tensor
+// memory (the A operand of S^T = K . Q^T is read from TMEM, so the converted
+// K never touches shared memory) and V into the same swizzled MN-major f16
+// layout the bf16 path gets from TMA, with rows past the context written as
+// zeros.  Both products run in f16 (Q^T converted in place once per unit,
+// P^T written as f16); k_scale is folded into the logit scale and v_scale
+// into the epilogue.
 #include <math.h>
 
 #include "common.cuh"
@@ -49,41 +61,54 @@ constexpr int kTile = kTcTileTokens;  // 128 tokens
 constexpr int kN = 16;                // MMA N: the query group padded to 16 heads
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
-constexpr int kThreads = 6 * 32;
+constexpr int kConvWarp0 = 6;   // FP8 only: warps 6-9 dequantise
 // A tile of 128 tokens lands as 8-token row groups 2 KB apart whatever the
 // block size (a block's box is block_size / 8 such groups), so the code below
 // addresses it in 16-token / 4 KB units.
 constexpr int kCacheTileBytes = 16 * kHeadDim * 2;  // 16 tokens: 4 KB
 constexpr int kTileBytes = kTile * kHeadDim * 2;    // 32 KB
-constexpr int kKStages = 3;
-constexpr int kVStages = 3;
 constexpr int kSmallHalf = kN * 128;     // 16 rows x 128 B
 constexpr int kSmallBytes = 2 * kSmallHalf;
-constexpr uint32_t kTmemCols = 64;
 constexpr uint32_t kColO = 32;   // O^T of unit u at kColO + (u & 1) * kN
+constexpr uint32_t kColK = 64;   // FP8: dequantised K of tile n at kColK + (n & 1) * 64
 constexpr float kLazyRescale = 8.0f;
 constexpr int kMaxSmemSeqs = 2048;
 
-constexpr int kOffK = 0;
-constexpr int kOffV = kOffK + kKStages * kTileBytes;
-constexpr int kOffQ = kOffV + kVStages * kTileBytes;  // 2 slots of Q^T
-constexpr int kOffP = kOffQ + 2 * kSmallBytes;        // 2 buffers of P^T
-constexpr int kOffRed = kOffP + 2 * kSmallBytes;      // [2][4][16] fp32
-constexpr int kOffLsum = kOffRed + 2 * 4 * kN * 4;    // [2][4][16] fp32
-constexpr int kOffBars = kOffLsum + 2 * 4 * kN * 4;
-// k_full[2] k_empty[2] v_full[4] v_empty[4] q_full[2] q_empty[2] s_full[2]
-// s_free[2] p_full[2] pv_done[2] o_free[2] rbar mma_done
-constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 * 7 + 2;
-constexpr int kOffMisc = kOffBars + kNumBars * 8;
-constexpr int kOffLens = kOffMisc + 64;
-constexpr int kSmemBytes = kOffLens + kMaxSmemSeqs * 4 + 1024;
+// Shared-memory layout.  bf16: 3 + 3 ring slots of 32 KB cache tiles.  FP8:
+// 4 + 4 slots of 16 KB code tiles, then two 32 KB f16 V tiles.
+template <bool kFp8>
+struct Lay {
+  static constexpr int kWarps = kFp8 ? 10 : 6;
+  static constexpr int kThreads = kWarps * 32;
+  static constexpr int kKStages = kFp8 ? 4 : 3;
+  static constexpr int kVStages = kFp8 ? 4 : 3;
+  static constexpr int kStageBytes = kFp8 ? kTile * kHeadDim : kTileBytes;
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kOffK + kKStages * kStageBytes;
+  static constexpr int kOffVc = kOffV + kVStages * kStageBytes;  // FP8: f16 V tiles
+  static constexpr int kOffQ = kOffVc + (kFp8 ? 2 * kTileBytes : 0);  // 2 slots of Q^T
+  static constexpr int kOffP = kOffQ + 2 * kSmallBytes;               // 2 buffers of P^T
+  static constexpr int kOffRed = kOffP + 2 * kSmallBytes;             // [2][4][16] fp32
+  static constexpr int kOffLsum = kOffRed + 2 * 4 * kN * 4;           // [2][4][16] fp32
+  static constexpr int kOffBars = kOffLsum + 2 * 4 * kN * 4;
+  // k_full/k_empty[kKStages] v_full/v_empty[kVStages] q_full q_empty s_full
+  // s_free p_full pv_done o_free [2] rbar mma_done; FP8 adds kc_full
+  // kc_empty vc_full vc_empty qc_full [2]
+  static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 * 7 + 2 + (kFp8 ? 10 : 0);
+  static constexpr int kOffMisc = kOffBars + kNumBars * 8;
+  static constexpr int kOffLens = kOffMisc + 64;
+  static constexpr int kSmemBytes = kOffLens + kMaxSmemSeqs * 4 + 1024;
+  static constexpr uint32_t kTmemCols = kFp8 ? 256 : 64;
+};
+static_assert(Lay<true>::kSmemBytes <= 227 * 1024, "FP8 decode shared memory");
+static_assert(Lay<false>::kSmemBytes <= 227 * 1024, "decode shared memory");
 
 struct Misc {
   uint32_t tmem;
   int abort;
   int b0;
   int off0;
-  int warp_sums[6];
+  int warp_sums[10];
 };
 
 __device__ __forceinline__ int seq_len_eff(const DecodeArgs& a, int b) {
@@ -129,7 +154,8 @@ __device__ __forceinline__ int64_t q_row_of(const DecodeArgs& a, int b) {
   return a.cu_seqlens_q != nullptr ? static_cast<int64_t>(a.cu_seqlens_q[b]) : b;
 }
 
-// Inclusive scan over the CTA's 192 threads.
+// Inclusive scan over the CTA's NW warps.
+template <int NW>
 __device__ __forceinline__ int block_scan(int v, int* warp_sums, int* block_total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
@@ -140,30 +166,34 @@ __device__ __forceinline__ int block_scan(int v, int* warp_sums, int* block_tota
   if (lane == 31) warp_sums[warp] = v;
   __syncthreads();
   if (warp == 0) {
-    int w = lane < 6 ? warp_sums[lane] : 0;
+    int w = lane < NW ? warp_sums[lane] : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int n = __shfl_up_sync(0xffffffffu, w, o);
       if (lane >= o) w += n;
     }
-    if (lane < 6) warp_sums[lane] = w;
+    if (lane < NW) warp_sums[lane] = w;
   }
   __syncthreads();
   const int add = warp > 0 ? warp_sums[warp - 1] : 0;
-  *block_total = warp_sums[5];
+  *block_total = warp_sums[NW - 1];
   __syncthreads();
   return v + add;
 }
 
-template <int G>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int G, bool kFp8>
+__global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
     paged_decode_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                            const __grid_constant__ CUtensorMap vmap,
                            const __grid_constant__ CUtensorMap qmap, const DecodeArgs a) {
+  using L = Lay<kFp8>;
+  constexpr int kThreads = L::kThreads;
+  constexpr int kKStages = L::kKStages;
+  constexpr int kVStages = L::kVStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBars);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBars);
   uint64_t* k_full = bars;
   uint64_t* k_empty = k_full + kKStages;
   uint64_t* v_full = k_empty + kKStages;
@@ -180,10 +210,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* o_free = pv_done + 2;
   uint64_t* rbar = o_free + 2;
   uint64_t* mma_done = rbar + 1;
-  Misc* misc = reinterpret_cast<Misc*>(smem + kOffMisc);
-  int* s_len = reinterpret_cast<int*>(smem + kOffLens);
-  float* red = reinterpret_cast<float*>(smem + kOffRed);
-  float* lsum = reinterpret_cast<float*>(smem + kOffLsum);
+  // FP8: kc_full[b] / vc_full[b] -- the converters have written K of tile n
+  // into TMEM / V of tile n as f16 (tiles of parity b); kc_empty / vc_empty
+  // -- the MMA that read them is done; qc_full[s] -- Q^T slot s is f16.
+  uint64_t* kc_full = mma_done + 1;
+  uint64_t* kc_empty = kc_full + 2;
+  uint64_t* vc_full = kc_empty + 2;
+  uint64_t* vc_empty = vc_full + 2;
+  uint64_t* qc_full = vc_empty + 2;
+  Misc* misc = reinterpret_cast<Misc*>(smem + L::kOffMisc);
+  int* s_len = reinterpret_cast<int*>(smem + L::kOffLens);
+  float* red = reinterpret_cast<float*>(smem + L::kOffRed);
+  float* lsum = reinterpret_cast<float*>(smem + L::kOffLsum);
   volatile int* abort_flag = &misc->abort;
   const uint32_t sbase = smem_u32(smem);
 
@@ -192,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int B = a.num_seqs;
   const int bpt = kTile / a.block_size;    // cache blocks per tile: 8, 4 or 2
   const int groups = a.block_size / 8;     // 8-row groups per block box
-  const uint32_t blk_bytes = static_cast<uint32_t>(a.block_size) * kHeadDim * 2;
+  const uint32_t blk_bytes = static_cast<uint32_t>(a.block_size) * kHeadDim * (kFp8 ? 1 : 2);
 
   prefetch_decode_metadata(a);
   // ---- plan: tile count, this CTA's run [c0, c1), its first unit ----
@@ -208,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     local += Hkv * ((L + kTile - 1) / kTile);
   }
   int total;
-  block_scan(local, misc->warp_sums, &total);
+  block_scan<L::kWarps>(local, misc->warp_sums, &total);
   const RunSplit split{total, static_cast<int>(gridDim.x), kTcMinTilesPerCta};
   const int c0 = split.begin(blockIdx.x);
   const int c1 = split.begin(blockIdx.x + 1);
@@ -218,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int L = b < B ? seq_len_cached(a, s_len, b) : 0;
     const int u = Hkv * ((L + kTile - 1) / kTile);
     int tile_total;
-    const int incl = block_scan(u, misc->warp_sums, &tile_total);
+    const int incl = block_scan<L::kWarps>(u, misc->warp_sums, &tile_total);
     const int excl = running + incl - u;
     if (u > 0 && excl <= c0 && c0 < excl + u) {
       misc->b0 = b;
@@ -235,13 +273,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- set-up: barriers, zeroed Q^T / P^T buffers, TMEM ----
   if (tid == 0) {
+    // FP8: the converter warps (4) release the code tiles; bf16: the MMA.
     for (int s = 0; s < kKStages; ++s) {
       mbar_init(&k_full[s], 1);
-      mbar_init(&k_empty[s], 1);
+      mbar_init(&k_empty[s], kFp8 ? 4 : 1);
     }
     for (int s = 0; s < kVStages; ++s) {
       mbar_init(&v_full[s], 1);
-      mbar_init(&v_empty[s], 1);
+      mbar_init(&v_empty[s], kFp8 ? 4 : 1);
+    }
+    if (kFp8) {
+      for (int s = 0; s < 2; ++s) {
+        mbar_init(&kc_full[s], 4);
+        mbar_init(&kc_empty[s], 1);
+        mbar_init(&vc_full[s], 4);
+        mbar_init(&vc_empty[s], 1);
+        mbar_init(&qc_full[s], 4);
+      }
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&q_full[s], 1);
@@ -258,10 +306,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_barrier_init();
   }
   for (int i = tid; i < 4 * kSmallBytes / 16; i += kThreads)
-    sts128(sbase + kOffQ + i * 16, 0u, 0u, 0u, 0u);  // rows >= G of Q^T stay zero
+    sts128(sbase + L::kOffQ + i * 16, 0u, 0u, 0u, 0u);  // rows >= G of Q^T stay zero
   fence_proxy_async_smem();
   if (warp == kMmaWarp) {
-    tmem_alloc(&misc->tmem, kTmemCols);
+    tmem_alloc(&misc->tmem, L::kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -303,9 +351,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       okv = __shfl_sync(0xffffffffu, okv, 0);
       if (!okv) return false;
-      if (lane < bpt && id_lane >= 0)
-        tma_load_cache_tile(smem + kOffV + vs * kTileBytes + lane * blk_bytes, &vmap,
-                            id_lane * Hkv + gg, groups, &v_full[vs]);
+      if (lane < bpt && id_lane >= 0) {
+        uint8_t* dst = smem + L::kOffV + vs * L::kStageBytes + lane * blk_bytes;
+        if constexpr (kFp8)
+          tma_load_2d(dst, &vmap, 0, (id_lane * Hkv + gg) * a.block_size, &v_full[vs]);
+        else
+          tma_load_cache_tile(dst, &vmap, id_lane * Hkv + gg, groups, &v_full[vs]);
+      }
       ++nv;
       return true;
     };
@@ -357,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = mbar_wait(&q_empty[qs], ((seg >> 1) & 1) ^ 1, abort_flag);
           if (ok) {
             mbar_arrive_expect_tx(&q_full[qs], 2 * G * 128);
-            uint8_t* qdst = smem + kOffQ + qs * kSmallBytes;
+            uint8_t* qdst = smem + L::kOffQ + qs * kSmallBytes;
             tma_load_3d(qdst, &qmap, 0, g * G, static_cast<int32_t>(cq), &q_full[qs]);
             tma_load_3d(qdst + kSmallHalf, &qmap, 64, g * G, static_cast<int32_t>(cq),
                         &q_full[qs]);
@@ -371,8 +423,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         if (lane < bpt && myid >= 0) {
-          tma_load_cache_tile(smem + kOffK + ks * kTileBytes + lane * blk_bytes, &kmap,
-                              myid * Hkv + g, groups, &k_full[ks]);
+          uint8_t* dst = smem + L::kOffK + ks * L::kStageBytes + lane * blk_bytes;
+          if constexpr (kFp8)
+            tma_load_2d(dst, &kmap, 0, (myid * Hkv + g) * a.block_size, &k_full[ks]);
+          else
+            tma_load_cache_tile(dst, &kmap, myid * Hkv + g, groups, &k_full[ks]);
         }
         ++n;  // K(n) issued
         if (n >= 2 && !issue_v(n - 2, prev_id, prev_g, prev_nvalid)) {
@@ -401,8 +456,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     // ============================== MMA issuer ===============================
     if (lane == 0) {
-      constexpr uint32_t idesc_qk = idesc_bf16_f32(kTile, kN, false, false);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(kHeadDim, kN, false, true);
+      constexpr uint32_t idesc_qk = kFp8 ? idesc_f16_f32(kTile, kN, false, false)
+                                         : idesc_bf16_f32(kTile, kN, false, false);
+      constexpr uint32_t idesc_pv = kFp8 ? idesc_f16_f32(kHeadDim, kN, false, true)
+                                         : idesc_bf16_f32(kHeadDim, kN, false, true);
       // QK and PV are each issued in tile order, but whichever is ready goes
       // first: PV(j) as soon as P(j) and V(j) are in (it frees V's ring
       // slot, the resource the producer waits on longest), QK(n) as soon as
@@ -420,15 +477,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int seg_j = pseg + (first ? 1 : 0);
           const int pb = pn & 1;
           bool ready = mbar_test(&p_full[pb], (pn >> 1) & 1) &&
-                       mbar_test(&v_full[pn % kVStages], (pn / kVStages) & 1);
+                       (kFp8 ? mbar_test(&vc_full[pn & 1], (pn >> 1) & 1)
+                             : mbar_test(&v_full[pn % kVStages], (pn / kVStages) & 1));
           // A unit's first P V overwrites O^T slot seg_j & 1, last read
           // for unit seg_j - 2.
           if (ready && first && seg_j >= 2)
             ready = mbar_test(&o_free[seg_j & 1], ((seg_j >> 1) - 1) & 1);
           if (ready) {
             tc_fence_after();
-            const uint32_t sv = sbase + kOffV + (pn % kVStages) * kTileBytes;
-            const uint32_t sp = sbase + kOffP + pb * kSmallBytes;
+            const uint32_t sv = kFp8 ? sbase + L::kOffVc + (pn & 1) * kTileBytes
+                                     : sbase + L::kOffV + (pn % kVStages) * kTileBytes;
+            const uint32_t sp = sbase + L::kOffP + pb * kSmallBytes;
 #pragma unroll
             for (int k = 0; k < kTile / 16; ++k) {
               // V tile as the MN-major A: the two 64-dim halves 1 KB apart
@@ -441,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                           (first && k == 0) ? 0u : 1u);
             }
             mma_commit(&pv_done[pb]);
-            mma_commit(&v_empty[pn % kVStages]);
+            mma_commit(kFp8 ? &vc_empty[pn & 1] : &v_empty[pn % kVStages]);
             if (first) pseg = seg_j;
             ++pn;
             walk_next(pw, a, s_len);
@@ -453,24 +512,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool last = (qn == nloc - 1) || (qw.i == qw.nt - 1);
           const int seg_q = qseg + (first ? 1 : 0);
           const int ks = qn % kKStages, sb = qn & 1;
-          bool ready = mbar_test(&k_full[ks], (qn / kKStages) & 1);
+          bool ready = kFp8 ? mbar_test(&kc_full[qn & 1], (qn >> 1) & 1)
+                            : mbar_test(&k_full[ks], (qn / kKStages) & 1);
           if (ready && qn >= 2) ready = mbar_test(&s_free[sb], ((qn >> 1) & 1) ^ 1);
-          if (ready && first) ready = mbar_test(&q_full[seg_q & 1], (seg_q >> 1) & 1);
+          if (ready && first)
+            ready = mbar_test(kFp8 ? &qc_full[seg_q & 1] : &q_full[seg_q & 1], (seg_q >> 1) & 1);
           if (ready) {
             tc_fence_after();
-            const uint32_t sk = sbase + kOffK + ks * kTileBytes;
-            const uint32_t sq = sbase + kOffQ + (seg_q & 1) * kSmallBytes;
+            const uint32_t sk = sbase + L::kOffK + ks * L::kStageBytes;
+            const uint32_t sq = sbase + L::kOffQ + (seg_q & 1) * kSmallBytes;
 #pragma unroll
             for (int k = 0; k < kHeadDim / 16; ++k) {
-              // K tile as the K-major A: dim half k/4 at +1 KB, 8-token groups
-              // 2 KB apart.
-              const uint64_t ad = sdesc_sw128(sk + (k >> 2) * 1024 + (k & 3) * 32, 16, 2048);
               const uint64_t bd =
                   sdesc_sw128(sq + (k >> 2) * kSmallHalf + (k & 3) * 32, 16, 1024);
-              mma_bf16_ss(tmem + sb * kN, ad, bd, idesc_qk, k > 0 ? 1u : 0u);
+              if constexpr (kFp8) {
+                // K from TMEM: dims 16k..16k+15 are columns 8k..8k+7
+                mma_f16_ts(tmem + sb * kN, tmem + kColK + (qn & 1) * 64 + k * 8, bd, idesc_qk,
+                           k > 0 ? 1u : 0u);
+              } else {
+                // K tile as the K-major A: dim half k/4 at +1 KB, 8-token
+                // groups 2 KB apart.
+                const uint64_t ad = sdesc_sw128(sk + (k >> 2) * 1024 + (k & 3) * 32, 16, 2048);
+                mma_bf16_ss(tmem + sb * kN, ad, bd, idesc_qk, k > 0 ? 1u : 0u);
+              }
             }
             mma_commit(&s_full[sb]);
-            mma_commit(&k_empty[ks]);
+            mma_commit(kFp8 ? &kc_empty[qn & 1] : &k_empty[ks]);
             if (last) mma_commit(&q_empty[seg_q & 1]);
             if (first) qseg = seg_q;
             ++qn;
@@ -495,6 +562,101 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait_drain(mma_done, 0);
     }
     __syncwarp();
+  } else if (kFp8 && warp >= kConvWarp0) {
+    // ============================ FP8 converters =============================
+    // Thread = token row r of a tile (warp w owns TMEM lanes 32 (w % 4) ..).
+    // Order K(0), then K(n+1) before V(n) -- the producer's issue order.
+    const int row = ((warp & 3) << 5) | lane;
+    const int ct = (warp - kConvWarp0) * 32 + lane;  // 0..127
+    const uint32_t k_lane = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    bool ok = true;
+    Walk kw = w0, vw = w0;
+    int seg = -1;
+    // K(n): Q^T first when the tile starts a unit, then the code row into
+    // TMEM columns kColK + (n & 1) * 64 (every row: the rows past the
+    // context are masked in the softmax).
+    auto conv_k = [&](int n) -> bool {
+      if (n == 0 || kw.i == 0) {
+        ++seg;
+        const int qs = seg & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(&q_full[qs], (seg >> 1) & 1, abort_flag)))
+          return false;
+        for (int c = ct; c < kSmallBytes / 16; c += 128) {
+          const uint32_t addr = sbase + L::kOffQ + qs * kSmallBytes + c * 16;
+          const uint4 x = lds128(addr);
+          sts128(addr, bf16x2_to_f16x2(x.x), bf16x2_to_f16x2(x.y), bf16x2_to_f16x2(x.z),
+                 bf16x2_to_f16x2(x.w));
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&qc_full[qs]);
+      }
+      const int ks = n % kKStages;
+      bool w_ok = mbar_wait(&k_full[ks], (n / kKStages) & 1, abort_flag);
+      if (w_ok && n >= 2) w_ok = mbar_wait(&kc_empty[n & 1], ((n >> 1) & 1) ^ 1, abort_flag);
+      if (!__all_sync(0xffffffffu, w_ok)) return false;
+      tc_fence_after();
+      const uint32_t src = sbase + L::kOffK + ks * L::kStageBytes + row * 128;
+      const uint32_t dst = k_lane + kColK + (n & 1) * 64;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint4 x = lds128(src + ((c ^ (row & 7)) << 4));
+        const uint32_t w[8] = {
+            cvt_f16x2_from_e4m3x2(x.x), cvt_f16x2_from_e4m3x2(x.x >> 16),
+            cvt_f16x2_from_e4m3x2(x.y), cvt_f16x2_from_e4m3x2(x.y >> 16),
+            cvt_f16x2_from_e4m3x2(x.z), cvt_f16x2_from_e4m3x2(x.z >> 16),
+            cvt_f16x2_from_e4m3x2(x.w), cvt_f16x2_from_e4m3x2(x.w >> 16)};
+        tmem_st8_nowait(dst + c * 8, w);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&k_empty[ks]);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&kc_full[n & 1]);
+      return true;
+    };
+    // V(j): the code row as f16 into the swizzled MN-major tile (chunk c of
+    // 8 dims at tile_chunk_offset), zeros for rows past the context.
+    auto conv_v = [&](int j) -> bool {
+      const int vs = j % kVStages;
+      const int nvalid_tok = min(kTile, vw.L - vw.i * kTile);
+      bool w_ok = mbar_wait(&v_full[vs], (j / kVStages) & 1, abort_flag);
+      if (w_ok && j >= 2) w_ok = mbar_wait(&vc_empty[j & 1], ((j >> 1) & 1) ^ 1, abort_flag);
+      if (!__all_sync(0xffffffffu, w_ok)) return false;
+      const uint32_t src = sbase + L::kOffV + vs * L::kStageBytes + row * 128;
+      const uint32_t dst = sbase + L::kOffVc + (j & 1) * kTileBytes + (row >> 4) * kCacheTileBytes;
+      const bool valid = row < nvalid_tok;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint4 x = make_uint4(0u, 0u, 0u, 0u);
+        if (valid) x = lds128(src + ((c ^ (row & 7)) << 4));
+        sts128(dst + tile_chunk_offset(row & 15, 2 * c), cvt_f16x2_from_e4m3x2(x.x),
+               cvt_f16x2_from_e4m3x2(x.x >> 16), cvt_f16x2_from_e4m3x2(x.y),
+               cvt_f16x2_from_e4m3x2(x.y >> 16));
+        sts128(dst + tile_chunk_offset(row & 15, 2 * c + 1), cvt_f16x2_from_e4m3x2(x.z),
+               cvt_f16x2_from_e4m3x2(x.z >> 16), cvt_f16x2_from_e4m3x2(x.w),
+               cvt_f16x2_from_e4m3x2(x.w >> 16));
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&v_empty[vs]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&vc_full[j & 1]);
+      return true;
+    };
+    for (int n = 0; n <= nloc && ok; ++n) {
+      if (n < nloc) {
+        ok = conv_k(n);
+        walk_next(kw, a, s_len);
+        if (!ok) break;
+      }
+      if (n >= 1) {
+        ok = conv_v(n - 1);
+        walk_next(vw, a, s_len);
+      }
+    }
+    if (!ok && lane == 0) set_err(a.err_word, QATTN_DEVERR_TIMEOUT);
   } else {
     // =============================== softmax ================================
     const int t = tid;  // token row of S^T / dimension row of O^T = TMEM lane
@@ -518,6 +680,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     // Epilogue of unit `useg` whose last tile here is j (walk state uw):
     // out = O^T / l, or this CTA's part of a unit that straddles CTAs.
+    // O / l, times v_scale for an FP8 cache.
+    auto out_val = [&](float o, float l) -> float {
+      if constexpr (kFp8)
+        return (o / l) * a.v_scale;
+      else
+        return o / l;
+    };
     auto finish = [&](const Walk& uw, int j, int useg, const float* mu,
                       const float* ltot) -> bool {
       if (!wait_pv(j)) return false;
@@ -538,11 +707,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) +
                               (row * a.num_heads + static_cast<int64_t>(uw.g) * G) * kHeadDim;
 #pragma unroll
-        for (int h = 0; h < G; ++h) orow[h * kHeadDim + t] = __float2bfloat16_rn(o[h] / ltot[h]);
+        for (int h = 0; h < G; ++h) orow[h * kHeadDim + t] = __float2bfloat16_rn(out_val(o[h], ltot[h]));
       } else if (fits) {
         const int64_t pidx = seg_id * a.ws.max_parts + a.part_base + part;
 #pragma unroll
-        for (int h = 0; h < G; ++h) a.ws.part_o[(pidx * G + h) * kHeadDim + t] = o[h] / ltot[h];
+        for (int h = 0; h < G; ++h) a.ws.part_o[(pidx * G + h) * kHeadDim + t] = out_val(o[h], ltot[h]);
         if (t < G) {
 #pragma unroll
           for (int h = 0; h < G; ++h)
@@ -647,13 +816,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       // denominator of O / l use the same weights (a consistent softmax;
       // summing the fp32 values would leave a 2^-9 relative mismatch per key).
       {
+        // (f16 for an FP8 cache, whose V^T is f16)
         unsigned short pbits[G];
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-          pbits[h] = __bfloat16_as_ushort(__float2bfloat16_rn(exp2f(s[h] - m_used[h])));
-          l_t[h] += __uint_as_float(static_cast<uint32_t>(pbits[h]) << 16);
+          const float p = exp2f(s[h] - m_used[h]);
+          if constexpr (kFp8) {
+            const __half ph = __float2half_rn(p);
+            pbits[h] = __half_as_ushort(ph);
+            l_t[h] += __half2float(ph);
+          } else {
+            pbits[h] = __bfloat16_as_ushort(__float2bfloat16_rn(p));
+            l_t[h] += __uint_as_float(static_cast<uint32_t>(pbits[h]) << 16);
+          }
         }
-        const uint32_t pbase = sbase + kOffP + pb * kSmallBytes + (t >> 6) * kSmallHalf;
+        const uint32_t pbase = sbase + L::kOffP + pb * kSmallBytes + (t >> 6) * kSmallHalf;
         const int c = t & 63;
 #pragma unroll
         for (int h = 0; h < kN; ++h) {
@@ -662,9 +839,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(bits) : "memory");
         }
       }
-      if (nvalid_tok < kTile) {
+      if (!kFp8 && nvalid_tok < kTile) {
         // V rows of tokens past the context: zero them before P V reads
-        // them, once V(n) has landed.  (PV(n-2) is done, hence V(n-3) landed:
+        // them, once V(n) has landed (the FP8 converters write them as zero).  (PV(n-2) is done, hence V(n-3) landed:
         // this slot's barrier is at most one phase behind.)
         if (!__all_sync(0xffffffffu,
                         mbar_wait(&v_full[n % kVStages], (n / kVStages) & 1, abort_flag))) {
@@ -672,7 +849,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         if (!valid) {
-          const uint32_t vtile = sbase + kOffV + (n % kVStages) * kTileBytes +
+          const uint32_t vtile = sbase + L::kOffV + (n % kVStages) * kTileBytes +
                                  (t >> 4) * kCacheTileBytes;
 #pragma unroll
           for (int c = 0; c < 16; ++c) sts128(vtile + tile_chunk_offset(t & 15, c), 0u, 0u, 0u, 0u);
@@ -735,25 +912,34 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
+  if (warp == kMmaWarp) tmem_dealloc(tmem, L::kTmemCols);
+}
+
+template <int G, bool kFp8>
+cudaError_t launch_tc_gf(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                         const CUtensorMap& qmap, int num_sms, cudaStream_t stream) {
+  using L = Lay<kFp8>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(paged_decode_tc_kernel<G, kFp8>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         L::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  cudaError_t e = launch_pdl(paged_decode_tc_kernel<G, kFp8>, dim3(num_sms), dim3(L::kThreads),
+                             L::kSmemBytes, stream, kmap, vmap, qmap, a);
+  if (e != cudaSuccess) return e;
+  e = cudaPeekAtLastError();
+  if (e != cudaSuccess) return e;
+  return launch_decode_merge(a, stream);
 }
 
 template <int G>
 cudaError_t launch_tc_g(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                         const CUtensorMap& qmap, int num_sms, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(paged_decode_tc_kernel<G>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  cudaError_t e = launch_pdl(paged_decode_tc_kernel<G>, dim3(num_sms), dim3(kThreads),
-                             kSmemBytes, stream, kmap, vmap, qmap, a);
-  if (e != cudaSuccess) return e;
-  e = cudaPeekAtLastError();
-  if (e != cudaSuccess) return e;
-  return launch_decode_merge(a, stream);
+  return a.kv_fp8 ? launch_tc_gf<G, true>(a, kmap, vmap, qmap, num_sms, stream)
+                  : launch_tc_gf<G, false>(a, kmap, vmap, qmap, num_sms, stream);
 }
 
 }  // namespace

@@ -26,6 +26,12 @@
 // then a pairwise tree -- see rmsnorm_group), v = fp32(mean + eps),
 // r = 1 / sqrt(v) with correctly rounded fp32 sqrt and division,
 // y = bf16(fp32(fp32(x * r) * w)).
+//
+// FP8 cache (kv_cache_dtype "fp8", fp8_e4m3fn with a cache scale per tensor,
+// "Qwen2大模型架构解析与vLLM优化实践" sections 4.1, 4.2, 6.3): the bf16 key
+// and value rows above are stored as e4m3(x / scale) -- fp32 division
+// rounded to nearest, then the hardware conversion to e4m3 with
+// round-to-nearest-even and saturation to +-448.
 #include "common.cuh"
 #include "internal.h"
 
@@ -111,8 +117,22 @@ __device__ __forceinline__ void rmsnorm_group(uint4& x1, uint4& x2, const __nv_b
   }
 }
 
-// kExtras: bias and/or norms present (the plain step compiles without them).
-template <bool kExtras>
+// 8 bf16 values -> 8 e4m3 codes of x / s (byte i = value i).
+__device__ __forceinline__ uint2 quantize8_e4m3(const uint4& x, float s) {
+  const uint32_t* xs = reinterpret_cast<const uint32_t*>(&x);
+  uint32_t pr[4];
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const float lo = __fdiv_rn(bf16lo_to_f32(xs[w]), s);
+    const float hi = __fdiv_rn(bf16hi_to_f32(xs[w]), s);
+    pr[w] = cvt_e4m3x2(lo, hi);
+  }
+  return make_uint2(pr[0] | (pr[1] << 16), pr[2] | (pr[3] << 16));
+}
+
+// kExtras: bias and/or norms present (the plain step compiles without them);
+// kFp8: the caches hold e4m3 codes.
+template <bool kExtras, bool kFp8>
 __global__ void __launch_bounds__(kThreads) rope_append_kernel(RopeAppendArgs a,
                                                                int tasks_per_token) {
   // A following decode kernel may start its set-up now; it reads nothing
@@ -196,10 +216,16 @@ __global__ void __launch_bounds__(kThreads) rope_append_kernel(RopeAppendArgs a,
         rmsnorm_group(x1, x2, static_cast<const __nv_bfloat16*>(a.k_norm_w), part, a.norm_eps);
       uint4 y1, y2;
       rotate8(x1, x2, c, s, y1, y2);
-      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.k_cache) + cache_row +
-                           static_cast<int64_t>(g) * BS * kHeadDim;
-      *reinterpret_cast<uint4*>(dst + part * 8) = y1;
-      *reinterpret_cast<uint4*>(dst + 64 + part * 8) = y2;
+      const int64_t dst = cache_row + static_cast<int64_t>(g) * BS * kHeadDim;
+      if (kFp8) {
+        uint8_t* d8 = static_cast<uint8_t*>(a.k_cache) + dst;
+        *reinterpret_cast<uint2*>(d8 + part * 8) = quantize8_e4m3(y1, a.k_scale);
+        *reinterpret_cast<uint2*>(d8 + 64 + part * 8) = quantize8_e4m3(y2, a.k_scale);
+      } else {
+        __nv_bfloat16* d16 = static_cast<__nv_bfloat16*>(a.k_cache) + dst;
+        *reinterpret_cast<uint4*>(d16 + part * 8) = y1;
+        *reinterpret_cast<uint4*>(d16 + 64 + part * 8) = y2;
+      }
     }
   } else {
     if (!write_cache) return;
@@ -207,13 +233,16 @@ __global__ void __launch_bounds__(kThreads) rope_append_kernel(RopeAppendArgs a,
     const int g = r2 >> 4, part = r2 & 15;
     const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(a.v) + t * a.v_row_stride +
                                static_cast<int64_t>(g) * kHeadDim;
-    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.v_cache) + cache_row +
-                         static_cast<int64_t>(g) * BS * kHeadDim;
+    const int64_t dst = cache_row + static_cast<int64_t>(g) * BS * kHeadDim + part * 8;
     uint4 x = *reinterpret_cast<const uint4*>(src + part * 8);
     if (kExtras && a.bias)
       x = add_bias8(x, static_cast<const __nv_bfloat16*>(a.bias) +
                            static_cast<int64_t>(H + Hkv + g) * kHeadDim + part * 8);
-    *reinterpret_cast<uint4*>(dst + part * 8) = x;
+    if (kFp8)
+      *reinterpret_cast<uint2*>(static_cast<uint8_t*>(a.v_cache) + dst) =
+          quantize8_e4m3(x, a.v_scale);
+    else
+      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.v_cache) + dst) = x;
   }
 }
 
@@ -224,12 +253,19 @@ cudaError_t launch_rope_append(const RopeAppendArgs& a, cudaStream_t stream) {
   const int64_t total = static_cast<int64_t>(a.num_tokens) * tasks_per_token;
   const int64_t blocks = (total + kThreads - 1) / kThreads;
   if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
-  if (a.bias != nullptr || a.q_norm_w != nullptr || a.k_norm_w != nullptr)
-    rope_append_kernel<true><<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(
-        a, tasks_per_token);
-  else
-    rope_append_kernel<false><<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(
-        a, tasks_per_token);
+  const bool extras = a.bias != nullptr || a.q_norm_w != nullptr || a.k_norm_w != nullptr;
+  const dim3 grid(static_cast<unsigned>(blocks));
+  if (a.kv_fp8) {
+    if (extras)
+      rope_append_kernel<true, true><<<grid, kThreads, 0, stream>>>(a, tasks_per_token);
+    else
+      rope_append_kernel<false, true><<<grid, kThreads, 0, stream>>>(a, tasks_per_token);
+  } else {
+    if (extras)
+      rope_append_kernel<true, false><<<grid, kThreads, 0, stream>>>(a, tasks_per_token);
+    else
+      rope_append_kernel<false, false><<<grid, kThreads, 0, stream>>>(a, tasks_per_token);
+  }
   return cudaPeekAtLastError();
 }
 

@@ -39,9 +39,11 @@ EXPORTED = [
     "qattn_rope_table_build_scaled",
     "qattn_rope_cache_append",
     "qattn_rope_cache_append_ex",
+    "qattn_rope_cache_append_fp8",
     "qattn_paged_decode_kernel",
     "qattn_paged_decode_workspace_size",
     "qattn_paged_decode",
+    "qattn_paged_decode_fp8",
     "qattn_paged_decode_noalloc",
     "qattn_paged_decode_shared_prefix_workspace_size",
     "qattn_paged_decode_shared_prefix",
@@ -101,6 +103,10 @@ def load_library(path: str | None = None):
             _P, _I64, _P, _I64, _P, _I64, _P, _P, _I32, _P, _P, _I32, _P, _I32, _P, _P, _P,
             ctypes.c_float, qattn_dims, _P, _P]
         L.qattn_rope_cache_append_ex.restype = ctypes.c_int
+        L.qattn_rope_cache_append_fp8.argtypes = [
+            _P, _I64, _P, _I64, _P, _I64, _P, _P, _I32, _P, _P, _I32, _P, _I32, _P, _P, _P,
+            ctypes.c_float, ctypes.c_float, ctypes.c_float, qattn_dims, _P, _P]
+        L.qattn_rope_cache_append_fp8.restype = ctypes.c_int
         L.qattn_paged_decode_kernel.argtypes = [qattn_dims]
         L.qattn_paged_decode_kernel.restype = ctypes.c_int
         L.qattn_paged_decode_workspace_size.argtypes = [_I32, _I32, qattn_dims]
@@ -108,6 +114,10 @@ def load_library(path: str | None = None):
         L.qattn_paged_decode.argtypes = [
             _P, _P, _I64, _P, _P, _I32, _P, _I32, _P, _I32, _I32, qattn_dims, _P, _SZ, _P, _P]
         L.qattn_paged_decode.restype = ctypes.c_int
+        L.qattn_paged_decode_fp8.argtypes = [
+            _P, _P, _I64, _P, _P, _I32, _P, _I32, _P, _I32, _I32, ctypes.c_float, ctypes.c_float,
+            qattn_dims, _P, _SZ, _P, _P]
+        L.qattn_paged_decode_fp8.restype = ctypes.c_int
         L.qattn_paged_decode_shared_prefix_workspace_size.argtypes = [_I32, _I32, qattn_dims]
         L.qattn_paged_decode_shared_prefix_workspace_size.restype = _SZ
         L.qattn_paged_decode_shared_prefix.argtypes = [
@@ -226,6 +236,34 @@ def qattn_rope_cache_append_ex(q, k, v, positions, slot_mapping, k_cache, v_cach
     _check("qattn_rope_cache_append_ex", rc)
 
 
+def _fp8_ptr(t: torch.Tensor, name: str):
+    """Device pointer of an e4m3 cache (uint8 or float8_e4m3fn storage)."""
+    if t.dtype not in (torch.uint8, torch.float8_e4m3fn):
+        raise ValueError(f"{name} must be uint8 or float8_e4m3fn, got {t.dtype}")
+    return _dev_ptr(t, name)
+
+
+def qattn_rope_cache_append_fp8(q, k, v, positions, slot_mapping, k_cache, v_cache, cos_sin,
+                                k_scale, v_scale, dims, qkv_bias=None, q_norm_weight=None,
+                                k_norm_weight=None, norm_eps=1e-6, err_word=None, stream=None):
+    """qattn_rope_cache_append_ex into e4m3 caches: keys and values stored
+    as e4m3(x / k_scale), e4m3(x / v_scale)."""
+    qp, qs = _rows(q, "q")
+    kp, ks = _rows(k, "k")
+    vp, vs = _rows(v, "v")
+    rc = lib().qattn_rope_cache_append_fp8(
+        qp, qs, kp, ks, vp, vs, _dev_ptr(positions, "positions", torch.int32),
+        _dev_ptr(slot_mapping, "slot_mapping", torch.int32), int(positions.shape[0]),
+        _fp8_ptr(k_cache, "k_cache"), _fp8_ptr(v_cache, "v_cache"),
+        int(k_cache.shape[0]), _dev_ptr(cos_sin, "cos_sin", torch.float32), int(cos_sin.shape[0]),
+        _dev_ptr(qkv_bias, "qkv_bias", torch.bfloat16),
+        _dev_ptr(q_norm_weight, "q_norm_weight", torch.bfloat16),
+        _dev_ptr(k_norm_weight, "k_norm_weight", torch.bfloat16), float(norm_eps),
+        float(k_scale), float(v_scale), dims,
+        _dev_ptr(err_word, "err_word", torch.int32), _stream(stream))
+    _check("qattn_rope_cache_append_fp8", rc)
+
+
 QATTN_DECODE_CUDA_CORE = 0
 QATTN_DECODE_TENSOR_CORE = 1
 
@@ -251,6 +289,22 @@ def qattn_paged_decode(out, q, k_cache, v_cache, block_tables, context_lens, max
         _dev_ptr(workspace, "workspace"), int(workspace.numel() * workspace.element_size()),
         _dev_ptr(err_word, "err_word", torch.int32), _stream(stream))
     _check("qattn_paged_decode", rc)
+
+
+def qattn_paged_decode_fp8(out, q, k_cache, v_cache, block_tables, context_lens,
+                           max_context_len, k_scale, v_scale, dims, workspace, err_word=None,
+                           stream=None):
+    """qattn_paged_decode over e4m3 caches read as code * scale."""
+    qp, qs = _rows(q, "q")
+    rc = lib().qattn_paged_decode_fp8(
+        _dev_ptr(out, "out", torch.bfloat16), qp, qs,
+        _fp8_ptr(k_cache, "k_cache"), _fp8_ptr(v_cache, "v_cache"),
+        int(k_cache.shape[0]), _dev_ptr(block_tables, "block_tables", torch.int32),
+        int(block_tables.shape[1]), _dev_ptr(context_lens, "context_lens", torch.int32),
+        int(context_lens.shape[0]), int(max_context_len), float(k_scale), float(v_scale), dims,
+        _dev_ptr(workspace, "workspace"), int(workspace.numel() * workspace.element_size()),
+        _dev_ptr(err_word, "err_word", torch.int32), _stream(stream))
+    _check("qattn_paged_decode_fp8", rc)
 
 
 def qattn_paged_decode_shared_prefix_workspace_size(num_seqs: int, max_context_len: int,

@@ -323,3 +323,26 @@ def permute_blocks(w: Workload, seed: int = 7) -> Workload:
     kw = dict(w.__dict__)
     kw.update(k_cache=k2, v_cache=v2, block_tables=bt2, slot_mapping=s2)
     return Workload(**kw)
+
+
+# FP8 caches: the per-tensor scales the workloads use (|x| / scale stays well
+# inside e4m3's +-448 for N(0, 1) data).
+FP8_K_SCALE = 0.0135
+FP8_V_SCALE = 0.0115
+
+
+def fp8_codes(cache: torch.Tensor, scale: float) -> torch.Tensor:
+    """Synthetic e4m3 cache contents: the bf16 cache (cached tokens N(0, 1),
+    unused slots NaN) divided by ``scale`` and converted with torch's
+    float8_e4m3fn cast, as uint8 codes.  Input generation only -- which
+    codes they are does not matter, both sides read the same ones."""
+    x = (cache.float() / scale).clamp(-448.0, 448.0)
+    return x.to(torch.float8_e4m3fn).view(torch.uint8)
+
+
+def with_fp8_cache(w: Workload, k_scale: float = FP8_K_SCALE,
+                   v_scale: float = FP8_V_SCALE) -> Workload:
+    """The workload with uint8 e4m3 caches in place of the bf16 ones."""
+    kw = dict(w.__dict__)
+    kw.update(k_cache=fp8_codes(w.k_cache, k_scale), v_cache=fp8_codes(w.v_cache, v_scale))
+    return Workload(**kw)
