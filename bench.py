@@ -53,6 +53,11 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-clocks", action="store_true")
+    p.add_argument("--block-size", type=int, choices=[16, 32, 64], default=16,
+                   help="cache block size of the decode / mixed workloads")
+    p.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
+                   help="cache dtype: bf16, or e4m3 codes with a per-tensor scale (decode "
+                        "workloads without a shared prefix)")
     p.add_argument("--extras", choices=["none", "bias", "qknorm", "both"], default="none",
                    help="add the qkv projection bias and/or the Qwen3 q/k RMSNorms to the "
                         "RoPE + append step (synthetic weights)")
@@ -222,7 +227,14 @@ def run_ours(args, dist: Dist):
     Q.load_library()
     dev = torch.device("cuda", dist.local_rank)
     torch.cuda.set_device(dev)
-    w = W.build(args.workload, seed=W.SEED_BASE + W.WORKLOAD_NAMES.index(args.workload) + 1000 * dist.rank)
+    w = W.build(args.workload, seed=W.SEED_BASE + W.WORKLOAD_NAMES.index(args.workload) + 1000 * dist.rank,
+                block_size=args.block_size)
+    fp8 = args.kv == "fp8"
+    if fp8:
+        if not w.is_decode or w.shared_prefix_tokens:
+            raise SystemExit("--kv fp8 times the plain decode workloads")
+        w = W.with_fp8_cache(w)
+    ks, vs = W.FP8_K_SCALE, W.FP8_V_SCALE
     H, Hkv, D, BS = w.num_heads, w.num_kv_heads, w.head_dim, w.block_size
     dims = Q.make_dims(H, Hkv, D, BS)
     g = W.to_device(w, dev)
@@ -253,7 +265,12 @@ def run_ours(args, dist: Dist):
         kn = (1.0 + 0.2 * torch.randn(D, generator=gx)).to(torch.bfloat16).to(dev)
 
     def append():
-        if args.extras == "none":
+        if fp8:
+            Q.qattn_rope_cache_append_fp8(g.q_view(), g.k_view(), g.v_view(), g.positions,
+                                          g.slot_mapping, g.k_cache, g.v_cache, table, ks, vs,
+                                          dims, qkv_bias=bias, q_norm_weight=qn,
+                                          k_norm_weight=kn, err_word=err)
+        elif args.extras == "none":
             Q.qattn_rope_cache_append(g.q_view(), g.k_view(), g.v_view(), g.positions,
                                       g.slot_mapping, g.k_cache, g.v_cache, table, dims, err)
         else:
@@ -267,6 +284,9 @@ def run_ours(args, dist: Dist):
             Q.qattn_paged_decode_shared_prefix(out, g.q_view(), g.k_cache, g.v_cache,
                                                g.block_tables, g.context_lens, max_ctx, prefix,
                                                dims, ws, err)
+        elif fp8:
+            Q.qattn_paged_decode_fp8(out, g.q_view(), g.k_cache, g.v_cache, g.block_tables,
+                                     g.context_lens, max_ctx, ks, vs, dims, ws, err)
         elif decode:
             Q.qattn_paged_decode(out, g.q_view(), g.k_cache, g.v_cache, g.block_tables,
                                  g.context_lens, max_ctx, dims, ws, err)
@@ -341,12 +361,12 @@ def run_ours(args, dist: Dist):
     elif decode:
         alg = kv_bytes + qo_bytes
         achieved = alg / attn_avg_s / 1e9
-        if Q.qattn_paged_decode_kernel(dims) == Q.QATTN_DECODE_TENSOR_CORE:
+        if fp8 or Q.qattn_paged_decode_kernel(dims) == Q.QATTN_DECODE_TENSOR_CORE:
             kname, src = "paged_decode_tc_kernel", "paged_decode_tc.cu"
         else:
             kname, src = "paged_decode_kernel", "paged_decode.cu"
         sha = kernel_source_sha([src, "common.cuh", "internal.h"])
-        traffic = profiled_traffic(kname, args.workload, sha)
+        traffic = profiled_traffic(kname + ("_fp8" if fp8 else ""), args.workload, sha)
         result["roofline"] = {"bound": "hbm", "kernel": kname,
                               "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                               "frac": round(achieved / hbm_peak, 4), "peak_kind": peak_kind,
@@ -362,7 +382,8 @@ def run_ours(args, dist: Dist):
     # ---- end to end through the C ABI with host buffers ----
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, w, dims, g, table, ws, err, dev, decode, max_ctx, dist, prefix)
+        e2e = run_e2e(args, w, dims, g, table, ws, err, dev, decode, max_ctx, dist, prefix,
+                      (ks, vs) if fp8 else None)
 
     clk = clocks.summary()
     line = {
@@ -376,13 +397,13 @@ def run_ours(args, dist: Dist):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": "bf16" if not fp8 else "bf16 q/out, e4m3 cache, f16 tensor-core products",
         "data": "synthetic (seeded N(0,1) q/k/v and cache, random block placement)",
         "config": {"workload": args.workload, "num_heads": H, "num_kv_heads": Hkv,
                    "head_dim": D, "block_size": BS, "batch": w.num_seqs,
                    "new_tokens": w.num_tokens, "kv_bytes_per_step": kv_bytes,
                    "max_context_len": max_ctx, "l2": "flushed before every timed step (512 MB write)",
-                   "append_extras": args.extras,
+                   "append_extras": args.extras, "kv_cache_dtype": args.kv,
                    "parallelism": f"replicas x{dist.world}"},
         "seqs_per_s": round(seqs_per_s, 1),
         "tokens_per_s": round(tokens_per_s, 1),
@@ -402,7 +423,8 @@ def run_ours(args, dist: Dist):
     return line
 
 
-def run_e2e(args, w, dims, g, table, ws, err, dev, decode, max_ctx, dist, prefix=0):
+def run_e2e(args, w, dims, g, table, ws, err, dev, decode, max_ctx, dist, prefix=0,
+            fp8_scales=None):
     """Same step through the public API, inputs copied from pinned host memory
     each step and the attention output read back."""
     from paged_kv_gqa_07_gb300 import qattn as Q
@@ -421,6 +443,16 @@ def run_e2e(args, w, dims, g, table, ws, err, dev, decode, max_ctx, dist, prefix
         for k in host_in:
             dev_in[k].copy_(host_in[k], non_blocking=True)
         qkv = dev_in["qkv"]
+        if fp8_scales is not None:
+            Q.qattn_rope_cache_append_fp8(qkv[:, :H * D], qkv[:, H * D:(H + Hkv) * D],
+                                          qkv[:, (H + Hkv) * D:], dev_in["positions"],
+                                          dev_in["slot_mapping"], g.k_cache, g.v_cache, table,
+                                          *fp8_scales, dims, err_word=err)
+            Q.qattn_paged_decode_fp8(out, qkv[:, :H * D], g.k_cache, g.v_cache,
+                                     dev_in["block_tables"], dev_in["context_lens"], max_ctx,
+                                     *fp8_scales, dims, ws, err)
+            host_out.copy_(out, non_blocking=True)
+            return
         Q.qattn_rope_cache_append(qkv[:, :H * D], qkv[:, H * D:(H + Hkv) * D],
                                   qkv[:, (H + Hkv) * D:], dev_in["positions"],
                                   dev_in["slot_mapping"], g.k_cache, g.v_cache, table, dims, err)
@@ -485,16 +517,30 @@ def oracle_time(w: W.Workload, n_seqs: int, reps: int = 1):
 
     def u16(t):
         return t.contiguous().view(torch.int16).numpy().view(np.uint16).copy()
-    kc0, vc0 = u16(s.k_cache), u16(s.v_cache)
+    fp8 = s.k_cache.dtype == torch.uint8
+    if fp8:
+        kc0, vc0 = s.k_cache.numpy().copy(), s.v_cache.numpy().copy()
+    else:
+        kc0, vc0 = u16(s.k_cache), u16(s.v_cache)
+    cu = None if s.is_decode else s.cu_seqlens_q
+    ks, vs = W.FP8_K_SCALE, W.FP8_V_SCALE
     times = []
     for _ in range(reps):
         qkv = u16(s.qkv)
         kc, vc = kc0.copy(), vc0.copy()
         t0 = time.perf_counter()
-        oracle.rope_cache_append(qkv, s.positions, s.slot_mapping, kc, vc, table, H, Hkv, D, BS)
-        q = np.ascontiguousarray(qkv[:, :H * D])
-        oracle.paged_attention(q, kc, vc, s.block_tables, s.context_lens, H, Hkv, D, BS,
-                               cu_seqlens_q=None if s.is_decode else s.cu_seqlens_q)
+        if fp8:
+            oracle.rope_cache_append_fp8(qkv, s.positions, s.slot_mapping, kc, vc, table, H,
+                                         Hkv, D, BS, ks, vs)
+            q = np.ascontiguousarray(qkv[:, :H * D])
+            oracle.paged_attention_fp8(q, kc, vc, ks, vs, s.block_tables, s.context_lens, H,
+                                       Hkv, D, BS, cu_seqlens_q=cu)
+        else:
+            oracle.rope_cache_append(qkv, s.positions, s.slot_mapping, kc, vc, table, H, Hkv,
+                                     D, BS)
+            q = np.ascontiguousarray(qkv[:, :H * D])
+            oracle.paged_attention(q, kc, vc, s.block_tables, s.context_lens, H, Hkv, D, BS,
+                                   cu_seqlens_q=cu)
         times.append(time.perf_counter() - t0)
     return statistics.median(times), s.kv_bytes_read(), s
 
@@ -530,7 +576,9 @@ def cpu_baseline(w: W.Workload, kv_bytes_full: int, budget_s: float = 10.0):
 
 def run_reference(args, dist: Dist):
     import oracle
-    w = W.build(args.workload)
+    w = W.build(args.workload, block_size=args.block_size)
+    if args.kv == "fp8":
+        w = W.with_fp8_cache(w)
     n = sample_size(w)
     for _ in range(args.warmup):
         oracle_time(w, n)
@@ -548,7 +596,8 @@ def run_reference(args, dist: Dist):
         "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * sum(per) / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": args.workload, "batch_sampled": n},
+        "config": {"workload": args.workload, "batch_sampled": n, "block_size": w.block_size,
+                   "kv_cache_dtype": args.kv},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "kind": "oracle",
                          "cores": oracle.default_threads(), "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,

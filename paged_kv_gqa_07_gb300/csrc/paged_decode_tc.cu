@@ -687,9 +687,12 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
       else
         return o / l;
     };
-    auto finish = [&](const Walk& uw, int j, int useg, const float* mu,
-                      const float* ltot) -> bool {
-      if (!wait_pv(j)) return false;
+    // pv_waited: PV(j) was already waited for in this step (a later PV may
+    // have completed since, so a second parity wait could be two phases
+    // behind).
+    auto finish = [&](const Walk& uw, int j, int useg, const float* mu, const float* ltot,
+                      bool pv_waited) -> bool {
+      if (!pv_waited && !wait_pv(j)) return false;
       tc_fence_after();
       float o[kN];
       tmem_ld16(lane_addr + kColO + (useg & 1) * kN, o);
@@ -726,9 +729,16 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
     bool ok = true;
     Walk sw = w0;
     int seg = -1;
-    for (int n = 0; n < nloc; ++n, walk_next(sw, a, s_len)) {
+    // A step is one tile, or two consecutive tiles of the same unit: the
+    // per-step latencies (S wait, the 4-warp max exchange, the P buffer
+    // wait, proxy fence) are then paid once per 256 tokens.
+    for (int n = 0; n < nloc;) {
+      const int cnt = (n + 1 < nloc && sw.i + 1 < sw.nt) ? 2 : 1;
+      const int nl = n + cnt - 1;  // the step's last tile
+      Walk lw = sw;
+      lw.i += cnt - 1;
       const bool seg_start = (n == 0) || (sw.i == 0);
-      const bool seg_end = (n == nloc - 1) || (sw.i == sw.nt - 1);
+      const bool seg_end = (nl == nloc - 1) || (lw.i == lw.nt - 1);
       if (seg_start) {
         ++seg;
 #pragma unroll
@@ -737,29 +747,42 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
           l_t[h] = 0.f;
         }
       }
-      const int sb = n & 1, pb = n & 1;
-      const int nvalid_tok = min(kTile, sw.L - sw.i * kTile);
-      const bool valid = t < nvalid_tok;
+      const int nv0 = min(kTile, sw.L - sw.i * kTile);
+      const int nv1 = cnt == 2 ? min(kTile, sw.L - (sw.i + 1) * kTile) : 0;
+      const int nv_last = cnt == 2 ? nv1 : nv0;  // only a unit's last tile is partial
 
-      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[sb], (n >> 1) & 1, abort_flag))) {
+      float s[2][kN];
+      bool w_ok = true;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        if (j < cnt) {
+          const int nj = n + j;
+          w_ok = w_ok && __all_sync(0xffffffffu,
+                                    mbar_wait(&s_full[nj & 1], (nj >> 1) & 1, abort_flag));
+          if (w_ok) {
+            tc_fence_after();
+            tmem_ld16(lane_addr + (nj & 1) * kN, s[j]);
+          }
+        }
+      }
+      if (!w_ok) {
         ok = false;
         break;
       }
-      tc_fence_after();
-      float s[kN];
-      tmem_ld16(lane_addr + sb * kN, s);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[sb]);
+      if (lane == 0)
+        for (int j = 0; j < cnt; ++j) mbar_arrive(&s_free[(n + j) & 1]);
 
-      // per-head max over the tile's tokens: shuffle tree, then 4 warps; the
-      // deferred unit's row sums ride along.
-      float* rd = red + (n & 1) * 4 * kN;
-      float* ls = lsum + (n & 1) * 4 * kN;
+      // per-head max over the step's tokens: shuffle tree, then 4 warps;
+      // the deferred unit's row sums ride along.
+      float* rd = red + (rphase & 1) * 4 * kN;
+      float* ls = lsum + (rphase & 1) * 4 * kN;
 #pragma unroll
       for (int h = 0; h < G; ++h) {
-        s[h] = valid ? s[h] * a.scale_log2 : -INFINITY;
-        const float wm = warp_max(s[h]);
+        s[0][h] = t < nv0 ? s[0][h] * a.scale_log2 : -INFINITY;
+        s[1][h] = t < nv1 ? s[1][h] * a.scale_log2 : -INFINITY;
+        const float wm = warp_max(fmaxf(s[0][h], s[1][h]));
         if (lane == 0) rd[warp * kN + h] = wm;
       }
       if (pend) {
@@ -776,8 +799,12 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
         break;
       }
       ++rphase;
-      // P^T buffer pb was last read by PV(n-2).
+      // P^T buffer of tile n + j was last read by PV(n + j - 2).
       if (n >= 2 && !wait_pv(n - 2)) {
+        ok = false;
+        break;
+      }
+      if (cnt == 2 && n >= 1 && !wait_pv(n - 1)) {
         ok = false;
         break;
       }
@@ -798,7 +825,7 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
       }
       if (any_rescale) {
         // O^T holds the unit's tiles so far: wait for PV(n-1), scale row t.
-        if (!wait_pv(n - 1)) {
+        if (cnt == 1 && !wait_pv(n - 1)) {
           ok = false;
           break;
         }
@@ -811,45 +838,51 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
 #pragma unroll
         for (int h = 0; h < G; ++h) l_t[h] *= alpha[h];
       }
-      // P^T row h, token t (bf16) into buffer pb.  The row sums add the
-      // bf16-rounded weights the MMA multiplies, so numerator and
-      // denominator of O / l use the same weights (a consistent softmax;
-      // summing the fp32 values would leave a 2^-9 relative mismatch per key).
-      {
-        // (f16 for an FP8 cache, whose V^T is f16)
-        unsigned short pbits[G];
+      // P^T row h, token t into buffer (n + j) & 1: bf16, or f16 for an FP8
+      // cache (whose V^T is f16).  The row sums add the rounded weights the
+      // MMA multiplies, so numerator and denominator of O / l use the same
+      // weights (a consistent softmax; summing the fp32 values would leave a
+      // 2^-9 relative mismatch per key).
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float p = exp2f(s[h] - m_used[h]);
-          if constexpr (kFp8) {
-            const __half ph = __float2half_rn(p);
-            pbits[h] = __half_as_ushort(ph);
-            l_t[h] += __half2float(ph);
-          } else {
-            pbits[h] = __bfloat16_as_ushort(__float2bfloat16_rn(p));
-            l_t[h] += __uint_as_float(static_cast<uint32_t>(pbits[h]) << 16);
+      for (int j = 0; j < 2; ++j) {
+        if (j < cnt) {
+          unsigned short pbits[G];
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            const float p = exp2f(s[j][h] - m_used[h]);
+            if constexpr (kFp8) {
+              const __half ph = __float2half_rn(p);
+              pbits[h] = __half_as_ushort(ph);
+              l_t[h] += __half2float(ph);
+            } else {
+              pbits[h] = __bfloat16_as_ushort(__float2bfloat16_rn(p));
+              l_t[h] += __uint_as_float(static_cast<uint32_t>(pbits[h]) << 16);
+            }
+          }
+          const uint32_t pbase =
+              sbase + L::kOffP + ((n + j) & 1) * kSmallBytes + (t >> 6) * kSmallHalf;
+          const int c = t & 63;
+#pragma unroll
+          for (int h = 0; h < kN; ++h) {
+            const uint32_t addr = pbase + h * 128 + ((((c >> 3) ^ (h & 7))) << 4) + (c & 7) * 2;
+            const unsigned short bits = h < G ? pbits[h < G ? h : 0] : 0;
+            asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(bits) : "memory");
           }
         }
-        const uint32_t pbase = sbase + L::kOffP + pb * kSmallBytes + (t >> 6) * kSmallHalf;
-        const int c = t & 63;
-#pragma unroll
-        for (int h = 0; h < kN; ++h) {
-          const uint32_t addr = pbase + h * 128 + ((((c >> 3) ^ (h & 7))) << 4) + (c & 7) * 2;
-          const unsigned short bits = h < G ? pbits[h < G ? h : 0] : 0;
-          asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(bits) : "memory");
-        }
       }
-      if (!kFp8 && nvalid_tok < kTile) {
-        // V rows of tokens past the context: zero them before P V reads
-        // them, once V(n) has landed (the FP8 converters write them as zero).  (PV(n-2) is done, hence V(n-3) landed:
-        // this slot's barrier is at most one phase behind.)
+      if (!kFp8 && nv_last < kTile) {
+        // V rows of tokens past the context (only the unit's last tile, the
+        // step's last): zero them before P V reads them, once V(nl) has
+        // landed (the FP8 converters write them as zero).  PV(nl-2) is done,
+        // hence V(nl-3) landed: this slot's barrier is at most one phase
+        // behind.
         if (!__all_sync(0xffffffffu,
-                        mbar_wait(&v_full[n % kVStages], (n / kVStages) & 1, abort_flag))) {
+                        mbar_wait(&v_full[nl % kVStages], (nl / kVStages) & 1, abort_flag))) {
           ok = false;
           break;
         }
-        if (!valid) {
-          const uint32_t vtile = sbase + L::kOffV + (n % kVStages) * kTileBytes +
+        if (t >= nv_last) {
+          const uint32_t vtile = sbase + L::kOffV + (nl % kVStages) * kTileBytes +
                                  (t >> 4) * kCacheTileBytes;
 #pragma unroll
           for (int c = 0; c < 16; ++c) sts128(vtile + tile_chunk_offset(t & 15, c), 0u, 0u, 0u, 0u);
@@ -858,24 +891,26 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[pb]);
+      if (lane == 0)
+        for (int j = 0; j < cnt; ++j) mbar_arrive(&p_full[(n + j) & 1]);
 
       if (pend) {
-        // the previous unit ended at tile n-1
+        // the previous unit ended at tile n-1 (waited for above in a
+        // two-tile step)
         float ltot[G];
 #pragma unroll
         for (int h = 0; h < G; ++h)
           ltot[h] = (ls[0 * kN + h] + ls[1 * kN + h]) + (ls[2 * kN + h] + ls[3 * kN + h]);
-        if (!finish(pend_w, n - 1, pend_seg, m_pend, ltot)) {
+        if (!finish(pend_w, n - 1, pend_seg, m_pend, ltot, cnt == 2)) {
           ok = false;
           break;
         }
         pend = false;
       }
-      if (seg_end && n < nloc - 1) {
+      if (seg_end && nl < nloc - 1) {
         pend = true;
         pend_seg = seg;
-        pend_w = sw;
+        pend_w = lw;
 #pragma unroll
         for (int h = 0; h < G; ++h) {
           m_pend[h] = m_used[h];
@@ -883,7 +918,7 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
         }
       } else if (seg_end) {
         // the run's last tile: its own row-sum exchange, then the epilogue
-        float* ls2 = lsum + ((n + 1) & 1) * 4 * kN;
+        float* ls2 = lsum + (rphase & 1) * 4 * kN;
 #pragma unroll
         for (int h = 0; h < G; ++h) {
           const float ws = warp_sum(l_t[h]);
@@ -900,11 +935,13 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
 #pragma unroll
         for (int h = 0; h < G; ++h)
           ltot[h] = (ls2[0 * kN + h] + ls2[1 * kN + h]) + (ls2[2 * kN + h] + ls2[3 * kN + h]);
-        if (!finish(sw, n, seg, m_used, ltot)) {
+        if (!finish(lw, nl, seg, m_used, ltot, false)) {
           ok = false;
           break;
         }
       }
+      n += cnt;
+      for (int j = 0; j < cnt; ++j) walk_next(sw, a, s_len);
     }
     if (!ok && lane == 0) set_err(a.err_word, QATTN_DEVERR_TIMEOUT);
   }

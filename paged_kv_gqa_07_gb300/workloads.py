@@ -111,12 +111,13 @@ class Workload:
         """Bytes of K and V a decode/varlen attention pass must read:
         sum over query rows of their visible keys, counted once per
         sequence (every query of a sequence shares its keys)."""
-        per_token = 2 * self.num_kv_heads * self.head_dim * 2
+        per_token = 2 * self.num_kv_heads * self.head_dim * self.k_cache.element_size()
         return int(self.context_lens.to(torch.int64).sum().item()) * per_token
 
     def unique_kv_bytes(self) -> int:
         """Bytes of distinct physical blocks referenced by the block tables."""
-        per_block = 2 * self.num_kv_heads * self.block_size * self.head_dim * 2
+        per_block = (2 * self.num_kv_heads * self.block_size * self.head_dim *
+                     self.k_cache.element_size())
         ids = []
         for b in range(self.num_seqs):
             nb = (int(self.context_lens[b]) + self.block_size - 1) // self.block_size
@@ -144,8 +145,11 @@ def _sentinel_cache(num_blocks, Hkv, BS, D) -> torch.Tensor:
     return c.view(torch.bfloat16)
 
 
-def build(name_or_index, seed: int | None = None, *, scale_batch: float = 1.0) -> Workload:
-    """Construct one of the five workloads (by name or index 0..4)."""
+def build(name_or_index, seed: int | None = None, *, scale_batch: float = 1.0,
+          block_size: int = BLOCK_SIZE) -> Workload:
+    """Construct one of the five workloads (by name or index 0..4).  The
+    decode and mixed workloads (1-3) also come with 32- or 64-token blocks
+    (same contexts and values, coarser placement)."""
     idx = name_or_index if isinstance(name_or_index, int) else WORKLOAD_NAMES.index(name_or_index)
     name = WORKLOAD_NAMES[idx]
     seed = SEED_BASE + idx if seed is None else seed
@@ -167,19 +171,20 @@ def build(name_or_index, seed: int | None = None, *, scale_batch: float = 1.0) -
     if idx == 1:
         B = max(1, int(round(64 * scale_batch)))
         ctx = torch.randint(128, 4096 + 1, (B,), generator=gen).tolist()
-        return _random_placement(name, seed, gen, QWEN2_7B, ctx, [1] * B)
+        return _random_placement(name, seed, gen, QWEN2_7B, ctx, [1] * B, block_size=block_size)
 
     if idx == 2:
         cached = torch.randint(0, 1536 + 1, (4,), generator=gen).tolist()
         dec = torch.randint(256, 2048 + 1, (60,), generator=gen).tolist()
         ctx = [c + 512 for c in cached] + dec
         q_lens = [512] * 4 + [1] * 60
-        return _random_placement(name, seed, gen, QWEN2_7B, ctx, q_lens)
+        return _random_placement(name, seed, gen, QWEN2_7B, ctx, q_lens, block_size=block_size)
 
     if idx == 3:
         B = max(1, int(round(8 * scale_batch)))
         ctx = [MAX_POS] * B
-        return _random_placement(name, seed, gen, QWEN2_7B, ctx, [1] * B, slack=0.0)
+        return _random_placement(name, seed, gen, QWEN2_7B, ctx, [1] * B, slack=0.0,
+                                 block_size=block_size)
 
     if idx == 4:
         B = max(1, int(round(128 * scale_batch)))
