@@ -188,6 +188,9 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
                            const __grid_constant__ CUtensorMap qmap, const DecodeArgs a) {
   using L = Lay<kFp8>;
   constexpr int kThreads = L::kThreads;
+  // The FP8 kernel (ten warps in five roles) is instruction-cache bound:
+  // its MMA loops are unrolled by 2 only (measured faster; bf16 keeps 8).
+  constexpr int kMmaUnroll = kFp8 ? 2 : 8;
   constexpr int kKStages = L::kKStages;
   constexpr int kVStages = L::kVStages;
   extern __shared__ uint8_t smem_raw[];
@@ -488,7 +491,7 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
             const uint32_t sv = kFp8 ? sbase + L::kOffVc + (pn & 1) * kTileBytes
                                      : sbase + L::kOffV + (pn % kVStages) * kTileBytes;
             const uint32_t sp = sbase + L::kOffP + pb * kSmallBytes;
-#pragma unroll
+#pragma unroll(kMmaUnroll)
             for (int k = 0; k < kTile / 16; ++k) {
               // V tile as the MN-major A: the two 64-dim halves 1 KB apart
               // (LBO), 8-token groups 2 KB apart (SBO); K step k = tokens
@@ -521,7 +524,7 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
             tc_fence_after();
             const uint32_t sk = sbase + L::kOffK + ks * L::kStageBytes;
             const uint32_t sq = sbase + L::kOffQ + (seg_q & 1) * kSmallBytes;
-#pragma unroll
+#pragma unroll(kMmaUnroll)
             for (int k = 0; k < kHeadDim / 16; ++k) {
               const uint64_t bd =
                   sdesc_sw128(sq + (k >> 2) * kSmallHalf + (k & 3) * 32, 16, 1024);
@@ -598,7 +601,9 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
       tc_fence_after();
       const uint32_t src = sbase + L::kOffK + ks * L::kStageBytes + row * 128;
       const uint32_t dst = k_lane + kColK + (n & 1) * 64;
-#pragma unroll
+      // (not unrolled: with ten warps in five roles the kernel's code is
+      // instruction-cache bound -- unrolling these loops measured slower)
+#pragma unroll 1
       for (int c = 0; c < 8; ++c) {
         const uint4 x = lds128(src + ((c ^ (row & 7)) << 4));
         const uint32_t w[8] = {
@@ -627,7 +632,7 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
       const uint32_t src = sbase + L::kOffV + vs * L::kStageBytes + row * 128;
       const uint32_t dst = sbase + L::kOffVc + (j & 1) * kTileBytes + (row >> 4) * kCacheTileBytes;
       const bool valid = row < nvalid_tok;
-#pragma unroll
+#pragma unroll 1
       for (int c = 0; c < 8; ++c) {
         uint4 x = make_uint4(0u, 0u, 0u, 0u);
         if (valid) x = lds128(src + ((c ^ (row & 7)) << 4));
