@@ -152,6 +152,28 @@ def test_host_validation_before_any_cuda_call(lib):
     assert st == Q.QATTN_ERR_UNSUPPORTED                      # group 9 > 8
 
 
+def test_fp8_host_validation_before_any_cuda_call(lib):
+    """The FP8 entry points reject bad scales and shapes on the host."""
+    fake = ctypes.c_void_p(256)
+    d = Q.make_dims(28, 4)
+    good = (fake, 4608, fake, 4608, fake, 4608, fake, fake, 4, fake, fake, 10, fake, 100,
+            None, None, None, 1e-6)
+    for ks, vs in [(0.0, 1.0), (1.0, -1.0), (float("nan"), 1.0), (1.0, float("inf")),
+                   (1e-40, 1.0)]:
+        assert lib.qattn_rope_cache_append_fp8(*good, ks, vs, d, None, None) == \
+            Q.QATTN_ERR_INVALID_ARG
+        assert lib.qattn_paged_decode_fp8(fake, fake, 4608, fake, fake, 10, fake, 4, fake, 3,
+                                          100, ks, vs, d, fake, 1 << 20, None, None) == \
+            Q.QATTN_ERR_INVALID_ARG
+    assert lib.qattn_rope_cache_append_fp8(*good, 0.5, 0.5, Q.make_dims(28, 4, 128, 48), None,
+                                           None) == Q.QATTN_ERR_UNSUPPORTED
+    assert lib.qattn_paged_decode_fp8(fake, fake, 4608, fake, fake, 10, fake, 4, fake, 0, 100,
+                                      0.5, 0.5, d, fake, 0, None, None) == Q.QATTN_OK
+    assert lib.qattn_paged_decode_fp8(None, fake, 4608, fake, fake, 10, fake, 4, fake, 3, 100,
+                                      0.5, 0.5, d, fake, 1 << 20, None, None) == \
+        Q.QATTN_ERR_INVALID_ARG
+
+
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(RuntimeError, match="not found"):
         Q.load_library(str(tmp_path / "missing.so"))
