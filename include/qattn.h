@@ -362,6 +362,37 @@ int qattn_varlen_prefill(void* out, const void* q, int64_t q_row_stride,
                          size_t workspace_bytes, int32_t* err_word,
                          void* stream);
 
+/* qattn_varlen_prefill over FP8 caches (uint8 e4m3 codes, see above).  The
+ * decode rows read the codes directly (as qattn_paged_decode_fp8); for the
+ * prefill rows (two or more new queries) the sequences' blocks are first
+ * copied into the workspace as bf16 values of the codes (exact: every e4m3
+ * value is a bf16 number), then the bf16 tensor-core prefill runs on the
+ * copy with k_scale folded into the logit scale and v_scale into the
+ * output.
+ *   num_prefill_seqs  host, an upper bound on the sequences with two or
+ *                     more new queries (the copy's capacity, in sequences
+ *                     of up to max_context_len tokens); a sequence beyond it
+ *                     sets QATTN_DEVERR_CONTEXT and its rows are
+ *                     unspecified.
+ *   workspace         qattn_varlen_prefill_fp8_workspace_size(num_seqs,
+ *                     num_prefill_seqs, max_context_len, dims) bytes.
+ * Same arguments and errors as qattn_varlen_prefill otherwise. */
+size_t qattn_varlen_prefill_fp8_workspace_size(int32_t num_seqs,
+                                               int32_t num_prefill_seqs,
+                                               int32_t max_context_len,
+                                               qattn_dims dims);
+int qattn_varlen_prefill_fp8(void* out, const void* q, int64_t q_row_stride,
+                             const int32_t* cu_seqlens_q, int32_t num_seqs,
+                             int32_t total_q, int32_t max_q_len,
+                             const void* k_cache, const void* v_cache,
+                             int32_t num_blocks, const int32_t* block_tables,
+                             int32_t max_blocks_per_seq,
+                             const int32_t* context_lens,
+                             int32_t max_context_len, int32_t num_prefill_seqs,
+                             float k_scale, float v_scale, qattn_dims dims,
+                             void* workspace, size_t workspace_bytes,
+                             int32_t* err_word, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

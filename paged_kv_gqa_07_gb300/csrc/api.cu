@@ -582,6 +582,7 @@ int qattn_paged_decode_shared_prefix(void* out, const void* q, int64_t q_row_str
   p.num_kv_heads = dims.num_kv_heads;
   p.block_size = dims.block_size;
   p.scale_log2 = scale_of(dims) * kLog2e;
+  p.out_scale = 1.0f;
   p.err_word = err_word;
   p.prefix_len = shared_prefix_len;
   p.prefix_splits = splits;
@@ -648,11 +649,140 @@ int qattn_varlen_prefill(void* out, const void* q, int64_t q_row_stride,
   p.num_kv_heads = dims.num_kv_heads;
   p.block_size = dims.block_size;
   p.scale_log2 = scale_of(dims) * kLog2e;
+  p.out_scale = 1.0f;
   p.err_word = err_word;
   p.prefix_len = 0;
   p.prefix_splits = 0;
   p.ws = DecodeWorkspace{};
   const cudaError_t e = launch_varlen_prefill(p, kmap, vmap, sms, s);
+  return e == cudaErrorNotSupported ? QATTN_ERR_UNSUPPORTED : cuda_status(e);
+}
+
+}  // extern "C"
+
+namespace {
+
+// FP8 prefill scratch behind the decode workspace: the scratch block table
+// [num_seqs][bps] and the bf16 copies of the prefill sequences' blocks.
+struct Fp8Scratch {
+  size_t decode_bytes, table_off, k_off, v_off, total;
+  int32_t bps;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+Fp8Scratch fp8_scratch_layout(int32_t num_seqs, int32_t num_prefill_seqs,
+                              int32_t max_context_len, const qattn_dims& d) {
+  Fp8Scratch f;
+  f.decode_bytes = align256(decode_workspace_bytes(num_seqs, max_context_len, d.num_kv_heads,
+                                                   d.num_heads / d.num_kv_heads));
+  f.bps = (max_context_len + d.block_size - 1) / d.block_size;
+  const size_t block_bytes = static_cast<size_t>(d.num_kv_heads) * d.block_size * kHeadDim * 2;
+  const size_t blocks = static_cast<size_t>(num_prefill_seqs) * f.bps;
+  f.table_off = f.decode_bytes;
+  f.k_off = f.table_off + align256(static_cast<size_t>(num_seqs) * f.bps * 4);
+  f.v_off = f.k_off + align256(blocks * block_bytes);
+  f.total = f.v_off + align256(blocks * block_bytes);
+  return f;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t qattn_varlen_prefill_fp8_workspace_size(int32_t num_seqs, int32_t num_prefill_seqs,
+                                               int32_t max_context_len, qattn_dims dims) {
+  if (check_dims(dims) != QATTN_OK || num_seqs < 0 || max_context_len < 0 ||
+      num_prefill_seqs < 0 || num_prefill_seqs > num_seqs)
+    return 0;
+  return fp8_scratch_layout(num_seqs, num_prefill_seqs, max_context_len, dims).total;
+}
+
+int qattn_varlen_prefill_fp8(void* out, const void* q, int64_t q_row_stride,
+                             const int32_t* cu_seqlens_q, int32_t num_seqs, int32_t total_q,
+                             int32_t max_q_len, const void* k_cache, const void* v_cache,
+                             int32_t num_blocks, const int32_t* block_tables,
+                             int32_t max_blocks_per_seq, const int32_t* context_lens,
+                             int32_t max_context_len, int32_t num_prefill_seqs, float k_scale,
+                             float v_scale, qattn_dims dims, void* workspace,
+                             size_t workspace_bytes, int32_t* err_word, void* stream) {
+  int st = check_dims(dims);
+  if (st != QATTN_OK) return st;
+  if (num_seqs < 0 || total_q < 0 || max_q_len < 0 || !valid_scale(k_scale) ||
+      !valid_scale(v_scale) || num_prefill_seqs < 0 || num_prefill_seqs > num_seqs)
+    return QATTN_ERR_INVALID_ARG;
+  if (num_seqs == 0 || total_q == 0) return QATTN_OK;
+  if (cu_seqlens_q == nullptr || max_q_len == 0) return QATTN_ERR_INVALID_ARG;
+  if ((max_q_len + 127) / 128 > kPrefillMaxPairs) return QATTN_ERR_UNSUPPORTED;
+  st = check_attention_args(out, q, q_row_stride, k_cache, v_cache, num_blocks, block_tables,
+                            max_blocks_per_seq, context_lens, max_context_len, dims);
+  if (st != QATTN_OK) return st;
+  const Fp8Scratch f = fp8_scratch_layout(num_seqs, num_prefill_seqs, max_context_len, dims);
+  if (workspace == nullptr || workspace_bytes < f.total ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return QATTN_ERR_WORKSPACE;
+  CUtensorMap kmap, vmap;
+  if (!cached_cache_map(&kmap, k_cache, num_blocks, dims.num_kv_heads, dims.block_size, 1) ||
+      !cached_cache_map(&vmap, v_cache, num_blocks, dims.num_kv_heads, dims.block_size, 1))
+    return QATTN_ERR_CUDA;
+  const int sms = num_sms_current();
+  if (sms <= 0) return QATTN_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // Decode rows (one query): the FP8 decode kernel reads the codes.
+  st = decode_common(out, q, q_row_stride, total_q, cu_seqlens_q, k_cache, v_cache, num_blocks,
+                     block_tables, max_blocks_per_seq, context_lens, num_seqs, max_context_len,
+                     dims, workspace, f.decode_bytes, err_word, s, kmap, vmap, sms, 0, 0, 0, 1,
+                     k_scale, v_scale);
+  if (st != QATTN_OK || max_q_len < 2 || num_prefill_seqs == 0) return st;
+  // Prefill rows: bf16 copies of the code values, then the bf16 prefill.
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  Fp8GatherArgs g;
+  g.k_codes = static_cast<const uint8_t*>(k_cache);
+  g.v_codes = static_cast<const uint8_t*>(v_cache);
+  g.num_blocks = num_blocks;
+  g.block_tables = block_tables;
+  g.max_blocks_per_seq = max_blocks_per_seq;
+  g.context_lens = context_lens;
+  g.cu_seqlens_q = cu_seqlens_q;
+  g.num_seqs = num_seqs;
+  g.num_kv_heads = dims.num_kv_heads;
+  g.block_size = dims.block_size;
+  g.blocks_per_seq = f.bps;
+  g.capacity = num_prefill_seqs;
+  g.k_out = reinterpret_cast<__nv_bfloat16*>(ws + f.k_off);
+  g.v_out = reinterpret_cast<__nv_bfloat16*>(ws + f.v_off);
+  g.table_out = reinterpret_cast<int32_t*>(ws + f.table_off);
+  g.err_word = err_word;
+  cudaError_t e = launch_fp8_gather(g, s);
+  if (e != cudaSuccess) return cuda_status(e);
+  const int32_t scratch_blocks = num_prefill_seqs * f.bps;
+  CUtensorMap skmap, svmap;
+  if (!cached_cache_map(&skmap, g.k_out, scratch_blocks, dims.num_kv_heads, dims.block_size) ||
+      !cached_cache_map(&svmap, g.v_out, scratch_blocks, dims.num_kv_heads, dims.block_size))
+    return QATTN_ERR_CUDA;
+  PrefillArgs p;
+  p.out = out;
+  p.q = q;
+  p.q_row_stride = q_row_stride;
+  p.cu_seqlens_q = cu_seqlens_q;
+  p.context_lens = context_lens;
+  p.block_tables = g.table_out;
+  p.max_blocks_per_seq = f.bps;
+  p.num_seqs = num_seqs;
+  p.num_blocks = scratch_blocks;
+  p.total_q = total_q;
+  p.max_q_len = max_q_len;
+  p.max_context_len = max_context_len;
+  p.num_heads = dims.num_heads;
+  p.num_kv_heads = dims.num_kv_heads;
+  p.block_size = dims.block_size;
+  p.scale_log2 = scale_of(dims) * kLog2e * k_scale;
+  p.out_scale = v_scale;
+  p.err_word = err_word;
+  p.prefix_len = 0;
+  p.prefix_splits = 0;
+  p.ws = DecodeWorkspace{};
+  e = launch_varlen_prefill(p, skmap, svmap, sms, s);
   return e == cudaErrorNotSupported ? QATTN_ERR_UNSUPPORTED : cuda_status(e);
 }
 

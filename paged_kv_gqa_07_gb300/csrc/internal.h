@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -245,6 +246,7 @@ struct PrefillArgs {
   int32_t num_kv_heads;
   int32_t block_size;      // tokens per cache block: 16, 32 or 64
   float scale_log2;
+  float out_scale;         // multiplies the output (v_scale over a dequantised FP8 cache)
   int32_t* err_word;
   // Shared-prefix pass (the same kernel, prefix_len > 0): every sequence's
   // query group against tokens 0 .. prefix_len - 1, held in the blocks of
@@ -260,6 +262,30 @@ struct PrefillArgs {
 constexpr int kPrefillMaxPairs = 384;
 cudaError_t launch_varlen_prefill(const PrefillArgs& a, const CUtensorMap& kmap,
                                   const CUtensorMap& vmap, int num_sms, cudaStream_t stream);
+
+// FP8 cache -> bf16 scratch cache for the sequences with two or more new
+// queries (the prefill rows): the e4m3 code values (exact in bf16), block
+// (b, j) of the k-th such sequence at scratch block k * blocks_per_seq + j,
+// and a scratch block table [num_seqs][blocks_per_seq] (-1 where unused).
+struct Fp8GatherArgs {
+  const uint8_t* k_codes;
+  const uint8_t* v_codes;
+  int32_t num_blocks;
+  const int32_t* block_tables;
+  int32_t max_blocks_per_seq;
+  const int32_t* context_lens;
+  const int32_t* cu_seqlens_q;
+  int32_t num_seqs;
+  int32_t num_kv_heads;
+  int32_t block_size;
+  int32_t blocks_per_seq;   // scratch table row length, ceil(max_context_len / block_size)
+  int32_t capacity;         // prefill sequences the scratch holds
+  __nv_bfloat16* k_out;
+  __nv_bfloat16* v_out;
+  int32_t* table_out;
+  int32_t* err_word;
+};
+cudaError_t launch_fp8_gather(const Fp8GatherArgs& a, cudaStream_t stream);
 // The shared-prefix pass; qmap: the query rows as [rows][heads][128] with a
 // box of 64 dims x G heads x (128 / G) rows.
 constexpr int kMaxPrefixSplits = 32;

@@ -547,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto finish = [&](const Pending& pd, float l) -> bool {
       if (!wait_pv(pd.n)) return false;
       tc_fence_after();
-      const float inv = 1.f / l;
+      const float inv = a.out_scale / l;
       const bool valid = t < pd.rows;
       const uint32_t col = kColO + (pd.r & 1) * kHeadDim + 64 * hf;
       if (prefix_mode) {

@@ -172,6 +172,16 @@ def test_fp8_host_validation_before_any_cuda_call(lib):
     assert lib.qattn_paged_decode_fp8(None, fake, 4608, fake, fake, 10, fake, 4, fake, 3, 100,
                                       0.5, 0.5, d, fake, 1 << 20, None, None) == \
         Q.QATTN_ERR_INVALID_ARG
+    vf = lib.qattn_varlen_prefill_fp8
+    assert vf(fake, fake, 4608, fake, 3, 10, 4, fake, fake, 10, fake, 4, fake, 100, 4, 0.5, 0.5,
+              d, fake, 1 << 30, None, None) == Q.QATTN_ERR_INVALID_ARG   # 4 prefill of 3
+    assert vf(fake, fake, 4608, fake, 3, 10, 4, fake, fake, 10, fake, 4, fake, 100, 2, 0.0, 0.5,
+              d, fake, 1 << 30, None, None) == Q.QATTN_ERR_INVALID_ARG   # bad k_scale
+    assert vf(fake, fake, 4608, fake, 3, 10, 4, fake, fake, 10, fake, 4, fake, 100, 2, 0.5, 0.5,
+              d, fake, 16, None, None) == Q.QATTN_ERR_WORKSPACE          # workspace too small
+    assert Q.qattn_varlen_prefill_fp8_workspace_size(3, 2, 100, d) > \
+        Q.qattn_varlen_prefill_fp8_workspace_size(3, 1, 100, d) > 0
+    assert Q.qattn_varlen_prefill_fp8_workspace_size(3, 4, 100, d) == 0
 
 
 def test_binding_fails_loudly_without_library(tmp_path):

@@ -88,6 +88,16 @@ class Fp8Run:
                                  self.ws, self.err)
         return self
 
+    def varlen(self, num_prefill_seqs=None):
+        g, w = self.g, self.w
+        npf = sum(1 for n in w.q_lens if n >= 2) if num_prefill_seqs is None else num_prefill_seqs
+        n = Q.qattn_varlen_prefill_fp8_workspace_size(w.num_seqs, npf, self.max_ctx, self.dims)
+        ws = torch.empty(max(n, 256), dtype=torch.uint8, device=self.dev)
+        Q.qattn_varlen_prefill_fp8(self.out, g.q_view(), g.cu_seqlens_q, w.max_q_len, g.k_cache,
+                                   g.v_cache, g.block_tables, g.context_lens, self.max_ctx, npf,
+                                   self.ks, self.vs, self.dims, ws, self.err)
+        return self
+
     def sync(self):
         torch.cuda.synchronize(self.dev)
         return self
@@ -179,3 +189,35 @@ def test_decode_fp8_bad_scale_rejected():
         r.ks = ks
         with pytest.raises(Q.QattnError):
             r.decode()
+
+
+def test_varlen_fp8_mixed_workload():
+    """4 prefill chunks of 512 on 0-1536 cached tokens + 60 decode rows."""
+    w = W.with_fp8_cache(W.build(2))
+    _, _, _, ref, _, e2 = oracle_fp8(w)
+    r = Fp8Run(w).append().varlen().sync()
+    assert int(r.err.item()) == 0 and e2 == 0
+    assert_close(r.out, ref)
+
+
+@pytest.mark.parametrize("bs", [16, 64])
+def test_varlen_fp8_ragged(bs):
+    ctx = [300, 700, 64, 1, 129, 900, 2, 40]
+    q_lens = [200, 33, 64, 1, 1, 130, 2, 1]
+    w = W.with_fp8_cache(W.custom(28, 4, ctx=ctx, q_lens=q_lens, seed=850 + bs, block_size=bs))
+    _, _, _, ref, _, e2 = oracle_fp8(w)
+    r = Fp8Run(w).append().varlen().sync()
+    assert int(r.err.item()) == 0 and e2 == 0
+    assert_close(r.out, ref)
+
+
+def test_varlen_fp8_capacity_exceeded_sets_error():
+    w = W.with_fp8_cache(W.custom(8, 2, ctx=[100, 200, 50], q_lens=[10, 20, 5], seed=860))
+    _, _, _, ref, _, _ = oracle_fp8(w)
+    r = Fp8Run(w).append().varlen(num_prefill_seqs=2).sync()
+    assert int(r.err.item()) & Q.DEVERR_CONTEXT
+    # the first two prefill sequences are still right
+    rows = slice(0, 30)
+    g = r.out.float().cpu().double().numpy()[rows]
+    d = np.abs(g - ref[rows]) - BF16_HALF_ULP * np.abs(ref[rows])
+    assert float(d.max()) <= ATOL
