@@ -303,6 +303,28 @@ int qattn_paged_decode_shared_prefix(void* out, const void* q, int64_t q_row_str
                                      void* workspace, size_t workspace_bytes,
                                      int32_t* err_word, void* stream);
 
+/* qattn_paged_decode_shared_prefix over FP8 caches (uint8 e4m3 codes).  The
+ * prefix blocks (those of table row 0) are copied into the workspace as bf16
+ * values of their codes (exact) and the prefix pass runs on the copy; each
+ * sequence's own tokens are read as codes by the FP8 decode.  Workspace:
+ * qattn_paged_decode_shared_prefix_fp8_workspace_size(num_seqs,
+ * max_context_len, shared_prefix_len, dims) bytes.  Same arguments and
+ * errors as qattn_paged_decode_shared_prefix, plus the scales. */
+size_t qattn_paged_decode_shared_prefix_fp8_workspace_size(int32_t num_seqs,
+                                                           int32_t max_context_len,
+                                                           int32_t shared_prefix_len,
+                                                           qattn_dims dims);
+int qattn_paged_decode_shared_prefix_fp8(void* out, const void* q, int64_t q_row_stride,
+                                         const void* k_cache, const void* v_cache,
+                                         int32_t num_blocks, const int32_t* block_tables,
+                                         int32_t max_blocks_per_seq,
+                                         const int32_t* context_lens, int32_t num_seqs,
+                                         int32_t max_context_len,
+                                         int32_t shared_prefix_len, float k_scale,
+                                         float v_scale, qattn_dims dims, void* workspace,
+                                         size_t workspace_bytes, int32_t* err_word,
+                                         void* stream);
+
 /* qattn_paged_decode for callers that cannot allocate device memory (code
  * running inside someone else's CUDA-graph capture, a serving loop whose
  * memory pool is fixed at start-up, a host that only lends the tensors it

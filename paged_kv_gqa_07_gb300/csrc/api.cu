@@ -786,4 +786,128 @@ int qattn_varlen_prefill_fp8(void* out, const void* q, int64_t q_row_stride,
   return e == cudaErrorNotSupported ? QATTN_ERR_UNSUPPORTED : cuda_status(e);
 }
 
+size_t qattn_paged_decode_shared_prefix_fp8_workspace_size(int32_t num_seqs,
+                                                           int32_t max_context_len,
+                                                           int32_t shared_prefix_len,
+                                                           qattn_dims dims) {
+  if (check_dims(dims) != QATTN_OK || num_seqs < 0 || max_context_len < 0 ||
+      shared_prefix_len < 0 || shared_prefix_len % dims.block_size != 0)
+    return 0;
+  const int32_t pb = shared_prefix_len / dims.block_size;
+  const size_t block_bytes =
+      static_cast<size_t>(dims.num_kv_heads) * dims.block_size * kHeadDim * 2;
+  return align256(qattn_paged_decode_shared_prefix_workspace_size(num_seqs, max_context_len,
+                                                                  dims)) +
+         align256(static_cast<size_t>(num_seqs) * pb * 4) + 2 * align256(pb * block_bytes);
+}
+
+int qattn_paged_decode_shared_prefix_fp8(void* out, const void* q, int64_t q_row_stride,
+                                         const void* k_cache, const void* v_cache,
+                                         int32_t num_blocks, const int32_t* block_tables,
+                                         int32_t max_blocks_per_seq,
+                                         const int32_t* context_lens, int32_t num_seqs,
+                                         int32_t max_context_len, int32_t shared_prefix_len,
+                                         float k_scale, float v_scale, qattn_dims dims,
+                                         void* workspace, size_t workspace_bytes,
+                                         int32_t* err_word, void* stream) {
+  int st = check_dims(dims);
+  if (st != QATTN_OK) return st;
+  if (num_seqs < 0 || !valid_scale(k_scale) || !valid_scale(v_scale))
+    return QATTN_ERR_INVALID_ARG;
+  if (num_seqs == 0) return QATTN_OK;
+  st = check_attention_args(out, q, q_row_stride, k_cache, v_cache, num_blocks, block_tables,
+                            max_blocks_per_seq, context_lens, max_context_len, dims);
+  if (st != QATTN_OK) return st;
+  if (shared_prefix_len < 0 || shared_prefix_len % dims.block_size != 0 ||
+      shared_prefix_len >= max_context_len ||
+      shared_prefix_len > static_cast<int64_t>(max_blocks_per_seq) * dims.block_size)
+    return QATTN_ERR_INVALID_ARG;
+  const size_t need = qattn_paged_decode_shared_prefix_fp8_workspace_size(
+      num_seqs, max_context_len, shared_prefix_len, dims);
+  if (workspace == nullptr || workspace_bytes < need ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return QATTN_ERR_WORKSPACE;
+  CUtensorMap kmap, vmap;
+  if (!cached_cache_map(&kmap, k_cache, num_blocks, dims.num_kv_heads, dims.block_size, 1) ||
+      !cached_cache_map(&vmap, v_cache, num_blocks, dims.num_kv_heads, dims.block_size, 1))
+    return QATTN_ERR_CUDA;
+  const int sms = num_sms_current();
+  if (sms <= 0) return QATTN_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t decode_bytes =
+      align256(qattn_paged_decode_shared_prefix_workspace_size(num_seqs, max_context_len, dims));
+  if (shared_prefix_len == 0)
+    return decode_common(out, q, q_row_stride, num_seqs, nullptr, k_cache, v_cache, num_blocks,
+                         block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                         max_context_len, dims, workspace, decode_bytes, err_word, s, kmap,
+                         vmap, sms, 0, 0, kMaxPrefixSplits, 1, k_scale, v_scale);
+  // The prefix as bf16 values of its codes (exact), then the prefix pass on
+  // the copy with the scales folded in.
+  const int32_t pb = shared_prefix_len / dims.block_size;
+  const size_t block_bytes =
+      static_cast<size_t>(dims.num_kv_heads) * dims.block_size * kHeadDim * 2;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  Fp8GatherArgs g{};
+  g.k_codes = static_cast<const uint8_t*>(k_cache);
+  g.v_codes = static_cast<const uint8_t*>(v_cache);
+  g.num_blocks = num_blocks;
+  g.block_tables = block_tables;
+  g.max_blocks_per_seq = max_blocks_per_seq;
+  g.num_seqs = num_seqs;
+  g.num_kv_heads = dims.num_kv_heads;
+  g.block_size = dims.block_size;
+  g.blocks_per_seq = pb;
+  g.table_out = reinterpret_cast<int32_t*>(ws + decode_bytes);
+  const size_t k_off = decode_bytes + align256(static_cast<size_t>(num_seqs) * pb * 4);
+  g.k_out = reinterpret_cast<__nv_bfloat16*>(ws + k_off);
+  g.v_out = reinterpret_cast<__nv_bfloat16*>(ws + k_off + align256(pb * block_bytes));
+  g.err_word = err_word;
+  cudaError_t e = launch_fp8_prefix_gather(g, s);
+  if (e != cudaSuccess) return cuda_status(e);
+  CUtensorMap skmap, svmap;
+  if (!cached_cache_map(&skmap, g.k_out, pb, dims.num_kv_heads, dims.block_size) ||
+      !cached_cache_map(&svmap, g.v_out, pb, dims.num_kv_heads, dims.block_size))
+    return QATTN_ERR_CUDA;
+  const int group = dims.num_heads / dims.num_kv_heads;
+  const int rows_per_tile = 128 / group;
+  const int row_tiles = (num_seqs + rows_per_tile - 1) / rows_per_tile;
+  const int prefix_tiles = (shared_prefix_len + 127) / 128;
+  int splits = sms / (dims.num_kv_heads * row_tiles);
+  if (splits > prefix_tiles) splits = prefix_tiles;
+  if (splits > kMaxPrefixSplits) splits = kMaxPrefixSplits;
+  if (splits < 1) splits = 1;
+  CUtensorMap qmap;
+  if (!encode_q_group_map(&qmap, q, q_row_stride, num_seqs, dims.num_heads, group,
+                          rows_per_tile))
+    return QATTN_ERR_CUDA;
+  PrefillArgs p{};
+  p.q = q;
+  p.q_row_stride = q_row_stride;
+  p.context_lens = context_lens;
+  p.block_tables = g.table_out;
+  p.max_blocks_per_seq = pb;
+  p.num_seqs = num_seqs;
+  p.num_blocks = pb;
+  p.total_q = num_seqs;
+  p.max_q_len = 1;
+  p.max_context_len = max_context_len;
+  p.num_heads = dims.num_heads;
+  p.num_kv_heads = dims.num_kv_heads;
+  p.block_size = dims.block_size;
+  p.scale_log2 = scale_of(dims) * kLog2e * k_scale;
+  p.out_scale = v_scale;
+  p.err_word = err_word;
+  p.prefix_len = shared_prefix_len;
+  p.prefix_splits = splits;
+  p.ws = carve_decode_workspace(workspace, num_seqs, max_context_len, dims.num_kv_heads, group,
+                                kMaxPrefixSplits);
+  st = cuda_status(launch_shared_prefix(p, qmap, skmap, svmap, sms, s));
+  if (st != QATTN_OK) return st;
+  // Each sequence's own tokens from the codes, then the merge of all parts.
+  return decode_common(out, q, q_row_stride, num_seqs, nullptr, k_cache, v_cache, num_blocks,
+                       block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                       max_context_len, dims, workspace, decode_bytes, err_word, s, kmap, vmap,
+                       sms, shared_prefix_len, splits, kMaxPrefixSplits, 1, k_scale, v_scale);
+}
+
 }  // extern "C"

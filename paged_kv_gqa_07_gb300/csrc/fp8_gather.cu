@@ -93,7 +93,52 @@ __global__ void __launch_bounds__(kThreads) fp8_gather_kernel(const Fp8GatherArg
   }
 }
 
+// The shared prefix of a batch (blocks 0 .. blocks_per_seq - 1 of table row
+// 0) to scratch blocks 0 .., every row of the scratch table pointing at them
+// (the prefix pass reads row 0 and compares the others with it); the real
+// check -- every sequence's table starts with row 0's prefix blocks -- is
+// made here on the caller's tables.  grid.x: copy CTAs of kBlocksPerCta
+// blocks; every CTA also takes a share of the (row, block) table entries.
+__global__ void __launch_bounds__(kThreads) fp8_prefix_gather_kernel(const Fp8GatherArgs a) {
+  const int pb = a.blocks_per_seq;
+  const int tid = threadIdx.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + tid;
+       i < static_cast<int64_t>(a.num_seqs) * pb; i += static_cast<int64_t>(gridDim.x) * kThreads) {
+    const int b = static_cast<int>(i / pb), j = static_cast<int>(i % pb);
+    const int id0 = a.block_tables[j];
+    const bool ok0 = id0 >= 0 && id0 < a.num_blocks;
+    if (b > 0 && a.block_tables[static_cast<int64_t>(b) * a.max_blocks_per_seq + j] != id0)
+      set_err(a.err_word, QATTN_DEVERR_PREFIX);
+    a.table_out[i] = ok0 ? j : -1;  // -1: flagged by the prefix pass
+  }
+  const int j0 = blockIdx.x * kBlocksPerCta;
+  const int j1 = min(pb, j0 + kBlocksPerCta);
+  const int chunks = a.num_kv_heads * a.block_size * (kHeadDim / 16);
+  for (int j = j0; j < j1; ++j) {
+    const int id = a.block_tables[j];
+    if (id < 0 || id >= a.num_blocks) continue;
+    const int64_t src = static_cast<int64_t>(id) * chunks;
+    const int64_t dst = static_cast<int64_t>(j) * chunks;
+    for (int c = tid; c < chunks; c += kThreads) {
+      uint4 lo, hi;
+      codes16_to_bf16(reinterpret_cast<const uint4*>(a.k_codes)[src + c], lo, hi);
+      reinterpret_cast<uint4*>(a.k_out)[2 * (dst + c)] = lo;
+      reinterpret_cast<uint4*>(a.k_out)[2 * (dst + c) + 1] = hi;
+      codes16_to_bf16(reinterpret_cast<const uint4*>(a.v_codes)[src + c], lo, hi);
+      reinterpret_cast<uint4*>(a.v_out)[2 * (dst + c)] = lo;
+      reinterpret_cast<uint4*>(a.v_out)[2 * (dst + c) + 1] = hi;
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_fp8_prefix_gather(const Fp8GatherArgs& a, cudaStream_t stream) {
+  if (a.num_seqs <= 0 || a.blocks_per_seq <= 0) return cudaSuccess;
+  const int grid = (a.blocks_per_seq + kBlocksPerCta - 1) / kBlocksPerCta;
+  fp8_prefix_gather_kernel<<<grid, kThreads, 0, stream>>>(a);
+  return cudaPeekAtLastError();
+}
 
 cudaError_t launch_fp8_gather(const Fp8GatherArgs& a, cudaStream_t stream) {
   if (a.num_seqs <= 0 || a.blocks_per_seq <= 0) return cudaSuccess;

@@ -286,6 +286,10 @@ struct Fp8GatherArgs {
   int32_t* err_word;
 };
 cudaError_t launch_fp8_gather(const Fp8GatherArgs& a, cudaStream_t stream);
+// The shared prefix (blocks_per_seq = prefix blocks of table row 0) to
+// scratch blocks 0 .., a scratch table of num_seqs identical rows, and the
+// check that every table starts with row 0's blocks (QATTN_DEVERR_PREFIX).
+cudaError_t launch_fp8_prefix_gather(const Fp8GatherArgs& a, cudaStream_t stream);
 // The shared-prefix pass; qmap: the query rows as [rows][heads][128] with a
 // box of 64 dims x G heads x (128 / G) rows.
 constexpr int kMaxPrefixSplits = 32;

@@ -47,6 +47,8 @@ EXPORTED = [
     "qattn_paged_decode_noalloc",
     "qattn_paged_decode_shared_prefix_workspace_size",
     "qattn_paged_decode_shared_prefix",
+    "qattn_paged_decode_shared_prefix_fp8_workspace_size",
+    "qattn_paged_decode_shared_prefix_fp8",
     "qattn_varlen_prefill_workspace_size",
     "qattn_varlen_prefill",
     "qattn_varlen_prefill_fp8_workspace_size",
@@ -126,6 +128,13 @@ def load_library(path: str | None = None):
             _P, _P, _I64, _P, _P, _I32, _P, _I32, _P, _I32, _I32, _I32, qattn_dims, _P, _SZ, _P,
             _P]
         L.qattn_paged_decode_shared_prefix.restype = ctypes.c_int
+        L.qattn_paged_decode_shared_prefix_fp8_workspace_size.argtypes = [_I32, _I32, _I32,
+                                                                          qattn_dims]
+        L.qattn_paged_decode_shared_prefix_fp8_workspace_size.restype = _SZ
+        L.qattn_paged_decode_shared_prefix_fp8.argtypes = [
+            _P, _P, _I64, _P, _P, _I32, _P, _I32, _P, _I32, _I32, _I32, ctypes.c_float,
+            ctypes.c_float, qattn_dims, _P, _SZ, _P, _P]
+        L.qattn_paged_decode_shared_prefix_fp8.restype = ctypes.c_int
         L.qattn_varlen_prefill_workspace_size.argtypes = [_I32, _I32, qattn_dims]
         L.qattn_varlen_prefill_workspace_size.restype = _SZ
         L.qattn_varlen_prefill.argtypes = [
@@ -380,3 +389,26 @@ def qattn_varlen_prefill_fp8(out, q, cu_seqlens_q, max_q_len, k_cache, v_cache, 
         _dev_ptr(workspace, "workspace"), int(workspace.numel() * workspace.element_size()),
         _dev_ptr(err_word, "err_word", torch.int32), _stream(stream))
     _check("qattn_varlen_prefill_fp8", rc)
+
+
+def qattn_paged_decode_shared_prefix_fp8_workspace_size(num_seqs: int, max_context_len: int,
+                                                        shared_prefix_len: int, dims) -> int:
+    return int(lib().qattn_paged_decode_shared_prefix_fp8_workspace_size(
+        int(num_seqs), int(max_context_len), int(shared_prefix_len), dims))
+
+
+def qattn_paged_decode_shared_prefix_fp8(out, q, k_cache, v_cache, block_tables, context_lens,
+                                         max_context_len, shared_prefix_len, k_scale, v_scale,
+                                         dims, workspace, err_word=None, stream=None):
+    """qattn_paged_decode_shared_prefix over e4m3 caches read as code * scale."""
+    qp, qs = _rows(q, "q")
+    rc = lib().qattn_paged_decode_shared_prefix_fp8(
+        _dev_ptr(out, "out", torch.bfloat16), qp, qs,
+        _fp8_ptr(k_cache, "k_cache"), _fp8_ptr(v_cache, "v_cache"),
+        int(k_cache.shape[0]), _dev_ptr(block_tables, "block_tables", torch.int32),
+        int(block_tables.shape[1]), _dev_ptr(context_lens, "context_lens", torch.int32),
+        int(context_lens.shape[0]), int(max_context_len), int(shared_prefix_len),
+        float(k_scale), float(v_scale), dims, _dev_ptr(workspace, "workspace"),
+        int(workspace.numel() * workspace.element_size()),
+        _dev_ptr(err_word, "err_word", torch.int32), _stream(stream))
+    _check("qattn_paged_decode_shared_prefix_fp8", rc)

@@ -221,3 +221,45 @@ def test_varlen_fp8_capacity_exceeded_sets_error():
     g = r.out.float().cpu().double().numpy()[rows]
     d = np.abs(g - ref[rows]) - BF16_HALF_ULP * np.abs(ref[rows])
     assert float(d.max()) <= ATOL
+
+
+def run_prefix_fp8(r, prefix):
+    g, w = r.g, r.w
+    n = Q.qattn_paged_decode_shared_prefix_fp8_workspace_size(w.num_seqs, r.max_ctx, prefix,
+                                                              r.dims)
+    ws = torch.empty(n, dtype=torch.uint8, device=r.dev)
+    Q.qattn_paged_decode_shared_prefix_fp8(r.out, g.q_view(), g.k_cache, g.v_cache,
+                                           g.block_tables, g.context_lens, r.max_ctx, prefix,
+                                           r.ks, r.vs, r.dims, ws, r.err)
+    return r.sync()
+
+
+def test_shared_prefix_fp8_workload():
+    """128 sequences on a 2048-token shared prefix (Qwen3-0.6B heads)."""
+    w = W.with_fp8_cache(W.build(4))
+    _, _, _, ref, _, e2 = oracle_fp8(w)
+    r = run_prefix_fp8(Fp8Run(w).append().sync(), w.shared_prefix_tokens)
+    assert int(r.err.item()) == 0 and e2 == 0
+    assert_close(r.out, ref)
+
+
+@pytest.mark.parametrize("group,kv,prefix,bs", [(1, 4, 16, 16), (7, 4, 400, 16),
+                                               (8, 2, 1024, 32), (2, 8, 192, 64)])
+def test_shared_prefix_fp8(group, kv, prefix, bs):
+    suffix = [1, 2, 15, 16, 17, 100, 128, 129, 300, 64]
+    ctx = [prefix + s_ for s_ in suffix]
+    w = W.with_fp8_cache(W.custom(group * kv, kv, ctx=ctx, q_lens=[1] * len(ctx),
+                                  seed=870 + group + bs, shared_prefix_tokens=prefix,
+                                  block_size=bs))
+    _, _, _, ref, _, e2 = oracle_fp8(w)
+    r = run_prefix_fp8(Fp8Run(w).append().sync(), prefix)
+    assert int(r.err.item()) == 0 and e2 == 0
+    assert_close(r.out, ref)
+
+
+def test_shared_prefix_fp8_table_mismatch_flagged():
+    w = W.with_fp8_cache(W.custom(16, 8, ctx=[300, 400], q_lens=[1, 1], seed=880,
+                                  shared_prefix_tokens=256))
+    w.block_tables[1, 3] = w.block_tables[1, 20]    # second table leaves the prefix
+    r = run_prefix_fp8(Fp8Run(w).append().sync(), 256)
+    assert int(r.err.item()) & Q.DEVERR_PREFIX
