@@ -56,8 +56,7 @@ def parse():
     p.add_argument("--block-size", type=int, choices=[16, 32, 64], default=16,
                    help="cache block size of the decode / mixed workloads")
     p.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
-                   help="cache dtype: bf16, or e4m3 codes with a per-tensor scale (decode "
-                        "workloads without a shared prefix)")
+                   help="cache dtype: bf16, or e4m3 codes with a per-tensor scale")
     p.add_argument("--extras", choices=["none", "bias", "qknorm", "both"], default="none",
                    help="add the qkv projection bias and/or the Qwen3 q/k RMSNorms to the "
                         "RoPE + append step (synthetic weights)")
@@ -231,8 +230,6 @@ def run_ours(args, dist: Dist):
                 block_size=args.block_size)
     fp8 = args.kv == "fp8"
     if fp8:
-        if not w.is_decode or w.shared_prefix_tokens:
-            raise SystemExit("--kv fp8 times the plain decode workloads")
         w = W.with_fp8_cache(w)
     ks, vs = W.FP8_K_SCALE, W.FP8_V_SCALE
     H, Hkv, D, BS = w.num_heads, w.num_kv_heads, w.head_dim, w.block_size
@@ -245,7 +242,13 @@ def run_ours(args, dist: Dist):
     max_ctx = w.max_context_len
     # a decode batch on a shared cached prefix takes the shared-prefix entry point
     prefix = w.shared_prefix_tokens if decode else 0
-    if prefix:
+    n_prefill = sum(1 for n in w.q_lens if n >= 2)
+    if prefix and fp8:
+        ws_size = Q.qattn_paged_decode_shared_prefix_fp8_workspace_size(w.num_seqs, max_ctx,
+                                                                         prefix, dims)
+    elif not decode and fp8:
+        ws_size = Q.qattn_varlen_prefill_fp8_workspace_size(w.num_seqs, n_prefill, max_ctx, dims)
+    elif prefix:
         ws_size = Q.qattn_paged_decode_shared_prefix_workspace_size(w.num_seqs, max_ctx, dims)
     elif decode:
         ws_size = Q.qattn_paged_decode_workspace_size(w.num_seqs, max_ctx, dims)
@@ -280,7 +283,15 @@ def run_ours(args, dist: Dist):
                                          err_word=err)
 
     def attend():
-        if prefix:
+        if prefix and fp8:
+            Q.qattn_paged_decode_shared_prefix_fp8(out, g.q_view(), g.k_cache, g.v_cache,
+                                                   g.block_tables, g.context_lens, max_ctx,
+                                                   prefix, ks, vs, dims, ws, err)
+        elif not decode and fp8:
+            Q.qattn_varlen_prefill_fp8(out, g.q_view(), g.cu_seqlens_q, w.max_q_len, g.k_cache,
+                                       g.v_cache, g.block_tables, g.context_lens, max_ctx,
+                                       n_prefill, ks, vs, dims, ws, err)
+        elif prefix:
             Q.qattn_paged_decode_shared_prefix(out, g.q_view(), g.k_cache, g.v_cache,
                                                g.block_tables, g.context_lens, max_ctx, prefix,
                                                dims, ws, err)
@@ -411,7 +422,9 @@ def run_ours(args, dist: Dist):
         "attention_ms": round(statistics.mean(attn_ms), 5),
         # per step: RoPE + append, the decode kernel and its merge kernel
         # (and, with prefill rows, the prefill kernel)
-        "gpu_launches": (4 if prefix else 3 if decode else 4) * args.steps,
+        # (+1 for the FP8 gather of the prefill / prefix blocks)
+        "gpu_launches": ((4 if prefix else 3 if decode else 4) +
+                         (1 if fp8 and (prefix or not decode) else 0)) * args.steps,
         **result,
     }
     if e2e is not None:
@@ -448,9 +461,20 @@ def run_e2e(args, w, dims, g, table, ws, err, dev, decode, max_ctx, dist, prefix
                                           qkv[:, (H + Hkv) * D:], dev_in["positions"],
                                           dev_in["slot_mapping"], g.k_cache, g.v_cache, table,
                                           *fp8_scales, dims, err_word=err)
-            Q.qattn_paged_decode_fp8(out, qkv[:, :H * D], g.k_cache, g.v_cache,
-                                     dev_in["block_tables"], dev_in["context_lens"], max_ctx,
-                                     *fp8_scales, dims, ws, err)
+            if prefix:
+                Q.qattn_paged_decode_shared_prefix_fp8(
+                    out, qkv[:, :H * D], g.k_cache, g.v_cache, dev_in["block_tables"],
+                    dev_in["context_lens"], max_ctx, prefix, *fp8_scales, dims, ws, err)
+            elif decode:
+                Q.qattn_paged_decode_fp8(out, qkv[:, :H * D], g.k_cache, g.v_cache,
+                                         dev_in["block_tables"], dev_in["context_lens"], max_ctx,
+                                         *fp8_scales, dims, ws, err)
+            else:
+                n_prefill = sum(1 for n in w.q_lens if n >= 2)
+                Q.qattn_varlen_prefill_fp8(out, qkv[:, :H * D], dev_in["cu_seqlens_q"],
+                                           w.max_q_len, g.k_cache, g.v_cache,
+                                           dev_in["block_tables"], dev_in["context_lens"],
+                                           max_ctx, n_prefill, *fp8_scales, dims, ws, err)
             host_out.copy_(out, non_blocking=True)
             return
         Q.qattn_rope_cache_append(qkv[:, :H * D], qkv[:, H * D:(H + Hkv) * D],
