@@ -213,6 +213,23 @@ __device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
 
 // ------------------------------------------------------ shared loads ------
 
+// max(a, b, c) in one instruction (three-input max).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// 2^x by the hardware approximation (ex2.approx.ftz: relative error near
+// 2^-22, results below 2^-126 flushed to zero) -- for softmax weights that
+// are rounded to bf16 or f16 right after, where exp2f's extra range handling
+// buys nothing.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Two fp32 values -> two e4m3 codes (lo in bits 0..7, hi in bits 8..15),
 // round to nearest even, saturating to +-448 (NaN stays NaN).
 __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {

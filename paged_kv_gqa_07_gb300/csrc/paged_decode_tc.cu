@@ -854,7 +854,7 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
           unsigned short pbits[G];
 #pragma unroll
           for (int h = 0; h < G; ++h) {
-            const float p = exp2f(s[j][h] - m_used[h]);
+            const float p = fast_exp2(s[j][h] - m_used[h]);
             if constexpr (kFp8) {
               const __half ph = __float2half_rn(p);
               pbits[h] = __half_as_ushort(ph);

@@ -632,11 +632,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         float mx8[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) mx8[i] = s[i];
+        for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(s[i], s[56 + i]);
 #pragma unroll
-        for (int c = 8; c < 64; c += 8) {
+        for (int c = 8; c < 56; c += 16) {
 #pragma unroll
-          for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], s[c + i]);
+          for (int i = 0; i < 8; ++i) mx8[i] = fmax3(mx8[i], s[c + i], s[c + 8 + i]);
         }
         const float mh = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                                fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
@@ -681,27 +681,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        // p = 2^(scale_log2 * s - m): one FMA and one exp2 per score; eight
-        // partial sums; P half hf of row t, swizzled K-major.
-        float sum8[8];
+        // p = 2^(scale_log2 * s - m): one FMA (packed two at a time) and one
+        // exp2 per score; eight partial sums (packed adds); P half hf of row
+        // t, swizzled K-major.
+        float2 sum2[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) sum8[i] = 0.f;
+        for (int i = 0; i < 4; ++i) sum2[i] = make_float2(0.f, 0.f);
         const uint32_t sp_row = sbase + kOffP + sb * kTileBytes + hf * kHalfBytes + t * 128;
-        const float neg_m = -m_run;
+        const float2 scale2 = make_float2(a.scale_log2, a.scale_log2);
+        const float2 neg_m2 = make_float2(-m_run, -m_run);
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc) {
           float p[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            p[i] = exp2f(fmaf(s[cc * 8 + i], a.scale_log2, neg_m));
-            sum8[i] += p[i];
+          for (int i = 0; i < 4; ++i) {
+            const float2 x =
+                __ffma2_rn(make_float2(s[cc * 8 + 2 * i], s[cc * 8 + 2 * i + 1]), scale2, neg_m2);
+            p[2 * i] = fast_exp2(x.x);
+            p[2 * i + 1] = fast_exp2(x.y);
+            sum2[i] = __fadd2_rn(sum2[i], make_float2(p[2 * i], p[2 * i + 1]));
           }
           sts128(sp_row + ((cc ^ (t & 7)) << 4), pack_bf16x2_rn(p[0], p[1]),
                  pack_bf16x2_rn(p[2], p[3]), pack_bf16x2_rn(p[4], p[5]),
                  pack_bf16x2_rn(p[6], p[7]));
         }
-        l_run += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
-                 ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+        l_run += ((sum2[0].x + sum2[0].y) + (sum2[1].x + sum2[1].y)) +
+                 ((sum2[2].x + sum2[2].y) + (sum2[3].x + sum2[3].y));
         if ((d_kt0 + kt) * kN + kN > d_L) {
           // The tile reaches past the context: zero V rows of keys >= L once
           // V(n) has landed (PV(n-2) is done, so this barrier is at most one
