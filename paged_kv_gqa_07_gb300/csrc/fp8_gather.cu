@@ -17,7 +17,7 @@ namespace qattn {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kBlocksPerCta = 8;
+constexpr int kBlocksPerCta = 2;
 
 // 16 e4m3 codes -> 16 bf16 values (exact: e4m3 -> f16 -> f32 -> bf16).
 __device__ __forceinline__ void codes16_to_bf16(const uint4& c, uint4& lo, uint4& hi) {
