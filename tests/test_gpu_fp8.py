@@ -263,3 +263,47 @@ def test_shared_prefix_fp8_table_mismatch_flagged():
     w.block_tables[1, 3] = w.block_tables[1, 20]    # second table leaves the prefix
     r = run_prefix_fp8(Fp8Run(w).append().sync(), 256)
     assert int(r.err.item()) & Q.DEVERR_PREFIX
+
+
+def test_decode_fp8_error_bits():
+    """A bad context or block id flags its bit and leaves the other rows
+    right (the same device-side checks as the bf16 path)."""
+    w = W.with_fp8_cache(W.build(0))
+    _, _, _, ref, _, _ = oracle_fp8(w)
+    r = Fp8Run(w).append().sync()
+    r.g.context_lens[1] = 0                     # invalid context: zero row
+    r.g.block_tables[2, 3] = w.num_blocks + 9   # bad block id
+    r.decode().sync()
+    bits = int(r.err.item())
+    assert bits & Q.DEVERR_CONTEXT and bits & Q.DEVERR_BLOCK and not bits & Q.DEVERR_TIMEOUT
+    assert torch.count_nonzero(r.out[1]) == 0
+    g = r.out.float().cpu().double().numpy()
+    for row in (0, 3):
+        d = np.abs(g[row] - ref[row]) - BF16_HALF_ULP * np.abs(ref[row])
+        assert float(d.max()) <= ATOL
+
+
+def test_fp8_step_graph_replay():
+    """Append + FP8 decode + merge captured in a CUDA graph replays to the
+    eager result."""
+    w = W.with_fp8_cache(W.build(1))
+    r = Fp8Run(w)
+    qkv0 = r.g.qkv.clone()
+    k0, v0 = r.g.k_cache.clone(), r.g.v_cache.clone()
+    r.append().decode().sync()
+    first = r.out.clone()
+    s = torch.cuda.Stream(device=r.dev)
+    s.wait_stream(torch.cuda.current_stream(r.dev))
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            r.g.qkv.copy_(qkv0)
+            r.g.k_cache.copy_(k0)
+            r.g.v_cache.copy_(v0)
+            r.append().decode()
+    for _ in range(3):
+        r.out.zero_()
+        graph.replay()
+        r.sync()
+        assert int(r.err.item()) == 0
+        assert torch.equal(r.out, first)
