@@ -20,9 +20,11 @@
 //   * Warp roles: warp 8 copies Q of an item and its K tiles (eight 16-token
 //     blocks gathered through the block table, one 4 KB TMA box per (block,
 //     kv head), 128-byte swizzle) into a 2-deep ring; warp 10 copies the V
-//     tiles into their own ring; one thread of warp 9 issues tcgen05.mma as
-//     soon as each operand set is ready (S = Q K^T into one of two TMEM S
-//     buffers, O += P V into the item's TMEM O slot); warps 0-7 do the
+//     tiles into their own ring; one thread of warp 9 issues the Q K^T
+//     stream (S into one of two TMEM S buffers) and one of warp 11 the P V
+//     stream (O += P V into the item's TMEM O slot), each as soon as its
+//     operands are ready -- two issuers, since a thread issuing tcgen05.mma
+//     waits for the pipe to take each one; warps 0-7 do the
 //     online softmax, two per TMEM lane quarter (rows 32q .. 32q + 31), one
 //     per half of the 128 keys of a tile: S half-row from TMEM, causal mask
 //     (only on tiles that cross the diagonal), half-row max swapped with the
@@ -53,7 +55,8 @@ constexpr int kSoftmaxWarps = 8;        // two per TMEM lane quarter: column hal
 constexpr int kProducerWarp = 8;        // Q and K copies
 constexpr int kMmaWarp = 9;
 constexpr int kVProducerWarp = 10;      // V copies
-constexpr int kWarps = 11;
+constexpr int kPvWarp = 11;             // issues the P V stream (warp 9: Q K^T)
+constexpr int kWarps = 12;
 constexpr int kThreads = kWarps * 32;
 constexpr int kHalfBytes = 128 * 128;   // 128 rows x 128 B (Q and P: [half][row])
 constexpr int kTileBytes = 2 * kHalfBytes;
@@ -71,8 +74,7 @@ constexpr int kOffV = kOffK + 2 * kTileBytes;      // 2 stages
 constexpr int kOffP = kOffV + 2 * kTileBytes;      // 2 buffers
 constexpr int kOffPairs = kOffP + 2 * kTileBytes;  // int[kPrefillMaxPairs], ranked
 constexpr int kOffDesc = kOffPairs + kPrefillMaxPairs * 4;  // ItemDesc[2]
-constexpr int kOffNkv = kOffDesc + 2 * 64;         // int[8]: MMA's item lengths
-constexpr int kOffBars = kOffNkv + 8 * 4;
+constexpr int kOffBars = kOffDesc + 2 * 64;
 // q_full q_empty desc_full[2] desc_empty[2] k_full[2] k_empty[2] v_full[2]
 // v_empty[2] s_full[2] s_free[2] p_full[2] pv_done[2] o_free[2] mma_done
 // pair[4]
@@ -139,7 +141,7 @@ __device__ __forceinline__ int item_index(int r) {
   return r * P + ((r & 1) ? (P - 1 - k) : k);
 }
 
-// 11 warps: 3 on three of the four SM sub-partitions, so at most 168
+// 12 warps: 3 on each of the four SM sub-partitions, so at most 168
 // registers a thread.
 __global__ void __launch_bounds__(kThreads, 1)
     varlen_prefill_kernel(const __grid_constant__ CUtensorMap qmap,
@@ -169,7 +171,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   Misc* misc = reinterpret_cast<Misc*>(smem + kOffMisc);
   ItemDesc* desc = reinterpret_cast<ItemDesc*>(smem + kOffDesc);
   int* pairs = reinterpret_cast<int*>(smem + kOffPairs);
-  int* nkv_ring = reinterpret_cast<int*>(smem + kOffNkv);
   volatile int* abort_flag = &misc->abort;
   const uint32_t sbase = smem_u32(smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -263,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(q_empty, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&desc_full[s], 1);
-      mbar_init(&desc_empty[s], 1 + kSoftmaxWarps);  // the MMA thread, the softmax warps
+      mbar_init(&desc_empty[s], 2 + kSoftmaxWarps);  // the two MMA threads, the softmax warps
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
       mbar_init(&v_full[s], 1);
@@ -274,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&pv_done[s], 1);
       mbar_init(&o_free[s], kSoftmaxWarps);
     }
-    mbar_init(mma_done, 1);
+    mbar_init(mma_done, 2);
     for (int q = 0; q < 4; ++q) mbar_init(&pair[q], 2);
     fence_barrier_init();
   }
@@ -410,55 +411,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (*abort_flag) set_err(a.err_word, QATTN_DEVERR_TIMEOUT);
     }
     __syncwarp();
-  } else if (warp == kMmaWarp) {
-    // ============================== MMA issuer ===============================
+  } else if (warp == kMmaWarp || warp == kPvWarp) {
+    // ============================= MMA issuers ===============================
+    // Warp 9 issues the Q K^T stream and warp 11 the P V stream: a thread
+    // issuing tcgen05.mma waits for the tensor pipe to take each one (~85
+    // cycles for 128 x 128 x 16), so with one issuer a ready Q K^T waited
+    // behind a tile's P V and the other way round.  The streams share no
+    // tensor memory (S vs O) and each thread's commits track its own MMAs.
     if (lane == 0) {
-      constexpr uint32_t idesc_qk = idesc_bf16_f32(kM, kN, false);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(kM, kHeadDim, true);
-      const uint32_t sq = sbase + kOffQ;
-      // Q K^T and P V are each issued in order, whichever is ready first
-      // (readiness probed without blocking).
-      int qr = 0, qkt = 0, q_nkv = 0;  // Q K^T stream: item, its tile, its length
-      int pr = 0, pkt = 0;             // P V stream
-      int qn = 0, pn = 0;              // KV tiles of each stream so far
       bool ok = true;
       uint64_t idle_since = 0;
-      while (pr < nitems && ok) {
-        bool progressed = false;
-        if (pn < qn) {
-          const bool first = pkt == 0;
-          bool ready = mbar_test(&p_full[pn & 1], (pn >> 1) & 1) &&
-                       mbar_test(&v_full[pn & 1], (pn >> 1) & 1);
-          // an item's first P V overwrites O slot pr & 1, last read for item pr - 2
-          if (ready && first && pr >= 2) ready = mbar_test(&o_free[pr & 1], ((pr >> 1) - 1) & 1);
-          if (ready) {
-            tc_fence_after();
-            const uint32_t sv = sbase + kOffV + (pn & 1) * kTileBytes;
-            const uint32_t sp_ = sbase + kOffP + (pn & 1) * kTileBytes;
-#pragma unroll
-            for (int k = 0; k < kN / 16; ++k) {
-              const uint64_t ad =
-                  sdesc_sw128(sp_ + (k >> 2) * kHalfBytes + (k & 3) * 32, 16, 1024);
-              // V tile as the MN-major B: dim halves 1 KB apart (LBO), 8-key
-              // groups 2 KB apart (SBO); K step k = keys 16k..16k+15.
-              const uint64_t bd = sdesc_sw128(sv + k * 4096, 1024, 2048);
-              mma_bf16_ss(tmem + kColO + (pr & 1) * kHeadDim, ad, bd, idesc_pv,
-                          (first && k == 0) ? 0u : 1u);
-            }
-            mma_commit(&pv_done[pn & 1]);
-            mma_commit(&v_empty[pn & 1]);
-            ++pn;
-            if (++pkt == nkv_ring[pr & 7]) {
-              pkt = 0;
-              ++pr;
-            }
-            progressed = true;
+      // No progress for kWaitTimeoutNs (or the abort flag): give up.
+      auto idle = [&](bool progressed) {
+        if (progressed) {
+          idle_since = 0;
+        } else {
+          const uint64_t now = globaltimer_ns();
+          if (idle_since == 0) {
+            idle_since = now;
+          } else if (*abort_flag || now - idle_since > kWaitTimeoutNs) {
+            *abort_flag = 1;
+            ok = false;
           }
         }
-        if (qr < nitems) {
+      };
+      if (warp == kMmaWarp) {
+        constexpr uint32_t idesc_qk = idesc_bf16_f32(kM, kN, false);
+        const uint32_t sq = sbase + kOffQ;
+        int qr = 0, qkt = 0, q_nkv = 0;  // item, its tile, its length
+        int qn = 0;                      // KV tiles so far
+        while (qr < nitems && ok) {
+          bool progressed = false;
           if (q_nkv == 0 && mbar_test(&desc_full[qr & 1], (qr >> 1) & 1)) {
             q_nkv = desc[qr & 1].nkv;
-            nkv_ring[qr & 7] = q_nkv;
             mbar_arrive(&desc_empty[qr & 1]);
             progressed = true;
           }
@@ -466,8 +451,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ready = mbar_test(&k_full[qn & 1], (qn >> 1) & 1);
             if (ready && qn >= 2) ready = mbar_test(&s_free[qn & 1], ((qn >> 1) & 1) ^ 1);
             if (ready && qkt == 0) ready = mbar_test(q_full, qr & 1);
-            // (the P V stream must not fall more than 8 items behind: nkv_ring)
-            if (ready && qr - pr >= 7) ready = false;
             if (ready) {
               tc_fence_after();
               const uint32_t sk = sbase + kOffK + (qn & 1) * kTileBytes;
@@ -491,20 +474,54 @@ __global__ void __launch_bounds__(kThreads, 1)
               progressed = true;
             }
           }
+          idle(progressed);
         }
-        if (progressed) {
-          idle_since = 0;
-        } else {
-          const uint64_t now = globaltimer_ns();
-          if (idle_since == 0) {
-            idle_since = now;
-          } else if (*abort_flag || now - idle_since > kWaitTimeoutNs) {
-            *abort_flag = 1;
-            ok = false;
+      } else {
+        constexpr uint32_t idesc_pv = idesc_bf16_f32(kM, kHeadDim, true);
+        int pr = 0, pkt = 0, p_nkv = 0;  // item, its tile, its length
+        int pn = 0;                      // KV tiles so far
+        while (pr < nitems && ok) {
+          bool progressed = false;
+          if (p_nkv == 0 && mbar_test(&desc_full[pr & 1], (pr >> 1) & 1)) {
+            p_nkv = desc[pr & 1].nkv;
+            mbar_arrive(&desc_empty[pr & 1]);
+            progressed = true;
           }
+          if (p_nkv > 0) {
+            const bool first = pkt == 0;
+            bool ready = mbar_test(&p_full[pn & 1], (pn >> 1) & 1) &&
+                         mbar_test(&v_full[pn & 1], (pn >> 1) & 1);
+            // an item's first P V overwrites O slot pr & 1, last read for item pr - 2
+            if (ready && first && pr >= 2) ready = mbar_test(&o_free[pr & 1], ((pr >> 1) - 1) & 1);
+            if (ready) {
+              tc_fence_after();
+              const uint32_t sv = sbase + kOffV + (pn & 1) * kTileBytes;
+              const uint32_t sp_ = sbase + kOffP + (pn & 1) * kTileBytes;
+#pragma unroll
+              for (int k = 0; k < kN / 16; ++k) {
+                const uint64_t ad =
+                    sdesc_sw128(sp_ + (k >> 2) * kHalfBytes + (k & 3) * 32, 16, 1024);
+                // V tile as the MN-major B: dim halves 1 KB apart (LBO), 8-key
+                // groups 2 KB apart (SBO); K step k = keys 16k..16k+15.
+                const uint64_t bd = sdesc_sw128(sv + k * 4096, 1024, 2048);
+                mma_bf16_ss(tmem + kColO + (pr & 1) * kHeadDim, ad, bd, idesc_pv,
+                            (first && k == 0) ? 0u : 1u);
+              }
+              mma_commit(&pv_done[pn & 1]);
+              mma_commit(&v_empty[pn & 1]);
+              ++pn;
+              if (++pkt == p_nkv) {
+                pkt = 0;
+                p_nkv = 0;
+                ++pr;
+              }
+              progressed = true;
+            }
+          }
+          idle(progressed);
         }
       }
-      // Drain: every MMA issued above completes before TMEM is released.
+      // Drain: every MMA of both threads completes before TMEM is released.
       mma_commit(mma_done);
       mbar_wait_drain(mma_done, 0);
     }
