@@ -30,7 +30,8 @@
 //     grid to finish; K2r's CTAs launch early and wait on the grid).
 //   * warp 4 issues TMA: Q^T of a unit (a G x 128 box of the query rows),
 //     K and V tiles (16 x 64 boxes, 128-byte swizzle) into 3-deep K and V
-//     rings; warp 5 (one thread) issues tcgen05.mma and commits; warps 0-3
+//     rings; one thread of warp 5 issues the Q K^T MMAs and one of warp 6
+//     the P V MMAs (two issuers: each MMA issue waits on the pipe); warps 0-3
 //     (thread = token for S, thread = dimension for O) run the softmax and
 //     write P^T as bf16 into swizzled shared memory.
 //   * O is rescaled lazily (only when a head's max grows by more than 2^8).
@@ -41,7 +42,7 @@
 // FP8 cache (kFp8; kv_cache_dtype "fp8", fp8_e4m3fn codes with a cache
 // scale per tensor, "Qwen2大模型架构解析与vLLM优化实践" sections 4.1, 4.2,
 // 6.3): the cache tiles are half the bytes (128 B per token row) and land
-// by TMA in 4-deep 16 KB rings; four more warps (6-9, thread = token row)
+// by TMA in 4-deep 16 KB rings; four more warps (7-10, thread = token row)
 // dequantise them -- the e4m3 -> f16 conversion is exact -- K into tensor
 // memory (the A operand of S^T = K . Q^T is read from TMEM, so the converted
 // K never touches shared memory) and V into the same swizzled MN-major f16
@@ -60,8 +61,9 @@ namespace {
 constexpr int kTile = kTcTileTokens;  // 128 tokens
 constexpr int kN = 16;                // MMA N: the query group padded to 16 heads
 constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr int kConvWarp0 = 6;   // FP8 only: warps 6-9 dequantise
+constexpr int kMmaWarp = 5;     // issues the Q K^T stream (and owns TMEM)
+constexpr int kPvWarp = 6;      // issues the P V stream
+constexpr int kConvWarp0 = 7;   // FP8 only: warps 7-10 dequantise
 // A tile of 128 tokens lands as 8-token row groups 2 KB apart whatever the
 // block size (a block's box is block_size / 8 such groups), so the code below
 // addresses it in 16-token / 4 KB units.
@@ -78,7 +80,7 @@ constexpr int kMaxSmemSeqs = 2048;
 // 4 + 4 slots of 16 KB code tiles, then two 32 KB f16 V tiles.
 template <bool kFp8>
 struct Lay {
-  static constexpr int kWarps = kFp8 ? 10 : 6;
+  static constexpr int kWarps = kFp8 ? 11 : 7;
   static constexpr int kThreads = kWarps * 32;
   static constexpr int kKStages = kFp8 ? 4 : 3;
   static constexpr int kVStages = kFp8 ? 4 : 3;
@@ -108,7 +110,7 @@ struct Misc {
   int abort;
   int b0;
   int off0;
-  int warp_sums[10];
+  int warp_sums[12];
 };
 
 __device__ __forceinline__ int seq_len_eff(const DecodeArgs& a, int b) {
@@ -305,7 +307,7 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
     mbar_init(&o_free[0], 4);
     mbar_init(&o_free[1], 4);
     mbar_init(rbar, 4);
-    mbar_init(mma_done, 1);
+    mbar_init(mma_done, 2);  // one commit per MMA-issuing thread
     fence_barrier_init();
   }
   for (int i = tid; i < 4 * kSmallBytes / 16; i += kThreads)
@@ -456,26 +458,41 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
       if (*abort_flag) set_err(a.err_word, QATTN_DEVERR_TIMEOUT);
     }
     __syncwarp();
-  } else if (warp == kMmaWarp) {
-    // ============================== MMA issuer ===============================
+  } else if (warp == kMmaWarp || warp == kPvWarp) {
+    // ============================= MMA issuers ===============================
+    // Warp 5 issues Q K^T(n) as soon as K(n) is in and S buffer n & 1 is
+    // free; warp 6 issues P V(j) as soon as P(j) and V(j) are in (it frees
+    // V's ring slot, the resource the producer waits on longest).  A thread
+    // issuing tcgen05.mma waits for the pipe to take each instruction (~90
+    // cycles even at N = 16, measured), so with one issuer each stream
+    // waited behind the other's eight MMAs.  The streams share no tensor
+    // memory (S vs O^T) and each thread's commits track its own MMAs.
     if (lane == 0) {
       constexpr uint32_t idesc_qk = kFp8 ? idesc_f16_f32(kTile, kN, false, false)
                                          : idesc_bf16_f32(kTile, kN, false, false);
       constexpr uint32_t idesc_pv = kFp8 ? idesc_f16_f32(kHeadDim, kN, false, true)
                                          : idesc_bf16_f32(kHeadDim, kN, false, true);
-      // QK and PV are each issued in tile order, but whichever is ready goes
-      // first: PV(j) as soon as P(j) and V(j) are in (it frees V's ring
-      // slot, the resource the producer waits on longest), QK(n) as soon as
-      // K(n) is in and S buffer n & 1 is free.  Readiness is probed without
-      // blocking; waiting on one condition while the other is ready used to
-      // hold V slots for a K load.
       bool ok = true;
-      Walk qw = w0, pw = w0;
-      int qn = 0, pn = 0, qseg = -1, pseg = -1;
       uint64_t idle_since = 0;
-      while (pn < nloc && ok) {
-        bool progressed = false;
-        if (pn < qn) {
+      // No progress for kWaitTimeoutNs (or the abort flag): give up.
+      auto idle = [&](bool progressed) {
+        if (progressed) {
+          idle_since = 0;
+        } else {
+          const uint64_t now = globaltimer_ns();
+          if (idle_since == 0) {
+            idle_since = now;
+          } else if (*abort_flag || now - idle_since > kWaitTimeoutNs) {
+            *abort_flag = 1;
+            ok = false;
+          }
+        }
+      };
+      if (warp == kPvWarp) {
+        Walk pw = w0;
+        int pn = 0, pseg = -1;
+        while (pn < nloc && ok) {
+          bool progressed = false;
           const bool first = (pn == 0) || (pw.i == 0);
           const int seg_j = pseg + (first ? 1 : 0);
           const int pb = pn & 1;
@@ -509,8 +526,13 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
             walk_next(pw, a, s_len);
             progressed = true;
           }
+          idle(progressed);
         }
-        if (qn < nloc) {
+      } else {
+        Walk qw = w0;
+        int qn = 0, qseg = -1;
+        while (qn < nloc && ok) {
+          bool progressed = false;
           const bool first = (qn == 0) || (qw.i == 0);
           const bool last = (qn == nloc - 1) || (qw.i == qw.nt - 1);
           const int seg_q = qseg + (first ? 1 : 0);
@@ -547,20 +569,10 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
             walk_next(qw, a, s_len);
             progressed = true;
           }
-        }
-        if (progressed) {
-          idle_since = 0;
-        } else {
-          const uint64_t now = globaltimer_ns();
-          if (idle_since == 0) {
-            idle_since = now;
-          } else if (*abort_flag || now - idle_since > kWaitTimeoutNs) {
-            *abort_flag = 1;
-            ok = false;
-          }
+          idle(progressed);
         }
       }
-      // Drain: every MMA issued above completes before TMEM is released.
+      // Drain: every MMA of both threads completes before TMEM is released.
       mma_commit(mma_done);
       mbar_wait_drain(mma_done, 0);
     }
