@@ -190,7 +190,7 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
                            const __grid_constant__ CUtensorMap qmap, const DecodeArgs a) {
   using L = Lay<kFp8>;
   constexpr int kThreads = L::kThreads;
-  // The FP8 kernel (ten warps in five roles) is instruction-cache bound:
+  // The FP8 kernel (eleven warps in six roles) is instruction-cache bound:
   // its MMA loops are unrolled by 2 only (measured faster; bf16 keeps 8).
   constexpr int kMmaUnroll = kFp8 ? 2 : 8;
   constexpr int kKStages = L::kKStages;
@@ -613,7 +613,7 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
       tc_fence_after();
       const uint32_t src = sbase + L::kOffK + ks * L::kStageBytes + row * 128;
       const uint32_t dst = k_lane + kColK + (n & 1) * 64;
-      // (not unrolled: with ten warps in five roles the kernel's code is
+      // (not unrolled: with eleven warps in six roles the kernel's code is
       // instruction-cache bound -- unrolling these loops measured slower)
 #pragma unroll 1
       for (int c = 0; c < 8; ++c) {
