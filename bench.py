@@ -53,6 +53,9 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-clocks", action="store_true")
+    p.add_argument("--append-sweep", action="store_true",
+                   help="supplementary: time RoPE + append alone at 16k and 64k new tokens "
+                        "(Qwen2-7B heads), one JSON line per size")
     p.add_argument("--block-size", type=int, choices=[16, 32, 64], default=16,
                    help="cache block size of the decode / mixed workloads")
     p.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
@@ -609,6 +612,51 @@ def cpu_baseline(w: W.Workload, kv_bytes_full: int, budget_s: float = 10.0):
                       f"x {reps} repetitions, append + attention in fp64, {total:.1f} s"}
 
 
+def run_append_sweep(args):
+    """K1 alone at sizes where bandwidth is meaningful (the decode step's
+    64-token append is launch-bound): T new tokens in sequences of 16384,
+    28/4 heads, L2 flushed before every timed launch."""
+    from paged_kv_gqa_07_gb300 import build as B
+    from paged_kv_gqa_07_gb300 import qattn as Q
+    B.build()
+    Q.load_library()
+    dev = torch.device("cuda", 0)
+    hbm_peak, _, peak_kind = measured_peaks()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for T in (16384, 65536):
+        n = T // 16384  # sequences of 16384 new tokens (positions stay below max_pos)
+        w = W.custom(28, 4, ctx=[16384] * n, q_lens=[16384] * n, seed=T)
+        g = W.to_device(w, dev)
+        dims = Q.make_dims(28, 4)
+        table = Q.qattn_rope_table_build(w.max_pos, 128, w.theta).to(dev)
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+        qkv0 = g.qkv.clone()
+
+        def append():
+            Q.qattn_rope_cache_append(g.q_view(), g.k_view(), g.v_view(), g.positions,
+                                      g.slot_mapping, g.k_cache, g.v_cache, table, dims, err)
+        for _ in range(args.warmup):
+            append()
+        ms = []
+        for i in range(args.steps):
+            g.qkv.copy_(qkv0)
+            flush.fill_(i & 0xff)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            append()
+            e1.record()
+            torch.cuda.synchronize(dev)
+            ms.append(e0.elapsed_time(e1))
+        assert int(err.item()) == 0
+        t = statistics.median(ms) * 1e-3
+        alg = T * 18944  # read q/k/v + a table row, write q and the cache rows
+        print(json.dumps({"metric": "rope + cache append GB/s (supplementary)", "tokens": T,
+                          "value": round(alg / t / 1e9, 1), "unit": "GB/s",
+                          "us": round(t * 1e6, 2), "algorithmic_bytes": alg,
+                          "frac": round(alg / t / 1e9 / hbm_peak, 4), "peak_kind": peak_kind,
+                          "l2": "flushed before every timed launch"}), flush=True)
+
+
 def run_reference(args, dist: Dist):
     import oracle
     w = W.build(args.workload, block_size=args.block_size)
@@ -643,6 +691,9 @@ def run_reference(args, dist: Dist):
 
 def main():
     args = parse()
+    if args.append_sweep:
+        run_append_sweep(args)
+        return
     if args.impl == "reference":
         # The reference arm is the CPU oracle: rank 0 alone runs it.
         if int(os.environ.get("RANK", "0")) == 0:
