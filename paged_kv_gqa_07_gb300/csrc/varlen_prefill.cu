@@ -586,24 +586,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (valid && hf == 0) a.ws.lse[pidx * G + j] = pd.m + log2f(l);
       } else {
-        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) +
-                              ((pd.row0 + t) * H + pd.h) * kHeadDim + 64 * hf;
+        // The bf16 half-rows go through this warp's 4 KB of the P buffer
+        // that P V(pd.n) has released (the rows it writes P into; swizzled
+        // like P), then out four whole 128-byte half-rows per store
+        // instruction: written straight from the TMEM lanes, every store
+        // touched 32 rows 7 KB apart.
+        const uint32_t stage =
+            sbase + kOffP + (pd.n & 1) * kTileBytes + hf * kHalfBytes + q4 * 32 * 128;
 #pragma unroll 1
         for (int c4 = 0; c4 < 2; ++c4) {
           float o[32];
           tmem_ld32(lane_addr + col + c4 * 32, o);
-          if (valid) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              uint4 v;
-              v.x = pack_bf16x2_rn(o[q * 8 + 0] * inv, o[q * 8 + 1] * inv);
-              v.y = pack_bf16x2_rn(o[q * 8 + 2] * inv, o[q * 8 + 3] * inv);
-              v.z = pack_bf16x2_rn(o[q * 8 + 4] * inv, o[q * 8 + 5] * inv);
-              v.w = pack_bf16x2_rn(o[q * 8 + 6] * inv, o[q * 8 + 7] * inv);
-              *reinterpret_cast<uint4*>(orow + c4 * 32 + q * 8) = v;
-            }
-          }
+          for (int q = 0; q < 4; ++q)
+            sts128(stage + lane * 128 + (((c4 * 4 + q) ^ (lane & 7)) << 4),
+                   pack_bf16x2_rn(o[q * 8 + 0] * inv, o[q * 8 + 1] * inv),
+                   pack_bf16x2_rn(o[q * 8 + 2] * inv, o[q * 8 + 3] * inv),
+                   pack_bf16x2_rn(o[q * 8 + 4] * inv, o[q * 8 + 5] * inv),
+                   pack_bf16x2_rn(o[q * 8 + 6] * inv, o[q * 8 + 7] * inv));
         }
+        __syncwarp();
+        const int cc = lane & 7;
+#pragma unroll 4
+        for (int i = 0; i < 8; ++i) {
+          const int rr = i * 4 + (lane >> 3);  // row q4 * 32 + rr of the tile
+          const uint4 v = lds128(stage + rr * 128 + ((cc ^ (rr & 7)) << 4));
+          if (q4 * 32 + rr < pd.rows)
+            *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) +
+                                      ((pd.row0 + q4 * 32 + rr) * H + pd.h) * kHeadDim +
+                                      64 * hf + cc * 8) = v;
+        }
+        __syncwarp();  // the staging rows are P rows again from here
       }
       tc_fence_before();
       __syncwarp();
