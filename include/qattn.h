@@ -23,7 +23,11 @@
  * Conventions for every entry point:
  *   - All tensor pointers are DEVICE pointers unless the argument says host.
  *     The caller owns every buffer; the library allocates no device memory
- *     and keeps no state between calls.
+ *     and keeps no device state between calls.
+ *   - Any entry point may be called from several host threads, and for any
+ *     device (the current device of the calling thread): the host-side
+ *     caches (SM counts, encoded tensor maps, the kernels' shared-memory
+ *     limits, set once per device) are lock-protected.
  *   - bf16 everywhere for activations and cache; int32 for every index.
  *   - Cache layout: k_cache and v_cache are [num_blocks][num_kv_heads]
  *     [block_size][head_dim] bf16, contiguous.  Token slot s lives in block

@@ -6,6 +6,8 @@
 #include <string.h>
 
 #include <mutex>
+#include <utility>
+#include <vector>
 
 #include "common.cuh"
 #include "internal.h"
@@ -53,12 +55,9 @@ int num_sms_current() {
 
 // ------------------------------------------------------------ tensor maps --
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+}  // namespace
 
-EncodeTiledFn encode_fn() {
+EncodeTiledFn qattn::encode_fn() {
   static std::once_flag once;
   static EncodeTiledFn fn = nullptr;
   std::call_once(once, [] {
@@ -71,6 +70,22 @@ EncodeTiledFn encode_fn() {
   });
   return fn;
 }
+
+cudaError_t qattn::set_max_dynamic_smem(const void* kernel, int bytes) {
+  static std::mutex mu;
+  static std::vector<std::pair<const void*, int>> done;  // (kernel, device)
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(mu);
+  for (const auto& d : done)
+    if (d.first == kernel && d.second == dev) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.emplace_back(kernel, dev);
+  return e;
+}
+
+namespace {
 
 // The paged cache [num_blocks][Hkv][BS][128] bf16 (BS = block size) seen as a
 // 4-D tensor (64 columns, 8 rows, 2 column halves, num_blocks * Hkv * BS / 8

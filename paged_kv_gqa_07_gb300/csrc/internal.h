@@ -14,6 +14,19 @@
 
 namespace qattn {
 
+// Raises a kernel's dynamic shared memory limit to `bytes` on the current
+// device, once per (kernel, device): the attribute belongs to the device's
+// context, so a process driving several GPUs sets it on each.  Thread-safe.
+cudaError_t set_max_dynamic_smem(const void* kernel, int bytes);
+
+// cuTensorMapEncodeTiled from the driver, looked up once (nullptr if the
+// driver lacks it).  Thread-safe.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_fn();
+
 // Launch with programmatic stream serialization (see grid_dep_wait).
 template <typename... Params, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,

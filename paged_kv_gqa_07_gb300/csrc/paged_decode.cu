@@ -686,15 +686,10 @@ cudaError_t launch_merge_g(const DecodeArgs& a, cudaStream_t stream) {
 template <int G>
 cudaError_t launch_g(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                      int num_sms, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<G>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
   cudaError_t e =
-      launch_pdl(paged_decode_kernel<G>, dim3(num_sms), dim3(kThreads), kSmemBytes, stream, kmap,
+      set_max_dynamic_smem(reinterpret_cast<const void*>(paged_decode_kernel<G>), kSmemBytes);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(paged_decode_kernel<G>, dim3(num_sms), dim3(kThreads), kSmemBytes, stream, kmap,
                  vmap, a);
   if (e != cudaSuccess) return e;
   e = cudaPeekAtLastError();

@@ -973,15 +973,10 @@ template <int G, bool kFp8>
 cudaError_t launch_tc_gf(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                          const CUtensorMap& qmap, int num_sms, cudaStream_t stream) {
   using L = Lay<kFp8>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(paged_decode_tc_kernel<G, kFp8>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         L::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  cudaError_t e = launch_pdl(paged_decode_tc_kernel<G, kFp8>, dim3(num_sms), dim3(L::kThreads),
+  cudaError_t e = set_max_dynamic_smem(
+      reinterpret_cast<const void*>(paged_decode_tc_kernel<G, kFp8>), L::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(paged_decode_tc_kernel<G, kFp8>, dim3(num_sms), dim3(L::kThreads),
                              L::kSmemBytes, stream, kmap, vmap, qmap, a);
   if (e != cudaSuccess) return e;
   e = cudaPeekAtLastError();

@@ -798,21 +798,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // head's 128-row tile), 128-byte swizzled.
 bool encode_q_map(CUtensorMap* map, const void* q, int64_t q_row_stride, int total_q,
                   int num_heads) {
-  using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                     const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                     const cuuint32_t*, CUtensorMapInterleave,
-                                     CUtensorMapSwizzle, CUtensorMapL2promotion,
-                                     CUtensorMapFloatOOBfill);
-  static EncodeTiledFn fn = nullptr;
-  if (fn == nullptr) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult qr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &qr) != cudaSuccess ||
-        qr != cudaDriverEntryPointSuccess)
-      return false;
-    fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
+  const EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(num_heads) * kHeadDim,
                               static_cast<cuuint64_t>(total_q)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(q_row_stride) * 2};
@@ -827,14 +814,7 @@ bool encode_q_map(CUtensorMap* map, const void* q, int64_t q_row_stride, int tot
 
 namespace {
 cudaError_t set_smem_attr() {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(varlen_prefill_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  return cudaSuccess;
+  return set_max_dynamic_smem(reinterpret_cast<const void*>(varlen_prefill_kernel), kSmemBytes);
 }
 }  // namespace
 
