@@ -2,9 +2,11 @@
 
 Each function has the name of the C entry point it calls and forwards
 ``tensor.data_ptr()``, row strides and the current CUDA stream; all work runs
-in the library's CUDA kernels.  A non-zero return code raises
-:class:`QattnError`.  There is no fallback: if the library is missing the
-first call raises.
+in the library's CUDA kernels.  Since the C ABI sees only pointers, each
+tensor's device, dtype, shape and layout are first checked against the call's
+dims (:class:`QattnArgError`, status QATTN_ERR_INVALID_ARG, if they disagree).
+A non-zero return code raises :class:`QattnError`.  There is no fallback: if
+the library is missing the first call raises.
 """
 from __future__ import annotations
 
@@ -60,6 +62,16 @@ class QattnError(RuntimeError):
     def __init__(self, fn: str, status: int):
         self.status = status
         super().__init__(f"{fn} returned {status} ({qattn_status_string(status)})")
+
+
+class QattnArgError(QattnError, ValueError):
+    """A tensor the binding refuses before calling the library (status
+    QATTN_ERR_INVALID_ARG): its device, dtype, shape or layout disagrees with
+    what the C ABI assumes of the pointer it would pass."""
+
+    def __init__(self, fn: str, detail: str):
+        self.status = QATTN_ERR_INVALID_ARG
+        RuntimeError.__init__(self, f"{fn}: {detail}")
 
 
 class qattn_dims(ctypes.Structure):
@@ -135,6 +147,9 @@ def load_library(path: str | None = None):
             _P, _P, _I64, _P, _P, _I32, _P, _I32, _P, _I32, _I32, _I32, ctypes.c_float,
             ctypes.c_float, qattn_dims, _P, _SZ, _P, _P]
         L.qattn_paged_decode_shared_prefix_fp8.restype = ctypes.c_int
+        L.qattn_paged_decode_noalloc.argtypes = [
+            _P, _P, _I64, _P, _P, _I32, _P, _I32, _P, _I32, _I32, qattn_dims, _P, _P]
+        L.qattn_paged_decode_noalloc.restype = ctypes.c_int
         L.qattn_varlen_prefill_workspace_size.argtypes = [_I32, _I32, qattn_dims]
         L.qattn_varlen_prefill_workspace_size.restype = _SZ
         L.qattn_varlen_prefill.argtypes = [
@@ -157,22 +172,106 @@ def lib():
 
 
 # ---------------------------------------------------------------- helpers --
+#
+# The C ABI sees plain pointers.  The layouts it assumes of them (include/
+# qattn.h) are checked here, where the tensors' metadata is still at hand, so
+# that a tensor of the wrong shape, dtype, layout or device is refused instead
+# of being read or written out of bounds on the device.
 
-def _dev_ptr(t: torch.Tensor | None, name: str, dtype=None):
-    if t is None:
-        return None
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
-    if dtype is not None and t.dtype != dtype:
-        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
-    return t.data_ptr()
+_BF16 = (torch.bfloat16,)
+_I32T = (torch.int32,)
+_F32 = (torch.float32,)
+_E4M3 = (torch.uint8, torch.float8_e4m3fn)
 
 
-def _rows(t: torch.Tensor, name: str):
-    """(pointer, row stride in elements) of a 2-D bf16 view with unit inner stride."""
-    if t.dim() != 2 or t.stride(1) != 1:
-        raise ValueError(f"{name} must be a 2-D view with unit inner stride")
-    return _dev_ptr(t, name, torch.bfloat16), t.stride(0)
+class _Args:
+    """The tensors of one call: checked, then reduced to device pointers."""
+
+    def __init__(self, fn: str, dims=None):
+        self.fn = fn
+        self.dims = dims
+        self.dev = None  # the current device, looked up at the first tensor
+
+    def bad(self, detail: str):
+        raise QattnArgError(self.fn, detail)
+
+    def ptr(self, t, name, dtypes=None, numel=0, contiguous=True):
+        """Device pointer of `t` (None stays None): of one of `dtypes`,
+        contiguous unless told otherwise, >= numel elements, on the current
+        device."""
+        if t is None:
+            return None
+        if dtypes is not None and t.dtype not in dtypes:
+            self.bad(f"{name} must be {' or '.join(str(d) for d in dtypes)}, got {t.dtype}")
+        if contiguous and not t.is_contiguous():
+            self.bad(f"{name} must be contiguous")
+        if numel and t.numel() < numel:
+            self.bad(f"{name} has {t.numel()} elements, needs at least {numel}")
+        return self.device_ptr(t, name)
+
+    def device_ptr(self, t, name):
+        if not t.is_cuda:
+            self.bad(f"{name} must be a CUDA tensor, got {t.device}")
+        if self.dev is None:
+            self.dev = torch.cuda.current_device()
+        if t.device.index != self.dev:
+            self.bad(f"{name} is on {t.device}, not on the current device cuda:{self.dev}")
+        return t.data_ptr()
+
+    def rows(self, t, name, rows, cols):
+        """(pointer, row stride in elements) of a bf16 row view: 2-D with unit
+        inner stride, at least `rows` rows of at least `cols` elements."""
+        if t.dim() != 2 or t.stride(1) != 1:
+            self.bad(f"{name} must be a 2-D view with unit inner stride")
+        if t.shape[0] < rows or t.shape[1] < cols:
+            self.bad(f"{name} is {tuple(t.shape)}, needs at least {rows} rows of {cols}")
+        return self.ptr(t, name, _BF16, contiguous=False), t.stride(0)
+
+    def vec(self, t, name, n=0):
+        """A contiguous 1-D int32 vector of at least n entries."""
+        if t.dim() != 1:
+            self.bad(f"{name} must be 1-D, got shape {tuple(t.shape)}")
+        return self.ptr(t, name, _I32T, numel=n)
+
+    def cache(self, k, v, fp8=False):
+        """K and V caches: contiguous [num_blocks, Hkv, block_size, head_dim]
+        (bf16, or e4m3 codes); returns their pointers and num_blocks."""
+        d = self.dims
+        want = (d.num_kv_heads, d.block_size, d.head_dim)
+        for t, name in ((k, "k_cache"), (v, "v_cache")):
+            if t.dim() != 4 or tuple(t.shape[1:]) != want:
+                self.bad(f"{name} is {tuple(t.shape)}, must be [num_blocks, {want[0]}, "
+                         f"{want[1]}, {want[2]}]")
+        if k.shape[0] != v.shape[0]:
+            self.bad("k_cache and v_cache must hold the same number of blocks")
+        dt = _E4M3 if fp8 else _BF16
+        return self.ptr(k, "k_cache", dt), self.ptr(v, "v_cache", dt), int(k.shape[0])
+
+    def table(self, bt, num_seqs):
+        """Block tables: contiguous int32 [>= num_seqs, max_blocks_per_seq]."""
+        if bt.dim() != 2 or bt.shape[0] < num_seqs:
+            self.bad(f"block_tables is {tuple(bt.shape)}, needs [>= {num_seqs}, "
+                     "max_blocks_per_seq]")
+        return self.ptr(bt, "block_tables", _I32T), int(bt.shape[1])
+
+    def out(self, t, rows):
+        """Output rows: contiguous bf16 [rows, num_heads, head_dim]."""
+        d = self.dims
+        return self.ptr(t, "out", _BF16, numel=rows * d.num_heads * d.head_dim)
+
+    def workspace(self, t):
+        """(pointer, bytes) of a contiguous workspace of any dtype."""
+        return self.ptr(t, "workspace"), int(t.numel() * t.element_size())
+
+    def err(self, t):
+        return self.ptr(t, "err_word", _I32T, numel=1)
+
+    def cos_sin(self, t):
+        """The cos/sin table: contiguous fp32 [max_pos, head_dim]; returns
+        its pointer and max_pos."""
+        if t.dim() != 2 or t.shape[1] != self.dims.head_dim:
+            self.bad(f"cos_sin is {tuple(t.shape)}, must be [max_pos, {self.dims.head_dim}]")
+        return self.ptr(t, "cos_sin", _F32), int(t.shape[0])
 
 
 def _stream(stream):
@@ -219,18 +318,33 @@ def qattn_rope_table_build_scaled(max_pos: int, head_dim: int, theta: float, sca
     return out
 
 
+def _append_args(a: _Args, q, k, v, positions, slot_mapping, k_cache, v_cache, cos_sin, fp8,
+                 qkv_bias=None, q_norm_weight=None, k_norm_weight=None):
+    """The argument list shared by the three append entry points, up to the
+    optional extras: q/k/v rows, positions, slots, caches and the table."""
+    d = a.dims
+    pos = a.vec(positions, "positions")
+    T = int(positions.shape[0])
+    qp, qs = a.rows(q, "q", T, d.num_heads * d.head_dim)
+    kp, ks = a.rows(k, "k", T, d.num_kv_heads * d.head_dim)
+    vp, vs = a.rows(v, "v", T, d.num_kv_heads * d.head_dim)
+    slots = a.vec(slot_mapping, "slot_mapping", T)
+    kc, vc, nb = a.cache(k_cache, v_cache, fp8)
+    cs, max_pos = a.cos_sin(cos_sin)
+    args = [qp, qs, kp, ks, vp, vs, pos, slots, T, kc, vc, nb, cs, max_pos]
+    extras = [a.ptr(qkv_bias, "qkv_bias", _BF16,
+                    numel=(d.num_heads + 2 * d.num_kv_heads) * d.head_dim),
+              a.ptr(q_norm_weight, "q_norm_weight", _BF16, numel=d.head_dim),
+              a.ptr(k_norm_weight, "k_norm_weight", _BF16, numel=d.head_dim)]
+    return args, extras
+
+
 def qattn_rope_cache_append(q, k, v, positions, slot_mapping, k_cache, v_cache, cos_sin, dims,
                             err_word=None, stream=None):
-    qp, qs = _rows(q, "q")
-    kp, ks = _rows(k, "k")
-    vp, vs = _rows(v, "v")
-    rc = lib().qattn_rope_cache_append(
-        qp, qs, kp, ks, vp, vs, _dev_ptr(positions, "positions", torch.int32),
-        _dev_ptr(slot_mapping, "slot_mapping", torch.int32), int(positions.shape[0]),
-        _dev_ptr(k_cache, "k_cache", torch.bfloat16), _dev_ptr(v_cache, "v_cache", torch.bfloat16),
-        int(k_cache.shape[0]), _dev_ptr(cos_sin, "cos_sin", torch.float32), int(cos_sin.shape[0]),
-        dims, _dev_ptr(err_word, "err_word", torch.int32), _stream(stream))
-    _check("qattn_rope_cache_append", rc)
+    fn = "qattn_rope_cache_append"
+    a = _Args(fn, dims)
+    args, _ = _append_args(a, q, k, v, positions, slot_mapping, k_cache, v_cache, cos_sin, False)
+    _check(fn, lib().qattn_rope_cache_append(*args, dims, a.err(err_word), _stream(stream)))
 
 
 def qattn_rope_cache_append_ex(q, k, v, positions, slot_mapping, k_cache, v_cache, cos_sin, dims,
@@ -238,47 +352,26 @@ def qattn_rope_cache_append_ex(q, k, v, positions, slot_mapping, k_cache, v_cach
                                norm_eps=1e-6, err_word=None, stream=None):
     """qattn_rope_cache_append with the qkv projection bias and the Qwen3
     per-head q/k RMSNorms applied before the rotation (None skips a step)."""
-    qp, qs = _rows(q, "q")
-    kp, ks = _rows(k, "k")
-    vp, vs = _rows(v, "v")
-    rc = lib().qattn_rope_cache_append_ex(
-        qp, qs, kp, ks, vp, vs, _dev_ptr(positions, "positions", torch.int32),
-        _dev_ptr(slot_mapping, "slot_mapping", torch.int32), int(positions.shape[0]),
-        _dev_ptr(k_cache, "k_cache", torch.bfloat16), _dev_ptr(v_cache, "v_cache", torch.bfloat16),
-        int(k_cache.shape[0]), _dev_ptr(cos_sin, "cos_sin", torch.float32), int(cos_sin.shape[0]),
-        _dev_ptr(qkv_bias, "qkv_bias", torch.bfloat16),
-        _dev_ptr(q_norm_weight, "q_norm_weight", torch.bfloat16),
-        _dev_ptr(k_norm_weight, "k_norm_weight", torch.bfloat16), float(norm_eps), dims,
-        _dev_ptr(err_word, "err_word", torch.int32), _stream(stream))
-    _check("qattn_rope_cache_append_ex", rc)
-
-
-def _fp8_ptr(t: torch.Tensor, name: str):
-    """Device pointer of an e4m3 cache (uint8 or float8_e4m3fn storage)."""
-    if t.dtype not in (torch.uint8, torch.float8_e4m3fn):
-        raise ValueError(f"{name} must be uint8 or float8_e4m3fn, got {t.dtype}")
-    return _dev_ptr(t, name)
+    fn = "qattn_rope_cache_append_ex"
+    a = _Args(fn, dims)
+    args, extras = _append_args(a, q, k, v, positions, slot_mapping, k_cache, v_cache, cos_sin,
+                                False, qkv_bias, q_norm_weight, k_norm_weight)
+    _check(fn, lib().qattn_rope_cache_append_ex(*args, *extras, float(norm_eps), dims,
+                                                a.err(err_word), _stream(stream)))
 
 
 def qattn_rope_cache_append_fp8(q, k, v, positions, slot_mapping, k_cache, v_cache, cos_sin,
                                 k_scale, v_scale, dims, qkv_bias=None, q_norm_weight=None,
                                 k_norm_weight=None, norm_eps=1e-6, err_word=None, stream=None):
-    """qattn_rope_cache_append_ex into e4m3 caches: keys and values stored
-    as e4m3(x / k_scale), e4m3(x / v_scale)."""
-    qp, qs = _rows(q, "q")
-    kp, ks = _rows(k, "k")
-    vp, vs = _rows(v, "v")
-    rc = lib().qattn_rope_cache_append_fp8(
-        qp, qs, kp, ks, vp, vs, _dev_ptr(positions, "positions", torch.int32),
-        _dev_ptr(slot_mapping, "slot_mapping", torch.int32), int(positions.shape[0]),
-        _fp8_ptr(k_cache, "k_cache"), _fp8_ptr(v_cache, "v_cache"),
-        int(k_cache.shape[0]), _dev_ptr(cos_sin, "cos_sin", torch.float32), int(cos_sin.shape[0]),
-        _dev_ptr(qkv_bias, "qkv_bias", torch.bfloat16),
-        _dev_ptr(q_norm_weight, "q_norm_weight", torch.bfloat16),
-        _dev_ptr(k_norm_weight, "k_norm_weight", torch.bfloat16), float(norm_eps),
-        float(k_scale), float(v_scale), dims,
-        _dev_ptr(err_word, "err_word", torch.int32), _stream(stream))
-    _check("qattn_rope_cache_append_fp8", rc)
+    """qattn_rope_cache_append_ex into e4m3 caches (uint8 or float8_e4m3fn
+    storage): keys and values stored as e4m3(x / k_scale), e4m3(x / v_scale)."""
+    fn = "qattn_rope_cache_append_fp8"
+    a = _Args(fn, dims)
+    args, extras = _append_args(a, q, k, v, positions, slot_mapping, k_cache, v_cache, cos_sin,
+                                True, qkv_bias, q_norm_weight, k_norm_weight)
+    _check(fn, lib().qattn_rope_cache_append_fp8(*args, *extras, float(norm_eps), float(k_scale),
+                                                 float(v_scale), dims, a.err(err_word),
+                                                 _stream(stream)))
 
 
 QATTN_DECODE_CUDA_CORE = 0
@@ -294,34 +387,48 @@ def qattn_paged_decode_workspace_size(num_seqs: int, max_context_len: int, dims)
     return int(lib().qattn_paged_decode_workspace_size(int(num_seqs), int(max_context_len), dims))
 
 
+def _decode_args(a: _Args, out, q, k_cache, v_cache, block_tables, context_lens, fp8):
+    """out, q rows, caches, tables and lengths of a decode call (one query
+    row per sequence)."""
+    d = a.dims
+    lens = a.vec(context_lens, "context_lens")
+    B = int(context_lens.shape[0])
+    qp, qs = a.rows(q, "q", B, d.num_heads * d.head_dim)
+    kc, vc, nb = a.cache(k_cache, v_cache, fp8)
+    bt, mbps = a.table(block_tables, B)
+    return [a.out(out, B), qp, qs, kc, vc, nb, bt, mbps, lens, B]
+
+
 def qattn_paged_decode(out, q, k_cache, v_cache, block_tables, context_lens, max_context_len,
                        dims, workspace, err_word=None, stream=None):
-    qp, qs = _rows(q, "q")
-    rc = lib().qattn_paged_decode(
-        _dev_ptr(out, "out", torch.bfloat16), qp, qs,
-        _dev_ptr(k_cache, "k_cache", torch.bfloat16), _dev_ptr(v_cache, "v_cache", torch.bfloat16),
-        int(k_cache.shape[0]), _dev_ptr(block_tables, "block_tables", torch.int32),
-        int(block_tables.shape[1]), _dev_ptr(context_lens, "context_lens", torch.int32),
-        int(context_lens.shape[0]), int(max_context_len), dims,
-        _dev_ptr(workspace, "workspace"), int(workspace.numel() * workspace.element_size()),
-        _dev_ptr(err_word, "err_word", torch.int32), _stream(stream))
-    _check("qattn_paged_decode", rc)
+    fn = "qattn_paged_decode"
+    a = _Args(fn, dims)
+    args = _decode_args(a, out, q, k_cache, v_cache, block_tables, context_lens, False)
+    _check(fn, lib().qattn_paged_decode(*args, int(max_context_len), dims, *a.workspace(workspace),
+                                        a.err(err_word), _stream(stream)))
 
 
 def qattn_paged_decode_fp8(out, q, k_cache, v_cache, block_tables, context_lens,
                            max_context_len, k_scale, v_scale, dims, workspace, err_word=None,
                            stream=None):
     """qattn_paged_decode over e4m3 caches read as code * scale."""
-    qp, qs = _rows(q, "q")
-    rc = lib().qattn_paged_decode_fp8(
-        _dev_ptr(out, "out", torch.bfloat16), qp, qs,
-        _fp8_ptr(k_cache, "k_cache"), _fp8_ptr(v_cache, "v_cache"),
-        int(k_cache.shape[0]), _dev_ptr(block_tables, "block_tables", torch.int32),
-        int(block_tables.shape[1]), _dev_ptr(context_lens, "context_lens", torch.int32),
-        int(context_lens.shape[0]), int(max_context_len), float(k_scale), float(v_scale), dims,
-        _dev_ptr(workspace, "workspace"), int(workspace.numel() * workspace.element_size()),
-        _dev_ptr(err_word, "err_word", torch.int32), _stream(stream))
-    _check("qattn_paged_decode_fp8", rc)
+    fn = "qattn_paged_decode_fp8"
+    a = _Args(fn, dims)
+    args = _decode_args(a, out, q, k_cache, v_cache, block_tables, context_lens, True)
+    _check(fn, lib().qattn_paged_decode_fp8(*args, int(max_context_len), float(k_scale),
+                                            float(v_scale), dims, *a.workspace(workspace),
+                                            a.err(err_word), _stream(stream)))
+
+
+def qattn_paged_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens,
+                               max_context_len, dims, err_word=None, stream=None):
+    """qattn_paged_decode with its split-KV scratch in the library's own
+    device array (no workspace); calls must not overlap on the GPU."""
+    fn = "qattn_paged_decode_noalloc"
+    a = _Args(fn, dims)
+    args = _decode_args(a, out, q, k_cache, v_cache, block_tables, context_lens, False)
+    _check(fn, lib().qattn_paged_decode_noalloc(*args, int(max_context_len), dims,
+                                                a.err(err_word), _stream(stream)))
 
 
 def qattn_paged_decode_shared_prefix_workspace_size(num_seqs: int, max_context_len: int,
@@ -333,62 +440,12 @@ def qattn_paged_decode_shared_prefix_workspace_size(num_seqs: int, max_context_l
 def qattn_paged_decode_shared_prefix(out, q, k_cache, v_cache, block_tables, context_lens,
                                      max_context_len, shared_prefix_len, dims, workspace,
                                      err_word=None, stream=None):
-    qp, qs = _rows(q, "q")
-    rc = lib().qattn_paged_decode_shared_prefix(
-        _dev_ptr(out, "out", torch.bfloat16), qp, qs,
-        _dev_ptr(k_cache, "k_cache", torch.bfloat16), _dev_ptr(v_cache, "v_cache", torch.bfloat16),
-        int(k_cache.shape[0]), _dev_ptr(block_tables, "block_tables", torch.int32),
-        int(block_tables.shape[1]), _dev_ptr(context_lens, "context_lens", torch.int32),
-        int(context_lens.shape[0]), int(max_context_len), int(shared_prefix_len), dims,
-        _dev_ptr(workspace, "workspace"), int(workspace.numel() * workspace.element_size()),
-        _dev_ptr(err_word, "err_word", torch.int32), _stream(stream))
-    _check("qattn_paged_decode_shared_prefix", rc)
-
-
-def qattn_varlen_prefill_workspace_size(num_seqs: int, max_context_len: int, dims) -> int:
-    return int(lib().qattn_varlen_prefill_workspace_size(int(num_seqs), int(max_context_len), dims))
-
-
-def qattn_varlen_prefill(out, q, cu_seqlens_q, max_q_len, k_cache, v_cache, block_tables,
-                         context_lens, max_context_len, dims, workspace, err_word=None,
-                         stream=None):
-    qp, qs = _rows(q, "q")
-    rc = lib().qattn_varlen_prefill(
-        _dev_ptr(out, "out", torch.bfloat16), qp, qs,
-        _dev_ptr(cu_seqlens_q, "cu_seqlens_q", torch.int32), int(cu_seqlens_q.shape[0]) - 1,
-        int(q.shape[0]), int(max_q_len),
-        _dev_ptr(k_cache, "k_cache", torch.bfloat16), _dev_ptr(v_cache, "v_cache", torch.bfloat16),
-        int(k_cache.shape[0]), _dev_ptr(block_tables, "block_tables", torch.int32),
-        int(block_tables.shape[1]), _dev_ptr(context_lens, "context_lens", torch.int32),
-        int(max_context_len), dims, _dev_ptr(workspace, "workspace"),
-        int(workspace.numel() * workspace.element_size()),
-        _dev_ptr(err_word, "err_word", torch.int32), _stream(stream))
-    _check("qattn_varlen_prefill", rc)
-
-
-
-def qattn_varlen_prefill_fp8_workspace_size(num_seqs: int, num_prefill_seqs: int,
-                                            max_context_len: int, dims) -> int:
-    return int(lib().qattn_varlen_prefill_fp8_workspace_size(
-        int(num_seqs), int(num_prefill_seqs), int(max_context_len), dims))
-
-
-def qattn_varlen_prefill_fp8(out, q, cu_seqlens_q, max_q_len, k_cache, v_cache, block_tables,
-                             context_lens, max_context_len, num_prefill_seqs, k_scale, v_scale,
-                             dims, workspace, err_word=None, stream=None):
-    """qattn_varlen_prefill over e4m3 caches read as code * scale."""
-    qp, qs = _rows(q, "q")
-    rc = lib().qattn_varlen_prefill_fp8(
-        _dev_ptr(out, "out", torch.bfloat16), qp, qs,
-        _dev_ptr(cu_seqlens_q, "cu_seqlens_q", torch.int32), int(cu_seqlens_q.shape[0]) - 1,
-        int(q.shape[0]), int(max_q_len), _fp8_ptr(k_cache, "k_cache"),
-        _fp8_ptr(v_cache, "v_cache"), int(k_cache.shape[0]),
-        _dev_ptr(block_tables, "block_tables", torch.int32), int(block_tables.shape[1]),
-        _dev_ptr(context_lens, "context_lens", torch.int32), int(max_context_len),
-        int(num_prefill_seqs), float(k_scale), float(v_scale), dims,
-        _dev_ptr(workspace, "workspace"), int(workspace.numel() * workspace.element_size()),
-        _dev_ptr(err_word, "err_word", torch.int32), _stream(stream))
-    _check("qattn_varlen_prefill_fp8", rc)
+    fn = "qattn_paged_decode_shared_prefix"
+    a = _Args(fn, dims)
+    args = _decode_args(a, out, q, k_cache, v_cache, block_tables, context_lens, False)
+    _check(fn, lib().qattn_paged_decode_shared_prefix(
+        *args, int(max_context_len), int(shared_prefix_len), dims, *a.workspace(workspace),
+        a.err(err_word), _stream(stream)))
 
 
 def qattn_paged_decode_shared_prefix_fp8_workspace_size(num_seqs: int, max_context_len: int,
@@ -401,14 +458,61 @@ def qattn_paged_decode_shared_prefix_fp8(out, q, k_cache, v_cache, block_tables,
                                          max_context_len, shared_prefix_len, k_scale, v_scale,
                                          dims, workspace, err_word=None, stream=None):
     """qattn_paged_decode_shared_prefix over e4m3 caches read as code * scale."""
-    qp, qs = _rows(q, "q")
-    rc = lib().qattn_paged_decode_shared_prefix_fp8(
-        _dev_ptr(out, "out", torch.bfloat16), qp, qs,
-        _fp8_ptr(k_cache, "k_cache"), _fp8_ptr(v_cache, "v_cache"),
-        int(k_cache.shape[0]), _dev_ptr(block_tables, "block_tables", torch.int32),
-        int(block_tables.shape[1]), _dev_ptr(context_lens, "context_lens", torch.int32),
-        int(context_lens.shape[0]), int(max_context_len), int(shared_prefix_len),
-        float(k_scale), float(v_scale), dims, _dev_ptr(workspace, "workspace"),
-        int(workspace.numel() * workspace.element_size()),
-        _dev_ptr(err_word, "err_word", torch.int32), _stream(stream))
-    _check("qattn_paged_decode_shared_prefix_fp8", rc)
+    fn = "qattn_paged_decode_shared_prefix_fp8"
+    a = _Args(fn, dims)
+    args = _decode_args(a, out, q, k_cache, v_cache, block_tables, context_lens, True)
+    _check(fn, lib().qattn_paged_decode_shared_prefix_fp8(
+        *args, int(max_context_len), int(shared_prefix_len), float(k_scale), float(v_scale),
+        dims, *a.workspace(workspace), a.err(err_word), _stream(stream)))
+
+
+def qattn_varlen_prefill_workspace_size(num_seqs: int, max_context_len: int, dims) -> int:
+    return int(lib().qattn_varlen_prefill_workspace_size(int(num_seqs), int(max_context_len), dims))
+
+
+def _varlen_args(a: _Args, out, q, cu_seqlens_q, max_q_len, k_cache, v_cache, block_tables,
+                 context_lens, fp8):
+    """out, q rows, sequence offsets, caches, tables and lengths of a varlen
+    call: q holds total_q = q.shape[0] rows, cu_seqlens_q num_seqs + 1."""
+    d = a.dims
+    cu = a.vec(cu_seqlens_q, "cu_seqlens_q", 1)
+    S = int(cu_seqlens_q.shape[0]) - 1
+    total_q = int(q.shape[0]) if q.dim() == 2 else 0
+    qp, qs = a.rows(q, "q", total_q, d.num_heads * d.head_dim)
+    kc, vc, nb = a.cache(k_cache, v_cache, fp8)
+    bt, mbps = a.table(block_tables, S)
+    lens = a.vec(context_lens, "context_lens", S)
+    return [a.out(out, total_q), qp, qs, cu, S, total_q, int(max_q_len), kc, vc, nb, bt, mbps,
+            lens]
+
+
+def qattn_varlen_prefill(out, q, cu_seqlens_q, max_q_len, k_cache, v_cache, block_tables,
+                         context_lens, max_context_len, dims, workspace, err_word=None,
+                         stream=None):
+    fn = "qattn_varlen_prefill"
+    a = _Args(fn, dims)
+    args = _varlen_args(a, out, q, cu_seqlens_q, max_q_len, k_cache, v_cache, block_tables,
+                        context_lens, False)
+    _check(fn, lib().qattn_varlen_prefill(*args, int(max_context_len), dims,
+                                          *a.workspace(workspace), a.err(err_word),
+                                          _stream(stream)))
+
+
+def qattn_varlen_prefill_fp8_workspace_size(num_seqs: int, num_prefill_seqs: int,
+                                            max_context_len: int, dims) -> int:
+    return int(lib().qattn_varlen_prefill_fp8_workspace_size(
+        int(num_seqs), int(num_prefill_seqs), int(max_context_len), dims))
+
+
+def qattn_varlen_prefill_fp8(out, q, cu_seqlens_q, max_q_len, k_cache, v_cache, block_tables,
+                             context_lens, max_context_len, num_prefill_seqs, k_scale, v_scale,
+                             dims, workspace, err_word=None, stream=None):
+    """qattn_varlen_prefill over e4m3 caches read as code * scale."""
+    fn = "qattn_varlen_prefill_fp8"
+    a = _Args(fn, dims)
+    args = _varlen_args(a, out, q, cu_seqlens_q, max_q_len, k_cache, v_cache, block_tables,
+                        context_lens, True)
+    _check(fn, lib().qattn_varlen_prefill_fp8(*args, int(max_context_len), int(num_prefill_seqs),
+                                              float(k_scale), float(v_scale), dims,
+                                              *a.workspace(workspace), a.err(err_word),
+                                              _stream(stream)))
