@@ -22,6 +22,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -596,6 +597,26 @@ def sample_size(w: W.Workload) -> int:
     return max(1, n)
 
 
+def cpu_model() -> str:
+    """The host CPU's model, for the record: /proc/cpuinfo's model name, or on
+    Arm (which prints none) its implementer and part numbers."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            lines = f.read().splitlines()
+    except OSError:
+        return platform.machine()
+    fields = {}
+    for line in lines:
+        k, _, v = line.partition(":")
+        fields.setdefault(k.strip(), v.strip())
+    if fields.get("model name"):
+        return fields["model name"]
+    if fields.get("CPU implementer") and fields.get("CPU part"):
+        return (f"{platform.machine()} (CPU implementer {fields['CPU implementer']}, "
+                f"part {fields['CPU part']})")
+    return platform.machine()
+
+
 def cpu_baseline(w: W.Workload, kv_bytes_full: int, budget_s: float = 10.0):
     """The oracle, as it stands, timed on this host: repeated over a sample
     of the workload for about budget_s seconds."""
@@ -607,7 +628,7 @@ def cpu_baseline(w: W.Workload, kv_bytes_full: int, budget_s: float = 10.0):
         total += sec
         reps += 1
     return {"value": round(kvb * reps / total / 1e9, 4), "unit": "GB/s",
-            "cores": oracle.default_threads(), "kind": "oracle",
+            "cores": oracle.default_threads(), "cpu_model": cpu_model(), "kind": "oracle",
             "sample": f"first {n} of {w.num_seqs} sequences ({kvb} of {kv_bytes_full} KV bytes) "
                       f"x {reps} repetitions, append + attention in fp64, {total:.1f} s"}
 
@@ -682,7 +703,8 @@ def run_reference(args, dist: Dist):
         "config": {"workload": args.workload, "batch_sampled": n, "block_size": w.block_size,
                    "kv_cache_dtype": args.kv},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "kind": "oracle",
-                         "cores": oracle.default_threads(), "sample": sample},
+                         "cores": oracle.default_threads(), "cpu_model": cpu_model(),
+                         "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "wall_s": round(total, 2),
