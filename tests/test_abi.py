@@ -187,3 +187,56 @@ def test_fp8_host_validation_before_any_cuda_call(lib):
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(RuntimeError, match="not found"):
         Q.load_library(str(tmp_path / "missing.so"))
+
+
+C_CLIENT = r"""
+#include <stdio.h>
+#include <stdlib.h>
+#include "qattn.h"
+
+int main(void) {
+  qattn_dims d = {28, 4, 128, 16, 0.0f};
+  float* table = (float*)malloc(sizeof(float) * 8 * 128);
+  int32_t ctx = 17;
+  int rc;
+  printf("version %d\n", qattn_version());
+  printf("status %s\n", qattn_status_string(QATTN_ERR_WORKSPACE));
+  rc = qattn_rope_table_build(table, 8, 128, 1e6);
+  printf("table %d %.9g %.9g\n", rc, table[0], table[64]);
+  printf("workspace %d\n", qattn_paged_decode_workspace_size(64, 4096, d) > 0);
+  /* host validation, before any CUDA call: null caches */
+  rc = qattn_paged_decode(NULL, NULL, 3584, NULL, NULL, 10, NULL, 4, &ctx, 1, 17, d, NULL, 0,
+                          NULL, NULL);
+  printf("decode %d\n", rc);
+  d.block_size = 48;
+  rc = qattn_paged_decode(NULL, NULL, 3584, NULL, NULL, 10, NULL, 4, &ctx, 1, 17, d, NULL, 0,
+                          NULL, NULL);
+  printf("unsupported %d\n", rc);
+  free(table);
+  return 0;
+}
+"""
+
+
+def test_header_is_plain_c_and_the_library_links_from_c(lib, tmp_path):
+    """include/qattn.h compiles as strict C99, and a C program linked against
+    libqattn.so runs its host-side entry points (no GPU needed)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "client.c"
+    src.write_text(C_CLIENT)
+    exe = tmp_path / "client"
+    libdir = os.path.dirname(B.LIB_PATH)
+    subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                    "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe),
+                    "-L", libdir, "-lqattn", f"-Wl,-rpath,{libdir}"], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split("\n")
+    assert out[0] == f"version {int(lib.qattn_version())}"
+    assert out[1] == "status " + lib.qattn_status_string(Q.QATTN_ERR_WORKSPACE).decode()
+    assert out[2] == "table 0 1 0"           # position 0: cos 1, sin 0
+    assert out[3] == "workspace 1"
+    assert out[4] == f"decode {Q.QATTN_ERR_INVALID_ARG}"
+    assert out[5] == f"unsupported {Q.QATTN_ERR_UNSUPPORTED}"
