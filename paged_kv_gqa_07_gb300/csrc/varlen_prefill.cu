@@ -32,7 +32,9 @@
 //     shared-memory P buffers (K-major, swizzled: the A operand of P V).
 //     With two S, two P and two O slots, S(n+1) and P V(n) run on the tensor
 //     cores while the softmax works on tile n, and an item's last P V and
-//     epilogue overlap the next item's first tile.
+//     epilogue overlap the next item's first tile.  The epilogue stages each
+//     warp's bf16 output rows in the P buffer that last P V released, so
+//     every store instruction writes whole 128-byte half-rows.
 //   * O is rescaled lazily: the running max is only moved when the new max
 //     exceeds it by more than 8 (log2 units), so most tiles skip the TMEM
 //     round trip; P values stay <= 2^8, well inside bf16.
