@@ -60,6 +60,7 @@ ERR_SLOT = 1
 ERR_BLOCK = 2
 ERR_CONTEXT = 4
 ERR_POSITION = 16
+ERR_NORM_INEXACT = 64  # oracle only: an RMSNorm sum of squares was rounded in fp64
 
 _P = ctypes.c_void_p
 _I32 = ctypes.c_int32
@@ -102,7 +103,7 @@ def lib():
             L.oracle_add_bias_head.argtypes = [_P, _P, _I32, _P]
             L.oracle_add_bias_head.restype = None
             L.oracle_rmsnorm_head.argtypes = [_P, _P, _I32, _F64, _P]
-            L.oracle_rmsnorm_head.restype = None
+            L.oracle_rmsnorm_head.restype = _I32
             L.oracle_rope_cache_append_ex.argtypes = (
                 L.oracle_rope_cache_append.argtypes + [_P, _P, _P, _F64])
             L.oracle_rope_cache_append_ex.restype = _I32
@@ -244,13 +245,15 @@ def add_bias_head(x, b):
     return y
 
 
-def rmsnorm_head(x, w, eps):
-    """RMSNorm of one head vector (uint16 bf16 bits) with weight w, eps."""
+def rmsnorm_head(x, w, eps, with_exactness=False):
+    """RMSNorm of one head vector (uint16 bf16 bits) with weight w, eps.
+    With ``with_exactness``, returns (y, exact) where exact says the fp64 sum
+    of squares was exact (the reading's premise)."""
     x = np.ascontiguousarray(x, dtype=np.uint16)
     w = np.ascontiguousarray(w, dtype=np.uint16)
     y = np.empty_like(x)
-    lib().oracle_rmsnorm_head(_ptr(x), _ptr(w), int(x.size), float(eps), _ptr(y))
-    return y
+    inexact = lib().oracle_rmsnorm_head(_ptr(x), _ptr(w), int(x.size), float(eps), _ptr(y))
+    return (y, inexact == 0) if with_exactness else y
 
 
 def rope_cache_append_ex(qkv, positions, slot_mapping, k_cache, v_cache, cos_sin,

@@ -53,6 +53,8 @@
 #define OR_ERR_BLOCK 2
 #define OR_ERR_CONTEXT 4
 #define OR_ERR_POSITION 16
+/* oracle only: an RMSNorm sum of squares was not exact in fp64 */
+#define OR_ERR_NORM_INEXACT 64
 
 /* ---------------------------------------------------------------- bf16 --- */
 
@@ -299,45 +301,44 @@ void oracle_add_bias_head(const uint16_t* x, const uint16_t* b, int32_t n, uint1
 
 /* RMSNorm of one head vector with a per-dimension weight (the Qwen3
  * attention's q_norm / k_norm, nano-vllm Qwen3 skeleton page, module tree;
- * eps = rms_norm_eps): y_i = x_i / sqrt(mean(x^2) + eps) * w_i.  Reading,
- * as a bf16 tensor op with fp32 arithmetic, every product and sum rounded
- * (no fused multiply-add): the head's n values are taken as 8 slices, slice
- * p = values 8p .. 8p+7 followed by values n/2+8p .. n/2+8p+7 (n = 128);
- * each slice's squares are summed in that order, the 8 slice sums are added
- * as the tree ((s0+s1)+(s2+s3))+((s4+s5)+(s6+s7)); v = fp32(ss/n + eps);
- * r = 1 / sqrt(v) with correctly rounded sqrt and division;
- * y_i = bf16(fp32(fp32(x_i * r) * w_i)).  n must be 128 (16 values a
- * slice). */
-void oracle_rmsnorm_head(const uint16_t* x, const uint16_t* w, int32_t n, double eps,
-                         uint16_t* y) {
-  const int32_t half = n / 2;
-  float part[8];
-  for (int32_t p = 0; p < 8; ++p) {
-    float acc = 0.0f;
-    for (int32_t j = 0; j < 8; ++j) {
-      float v = bf16_to_f32(x[8 * p + j]);
-      float sq = v * v;
-      acc = acc + sq;
-    }
-    for (int32_t j = 0; j < 8; ++j) {
-      float v = bf16_to_f32(x[half + 8 * p + j]);
-      float sq = v * v;
-      acc = acc + sq;
-    }
-    part[p] = acc;
-  }
-  float t01 = part[0] + part[1], t23 = part[2] + part[3];
-  float t45 = part[4] + part[5], t67 = part[6] + part[7];
-  float u0 = t01 + t23, u1 = t45 + t67;
-  float ss = u0 + u1;
-  float mean = ss * (1.0f / (float)n);
-  float v = mean + (float)eps;
-  float r = 1.0f / sqrtf(v);
+ * eps = rms_norm_eps): y_i = x_i / sqrt(mean(x^2) + eps) * w_i.  The page
+ * names the module, not its rounding.  Reading: a bf16 tensor operation
+ * around an exact mean square --
+ *   ss = the exact sum of the squares of the n bf16 values.  It is summed
+ *        in fp64 in index order: a bf16 square has 16 significant bits, so
+ *        every square and every partial sum is exact unless the head's
+ *        nonzero magnitudes span more than about 2^18; the function
+ *        returns 1 if any addition was rounded (the reading then does not
+ *        hold), else 0;
+ *   v  = fp32(ss / n + eps), one rounding, with eps taken as the fp32
+ *        number the C interface passes;
+ *   r  = 1 / sqrt(v), correctly rounded fp32 square root and division;
+ *   y_i = bf16(fp32(fp32(x_i * r) * w_i)). */
+int32_t oracle_rmsnorm_head(const uint16_t* x, const uint16_t* w, int32_t n, double eps,
+                            uint16_t* y) {
+  double ss = 0.0;
+  int32_t inexact = 0;
   for (int32_t i = 0; i < n; ++i) {
-    float t = bf16_to_f32(x[i]) * r;
-    float u = t * bf16_to_f32(w[i]);
+    const double xi = bf16_to_f64(x[i]);
+    const double sq = xi * xi; /* exact: 8 significant bits squared */
+    const double t = ss + sq;
+    if (isfinite(t)) {
+      /* error of the rounded addition (Knuth's two-sum) */
+      const double bv = t - ss;
+      const double e = (ss - (t - bv)) + (sq - bv);
+      if (e != 0.0) inexact = 1;
+    }
+    ss = t;
+  }
+  const double e32 = (double)(float)eps;
+  const float v = (float)(ss / (double)n + e32);
+  const float r = 1.0f / sqrtf(v);
+  for (int32_t i = 0; i < n; ++i) {
+    const float t = bf16_to_f32(x[i]) * r;
+    const float u = t * bf16_to_f32(w[i]);
     y[i] = f32_to_bf16_rne(u);
   }
+  return inexact;
 }
 
 /* oracle_rope_cache_append with the projection bias and the Qwen3 head
@@ -369,7 +370,7 @@ int32_t oracle_rope_cache_append_ex(
       memcpy(a, qh, sizeof(uint16_t) * (size_t)D);
       if (bias) oracle_add_bias_head(a, bias + (int64_t)h * D, D, a);
       if (q_norm_w) {
-        oracle_rmsnorm_head(a, q_norm_w, D, eps, b);
+        if (oracle_rmsnorm_head(a, q_norm_w, D, eps, b)) err |= OR_ERR_NORM_INEXACT;
         memcpy(a, b, sizeof(uint16_t) * (size_t)D);
       }
       oracle_rope_head_exact(a, D, row, qh);
@@ -388,7 +389,7 @@ int32_t oracle_rope_cache_append_ex(
       memcpy(a, kh, sizeof(uint16_t) * (size_t)D);
       if (bias) oracle_add_bias_head(a, bias + (int64_t)(num_heads + g) * D, D, a);
       if (k_norm_w) {
-        oracle_rmsnorm_head(a, k_norm_w, D, eps, b);
+        if (oracle_rmsnorm_head(a, k_norm_w, D, eps, b)) err |= OR_ERR_NORM_INEXACT;
         memcpy(a, b, sizeof(uint16_t) * (size_t)D);
       }
       oracle_rope_head_exact(a, D, row, k_cache + dst);
@@ -432,7 +433,7 @@ int32_t oracle_rope_cache_append_fp8(
         slot < 0 ? &slot : &zero, 1, kb, vb, 1, cos_sin, max_pos, num_heads,
         num_kv_heads, D, 1, bias, q_norm_w, k_norm_w, eps);
     err |= e;
-    if (e || slot < 0) continue;
+    if ((e & ~OR_ERR_NORM_INEXACT) || slot < 0) continue;
     if ((int64_t)slot >= (int64_t)num_blocks * block_size) {
       err |= OR_ERR_SLOT;
       continue;

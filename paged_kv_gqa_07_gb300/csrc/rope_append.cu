@@ -22,10 +22,9 @@
 // "Qwen2大模型架构解析与vLLM优化实践"; the Qwen3 attention's q_norm / k_norm
 // RMSNorms, nano-vllm Qwen3 skeleton page, module tree), each a bf16 tensor
 // operation: x' = bf16(x + b) rounded once; RMSNorm over the head's 128
-// values with the sum of squares in fp32 in a fixed order (8 slices of 16,
-// then a pairwise tree -- see rmsnorm_group), v = fp32(mean + eps),
-// r = 1 / sqrt(v) with correctly rounded fp32 sqrt and division,
-// y = bf16(fp32(fp32(x * r) * w)).
+// values around the exact sum of their squares (integer arithmetic, see
+// rmsnorm_group), v = fp32(mean + eps), r = 1 / sqrt(v) with correctly
+// rounded fp32 sqrt and division, y = bf16(fp32(fp32(x * r) * w)).
 //
 // FP8 cache (kv_cache_dtype "fp8", fp8_e4m3fn with a cache scale per tensor,
 // "Qwen2大模型架构解析与vLLM优化实践" sections 4.1, 4.2, 6.3): the bf16 key
@@ -76,33 +75,81 @@ __device__ __forceinline__ uint4 add_bias8(const uint4& x, const __nv_bfloat16* 
   return y;
 }
 
+// Exponent key of a bf16 value for the exact sum of squares: a value is
+// sig * 2^(e - 134) with an 8-bit significand sig and e = max(exponent
+// field, 1) (subnormals share e = 1, sig without the implicit bit).
+__device__ __forceinline__ int bf16_sq_exp(uint32_t bits) {
+  const int ef = static_cast<int>((bits >> 7) & 0xffu);
+  return (bits & 0x7fffu) != 0u ? max(ef, 1) : 0;
+}
+
+// sig^2 * 2^(2 (e - emax) + 41): an integer for e >= emax - 20; smaller
+// squares (below 2^-40 of the largest) are truncated.  At most 2^57 each,
+// so the 128 terms of a head fit in 64 bits.
+__device__ __forceinline__ uint64_t bf16_sq_term(uint32_t bits, int emax) {
+  const uint32_t ef = (bits >> 7) & 0xffu;
+  const uint32_t sig = (bits & 0x7fu) | (ef != 0u ? 0x80u : 0u);
+  const uint64_t sq = static_cast<uint64_t>(sig * sig);
+  const int sh = 2 * (max(static_cast<int>(ef), 1) - emax) + 41;
+  if (sh >= 0) return sq << sh;
+  return sh > -64 ? sq >> (-sh) : 0ull;
+}
+
 // RMSNorm of one head whose 128 values are spread over the 8 lanes of an
 // aligned lane group (x1: dims 8p .. 8p+7, x2: dims 64+8p .. 64+8p+7 of
-// lane p of the group).  Sum of squares in fp32, each step rounded: lane p
-// adds its 16 squares in dimension order, then the butterfly over the group
-// forms ((s0+s1)+(s2+s3))+((s4+s5)+(s6+s7)) in every lane.
+// lane p of the group).  The mean square is formed from the exact sum of
+// the squares: each square as a 64-bit integer multiple of a power of two
+// fixed by the head's largest exponent, summed in integers (exact, so the
+// order of the lanes does not matter), then scaled to fp64 -- the value an
+// fp64 sum of the squares gives whenever that sum is exact.  Then
+// v = fp32(ss / 128 + eps), r = 1 / sqrt(v) with correctly rounded fp32
+// sqrt and division, y = bf16(fp32(fp32(x * r) * w)).
 __device__ __forceinline__ void rmsnorm_group(uint4& x1, uint4& x2, const __nv_bfloat16* w,
                                               int part, float eps) {
   const uint32_t mask = 0xffu << ((threadIdx.x & 31) & 24);
   uint32_t* u1 = reinterpret_cast<uint32_t*>(&x1);
   uint32_t* u2 = reinterpret_cast<uint32_t*>(&x2);
-  float ss = 0.0f;
+  uint32_t h[16];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float a = bf16lo_to_f32(u1[i]), b = bf16hi_to_f32(u1[i]);
-    ss = __fadd_rn(ss, __fmul_rn(a, a));
-    ss = __fadd_rn(ss, __fmul_rn(b, b));
+    h[2 * i] = u1[i] & 0xffffu;
+    h[2 * i + 1] = u1[i] >> 16;
+    h[8 + 2 * i] = u2[i] & 0xffffu;
+    h[8 + 2 * i + 1] = u2[i] >> 16;
   }
+  int emax = 0;
+  bool nan = false, inf = false;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float c = bf16lo_to_f32(u2[i]), d = bf16hi_to_f32(u2[i]);
-    ss = __fadd_rn(ss, __fmul_rn(c, c));
-    ss = __fadd_rn(ss, __fmul_rn(d, d));
+  for (int i = 0; i < 16; ++i) {
+    emax = max(emax, bf16_sq_exp(h[i]));
+    const bool special = (h[i] & 0x7f80u) == 0x7f80u;
+    nan = nan || (special && (h[i] & 0x7fu) != 0u);
+    inf = inf || (special && (h[i] & 0x7fu) == 0u);
   }
-  ss = __fadd_rn(ss, __shfl_xor_sync(mask, ss, 1));
-  ss = __fadd_rn(ss, __shfl_xor_sync(mask, ss, 2));
-  ss = __fadd_rn(ss, __shfl_xor_sync(mask, ss, 4));
-  const float v = __fadd_rn(__fmul_rn(ss, 1.0f / 128.0f), eps);
+  emax = max(emax, __shfl_xor_sync(mask, emax, 1));
+  emax = max(emax, __shfl_xor_sync(mask, emax, 2));
+  emax = max(emax, __shfl_xor_sync(mask, emax, 4));
+  nan = __any_sync(mask, nan);
+  inf = __any_sync(mask, inf);
+  uint64_t acc = 0;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) acc += bf16_sq_term(h[i], emax);
+  acc += __shfl_xor_sync(mask, acc, 1);
+  acc += __shfl_xor_sync(mask, acc, 2);
+  acc += __shfl_xor_sync(mask, acc, 4);
+  double ss;
+  if (nan) {
+    ss = __longlong_as_double(0x7ff8000000000000ll);
+  } else if (inf) {
+    ss = __longlong_as_double(0x7ff0000000000000ll);
+  } else {
+    // x^2 = term * 2^(2 emax - 309); emax in 1..254 keeps the scale normal
+    const int k = emax > 0 ? 2 * emax - 309 : 0;
+    ss = __dmul_rn(__ull2double_rn(acc),
+                   __longlong_as_double(static_cast<long long>(k + 1023) << 52));
+  }
+  const float v = __double2float_rn(__dadd_rn(__dmul_rn(ss, 1.0 / 128.0),
+                                              static_cast<double>(eps)));
   const float r = __fdiv_rn(1.0f, __fsqrt_rn(v));
   const uint4 w1 = *reinterpret_cast<const uint4*>(w + part * 8);
   const uint4 w2 = *reinterpret_cast<const uint4*>(w + 64 + part * 8);

@@ -1,6 +1,13 @@
 """GPU parity of the extended append (qattn_rope_cache_append_ex: qkv
 projection bias and Qwen3 per-head q/k RMSNorm before RoPE) against the
-oracle: bit-exact over the whole cache and the rotated queries."""
+oracle: bit-exact over the whole cache and the rotated queries.  The oracle's
+RMSNorm sums the squares in fp64 in index order (the plain definition); the
+kernel forms the exact sum in integers and rounds it to fp64 once, so the two
+agree wherever the fp64 sum is exact.  N(0, 1) heads occasionally hold a
+value below 2^-18 of their largest, where the fp64 sum rounds (the oracle
+reports it, ERR_NORM_INEXACT); the sums then differ by a few fp64 ulps,
+which reach the bf16 output only if fp32(ss / 128 + eps) sits on a rounding
+boundary -- the tests still require bit equality there."""
 import numpy as np
 import pytest
 import torch
@@ -59,7 +66,34 @@ def test_append_ex_bit_exact(idx, bias, norm):
     b, qn, kn = extras(w, 500 + idx, bias, norm)
     qkv, kc, vc, e = oracle_append_ex(w, b, qn, kn)
     r = gpu_append_ex(GpuRun(w), b, qn, kn)
-    assert e == 0 and r.err_bits == 0
+    assert (e & ~oracle.ERR_NORM_INEXACT) == 0 and r.err_bits == 0
+    assert np.array_equal(u16(r.g.k_cache), kc), "k_cache differs"
+    assert np.array_equal(u16(r.g.v_cache), vc), "v_cache differs"
+    assert np.array_equal(u16(r.g.qkv), qkv), "rotated q differs"
+
+
+def test_append_ex_norm_wide_range_bit_exact():
+    """Heads whose values span about 2^15 (a different power-of-two scale
+    per element), exact zeros, and heads made only of bf16 subnormals: the
+    kernel's integer sum of squares must meet the oracle's fp64 sum bit for
+    bit wherever that sum is exact."""
+    w = W.custom(16, 8, ctx=[40, 75, 130], q_lens=[5, 1, 3], seed=530)
+    g = torch.Generator().manual_seed(531)
+    T, width = w.qkv.shape
+    z = torch.randn(T, width, generator=g)
+    base = torch.sign(z) * (0.25 + z.abs())
+    expo = torch.randint(-8, 4, (T, width), generator=g).float()
+    x = base * torch.exp2(expo)
+    x[torch.rand(T, width, generator=g) < 0.05] = 0.0
+    # token 0: every head subnormal (|x| < 2^-126); token 1: q head 3 all zero
+    x[0] = torch.randn(width, generator=g) * 2.0 ** -130
+    x[1, 3 * 128:4 * 128] = 0.0
+    w.qkv = x.to(torch.bfloat16)
+    b, qn, kn = extras(w, 532, bias=False, norm=True)
+    qkv, kc, vc, e = oracle_append_ex(w, b, qn, kn)
+    assert e == 0, "the oracle's fp64 sum of squares was not exact on this input"
+    r = gpu_append_ex(GpuRun(w), b, qn, kn)
+    assert r.err_bits == 0
     assert np.array_equal(u16(r.g.k_cache), kc), "k_cache differs"
     assert np.array_equal(u16(r.g.v_cache), vc), "v_cache differs"
     assert np.array_equal(u16(r.g.qkv), qkv), "rotated q differs"

@@ -125,7 +125,7 @@ def test_append_fp8_with_bias_and_norm_bit_exact():
     host = {k: u16(v) for k, v in extras.items()}
     qkv, kc, vc, _, e1, _ = oracle_fp8(w, extras=host)
     r = Fp8Run(w).append(extras).sync()
-    assert int(r.err.item()) == 0 and e1 == 0
+    assert int(r.err.item()) == 0 and (e1 & ~oracle.ERR_NORM_INEXACT) == 0
     assert np.array_equal(u16(r.g.qkv), qkv)
     assert np.array_equal(r.g.k_cache.cpu().numpy(), kc)
     assert np.array_equal(r.g.v_cache.cpu().numpy(), vc)

@@ -357,6 +357,52 @@ def test_rmsnorm_scale_invariance_and_unit_rms():
     assert np.all(np.abs(got - ref) <= np.abs(ref) * 2.0 ** -8 + 1e-30)
 
 
+def test_rmsnorm_against_40_digit_arithmetic():
+    """The defining formula y = x / sqrt(mean(x^2) + eps) * w evaluated with
+    40-digit arithmetic on small integer-valued heads (and the same heads
+    scaled by 2^-10, where eps = fp32(1e-6) is about 5% of mean(x^2)): the
+    oracle's fp32 steps stay within 2^-21 relative of the exact value, so its
+    bf16 result is the exact value's bf16 rounding up to that margin."""
+    mp = pytest.importorskip("mpmath")
+    mp.mp.dps = 40
+    rng = np.random.default_rng(21)
+    D = 128
+    eps32 = float(np.float32(1e-6))
+    mismatched = 0
+    for scale_exp in (0, -10):
+        for _ in range(6):
+            xi = rng.integers(-8, 9, D).astype(np.float64) * 2.0 ** scale_exp
+            wi = rng.integers(-6, 7, D).astype(np.float64) / 4.0
+            x, w = bf16_of(xi), bf16_of(wi)
+            assert np.array_equal(f64(x), xi) and np.array_equal(f64(w), wi)
+            y, exact = oracle.rmsnorm_head(x, w, 1e-6, with_exactness=True)
+            assert exact
+            ms = mp.fsum(mp.mpf(float(v)) ** 2 for v in xi) / D
+            r = 1 / mp.sqrt(ms + mp.mpf(eps32))
+            got = f64(y)
+            for i in range(D):
+                ref = mp.mpf(float(xi[i])) * r * mp.mpf(float(wi[i]))
+                err = abs(mp.mpf(float(got[i])) - ref)
+                assert err <= (2.0 ** -8 + 2.0 ** -21) * abs(ref) + mp.mpf(10) ** -30
+                if got[i] != f64(bf16_of([float(ref)]))[0]:
+                    mismatched += 1
+    # only values within 2^-21 of a bf16 rounding boundary may round the other way
+    assert mismatched <= 4
+
+
+def test_rmsnorm_reports_an_inexact_sum_of_squares():
+    """The reading needs the exact sum of squares; the oracle says when fp64
+    could not hold it (magnitudes spanning ~2^60) and holds it otherwise."""
+    D = 128
+    w1 = bf16_of(np.ones(D))
+    g = torch.Generator().manual_seed(22)
+    x = u16(torch.randn(D, generator=g).to(torch.bfloat16))
+    assert oracle.rmsnorm_head(x, w1, 1e-6, with_exactness=True)[1]
+    wide = np.concatenate([np.full(D // 2, 1.0), np.full(D // 2, 1.0 + 2.0 ** -7) * 2.0 ** -60])
+    _, exact = oracle.rmsnorm_head(bf16_of(wide), w1, 1e-6, with_exactness=True)
+    assert not exact
+
+
 def test_append_ex_without_extras_equals_append():
     w = W.build(0)
     a_qkv, a_kc, a_vc = u16(w.qkv), u16(w.k_cache), u16(w.v_cache)
