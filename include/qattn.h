@@ -23,7 +23,9 @@
  * Conventions for every entry point:
  *   - All tensor pointers are DEVICE pointers unless the argument says host.
  *     The caller owns every buffer; the library allocates no device memory
- *     and keeps no device state between calls.
+ *     and keeps no device state between calls -- with one exception,
+ *     qattn_paged_decode_noalloc, whose split-KV scratch is a fixed array
+ *     inside the library (see its declaration).
  *   - Any entry point may be called from several host threads, and for any
  *     device (the current device of the calling thread): the host-side
  *     caches (SM counts, encoded tensor maps, the kernels' shared-memory
@@ -226,17 +228,22 @@ size_t qattn_paged_decode_workspace_size(int32_t num_seqs,
                                          int32_t max_context_len,
                                          qattn_dims dims);
 
-/* Which kernel qattn_paged_decode (and the decode rows of
- * qattn_varlen_prefill, and the shared-prefix decode) launches for these
- * dims: QATTN_DECODE_TENSOR_CORE (tcgen05 with the query group as the MMA N
- * dimension; the default for every group size) or QATTN_DECODE_CUDA_CORE
- * (the group's dot products on CUDA cores; 16-token blocks only), selected
- * by the environment variable QATTN_DECODE_KERNEL=cuda (read once per
- * process) when block_size is 16.  Returns -1
- * for invalid dims. */
-#define QATTN_DECODE_CUDA_CORE 0
-#define QATTN_DECODE_TENSOR_CORE 1
-int qattn_paged_decode_kernel(qattn_dims dims);
+/* Testing hook for the decode kernel's failure path (the pages have no
+ * counterpart).  Every decode launch after this call (qattn_paged_decode,
+ * its FP8 and no-allocation variants, the decode rows of the varlen and
+ * shared-prefix calls) limits each of its bounded waits to wait_limit_ns
+ * (0 restores the default of 2 s; otherwise 1000 .. 2e9), and, if
+ * skip_k_copy >= 0, the decode kernel's first CTA does not issue the copy of
+ * its K tile number skip_k_copy, so that the waits on that tile run out.
+ * Such a call still returns QATTN_OK; on the device every role of the
+ * stalled CTA gives up, its copies and MMAs in flight are drained (at most
+ * max(wait_limit_ns, 10 ms) each) and its tensor memory is freed, and
+ * QATTN_DEVERR_TIMEOUT is set in the error word; that call's output is
+ * unspecified, and the next call with the defaults restored is unaffected.
+ * Process-wide state, not synchronised with calls in flight on other host
+ * threads: for tests only.  Returns QATTN_ERR_INVALID_ARG for values out of
+ * range. */
+int qattn_debug_decode_faults(int64_t wait_limit_ns, int32_t skip_k_copy);
 
 /* Step 3, decode: one query row per sequence.
  *   out          [num_seqs, num_heads, head_dim] bf16, contiguous;

@@ -18,7 +18,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libqattn.so")
-SOURCES = ["api.cu", "rope_append.cu", "paged_decode.cu", "paged_decode_tc.cu", "fp8_gather.cu",
+SOURCES = ["api.cu", "rope_append.cu", "decode_merge.cu", "paged_decode_tc.cu", "fp8_gather.cu",
            "varlen_prefill.cu", "decode_noalloc.cu"]
 HEADERS = ["common.cuh", "internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -5,6 +5,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 #include <utility>
 #include <vector>
@@ -196,23 +197,6 @@ bool encode_q_group_map(CUtensorMap* map, const void* q, int64_t q_row_stride, i
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Which decode kernel serves a shape: the tensor-core kernel (measured
-// faster for every group size, 1..8); the environment variable
-// QATTN_DECODE_KERNEL=cuda selects the CUDA-core kernel instead where it
-// applies (16-token blocks).
-bool use_tc_decode(int group, int block_size) {
-  static int forced = [] {
-    const char* e = getenv("QATTN_DECODE_KERNEL");
-    if (e == nullptr) return 0;
-    if (strcmp(e, "cuda") == 0) return 1;
-    if (strcmp(e, "tc") == 0) return 2;
-    return 0;
-  }();
-  if (block_size != kBlockSize) return true;
-  if (forced == 1) return false;
-  return group >= 1 && group <= 8;
-}
-
 int check_cache(const void* k_cache, const void* v_cache, int32_t num_blocks,
                 const qattn_dims& d) {
   if (k_cache == nullptr || v_cache == nullptr || num_blocks <= 0) return QATTN_ERR_INVALID_ARG;
@@ -224,6 +208,13 @@ int check_cache(const void* k_cache, const void* v_cache, int32_t num_blocks,
 }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? QATTN_OK : QATTN_ERR_CUDA; }
+
+// Testing hook state (qattn_debug_decode_faults): the decode kernel's wait
+// limit (0: the default) and the K copy its first CTA skips (-1: none).
+std::atomic<long long> g_debug_wait_ns{0};
+std::atomic<int> g_debug_skip_k{-1};
+
+constexpr uint64_t kMinDrainNs = 10000000ull;  // 10 ms
 
 // A cache scale: finite, positive and normal (its reciprocal stays finite).
 bool valid_scale(float s) { return s == s && !isinf(s) && s >= 1.17549435e-38f; }
@@ -394,11 +385,13 @@ int qattn_rope_cache_append(void* q, int64_t q_row_stride, const void* k, int64_
                                     0.0f, dims, err_word, stream);
 }
 
-int qattn_paged_decode_kernel(qattn_dims dims) {
-  if (check_dims(dims) != QATTN_OK) return -1;
-  return use_tc_decode(dims.num_heads / dims.num_kv_heads, dims.block_size)
-             ? QATTN_DECODE_TENSOR_CORE
-             : QATTN_DECODE_CUDA_CORE;
+int qattn_debug_decode_faults(int64_t wait_limit_ns, int32_t skip_k_copy) {
+  if (wait_limit_ns < 0 || (wait_limit_ns > 0 && wait_limit_ns < 1000) ||
+      wait_limit_ns > static_cast<int64_t>(kWaitTimeoutNs) || skip_k_copy < -1)
+    return QATTN_ERR_INVALID_ARG;
+  g_debug_wait_ns.store(wait_limit_ns);
+  g_debug_skip_k.store(skip_k_copy);
+  return QATTN_OK;
 }
 
 size_t qattn_paged_decode_workspace_size(int32_t num_seqs, int32_t max_context_len,
@@ -447,14 +440,16 @@ int decode_common(void* out, const void* q, int64_t q_row_stride, int32_t q_rows
                                 dims.num_heads / dims.num_kv_heads, extra_parts);
   a.prefix_len = prefix_len;
   a.part_base = part_base;
+  const long long w = g_debug_wait_ns.load();
+  a.wait_ns = w > 0 ? static_cast<uint64_t>(w) : kWaitTimeoutNs;
+  a.drain_ns = a.wait_ns < kMinDrainNs ? kMinDrainNs
+                                        : (a.wait_ns > kWaitTimeoutNs ? kWaitTimeoutNs : a.wait_ns);
+  a.debug_skip_k = g_debug_skip_k.load();
   const int group = dims.num_heads / dims.num_kv_heads;
-  if (kv_fp8 || use_tc_decode(group, dims.block_size)) {
-    CUtensorMap qmap;
-    if (!encode_q_group_map(&qmap, q, q_row_stride, q_rows, dims.num_heads, group))
-      return QATTN_ERR_CUDA;
-    return cuda_status(launch_paged_decode_tc(a, kmap, vmap, qmap, num_sms, stream));
-  }
-  return cuda_status(launch_paged_decode(a, kmap, vmap, num_sms, stream));
+  CUtensorMap qmap;
+  if (!encode_q_group_map(&qmap, q, q_row_stride, q_rows, dims.num_heads, group))
+    return QATTN_ERR_CUDA;
+  return cuda_status(launch_paged_decode_tc(a, kmap, vmap, qmap, num_sms, stream));
 }
 
 int check_attention_args(void* out, const void* q, int64_t q_row_stride, const void* k_cache,

@@ -17,7 +17,6 @@
 namespace qattn {
 
 constexpr int kHeadDim = 128;
-constexpr int kBlockSize = 16;      // the CUDA-core decode's block size; others take 16/32/64
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s
 
 // ------------------------------------------------------------ addresses ---
@@ -110,17 +109,17 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete.  Returns false if
-// *abort becomes non-zero or the wait exceeds kWaitTimeoutNs; in the latter
-// case it raises *abort itself so the rest of the CTA unwinds quickly.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          volatile int* abort) {
+// *abort becomes non-zero or the wait exceeds limit_ns; in the latter case it
+// raises *abort itself so the rest of the CTA unwinds quickly.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          uint64_t limit_ns = kWaitTimeoutNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 0;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 15u) == 15u) {
       if (abort != nullptr && *abort) return false;
-      if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         if (abort != nullptr) *abort = 1;
         return false;
       }
@@ -129,12 +128,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
 }
 
 // The same wait without an abort flag (used when draining copies in flight
-// before exit); bounded by the timeout alone.
-__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
+// before exit); bounded by the limit alone.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity,
+                                                uint64_t limit_ns = kWaitTimeoutNs) {
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 

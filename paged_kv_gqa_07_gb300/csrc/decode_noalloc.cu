@@ -18,10 +18,13 @@
 // QATTN_ERR_WORKSPACE before anything is launched.
 //
 // In host code the array's name is only a stand-in, not a device address:
-// the device address is looked up with cudaGetSymbolAddress, once per
-// device, on the first call made while that device is current (the lookup
-// may load the library's device code, so make that first call outside any
-// stream capture).
+// the device address is looked up with cudaGetSymbolAddress on the first
+// call made while a device is current, and again whenever the calling
+// thread's current context on that device is not the one the address was
+// taken in (after cudaDeviceReset, or from a context the caller created
+// itself); each context has its own copy of the array.  The lookup may load
+// the library's device code, so make the first call in a context outside
+// any stream capture.
 //
 // All calls share the one array and it keeps whatever the last call left
 // in it.  Nothing in it has to start at zero: the decode kernels write every
@@ -43,20 +46,45 @@ static __device__ __align__(256) uint8_t g_decode_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
 
-// Device address of g_decode_scratch on the current device (looked up once
-// per device), or nullptr if the lookup failed.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
+// cuCtxGetCurrent from the driver, looked up once (nullptr if unavailable).
+CtxGetCurrentFn ctx_get_current() {
+  static std::once_flag once;
+  static CtxGetCurrentFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  return fn;
+}
+
+// Device address of g_decode_scratch in the current context of the current
+// device (looked up again when that context changes), or nullptr if the
+// lookup failed.
 void* scratch_on_current_device() {
   static std::mutex mu;
   static void* addr[kMaxDevices] = {nullptr};
+  static CUcontext owner[kMaxDevices] = {nullptr};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  CtxGetCurrentFn get = ctx_get_current();
+  CUcontext ctx = nullptr;
+  if (get == nullptr || get(&ctx) != CUDA_SUCCESS) return nullptr;
   std::lock_guard<std::mutex> lk(mu);
-  if (addr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess) return nullptr;
-    addr[dev] = p;
-  }
-  return addr[dev];
+  if (ctx != nullptr && addr[dev] != nullptr && owner[dev] == ctx) return addr[dev];
+  // (the lookup also makes the device's primary context current if no
+  // context was)
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess) return nullptr;
+  if (get(&ctx) != CUDA_SUCCESS || ctx == nullptr) return nullptr;
+  addr[dev] = p;
+  owner[dev] = ctx;
+  return p;
 }
 
 }  // namespace

@@ -103,12 +103,19 @@ struct RopeAppendArgs {
 };
 cudaError_t launch_rope_append(const RopeAppendArgs& a, cudaStream_t stream);
 
-// ---- paged decode (paged_decode.cu) ----
-// Decode-mode work comes in fixed chunks of 32 tokens (two cache blocks);
-// every CTA of the persistent grid owns a contiguous run of at least
-// kMinChunksPerCta chunks of the (sequence, kv head, chunk) space.
-constexpr int kChunkTokens = 32;
-constexpr int kMinChunksPerCta = 8;
+// ---- paged decode (paged_decode_tc.cu) and its merge (decode_merge.cu) ----
+// Decode work comes in 128-token tiles; every CTA of the persistent grid owns
+// a contiguous run of at least kTcMinTilesPerCta tiles of the (sequence, kv
+// head, tile) list.
+constexpr int kTcTileTokens = 128;
+constexpr int kTcMinTilesPerCta = 2;
+
+// Parts a unit of max_context_len tokens can leave in the workspace: a run
+// of n tiles meets at most ceil(n / kTcMinTilesPerCta) + 1 CTAs.
+__host__ __device__ inline int64_t decode_max_parts(int64_t max_context_len) {
+  const int64_t tiles = (max_context_len + kTcTileTokens - 1) / kTcTileTokens;
+  return (tiles + kTcMinTilesPerCta - 1) / kTcMinTilesPerCta + 1;
+}
 
 struct DecodeWorkspace {
   int32_t* nparts;  // [num_seqs * Hkv] parts of each (sequence, kv head) unit, written
@@ -139,9 +146,9 @@ struct DecodeArgs {
   int32_t max_context_len;
   int32_t num_heads;
   int32_t num_kv_heads;
-  int32_t block_size;      // tokens per cache block: 16, 32 or 64 (16 for K2)
+  int32_t block_size;      // tokens per cache block: 16, 32 or 64
   float scale_log2;        // softmax scale * log2(e) (* k_scale for an FP8 cache)
-  int32_t kv_fp8;          // the caches hold e4m3 codes (tensor-core kernel only)
+  int32_t kv_fp8;          // the caches hold e4m3 codes
   float v_scale;           // FP8: multiplies the output
   int32_t* err_word;
   DecodeWorkspace ws;
@@ -151,13 +158,16 @@ struct DecodeArgs {
   // output rows.  Plain decode: both 0.
   int32_t prefix_len;
   int32_t part_base;
+  // Limits of the kernel's bounded waits: every wait while working, and the
+  // drain of copies and MMAs in flight before exit (never below 10 ms, so
+  // that a short test limit cannot cut a drain short).
+  uint64_t wait_ns;
+  uint64_t drain_ns;
+  // Testing only: the first CTA skips the copy of its K tile with this
+  // index (-1: none), so that the wait on it runs out.
+  int32_t debug_skip_k;
 };
-// CUDA-core decode (K2): 32-token chunks, the GQA group on CUDA cores.
-cudaError_t launch_paged_decode(const DecodeArgs& a, const CUtensorMap& kmap,
-                                const CUtensorMap& vmap, int num_sms, cudaStream_t stream);
 // Tensor-core decode (K2t): 128-token tiles, the GQA group as the MMA N dimension.
-constexpr int kTcTileTokens = 128;
-constexpr int kTcMinTilesPerCta = 2;
 cudaError_t launch_paged_decode_tc(const DecodeArgs& a, const CUtensorMap& kmap,
                                    const CUtensorMap& vmap, const CUtensorMap& qmap,
                                    int num_sms, cudaStream_t stream);
@@ -238,7 +248,7 @@ __device__ __forceinline__ void finish_invalid_rows(const DecodeArgs& a, const i
 }
 #endif
 
-// K2r: merge the parts of straddling units (either decode kernel's).
+// K2r: merge the parts of straddling units.
 cudaError_t launch_decode_merge(const DecodeArgs& a, cudaStream_t stream);
 
 // ---- varlen prefill (varlen_prefill.cu) ----

@@ -351,7 +351,7 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
       const int vs = j % kVStages;
       bool okv = true;
       if (lane == 0) {
-        okv = mbar_wait(&v_empty[vs], ((j / kVStages) & 1) ^ 1, abort_flag);
+        okv = mbar_wait(&v_empty[vs], ((j / kVStages) & 1) ^ 1, abort_flag, a.wait_ns);
         if (okv) mbar_arrive_expect_tx(&v_full[vs], nval * blk_bytes);
       }
       okv = __shfl_sync(0xffffffffu, okv, 0);
@@ -411,7 +411,7 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
         if (lane == 0 && (ci == 0 || n == 0)) {
           ++seg;
           const int qs = seg & 1;
-          ok = mbar_wait(&q_empty[qs], ((seg >> 1) & 1) ^ 1, abort_flag);
+          ok = mbar_wait(&q_empty[qs], ((seg >> 1) & 1) ^ 1, abort_flag, a.wait_ns);
           if (ok) {
             mbar_arrive_expect_tx(&q_full[qs], 2 * G * 128);
             uint8_t* qdst = smem + L::kOffQ + qs * kSmallBytes;
@@ -422,12 +422,15 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
         }
         const int ks = n % kKStages;
         if (lane == 0 && ok) {
-          ok = mbar_wait(&k_empty[ks], ((n / kKStages) & 1) ^ 1, abort_flag);
+          ok = mbar_wait(&k_empty[ks], ((n / kKStages) & 1) ^ 1, abort_flag, a.wait_ns);
           if (ok) mbar_arrive_expect_tx(&k_full[ks], nvalid * blk_bytes);
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
-        if (lane < bpt && myid >= 0) {
+        // (a test may ask the first CTA to skip one copy: its K barrier
+        // then never completes and the waits on it run out)
+        const bool skip = blockIdx.x == 0 && n == a.debug_skip_k;
+        if (lane < bpt && myid >= 0 && !skip) {
           uint8_t* dst = smem + L::kOffK + ks * L::kStageBytes + lane * blk_bytes;
           if constexpr (kFp8)
             tma_load_2d(dst, &kmap, 0, (myid * Hkv + g) * a.block_size, &k_full[ks]);
@@ -451,10 +454,10 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
     if (lane == 0) {
       const int nk = n;
       for (int j = nk - 1; j >= 0 && j >= nk - kKStages; --j)
-        mbar_wait_drain(&k_full[j % kKStages], (j / kKStages) & 1);
+        mbar_wait_drain(&k_full[j % kKStages], (j / kKStages) & 1, a.drain_ns);
       for (int j = nv - 1; j >= 0 && j >= nv - kVStages; --j)
-        mbar_wait_drain(&v_full[j % kVStages], (j / kVStages) & 1);
-      for (int s = seg; s >= 0 && s >= seg - 1; --s) mbar_wait_drain(&q_full[s & 1], (s >> 1) & 1);
+        mbar_wait_drain(&v_full[j % kVStages], (j / kVStages) & 1, a.drain_ns);
+      for (int s = seg; s >= 0 && s >= seg - 1; --s) mbar_wait_drain(&q_full[s & 1], (s >> 1) & 1, a.drain_ns);
       if (*abort_flag) set_err(a.err_word, QATTN_DEVERR_TIMEOUT);
     }
     __syncwarp();
@@ -474,7 +477,7 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
                                          : idesc_bf16_f32(kHeadDim, kN, false, true);
       bool ok = true;
       uint64_t idle_since = 0;
-      // No progress for kWaitTimeoutNs (or the abort flag): give up.
+      // No progress for the wait limit (or the abort flag): give up.
       auto idle = [&](bool progressed) {
         if (progressed) {
           idle_since = 0;
@@ -482,7 +485,7 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
           const uint64_t now = globaltimer_ns();
           if (idle_since == 0) {
             idle_since = now;
-          } else if (*abort_flag || now - idle_since > kWaitTimeoutNs) {
+          } else if (*abort_flag || now - idle_since > a.wait_ns) {
             *abort_flag = 1;
             ok = false;
           }
@@ -574,7 +577,7 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
       }
       // Drain: every MMA of both threads completes before TMEM is released.
       mma_commit(mma_done);
-      mbar_wait_drain(mma_done, 0);
+      mbar_wait_drain(mma_done, 0, a.drain_ns);
     }
     __syncwarp();
   } else if (kFp8 && warp >= kConvWarp0) {
@@ -594,7 +597,7 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
       if (n == 0 || kw.i == 0) {
         ++seg;
         const int qs = seg & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(&q_full[qs], (seg >> 1) & 1, abort_flag)))
+        if (!__all_sync(0xffffffffu, mbar_wait(&q_full[qs], (seg >> 1) & 1, abort_flag, a.wait_ns)))
           return false;
         for (int c = ct; c < kSmallBytes / 16; c += 128) {
           const uint32_t addr = sbase + L::kOffQ + qs * kSmallBytes + c * 16;
@@ -607,8 +610,8 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
         if (lane == 0) mbar_arrive(&qc_full[qs]);
       }
       const int ks = n % kKStages;
-      bool w_ok = mbar_wait(&k_full[ks], (n / kKStages) & 1, abort_flag);
-      if (w_ok && n >= 2) w_ok = mbar_wait(&kc_empty[n & 1], ((n >> 1) & 1) ^ 1, abort_flag);
+      bool w_ok = mbar_wait(&k_full[ks], (n / kKStages) & 1, abort_flag, a.wait_ns);
+      if (w_ok && n >= 2) w_ok = mbar_wait(&kc_empty[n & 1], ((n >> 1) & 1) ^ 1, abort_flag, a.wait_ns);
       if (!__all_sync(0xffffffffu, w_ok)) return false;
       tc_fence_after();
       const uint32_t src = sbase + L::kOffK + ks * L::kStageBytes + row * 128;
@@ -638,8 +641,8 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
     auto conv_v = [&](int j) -> bool {
       const int vs = j % kVStages;
       const int nvalid_tok = min(kTile, vw.L - vw.i * kTile);
-      bool w_ok = mbar_wait(&v_full[vs], (j / kVStages) & 1, abort_flag);
-      if (w_ok && j >= 2) w_ok = mbar_wait(&vc_empty[j & 1], ((j >> 1) & 1) ^ 1, abort_flag);
+      bool w_ok = mbar_wait(&v_full[vs], (j / kVStages) & 1, abort_flag, a.wait_ns);
+      if (w_ok && j >= 2) w_ok = mbar_wait(&vc_empty[j & 1], ((j >> 1) & 1) ^ 1, abort_flag, a.wait_ns);
       if (!__all_sync(0xffffffffu, w_ok)) return false;
       const uint32_t src = sbase + L::kOffV + vs * L::kStageBytes + row * 128;
       const uint32_t dst = sbase + L::kOffVc + (j & 1) * kTileBytes + (row >> 4) * kCacheTileBytes;
@@ -693,7 +696,7 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
     // (rescale, deferred epilogue) or PV(n) (last tile) neither barrier is
     // two phases behind -- the condition a parity wait needs.
     auto wait_pv = [&](int j) -> bool {
-      return __all_sync(0xffffffffu, mbar_wait(&pv_done[j & 1], (j >> 1) & 1, abort_flag));
+      return __all_sync(0xffffffffu, mbar_wait(&pv_done[j & 1], (j >> 1) & 1, abort_flag, a.wait_ns));
     };
     // Epilogue of unit `useg` whose last tile here is j (walk state uw):
     // out = O^T / l, or this CTA's part of a unit that straddles CTAs.
@@ -775,7 +778,7 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
         if (j < cnt) {
           const int nj = n + j;
           w_ok = w_ok && __all_sync(0xffffffffu,
-                                    mbar_wait(&s_full[nj & 1], (nj >> 1) & 1, abort_flag));
+                                    mbar_wait(&s_full[nj & 1], (nj >> 1) & 1, abort_flag, a.wait_ns));
           if (w_ok) {
             tc_fence_after();
             tmem_ld16(lane_addr + (nj & 1) * kN, s[j]);
@@ -811,7 +814,7 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(rbar);
-      if (!__all_sync(0xffffffffu, mbar_wait(rbar, rphase & 1, abort_flag))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(rbar, rphase & 1, abort_flag, a.wait_ns))) {
         ok = false;
         break;
       }
@@ -894,7 +897,7 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
         // hence V(nl-3) landed: this slot's barrier is at most one phase
         // behind.
         if (!__all_sync(0xffffffffu,
-                        mbar_wait(&v_full[nl % kVStages], (nl / kVStages) & 1, abort_flag))) {
+                        mbar_wait(&v_full[nl % kVStages], (nl / kVStages) & 1, abort_flag, a.wait_ns))) {
           ok = false;
           break;
         }
@@ -943,7 +946,7 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(rbar);
-        if (!__all_sync(0xffffffffu, mbar_wait(rbar, rphase & 1, abort_flag))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(rbar, rphase & 1, abort_flag, a.wait_ns))) {
           ok = false;
           break;
         }

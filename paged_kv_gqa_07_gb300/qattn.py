@@ -42,7 +42,7 @@ EXPORTED = [
     "qattn_rope_cache_append",
     "qattn_rope_cache_append_ex",
     "qattn_rope_cache_append_fp8",
-    "qattn_paged_decode_kernel",
+    "qattn_debug_decode_faults",
     "qattn_paged_decode_workspace_size",
     "qattn_paged_decode",
     "qattn_paged_decode_fp8",
@@ -123,8 +123,8 @@ def load_library(path: str | None = None):
             _P, _I64, _P, _I64, _P, _I64, _P, _P, _I32, _P, _P, _I32, _P, _I32, _P, _P, _P,
             ctypes.c_float, ctypes.c_float, ctypes.c_float, qattn_dims, _P, _P]
         L.qattn_rope_cache_append_fp8.restype = ctypes.c_int
-        L.qattn_paged_decode_kernel.argtypes = [qattn_dims]
-        L.qattn_paged_decode_kernel.restype = ctypes.c_int
+        L.qattn_debug_decode_faults.argtypes = [_I64, _I32]
+        L.qattn_debug_decode_faults.restype = ctypes.c_int
         L.qattn_paged_decode_workspace_size.argtypes = [_I32, _I32, qattn_dims]
         L.qattn_paged_decode_workspace_size.restype = _SZ
         L.qattn_paged_decode.argtypes = [
@@ -374,13 +374,11 @@ def qattn_rope_cache_append_fp8(q, k, v, positions, slot_mapping, k_cache, v_cac
                                                  _stream(stream)))
 
 
-QATTN_DECODE_CUDA_CORE = 0
-QATTN_DECODE_TENSOR_CORE = 1
-
-
-def qattn_paged_decode_kernel(dims) -> int:
-    """QATTN_DECODE_CUDA_CORE or QATTN_DECODE_TENSOR_CORE: the decode kernel used for dims."""
-    return int(lib().qattn_paged_decode_kernel(dims))
+def qattn_debug_decode_faults(wait_limit_ns: int, skip_k_copy: int) -> None:
+    """Testing hook: the wait limit of later decode launches (0: default)
+    and the K copy the decode kernel's first CTA skips (-1: none)."""
+    _check("qattn_debug_decode_faults",
+           lib().qattn_debug_decode_faults(int(wait_limit_ns), int(skip_k_copy)))
 
 
 def qattn_paged_decode_workspace_size(num_seqs: int, max_context_len: int, dims) -> int:

@@ -90,18 +90,15 @@ def test_workspace_size_grows_with_context(lib):
     assert Q.qattn_paged_decode_workspace_size(64, 4096, Q.make_dims(28, 5)) == 0
 
 
-@pytest.mark.skipif("QATTN_DECODE_KERNEL" in os.environ, reason="kernel choice forced")
-def test_decode_kernel_choice(lib):
-    # tcgen05 decode for every group size unless QATTN_DECODE_KERNEL=cuda
-    assert Q.qattn_paged_decode_kernel(Q.make_dims(16, 16)) == Q.QATTN_DECODE_TENSOR_CORE
-    assert Q.qattn_paged_decode_kernel(Q.make_dims(16, 8)) == Q.QATTN_DECODE_TENSOR_CORE
-    assert Q.qattn_paged_decode_kernel(Q.make_dims(12, 4)) == Q.QATTN_DECODE_TENSOR_CORE
-    assert Q.qattn_paged_decode_kernel(Q.make_dims(28, 4)) == Q.QATTN_DECODE_TENSOR_CORE
-    assert Q.qattn_paged_decode_kernel(Q.make_dims(32, 4)) == Q.QATTN_DECODE_TENSOR_CORE
-    assert Q.qattn_paged_decode_kernel(Q.make_dims(28, 5)) == -1
-    assert Q.qattn_paged_decode_kernel(Q.make_dims(28, 4, 128, 32)) == Q.QATTN_DECODE_TENSOR_CORE
-    assert Q.qattn_paged_decode_kernel(Q.make_dims(28, 4, 128, 64)) == Q.QATTN_DECODE_TENSOR_CORE
-    assert Q.qattn_paged_decode_kernel(Q.make_dims(28, 4, 128, 128)) == -1
+def test_debug_fault_hook_checks_its_range(lib):
+    """The decode testing hook refuses limits below 1 us or above 2 s and
+    skip indices below -1, and (0, -1) restores the defaults; host only."""
+    f = lib.qattn_debug_decode_faults
+    assert f(5, -1) == Q.QATTN_ERR_INVALID_ARG
+    assert f(3_000_000_000, -1) == Q.QATTN_ERR_INVALID_ARG
+    assert f(0, -2) == Q.QATTN_ERR_INVALID_ARG
+    assert f(1_000_000, 3) == Q.QATTN_OK
+    assert f(0, -1) == Q.QATTN_OK
 
 
 def test_host_validation_before_any_cuda_call(lib):

@@ -1,13 +1,12 @@
-"""Host-side work planning of the decode kernels, compiled with the host C++
+"""Host-side work planning of the decode kernel, compiled with the host C++
 compiler and checked on the CPU over many random sizes.
 
-RunSplit (csrc/internal.h) cuts the T work items of a decode launch (32-token
-chunks for the CUDA-core kernel, 128-token tiles for the tensor-core kernel)
-into one contiguous run per CTA.  The split-KV workspace is sized from its
-promise that a unit of n consecutive items touches at most ceil(n / min_run)
-+ 1 runs, i.e. leaves at most that many partial results (the split-KV
-partition of the decode pages).  These checks pin that promise and the runs'
-coverage, independently of any GPU.
+RunSplit (csrc/internal.h) cuts the T work items of a decode launch
+(128-token tiles) into one contiguous run per CTA.  The split-KV workspace is
+sized from its promise that a unit of n consecutive items touches at most
+ceil(n / min_run) + 1 runs, i.e. leaves at most that many partial results
+(the split-KV partition of the decode pages).  These checks pin that promise
+and the runs' coverage, independently of any GPU.
 """
 import os
 import shutil
@@ -67,15 +66,12 @@ int main() {
       u0 = u1;
     }
   }
-  // The workspace's part bound, ceil(ceil(L / 32) / kMinChunksPerCta) + 1,
-  // covers the tensor-core kernel's units too (128-token tiles, runs of at
-  // least kTcMinTilesPerCta tiles).
+  // The workspace's part bound covers the runs a unit of L tokens can meet
+  // (128-token tiles, runs of at least kTcMinTilesPerCta tiles).
   for (int L = 1; L <= 70000; ++L) {
-    const int chunks = (L + qattn::kChunkTokens - 1) / qattn::kChunkTokens;
-    const int parts_cuda = (chunks + qattn::kMinChunksPerCta - 1) / qattn::kMinChunksPerCta + 1;
     const int tiles = (L + qattn::kTcTileTokens - 1) / qattn::kTcTileTokens;
-    const int parts_tc = (tiles + qattn::kTcMinTilesPerCta - 1) / qattn::kTcMinTilesPerCta + 1;
-    CHECK(parts_tc <= parts_cuda, "L=%d: %d tensor-core parts > %d\n", L, parts_tc, parts_cuda);
+    const int parts = (tiles + qattn::kTcMinTilesPerCta - 1) / qattn::kTcMinTilesPerCta + 1;
+    CHECK(parts <= qattn::decode_max_parts(L), "L=%d: %d parts > workspace bound\n", L, parts);
   }
   std::printf("%s %ld\n", fails ? "FAIL" : "ok", units_checked);
   return fails ? 1 : 0;

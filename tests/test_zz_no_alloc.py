@@ -4,10 +4,11 @@ Some callers may not call cudaMalloc at all -- code inside another
 framework's CUDA-graph capture, a serving loop with a memory pool fixed at
 start-up -- so they cannot hand qattn_paged_decode a workspace.
 qattn_paged_decode_noalloc keeps its split-KV scratch in a fixed array inside
-the library instead.  This test calls it through the C ABI twice in a row
-(the second call starts from whatever the first left in the shared array)
+the library instead.  This test calls it through the C ABI three times in a row
+(each call starts from whatever the previous one left in the shared array)
 and checks each result against qattn_paged_decode with a workspace of its
-own, within the tolerance the parity tests use.  It lives in its own file,
+own, within the tolerance the parity tests use, and that the device's free
+memory does not move across the later calls.  It lives in its own file,
 named to be collected last, and passes alone or after the other tests.
 """
 import ctypes
@@ -50,14 +51,22 @@ def test_noalloc_decode_matches_workspace_decode_twice(idx):
     r = GpuRun(w).append().sync()
     ref = r.attend().sync().out.clone()
     assert r.err_bits == 0
-    for _ in range(2):
-        out = torch.full_like(ref, float("nan"))
+    outs = [torch.full_like(ref, float("nan")) for _ in range(3)]
+    free = []
+    for out in outs:   # nothing in this loop allocates on the torch side
+        torch.cuda.synchronize()
+        free.append(torch.cuda.mem_get_info()[0])
         assert _call(fn, r, out) == Q.QATTN_OK
         torch.cuda.synchronize()
-        assert r.err_bits == 0
+    free.append(torch.cuda.mem_get_info()[0])
+    assert r.err_bits == 0
+    for out in outs:
         d = (out.float() - ref.float()).abs().max().item()
         scale = ref.float().abs().max().item()
         assert d <= ATOL and d / scale <= RTOL
+    # after the first call (which may load the library's device code), the
+    # calls take no device memory
+    assert free[1] == free[2] == free[3]
 
 
 def test_noalloc_refuses_shapes_beyond_its_scratch():
