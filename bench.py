@@ -3,11 +3,16 @@
 A step is the whole path for one batch: RoPE + cache append of the new tokens
 (qattn_rope_cache_append), then paged GQA attention (qattn_paged_decode for a
 decode workload, qattn_varlen_prefill for a mixed one).  Inputs are resident
-in HBM when timing starts; L2 is flushed (a 512 MB buffer is written)
-before every timed step, and each step is timed with CUDA events on the
-launching stream.  The headline workload is the Qwen2-7B-shaped decode step
-(28 query / 4 KV heads, head_dim 128, batch 64, contexts U[128, 4096], block
-size 16, random block placement).
+in HBM when timing starts.  The workload's cache and QKV rows are repeated as
+a stack of layers at different addresses and consecutive steps use
+consecutive layers, as a model's forward pass does, so every step's KV comes
+from HBM (the layers between two uses of one span more than L2) without a
+flush kernel.  Each step is timed with CUDA events on the launching stream.
+The headline workload is the Qwen2-7B-shaped decode step (28 query / 4 KV
+heads, head_dim 128, batch 64, contexts U[128, 4096], block size 16, random
+block placement); a single-GPU run also times the other configurations
+(tiny decode, mixed prefill + decode, long-context decode, shared-prefix
+decode, FP8 cache) with the same harness under "workloads".
 
 Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle on a
 bounded sample of the same workload instead.
@@ -54,6 +59,9 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-clocks", action="store_true")
+    p.add_argument("--no-workloads", action="store_true",
+                   help="time only --workload (by default a single-GPU run of the headline "
+                        "workload also times the other four configurations and the FP8 cache)")
     p.add_argument("--append-sweep", action="store_true",
                    help="supplementary: time RoPE + append alone at 16k and 64k new tokens "
                         "(Qwen2-7B heads), one JSON line per size")
@@ -221,8 +229,185 @@ def profiled_traffic(kernel: str, workload: str, sha: str):
 
 # ----------------------------------------------------------------- ours --
 
+# Launches per call of each entry point, as the library issues them: the
+# append is one kernel; a decode call is the decode kernel and its merge
+# kernel; a shared-prefix call adds the prefix pass; a varlen call with
+# decode rows is the prefill kernel plus the decode pair; an FP8 varlen or
+# shared-prefix call adds the gather of the blocks the prefill kernel reads.
+LAUNCHES = {"append": 1, "decode": 2, "prefix": 3, "varlen": 3, "varlen_fp8": 4,
+            "prefix_fp8": 4}
+
+# Bytes of cache the rotated layers must span so that a call never finds its
+# KV in L2 (129 MB) from the previous calls.
+LAYER_SPAN_BYTES = 512 << 20
+
+
+class Harness:
+    """One workload resident on the device, with `layers` independent copies
+    of its KV cache and QKV rows at different addresses -- the same layer
+    shape repeated, as in a model's stack.  Timed calls cycle through the
+    layers, so every call reads KV that the previous calls left out of L2
+    (each layer's cache, or the span of layers between two uses of one, is
+    larger than L2), with no flush kernel between calls."""
+
+    def __init__(self, args, name, dev, kv="bf16", rank=0, sub_seqs=None, extras="none"):
+        from paged_kv_gqa_07_gb300 import qattn as Q
+        self.Q = Q
+        idx = W.WORKLOAD_NAMES.index(name)
+        w = W.build(name, seed=W.SEED_BASE + idx + 1000 * rank, block_size=args.block_size)
+        if sub_seqs is not None:
+            w = first_sequences(w, sub_seqs)
+        self.fp8 = kv == "fp8"
+        if self.fp8:
+            w = W.with_fp8_cache(w)
+        self.w, self.dev, self.extras = w, dev, extras
+        self.ks, self.vs = W.FP8_K_SCALE, W.FP8_V_SCALE
+        H, Hkv, D, BS = w.num_heads, w.num_kv_heads, w.head_dim, w.block_size
+        self.dims = Q.make_dims(H, Hkv, D, BS)
+        g = W.to_device(w, dev)
+        self.g = g
+        self.table = Q.qattn_rope_table_build(w.max_pos, D, w.theta).to(dev)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.decode = w.is_decode
+        self.max_ctx = w.max_context_len
+        self.prefix = w.shared_prefix_tokens if self.decode else 0
+        self.n_prefill = sum(1 for n in w.q_lens if n >= 2)
+        B = w.num_seqs
+        if self.prefix and self.fp8:
+            ws = Q.qattn_paged_decode_shared_prefix_fp8_workspace_size(B, self.max_ctx,
+                                                                      self.prefix, self.dims)
+        elif not self.decode and self.fp8:
+            ws = Q.qattn_varlen_prefill_fp8_workspace_size(B, self.n_prefill, self.max_ctx,
+                                                           self.dims)
+        elif self.prefix:
+            ws = Q.qattn_paged_decode_shared_prefix_workspace_size(B, self.max_ctx, self.dims)
+        elif self.decode:
+            ws = Q.qattn_paged_decode_workspace_size(B, self.max_ctx, self.dims)
+        else:
+            ws = Q.qattn_varlen_prefill_workspace_size(B, self.max_ctx, self.dims)
+        self.ws = torch.empty(max(ws, 256), dtype=torch.uint8, device=dev)
+        self.out = torch.empty((w.num_tokens, H, D), dtype=torch.bfloat16, device=dev)
+        cache_bytes = 2 * g.k_cache.numel() * g.k_cache.element_size()
+        self.nlayers = max(2, min(256, -(-LAYER_SPAN_BYTES // max(cache_bytes, 1))))
+        self.layers = [(g.qkv, g.k_cache, g.v_cache)]
+        for _ in range(self.nlayers - 1):
+            self.layers.append((g.qkv.clone(), g.k_cache.clone(), g.v_cache.clone()))
+        gx = torch.Generator().manual_seed(W.SEED_BASE + 77)
+        self.bias = self.qn = self.kn = None
+        if extras in ("bias", "both"):
+            self.bias = (0.5 * torch.randn((H + 2 * Hkv) * D, generator=gx)).to(torch.bfloat16).to(dev)
+        if extras in ("qknorm", "both"):
+            self.qn = (1.0 + 0.2 * torch.randn(D, generator=gx)).to(torch.bfloat16).to(dev)
+            self.kn = (1.0 + 0.2 * torch.randn(D, generator=gx)).to(torch.bfloat16).to(dev)
+
+    @property
+    def kind(self) -> str:
+        if self.prefix:
+            return "prefix_fp8" if self.fp8 else "prefix"
+        if self.decode:
+            return "decode"
+        return "varlen_fp8" if self.fp8 and self.n_prefill else "varlen"
+
+    def views(self, qkv):
+        w = self.w
+        H, Hkv, D = w.num_heads, w.num_kv_heads, w.head_dim
+        return qkv[:, :H * D], qkv[:, H * D:(H + Hkv) * D], qkv[:, (H + Hkv) * D:]
+
+    def append(self, l, qkv=None, positions=None, slots=None):
+        Q, g = self.Q, self.g
+        lq, kc, vc = self.layers[l % self.nlayers]
+        q, k, v = self.views(lq if qkv is None else qkv)
+        pos = g.positions if positions is None else positions
+        sl = g.slot_mapping if slots is None else slots
+        if self.fp8:
+            Q.qattn_rope_cache_append_fp8(q, k, v, pos, sl, kc, vc, self.table, self.ks, self.vs,
+                                          self.dims, qkv_bias=self.bias, q_norm_weight=self.qn,
+                                          k_norm_weight=self.kn, err_word=self.err)
+        elif self.extras == "none":
+            Q.qattn_rope_cache_append(q, k, v, pos, sl, kc, vc, self.table, self.dims, self.err)
+        else:
+            Q.qattn_rope_cache_append_ex(q, k, v, pos, sl, kc, vc, self.table, self.dims,
+                                         qkv_bias=self.bias, q_norm_weight=self.qn,
+                                         k_norm_weight=self.kn, err_word=self.err)
+
+    def attend(self, l, qkv=None, block_tables=None, context_lens=None, cu=None, out=None):
+        Q, g, w = self.Q, self.g, self.w
+        lq, kc, vc = self.layers[l % self.nlayers]
+        q = self.views(lq if qkv is None else qkv)[0]
+        bt = g.block_tables if block_tables is None else block_tables
+        cl = g.context_lens if context_lens is None else context_lens
+        cu = g.cu_seqlens_q if cu is None else cu
+        out = self.out if out is None else out
+        mc, ws, err, d = self.max_ctx, self.ws, self.err, self.dims
+        if self.prefix and self.fp8:
+            Q.qattn_paged_decode_shared_prefix_fp8(out, q, kc, vc, bt, cl, mc, self.prefix,
+                                                   self.ks, self.vs, d, ws, err)
+        elif not self.decode and self.fp8:
+            Q.qattn_varlen_prefill_fp8(out, q, cu, w.max_q_len, kc, vc, bt, cl, mc,
+                                       self.n_prefill, self.ks, self.vs, d, ws, err)
+        elif self.prefix:
+            Q.qattn_paged_decode_shared_prefix(out, q, kc, vc, bt, cl, mc, self.prefix, d, ws,
+                                               err)
+        elif self.fp8:
+            Q.qattn_paged_decode_fp8(out, q, kc, vc, bt, cl, mc, self.ks, self.vs, d, ws, err)
+        elif self.decode:
+            Q.qattn_paged_decode(out, q, kc, vc, bt, cl, mc, d, ws, err)
+        else:
+            Q.qattn_varlen_prefill(out, q, cu, w.max_q_len, kc, vc, bt, cl, mc, d, ws, err)
+
+    def step(self, l):
+        self.append(l)
+        self.attend(l)
+
+    def timed(self, fn, steps, warmup, stream):
+        """Per-call device times (ms) of `steps` calls fn(layer), layers in
+        rotation, after `warmup` untimed calls.  A GPU sleep queued first
+        lets the host enqueue ahead, so the events time the device."""
+        for i in range(warmup):
+            fn(i)
+        torch.cuda.synchronize(self.dev)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        if hasattr(torch.cuda, "_sleep"):
+            torch.cuda._sleep(20_000_000)
+        for s in range(steps):
+            evs[s][0].record(stream)
+            fn(warmup + s)
+            evs[s][1].record(stream)
+        torch.cuda.synchronize(self.dev)
+        assert int(self.err.item()) == 0, f"device error bits {int(self.err.item())}"
+        return [a.elapsed_time(b) for a, b in evs]
+
+    def qo_bytes(self) -> int:
+        w = self.w
+        return 2 * w.num_tokens * w.num_heads * w.head_dim * 2
+
+    def free(self):
+        self.layers = None
+        self.g = None
+
+
+def decode_summary(h: Harness, attn_ms, step_ms, hbm_peak, peak_kind):
+    """KV bandwidth of a decode call and its fraction of the HBM peak."""
+    w = h.w
+    a = statistics.median(attn_ms) * 1e-3
+    s = statistics.median(step_ms) * 1e-3
+    kv = w.kv_bytes_read()
+    alg = kv + h.qo_bytes()
+    d = {"attention_us": round(a * 1e6, 2), "step_us": round(s * 1e6, 2),
+         "kv_bytes": kv, "algorithmic_bytes": alg,
+         "kv_GBps": round(alg / a / 1e9, 1), "frac": round(alg / a / 1e9 / hbm_peak, 4),
+         "peak_kind": peak_kind, "seqs_per_s": round(w.num_seqs / s, 1)}
+    if h.prefix:
+        uniq = w.unique_kv_bytes() + h.qo_bytes()
+        d.update(logical_kv_GBps=d.pop("kv_GBps"), distinct_bytes=uniq,
+                 distinct_GBps=round(uniq / a / 1e9, 1),
+                 frac=round(uniq / a / 1e9 / hbm_peak, 4),
+                 frac_basis="distinct blocks (each read from DRAM once)")
+    return d
+
+
 def run_ours(args, dist: Dist):
-    import numpy as np  # noqa: F401
     from paged_kv_gqa_07_gb300 import build as B
     from paged_kv_gqa_07_gb300 import qattn as Q
 
@@ -230,141 +415,37 @@ def run_ours(args, dist: Dist):
     Q.load_library()
     dev = torch.device("cuda", dist.local_rank)
     torch.cuda.set_device(dev)
-    w = W.build(args.workload, seed=W.SEED_BASE + W.WORKLOAD_NAMES.index(args.workload) + 1000 * dist.rank,
-                block_size=args.block_size)
-    fp8 = args.kv == "fp8"
-    if fp8:
-        w = W.with_fp8_cache(w)
-    ks, vs = W.FP8_K_SCALE, W.FP8_V_SCALE
-    H, Hkv, D, BS = w.num_heads, w.num_kv_heads, w.head_dim, w.block_size
-    dims = Q.make_dims(H, Hkv, D, BS)
-    g = W.to_device(w, dev)
-    qkv0 = g.qkv.clone()
-    table = Q.qattn_rope_table_build(w.max_pos, D, w.theta).to(dev)
-    err = torch.zeros(1, dtype=torch.int32, device=dev)
-    decode = w.is_decode
-    max_ctx = w.max_context_len
-    # a decode batch on a shared cached prefix takes the shared-prefix entry point
-    prefix = w.shared_prefix_tokens if decode else 0
-    n_prefill = sum(1 for n in w.q_lens if n >= 2)
-    if prefix and fp8:
-        ws_size = Q.qattn_paged_decode_shared_prefix_fp8_workspace_size(w.num_seqs, max_ctx,
-                                                                         prefix, dims)
-    elif not decode and fp8:
-        ws_size = Q.qattn_varlen_prefill_fp8_workspace_size(w.num_seqs, n_prefill, max_ctx, dims)
-    elif prefix:
-        ws_size = Q.qattn_paged_decode_shared_prefix_workspace_size(w.num_seqs, max_ctx, dims)
-    elif decode:
-        ws_size = Q.qattn_paged_decode_workspace_size(w.num_seqs, max_ctx, dims)
-    else:
-        ws_size = Q.qattn_varlen_prefill_workspace_size(w.num_seqs, max_ctx, dims)
-    ws = torch.empty(max(ws_size, 256), dtype=torch.uint8, device=dev)
-    out = torch.empty((w.num_tokens, H, D), dtype=torch.bfloat16, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+    hbm_peak, tf_peak, peak_kind = measured_peaks()
+    h = Harness(args, args.workload, dev, kv=args.kv, rank=dist.rank, extras=args.extras)
+    w = h.w
+    H, Hkv, D, BS = w.num_heads, w.num_kv_heads, w.head_dim, w.block_size
 
-    gx = torch.Generator().manual_seed(W.SEED_BASE + 77)
-    bias = qn = kn = None
-    if args.extras in ("bias", "both"):
-        bias = (0.5 * torch.randn((H + 2 * Hkv) * D, generator=gx)).to(torch.bfloat16).to(dev)
-    if args.extras in ("qknorm", "both"):
-        qn = (1.0 + 0.2 * torch.randn(D, generator=gx)).to(torch.bfloat16).to(dev)
-        kn = (1.0 + 0.2 * torch.randn(D, generator=gx)).to(torch.bfloat16).to(dev)
-
-    def append():
-        if fp8:
-            Q.qattn_rope_cache_append_fp8(g.q_view(), g.k_view(), g.v_view(), g.positions,
-                                          g.slot_mapping, g.k_cache, g.v_cache, table, ks, vs,
-                                          dims, qkv_bias=bias, q_norm_weight=qn,
-                                          k_norm_weight=kn, err_word=err)
-        elif args.extras == "none":
-            Q.qattn_rope_cache_append(g.q_view(), g.k_view(), g.v_view(), g.positions,
-                                      g.slot_mapping, g.k_cache, g.v_cache, table, dims, err)
-        else:
-            Q.qattn_rope_cache_append_ex(g.q_view(), g.k_view(), g.v_view(), g.positions,
-                                         g.slot_mapping, g.k_cache, g.v_cache, table, dims,
-                                         qkv_bias=bias, q_norm_weight=qn, k_norm_weight=kn,
-                                         err_word=err)
-
-    def attend():
-        if prefix and fp8:
-            Q.qattn_paged_decode_shared_prefix_fp8(out, g.q_view(), g.k_cache, g.v_cache,
-                                                   g.block_tables, g.context_lens, max_ctx,
-                                                   prefix, ks, vs, dims, ws, err)
-        elif not decode and fp8:
-            Q.qattn_varlen_prefill_fp8(out, g.q_view(), g.cu_seqlens_q, w.max_q_len, g.k_cache,
-                                       g.v_cache, g.block_tables, g.context_lens, max_ctx,
-                                       n_prefill, ks, vs, dims, ws, err)
-        elif prefix:
-            Q.qattn_paged_decode_shared_prefix(out, g.q_view(), g.k_cache, g.v_cache,
-                                               g.block_tables, g.context_lens, max_ctx, prefix,
-                                               dims, ws, err)
-        elif fp8:
-            Q.qattn_paged_decode_fp8(out, g.q_view(), g.k_cache, g.v_cache, g.block_tables,
-                                     g.context_lens, max_ctx, ks, vs, dims, ws, err)
-        elif decode:
-            Q.qattn_paged_decode(out, g.q_view(), g.k_cache, g.v_cache, g.block_tables,
-                                 g.context_lens, max_ctx, dims, ws, err)
-        else:
-            Q.qattn_varlen_prefill(out, g.q_view(), g.cu_seqlens_q, w.max_q_len, g.k_cache,
-                                   g.v_cache, g.block_tables, g.context_lens, max_ctx, dims, ws,
-                                   err)
-
-    for _ in range(args.warmup):
-        g.qkv.copy_(qkv0)
-        append()
-        attend()
-    torch.cuda.synchronize(dev)
-
-    # (A) the step: events only at step boundaries, so the attention kernel
-    # may overlap the append kernel's tail (programmatic dependent launch).
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    # (A) the step (append + attention), layers in rotation: events only at
+    # step boundaries, so the attention kernels may overlap the append
+    # kernel's tail (programmatic dependent launch).
     with ClockSampler(dev.index, enabled=not args.no_clocks) as clocks:
         dist.barrier()
         torch.cuda.synchronize(dev)
-        for s in range(args.steps):
-            flush.fill_(s & 0xff)        # evict the cache and KV from L2
-            g.qkv.copy_(qkv0)            # every step starts from the same rows
-            ev[s][0].record(stream)
-            append()
-            attend()
-            ev[s][1].record(stream)
+        step_ms = h.timed(h.step, args.steps, args.warmup, stream)
         torch.cuda.synchronize(dev)
         dist.barrier()
-    assert int(err.item()) == 0, f"device error bits {int(err.item())}"
-    step_ms = [ev[s][0].elapsed_time(ev[s][1]) for s in range(args.steps)]
-
-    # (B) the attention call alone (its kernels, on the launching stream), L2
-    # flushed before each: the roofline's kernel duration.  (C) the append.
-    def timed(fn, n):
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(n)]
-        for i in range(n):
-            flush.fill_(i & 0xff)
-            evs[i][0].record(stream)
-            fn()
-            evs[i][1].record(stream)
-        torch.cuda.synchronize(dev)
-        return [a.elapsed_time(b) for a, b in evs]
-    attn_ms = timed(attend, args.steps)
-    app_ms = timed(append, args.steps)
-    assert int(err.item()) == 0, f"device error bits {int(err.item())}"
+    # (B) the attention call alone: the roofline's kernel duration.  (C) the append.
+    attn_ms = h.timed(h.attend, args.steps, args.warmup, stream)
+    app_ms = h.timed(h.append, args.steps, args.warmup, stream)
     local_total_ms = sum(step_ms)
     total_ms = dist.max(local_total_ms)
     ms_per_step = total_ms / args.steps
 
     kv_bytes = w.kv_bytes_read()
-    qo_bytes = 2 * w.num_tokens * H * D * 2
-    all_kv = dist.sum(kv_bytes)
-    value = all_kv * args.steps / (total_ms * 1e-3) / 1e9
+    qo_bytes = h.qo_bytes()
+    value = dist.sum(kv_bytes) * args.steps / (total_ms * 1e-3) / 1e9
     seqs_per_s = dist.sum(w.num_seqs) * args.steps / (total_ms * 1e-3)
     tokens_per_s = dist.sum(w.num_tokens) * args.steps / (total_ms * 1e-3)
 
-    hbm_peak, tf_peak, peak_kind = measured_peaks()
     attn_avg_s = statistics.mean(attn_ms) * 1e-3
     result = {}
-    if prefix:
-        # HBM-bound on the distinct blocks: each is read from DRAM once
+    if h.prefix:
         alg = w.unique_kv_bytes() + qo_bytes
         achieved = alg / attn_avg_s / 1e9
         result["roofline"] = {"bound": "hbm",
@@ -373,16 +454,14 @@ def run_ours(args, dist: Dist):
                               "frac": round(achieved / hbm_peak, 4), "peak_kind": peak_kind,
                               "traffic": None, "algorithmic_bytes_per_launch": alg,
                               "logical_kv_bytes_per_launch": kv_bytes}
-    elif decode:
+    elif h.decode:
         alg = kv_bytes + qo_bytes
         achieved = alg / attn_avg_s / 1e9
-        if fp8 or Q.qattn_paged_decode_kernel(dims) == Q.QATTN_DECODE_TENSOR_CORE:
-            kname, src = "paged_decode_tc_kernel", "paged_decode_tc.cu"
-        else:
-            kname, src = "paged_decode_kernel", "paged_decode.cu"
-        sha = kernel_source_sha([src, "common.cuh", "internal.h"])
-        traffic = profiled_traffic(kname + ("_fp8" if fp8 else ""), args.workload, sha)
-        result["roofline"] = {"bound": "hbm", "kernel": kname,
+        kname = "paged_decode_tc_kernel"
+        sha = kernel_source_sha(["paged_decode_tc.cu", "decode_merge.cu", "common.cuh",
+                                 "internal.h"])
+        traffic = profiled_traffic(kname + ("_fp8" if h.fp8 else ""), args.workload, sha)
+        result["roofline"] = {"bound": "hbm", "kernel": kname + " + decode_merge_kernel",
                               "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                               "frac": round(achieved / hbm_peak, 4), "peak_kind": peak_kind,
                               "traffic": traffic, "algorithmic_bytes_per_launch": alg}
@@ -397,8 +476,17 @@ def run_ours(args, dist: Dist):
     # ---- end to end through the C ABI with host buffers ----
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, w, dims, g, table, ws, err, dev, decode, max_ctx, dist, prefix,
-                      (ks, vs) if fp8 else None)
+        e2e = run_e2e(args, h, dist, stream)
+    nlayers, kind, fp8 = h.nlayers, h.kind, h.fp8
+    h.free()
+    del h
+    torch.cuda.empty_cache()
+
+    # ---- the other workloads, same harness (rank 0 of a single-GPU run) ----
+    others = None
+    if not args.no_workloads and dist.world == 1 and args.workload == DEFAULT_WORKLOAD \
+            and args.kv == "bf16" and args.extras == "none" and args.block_size == 16:
+        others = run_other_workloads(args, dev, stream, hbm_peak, tf_peak, peak_kind)
 
     clk = clocks.summary()
     line = {
@@ -417,22 +505,22 @@ def run_ours(args, dist: Dist):
         "config": {"workload": args.workload, "num_heads": H, "num_kv_heads": Hkv,
                    "head_dim": D, "block_size": BS, "batch": w.num_seqs,
                    "new_tokens": w.num_tokens, "kv_bytes_per_step": kv_bytes,
-                   "max_context_len": max_ctx, "l2": "flushed before every timed step (512 MB write)",
+                   "max_context_len": w.max_context_len,
+                   "l2": (f"inputs larger than L2: {nlayers} layers of the workload's cache "
+                          "and QKV rows in rotation, consecutive steps read different layers"),
                    "append_extras": args.extras, "kv_cache_dtype": args.kv,
                    "parallelism": f"replicas x{dist.world}"},
         "seqs_per_s": round(seqs_per_s, 1),
         "tokens_per_s": round(tokens_per_s, 1),
         "append_ms": round(statistics.mean(app_ms), 5),
         "attention_ms": round(statistics.mean(attn_ms), 5),
-        # per step: RoPE + append, the decode kernel and its merge kernel
-        # (and, with prefill rows, the prefill kernel)
-        # (+1 for the FP8 gather of the prefill / prefix blocks)
-        "gpu_launches": ((4 if prefix else 3 if decode else 4) +
-                         (1 if fp8 and (prefix or not decode) else 0)) * args.steps,
+        "gpu_launches": (LAUNCHES["append"] + LAUNCHES[kind]) * args.steps,
         **result,
     }
     if e2e is not None:
         line["e2e"] = e2e
+    if others is not None:
+        line["workloads"] = others
     if clk is not None:
         line["clocks"] = clk
     if dist.rank == 0 and not args.no_cpu_baseline and dist.world == 1:
@@ -440,13 +528,71 @@ def run_ours(args, dist: Dist):
     return line
 
 
-def run_e2e(args, w, dims, g, table, ws, err, dev, decode, max_ctx, dist, prefix=0,
-            fp8_scales=None):
-    """Same step through the public API, inputs copied from pinned host memory
-    each step and the attention output read back."""
-    from paged_kv_gqa_07_gb300 import qattn as Q
+def run_other_workloads(args, dev, stream, hbm_peak, tf_peak, peak_kind):
+    """Every other configuration of the benchmark through the same harness:
+    the tiny Qwen3 decode (launch-bound), the mixed prefill + decode batch
+    (and its prefill part alone), the long-context decode, the shared-prefix
+    decode, and the FP8-cache b64 decode."""
+    res = {}
 
-    H, D = w.num_heads, w.head_dim
+    def measure(name, **kw):
+        h = Harness(args, name, dev, **kw)
+        attn = h.timed(h.attend, args.steps, args.warmup, stream)
+        if kw.get("sub_seqs") is None:
+            step = h.timed(h.step, args.steps, args.warmup, stream)
+        else:
+            step = attn
+        return h, attn, step
+
+    h, attn, step = measure("tiny_qwen3_decode")
+    d = decode_summary(h, attn, step, hbm_peak, peak_kind)
+    d["bound"] = "launch (4 sequences, 1.8 MB of KV): the fraction is not a roofline claim"
+    res["tiny_qwen3_decode"] = d
+    h.free()
+
+    h, attn, step = measure("qwen2_7b_long_decode")
+    res["qwen2_7b_long_decode"] = decode_summary(h, attn, step, hbm_peak, peak_kind)
+    h.free()
+
+    h, attn, step = measure("qwen3_prefix_decode")
+    res["qwen3_prefix_decode"] = decode_summary(h, attn, step, hbm_peak, peak_kind)
+    h.free()
+
+    h, attn, step = measure("qwen2_7b_decode_b64", kv="fp8")
+    d = decode_summary(h, attn, step, hbm_peak, peak_kind)
+    d["kv_cache_dtype"] = "fp8 (e4m3 codes, 1 byte per value)"
+    res["qwen2_7b_decode_b64_fp8"] = d
+    h.free()
+
+    # the mixed batch: one varlen call (4 prefill chunks + 60 decode rows)
+    h, attn, step = measure("qwen2_7b_mixed_varlen")
+    w = h.w
+    a, s = statistics.median(attn) * 1e-3, statistics.median(step) * 1e-3
+    flops = 4 * w.head_dim * w.causal_pairs()
+    mixed = {"attention_us": round(a * 1e6, 2), "step_us": round(s * 1e6, 2),
+             "new_tokens": w.num_tokens, "tokens_per_s": round(w.num_tokens / s, 1),
+             "causal_flops": flops, "call_TFLOPs": round(flops / a / 1e12, 2)}
+    h.free()
+    # its prefill part alone (the 4 chunks, no decode rows): the prefill kernel
+    h, attn, _ = measure("qwen2_7b_mixed_varlen", sub_seqs=4)
+    w = h.w
+    k3 = statistics.median(attn) * 1e-3
+    pf = 4 * w.head_dim * w.causal_pairs()
+    mixed.update(prefill_only_us=round(k3 * 1e6, 2), prefill_tokens=w.num_tokens,
+                 prefill_tokens_per_s=round(w.num_tokens / k3, 1),
+                 prefill_TFLOPs=round(pf / k3 / 1e12, 2),
+                 prefill_frac=round(pf / k3 / 1e12 / tf_peak, 4), peak_kind=peak_kind,
+                 prefill_bound="tensor (bf16 dense peak)")
+    res["qwen2_7b_mixed_varlen"] = mixed
+    h.free()
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_e2e(args, h: Harness, dist, stream):
+    """The same step through the public API, its inputs copied from pinned
+    host memory every step and the attention output read back."""
+    w, dev = h.w, h.dev
     # The step's host inputs packed into one pinned buffer (256-byte aligned
     # segments): one host->device copy per step, the device tensors are views.
     names = ("qkv", "positions", "slot_mapping", "block_tables", "context_lens", "cu_seqlens_q")
@@ -462,77 +608,32 @@ def run_e2e(args, w, dims, g, table, ws, err, dev, decode, max_ctx, dist, prefix
         n = t.numel() * t.element_size()
         host_buf[offs[k]:offs[k] + n].copy_(t.view(-1).view(torch.uint8))
         dev_in[k] = dev_buf[offs[k]:offs[k] + n].view(t.dtype).view(t.shape)
-    out = torch.empty((w.num_tokens, H, D), dtype=torch.bfloat16, device=dev)
+    out = torch.empty_like(h.out)
     host_out = torch.empty_like(out, device="cpu").pin_memory()
-    stream = torch.cuda.current_stream(dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    Hkv = w.num_kv_heads
 
-    def step():
+    def step(l):
         dev_buf.copy_(host_buf, non_blocking=True)
-        qkv = dev_in["qkv"]
-        if fp8_scales is not None:
-            Q.qattn_rope_cache_append_fp8(qkv[:, :H * D], qkv[:, H * D:(H + Hkv) * D],
-                                          qkv[:, (H + Hkv) * D:], dev_in["positions"],
-                                          dev_in["slot_mapping"], g.k_cache, g.v_cache, table,
-                                          *fp8_scales, dims, err_word=err)
-            if prefix:
-                Q.qattn_paged_decode_shared_prefix_fp8(
-                    out, qkv[:, :H * D], g.k_cache, g.v_cache, dev_in["block_tables"],
-                    dev_in["context_lens"], max_ctx, prefix, *fp8_scales, dims, ws, err)
-            elif decode:
-                Q.qattn_paged_decode_fp8(out, qkv[:, :H * D], g.k_cache, g.v_cache,
-                                         dev_in["block_tables"], dev_in["context_lens"], max_ctx,
-                                         *fp8_scales, dims, ws, err)
-            else:
-                n_prefill = sum(1 for n in w.q_lens if n >= 2)
-                Q.qattn_varlen_prefill_fp8(out, qkv[:, :H * D], dev_in["cu_seqlens_q"],
-                                           w.max_q_len, g.k_cache, g.v_cache,
-                                           dev_in["block_tables"], dev_in["context_lens"],
-                                           max_ctx, n_prefill, *fp8_scales, dims, ws, err)
-            host_out.copy_(out, non_blocking=True)
-            return
-        Q.qattn_rope_cache_append(qkv[:, :H * D], qkv[:, H * D:(H + Hkv) * D],
-                                  qkv[:, (H + Hkv) * D:], dev_in["positions"],
-                                  dev_in["slot_mapping"], g.k_cache, g.v_cache, table, dims, err)
-        if prefix:
-            Q.qattn_paged_decode_shared_prefix(out, qkv[:, :H * D], g.k_cache, g.v_cache,
-                                               dev_in["block_tables"], dev_in["context_lens"],
-                                               max_ctx, prefix, dims, ws, err)
-        elif decode:
-            Q.qattn_paged_decode(out, qkv[:, :H * D], g.k_cache, g.v_cache, dev_in["block_tables"],
-                                 dev_in["context_lens"], max_ctx, dims, ws, err)
-        else:
-            Q.qattn_varlen_prefill(out, qkv[:, :H * D], dev_in["cu_seqlens_q"], w.max_q_len,
-                                   g.k_cache, g.v_cache, dev_in["block_tables"],
-                                   dev_in["context_lens"], max_ctx, dims, ws, err)
+        h.append(l, qkv=dev_in["qkv"], positions=dev_in["positions"],
+                 slots=dev_in["slot_mapping"])
+        h.attend(l, qkv=dev_in["qkv"], block_tables=dev_in["block_tables"],
+                 context_lens=dev_in["context_lens"], cu=dev_in["cu_seqlens_q"], out=out)
         host_out.copy_(out, non_blocking=True)
 
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize(dev)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
     dist.barrier()
-    for s in range(args.steps):
-        flush.fill_(s & 0xff)
-        evs[s][0].record(stream)
-        step()
-        evs[s][1].record(stream)
-    torch.cuda.synchronize(dev)
+    ms = h.timed(step, args.steps, args.warmup, stream)
     dist.barrier()
-    total_ms = dist.max(sum(a.elapsed_time(b) for a, b in evs))
-    h2d = total
+    total_ms = dist.max(sum(ms))
     d2h = host_out.numel() * host_out.element_size()
     value = dist.sum(w.kv_bytes_read()) * args.steps / (total_ms * 1e-3) / 1e9
-    return {"value": round(value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+    return {"value": round(value, 2), "unit": "GB/s", "h2d_bytes_per_step": total,
             "d2h_bytes_per_step": d2h, "ms_per_step": round(total_ms / args.steps, 5)}
 
 
 # --------------------------------------------------------------- oracle --
 
-def oracle_sample(w: W.Workload, n_seqs: int):
-    """The first n_seqs sequences of the workload as a smaller workload."""
+def first_sequences(w: W.Workload, n_seqs: int):
+    """The first n_seqs sequences of the workload as a smaller workload
+    (input slicing only)."""
     q_lens = w.q_lens[:n_seqs]
     T = sum(q_lens)
     sub = dict(w.__dict__)
@@ -550,7 +651,7 @@ def oracle_time(w: W.Workload, n_seqs: int, reps: int = 1):
 
     import oracle
 
-    s = oracle_sample(w, n_seqs)
+    s = first_sequences(w, n_seqs)
     H, Hkv, D, BS = s.num_heads, s.num_kv_heads, s.head_dim, s.block_size
     table = oracle.rope_table(s.theta, s.max_pos, D)
 
