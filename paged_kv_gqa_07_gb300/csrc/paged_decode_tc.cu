@@ -33,7 +33,11 @@
 //     rings; one thread of warp 5 issues the Q K^T MMAs and one of warp 6
 //     the P V MMAs (two issuers: each MMA issue waits on the pipe); warps 0-3
 //     (thread = token for S, thread = dimension for O) run the softmax and
-//     write P^T as bf16 into swizzled shared memory.
+//     write P^T as bf16 into swizzled shared memory; four epilogue warps (7-10,
+//     FP8 11-14) finish each unit: O^T / l into the output, or the CTA's part
+//     of a straddling unit (measured: done by the softmax warps, each unit's
+//     epilogue took ~1.4 us of their time, and runs holding many short units
+//     fell behind the others).
 //   * O is rescaled lazily (only when a head's max grows by more than 2^8).
 //   * keys past the context are masked in S and their V rows zeroed.
 //   * every wait is bounded; on a timeout all roles unwind, drain their
@@ -64,6 +68,8 @@ constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;     // issues the Q K^T stream (and owns TMEM)
 constexpr int kPvWarp = 6;      // issues the P V stream
 constexpr int kConvWarp0 = 7;   // FP8 only: warps 7-10 dequantise
+// The four epilogue warps (7-10 for bf16, 11-14 for FP8) cover the four
+// tensor-memory lane quarters between them.
 // A tile of 128 tokens lands as 8-token row groups 2 KB apart whatever the
 // block size (a block's box is block_size / 8 such groups), so the code below
 // addresses it in 16-token / 4 KB units.
@@ -80,7 +86,8 @@ constexpr int kMaxSmemSeqs = 2048;
 // 4 + 4 slots of 16 KB code tiles, then two 32 KB f16 V tiles.
 template <bool kFp8>
 struct Lay {
-  static constexpr int kWarps = kFp8 ? 11 : 7;
+  static constexpr int kWarps = kFp8 ? 15 : 11;
+  static constexpr int kEpiWarp0 = kFp8 ? 11 : 7;
   static constexpr int kThreads = kWarps * 32;
   static constexpr int kKStages = kFp8 ? 4 : 3;
   static constexpr int kVStages = kFp8 ? 4 : 3;
@@ -91,14 +98,15 @@ struct Lay {
   static constexpr int kOffQ = kOffVc + (kFp8 ? 2 * kTileBytes : 0);  // 2 slots of Q^T
   static constexpr int kOffP = kOffQ + 2 * kSmallBytes;               // 2 buffers of P^T
   static constexpr int kOffRed = kOffP + 2 * kSmallBytes;             // [2][4][16] fp32
-  static constexpr int kOffLsum = kOffRed + 2 * 4 * kN * 4;           // [2][4][16] fp32
-  static constexpr int kOffBars = kOffLsum + 2 * 4 * kN * 4;
+  static constexpr int kOffEpiL = kOffRed + 2 * 4 * kN * 4;           // [2][4][16] fp32
+  static constexpr int kOffEpiM = kOffEpiL + 2 * 4 * kN * 4;          // [2][16] fp32
+  static constexpr int kOffBars = kOffEpiM + 2 * kN * 4;
   // k_full/k_empty[kKStages] v_full/v_empty[kVStages] q_full q_empty s_full
-  // s_free p_full pv_done o_free [2] rbar mma_done; FP8 adds kc_full
-  // kc_empty vc_full vc_empty qc_full [2]
-  static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 * 7 + 2 + (kFp8 ? 10 : 0);
+  // s_free p_full pv_done o_free epi_full epi_empty seg_done [2] rbar
+  // mma_done; FP8 adds kc_full kc_empty vc_full vc_empty qc_full [2]
+  static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 * 10 + 2 + (kFp8 ? 10 : 0);
   static constexpr int kOffMisc = kOffBars + kNumBars * 8;
-  static constexpr int kOffLens = kOffMisc + 64;
+  static constexpr int kOffLens = kOffMisc + 128;  // Misc
   static constexpr int kSmemBytes = kOffLens + kMaxSmemSeqs * 4 + 1024;
   static constexpr uint32_t kTmemCols = kFp8 ? 256 : 64;
 };
@@ -110,8 +118,9 @@ struct Misc {
   int abort;
   int b0;
   int off0;
-  int warp_sums[12];
+  int warp_sums[16];
 };
+static_assert(sizeof(Misc) <= 128, "Misc overlaps the context lengths");
 
 __device__ __forceinline__ int seq_len_eff(const DecodeArgs& a, int b) {
   return decode_len_eff(a, b);
@@ -213,7 +222,13 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
   uint64_t* pv_done = p_full + 2;
   // o_free[b]: the softmax has read O^T slot b (units of parity b).
   uint64_t* o_free = pv_done + 2;
-  uint64_t* rbar = o_free + 2;
+  // epi_full[s] / epi_empty[s]: the softmax has handed segment k's maximum
+  // and row sums (k & 1 == s) to the epilogue warps / they have read them;
+  // seg_done[s]: segment k's last P V is complete (its O^T is final).
+  uint64_t* epi_full = o_free + 2;
+  uint64_t* epi_empty = epi_full + 2;
+  uint64_t* seg_done = epi_empty + 2;
+  uint64_t* rbar = seg_done + 2;
   uint64_t* mma_done = rbar + 1;
   // FP8: kc_full[b] / vc_full[b] -- the converters have written K of tile n
   // into TMEM / V of tile n as f16 (tiles of parity b); kc_empty / vc_empty
@@ -226,7 +241,8 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
   Misc* misc = reinterpret_cast<Misc*>(smem + L::kOffMisc);
   int* s_len = reinterpret_cast<int*>(smem + L::kOffLens);
   float* red = reinterpret_cast<float*>(smem + L::kOffRed);
-  float* lsum = reinterpret_cast<float*>(smem + L::kOffLsum);
+  float* epi_l = reinterpret_cast<float*>(smem + L::kOffEpiL);
+  float* epi_m = reinterpret_cast<float*>(smem + L::kOffEpiM);
   volatile int* abort_flag = &misc->abort;
   const uint32_t sbase = smem_u32(smem);
 
@@ -304,8 +320,12 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
       mbar_init(&p_full[s], 4);
       mbar_init(&pv_done[s], 1);
     }
-    mbar_init(&o_free[0], 4);
-    mbar_init(&o_free[1], 4);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&o_free[s], 4);     // the four epilogue warps
+      mbar_init(&epi_full[s], 4);   // the four softmax warps
+      mbar_init(&epi_empty[s], 4);  // the four epilogue warps
+      mbar_init(&seg_done[s], 1);   // the P V thread's commit
+    }
     mbar_init(rbar, 4);
     mbar_init(mma_done, 2);  // one commit per MMA-issuing thread
     fence_barrier_init();
@@ -497,6 +517,7 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
         while (pn < nloc && ok) {
           bool progressed = false;
           const bool first = (pn == 0) || (pw.i == 0);
+          const bool last = (pn == nloc - 1) || (pw.i == pw.nt - 1);
           const int seg_j = pseg + (first ? 1 : 0);
           const int pb = pn & 1;
           bool ready = mbar_test(&p_full[pb], (pn >> 1) & 1) &&
@@ -524,6 +545,7 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
             }
             mma_commit(&pv_done[pb]);
             mma_commit(kFp8 ? &vc_empty[pn & 1] : &v_empty[pn % kVStages]);
+            if (last) mma_commit(&seg_done[seg_j & 1]);
             if (first) pseg = seg_j;
             ++pn;
             walk_next(pw, a, s_len);
@@ -580,6 +602,86 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
       mbar_wait_drain(mma_done, 0, a.drain_ns);
     }
     __syncwarp();
+  } else if (warp >= L::kEpiWarp0) {
+    // ============================== epilogue ================================
+    // Thread = dimension row d of O^T (warp w reads TMEM lanes 32 (w % 4) ..
+    // 32 (w % 4) + 31).  For each segment (a unit's tiles in this CTA's run):
+    // wait for the softmax's maximum and row sums and for the segment's last
+    // P V, read O^T, release its TMEM slot, and write out = O / l -- or, when
+    // the unit straddles CTAs, this CTA's normalised part and its log2-sum-exp
+    // for the merge kernel.  Off the softmax warps, a unit boundary costs the
+    // softmax only its row-sum hand-over.
+    const int d = ((warp & 3) << 5) | lane;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    bool ok = true;
+    Walk ew = w0;
+    int seg = -1;
+    for (int j = 0; j < nloc && ok; ++j) {
+      const bool first = (j == 0) || (ew.i == 0);
+      const bool last = (j == nloc - 1) || (ew.i == ew.nt - 1);
+      if (first) ++seg;
+      if (last) {
+        const int es = seg & 1;
+        bool w_ok = mbar_wait(&epi_full[es], (seg >> 1) & 1, abort_flag, a.wait_ns);
+        if (w_ok) w_ok = mbar_wait(&seg_done[es], (seg >> 1) & 1, abort_flag, a.wait_ns);
+        if (!__all_sync(0xffffffffu, w_ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        float o[kN];
+        tmem_ld16(lane_addr + kColO + es * kN, o);
+        float ltot[G], mu[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float* el = epi_l + es * 4 * kN + h;
+          ltot[h] = (el[0 * kN] + el[1 * kN]) + (el[2 * kN] + el[3 * kN]);
+          mu[h] = epi_m[es * kN + h];
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&o_free[es]);
+          mbar_arrive(&epi_empty[es]);
+        }
+        const int u0 = c0 + j - ew.i;  // list index of the unit's first tile
+        const int first_cta = split.cta_of(u0), last_cta = split.cta_of(u0 + ew.nt - 1);
+        const int nparts = last_cta - first_cta + 1;
+        const int part = static_cast<int>(blockIdx.x) - first_cta;
+        const int64_t row = q_row_of(a, ew.b);
+        const int64_t seg_id = static_cast<int64_t>(ew.b) * Hkv + ew.g;
+        const bool fits = a.part_base + nparts <= a.ws.max_parts;
+        // O / l, times v_scale for an FP8 cache
+        auto out_val = [&](float ov, float l) -> float {
+          if constexpr (kFp8)
+            return (ov / l) * a.v_scale;
+          else
+            return ov / l;
+        };
+        if (nparts == 1 && a.part_base == 0) {
+          __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) +
+                                (row * a.num_heads + static_cast<int64_t>(ew.g) * G) * kHeadDim;
+#pragma unroll
+          for (int h = 0; h < G; ++h)
+            orow[h * kHeadDim + d] = __float2bfloat16_rn(out_val(o[h], ltot[h]));
+        } else if (fits) {
+          const int64_t pidx = seg_id * a.ws.max_parts + a.part_base + part;
+#pragma unroll
+          for (int h = 0; h < G; ++h)
+            a.ws.part_o[(pidx * G + h) * kHeadDim + d] = out_val(o[h], ltot[h]);
+          if (d < G) {
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+              if (h == d) a.ws.lse[pidx * G + h] = mu[h] + log2f(ltot[h]);
+          }
+        } else if (d == 0) {
+          set_err(a.err_word, QATTN_DEVERR_CONTEXT);
+        }
+        if (part == 0 && d == 0) record_parts(a, seg_id, fits ? a.part_base + nparts : 0);
+      }
+      walk_next(ew, a, s_len);
+    }
+    if (!ok && lane == 0) set_err(a.err_word, QATTN_DEVERR_TIMEOUT);
   } else if (kFp8 && warp >= kConvWarp0) {
     // ============================ FP8 converters =============================
     // Thread = token row r of a tile (warp w owns TMEM lanes 32 (w % 4) ..).
@@ -682,69 +784,13 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
     const int t = tid;  // token row of S^T / dimension row of O^T = TMEM lane
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     float m_used[G], l_t[G];
-    // A unit's epilogue (its last P V, O^T / l, output or partial) waits on
-    // that P V, so it is deferred by one tile: the next unit's first tile
-    // is scored and its P^T handed over first.  Its row sums travel with
-    // that tile's max exchange; its O^T stays in its own TMEM slot.
-    float m_pend[G], l_pend[G];
-    bool pend = false;
-    int pend_seg = 0;
-    Walk pend_w = w0;
     int rphase = 0;
     // PV(j) completes phase j >> 1 of pv_done[j & 1].  Tile n always waits
     // for PV(n-2) (P^T buffer reuse), so when it later waits for PV(n-1)
-    // (rescale, deferred epilogue) or PV(n) (last tile) neither barrier is
-    // two phases behind -- the condition a parity wait needs.
+    // (rescale) neither barrier is two phases behind -- the condition a
+    // parity wait needs.
     auto wait_pv = [&](int j) -> bool {
       return __all_sync(0xffffffffu, mbar_wait(&pv_done[j & 1], (j >> 1) & 1, abort_flag, a.wait_ns));
-    };
-    // Epilogue of unit `useg` whose last tile here is j (walk state uw):
-    // out = O^T / l, or this CTA's part of a unit that straddles CTAs.
-    // O / l, times v_scale for an FP8 cache.
-    auto out_val = [&](float o, float l) -> float {
-      if constexpr (kFp8)
-        return (o / l) * a.v_scale;
-      else
-        return o / l;
-    };
-    // pv_waited: PV(j) was already waited for in this step (a later PV may
-    // have completed since, so a second parity wait could be two phases
-    // behind).
-    auto finish = [&](const Walk& uw, int j, int useg, const float* mu, const float* ltot,
-                      bool pv_waited) -> bool {
-      if (!pv_waited && !wait_pv(j)) return false;
-      tc_fence_after();
-      float o[kN];
-      tmem_ld16(lane_addr + kColO + (useg & 1) * kN, o);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&o_free[useg & 1]);
-      const int u0 = c0 + j - uw.i;  // list index of the unit's first tile
-      const int first = split.cta_of(u0), last = split.cta_of(u0 + uw.nt - 1);
-      const int nparts = last - first + 1;
-      const int part = static_cast<int>(blockIdx.x) - first;
-      const int64_t row = q_row_of(a, uw.b);
-      const int64_t seg_id = static_cast<int64_t>(uw.b) * Hkv + uw.g;
-      const bool fits = a.part_base + nparts <= a.ws.max_parts;
-      if (nparts == 1 && a.part_base == 0) {
-        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) +
-                              (row * a.num_heads + static_cast<int64_t>(uw.g) * G) * kHeadDim;
-#pragma unroll
-        for (int h = 0; h < G; ++h) orow[h * kHeadDim + t] = __float2bfloat16_rn(out_val(o[h], ltot[h]));
-      } else if (fits) {
-        const int64_t pidx = seg_id * a.ws.max_parts + a.part_base + part;
-#pragma unroll
-        for (int h = 0; h < G; ++h) a.ws.part_o[(pidx * G + h) * kHeadDim + t] = out_val(o[h], ltot[h]);
-        if (t < G) {
-#pragma unroll
-          for (int h = 0; h < G; ++h)
-            if (h == t) a.ws.lse[pidx * G + h] = mu[h] + log2f(ltot[h]);
-        }
-      } else if (t == 0) {
-        set_err(a.err_word, QATTN_DEVERR_CONTEXT);
-      }
-      if (part == 0 && t == 0) record_parts(a, seg_id, fits ? a.part_base + nparts : 0);
-      return true;
     };
     bool ok = true;
     Walk sw = w0;
@@ -794,23 +840,14 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
       if (lane == 0)
         for (int j = 0; j < cnt; ++j) mbar_arrive(&s_free[(n + j) & 1]);
 
-      // per-head max over the step's tokens: shuffle tree, then 4 warps;
-      // the deferred unit's row sums ride along.
+      // per-head max over the step's tokens: shuffle tree, then 4 warps
       float* rd = red + (rphase & 1) * 4 * kN;
-      float* ls = lsum + (rphase & 1) * 4 * kN;
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         s[0][h] = t < nv0 ? s[0][h] * a.scale_log2 : -INFINITY;
         s[1][h] = t < nv1 ? s[1][h] * a.scale_log2 : -INFINITY;
         const float wm = warp_max(fmaxf(s[0][h], s[1][h]));
         if (lane == 0) rd[warp * kN + h] = wm;
-      }
-      if (pend) {
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float ws = warp_sum(l_pend[h]);
-          if (lane == 0) ls[warp * kN + h] = ws;
-        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(rbar);
@@ -914,51 +951,28 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
       if (lane == 0)
         for (int j = 0; j < cnt; ++j) mbar_arrive(&p_full[(n + j) & 1]);
 
-      if (pend) {
-        // the previous unit ended at tile n-1 (waited for above in a
-        // two-tile step)
-        float ltot[G];
-#pragma unroll
-        for (int h = 0; h < G; ++h)
-          ltot[h] = (ls[0 * kN + h] + ls[1 * kN + h]) + (ls[2 * kN + h] + ls[3 * kN + h]);
-        if (!finish(pend_w, n - 1, pend_seg, m_pend, ltot, cnt == 2)) {
+      if (seg_end) {
+        // Hand the segment's per-head maximum and the four warps' row sums
+        // to the epilogue warps (its O^T / l and the output or part are
+        // theirs), once they have taken the segment two before out of this
+        // slot.
+        const int es = seg & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(&epi_empty[es], ((seg >> 1) & 1) ^ 1, abort_flag,
+                                               a.wait_ns))) {
           ok = false;
           break;
         }
-        pend = false;
-      }
-      if (seg_end && nl < nloc - 1) {
-        pend = true;
-        pend_seg = seg;
-        pend_w = lw;
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          m_pend[h] = m_used[h];
-          l_pend[h] = l_t[h];
-        }
-      } else if (seg_end) {
-        // the run's last tile: its own row-sum exchange, then the epilogue
-        float* ls2 = lsum + (rphase & 1) * 4 * kN;
 #pragma unroll
         for (int h = 0; h < G; ++h) {
           const float ws = warp_sum(l_t[h]);
-          if (lane == 0) ls2[warp * kN + h] = ws;
+          if (lane == 0) epi_l[(es * 4 + warp) * kN + h] = ws;
+        }
+        if (warp == 0 && lane == 0) {
+#pragma unroll
+          for (int h = 0; h < G; ++h) epi_m[es * kN + h] = m_used[h];
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(rbar);
-        if (!__all_sync(0xffffffffu, mbar_wait(rbar, rphase & 1, abort_flag, a.wait_ns))) {
-          ok = false;
-          break;
-        }
-        ++rphase;
-        float ltot[G];
-#pragma unroll
-        for (int h = 0; h < G; ++h)
-          ltot[h] = (ls2[0 * kN + h] + ls2[1 * kN + h]) + (ls2[2 * kN + h] + ls2[3 * kN + h]);
-        if (!finish(lw, nl, seg, m_used, ltot, false)) {
-          ok = false;
-          break;
-        }
+        if (lane == 0) mbar_arrive(&epi_full[es]);
       }
       n += cnt;
       for (int j = 0; j < cnt; ++j) walk_next(sw, a, s_len);
