@@ -533,6 +533,19 @@ __device__ __forceinline__ void tma_load_cache_tile(void* smem_dst, const CUtens
       : "memory");
 }
 
+// The same load with an L2 cache-policy hint (e.g. evict-first for data
+// streamed once, so that it does not push out what is read again soon).
+__device__ __forceinline__ void tma_load_cache_tile_hint(void* smem_dst, const CUtensorMap* map,
+                                                         int32_t tile, int32_t groups,
+                                                         uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::"
+      "cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(0), "r"(0), "r"(tile * groups),
+      "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
 // Byte offset, inside a cache tile in shared memory, of 16-byte chunk
 // `chunk` (0..15 along the 128 dims) of row `r` (0..15): the layout is
 // [row group][column half][8 rows][128 B], 128-byte swizzled.

@@ -15,48 +15,36 @@
 namespace qattn {
 namespace {
 
-// K2r: merge the parts of units that straddled CTAs.  One CTA of four
-// warps per (sequence, kv head, query head of the group); lane = 4
-// dimensions.
-//   out[row, g*G + h] = sum_p 2^(lse_p - M) o_p / sum_p 2^(lse_p - M).
-// A unit of up to kMergeBatch parts is folded by warp 0 alone, its parts
-// loaded together with the part count (their addresses do not depend on
-// it): one memory round trip.  Longer part lists (a long sequence spread
-// over many CTAs) are cut into four consecutive ranges,
-// one per warp, each folded in part order, kMergeBatch loads in flight; the
-// four partial states are then combined in warp order through shared
-// memory.  The order is fixed, so results are deterministic.
+// K2r: merge the parts of units that straddled CTAs.  One CTA per
+// (sequence, kv head) unit, one warp per query head of its group, lane = 4
+// dimensions:
+//   out[row, g*G + h] = sum_p 2^(lse_p - M) o_p / sum_p 2^(lse_p - M),
+// folded in part order with a running maximum M (deterministic).  The first
+// two parts are loaded with the part count, the rest kMergeBatch at a time.  The CTAs are small enough to become resident beside
+// the decode kernel's (the launch is a programmatic dependent one) and wait
+// there for its grid to finish.
 constexpr int kMergeBatch = 8;
-constexpr int kMergeWarps = 4;
 
-struct FoldState {
-  float m, den;
-  float4 num;
-};
-
-__device__ __forceinline__ void fold_one(FoldState& st, float lse, const float4& o) {
-  const float mn = fmaxf(st.m, lse);
-  const float sc = exp2f(st.m - mn);  // 0 for the first part
+__device__ __forceinline__ void fold_one(float& m, float& den, float4& num, float lse,
+                                         const float4& o) {
+  const float mn = fmaxf(m, lse);
+  const float sc = exp2f(m - mn);  // 0 for the first part
   const float f = exp2f(lse - mn);
-  st.den = fmaf(st.den, sc, f);
-  st.num.x = fmaf(st.num.x, sc, f * o.x);
-  st.num.y = fmaf(st.num.y, sc, f * o.y);
-  st.num.z = fmaf(st.num.z, sc, f * o.z);
-  st.num.w = fmaf(st.num.w, sc, f * o.w);
-  st.m = mn;
+  den = fmaf(den, sc, f);
+  num.x = fmaf(num.x, sc, f * o.x);
+  num.y = fmaf(num.y, sc, f * o.y);
+  num.z = fmaf(num.z, sc, f * o.z);
+  num.w = fmaf(num.w, sc, f * o.w);
+  m = mn;
 }
 
 template <int G>
-__global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const DecodeArgs a) {
-  __shared__ float s_m[kMergeWarps], s_den[kMergeWarps];
-  __shared__ float4 s_num[kMergeWarps][32];
+__global__ void __launch_bounds__(G * 32) decode_merge_kernel(const DecodeArgs a) {
   grid_dep_wait();  // the parts come from the decode grid
   const int Hkv = a.num_kv_heads;
-  const int64_t wid = blockIdx.x;
-  const int h = static_cast<int>(wid % G);
-  const int64_t seg = wid / G;
+  const int64_t seg = blockIdx.x;
   const int b = static_cast<int>(seg / Hkv), g = static_cast<int>(seg % Hkv);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t pbase = seg * a.ws.max_parts * G + h;  // part p at pbase + p * G
   const float* lse = a.ws.lse + pbase;
   const float* po = a.ws.part_o + pbase * kHeadDim + lane * 4;
@@ -66,12 +54,11 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const De
   };
   float lv[kMergeBatch];
   float4 ov[kMergeBatch];
-  if (warp == 0) {
-#pragma unroll
-    for (int j = 0; j < kMergeBatch; ++j)
-      if (j < a.ws.max_parts) load(j, lv[j], ov[j]);  // inside this unit's part slots
-  }
-  // The count comes from the decode kernel; a unit whose first piece was
+  // The first two parts (most units have at most two) are loaded with the
+  // count; their slots exist whatever the count (max_parts >= 2).
+  load(0, lv[0], ov[0]);
+  load(1, lv[1], ov[1]);
+  // The count comes from the decode kernel; a unit whose first part was
   // never finished (a CTA that gave up after a timeout) leaves whatever the
   // workspace held, so it is clamped to the unit's part slots: the output
   // of such a call is unspecified, but nothing is read out of bounds.
@@ -83,65 +70,36 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const De
     ql = a.cu_seqlens_q[b + 1] - static_cast<int>(row);
   }
   if (ql != 1 || nparts <= 1) return;  // not a decode row, or written by the decode kernel
-  const bool split = nparts > kMergeBatch;
-  const int per = split ? (nparts + kMergeWarps - 1) / kMergeWarps : nparts;
-  const int p_begin = warp * per;
-  const int p_end = min(nparts, p_begin + per);
-  FoldState st{-INFINITY, 0.f, make_float4(0.f, 0.f, 0.f, 0.f)};
-  if (warp == 0 || split) {
-    for (int p0 = p_begin; p0 < p_end; p0 += kMergeBatch) {
-      if (!(warp == 0 && p0 == 0)) {  // warp 0's first batch is already loaded
+  float m = -INFINITY, den = 0.f;
+  float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+  // parts 2 .. kMergeBatch - 1 of the first batch, then whole batches
 #pragma unroll
-        for (int j = 0; j < kMergeBatch; ++j)
-          if (p0 + j < p_end) load(p0 + j, lv[j], ov[j]);
-      }
+  for (int j = 2; j < kMergeBatch; ++j)
+    if (j < nparts) load(j, lv[j], ov[j]);
+  for (int p0 = 0;;) {
 #pragma unroll
-      for (int j = 0; j < kMergeBatch; ++j)
-        if (p0 + j < p_end) fold_one(st, lv[j], ov[j]);
-    }
-  }
-  if (split) {
-    if (lane == 0) {
-      s_m[warp] = st.m;
-      s_den[warp] = st.den;
-    }
-    s_num[warp][lane] = st.num;
-    __syncthreads();
-    if (warp != 0) return;
-    // warp 0 holds range 0; fold ranges 1..3 in order, each as a part of
-    // log2-weight m + log2(den) and value num / den
+    for (int j = 0; j < kMergeBatch; ++j)
+      if (p0 + j < nparts) fold_one(m, den, num, lv[j], ov[j]);
+    p0 += kMergeBatch;
+    if (p0 >= nparts) break;
 #pragma unroll
-    for (int w = 1; w < kMergeWarps; ++w) {
-      const float m = s_m[w], den = s_den[w];
-      if (den > 0.f) {
-        const float4 n = s_num[w][lane];
-        const float mn = fmaxf(st.m, m);
-        const float sa = exp2f(st.m - mn), sb = exp2f(m - mn);
-        st.den = st.den * sa + den * sb;
-        st.num.x = st.num.x * sa + n.x * sb;
-        st.num.y = st.num.y * sa + n.y * sb;
-        st.num.z = st.num.z * sa + n.z * sb;
-        st.num.w = st.num.w * sa + n.w * sb;
-        st.m = mn;
-      }
-    }
-  } else if (warp != 0) {
-    return;
+    for (int j = 0; j < kMergeBatch; ++j)
+      if (p0 + j < nparts) load(p0 + j, lv[j], ov[j]);
   }
   __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) +
                         (row * a.num_heads + static_cast<int64_t>(g) * G + h) * kHeadDim + lane * 4;
-  const float inv = 1.f / st.den;
+  const float inv = 1.f / den;
   uint2 packed;
-  packed.x = pack_bf16x2_rn(st.num.x * inv, st.num.y * inv);
-  packed.y = pack_bf16x2_rn(st.num.z * inv, st.num.w * inv);
+  packed.x = pack_bf16x2_rn(num.x * inv, num.y * inv);
+  packed.y = pack_bf16x2_rn(num.z * inv, num.w * inv);
   *reinterpret_cast<uint2*>(orow) = packed;
 }
 
 template <int G>
 cudaError_t launch_merge_g(const DecodeArgs& a, cudaStream_t stream) {
-  const int64_t ctas = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads * G;
-  cudaError_t e = launch_pdl(decode_merge_kernel<G>, dim3(static_cast<unsigned>(ctas)),
-                             dim3(kMergeWarps * 32), 0, stream, a);
+  const int64_t units = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads;
+  cudaError_t e = launch_pdl(decode_merge_kernel<G>, dim3(static_cast<unsigned>(units)),
+                             dim3(G * 32), 0, stream, a);
   if (e != cudaSuccess) return e;
   return cudaPeekAtLastError();
 }

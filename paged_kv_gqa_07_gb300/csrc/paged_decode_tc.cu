@@ -363,6 +363,10 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
     // V lands about when P V needs it instead of idling in its ring slot
     // while the softmax runs, and at start-up the first K tiles are served
     // ahead of the V burst.
+    // The KV tiles are read once: evict-first in L2, so that they do not
+    // push out the parts the merge kernel reads back, the query rows and
+    // the block tables.
+    const uint64_t kv_policy = policy_evict_first();
     int n = 0, seg = -1, nv = 0;
     int prev_id = -1, prev_g = 0;
     uint32_t prev_nvalid = 0;
@@ -379,9 +383,9 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
       if (lane < bpt && id_lane >= 0) {
         uint8_t* dst = smem + L::kOffV + vs * L::kStageBytes + lane * blk_bytes;
         if constexpr (kFp8)
-          tma_load_2d(dst, &vmap, 0, (id_lane * Hkv + gg) * a.block_size, &v_full[vs]);
+          tma_load_2d_hint(dst, &vmap, 0, (id_lane * Hkv + gg) * a.block_size, &v_full[vs], kv_policy);
         else
-          tma_load_cache_tile(dst, &vmap, id_lane * Hkv + gg, groups, &v_full[vs]);
+          tma_load_cache_tile_hint(dst, &vmap, id_lane * Hkv + gg, groups, &v_full[vs], kv_policy);
       }
       ++nv;
       return true;
@@ -453,9 +457,9 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
         if (lane < bpt && myid >= 0 && !skip) {
           uint8_t* dst = smem + L::kOffK + ks * L::kStageBytes + lane * blk_bytes;
           if constexpr (kFp8)
-            tma_load_2d(dst, &kmap, 0, (myid * Hkv + g) * a.block_size, &k_full[ks]);
+            tma_load_2d_hint(dst, &kmap, 0, (myid * Hkv + g) * a.block_size, &k_full[ks], kv_policy);
           else
-            tma_load_cache_tile(dst, &kmap, myid * Hkv + g, groups, &k_full[ks]);
+            tma_load_cache_tile_hint(dst, &kmap, myid * Hkv + g, groups, &k_full[ks], kv_policy);
         }
         ++n;  // K(n) issued
         if (n >= 2 && !issue_v(n - 2, prev_id, prev_g, prev_nvalid)) {
