@@ -254,46 +254,11 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
   const uint32_t blk_bytes = static_cast<uint32_t>(a.block_size) * kHeadDim * (kFp8 ? 1 : 2);
 
   prefetch_decode_metadata(a);
-  // ---- plan: tile count, this CTA's run [c0, c1), its first unit ----
-  if (tid == 0) {
-    misc->abort = 0;
-    misc->b0 = -1;
-    misc->off0 = 0;
-  }
-  int local = 0;
-  for (int b = tid; b < B; b += kThreads) {
-    const int L = seq_len_eff(a, b);
-    if (B <= kMaxSmemSeqs) s_len[b] = L;
-    local += Hkv * ((L + kTile - 1) / kTile);
-  }
-  int total;
-  block_scan<L::kWarps>(local, misc->warp_sums, &total);
-  const RunSplit split{total, static_cast<int>(gridDim.x), kTcMinTilesPerCta};
-  const int c0 = split.begin(blockIdx.x);
-  const int c1 = split.begin(blockIdx.x + 1);
-  int running = 0;
-  for (int base = 0; base < B; base += kThreads) {
-    const int b = base + tid;
-    const int L = b < B ? seq_len_cached(a, s_len, b) : 0;
-    const int u = Hkv * ((L + kTile - 1) / kTile);
-    int tile_total;
-    const int incl = block_scan<L::kWarps>(u, misc->warp_sums, &tile_total);
-    const int excl = running + incl - u;
-    if (u > 0 && excl <= c0 && c0 < excl + u) {
-      misc->b0 = b;
-      misc->off0 = c0 - excl;
-    }
-    running += tile_total;
-  }
-  __syncthreads();
-  // The next kernel on the stream may start its own set-up now.
-  grid_dep_launch();
-  finish_invalid_rows(a, B <= kMaxSmemSeqs ? s_len : nullptr);
-  if (c0 >= c1) return;  // nothing for this CTA: no barrier, copy or TMEM in use yet
-  const int nloc = c1 - c0;
-
-  // ---- set-up: barriers, zeroed Q^T / P^T buffers, TMEM ----
-  if (tid == 0) {
+  // Barriers and the zeroed Q^T / P^T buffers do not depend on the plan:
+  // set them up while the context lengths are on their way (the last
+  // thread, whose share of the plan is smallest, initialises the barriers;
+  // the barrier after the plan publishes them).
+  if (tid == kThreads - 1) {
     // FP8: the converter warps (4) release the code tiles; bf16: the MMA.
     for (int s = 0; s < kKStages; ++s) {
       mbar_init(&k_full[s], 1);
@@ -333,6 +298,67 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
   for (int i = tid; i < 4 * kSmallBytes / 16; i += kThreads)
     sts128(sbase + L::kOffQ + i * 16, 0u, 0u, 0u, 0u);  // rows >= G of Q^T stay zero
   fence_proxy_async_smem();
+  // ---- plan: tile count, this CTA's run [c0, c1), its first unit ----
+  if (tid == 0) {
+    misc->abort = 0;
+    misc->b0 = -1;
+    misc->off0 = 0;
+  }
+  int total, c0, c1;
+  RunSplit split;
+  if (B <= kThreads) {
+    // one sequence per thread: a single scan gives the total and each
+    // sequence's first tile
+    const int b = tid;
+    int u = 0;
+    if (b < B) {
+      const int L = seq_len_eff(a, b);
+      if (B <= kMaxSmemSeqs) s_len[b] = L;
+      u = Hkv * ((L + kTile - 1) / kTile);
+    }
+    const int incl = block_scan<L::kWarps>(u, misc->warp_sums, &total);
+    split = RunSplit{total, static_cast<int>(gridDim.x), kTcMinTilesPerCta};
+    c0 = split.begin(blockIdx.x);
+    c1 = split.begin(blockIdx.x + 1);
+    const int excl = incl - u;
+    if (u > 0 && excl <= c0 && c0 < excl + u) {
+      misc->b0 = b;
+      misc->off0 = c0 - excl;
+    }
+  } else {
+    int local = 0;
+    for (int b = tid; b < B; b += kThreads) {
+      const int L = seq_len_eff(a, b);
+      if (B <= kMaxSmemSeqs) s_len[b] = L;
+      local += Hkv * ((L + kTile - 1) / kTile);
+    }
+    block_scan<L::kWarps>(local, misc->warp_sums, &total);
+    split = RunSplit{total, static_cast<int>(gridDim.x), kTcMinTilesPerCta};
+    c0 = split.begin(blockIdx.x);
+    c1 = split.begin(blockIdx.x + 1);
+    int running = 0;
+    for (int base = 0; base < B; base += kThreads) {
+      const int b = base + tid;
+      const int L = b < B ? seq_len_cached(a, s_len, b) : 0;
+      const int u = Hkv * ((L + kTile - 1) / kTile);
+      int tile_total;
+      const int incl = block_scan<L::kWarps>(u, misc->warp_sums, &tile_total);
+      const int excl = running + incl - u;
+      if (u > 0 && excl <= c0 && c0 < excl + u) {
+        misc->b0 = b;
+        misc->off0 = c0 - excl;
+      }
+      running += tile_total;
+    }
+  }
+  __syncthreads();
+  // The next kernel on the stream may start its own set-up now.
+  grid_dep_launch();
+  finish_invalid_rows(a, B <= kMaxSmemSeqs ? s_len : nullptr);
+  if (c0 >= c1) return;  // nothing for this CTA: no copy or TMEM in use yet
+  const int nloc = c1 - c0;
+
+  // ---- set-up: TMEM ----
   if (warp == kMmaWarp) {
     tmem_alloc(&misc->tmem, L::kTmemCols);
     tmem_relinquish();
