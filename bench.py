@@ -62,6 +62,9 @@ def parse():
     p.add_argument("--no-workloads", action="store_true",
                    help="time only --workload (by default a single-GPU run of the headline "
                         "workload also times the other four configurations and the FP8 cache)")
+    p.add_argument("--phases", action="store_true",
+                   help="diagnostic: the tracing build's per-CTA phase stamps of the decode "
+                        "call (b64 and 8 x 32K), one JSON line per workload")
     p.add_argument("--append-sweep", action="store_true",
                    help="supplementary: time RoPE + append alone at 16k and 64k new tokens "
                         "(Qwen2-7B heads), one JSON line per size")
@@ -779,6 +782,74 @@ def run_append_sweep(args):
                           "l2": "flushed before every timed launch"}), flush=True)
 
 
+def run_phases(args):
+    """Where the decode call's time goes, from the tracing build
+    (include/qattn_trace.h): per-CTA %globaltimer stamps of the decode kernel
+    and the merge kernel, layers in rotation as in the timed runs.  Times are
+    us from the first decode CTA's entry; medians over the calls."""
+    import ctypes
+
+    import numpy as np
+
+    from paged_kv_gqa_07_gb300 import build as B
+    from paged_kv_gqa_07_gb300 import qattn as Q
+    B.build()
+    L = Q.load_library(B.build(trace=True))
+    Q._lib = L
+    L.qattn_trace_dims.argtypes = [ctypes.c_void_p] * 3
+    L.qattn_trace_read.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    dims = (ctypes.c_int32 * 3)()
+    L.qattn_trace_dims(ctypes.byref(dims, 0), ctypes.byref(dims, 4), ctypes.byref(dims, 8))
+    n_dec, n_slot, n_merge = int(dims[0]), int(dims[1]), int(dims[2])
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    for name in ("qwen2_7b_decode_b64", "qwen2_7b_long_decode"):
+        h = Harness(args, name, dev)
+        event_ms = h.timed(h.attend, args.steps, args.warmup, stream)
+        rows = []
+        for r in range(max(5, args.steps)):
+            assert L.qattn_trace_clear() == 0
+            h.attend(r)
+            torch.cuda.synchronize(dev)
+            dec = np.zeros(n_dec * n_slot, dtype=np.uint64)
+            mer = np.zeros(n_merge * 4, dtype=np.uint64)
+            assert L.qattn_trace_read(dec.ctypes.data, mer.ctypes.data) == 0
+            d = dec.reshape(n_dec, n_slot).astype(np.int64)
+            d = d[d[:, 0] > 0]
+            m = mer.reshape(n_merge, 4).astype(np.int64)
+            m = m[m[:, 1] > 0]
+            t0 = d[:, 0].min()
+            us = lambda x: (x - t0) / 1e3
+            rows.append({
+                "plan_done": float(np.median(us(d[:, 1]))),
+                "first_scores": float(np.median(us(d[:, 2]))),
+                "copies_issued": float(np.median(us(d[:, 3]))),
+                "softmax_done_median": float(np.median(us(d[:, 4]))),
+                "softmax_done_max": float(us(d[:, 4]).max()),
+                "cta_done_max": float(us(d[:, 5]).max()),
+                "merge_released": float(us(m[:, 1]).min()),
+                "merge_done": float(us(m[:, 2]).max()),
+            })
+        med = {k: round(statistics.median(r[k] for r in rows), 2) for k in rows[0]}
+        phases = {
+            "startup_us": med["first_scores"],
+            "stream_us": round(med["softmax_done_median"] - med["first_scores"], 2),
+            "tail_us": round(med["cta_done_max"] - med["softmax_done_median"], 2),
+            "grid_end_to_merge_us": round(med["merge_released"] - med["cta_done_max"], 2),
+            "merge_us": round(med["merge_done"] - med["merge_released"], 2),
+            "kernels_us": med["merge_done"],
+        }
+        print(json.dumps({"phases": name, "ctas": int(d.shape[0]), "calls": len(rows),
+                          "event_us_median": round(statistics.median(event_ms) * 1e3, 2),
+                          "stamps_us_median": med, **phases,
+                          "note": "tracing build; us from the first decode CTA's entry; "
+                                  "event_us also holds the launch latency before it"}),
+              flush=True)
+        h.free()
+        torch.cuda.empty_cache()
+
+
 def run_reference(args, dist: Dist):
     import oracle
     w = W.build(args.workload, block_size=args.block_size)
@@ -816,6 +887,9 @@ def main():
     args = parse()
     if args.append_sweep:
         run_append_sweep(args)
+        return
+    if args.phases:
+        run_phases(args)
         return
     if args.impl == "reference":
         # The reference arm is the CPU oracle: rank 0 alone runs it.

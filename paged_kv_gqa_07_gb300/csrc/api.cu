@@ -81,7 +81,16 @@ cudaError_t qattn::set_max_dynamic_smem(const void* kernel, int bytes) {
   std::lock_guard<std::mutex> lk(mu);
   for (const auto& d : done)
     if (d.first == kernel && d.second == dev) return cudaSuccess;
-  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (bytes > 0) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+  }
+  // Every kernel of the library asks for the largest shared-memory carve-out,
+  // so that an SM need not change its L1 / shared split between the decode
+  // and prefill kernels (which need almost all of it) and the kernels around
+  // them.
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared);
   if (e == cudaSuccess) done.emplace_back(kernel, dev);
   return e;
 }
@@ -384,6 +393,34 @@ int qattn_rope_cache_append(void* q, int64_t q_row_stride, const void* k, int64_
                                     num_blocks, cos_sin, max_pos, nullptr, nullptr, nullptr,
                                     0.0f, dims, err_word, stream);
 }
+
+#ifdef QATTN_TRACE
+// Tracing build only (include/qattn_trace.h).
+int qattn_trace_dims(int32_t* decode_ctas, int32_t* decode_slots, int32_t* merge_ctas) {
+  if (decode_ctas == nullptr || decode_slots == nullptr || merge_ctas == nullptr)
+    return QATTN_ERR_INVALID_ARG;
+  *decode_ctas = kTraceCtas;
+  *decode_slots = kTraceSlots;
+  *merge_ctas = kTraceMergeCtas;
+  return QATTN_OK;
+}
+
+int qattn_trace_clear(void) {
+  if (clear_decode_trace() != cudaSuccess || clear_merge_trace() != cudaSuccess)
+    return QATTN_ERR_CUDA;
+  return QATTN_OK;
+}
+
+int qattn_trace_read(uint64_t* decode_host, uint64_t* merge_host) {
+  if (decode_host == nullptr || merge_host == nullptr) return QATTN_ERR_INVALID_ARG;
+  if (read_decode_trace(reinterpret_cast<unsigned long long*>(decode_host),
+                        static_cast<size_t>(kTraceCtas) * kTraceSlots) != cudaSuccess ||
+      read_merge_trace(reinterpret_cast<unsigned long long*>(merge_host),
+                       static_cast<size_t>(kTraceMergeCtas) * 4) != cudaSuccess)
+    return QATTN_ERR_CUDA;
+  return QATTN_OK;
+}
+#endif
 
 int qattn_debug_decode_faults(int64_t wait_limit_ns, int32_t skip_k_copy) {
   if (wait_limit_ns < 0 || (wait_limit_ns > 0 && wait_limit_ns < 1000) ||

@@ -12,6 +12,21 @@
 #include "common.cuh"
 #include "internal.h"
 
+#ifdef QATTN_TRACE
+// Tracing build only: %globaltimer stamps of the merge CTAs (entry, the
+// decode grid's completion seen, done).
+__device__ unsigned long long g_qattn_merge_trace[qattn::kTraceMergeCtas * 4];
+#define QATTN_MSTAMP(slot)                                                                  \
+  do {                                                                                      \
+    if (blockIdx.x < qattn::kTraceMergeCtas)                                                \
+      g_qattn_merge_trace[blockIdx.x * 4 + (slot)] = qattn::globaltimer_ns();               \
+  } while (0)
+#else
+#define QATTN_MSTAMP(slot) \
+  do {                     \
+  } while (0)
+#endif
+
 namespace qattn {
 namespace {
 
@@ -40,7 +55,9 @@ __device__ __forceinline__ void fold_one(float& m, float& den, float4& num, floa
 
 template <int G>
 __global__ void __launch_bounds__(G * 32) decode_merge_kernel(const DecodeArgs a) {
+  if (threadIdx.x == 0) QATTN_MSTAMP(0);
   grid_dep_wait();  // the parts come from the decode grid
+  if (threadIdx.x == 0) QATTN_MSTAMP(1);
   const int Hkv = a.num_kv_heads;
   const int64_t seg = blockIdx.x;
   const int b = static_cast<int>(seg / Hkv), g = static_cast<int>(seg % Hkv);
@@ -69,7 +86,10 @@ __global__ void __launch_bounds__(G * 32) decode_merge_kernel(const DecodeArgs a
     row = a.cu_seqlens_q[b];
     ql = a.cu_seqlens_q[b + 1] - static_cast<int>(row);
   }
-  if (ql != 1 || nparts <= 1) return;  // not a decode row, or written by the decode kernel
+  if (ql != 1 || nparts <= 1) {  // not a decode row, or written by the decode kernel
+    if (threadIdx.x == 0) QATTN_MSTAMP(2);
+    return;
+  }
   float m = -INFINITY, den = 0.f;
   float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
   // parts 2 .. kMergeBatch - 1 of the first batch, then whole batches
@@ -93,12 +113,15 @@ __global__ void __launch_bounds__(G * 32) decode_merge_kernel(const DecodeArgs a
   packed.x = pack_bf16x2_rn(num.x * inv, num.y * inv);
   packed.y = pack_bf16x2_rn(num.z * inv, num.w * inv);
   *reinterpret_cast<uint2*>(orow) = packed;
+  if (threadIdx.x == 0) QATTN_MSTAMP(2);
 }
 
 template <int G>
 cudaError_t launch_merge_g(const DecodeArgs& a, cudaStream_t stream) {
   const int64_t units = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads;
-  cudaError_t e = launch_pdl(decode_merge_kernel<G>, dim3(static_cast<unsigned>(units)),
+  cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(decode_merge_kernel<G>), 0);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(decode_merge_kernel<G>, dim3(static_cast<unsigned>(units)),
                              dim3(G * 32), 0, stream, a);
   if (e != cudaSuccess) return e;
   return cudaPeekAtLastError();
@@ -145,5 +168,15 @@ cudaError_t launch_decode_merge(const DecodeArgs& a, cudaStream_t stream) {
     default: return cudaErrorInvalidValue;
   }
 }
+
+#ifdef QATTN_TRACE
+cudaError_t read_merge_trace(unsigned long long* host, size_t n) {
+  return cudaMemcpyFromSymbol(host, g_qattn_merge_trace, n * sizeof(unsigned long long));
+}
+cudaError_t clear_merge_trace() {
+  static unsigned long long zero[kTraceMergeCtas * 4];
+  return cudaMemcpyToSymbol(g_qattn_merge_trace, zero, sizeof(zero));
+}
+#endif
 
 }  // namespace qattn

@@ -136,6 +136,9 @@ __global__ void __launch_bounds__(kThreads) fp8_prefix_gather_kernel(const Fp8Ga
 cudaError_t launch_fp8_prefix_gather(const Fp8GatherArgs& a, cudaStream_t stream) {
   if (a.num_seqs <= 0 || a.blocks_per_seq <= 0) return cudaSuccess;
   const int grid = (a.blocks_per_seq + kBlocksPerCta - 1) / kBlocksPerCta;
+  const cudaError_t e =
+      set_max_dynamic_smem(reinterpret_cast<const void*>(fp8_prefix_gather_kernel), 0);
+  if (e != cudaSuccess) return e;
   fp8_prefix_gather_kernel<<<grid, kThreads, 0, stream>>>(a);
   return cudaPeekAtLastError();
 }
@@ -144,6 +147,8 @@ cudaError_t launch_fp8_gather(const Fp8GatherArgs& a, cudaStream_t stream) {
   if (a.num_seqs <= 0 || a.blocks_per_seq <= 0) return cudaSuccess;
   const dim3 grid(a.num_seqs, (a.blocks_per_seq + kBlocksPerCta - 1) / kBlocksPerCta);
   if (grid.y > 65535) return cudaErrorInvalidConfiguration;
+  const cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(fp8_gather_kernel), 0);
+  if (e != cudaSuccess) return e;
   fp8_gather_kernel<<<grid, kThreads, 0, stream>>>(a);
   return cudaPeekAtLastError();
 }

@@ -14,9 +14,10 @@
 
 namespace qattn {
 
-// Raises a kernel's dynamic shared memory limit to `bytes` on the current
-// device, once per (kernel, device): the attribute belongs to the device's
-// context, so a process driving several GPUs sets it on each.  Thread-safe.
+// Raises a kernel's dynamic shared memory limit to `bytes` (0: leaves it)
+// and asks for the largest shared-memory carve-out, on the current device,
+// once per (kernel, device): the attributes belong to the device's context,
+// so a process driving several GPUs sets them on each.  Thread-safe.
 cudaError_t set_max_dynamic_smem(const void* kernel, int bytes);
 
 // cuTensorMapEncodeTiled from the driver, looked up once (nullptr if the
@@ -250,6 +251,19 @@ __device__ __forceinline__ void finish_invalid_rows(const DecodeArgs& a, const i
 
 // K2r: merge the parts of straddling units.
 cudaError_t launch_decode_merge(const DecodeArgs& a, cudaStream_t stream);
+
+// Tracing build (-DQATTN_TRACE): per-CTA %globaltimer stamps of the decode
+// kernel (slots: entry, plan done, first scores, every copy issued, softmax
+// done, CTA done) and of the merge kernel (entry, decode grid seen, done).
+constexpr int kTraceCtas = 1024;
+constexpr int kTraceSlots = 8;
+constexpr int kTraceMergeCtas = 16384;
+#ifdef QATTN_TRACE
+cudaError_t read_decode_trace(unsigned long long* host, size_t n);
+cudaError_t clear_decode_trace();
+cudaError_t read_merge_trace(unsigned long long* host, size_t n);
+cudaError_t clear_merge_trace();
+#endif
 
 // ---- varlen prefill (varlen_prefill.cu) ----
 struct PrefillArgs {

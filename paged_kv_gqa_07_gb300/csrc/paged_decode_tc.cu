@@ -59,6 +59,22 @@
 #include "common.cuh"
 #include "internal.h"
 
+// Tracing build only (compiled with -DQATTN_TRACE, never in the library the
+// entry points ship in): %globaltimer stamps per CTA at the kernel's phase
+// boundaries, read back with qattn_trace_read (include/qattn_trace.h).
+#ifdef QATTN_TRACE
+__device__ unsigned long long g_qattn_decode_trace[qattn::kTraceCtas * qattn::kTraceSlots];
+#define QATTN_STAMP(slot)                                                                   \
+  do {                                                                                      \
+    if (blockIdx.x < qattn::kTraceCtas)                                                     \
+      g_qattn_decode_trace[blockIdx.x * qattn::kTraceSlots + (slot)] = qattn::globaltimer_ns(); \
+  } while (0)
+#else
+#define QATTN_STAMP(slot) \
+  do {                    \
+  } while (0)
+#endif
+
 namespace qattn {
 namespace {
 
@@ -247,6 +263,7 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
   const uint32_t sbase = smem_u32(smem);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) QATTN_STAMP(0);  // entry
   const int Hkv = a.num_kv_heads;
   const int B = a.num_seqs;
   const int bpt = kTile / a.block_size;    // cache blocks per tile: 8, 4 or 2
@@ -352,6 +369,7 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
     }
   }
   __syncthreads();
+  if (tid == 0) QATTN_STAMP(1);  // plan done
   // The next kernel on the stream may start its own set-up now.
   grid_dep_launch();
   finish_invalid_rows(a, B <= kMaxSmemSeqs ? s_len : nullptr);
@@ -499,6 +517,7 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
       bw = shfl_walk_helper(mw, cnt - 1);
       walk_next(bw, a, s_len);
     }
+    if (lane == 0) QATTN_STAMP(3);  // every copy issued
     if (ok && n > 0 && nv < n) issue_v(n - 1, prev_id, prev_g, prev_nvalid);
     // Drain: the most recent K, V and Q copies land before the CTA exits.
     if (lane == 0) {
@@ -865,6 +884,7 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
         ok = false;
         break;
       }
+      if (n == 0 && t == 0) QATTN_STAMP(2);  // first scores
       tc_fence_before();
       __syncwarp();
       if (lane == 0)
@@ -1007,12 +1027,14 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
       n += cnt;
       for (int j = 0; j < cnt; ++j) walk_next(sw, a, s_len);
     }
+    if (t == 0) QATTN_STAMP(4);  // softmax done
     if (!ok && lane == 0) set_err(a.err_word, QATTN_DEVERR_TIMEOUT);
   }
 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (tid == 0) QATTN_STAMP(5);  // CTA done
   if (warp == kMmaWarp) tmem_dealloc(tmem, L::kTmemCols);
 }
 
@@ -1055,5 +1077,15 @@ cudaError_t launch_paged_decode_tc(const DecodeArgs& a, const CUtensorMap& kmap,
     default: return cudaErrorInvalidValue;
   }
 }
+
+#ifdef QATTN_TRACE
+cudaError_t read_decode_trace(unsigned long long* host, size_t n) {
+  return cudaMemcpyFromSymbol(host, g_qattn_decode_trace, n * sizeof(unsigned long long));
+}
+cudaError_t clear_decode_trace() {
+  static unsigned long long zero[kTraceCtas * kTraceSlots];
+  return cudaMemcpyToSymbol(g_qattn_decode_trace, zero, sizeof(zero));
+}
+#endif
 
 }  // namespace qattn

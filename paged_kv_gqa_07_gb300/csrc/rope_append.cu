@@ -302,6 +302,13 @@ cudaError_t launch_rope_append(const RopeAppendArgs& a, cudaStream_t stream) {
   if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
   const bool extras = a.bias != nullptr || a.q_norm_w != nullptr || a.k_norm_w != nullptr;
   const dim3 grid(static_cast<unsigned>(blocks));
+  const void* fn =
+      a.kv_fp8 ? (extras ? reinterpret_cast<const void*>(rope_append_kernel<true, true>)
+                         : reinterpret_cast<const void*>(rope_append_kernel<false, true>))
+               : (extras ? reinterpret_cast<const void*>(rope_append_kernel<true, false>)
+                         : reinterpret_cast<const void*>(rope_append_kernel<false, false>));
+  const cudaError_t e = set_max_dynamic_smem(fn, 0);
+  if (e != cudaSuccess) return e;
   if (a.kv_fp8) {
     if (extras)
       rope_append_kernel<true, true><<<grid, kThreads, 0, stream>>>(a, tasks_per_token);
