@@ -29,7 +29,8 @@
  *   - Any entry point may be called from several host threads, and for any
  *     device (the current device of the calling thread): the host-side
  *     caches (SM counts, encoded tensor maps, the kernels' shared-memory
- *     limits, set once per device) are lock-protected.
+ *     limits, set once per device; the shared-prefix calls' side stream and
+ *     events, created once per device) are lock-protected.
  *   - bf16 everywhere for activations and cache; int32 for every index.
  *   - Cache layout: k_cache and v_cache are [num_blocks][num_kv_heads]
  *     [block_size][head_dim] bf16, contiguous.  Token slot s lives in block
@@ -299,9 +300,13 @@ size_t qattn_paged_decode_shared_prefix_workspace_size(int32_t num_seqs,
  *   shared_prefix_len  host, a multiple of block_size, 0 <= it < every context_len
  *                      (0: plain decode), < max_context_len.
  * The prefix is attended once per kv head for the whole batch on tensor
- * cores (all sequences' query groups against the prefix tiles, split over
- * the SMs), each sequence's remaining tokens by the decode kernels, and the
- * parts are merged in a fixed order (deterministic).  Device errors: those
+ * cores (all sequences' query groups against the prefix tiles) on an eighth
+ * of the SMs, at the same time as the decode kernel reads each sequence's
+ * remaining tokens on the others, and the parts are merged in a fixed order
+ * (deterministic).  The prefix pass runs on a stream of the library's own,
+ * forked from and joined back into `stream` with events (one stream and two
+ * events per device, created on the first call): the work is still ordered
+ * on `stream`, and the call may be captured into a CUDA graph.  Device errors: those
  * of qattn_paged_decode, a context_len <= shared_prefix_len gives a zero row
  * and QATTN_DEVERR_CONTEXT, a table that does not start with row 0's prefix
  * blocks QATTN_DEVERR_PREFIX (its result is then unspecified). */

@@ -54,6 +54,35 @@ int num_sms_current() {
   return cached[dev];
 }
 
+// ------------------------------------------------------------ side stream --
+//
+// The shared-prefix calls run their prefix pass on a stream of the
+// library's own, beside the decode of the sequences' own tokens on the
+// caller's stream (the two kernels take disjoint sets of SMs), forked from
+// and joined back into the caller's stream with two events: one stream and
+// two events per device, created on first use.  The lock is held from the
+// fork to the join, so that calls from several host threads do not
+// interleave their records.
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+std::mutex g_side_mu;
+
+SideStream* side_stream_current() {  // with g_side_mu held
+  static SideStream per_dev[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  SideStream& ss = per_dev[dev];
+  if (ss.stream == nullptr) {
+    if (cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&ss.stream, cudaStreamNonBlocking) != cudaSuccess)
+      return nullptr;
+  }
+  return &ss;
+}
+
 // ------------------------------------------------------------ tensor maps --
 
 }  // namespace
@@ -449,7 +478,8 @@ int decode_common(void* out, const void* q, int64_t q_row_stride, int32_t q_rows
                   int32_t* err_word, cudaStream_t stream, const CUtensorMap& kmap,
                   const CUtensorMap& vmap, int num_sms, int32_t prefix_len = 0,
                   int32_t part_base = 0, int32_t extra_parts = 0, int32_t kv_fp8 = 0,
-                  float k_scale = 1.0f, float v_scale = 1.0f) {
+                  float k_scale = 1.0f, float v_scale = 1.0f,
+                  cudaEvent_t merge_after = nullptr) {
   const size_t need = decode_workspace_bytes(num_seqs, max_context_len, dims.num_kv_heads,
                                              dims.num_heads / dims.num_kv_heads, extra_parts);
   if (workspace == nullptr || workspace_bytes < need ||
@@ -486,7 +516,22 @@ int decode_common(void* out, const void* q, int64_t q_row_stride, int32_t q_rows
   CUtensorMap qmap;
   if (!encode_q_group_map(&qmap, q, q_row_stride, q_rows, dims.num_heads, group))
     return QATTN_ERR_CUDA;
-  return cuda_status(launch_paged_decode_tc(a, kmap, vmap, qmap, num_sms, stream));
+  return cuda_status(launch_paged_decode_tc(a, kmap, vmap, qmap, num_sms, stream, merge_after));
+}
+
+// The shared-prefix pass beside the decode: the prefix in splits of at most
+// 16 KV tiles (an item then takes ~20 us), on at most an eighth of the SMs;
+// the decode of the sequences' own tokens keeps the rest.
+void prefix_plan(int sms, int num_kv_heads, int row_tiles, int prefix_tiles, int* splits,
+                 int* grid) {
+  int sp = (prefix_tiles + 15) / 16;
+  if (sp > kMaxPrefixSplits) sp = kMaxPrefixSplits;
+  if (sp < 1) sp = 1;
+  const int64_t items = static_cast<int64_t>(num_kv_heads) * row_tiles * sp;
+  int g = sms / 8 > 1 ? sms / 8 : 1;
+  if (items < g) g = static_cast<int>(items);
+  *splits = sp;
+  *grid = g;
 }
 
 int check_attention_args(void* out, const void* q, int64_t q_row_stride, const void* k_cache,
@@ -601,15 +646,16 @@ int qattn_paged_decode_shared_prefix(void* out, const void* q, int64_t q_row_str
                          max_context_len, dims, workspace, workspace_bytes, err_word, s, kmap,
                          vmap, sms, 0, 0, kMaxPrefixSplits);
   // Pass 1: the prefix, once per kv head for all sequences (tensor cores),
-  // as parts 0 .. splits - 1 of every unit.
+  // as parts 0 .. splits - 1 of every unit, on the side stream; pass 2
+  // beside it: each sequence's own tokens (the decode kernel, parts from
+  // `splits` on) on the other SMs; then, once both are done, the merge of
+  // all parts.
   const int group = dims.num_heads / dims.num_kv_heads;
   const int rows_per_tile = 128 / group;
   const int row_tiles = (num_seqs + rows_per_tile - 1) / rows_per_tile;
   const int prefix_tiles = (shared_prefix_len + 127) / 128;
-  int splits = sms / (dims.num_kv_heads * row_tiles);
-  if (splits > prefix_tiles) splits = prefix_tiles;
-  if (splits > kMaxPrefixSplits) splits = kMaxPrefixSplits;
-  if (splits < 1) splits = 1;
+  int splits = 1, pgrid = 1;
+  prefix_plan(sms, dims.num_kv_heads, row_tiles, prefix_tiles, &splits, &pgrid);
   CUtensorMap qmap;
   if (!encode_q_group_map(&qmap, q, q_row_stride, num_seqs, dims.num_heads, group,
                           rows_per_tile))
@@ -635,14 +681,19 @@ int qattn_paged_decode_shared_prefix(void* out, const void* q, int64_t q_row_str
   p.prefix_splits = splits;
   p.ws = carve_decode_workspace(workspace, num_seqs, max_context_len, dims.num_kv_heads, group,
                                 kMaxPrefixSplits);
-  st = cuda_status(launch_shared_prefix(p, qmap, kmap, vmap, sms, s));
+  std::lock_guard<std::mutex> lk(g_side_mu);
+  SideStream* ss = side_stream_current();
+  if (ss == nullptr || cudaEventRecord(ss->fork, s) != cudaSuccess ||
+      cudaStreamWaitEvent(ss->stream, ss->fork, 0) != cudaSuccess)
+    return QATTN_ERR_CUDA;
+  st = cuda_status(launch_shared_prefix(p, qmap, kmap, vmap, pgrid, ss->stream));
   if (st != QATTN_OK) return st;
-  // Pass 2: each sequence's own tokens (the decode kernels, parts from
-  // `splits` on), then the merge of all parts.
+  if (cudaEventRecord(ss->join, ss->stream) != cudaSuccess) return QATTN_ERR_CUDA;
   return decode_common(out, q, q_row_stride, num_seqs, nullptr, k_cache, v_cache, num_blocks,
                        block_tables, max_blocks_per_seq, context_lens, num_seqs,
                        max_context_len, dims, workspace, workspace_bytes, err_word, s, kmap,
-                       vmap, sms, shared_prefix_len, splits, kMaxPrefixSplits);
+                       vmap, sms - pgrid, shared_prefix_len, splits, kMaxPrefixSplits, 0, 1.0f,
+                       1.0f, ss->join);
 }
 
 size_t qattn_varlen_prefill_workspace_size(int32_t num_seqs, int32_t max_context_len,
@@ -888,8 +939,9 @@ int qattn_paged_decode_shared_prefix_fp8(void* out, const void* q, int64_t q_row
                          block_tables, max_blocks_per_seq, context_lens, num_seqs,
                          max_context_len, dims, workspace, decode_bytes, err_word, s, kmap,
                          vmap, sms, 0, 0, kMaxPrefixSplits, 1, k_scale, v_scale);
-  // The prefix as bf16 values of its codes (exact), then the prefix pass on
-  // the copy with the scales folded in.
+  // On the side stream: the prefix as bf16 values of its codes (exact), then
+  // the prefix pass on the copy with the scales folded in; beside them, each
+  // sequence's own tokens from the codes; then the merge of all parts.
   const int32_t pb = shared_prefix_len / dims.block_size;
   const size_t block_bytes =
       static_cast<size_t>(dims.num_kv_heads) * dims.block_size * kHeadDim * 2;
@@ -909,8 +961,6 @@ int qattn_paged_decode_shared_prefix_fp8(void* out, const void* q, int64_t q_row
   g.k_out = reinterpret_cast<__nv_bfloat16*>(ws + k_off);
   g.v_out = reinterpret_cast<__nv_bfloat16*>(ws + k_off + align256(pb * block_bytes));
   g.err_word = err_word;
-  cudaError_t e = launch_fp8_prefix_gather(g, s);
-  if (e != cudaSuccess) return cuda_status(e);
   CUtensorMap skmap, svmap;
   if (!cached_cache_map(&skmap, g.k_out, pb, dims.num_kv_heads, dims.block_size) ||
       !cached_cache_map(&svmap, g.v_out, pb, dims.num_kv_heads, dims.block_size))
@@ -919,10 +969,8 @@ int qattn_paged_decode_shared_prefix_fp8(void* out, const void* q, int64_t q_row
   const int rows_per_tile = 128 / group;
   const int row_tiles = (num_seqs + rows_per_tile - 1) / rows_per_tile;
   const int prefix_tiles = (shared_prefix_len + 127) / 128;
-  int splits = sms / (dims.num_kv_heads * row_tiles);
-  if (splits > prefix_tiles) splits = prefix_tiles;
-  if (splits > kMaxPrefixSplits) splits = kMaxPrefixSplits;
-  if (splits < 1) splits = 1;
+  int splits = 1, pgrid = 1;
+  prefix_plan(sms, dims.num_kv_heads, row_tiles, prefix_tiles, &splits, &pgrid);
   CUtensorMap qmap;
   if (!encode_q_group_map(&qmap, q, q_row_stride, num_seqs, dims.num_heads, group,
                           rows_per_tile))
@@ -948,13 +996,21 @@ int qattn_paged_decode_shared_prefix_fp8(void* out, const void* q, int64_t q_row
   p.prefix_splits = splits;
   p.ws = carve_decode_workspace(workspace, num_seqs, max_context_len, dims.num_kv_heads, group,
                                 kMaxPrefixSplits);
-  st = cuda_status(launch_shared_prefix(p, qmap, skmap, svmap, sms, s));
+  std::lock_guard<std::mutex> lk(g_side_mu);
+  SideStream* ss = side_stream_current();
+  if (ss == nullptr || cudaEventRecord(ss->fork, s) != cudaSuccess ||
+      cudaStreamWaitEvent(ss->stream, ss->fork, 0) != cudaSuccess)
+    return QATTN_ERR_CUDA;
+  cudaError_t e = launch_fp8_prefix_gather(g, ss->stream);
+  if (e != cudaSuccess) return cuda_status(e);
+  st = cuda_status(launch_shared_prefix(p, qmap, skmap, svmap, pgrid, ss->stream));
   if (st != QATTN_OK) return st;
-  // Each sequence's own tokens from the codes, then the merge of all parts.
+  if (cudaEventRecord(ss->join, ss->stream) != cudaSuccess) return QATTN_ERR_CUDA;
   return decode_common(out, q, q_row_stride, num_seqs, nullptr, k_cache, v_cache, num_blocks,
                        block_tables, max_blocks_per_seq, context_lens, num_seqs,
                        max_context_len, dims, workspace, decode_bytes, err_word, s, kmap, vmap,
-                       sms, shared_prefix_len, splits, kMaxPrefixSplits, 1, k_scale, v_scale);
+                       sms - pgrid, shared_prefix_len, splits, kMaxPrefixSplits, 1, k_scale,
+                       v_scale, ss->join);
 }
 
 }  // extern "C"

@@ -168,10 +168,14 @@ struct DecodeArgs {
   // index (-1: none), so that the wait on it runs out.
   int32_t debug_skip_k;
 };
-// Tensor-core decode (K2t): 128-token tiles, the GQA group as the MMA N dimension.
+// Tensor-core decode (K2t): 128-token tiles, the GQA group as the MMA N
+// dimension, on a grid of num_sms CTAs; then the merge (K2r), after
+// merge_after (an event of work on another stream that writes parts), if
+// given.
 cudaError_t launch_paged_decode_tc(const DecodeArgs& a, const CUtensorMap& kmap,
                                    const CUtensorMap& vmap, const CUtensorMap& qmap,
-                                   int num_sms, cudaStream_t stream);
+                                   int num_sms, cudaStream_t stream,
+                                   cudaEvent_t merge_after = nullptr);
 #ifdef __CUDACC__
 // Every CTA of a decode kernel touches the context lengths (planning) and,
 // right after, a slice of the block tables it cannot know in advance.

@@ -1040,7 +1040,8 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
 
 template <int G, bool kFp8>
 cudaError_t launch_tc_gf(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                         const CUtensorMap& qmap, int num_sms, cudaStream_t stream) {
+                         const CUtensorMap& qmap, int num_sms, cudaStream_t stream,
+                         cudaEvent_t merge_after) {
   using L = Lay<kFp8>;
   cudaError_t e = set_max_dynamic_smem(
       reinterpret_cast<const void*>(paged_decode_tc_kernel<G, kFp8>), L::kSmemBytes);
@@ -1050,30 +1051,35 @@ cudaError_t launch_tc_gf(const DecodeArgs& a, const CUtensorMap& kmap, const CUt
   if (e != cudaSuccess) return e;
   e = cudaPeekAtLastError();
   if (e != cudaSuccess) return e;
+  if (merge_after != nullptr) {  // parts that work on another stream writes
+    e = cudaStreamWaitEvent(stream, merge_after, 0);
+    if (e != cudaSuccess) return e;
+  }
   return launch_decode_merge(a, stream);
 }
 
 template <int G>
 cudaError_t launch_tc_g(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                        const CUtensorMap& qmap, int num_sms, cudaStream_t stream) {
-  return a.kv_fp8 ? launch_tc_gf<G, true>(a, kmap, vmap, qmap, num_sms, stream)
-                  : launch_tc_gf<G, false>(a, kmap, vmap, qmap, num_sms, stream);
+                        const CUtensorMap& qmap, int num_sms, cudaStream_t stream,
+                        cudaEvent_t merge_after) {
+  return a.kv_fp8 ? launch_tc_gf<G, true>(a, kmap, vmap, qmap, num_sms, stream, merge_after)
+                  : launch_tc_gf<G, false>(a, kmap, vmap, qmap, num_sms, stream, merge_after);
 }
 
 }  // namespace
 
 cudaError_t launch_paged_decode_tc(const DecodeArgs& a, const CUtensorMap& kmap,
                                    const CUtensorMap& vmap, const CUtensorMap& qmap, int num_sms,
-                                   cudaStream_t stream) {
+                                   cudaStream_t stream, cudaEvent_t merge_after) {
   switch (a.num_heads / a.num_kv_heads) {
-    case 1: return launch_tc_g<1>(a, kmap, vmap, qmap, num_sms, stream);
-    case 2: return launch_tc_g<2>(a, kmap, vmap, qmap, num_sms, stream);
-    case 3: return launch_tc_g<3>(a, kmap, vmap, qmap, num_sms, stream);
-    case 4: return launch_tc_g<4>(a, kmap, vmap, qmap, num_sms, stream);
-    case 5: return launch_tc_g<5>(a, kmap, vmap, qmap, num_sms, stream);
-    case 6: return launch_tc_g<6>(a, kmap, vmap, qmap, num_sms, stream);
-    case 7: return launch_tc_g<7>(a, kmap, vmap, qmap, num_sms, stream);
-    case 8: return launch_tc_g<8>(a, kmap, vmap, qmap, num_sms, stream);
+    case 1: return launch_tc_g<1>(a, kmap, vmap, qmap, num_sms, stream, merge_after);
+    case 2: return launch_tc_g<2>(a, kmap, vmap, qmap, num_sms, stream, merge_after);
+    case 3: return launch_tc_g<3>(a, kmap, vmap, qmap, num_sms, stream, merge_after);
+    case 4: return launch_tc_g<4>(a, kmap, vmap, qmap, num_sms, stream, merge_after);
+    case 5: return launch_tc_g<5>(a, kmap, vmap, qmap, num_sms, stream, merge_after);
+    case 6: return launch_tc_g<6>(a, kmap, vmap, qmap, num_sms, stream, merge_after);
+    case 7: return launch_tc_g<7>(a, kmap, vmap, qmap, num_sms, stream, merge_after);
+    case 8: return launch_tc_g<8>(a, kmap, vmap, qmap, num_sms, stream, merge_after);
     default: return cudaErrorInvalidValue;
   }
 }
