@@ -804,8 +804,8 @@ def run_phases(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream(dev)
-    for name in ("qwen2_7b_decode_b64", "qwen2_7b_long_decode"):
-        h = Harness(args, name, dev)
+    for name in ("qwen2_7b_decode_b64", "qwen2_7b_long_decode", "qwen3_prefix_decode"):
+        h = Harness(args, name, dev, kv=args.kv)
         event_ms = h.timed(h.attend, args.steps, args.warmup, stream)
         rows = []
         for r in range(max(5, args.steps)):
@@ -840,7 +840,7 @@ def run_phases(args):
             "merge_us": round(med["merge_done"] - med["merge_released"], 2),
             "kernels_us": med["merge_done"],
         }
-        print(json.dumps({"phases": name, "ctas": int(d.shape[0]), "calls": len(rows),
+        print(json.dumps({"phases": name, "kv_cache_dtype": args.kv, "ctas": int(d.shape[0]), "calls": len(rows),
                           "event_us_median": round(statistics.median(event_ms) * 1e3, 2),
                           "stamps_us_median": med, **phases,
                           "note": "tracing build; us from the first decode CTA's entry; "
