@@ -6,9 +6,9 @@ start-up -- so they cannot hand qattn_paged_decode a workspace.
 qattn_paged_decode_noalloc keeps its split-KV scratch in a fixed array inside
 the library instead.  This test calls it through the C ABI three times in a row
 (each call starts from whatever the previous one left in the shared array)
-and checks each result against qattn_paged_decode with a workspace of its
-own, within the tolerance the parity tests use, and that the device's free
-memory does not move across the later calls.  It lives in its own file,
+and checks each result against the CPU oracle and against qattn_paged_decode
+with a workspace of its own, within the tolerance the parity tests use, and
+that the device's free memory does not move across the later calls.  It lives in its own file,
 named to be collected last, and passes alone or after the other tests.
 """
 import ctypes
@@ -20,7 +20,7 @@ from paged_kv_gqa_07_gb300 import build as B
 from paged_kv_gqa_07_gb300 import qattn as Q
 from paged_kv_gqa_07_gb300 import workloads as W
 
-from _util import ATOL, RTOL, GpuRun
+from _util import ATOL, RTOL, GpuRun, assert_close, oracle_for
 
 pytestmark = pytest.mark.gpu
 
@@ -60,7 +60,10 @@ def test_noalloc_decode_matches_workspace_decode_twice(idx):
         torch.cuda.synchronize()
     free.append(torch.cuda.mem_get_info()[0])
     assert r.err_bits == 0
+    _, _, _, oracle_out, e1, e2 = oracle_for(idx)
+    assert e1 == e2 == 0
     for out in outs:
+        assert_close(out, oracle_out)
         d = (out.float() - ref.float()).abs().max().item()
         scale = ref.float().abs().max().item()
         assert d <= ATOL and d / scale <= RTOL
