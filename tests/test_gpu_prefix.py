@@ -1,6 +1,6 @@
 """GPU parity of the shared-prefix decode (qattn_paged_decode_shared_prefix:
-the prefix once per kv head for the whole batch on tensor cores, each
-sequence's own tokens by the decode kernels, parts merged) against the CPU
+the prefix once per kv head for the whole batch on tensor cores, beside the
+decode kernel on each sequence's own tokens, parts merged) against the CPU
 oracle's plain paged attention on the same inputs."""
 import numpy as np
 import pytest
@@ -96,6 +96,47 @@ def test_prefix_errors():
 
 def oracle_for_custom(w):
     return oracle_step(w)
+
+
+def test_prefix_long_prefix_several_splits():
+    """A 2304-token prefix (18 tiles: two splits of the prefix pass, the
+    second ragged) under short and long suffixes."""
+    ctx = [2304 + s for s in (1, 64, 129, 700, 1500, 33, 256, 2)]
+    w = W.custom(28, 4, ctx=ctx, q_lens=[1] * len(ctx), seed=450, shared_prefix_tokens=2304)
+    _, _, _, ref, _, e2 = oracle_step(w)
+    r = run_prefix(GpuRun(w).append().sync(), 2304)
+    assert r.err_bits == 0 and e2 == 0
+    assert_close(r.out, ref)
+
+
+def test_prefix_graph_replay():
+    """The append and the shared-prefix call (its prefix pass on the
+    library's side stream, forked from and joined back into the captured
+    stream) captured in a CUDA graph replay to the eager result."""
+    w = W.build(4)
+    r = GpuRun(w)
+    qkv0 = r.g.qkv.clone()
+    n = Q.qattn_paged_decode_shared_prefix_workspace_size(w.num_seqs, r.max_ctx, r.dims)
+    ws = torch.empty(n, dtype=torch.uint8, device=r.dev)
+    run_prefix(r.append().sync(), w.shared_prefix_tokens, ws)
+    first = r.out.clone()
+    g = r.g
+    s = torch.cuda.Stream(device=r.dev)
+    s.wait_stream(torch.cuda.current_stream(r.dev))
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            g.qkv.copy_(qkv0)
+            r.append()
+            Q.qattn_paged_decode_shared_prefix(r.out, g.q_view(), g.k_cache, g.v_cache,
+                                               g.block_tables, g.context_lens, r.max_ctx,
+                                               w.shared_prefix_tokens, r.dims, ws, r.err)
+    for _ in range(2):
+        r.out.zero_()
+        graph.replay()
+        r.sync()
+        assert r.err_bits == 0
+        assert torch.equal(r.out, first)
 
 
 def test_prefix_host_validation():
