@@ -46,14 +46,19 @@
 // FP8 cache (kFp8; kv_cache_dtype "fp8", fp8_e4m3fn codes with a cache
 // scale per tensor, "Qwen2大模型架构解析与vLLM优化实践" sections 4.1, 4.2,
 // 6.3): the cache tiles are half the bytes (128 B per token row) and land
-// by TMA in 4-deep 16 KB rings; four more warps (7-10, thread = token row)
-// dequantise them -- the e4m3 -> f16 conversion is exact -- K into tensor
-// memory (the A operand of S^T = K . Q^T is read from TMEM, so the converted
-// K never touches shared memory) and V into the same swizzled MN-major f16
-// layout the bf16 path gets from TMA, with rows past the context written as
-// zeros.  Both products run in f16 (Q^T converted in place once per unit,
-// P^T written as f16); k_scale is folded into the logit scale and v_scale
-// into the epilogue.
+// by TMA in 4-deep 16 KB rings.  S^T = K . Q^T runs on the codes themselves
+// (kind::f8f6f4, the K tile straight from the ring as the K-major e4m3 A):
+// per unit four more warps (7-10) write Q^T as two e4m3 rows per head,
+// hi = e4m3(q 2^e) and lo = e4m3(q 2^e - hi), with 2^e the power of two that
+// puts the head's largest |q| in [128, 256).  hi + lo is the bf16 value
+// exactly for every element within 2^10 of that maximum (hi keeps four
+// significant bits, the residue at most four more), so the score is the two
+// columns' sum times 2^-e -- the same dot product as the bf16 path up to
+// fp32 rounding.  The same warps dequantise V (e4m3 -> f16 is exact) into
+// the swizzled MN-major f16 layout the bf16 path gets from TMA, with rows
+// past the context written as zeros, and P V runs in f16 (P^T written as
+// f16); k_scale is folded into the logit scale and v_scale into the
+// epilogue.
 #include <math.h>
 
 #include "common.cuh"
@@ -93,13 +98,15 @@ constexpr int kCacheTileBytes = 16 * kHeadDim * 2;  // 16 tokens: 4 KB
 constexpr int kTileBytes = kTile * kHeadDim * 2;    // 32 KB
 constexpr int kSmallHalf = kN * 128;     // 16 rows x 128 B
 constexpr int kSmallBytes = 2 * kSmallHalf;
+constexpr int kQ8Bytes = kN * 128;      // FP8: Q^T as e4m3, 16 rows x 128 B
 constexpr uint32_t kColO = 32;   // O^T of unit u at kColO + (u & 1) * kN
-constexpr uint32_t kColK = 64;   // FP8: dequantised K of tile n at kColK + (n & 1) * 64
 constexpr float kLazyRescale = 8.0f;
 constexpr int kMaxSmemSeqs = 2048;
 
 // Shared-memory layout.  bf16: 3 + 3 ring slots of 32 KB cache tiles.  FP8:
-// 4 + 4 slots of 16 KB code tiles, then two 32 KB f16 V tiles.
+// 4 + 4 slots of 16 KB code tiles, then two 32 KB f16 V tiles; after the
+// P^T buffers two slots of e4m3 Q^T and, after the epilogue's maxima, the
+// per-head scales 2^-e of the two units those slots belong to.
 template <bool kFp8>
 struct Lay {
   static constexpr int kWarps = kFp8 ? 15 : 11;
@@ -113,19 +120,22 @@ struct Lay {
   static constexpr int kOffVc = kOffV + kVStages * kStageBytes;  // FP8: f16 V tiles
   static constexpr int kOffQ = kOffVc + (kFp8 ? 2 * kTileBytes : 0);  // 2 slots of Q^T
   static constexpr int kOffP = kOffQ + 2 * kSmallBytes;               // 2 buffers of P^T
-  static constexpr int kOffRed = kOffP + 2 * kSmallBytes;             // [2][4][16] fp32
+  static constexpr int kOffQ8 = kOffP + 2 * kSmallBytes;              // FP8: 2 x e4m3 Q^T
+  static constexpr int kOffRed = kOffQ8 + (kFp8 ? 2 * kQ8Bytes : 0);  // [2][4][16] fp32
   static constexpr int kOffEpiL = kOffRed + 2 * 4 * kN * 4;           // [2][4][16] fp32
   static constexpr int kOffEpiM = kOffEpiL + 2 * 4 * kN * 4;          // [2][16] fp32
-  static constexpr int kOffBars = kOffEpiM + 2 * kN * 4;
+  static constexpr int kOffQs = kOffEpiM + 2 * kN * 4;                // FP8: [2][16] fp32
+  static constexpr int kOffBars = kOffQs + (kFp8 ? 2 * kN * 4 : 0);
   // k_full/k_empty[kKStages] v_full/v_empty[kVStages] q_full q_empty s_full
   // s_free p_full pv_done o_free epi_full epi_empty seg_done [2] rbar
-  // mma_done; FP8 adds kc_full kc_empty vc_full vc_empty qc_full [2]
-  static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 * 10 + 2 + (kFp8 ? 10 : 0);
+  // mma_done; FP8 adds vc_full vc_empty qc_full sc_free [2]
+  static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 * 10 + 2 + (kFp8 ? 8 : 0);
   static constexpr int kOffMisc = kOffBars + kNumBars * 8;
   static constexpr int kOffLens = kOffMisc + 128;  // Misc
   static constexpr int kSmemBytes = kOffLens + kMaxSmemSeqs * 4 + 1024;
-  static constexpr uint32_t kTmemCols = kFp8 ? 256 : 64;
+  static constexpr uint32_t kTmemCols = 64;
 };
+static_assert(Lay<true>::kOffQ8 % 1024 == 0, "e4m3 Q^T slots on the 128-byte swizzle's period");
 static_assert(Lay<true>::kSmemBytes <= 227 * 1024, "FP8 decode shared memory");
 static_assert(Lay<false>::kSmemBytes <= 227 * 1024, "decode shared memory");
 
@@ -246,19 +256,20 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
   uint64_t* seg_done = epi_empty + 2;
   uint64_t* rbar = seg_done + 2;
   uint64_t* mma_done = rbar + 1;
-  // FP8: kc_full[b] / vc_full[b] -- the converters have written K of tile n
-  // into TMEM / V of tile n as f16 (tiles of parity b); kc_empty / vc_empty
-  // -- the MMA that read them is done; qc_full[s] -- Q^T slot s is f16.
-  uint64_t* kc_full = mma_done + 1;
-  uint64_t* kc_empty = kc_full + 2;
-  uint64_t* vc_full = kc_empty + 2;
+  // FP8: vc_full[b] -- the converters have written V of tile n as f16 (tiles
+  // of parity b); vc_empty[b] -- the P V that read it is done; qc_full[s] --
+  // the e4m3 Q^T and the scales of slot s are written; sc_free[s] -- the
+  // softmax has read slot s's scales.
+  uint64_t* vc_full = mma_done + 1;
   uint64_t* vc_empty = vc_full + 2;
   uint64_t* qc_full = vc_empty + 2;
+  uint64_t* sc_free = qc_full + 2;
   Misc* misc = reinterpret_cast<Misc*>(smem + L::kOffMisc);
   int* s_len = reinterpret_cast<int*>(smem + L::kOffLens);
   float* red = reinterpret_cast<float*>(smem + L::kOffRed);
   float* epi_l = reinterpret_cast<float*>(smem + L::kOffEpiL);
   float* epi_m = reinterpret_cast<float*>(smem + L::kOffEpiM);
+  float* q_inv = reinterpret_cast<float*>(smem + L::kOffQs);  // FP8: 2^-e per head
   volatile int* abort_flag = &misc->abort;
   const uint32_t sbase = smem_u32(smem);
 
@@ -276,10 +287,11 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
   // thread, whose share of the plan is smallest, initialises the barriers;
   // the barrier after the plan publishes them).
   if (tid == kThreads - 1) {
-    // FP8: the converter warps (4) release the code tiles; bf16: the MMA.
+    // K slots are released by the MMA; V slots by the MMA (bf16) or the four
+    // converter warps (FP8).
     for (int s = 0; s < kKStages; ++s) {
       mbar_init(&k_full[s], 1);
-      mbar_init(&k_empty[s], kFp8 ? 4 : 1);
+      mbar_init(&k_empty[s], 1);
     }
     for (int s = 0; s < kVStages; ++s) {
       mbar_init(&v_full[s], 1);
@@ -287,11 +299,10 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
     }
     if (kFp8) {
       for (int s = 0; s < 2; ++s) {
-        mbar_init(&kc_full[s], 4);
-        mbar_init(&kc_empty[s], 1);
         mbar_init(&vc_full[s], 4);
         mbar_init(&vc_empty[s], 1);
         mbar_init(&qc_full[s], 4);
+        mbar_init(&sc_free[s], 4);
       }
     }
     for (int s = 0; s < 2; ++s) {
@@ -312,8 +323,9 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
     mbar_init(mma_done, 2);  // one commit per MMA-issuing thread
     fence_barrier_init();
   }
-  for (int i = tid; i < 4 * kSmallBytes / 16; i += kThreads)
-    sts128(sbase + L::kOffQ + i * 16, 0u, 0u, 0u, 0u);  // rows >= G of Q^T stay zero
+  // Rows >= G of Q^T (and the e4m3 rows of no head) stay zero.
+  for (int i = tid; i < (4 * kSmallBytes + (kFp8 ? 2 * kQ8Bytes : 0)) / 16; i += kThreads)
+    sts128(sbase + L::kOffQ + i * 16, 0u, 0u, 0u, 0u);
   fence_proxy_async_smem();
   // ---- plan: tile count, this CTA's run [c0, c1), its first unit ----
   if (tid == 0) {
@@ -540,7 +552,7 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
     // waited behind the other's eight MMAs.  The streams share no tensor
     // memory (S vs O^T) and each thread's commits track its own MMAs.
     if (lane == 0) {
-      constexpr uint32_t idesc_qk = kFp8 ? idesc_f16_f32(kTile, kN, false, false)
+      constexpr uint32_t idesc_qk = kFp8 ? idesc_e4m3_f32(kTile, kN)
                                          : idesc_bf16_f32(kTile, kN, false, false);
       constexpr uint32_t idesc_pv = kFp8 ? idesc_f16_f32(kHeadDim, kN, false, true)
                                          : idesc_bf16_f32(kHeadDim, kN, false, true);
@@ -611,24 +623,31 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
           const bool last = (qn == nloc - 1) || (qw.i == qw.nt - 1);
           const int seg_q = qseg + (first ? 1 : 0);
           const int ks = qn % kKStages, sb = qn & 1;
-          bool ready = kFp8 ? mbar_test(&kc_full[qn & 1], (qn >> 1) & 1)
-                            : mbar_test(&k_full[ks], (qn / kKStages) & 1);
+          bool ready = mbar_test(&k_full[ks], (qn / kKStages) & 1);
           if (ready && qn >= 2) ready = mbar_test(&s_free[sb], ((qn >> 1) & 1) ^ 1);
           if (ready && first)
             ready = mbar_test(kFp8 ? &qc_full[seg_q & 1] : &q_full[seg_q & 1], (seg_q >> 1) & 1);
           if (ready) {
             tc_fence_after();
             const uint32_t sk = sbase + L::kOffK + ks * L::kStageBytes;
-            const uint32_t sq = sbase + L::kOffQ + (seg_q & 1) * kSmallBytes;
+            if constexpr (kFp8) {
+              // The code tile as the K-major e4m3 A: 128-byte token rows,
+              // 8-row groups 1 KB apart; K step k = dims 32k..32k+31 (32 B
+              // into the swizzle row).  B: the slot's e4m3 Q^T, hi rows
+              // 0..G-1 and lo rows 8..8+G-1, in the same layout.
+              const uint32_t sq = sbase + L::kOffQ8 + (seg_q & 1) * kQ8Bytes;
 #pragma unroll(kMmaUnroll)
-            for (int k = 0; k < kHeadDim / 16; ++k) {
-              const uint64_t bd =
-                  sdesc_sw128(sq + (k >> 2) * kSmallHalf + (k & 3) * 32, 16, 1024);
-              if constexpr (kFp8) {
-                // K from TMEM: dims 16k..16k+15 are columns 8k..8k+7
-                mma_f16_ts(tmem + sb * kN, tmem + kColK + (qn & 1) * 64 + k * 8, bd, idesc_qk,
-                           k > 0 ? 1u : 0u);
-              } else {
+              for (int k = 0; k < kHeadDim / 32; ++k) {
+                const uint64_t ad = sdesc_sw128(sk + k * 32, 16, 1024);
+                const uint64_t bd = sdesc_sw128(sq + k * 32, 16, 1024);
+                mma_e4m3_ss(tmem + sb * kN, ad, bd, idesc_qk, k > 0 ? 1u : 0u);
+              }
+            } else {
+              const uint32_t sq = sbase + L::kOffQ + (seg_q & 1) * kSmallBytes;
+#pragma unroll(kMmaUnroll)
+              for (int k = 0; k < kHeadDim / 16; ++k) {
+                const uint64_t bd =
+                    sdesc_sw128(sq + (k >> 2) * kSmallHalf + (k & 3) * 32, 16, 1024);
                 // K tile as the K-major A: dim half k/4 at +1 KB, 8-token
                 // groups 2 KB apart.
                 const uint64_t ad = sdesc_sw128(sk + (k >> 2) * 1024 + (k & 3) * 32, 16, 2048);
@@ -636,7 +655,7 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
               }
             }
             mma_commit(&s_full[sb]);
-            mma_commit(kFp8 ? &kc_empty[qn & 1] : &k_empty[ks]);
+            mma_commit(&k_empty[ks]);
             if (last) mma_commit(&q_empty[seg_q & 1]);
             if (first) qseg = seg_q;
             ++qn;
@@ -733,58 +752,55 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
     if (!ok && lane == 0) set_err(a.err_word, QATTN_DEVERR_TIMEOUT);
   } else if (kFp8 && warp >= kConvWarp0) {
     // ============================ FP8 converters =============================
-    // Thread = token row r of a tile (warp w owns TMEM lanes 32 (w % 4) ..).
-    // Order K(0), then K(n+1) before V(n) -- the producer's issue order.
+    // Per unit, Q^T as e4m3 pairs (warp w takes heads w and w + 4, lane =
+    // dims 4 lane .. 4 lane + 3); per tile, V as f16 (thread = token row).
+    // Order: the Q^T of the unit tile n starts, then V(n-1) -- the
+    // producer's issue order.
     const int row = ((warp & 3) << 5) | lane;
-    const int ct = (warp - kConvWarp0) * 32 + lane;  // 0..127
-    const uint32_t k_lane = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const int cw = warp - kConvWarp0;  // 0..3
     bool ok = true;
     Walk kw = w0, vw = w0;
     int seg = -1;
-    // K(n): Q^T first when the tile starts a unit, then the code row into
-    // TMEM columns kColK + (n & 1) * 64 (every row: the rows past the
-    // context are masked in the softmax).
-    auto conv_k = [&](int n) -> bool {
-      if (n == 0 || kw.i == 0) {
-        ++seg;
-        const int qs = seg & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(&q_full[qs], (seg >> 1) & 1, abort_flag, a.wait_ns)))
-          return false;
-        for (int c = ct; c < kSmallBytes / 16; c += 128) {
-          const uint32_t addr = sbase + L::kOffQ + qs * kSmallBytes + c * 16;
-          const uint4 x = lds128(addr);
-          sts128(addr, bf16x2_to_f16x2(x.x), bf16x2_to_f16x2(x.y), bf16x2_to_f16x2(x.z),
-                 bf16x2_to_f16x2(x.w));
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&qc_full[qs]);
-      }
-      const int ks = n % kKStages;
-      bool w_ok = mbar_wait(&k_full[ks], (n / kKStages) & 1, abort_flag, a.wait_ns);
-      if (w_ok && n >= 2) w_ok = mbar_wait(&kc_empty[n & 1], ((n >> 1) & 1) ^ 1, abort_flag, a.wait_ns);
+    // Q^T of the next unit into e4m3 slot seg & 1 (row h = hi, row 8 + h =
+    // lo, 128-byte swizzle) and 2^-e of each head into q_inv, once the bf16
+    // Q^T has landed and the softmax has read the slot's previous scales.
+    auto conv_q = [&]() -> bool {
+      ++seg;
+      const int qs = seg & 1;
+      bool w_ok = mbar_wait(&q_full[qs], (seg >> 1) & 1, abort_flag, a.wait_ns);
+      if (w_ok && seg >= 2)
+        w_ok = mbar_wait(&sc_free[qs], ((seg >> 1) & 1) ^ 1, abort_flag, a.wait_ns);
       if (!__all_sync(0xffffffffu, w_ok)) return false;
-      tc_fence_after();
-      const uint32_t src = sbase + L::kOffK + ks * L::kStageBytes + row * 128;
-      const uint32_t dst = k_lane + kColK + (n & 1) * 64;
-      // (not unrolled: with eleven warps in six roles the kernel's code is
-      // instruction-cache bound -- unrolling these loops measured slower)
-#pragma unroll 1
-      for (int c = 0; c < 8; ++c) {
-        const uint4 x = lds128(src + ((c ^ (row & 7)) << 4));
-        const uint32_t w[8] = {
-            cvt_f16x2_from_e4m3x2(x.x), cvt_f16x2_from_e4m3x2(x.x >> 16),
-            cvt_f16x2_from_e4m3x2(x.y), cvt_f16x2_from_e4m3x2(x.y >> 16),
-            cvt_f16x2_from_e4m3x2(x.z), cvt_f16x2_from_e4m3x2(x.z >> 16),
-            cvt_f16x2_from_e4m3x2(x.w), cvt_f16x2_from_e4m3x2(x.w >> 16)};
-        tmem_st8_nowait(dst + c * 8, w);
+      for (int h = cw; h < G; h += 4) {
+        // bf16 Q^T row h: dims 64 (lane / 16) + 4 (lane % 16) .. + 3, i.e.
+        // 4 lane .. 4 lane + 3, in the 128-byte-swizzled half lane / 16
+        const uint2 x = lds64(sbase + L::kOffQ + qs * kSmallBytes + (lane >> 4) * kSmallHalf +
+                              h * 128 + ((((lane & 15) >> 1) ^ (h & 7)) << 4) + (lane & 1) * 8);
+        float v[4] = {bf16lo_to_f32(x.x), bf16hi_to_f32(x.x), bf16lo_to_f32(x.y),
+                      bf16hi_to_f32(x.y)};
+        const float mx = warp_max(fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])),
+                                        fmaxf(fabsf(v[2]), fabsf(v[3]))));
+        // 2^e with the maximum's exponent E: max |q| 2^e in [128, 256)
+        int e = 7 - (static_cast<int>((__float_as_uint(mx) >> 23) & 0xffu) - 127);
+        e = max(-126, min(126, e));
+        const float up = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] *= up;  // exact: a power of two
+        const uint32_t h01 = cvt_e4m3x2(v[0], v[1]), h23 = cvt_e4m3x2(v[2], v[3]);
+        const uint32_t c01 = cvt_f16x2_from_e4m3x2(h01), c23 = cvt_f16x2_from_e4m3x2(h23);
+        const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&c01));
+        const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&c23));
+        const uint32_t l01 = cvt_e4m3x2(v[0] - f01.x, v[1] - f01.y);
+        const uint32_t l23 = cvt_e4m3x2(v[2] - f23.x, v[3] - f23.y);
+        const uint32_t dst = sbase + L::kOffQ8 + qs * kQ8Bytes + ((((lane >> 2) ^ (h & 7))) << 4) +
+                             (lane & 3) * 4;
+        sts32(dst + h * 128, h01 | (h23 << 16));
+        sts32(dst + (8 + h) * 128, l01 | (l23 << 16));
+        if (lane == 0) q_inv[qs * kN + h] = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
       }
+      fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&k_empty[ks]);
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&kc_full[n & 1]);
+      if (lane == 0) mbar_arrive(&qc_full[qs]);
       return true;
     };
     // V(j): the code row as f16 into the swizzled MN-major tile (chunk c of
@@ -818,7 +834,7 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
     };
     for (int n = 0; n <= nloc && ok; ++n) {
       if (n < nloc) {
-        ok = conv_k(n);
+        if (n == 0 || kw.i == 0) ok = conv_q();
         walk_next(kw, a, s_len);
         if (!ok) break;
       }
@@ -833,6 +849,10 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
     const int t = tid;  // token row of S^T / dimension row of O^T = TMEM lane
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     float m_used[G], l_t[G];
+    // FP8: the logit scale of head h for the current unit, scale_log2 * 2^-e
+    float qsc[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) qsc[h] = a.scale_log2;
     int rphase = 0;
     // PV(j) completes phase j >> 1 of pv_done[j & 1].  Tile n always waits
     // for PV(n-2) (P^T buffer reuse), so when it later waits for PV(n-1)
@@ -860,6 +880,19 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
         for (int h = 0; h < G; ++h) {
           m_used[h] = -INFINITY;
           l_t[h] = 0.f;
+        }
+        if constexpr (kFp8) {
+          // the unit's 2^-e per head (written with its e4m3 Q^T); slot
+          // seg & 1 is rewritten for unit seg + 2 only after this read
+          if (!__all_sync(0xffffffffu, mbar_wait(&qc_full[seg & 1], (seg >> 1) & 1, abort_flag,
+                                                 a.wait_ns))) {
+            ok = false;
+            break;
+          }
+#pragma unroll
+          for (int h = 0; h < G; ++h) qsc[h] = a.scale_log2 * q_inv[(seg & 1) * kN + h];
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sc_free[seg & 1]);
         }
       }
       const int nv0 = min(kTile, sw.L - sw.i * kTile);
@@ -894,8 +927,13 @@ __global__ void __launch_bounds__(Lay<kFp8>::kThreads, 1)
       float* rd = red + (rphase & 1) * 4 * kN;
 #pragma unroll
       for (int h = 0; h < G; ++h) {
-        s[0][h] = t < nv0 ? s[0][h] * a.scale_log2 : -INFINITY;
-        s[1][h] = t < nv1 ? s[1][h] * a.scale_log2 : -INFINITY;
+        if constexpr (kFp8) {  // hi column h plus lo column 8 + h
+          s[0][h] = t < nv0 ? (s[0][h] + s[0][8 + h]) * qsc[h] : -INFINITY;
+          s[1][h] = t < nv1 ? (s[1][h] + s[1][8 + h]) * qsc[h] : -INFINITY;
+        } else {
+          s[0][h] = t < nv0 ? s[0][h] * a.scale_log2 : -INFINITY;
+          s[1][h] = t < nv1 ? s[1][h] * a.scale_log2 : -INFINITY;
+        }
         const float wm = warp_max(fmaxf(s[0][h], s[1][h]));
         if (lane == 0) rd[warp * kN + h] = wm;
       }

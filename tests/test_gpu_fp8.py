@@ -171,6 +171,30 @@ def test_decode_fp8_long_split_and_scales():
         assert_close(r.out, ref)
 
 
+@pytest.mark.parametrize("group,kv", [(7, 4), (8, 2), (1, 8)])
+def test_decode_fp8_query_magnitude_per_head(group, kv):
+    """Query heads whose magnitudes differ by up to 2^16, and all-zero heads:
+    the decode takes the dot products on the e4m3 codes, with q split into
+    two e4m3 parts under a power-of-two scale of its own per head."""
+    ctx = [1, 17, 100, 700, 1500, 129, 3000]
+    w = W.with_fp8_cache(W.custom(group * kv, kv, ctx=ctx, q_lens=[1] * len(ctx),
+                                  seed=840 + group))
+    H, D = w.num_heads, w.head_dim
+    exps = [-12, -3, 0, 2, 4, None]
+    with torch.no_grad():
+        for h in range(H):
+            e = exps[h % len(exps)]
+            cols = w.qkv[:, h * D:(h + 1) * D]
+            if e is None:
+                cols.zero_()
+            else:
+                cols.mul_(2.0 ** e)  # exact in bf16: a power of two
+    _, _, _, ref, _, e2 = oracle_fp8(w)
+    r = Fp8Run(w).append().decode().sync()
+    assert int(r.err.item()) == 0 and e2 == 0
+    assert_close(r.out, ref)
+
+
 def test_decode_fp8_workload_b64_and_deterministic():
     w = W.with_fp8_cache(W.build(1))
     _, _, _, ref, _, _ = oracle_fp8(w)
