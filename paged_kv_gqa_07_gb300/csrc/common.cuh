@@ -271,10 +271,12 @@ __device__ __forceinline__ float4 lds128f(uint32_t addr) {
 
 // --------------------------------------------------------- warp math ------
 
+// Maximum over the warp in one instruction (NaN inputs ignored, as fmaxf
+// does).
 __device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
