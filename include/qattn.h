@@ -198,12 +198,18 @@ int qattn_rope_cache_append_ex(void* q, int64_t q_row_stride, const void* k,
  * [block_size][head_dim] uint8, 16-byte aligned.  Element x of a bf16 cache
  * is stored as e4m3(x / scale): the fp32 quotient (correctly rounded)
  * rounded to the nearest e4m3fn value, ties to even, magnitudes past 448
- * saturated to 448.  The attention entry points read code * scale: the
- * codes are converted exactly to f16 and both tensor-core products run in
- * f16 with fp32 accumulation (q and the softmax weights are rounded to f16;
- * q must stay within f16's range, |q| < 65504), k_scale multiplies the
- * logits' scale and v_scale the output.  Scales must be finite, positive
- * and normal fp32 (QATTN_ERR_INVALID_ARG otherwise). */
+ * saturated to 448.  The attention entry points read code * scale.  Decode
+ * takes q . k on the codes themselves (e4m3 tensor-core products, fp32
+ * accumulation), with each head's q as the sum of two e4m3 parts under a
+ * power-of-two scale of that head: the sum equals the bf16 q exactly for
+ * every element within a factor 2^10 of the head's largest |q|, and is off
+ * by less than 2^-17 of that largest |q| for the others.  P V in decode,
+ * and both products of prefill and the shared-prefix pass, run on the
+ * codes converted exactly (to f16 in decode, with the softmax weights
+ * rounded to f16; to bf16 in prefill).  k_scale multiplies the logits'
+ * scale and v_scale the output.
+ * Scales must be finite, positive and normal fp32 (QATTN_ERR_INVALID_ARG
+ * otherwise). */
 
 /* qattn_rope_cache_append_ex into an FP8 cache: the bf16 key (after bias,
  * norm and RoPE) and value rows are stored as e4m3(x / k_scale) and
