@@ -508,7 +508,7 @@ def run_ours(args, dist: Dist):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16" if not fp8 else "bf16 q/out, e4m3 cache, f16 tensor-core products",
+        "dtype": "bf16" if not fp8 else "bf16 q/out, e4m3 cache; decode q.k on e4m3 codes, P V in f16",
         "data": "synthetic (seeded N(0,1) q/k/v and cache, random block placement)",
         "config": {"workload": args.workload, "num_heads": H, "num_kv_heads": Hkv,
                    "head_dim": D, "block_size": BS, "batch": w.num_seqs,
