@@ -70,6 +70,10 @@ def parse():
     p.add_argument("--phases", action="store_true",
                    help="diagnostic: the tracing build's per-CTA phase stamps of the decode "
                         "call (b64 and 8 x 32K), one JSON line per workload")
+    p.add_argument("--copy-ceiling", action="store_true",
+                   help="diagnostic: the tracing build's copy probe -- the decode's K/V tile "
+                        "copies alone -- beside the decode call, b64 and 8 x 32K, bf16 and "
+                        "FP8, one JSON line each")
     p.add_argument("--append-sweep", action="store_true",
                    help="supplementary: time RoPE + append alone at 16k and 64k new tokens "
                         "(Qwen2-7B heads), one JSON line per size")
@@ -924,6 +928,81 @@ def run_phases(args):
         torch.cuda.empty_cache()
 
 
+def decode_tile_list(w):
+    """The decode kernel's work list: per (sequence, kv head) unit its
+    128-token tiles, each as [kv head, block id of each cache block of the
+    tile, -1 where there is none]; and the cache blocks it names."""
+    bs = w.block_size
+    bpt = 128 // bs
+    bt = w.block_tables.tolist()
+    tiles, nblocks = [], 0
+    for b, L in enumerate(w.context_lens.tolist()):
+        nblk = (L + bs - 1) // bs
+        for g in range(w.num_kv_heads):
+            for i in range((L + 127) // 128):
+                ids = [-1] * 8
+                for j in range(bpt):
+                    if i * bpt + j < nblk:
+                        ids[j] = bt[b][i * bpt + j]
+                        nblocks += 1
+                tiles.append([g] + ids)
+    return tiles, nblocks
+
+
+def run_copy_ceiling(args):
+    """The copy pattern's own time: the tracing build's copy probe issues,
+    per SM, the decode's K and V tile boxes (same tensor maps, same tiles,
+    the decode's ring depth) with nothing consuming them, layers in
+    rotation as in the timed runs; the decode call of the same harness is
+    timed beside it with the regular library."""
+    import ctypes
+
+    from paged_kv_gqa_07_gb300 import build as B
+    from paged_kv_gqa_07_gb300 import qattn as Q
+    B.build()
+    Q.load_library()
+    T = ctypes.CDLL(B.build(trace=True))
+    P, I32 = ctypes.c_void_p, ctypes.c_int32
+    T.qattn_trace_copy_stream.argtypes = [P, P, I32, Q.qattn_dims, I32, P, I32, I32, P, P]
+    T.qattn_trace_copy_stream.restype = ctypes.c_int
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)  # as in the timed runs
+    torch.cuda.set_stream(stream)
+    hbm_peak, _, peak_kind = measured_peaks()
+    for name in ("qwen2_7b_decode_b64", "qwen2_7b_long_decode"):
+        for kv in ("bf16", "fp8"):
+            h = Harness(args, name, dev, kv=kv)
+            w = h.w
+            tiles, nblocks = decode_tile_list(w)
+            d_tiles = torch.tensor(tiles, dtype=torch.int32, device=dev)
+            stages = 4 if kv == "fp8" else 3  # the decode kernel's K / V ring depth
+            copy_bytes = 2 * nblocks * w.block_size * 128 * (1 if kv == "fp8" else 2)
+
+            def copy(l):
+                _, kc, vc = h.layers[l % h.nlayers]
+                rc = T.qattn_trace_copy_stream(kc.data_ptr(), vc.data_ptr(), int(kc.shape[0]),
+                                               h.dims, 1 if kv == "fp8" else 0,
+                                               d_tiles.data_ptr(), len(tiles), stages,
+                                               h.err.data_ptr(), stream.cuda_stream)
+                assert rc == 0, rc
+
+            copy_ms = h.timed(copy, args.steps, args.warmup, stream)
+            attn_ms = h.timed(h.attend, args.steps, args.warmup, stream)
+            c = statistics.median(copy_ms) * 1e-3
+            a = statistics.median(attn_ms) * 1e-3
+            print(json.dumps({"copy_ceiling": name, "kv_cache_dtype": kv,
+                              "block_size": w.block_size, "stages": stages,
+                              "copy_bytes": copy_bytes, "copy_us": round(c * 1e6, 2),
+                              "copy_GBps": round(copy_bytes / c / 1e9, 1),
+                              "copy_frac": round(copy_bytes / c / 1e9 / hbm_peak, 4),
+                              "peak_kind": peak_kind, "decode_us": round(a * 1e6, 2),
+                              "copy_over_decode": round(c / a, 3)}), flush=True)
+            h.free()
+            del d_tiles
+            torch.cuda.empty_cache()
+
+
 def run_reference(args, dist: Dist):
     import oracle
     w = W.build(args.workload, block_size=args.block_size)
@@ -964,6 +1043,9 @@ def main():
         return
     if args.phases:
         run_phases(args)
+        return
+    if args.copy_ceiling:
+        run_copy_ceiling(args)
         return
     if args.impl == "reference":
         # The reference arm is the CPU oracle: rank 0 alone runs it.

@@ -24,7 +24,7 @@ LIB_PATH = os.path.join(BUILD_DIR, "libqattn.so")
 TRACE_DIR = os.path.join(BUILD_DIR, "trace")
 TRACE_LIB_PATH = os.path.join(TRACE_DIR, "libqattn_trace.so")
 SOURCES = ["api.cu", "rope_append.cu", "decode_merge.cu", "paged_decode_tc.cu", "fp8_gather.cu",
-           "varlen_prefill.cu", "decode_noalloc.cu"]
+           "varlen_prefill.cu", "decode_noalloc.cu", "copy_probe.cu"]
 HEADERS = ["common.cuh", "internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

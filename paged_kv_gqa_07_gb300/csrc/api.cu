@@ -15,6 +15,17 @@
 
 using namespace qattn;
 
+#ifdef QATTN_TRACE
+// The copy probe of the tracing build (copy_probe.cu).
+namespace qattn {
+int copy_stream_max_stages(bool kv_fp8);
+cudaError_t launch_copy_stream(const CUtensorMap& kmap, const CUtensorMap& vmap, bool kv_fp8,
+                               const int32_t* tiles, int32_t num_tiles, int32_t num_kv_heads,
+                               int32_t num_blocks, int32_t block_size, int32_t stages,
+                               int32_t* err_word, int num_sms, cudaStream_t stream);
+}  // namespace qattn
+#endif
+
 namespace {
 
 constexpr int kVersion = 100;  // 0.1.0
@@ -438,6 +449,28 @@ int qattn_trace_clear(void) {
   if (clear_decode_trace() != cudaSuccess || clear_merge_trace() != cudaSuccess)
     return QATTN_ERR_CUDA;
   return QATTN_OK;
+}
+
+int qattn_trace_copy_stream(const void* k_cache, const void* v_cache, int32_t num_blocks,
+                            qattn_dims dims, int32_t kv_fp8, const int32_t* tiles,
+                            int32_t num_tiles, int32_t stages, int32_t* err_word, void* stream) {
+  int st = check_dims(dims);
+  if (st != QATTN_OK) return st;
+  if (tiles == nullptr || num_tiles < 0 || num_blocks <= 0 || (kv_fp8 != 0 && kv_fp8 != 1) ||
+      stages < 2 || stages > copy_stream_max_stages(kv_fp8 != 0))
+    return QATTN_ERR_INVALID_ARG;
+  st = check_cache(k_cache, v_cache, num_blocks, dims);
+  if (st != QATTN_OK) return st;
+  if (num_tiles == 0) return QATTN_OK;
+  CUtensorMap kmap, vmap;
+  if (!cached_cache_map(&kmap, k_cache, num_blocks, dims.num_kv_heads, dims.block_size, kv_fp8) ||
+      !cached_cache_map(&vmap, v_cache, num_blocks, dims.num_kv_heads, dims.block_size, kv_fp8))
+    return QATTN_ERR_CUDA;
+  const int sms = num_sms_current();
+  if (sms <= 0) return QATTN_ERR_CUDA;
+  return cuda_status(launch_copy_stream(kmap, vmap, kv_fp8 != 0, tiles, num_tiles,
+                                        dims.num_kv_heads, num_blocks, dims.block_size, stages,
+                                        err_word, sms, static_cast<cudaStream_t>(stream)));
 }
 
 int qattn_trace_read(uint64_t* decode_host, uint64_t* merge_host) {

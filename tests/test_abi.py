@@ -40,15 +40,17 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_tracing_build_exports_its_readers_and_the_regular_one_does_not(lib):
-    """The tracing build (-DQATTN_TRACE) exports the three functions of
-    include/qattn_trace.h on top of the regular entry points; the library
-    the entry points ship in has none of them."""
+    """The tracing build (-DQATTN_TRACE) exports the functions of
+    include/qattn_trace.h (stamp readers and the copy probe) on top of the
+    regular entry points; the library the entry points ship in has none of
+    them."""
     path = B.build(trace=True)
     tl = ctypes.CDLL(path)
     src = re.sub(r"/\*.*?\*/", "", open(os.path.join(ROOT, "include", "qattn_trace.h")).read(),
                  flags=re.S)
     names = sorted(set(re.findall(r"\b(qattn_[a-z_0-9]+)\s*\(", src)))
-    assert names == ["qattn_trace_clear", "qattn_trace_dims", "qattn_trace_read"]
+    assert names == ["qattn_trace_clear", "qattn_trace_copy_stream", "qattn_trace_dims",
+                     "qattn_trace_read"]
     for name in names + declared_symbols():
         assert hasattr(tl, name), name
     for name in names:
