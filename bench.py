@@ -428,8 +428,7 @@ def run_ours(args, dist: Dist):
     dev = torch.device("cuda", dist.local_rank)
     torch.cuda.set_device(dev)
     # The calls run on a stream of their own, as in a serving engine, not on
-    # the legacy default stream (where the shared-prefix call, whose prefix
-    # pass forks onto a second stream, measured ~2 us slower).
+    # the legacy default stream.
     stream = torch.cuda.Stream(dev)
     torch.cuda.set_stream(stream)
     hbm_peak, tf_peak, peak_kind = measured_peaks()
