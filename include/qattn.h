@@ -202,8 +202,8 @@ int qattn_rope_cache_append_ex(void* q, int64_t q_row_stride, const void* k,
  * takes q . k on the codes themselves (e4m3 tensor-core products, fp32
  * accumulation), with each head's q as the sum of two e4m3 parts under a
  * power-of-two scale of that head: the sum equals the bf16 q exactly for
- * every element within a factor 2^10 of the head's largest |q|, and is off
- * by less than 2^-17 of that largest |q| for the others (q must be finite:
+ * every element within a factor 2^9 of the head's largest |q|, and is off
+ * by at most 2^-17 of that largest |q| for the others (q must be finite:
  * the e4m3 conversion saturates an infinite element to the format's range;
  * a NaN stays NaN).  P V in decode,
  * and both products of prefill and the shared-prefix pass, run on the

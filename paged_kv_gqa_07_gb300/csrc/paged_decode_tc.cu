@@ -51,10 +51,11 @@
 // per unit four more warps (7-10) write Q^T as two e4m3 rows per head,
 // hi = e4m3(q 2^e) and lo = e4m3(q 2^e - hi), with 2^e the power of two that
 // puts the head's largest |q| in [128, 256).  hi + lo is the bf16 value
-// exactly for every element within 2^10 of that maximum (hi keeps four
-// significant bits, the residue at most four more), so the score is the two
-// columns' sum times 2^-e -- the same dot product as the bf16 path up to
-// fp32 rounding.  The same warps dequantise V (e4m3 -> f16 is exact) into
+// exactly for every element within 2^9 of that maximum (hi keeps four
+// significant bits, the residue at most four more, none of them below the
+// e4m3 subnormal step 2^-9 while the scaled |q| >= 2^-2; smaller elements
+// are off by at most 2^-10 scaled), so the score is the two columns' sum
+// times 2^-e -- the bf16 path's dot product up to fp32 rounding.  The same warps dequantise V (e4m3 -> f16 is exact) into
 // the swizzled MN-major f16 layout the bf16 path gets from TMA, with rows
 // past the context written as zeros, and P V runs in f16 (P^T written as
 // f16); k_scale is folded into the logit scale and v_scale into the
