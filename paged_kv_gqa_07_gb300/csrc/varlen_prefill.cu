@@ -456,7 +456,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ready) {
               tc_fence_after();
               const uint32_t sk = sbase + kOffK + (qn & 1) * kTileBytes;
-#pragma unroll
+              // (both MMA loops unrolled by 4: measured 0-1.4 % faster than 8)
+#pragma unroll 4
               for (int k = 0; k < kHeadDim / 16; ++k) {
                 const uint64_t ad =
                     sdesc_sw128(sq + (k >> 2) * kHalfBytes + (k & 3) * 32, 16, 1024);
@@ -499,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc_fence_after();
               const uint32_t sv = sbase + kOffV + (pn & 1) * kTileBytes;
               const uint32_t sp_ = sbase + kOffP + (pn & 1) * kTileBytes;
-#pragma unroll
+#pragma unroll 4
               for (int k = 0; k < kN / 16; ++k) {
                 const uint64_t ad =
                     sdesc_sw128(sp_ + (k >> 2) * kHalfBytes + (k & 3) * 32, 16, 1024);
